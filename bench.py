@@ -1,0 +1,451 @@
+"""Benchmark of the fused MoE expert computation on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--M M] [--no-cpu-baseline]
+
+A step is one pass of the whole hot path (sort/pad, activation quantisation
+where the format has one, w13 GEMM + activation, w2 GEMM + weighted reduce,
+bf16 output) over one batch, launched as one CUDA graph.  The default
+workload is the GPT-OSS-20B-shaped MXFP4 w4a16 decode layer (M=64, K=N=2880,
+E=32, top-4); every step streams all 32 experts' weights (424 MB > 129 MB L2),
+so no L2 flush is needed between steps.  Under torchrun each rank runs an
+independent replica (weak scaling: the path has no exchange step on one GPU).
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+token sample of the same workload (the slow program parity is checked
+against), rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "gptoss20b_mxfp4_m64"
+METRIC = "MoE layer tokens/s on 1 GB300"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--M", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = f"/tmp/moe_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]),
+                                 hw=parts[5], hw_thermal=parts[6], sw_thermal=parts[7],
+                                 sw_power=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        return rows
+
+
+def summarize_clocks(rows, window):
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
+    reasons = set()
+    for r in rows:
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if r[key].lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+            "sm_max_mhz": max(r["sm_max"] for r in rows), "reasons": sorted(reasons),
+            "samples": len(rows), "window": window}
+
+
+# ---------------------------------------------------------------- bytes / flops
+def algorithmic(wl, counts):
+    """Algorithmic bytes and FLOPs of one layer call: weight bytes (codes,
+    scales, biases, globals) of the local experts that received a slot, bf16
+    input and output, ids and router weights; FLOPs 6*N*K per live slot."""
+    active = [e for e in range(wl.El) if counts[e] > 0]
+    live = int(sum(counts))
+
+    def wbytes(w, which):
+        n = 0
+        for key, t in w.items():
+            if t is None:
+                continue
+            per_expert = t.numel() * t.element_size() // wl.El
+            n += per_expert * len(active)
+        return n
+
+    w13 = wbytes(wl.w13, "w13")
+    w2 = wbytes(wl.w2, "w2")
+    act = wl.M * wl.K * 2
+    out = wl.M * wl.K * 2
+    ids = wl.M * wl.T * 8
+    return dict(w13_bytes=w13, w2_bytes=w2, layer_bytes=w13 + w2 + act + out + ids,
+                w13_kernel_bytes=w13 + act, flops=6.0 * wl.N * wl.K * live, live_slots=live,
+                active_experts=len(active))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def profile_traffic(kernel_tag, workload):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (source hash recorded in the summary)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}__{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    src = vals.get("source_sha256")
+    if not src or src != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "quantized_moe_expert_topk_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------- cpu baseline
+def cpu_baseline(wl, seconds, max_tokens=None):
+    """Time the fp64 oracle, as it stands, on this host's cores over whole
+    copies of the step (or the first `max_tokens` tokens) until `seconds`."""
+    import numpy as np
+
+    import oracle
+    from moe_workloads import to_host
+    host = to_host(wl)
+    n = wl.M if max_tokens is None else min(wl.M, max_tokens)
+    tokens = np.arange(n, dtype=np.int32)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.fused_experts(host["problem"], host["x"], host["w13"], host["w2"],
+                             host["topk_ids"], host["topk_weights"], host["expert_map"], tokens)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return dict(value=reps * n / dt, unit=UNIT, cores=oracle.num_threads(), kind="oracle",
+                sample=f"{reps} x {n} of {wl.M} tokens of {wl.name} (all their slots), fp64, "
+                       f"{dt:.1f} s")
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args):
+    rank, local_rank, world = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+
+    import oracle
+    from moe_workloads import make_workload, to_host
+    over = {"M": args.M} if args.M else {}
+    wl = make_workload(args.workload, device="cpu", **over)
+    host = to_host(wl)
+    import numpy as np
+    # one token per step keeps (warmup + steps) within a few minutes
+    sample = 1
+    step_times = []
+    for i in range(args.warmup + args.steps):
+        tok = np.array([i % wl.M], np.int32)
+        t0 = time.perf_counter()
+        oracle.fused_experts(host["problem"], host["x"], host["w13"], host["w2"],
+                             host["topk_ids"], host["topk_weights"], host["expert_map"], tok)
+        if i >= args.warmup:
+            step_times.append(time.perf_counter() - t0)
+    total = sum(step_times)
+    value = sample * len(step_times) / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(step_times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{sample} token per step of {wl.name} (all its slots), fp64"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N, "E": wl.E,
+            "E_local": wl.El, "topk": wl.T, "wfmt": wl.wfmt, "afmt": wl.afmt, "act": wl.act,
+            "gate": wl.gate, "recipe": wl.recipe}
+
+
+def launches_per_step(wl):
+    import quantized_moe_expert_topk_gb300 as moe
+    n = 1                                  # sort / pad (+ zero the accumulator)
+    n += wl.afmt != "bf16"                 # stage-1 activation quantiser
+    n += 1                                 # w13 GEMM + activation
+    n += moe.stage2_format(wl.wfmt, wl.afmt) != "bf16"  # stage-2 requantiser
+    n += 2                                 # w2 GEMM + reduce, bf16 finalize
+    return n
+
+
+def run_ours(args):
+    import torch
+    rank, local_rank, world = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    import quantized_moe_expert_topk_gb300 as moe
+    from quantized_moe_expert_topk_gb300 import build as cuda_build
+    from moe_workloads import make_workload
+    cuda_build.build()
+    over = {"M": args.M} if args.M else {}
+    wl = make_workload(args.workload, device=dev, **over)
+    layer = moe.FusedExperts.from_workload(wl)
+    out = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        layer(wl.x, wl.topk_ids, wl.topk_weights, wl.expert_map, out=out, stream=stream)
+
+    # eager warm-up, then capture one step as a CUDA graph
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+
+    # expert counts (for the algorithmic bytes) from the sort the step ran
+    ws = layer.workspace
+    cap = moe.moe_align_capacity(wl.M, wl.T, wl.El)
+    counts = expert_counts(moe, wl, dev)
+    alg = algorithmic(wl, counts)
+
+    sampler = ClockSampler(local_rank)
+    # clock soak: ~1 s of steps right before the timed region so that the
+    # sampler sees the loaded clocks even when the timed region is short
+    sampler.start()
+    t_end = time.perf_counter() + 1.0
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+        while time.perf_counter() < t_end:
+            for _ in range(50):
+                graph.replay()
+            stream.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    rows = sampler.stop()
+    ms = start.elapsed_time(end) / args.steps
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    value = world * wl.M / (ms / 1e3)
+
+    # dominant kernel (w13 GEMM + activation), timed alone on its own stream
+    k_ms = time_w13_kernel(moe, wl, layer, dev, stream, max(args.steps, 50))
+    hbm, bf16_tf, peak_src = measured_peaks()
+    achieved = alg["w13_kernel_bytes"] / (k_ms / 1e3) / 1e9
+    traffic = profile_traffic("moe_w13_gemm", wl.name)
+    layer_roof_ms = max(alg["layer_bytes"] / (hbm * 1e9), alg["flops"] / (bf16_tf * 1e12)) * 1e3
+
+    # end to end through the C ABI with host buffers (pinned), copies inside
+    e2e = time_e2e(moe, wl, layer, dev, stream, args.steps, args.warmup)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(wl), parallelism=f"replicas{world}",
+                       l2="no flush: each step streams all active experts' weights "
+                          f"({alg['w13_bytes'] + alg['w2_bytes']} B > 129 MB L2)",
+                       launch="CUDA graph of one step"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "kernel": "w13 grouped GEMM + activation",
+                     "alg_bytes_per_launch": alg["w13_kernel_bytes"],
+                     "kernel_ms": k_ms, "peak_source": peak_src},
+        "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms,
+                           "alg_bytes": alg["layer_bytes"], "alg_flops": alg["flops"],
+                           "active_experts": alg["active_experts"], "live_slots": alg["live_slots"]},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step(wl) * args.steps,
+        "clocks": summarize_clocks(rows, "warmup soak + timed region"),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def expert_counts(moe, wl, dev):
+    import torch
+    cap = moe.moe_align_capacity(wl.M, wl.T, wl.El)
+    sorted_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(max(cap // moe.BLOCK_M, 1), dtype=torch.int32, device=dev)
+    ntp = torch.empty(1, dtype=torch.int32, device=dev)
+    counts = torch.empty(wl.El, dtype=torch.int32, device=dev)
+    moe.moe_align_block_size(wl.topk_ids, wl.expert_map, wl.E, wl.El, moe.BLOCK_M, sorted_ids,
+                             expert_ids, ntp, counts)
+    torch.cuda.synchronize()
+    return counts.cpu().tolist()
+
+
+def time_w13_kernel(moe, wl, layer, dev, stream, iters):
+    """Average duration of the w13 grouped GEMM launch (CUDA events on the
+    stream it is launched on)."""
+    import torch
+    cap = moe.moe_align_capacity(wl.M, wl.T, wl.El)
+    sorted_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(max(cap // moe.BLOCK_M, 1), dtype=torch.int32, device=dev)
+    ntp = torch.empty(1, dtype=torch.int32, device=dev)
+    s2 = moe.stage2_format(wl.wfmt, wl.afmt)
+    with torch.cuda.stream(stream):
+        moe.moe_align_block_size(wl.topk_ids, wl.expert_map, wl.E, wl.El, moe.BLOCK_M, sorted_ids,
+                                 expert_ids, ntp, None, stream=stream)
+        if wl.afmt != "bf16" or s2 != "bf16":
+            raise NotImplementedError("dominant-kernel timing covers the bf16-activation formats")
+        inter = torch.empty((cap, wl.N), dtype=torch.bfloat16, device=dev)
+        for _ in range(5):
+            moe.moe_grouped_gemm_w13_act(layer.prob, wl.x, None, wl.w13, sorted_ids, expert_ids,
+                                         ntp, inter, stream=stream)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(iters):
+            moe.moe_grouped_gemm_w13_act(layer.prob, wl.x, None, wl.w13, sorted_ids, expert_ids,
+                                         ntp, inter, stream=stream)
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / iters
+
+
+def time_e2e(moe, wl, layer, dev, stream, steps, warmup):
+    import torch
+    x_h = wl.x.cpu().pin_memory()
+    ids_h = wl.topk_ids.cpu().pin_memory()
+    w_h = wl.topk_weights.cpu().pin_memory()
+    out_h = torch.empty((wl.M, wl.K), dtype=torch.bfloat16).pin_memory()
+    x_d, ids_d, w_d = torch.empty_like(wl.x), torch.empty_like(wl.topk_ids), torch.empty_like(
+        wl.topk_weights)
+    out_d = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device=dev)
+
+    def one():
+        x_d.copy_(x_h, non_blocking=True)
+        ids_d.copy_(ids_h, non_blocking=True)
+        w_d.copy_(w_h, non_blocking=True)
+        layer(x_d, ids_d, w_d, wl.expert_map, out=out_d, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            one()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            one()
+        end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
+    return {"value": wl.M / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": out_h.numel() * 2, "ms_per_step": ms,
+            "path": "moe_fused_experts with pinned host buffers, eager launches"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

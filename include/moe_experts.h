@@ -1,0 +1,206 @@
+/*
+ * moe_experts.h -- C ABI of the GB300 (sm_103a) fused Mixture-of-Experts
+ * expert computation: route -> gate/up GEMM -> activation -> down GEMM ->
+ * top-k weighted reduce, with bf16, FP8 (per-tensor, per-channel, 128x128
+ * block), MXFP4 and NVFP4 weights.
+ *
+ * The operation is the fused-experts contract of the page
+ * "vllm.model_executor.layers.fused_moe.experts.rocm_aiter_moe":
+ * rocm_aiter_fused_experts(hidden_states, w1, w2, topk_weights, topk_ids,
+ * activation, expert_mask, quant_config, ...) as called from
+ * AiterExperts.apply, which writes the (M, K) result into a caller-owned
+ * output.  Weight layouts follow GptOssMxfp4MoEMethod.create_weights on
+ * "vLLM/vllm/model_executor/layers/quantization/mxfp4.py" and
+ * QuarkNvfp4MoEMethod.create_weights on
+ * "vllm.model_executor.layers.quantization.quark.quark_moe".
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or synchronises.  Work is enqueued on `stream`
+ *    (a cudaStream_t passed as void*; NULL = the legacy default stream).
+ *  - Arguments are validated on the host before anything is launched; a
+ *    failed check returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *    MOE_ERR_WORKSPACE and enqueues nothing.  A launch failure returns
+ *    MOE_ERR_CUDA.  Device-side values (ids, counts) are not validated on the
+ *    host: an expert id outside [0, E) or mapped outside [0, E_l) is treated
+ *    as a dropped slot, exactly like an expert-map entry of -1.
+ *  - Layouts are row-major with the reduction dimension contiguous.
+ *    Packed e2m1 ("fp4"): two elements per byte, element 2i in the low nibble.
+ *  - Returned status codes are plain ints (moe_status).
+ */
+#ifndef MOE_EXPERTS_H_
+#define MOE_EXPERTS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad enum value          */
+  MOE_ERR_UNSUPPORTED = 2, /* valid but unsupported combination               */
+  MOE_ERR_WORKSPACE = 3,   /* workspace smaller than moe_workspace_size()     */
+  MOE_ERR_CUDA = 4,        /* a CUDA launch / runtime call failed             */
+  MOE_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (device word) */
+} moe_status;
+
+/* Weight formats: the AITER leaf classes' quant methods on the rocm_aiter_moe
+ * page (QuantMethod NO / PER_TENSOR / PER_TOKEN / BLOCK_128x128 / BLOCK_1X32)
+ * plus QuarkNvfp4MoEMethod. */
+typedef enum {
+  MOE_W_BF16 = 0,         /* bf16 [E_l,R,C]                                     */
+  MOE_W_FP8_TENSOR = 1,   /* e4m3 [E_l,R,C], scales f32 [E_l]                   */
+  MOE_W_FP8_CHANNEL = 2,  /* e4m3 [E_l,R,C], scales f32 [E_l,R]                 */
+  MOE_W_FP8_BLOCK128 = 3, /* e4m3 [E_l,R,C], scales f32 [E_l,ceil(R/128),ceil(C/128)] */
+  MOE_W_MXFP4 = 4,        /* e2m1 u8 [E_l,R,C/2], e8m0 u8 [E_l,R,C/32]          */
+  MOE_W_NVFP4 = 5         /* e2m1 u8 [E_l,R,C/2], e4m3 u8 [E_l,R,C/16], global f32 [E_l] */
+} moe_wfmt;
+
+/* Activation (stage-1 input) formats.  Supported (weight, activation) pairs,
+ * as the leaves' _supports_quant_scheme lists them:
+ *   BF16 + BF16; FP8_TENSOR + FP8_TENSOR_STATIC | FP8_TENSOR_DYN;
+ *   FP8_CHANNEL + FP8_TOKEN_DYN; FP8_BLOCK128 + FP8_GROUP128_DYN;
+ *   MXFP4 + BF16 (w4a16); NVFP4 + NVFP4_DYN.
+ * The intermediate (stage-2 input) uses the same scheme: per-tensor static
+ * (a2_scale) or dynamic, per-token dynamic, 1x128 dynamic, NVFP4 x16 dynamic
+ * with a per-expert global; bf16 for BF16 and MXFP4 weights. */
+typedef enum {
+  MOE_A_BF16 = 0,
+  MOE_A_FP8_TENSOR_STATIC = 1, /* scale f32 [1] given                          */
+  MOE_A_FP8_TENSOR_DYN = 2,    /* scale f32 [1] = amax/448 over the tensor     */
+  MOE_A_FP8_TOKEN_DYN = 3,     /* scales f32 [rows]                            */
+  MOE_A_FP8_GROUP128_DYN = 4,  /* scales f32 [rows, ceil(cols/128)]            */
+  MOE_A_NVFP4_DYN = 5          /* codes u8 [rows, cols/2], scales e4m3 [rows, cols/16] */
+} moe_afmt;
+
+/* Activations of the gated MLP (_resolve_aiter_activation; SITU is not
+ * supported: its formula is not given). */
+typedef enum { MOE_ACT_SILU = 0, MOE_ACT_GELU = 1, MOE_ACT_SWIGLU_OAI = 2 } moe_act;
+
+/* Row order of w13 (gate-mode selection in rocm_aiter_fused_experts):
+ * SEPARATED = [gate rows 0..N-1 ; up rows 0..N-1];
+ * INTERLEAVED = gate_j at row 2j, up_j at row 2j+1. */
+typedef enum { MOE_GATE_SEPARATED = 0, MOE_GATE_INTERLEAVED = 1 } moe_gate_layout;
+
+/* One weight tensor set (w13 with R=2N, C=K; or w2 with R=K, C=N).  Device
+ * pointers, caller-owned, layouts as listed under moe_wfmt. */
+typedef struct {
+  const void *codes;
+  const void *scales;        /* NULL for MOE_W_BF16                         */
+  const float *global_scale; /* MOE_W_NVFP4 only: f32 [E_l] (dequant multiplies) */
+  const void *bias;          /* optional [E_l,R]: bf16, or f32 if bias_is_f32 */
+  int bias_is_f32;
+} moe_weight_t;
+
+typedef struct {
+  int M;                  /* tokens                                              */
+  int K;                  /* hidden size                                         */
+  int N;                  /* intermediate size (per partition)                   */
+  int topk;               /* slots per token, shared-expert slots included       */
+  int num_experts;        /* E: global expert ids in topk_ids are in [0, E)      */
+  int num_local_experts;  /* E_l: leading dimension of the weight tensors        */
+  int wfmt, afmt, act, gate; /* moe_wfmt, moe_afmt, moe_act, moe_gate_layout     */
+  float swiglu_alpha;     /* SwiGLU-OAI: z = (clamp(u)+beta) * g' * sigmoid(alpha*g') */
+  float swiglu_beta;
+  float swiglu_limit;     /* g' = min(g, limit), u clamped to [-limit, limit]; 0 = no clamp */
+  const float *a1_scale;  /* device: FP8_TENSOR_STATIC stage-1 scale [1]; NVFP4 stage-1 global [1] */
+  const float *a2_scale;  /* device: FP8_TENSOR_STATIC stage-2 scale [1]; NVFP4 stage-2 global [E_l] */
+} moe_problem_t;
+
+/* Library / ABI identification. */
+int moe_abi_version(void);
+const char *moe_status_str(int status);
+
+/* Workspace bytes moe_fused_experts needs for this problem (like the
+ * workspace_shapes query of AiterExperts).  0 for an invalid problem. */
+size_t moe_workspace_size(const moe_problem_t *p);
+
+/* Entries of sorted_ids for (M, topk, E_l, block_m): every slot plus up to
+ * block_m-1 padding entries per expert that has a slot, rounded up to whole
+ * blocks.  expert_ids needs moe_align_capacity()/block_m entries. */
+long moe_align_capacity(int M, int topk, int num_local_experts, int block_m);
+
+/* Expert sort / block padding (the dispatch step named by
+ * moe_sorting_dispatch_policy in AiterExperts.apply; the rule is this
+ * library's): per local expert in ascending id, the flat slot ids t*topk+k in
+ * ascending order, padded with the sentinel S = M*topk to a multiple of
+ * block_m; empty experts get no block.  Tails: sorted_ids = S, expert_ids = -1.
+ *   topk_ids     int32 [M, topk] (global ids)
+ *   expert_map   int32 [E] global->local, -1 = dropped; NULL = identity
+ *   sorted_ids   int32 [moe_align_capacity()]
+ *   expert_ids   int32 [moe_align_capacity()/block_m]
+ *   num_post_pad int32 [1]  total padded length
+ *   expert_counts int32 [E_l] live slots per local expert (may be NULL)
+ * block_m must be in [1, 1024]; E_l <= 1024. */
+int moe_align_block_size(const int32_t *topk_ids, int M, int topk, const int32_t *expert_map,
+                         int num_experts, int num_local_experts, int block_m,
+                         int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
+                         int32_t *expert_counts, void *stream);
+
+/* Stage-1 activation quantiser (AiterFp8TensorExperts, AiterFp8ChannelExperts,
+ * AiterFp8BlockExperts, QuarkNvfp4MoEMethod).  x is bf16 [rows, cols].
+ *   fp8: scale = fl32(max(amax, 1e-12) / 448); code = e4m3_rne_sat(fl32(x / scale)).
+ *   NVFP4 (cols % 16 == 0): per 16 elements s = e4m3_rne_sat(fl32(fl32(amax/6)/g)),
+ *     code = e2m1_rne_sat(fl32(x / fl32(e4m3(s) * g))); s == 0 gives zero codes.
+ *   scale_in: device f32 [1] -- the static fp8 scale, or the NVFP4 global g.
+ *   codes: u8 [rows, cols] (fp8) or [rows, cols/2] (NVFP4); scales as under moe_afmt.
+ * MOE_A_BF16 is rejected (nothing to quantise). */
+int moe_quant_act(const void *x_bf16, int rows, int cols, int afmt, const float *scale_in,
+                  void *codes, void *scales, void *stream);
+
+/* Stage-1 grouped GEMM + activation (+ stage-2 requantisation).
+ * For every sorted row r < *num_post_pad with slot s = sorted_ids[r] < S,
+ * token t = s / topk, local expert e = expert_ids[r / block_m]:
+ *   h = dequant(A[t]) . dequant(W13[e])^T + b13[e];  z_j = act(gate_j, up_j)
+ * and writes row r of the intermediate: bf16 [cap, N] for BF16 / MXFP4
+ * weights; otherwise codes + scales in the stage-2 format
+ * (u8 [cap, N] or [cap, N/2], scales f32 [cap] / [cap, ceil(N/128)] /
+ * [1] or e4m3 [cap, N/16]).  Padding rows are written as zeros.
+ *   a_codes / a_scales: x bf16 [M, K] for bf16 activations, else the output of
+ *   moe_quant_act.  block_m must be 64 (the tile height of this kernel).
+ *   workspace: device scratch of moe_w13_workspace_size() bytes (fp32 staging
+ *   of the pre-quantisation intermediate); may be NULL when that size is 0. */
+size_t moe_w13_workspace_size(const moe_problem_t *p, int block_m);
+int moe_grouped_gemm_w13_act(const moe_problem_t *p, const void *a_codes, const void *a_scales,
+                             const moe_weight_t *w13, const int32_t *sorted_ids,
+                             const int32_t *expert_ids, const int32_t *num_post_pad, int block_m,
+                             void *inter, void *inter_scales, void *workspace, size_t ws_bytes,
+                             void *stream);
+
+/* Stage-2 grouped GEMM + top-k weighted reduce (TopKWeightAndReduceNoOP: the
+ * reduce happens inside the experts computation).  For every live sorted row:
+ *   y = dequant(inter[r]) . dequant(W2[e])^T + b2[e];  acc[t] += topk_weights[s] * y
+ * then out_bf16 = bf16_rne(acc).  acc_f32 [M, K] is caller scratch; it is
+ * zeroed by this call before the reduce.  Tokens with no live slot give 0. */
+int moe_grouped_gemm_w2_reduce(const moe_problem_t *p, const void *inter, const void *inter_scales,
+                               const moe_weight_t *w2, const float *topk_weights,
+                               const int32_t *sorted_ids, const int32_t *expert_ids,
+                               const int32_t *num_post_pad, int block_m, float *acc_f32,
+                               void *out_bf16, void *stream);
+
+/* The whole fused-experts call (rocm_aiter_fused_experts): sort/pad,
+ * stage-1 quantisation, w13 GEMM + activation, w2 GEMM + reduce, bf16 output.
+ *   hidden_bf16  bf16 [M, K];  topk_ids int32 [M, topk];  topk_weights f32 [M, topk]
+ *   expert_map   int32 [E] or NULL;  out_bf16 bf16 [M, K] (overwritten)
+ *   workspace    device scratch of at least moe_workspace_size(p) bytes, 256-B aligned. */
+int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe_weight_t *w13,
+                      const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
+                      const int32_t *expert_map, void *workspace, size_t ws_bytes, void *out_bf16,
+                      void *stream);
+
+/* Device error word: first error recorded by a bounded device wait or a
+ * device-side check since the last reset (0 = none).  Reads synchronously
+ * (call after synchronising the streams that ran the kernels). */
+int moe_get_device_error(int *err_out);
+int moe_reset_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_EXPERTS_H_ */

@@ -1,0 +1,231 @@
+"""Thin ctypes binding over libmoe_gb300.so (include/moe_experts.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  Tensors are torch CUDA tensors (torch supplies
+device memory and streams); each wrapper passes their data pointers, the
+current stream, and raises ``MoEError`` on a non-zero status.  If the shared
+library is missing the import fails loudly -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+WFMT = {"bf16": 0, "fp8_tensor": 1, "fp8_channel": 2, "fp8_block128": 3, "mxfp4": 4, "nvfp4": 5}
+AFMT = {"bf16": 0, "fp8_tensor_static": 1, "fp8_tensor_dyn": 2, "fp8_token_dyn": 3,
+        "fp8_group128_dyn": 4, "nvfp4_dyn": 5}
+ACT = {"silu": 0, "gelu": 1, "swiglu_oai": 2}
+GATE = {"separated": 0, "interleaved": 1}
+STAGE2 = {"fp8_channel": "fp8_token_dyn", "fp8_block128": "fp8_group128_dyn", "nvfp4": "nvfp4_dyn"}
+BLOCK_M = 64
+
+# Every symbol include/moe_experts.h declares.
+EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align_capacity",
+           "moe_align_block_size", "moe_quant_act", "moe_w13_workspace_size",
+           "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_reduce", "moe_fused_experts",
+           "moe_get_device_error", "moe_reset_device_error")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn}: status {status} ({status_str(status)})")
+        self.status = status
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int), ("K", ctypes.c_int), ("N", ctypes.c_int),
+                ("topk", ctypes.c_int), ("num_experts", ctypes.c_int),
+                ("num_local_experts", ctypes.c_int), ("wfmt", ctypes.c_int),
+                ("afmt", ctypes.c_int), ("act", ctypes.c_int), ("gate", ctypes.c_int),
+                ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
+                ("swiglu_limit", ctypes.c_float), ("a1_scale", ctypes.c_void_p),
+                ("a2_scale", ctypes.c_void_p)]
+
+
+class Weight(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("global_scale", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("bias_is_f32", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    i, p, sz, l = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_long
+    P, W = ctypes.POINTER(Problem), ctypes.POINTER(Weight)
+    sig = {
+        "moe_abi_version": (i, []),
+        "moe_status_str": (ctypes.c_char_p, [i]),
+        "moe_workspace_size": (sz, [P]),
+        "moe_align_capacity": (l, [i, i, i, i]),
+        "moe_align_block_size": (i, [p, i, i, p, i, i, i, p, p, p, p, p]),
+        "moe_quant_act": (i, [p, i, i, i, p, p, p, p]),
+        "moe_w13_workspace_size": (sz, [P, i]),
+        "moe_grouped_gemm_w13_act": (i, [P, p, p, W, p, p, p, i, p, p, p, sz, p]),
+        "moe_grouped_gemm_w2_reduce": (i, [P, p, p, W, p, p, p, p, i, p, p, p]),
+        "moe_fused_experts": (i, [P, p, W, W, p, p, p, p, sz, p, p]),
+        "moe_get_device_error": (i, [ctypes.POINTER(ctypes.c_int)]),
+        "moe_reset_device_error": (i, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype, f.argtypes = res, args
+    _lib = L
+    return L
+
+
+def status_str(s: int) -> str:
+    return lib().moe_status_str(int(s)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise MoEError(fn, rc)
+
+
+def make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha=1.702,
+                 swiglu_beta=1.0, swiglu_limit=7.0, a1_scale=None, a2_scale=None) -> Problem:
+    return Problem(M, K, N, topk, E, El, WFMT[wfmt], AFMT[afmt], ACT[act], GATE[gate],
+                   swiglu_alpha, swiglu_beta, swiglu_limit, _ptr(a1_scale), _ptr(a2_scale))
+
+
+def make_weight(w: dict) -> Weight:
+    bias = w.get("bias")
+    return Weight(_ptr(w["codes"]), _ptr(w.get("scales")), _ptr(w.get("global_scale")),
+                  _ptr(bias), int(bias is not None and bias.dtype == torch.float32))
+
+
+def stage2_format(wfmt: str, afmt: str) -> str:
+    if wfmt == "fp8_tensor":
+        return afmt
+    return STAGE2.get(wfmt, "bf16")
+
+
+# ------------------------------------------------------------------- ABI calls
+def moe_abi_version() -> int:
+    return lib().moe_abi_version()
+
+
+def moe_align_capacity(M, topk, El, block_m=BLOCK_M) -> int:
+    return int(lib().moe_align_capacity(M, topk, El, block_m))
+
+
+def moe_workspace_size(prob: Problem) -> int:
+    return int(lib().moe_workspace_size(ctypes.byref(prob)))
+
+
+def moe_w13_workspace_size(prob: Problem, block_m=BLOCK_M) -> int:
+    return int(lib().moe_w13_workspace_size(ctypes.byref(prob), block_m))
+
+
+def moe_align_block_size(topk_ids, expert_map, E, El, block_m, sorted_ids, expert_ids,
+                         num_post_pad, expert_counts=None, stream=None):
+    M, T = topk_ids.shape
+    _check("moe_align_block_size", lib().moe_align_block_size(
+        _ptr(topk_ids), M, T, _ptr(expert_map), E, El, block_m, _ptr(sorted_ids),
+        _ptr(expert_ids), _ptr(num_post_pad), _ptr(expert_counts), _stream(stream)))
+
+
+def moe_quant_act(x, afmt: str, scale_in, codes, scales, stream=None):
+    rows, cols = x.shape
+    _check("moe_quant_act", lib().moe_quant_act(_ptr(x), rows, cols, AFMT[afmt], _ptr(scale_in),
+                                                _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def moe_grouped_gemm_w13_act(prob: Problem, a_codes, a_scales, w13: dict, sorted_ids,
+                             expert_ids, num_post_pad, inter, inter_scales=None, workspace=None,
+                             block_m=BLOCK_M, stream=None):
+    W = make_weight(w13)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("moe_grouped_gemm_w13_act", lib().moe_grouped_gemm_w13_act(
+        ctypes.byref(prob), _ptr(a_codes), _ptr(a_scales), ctypes.byref(W), _ptr(sorted_ids),
+        _ptr(expert_ids), _ptr(num_post_pad), block_m, _ptr(inter), _ptr(inter_scales),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_grouped_gemm_w2_reduce(prob: Problem, inter, inter_scales, w2: dict, topk_weights,
+                               sorted_ids, expert_ids, num_post_pad, acc, out, block_m=BLOCK_M,
+                               stream=None):
+    W = make_weight(w2)
+    _check("moe_grouped_gemm_w2_reduce", lib().moe_grouped_gemm_w2_reduce(
+        ctypes.byref(prob), _ptr(inter), _ptr(inter_scales), ctypes.byref(W), _ptr(topk_weights),
+        _ptr(sorted_ids), _ptr(expert_ids), _ptr(num_post_pad), block_m, _ptr(acc), _ptr(out),
+        _stream(stream)))
+
+
+def moe_fused_experts(prob: Problem, hidden, w13: dict, w2: dict, topk_ids, topk_weights,
+                      expert_map, workspace, out, stream=None):
+    W13, W2 = make_weight(w13), make_weight(w2)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("moe_fused_experts", lib().moe_fused_experts(
+        ctypes.byref(prob), _ptr(hidden), ctypes.byref(W13), ctypes.byref(W2), _ptr(topk_ids),
+        _ptr(topk_weights), _ptr(expert_map), _ptr(workspace), ws_bytes, _ptr(out),
+        _stream(stream)))
+
+
+def moe_get_device_error() -> int:
+    v = ctypes.c_int(0)
+    _check("moe_get_device_error", lib().moe_get_device_error(ctypes.byref(v)))
+    return v.value
+
+
+def moe_reset_device_error():
+    _check("moe_reset_device_error", lib().moe_reset_device_error())
+
+
+# ------------------------------------------------------------------- convenience
+class FusedExperts:
+    """Holds the problem description and a workspace; ``__call__`` runs the
+    whole fused-experts computation through ``moe_fused_experts``."""
+
+    def __init__(self, M, K, N, topk, E, El, wfmt, afmt, act, gate, w13: dict, w2: dict,
+                 a1_scale=None, a2_scale=None, swiglu_alpha=1.702, swiglu_beta=1.0,
+                 swiglu_limit=7.0, device="cuda"):
+        self.prob = make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha,
+                                 swiglu_beta, swiglu_limit, a1_scale, a2_scale)
+        self._keep = (a1_scale, a2_scale)
+        self.w13, self.w2 = w13, w2
+        self.M, self.K = M, K
+        nbytes = moe_workspace_size(self.prob)
+        if nbytes == 0:
+            raise MoEError("moe_workspace_size", 1)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, hidden, topk_ids, topk_weights, expert_map=None, out=None, stream=None):
+        if out is None:
+            out = torch.empty((self.M, self.K), dtype=torch.bfloat16, device=hidden.device)
+        moe_fused_experts(self.prob, hidden, self.w13, self.w2, topk_ids, topk_weights,
+                          expert_map, self.workspace, out, stream)
+        return out
+
+    @classmethod
+    def from_workload(cls, wl, **kw):
+        return cls(wl.M, wl.K, wl.N, wl.T, wl.E, wl.El, wl.wfmt, wl.afmt, wl.act, wl.gate,
+                   wl.w13, wl.w2, wl.a1_scale, wl.a2_scale, wl.swiglu_alpha, wl.swiglu_beta,
+                   wl.swiglu_limit, device=wl.x.device, **kw)

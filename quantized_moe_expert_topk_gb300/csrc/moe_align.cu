@@ -1,0 +1,171 @@
+// moe_align.cu -- expert sort / block padding (moe_align_block_size).
+//
+// The dispatch step named by moe_sorting_dispatch_policy in AiterExperts.apply
+// (page "vllm.model_executor.layers.fused_moe.experts.rocm_aiter_moe").  The
+// pages do not print the algorithm; this kernel implements the rule stated in
+// include/moe_experts.h: per local expert (ascending), the flat slot ids in
+// ascending order, padded with S = M*T to a multiple of BM.
+//
+// One CTA of 32 warps does the sort; it is latency-bound and tiny next to the
+// GEMMs.  Each warp owns a contiguous range of slots:
+//   A. per-warp histograms: __match_any_sync groups the lanes holding the
+//      same expert, the group leader adds the group size (no smem atomics);
+//   B. per expert, an exclusive prefix over warps (stable order) and the
+//      padded size; an exclusive scan over experts gives the block offsets;
+//   C. each warp walks its range in order and scatters every slot to
+//      base[warp][e] + (rank among earlier lanes of its group);
+//   D. padding entries, expert_ids, tails.
+// Extra CTAs (blockIdx.x > 0) zero an optional fp32 buffer (the stage-2
+// accumulator) so the fused path needs no separate memset launch.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
+
+__device__ __forceinline__ int local_of(const int32_t *ids, const int32_t *emap, long s, int E,
+                                        int El) {
+  int g = ids[s];
+  if (g < 0 || g >= E) return -1;
+  int l = emap ? emap[g] : g;
+  return (l >= 0 && l < El) ? l : -1;
+}
+
+__global__ void __launch_bounds__(kAlignThreads)
+align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict__ emap, int E,
+             int El, int BM, int32_t *__restrict__ sorted, int32_t *__restrict__ expert_ids,
+             int32_t *__restrict__ ntp, int32_t *__restrict__ counts, long cap,
+             float *__restrict__ zero_buf, long zero_n) {
+  if (blockIdx.x > 0) {
+    // zeroing CTAs: 16-byte stores over the aligned body, scalar tail
+    const long n4 = zero_n / 4;
+    float4 *p4 = reinterpret_cast<float4 *>(zero_buf);
+    const long stride = (long)(gridDim.x - 1) * blockDim.x;
+    for (long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < n4; i += stride)
+      p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long i = n4 * 4 + (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < zero_n;
+         i += stride)
+      zero_buf[i] = 0.f;
+    return;
+  }
+  extern __shared__ int smem[];
+  int *cnt = smem;                     // [kAlignWarps][El]  per-warp counts -> prefixes
+  int *off = smem + kAlignWarps * El;  // [El + 1]           expert offsets
+  int *pad = off + El + 1;             // [El]               padded sizes
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+
+  for (int i = threadIdx.x; i < kAlignWarps * El; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+
+  const long per = ceil_div(S, kAlignWarps);
+  const long beg = (long)warp * per;
+  const long end = beg + per < S ? beg + per : S;
+
+  // A. per-warp histogram
+  for (long base = beg; base < end; base += 32) {
+    const long s = base + lane;
+    const int l = s < end ? local_of(ids, emap, s, E, El) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, l);
+    if (l >= 0 && lane == __ffs(peers) - 1) cnt[warp * El + l] += __popc(peers);
+  }
+  __syncthreads();
+
+  // B. stable prefix over warps, totals and padded sizes
+  for (int e = threadIdx.x; e < El; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kAlignWarps; ++w) {
+      const int c = cnt[w * El + e];
+      cnt[w * El + e] = run;
+      run += c;
+    }
+    if (counts) counts[e] = run;
+    pad[e] = (int)(ceil_div(run, BM) * BM);
+    off[e] = run;  // live count, kept for step D
+  }
+  __syncthreads();
+  // exclusive scan of pad[] by warp 0 (El <= 1024: 32 consecutive experts per lane)
+  if (warp == 0) {
+    const int chunk = (El + 31) / 32;
+    const int e0 = lane * chunk;
+    int local = 0;
+    for (int e = e0; e < e0 + chunk && e < El; ++e) local += pad[e];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e0 + chunk && e < El; ++e) {
+      const int p = pad[e];
+      pad[e] = run;  // pad[] now holds the exclusive offsets
+      run += p;
+    }
+    if (lane == 31) off[El] = incl;
+  }
+  __syncthreads();
+  // pad[e] = offset of expert e, off[e] = live count of e, off[El] = total
+  for (int i = threadIdx.x; i < kAlignWarps * El; i += blockDim.x) cnt[i] += pad[i % El];
+  __syncthreads();
+
+  // C. stable scatter
+  for (long base = beg; base < end; base += 32) {
+    const long s = base + lane;
+    const int l = s < end ? local_of(ids, emap, s, E, El) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, l);
+    int pos = 0;
+    if (l >= 0) pos = cnt[warp * El + l] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (l >= 0) {
+      sorted[pos] = (int32_t)s;
+      if (lane == __ffs(peers) - 1) cnt[warp * El + l] += __popc(peers);
+    }
+    __syncwarp();
+  }
+
+  // D. padding, block -> expert table, tails
+  const int total = off[El];
+  for (int e = warp; e < El; e += kAlignWarps) {
+    const int o = pad[e], live = off[e];
+    const int padded = (int)(ceil_div(live, BM) * BM);
+    for (int i = live + lane; i < padded; i += 32) sorted[o + i] = (int32_t)S;
+    for (int b = lane; b < padded / BM; b += 32) expert_ids[o / BM + b] = e;
+  }
+  for (long i = total + threadIdx.x; i < cap; i += blockDim.x) sorted[i] = (int32_t)S;
+  for (long b = total / BM + threadIdx.x; b < cap / BM; b += blockDim.x) expert_ids[b] = -1;
+  if (threadIdx.x == 0) *ntp = total;
+}
+
+}  // namespace
+
+cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *expert_map, int E,
+                         int El, int BM, int32_t *sorted_ids, int32_t *expert_ids,
+                         int32_t *num_post_pad, int32_t *counts, long cap, float *zero_buf,
+                         long zero_n, cudaStream_t stream) {
+  const size_t smem = sizeof(int) * ((size_t)kAlignWarps * El + 2 * (size_t)El + 1);
+  if (smem > 48 * 1024) {
+    // opt in once to the largest size this kernel can ask for (El = 1024), so
+    // later calls (for instance inside a stream capture) make no attribute call
+    static const cudaError_t opt_in = cudaFuncSetAttribute(
+        align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)(sizeof(int) * ((size_t)kAlignWarps * 1024 + 2 * 1024 + 1)));
+    if (opt_in != cudaSuccess) return opt_in;
+  }
+  int zero_ctas = 0;
+  if (zero_buf && zero_n > 0) {
+    const long per_cta = (long)kAlignThreads * 4 * 8;
+    zero_ctas = (int)ceil_div(zero_n, per_cta);
+    if (zero_ctas > 4 * 152) zero_ctas = 4 * 152;
+  }
+  align_kernel<<<1 + zero_ctas, kAlignThreads, smem, stream>>>(
+      topk_ids, (long)M * T, expert_map, E, El, BM, sorted_ids, expert_ids, num_post_pad, counts,
+      cap, zero_buf, zero_n);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

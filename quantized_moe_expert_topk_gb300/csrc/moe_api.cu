@@ -1,0 +1,361 @@
+// moe_api.cu -- the C ABI (include/moe_experts.h): host-side validation,
+// workspace layout and the launch sequence of the fused experts.
+//
+// Contract: rocm_aiter_fused_experts / AiterExperts.apply on the page
+// "vllm.model_executor.layers.fused_moe.experts.rocm_aiter_moe" (output (M, K)
+// written into a caller-owned buffer; workspaces sized by a query, like
+// AiterExperts.workspace_shapes; unsupported combinations rejected, like the
+// leaves' _supports_quant_scheme / _supports_activation checks).  Shape rules
+// follow GptOssMxfp4MoEMethod._setup_kernel's assertions on
+// "vLLM/vllm/model_executor/layers/quantization/mxfp4.py" (K and N multiples of
+// the 32-element MXFP4 block) and QuarkNvfp4MoEMethod (group of 16).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/moe_experts.h"
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+__device__ int g_device_error_word = 0;
+}
+
+namespace {
+
+using namespace moe;
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Stage-2 (intermediate) format implied by the weight / activation formats.
+int stage2_afmt(const moe_problem_t *p) {
+  switch (p->wfmt) {
+    case W_FP8_TENSOR: return p->afmt;
+    case W_FP8_CHANNEL: return A_FP8_TOKEN_DYN;
+    case W_FP8_BLOCK128: return A_FP8_GROUP128_DYN;
+    case W_NVFP4: return A_NVFP4_DYN;
+    default: return A_BF16;
+  }
+}
+
+bool pair_supported(int wfmt, int afmt) {
+  switch (wfmt) {
+    case W_BF16: return afmt == A_BF16;
+    case W_FP8_TENSOR: return afmt == A_FP8_TENSOR_STATIC || afmt == A_FP8_TENSOR_DYN;
+    case W_FP8_CHANNEL: return afmt == A_FP8_TOKEN_DYN;
+    case W_FP8_BLOCK128: return afmt == A_FP8_GROUP128_DYN;
+    case W_MXFP4: return afmt == A_BF16;
+    case W_NVFP4: return afmt == A_NVFP4_DYN;
+    default: return false;
+  }
+}
+
+size_t codes_bytes(int afmt, long rows, long cols) {
+  if (afmt == A_BF16) return 0;
+  return afmt == A_NVFP4_DYN ? (size_t)rows * cols / 2 : (size_t)rows * cols;
+}
+
+size_t scales_bytes(int afmt, long rows, long cols) {
+  switch (afmt) {
+    case A_FP8_TENSOR_STATIC:
+    case A_FP8_TENSOR_DYN: return 4;
+    case A_FP8_TOKEN_DYN: return (size_t)rows * 4;
+    case A_FP8_GROUP128_DYN: return (size_t)rows * ceil_div(cols, 128) * 4;
+    case A_NVFP4_DYN: return (size_t)rows * (cols / 16);
+    default: return 0;
+  }
+}
+
+int validate_problem(const moe_problem_t *p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (p->M < 0 || p->K <= 0 || p->N <= 0 || p->topk < 1 || p->num_experts < 1 ||
+      p->num_local_experts < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (p->wfmt < W_BF16 || p->wfmt > W_NVFP4 || p->afmt < A_BF16 || p->afmt > A_NVFP4_DYN ||
+      p->act < ACT_SILU || p->act > ACT_SWIGLU_OAI || p->gate < GATE_SEPARATED ||
+      p->gate > GATE_INTERLEAVED)
+    return MOE_ERR_INVALID_ARG;
+  if (!pair_supported(p->wfmt, p->afmt)) return MOE_ERR_UNSUPPORTED;
+  if (p->num_local_experts > 1024) return MOE_ERR_UNSUPPORTED;
+  // 32-element reduction tiles (and the 32-element MXFP4 / 16-element NVFP4 groups)
+  if (p->K % 32 != 0 || p->N % 32 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((long)p->M * p->topk > (1L << 30)) return MOE_ERR_UNSUPPORTED;
+  const int s2 = stage2_afmt(p);
+  if ((p->afmt == A_FP8_TENSOR_STATIC || p->afmt == A_NVFP4_DYN) && !p->a1_scale)
+    return MOE_ERR_INVALID_ARG;
+  if ((s2 == A_FP8_TENSOR_STATIC || s2 == A_NVFP4_DYN) && !p->a2_scale) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+int validate_weight(const moe_problem_t *p, const moe_weight_t *w) {
+  if (!w || !w->codes || !aligned16(w->codes)) return MOE_ERR_INVALID_ARG;
+  if (p->wfmt != W_BF16 && !w->scales) return MOE_ERR_INVALID_ARG;
+  if (p->wfmt == W_NVFP4 && !w->global_scale) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// Workspace layout of moe_fused_experts.
+struct Layout {
+  long cap, blocks;
+  size_t sorted, expert_ids, ntp, counts, a1_codes, a1_scales, inter, inter_scales, staging, acc,
+      total;
+};
+
+Layout make_layout(const moe_problem_t *p) {
+  Layout L;
+  const int BM = kGenericBlockM;
+  L.cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, BM);
+  L.blocks = L.cap / BM;
+  const int s2 = stage2_afmt(p);
+  size_t o = 0;
+  L.sorted = o; o = align_up(o + (size_t)L.cap * 4);
+  L.expert_ids = o; o = align_up(o + (size_t)L.blocks * 4);
+  L.ntp = o; o = align_up(o + 4);
+  L.counts = o; o = align_up(o + (size_t)p->num_local_experts * 4);
+  L.a1_codes = o; o = align_up(o + codes_bytes(p->afmt, p->M, p->K));
+  L.a1_scales = o; o = align_up(o + scales_bytes(p->afmt, p->M, p->K));
+  if (s2 == A_BF16) {
+    L.inter = o; o = align_up(o + (size_t)L.cap * p->N * 2);
+    L.inter_scales = o;
+    L.staging = o;
+  } else {
+    L.inter = o; o = align_up(o + codes_bytes(s2, L.cap, p->N));
+    L.inter_scales = o; o = align_up(o + scales_bytes(s2, L.cap, p->N));
+    L.staging = o; o = align_up(o + (size_t)L.cap * p->N * 4);
+  }
+  L.acc = o; o = align_up(o + (size_t)p->M * p->K * 4);
+  L.total = o;
+  return L;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+GemmArgs gemm_args(const moe_problem_t *p, int BM) {
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.M = p->M; g.K = p->K; g.N = p->N; g.T = p->topk; g.El = p->num_local_experts; g.BM = BM;
+  g.wfmt = p->wfmt; g.act = p->act; g.gate = p->gate;
+  g.alpha = p->swiglu_alpha; g.beta = p->swiglu_beta; g.limit = p->swiglu_limit;
+  g.S = p->M * p->topk;
+  return g;
+}
+
+// Stage-1 GEMM (+ requantisation).  `staging` is the fp32 scratch when the
+// intermediate is requantised.
+int run_w13(const moe_problem_t *p, const void *a_codes, const void *a_scales,
+            const moe_weight_t *w13, const int32_t *sorted, const int32_t *eids,
+            const int32_t *ntp, void *inter, void *inter_scales, void *staging, long cap,
+            cudaStream_t st) {
+  const int s2 = stage2_afmt(p);
+  GemmArgs g = gemm_args(p, kGenericBlockM);
+  g.afmt = p->afmt;
+  g.a_codes = a_codes; g.a_scales = a_scales; g.a_global = p->a1_scale;
+  g.w_codes = w13->codes; g.w_scales = w13->scales; g.w_global = w13->global_scale;
+  g.w_bias = w13->bias; g.bias_f32 = w13->bias_is_f32;
+  g.sorted_ids = sorted; g.expert_ids = eids; g.num_post_pad = ntp;
+  g.out = s2 == A_BF16 ? inter : staging;
+  g.out_f32 = s2 != A_BF16;
+  int rc = cuda_status(launch_gemm_w13(g, cap, st));
+  if (rc != MOE_OK || s2 == A_BF16) return rc;
+  QuantArgs q;
+  q.x = staging; q.x_is_f32 = 1; q.rows = cap; q.cols = p->N; q.afmt = s2;
+  q.param = p->a2_scale; q.sorted_ids = sorted; q.expert_ids = eids; q.num_post_pad = ntp;
+  q.S = p->M * p->topk; q.BM = kGenericBlockM; q.codes = inter; q.scales = inter_scales;
+  return cuda_status(launch_quant(q, st));
+}
+
+int run_w2(const moe_problem_t *p, const void *inter, const void *inter_scales,
+           const moe_weight_t *w2, const float *topk_weights, const int32_t *sorted,
+           const int32_t *eids, const int32_t *ntp, float *acc, void *out, long cap,
+           cudaStream_t st) {
+  GemmArgs g = gemm_args(p, kGenericBlockM);
+  g.afmt = stage2_afmt(p);
+  g.a_codes = inter; g.a_scales = inter_scales; g.a_global = p->a2_scale;
+  g.w_codes = w2->codes; g.w_scales = w2->scales; g.w_global = w2->global_scale;
+  g.w_bias = w2->bias; g.bias_f32 = w2->bias_is_f32;
+  g.sorted_ids = sorted; g.expert_ids = eids; g.num_post_pad = ntp;
+  g.acc = acc; g.topk_weights = topk_weights;
+  int rc = cuda_status(launch_gemm_w2(g, cap, st));
+  if (rc != MOE_OK) return rc;
+  return cuda_status(launch_finalize(acc, (long)p->M * p->K, out, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char *moe_status_str(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported combination";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+long moe_align_capacity(int M, int topk, int num_local_experts, int block_m) {
+  if (M < 0 || topk < 1 || num_local_experts < 1 || block_m < 1) return 0;
+  const long S = (long)M * topk;
+  const long nonempty = S < num_local_experts ? S : num_local_experts;
+  return ceil_div(S + nonempty * (block_m - 1), block_m) * block_m;
+}
+
+size_t moe_workspace_size(const moe_problem_t *p) {
+  if (validate_problem(p) != MOE_OK) return 0;
+  return make_layout(p).total;
+}
+
+int moe_align_block_size(const int32_t *topk_ids, int M, int topk, const int32_t *expert_map,
+                         int num_experts, int num_local_experts, int block_m,
+                         int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
+                         int32_t *expert_counts, void *stream) {
+  if (M < 0 || topk < 1 || num_experts < 1 || num_local_experts < 1 ||
+      num_local_experts > 1024 || block_m < 1 || block_m > 1024)
+    return MOE_ERR_INVALID_ARG;
+  if ((M > 0 && !topk_ids) || !sorted_ids || !expert_ids || !num_post_pad)
+    return MOE_ERR_INVALID_ARG;
+  if ((long)M * topk > (1L << 30)) return MOE_ERR_UNSUPPORTED;
+  const long cap = moe_align_capacity(M, topk, num_local_experts, block_m);
+  return cuda_status(launch_align(topk_ids, M, topk, expert_map, num_experts, num_local_experts,
+                                  block_m, sorted_ids, expert_ids, num_post_pad, expert_counts,
+                                  cap, nullptr, 0, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_quant_act(const void *x_bf16, int rows, int cols, int afmt, const float *scale_in,
+                  void *codes, void *scales, void *stream) {
+  if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+  if (afmt <= A_BF16 || afmt > A_NVFP4_DYN) return MOE_ERR_INVALID_ARG;
+  if (afmt == A_NVFP4_DYN && cols % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((afmt == A_FP8_TENSOR_STATIC || afmt == A_NVFP4_DYN) && !scale_in) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x_bf16 || !codes || !scales || !aligned16(codes) || !aligned16(scales))
+    return MOE_ERR_INVALID_ARG;
+  QuantArgs q;
+  memset(&q, 0, sizeof(q));
+  q.x = x_bf16; q.x_is_f32 = 0; q.rows = rows; q.cols = cols; q.afmt = afmt; q.param = scale_in;
+  q.codes = codes; q.scales = scales; q.BM = 1;
+  return cuda_status(launch_quant(q, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_w13_workspace_size(const moe_problem_t *p, int block_m) {
+  if (validate_problem(p) != MOE_OK || block_m != kGenericBlockM) return 0;
+  if (stage2_afmt(p) == A_BF16) return 0;
+  return (size_t)moe_align_capacity(p->M, p->topk, p->num_local_experts, block_m) * p->N * 4;
+}
+
+int moe_grouped_gemm_w13_act(const moe_problem_t *p, const void *a_codes, const void *a_scales,
+                             const moe_weight_t *w13, const int32_t *sorted_ids,
+                             const int32_t *expert_ids, const int32_t *num_post_pad, int block_m,
+                             void *inter, void *inter_scales, void *workspace, size_t ws_bytes,
+                             void *stream) {
+  int rc = validate_problem(p);
+  if (rc != MOE_OK) return rc;
+  if (block_m != kGenericBlockM) return MOE_ERR_UNSUPPORTED;
+  if ((rc = validate_weight(p, w13)) != MOE_OK) return rc;
+  if (p->M == 0) return MOE_OK;
+  if (!a_codes || !aligned16(a_codes) || !sorted_ids || !expert_ids || !num_post_pad || !inter ||
+      !aligned16(inter))
+    return MOE_ERR_INVALID_ARG;
+  if (p->afmt != A_BF16 && !a_scales) return MOE_ERR_INVALID_ARG;
+  const int s2 = stage2_afmt(p);
+  if (s2 != A_BF16) {
+    if (!inter_scales || !aligned16(inter_scales)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < moe_w13_workspace_size(p, block_m))
+      return MOE_ERR_WORKSPACE;
+  }
+  const long cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, block_m);
+  return run_w13(p, a_codes, a_scales, w13, sorted_ids, expert_ids, num_post_pad, inter,
+                 inter_scales, workspace, cap, static_cast<cudaStream_t>(stream));
+}
+
+int moe_grouped_gemm_w2_reduce(const moe_problem_t *p, const void *inter, const void *inter_scales,
+                               const moe_weight_t *w2, const float *topk_weights,
+                               const int32_t *sorted_ids, const int32_t *expert_ids,
+                               const int32_t *num_post_pad, int block_m, float *acc_f32,
+                               void *out_bf16, void *stream) {
+  int rc = validate_problem(p);
+  if (rc != MOE_OK) return rc;
+  if (block_m != kGenericBlockM) return MOE_ERR_UNSUPPORTED;
+  if ((rc = validate_weight(p, w2)) != MOE_OK) return rc;
+  if (p->M == 0) return MOE_OK;
+  if (!inter || !aligned16(inter) || !topk_weights || !sorted_ids || !expert_ids ||
+      !num_post_pad || !acc_f32 || !aligned16(acc_f32) || !out_bf16 || !aligned16(out_bf16))
+    return MOE_ERR_INVALID_ARG;
+  if (stage2_afmt(p) != A_BF16 && !inter_scales) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, block_m);
+  if ((rc = cuda_status(launch_zero(acc_f32, (long)p->M * p->K, st))) != MOE_OK) return rc;
+  return run_w2(p, inter, inter_scales, w2, topk_weights, sorted_ids, expert_ids, num_post_pad,
+                acc_f32, out_bf16, cap, st);
+}
+
+int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe_weight_t *w13,
+                      const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
+                      const int32_t *expert_map, void *workspace, size_t ws_bytes, void *out_bf16,
+                      void *stream) {
+  int rc = validate_problem(p);
+  if (rc != MOE_OK) return rc;
+  if ((rc = validate_weight(p, w13)) != MOE_OK) return rc;
+  if ((rc = validate_weight(p, w2)) != MOE_OK) return rc;
+  if (p->M == 0) return MOE_OK;
+  if (!hidden_bf16 || !aligned16(hidden_bf16) || !topk_ids || !topk_weights || !out_bf16 ||
+      !aligned16(out_bf16))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(p);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 || ws_bytes < L.total)
+    return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+  int32_t *eids = reinterpret_cast<int32_t *>(ws + L.expert_ids);
+  int32_t *ntp = reinterpret_cast<int32_t *>(ws + L.ntp);
+  int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+  float *acc = reinterpret_cast<float *>(ws + L.acc);
+  const long MK = (long)p->M * p->K;
+
+  // 1. sort / pad (+ zero the stage-2 accumulator in the same launch)
+  if ((rc = cuda_status(launch_align(topk_ids, p->M, p->topk, expert_map, p->num_experts,
+                                     p->num_local_experts, kGenericBlockM, sorted, eids, ntp,
+                                     counts, L.cap, acc, MK, st))) != MOE_OK)
+    return rc;
+  // 2. stage-1 activation quantisation
+  const void *a_codes = hidden_bf16;
+  const void *a_scales = nullptr;
+  if (p->afmt != A_BF16) {
+    QuantArgs q;
+    memset(&q, 0, sizeof(q));
+    q.x = hidden_bf16; q.rows = p->M; q.cols = p->K; q.afmt = p->afmt; q.param = p->a1_scale;
+    q.codes = ws + L.a1_codes; q.scales = ws + L.a1_scales; q.BM = 1;
+    if ((rc = cuda_status(launch_quant(q, st))) != MOE_OK) return rc;
+    a_codes = ws + L.a1_codes;
+    a_scales = ws + L.a1_scales;
+  }
+  // 3. gate/up GEMM + activation (+ requantisation)
+  if ((rc = run_w13(p, a_codes, a_scales, w13, sorted, eids, ntp, ws + L.inter,
+                    ws + L.inter_scales, ws + L.staging, L.cap, st)) != MOE_OK)
+    return rc;
+  // 4. down GEMM + weighted reduce + bf16 output
+  return run_w2(p, ws + L.inter, ws + L.inter_scales, w2, topk_weights, sorted, eids, ntp, acc,
+                out_bf16, L.cap, st);
+}
+
+int moe_get_device_error(int *err_out) {
+  if (!err_out) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemcpyFromSymbol(err_out, moe::g_device_error_word, sizeof(int)));
+}
+
+int moe_reset_device_error(void) {
+  const int zero = 0;
+  return cuda_status(cudaMemcpyToSymbol(moe::g_device_error_word, &zero, sizeof(int)));
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// moe_common.cuh -- device-side element codecs and small helpers shared by the
+// kernels of this library (internal header, not part of the ABI).
+//
+// Element formats (the OCP microscaling formats the MoE pages use:
+// "vLLM/vllm/model_executor/layers/quantization/mxfp4.py",
+// GptOssMxfp4MoEMethod.create_weights; "vllm.model_executor.layers.quantization.
+// quark.quark_moe", QuarkNvfp4MoEMethod.create_weights):
+//   e2m1   sign | 2-bit exponent (bias 1) | 1-bit mantissa; 0,.5,1,1.5,2,3,4,6
+//   e4m3fn sign | 4-bit exponent (bias 7) | 3-bit mantissa; max 448, no inf
+//   e8m0   2^(c-127)
+// Every decode below is exact: each decoded value (and each product of an
+// e2m1 code with its e8m0 or e4m3 scale) is representable in bf16 over the
+// formats' usual ranges, so the tensor-core operands carry no rounding.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------- enums (ABI values)
+enum WFmt { W_BF16 = 0, W_FP8_TENSOR = 1, W_FP8_CHANNEL = 2, W_FP8_BLOCK128 = 3, W_MXFP4 = 4,
+            W_NVFP4 = 5 };
+enum AFmt { A_BF16 = 0, A_FP8_TENSOR_STATIC = 1, A_FP8_TENSOR_DYN = 2, A_FP8_TOKEN_DYN = 3,
+            A_FP8_GROUP128_DYN = 4, A_NVFP4_DYN = 5 };
+enum Act { ACT_SILU = 0, ACT_GELU = 1, ACT_SWIGLU_OAI = 2 };
+enum Gate { GATE_SEPARATED = 0, GATE_INTERLEAVED = 1 };
+
+constexpr float kFp8Max = 448.0f;
+constexpr float kE2m1Max = 6.0f;
+constexpr float kScaleFloor = 1e-12f;
+
+// Device error word (first error wins).  Kernels receive its address (taken
+// once on the host with cudaGetSymbolAddress) and record a code with this.
+__device__ __forceinline__ void record_device_error(int *word, int code) {
+  if (word) atomicCAS(word, 0, code);
+}
+
+// ---------------------------------------------------------------- decode
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// e4m3fn code -> fp32 (exact).  Normal: (1 + m/8) 2^(e-7); subnormal: m 2^-9.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  float v = (e == 0) ? static_cast<float>(m) * 0.001953125f
+                     : __uint_as_float(((e + 120u) << 23) | (m << 20));
+  return (c & 0x80u) ? -v : v;
+}
+
+// e2m1 nibble -> fp32 (exact).
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  float v = (e == 0) ? 0.5f * static_cast<float>(m)
+                     : __uint_as_float(((e + 126u) << 23) | (m << 22));
+  return (c & 8u) ? -v : v;
+}
+
+// e8m0 code -> fp32 (2^(c-127)); codes 0 and 255 are outside fp32's normal
+// range and are mapped to 2^-127 (subnormal) / NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t c) {
+  if (c == 0) return __uint_as_float(0x00400000u);
+  if (c == 255) return __uint_as_float(0x7fc00000u);
+  return __uint_as_float(c << 23);
+}
+
+// ---------------------------------------------------------------- encode
+// fp32 -> e4m3fn, round-to-nearest-even, saturating to +-448 (sign kept).
+__device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return r & 0xffu;
+}
+
+// (lo, hi) fp32 -> one byte of two e2m1 codes (lo in bits 3..0), RNE, saturating at +-6.
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{ .reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
+  return r & 0xffu;
+}
+
+// fp8 dynamic scale of a group: fl32(max(amax, 1e-12) / 448), IEEE divide.
+__device__ __forceinline__ float fp8_group_scale(float amax) {
+  return __fdiv_rn(fmaxf(amax, kScaleFloor), kFp8Max);
+}
+
+// ---------------------------------------------------------------- activations
+__device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + expf(-v)); }
+
+__device__ __forceinline__ float act_and_mul(int act, float g, float u, float alpha, float beta,
+                                             float limit) {
+  if (act == ACT_SILU) return g * sigmoidf_(g) * u;
+  if (act == ACT_GELU) return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f)) * u;
+  // SwiGLU-OAI: clamp, then (u + beta) * g * sigmoid(alpha * g)
+  if (limit > 0.0f) {
+    g = fminf(g, limit);
+    u = fminf(fmaxf(u, -limit), limit);
+  }
+  return (u + beta) * g * sigmoidf_(alpha * g);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__host__ __device__ __forceinline__ long ceil_div(long a, long b) { return (a + b - 1) / b; }
+
+}  // namespace moe

@@ -1,0 +1,211 @@
+// moe_quant.cu -- dynamic / static activation quantisers (moe_quant_act) and
+// the stage-2 requantisation of the intermediate.
+//
+// Schemes of the AITER leaves on the page
+// "vllm.model_executor.layers.fused_moe.experts.rocm_aiter_moe":
+// AiterFp8TensorExperts (per-tensor static or dynamic), AiterFp8ChannelExperts
+// (per-token dynamic), AiterFp8BlockExperts (1x128 dynamic), and NVFP4 x16
+// with an fp32 global (QuarkNvfp4MoEMethod, page
+// "vllm.model_executor.layers.quantization.quark.quark_moe").
+//
+// Decision rules (both the scale and the codes are taken in fp32, with IEEE
+// round-to-nearest divides and the hardware's RNE saturating converts):
+//   fp8   scale = fl32(max(amax, 1e-12) / 448);  code = e4m3(fl32(x / scale))
+//   NVFP4 s = e4m3(fl32(fl32(amax / 6) / g));   code = e2m1(fl32(x / fl32(s * g)))
+//         (s == 0 gives zero codes)
+// All kernels are HBM-bound streaming passes: 16-byte loads, one warp (or
+// thread) per group, codes written with 4- or 8-byte stores.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+template <typename InT>
+__device__ __forceinline__ float load_elem(const InT *x, long i);
+template <>
+__device__ __forceinline__ float load_elem<uint16_t>(const uint16_t *x, long i) {
+  return bf16_to_f32(x[i]);
+}
+template <>
+__device__ __forceinline__ float load_elem<float>(const float *x, long i) {
+  return x[i];
+}
+
+// Row state of a sorted intermediate row: -1 beyond num_post_pad (skip),
+// 0 padding row (zero codes), 1 live row.
+__device__ __forceinline__ int row_state(const QuantArgs &a, long r) {
+  if (!a.sorted_ids) return 1;
+  if (r >= *a.num_post_pad) return -1;
+  return a.sorted_ids[r] < a.S ? 1 : 0;
+}
+
+// ---- fp8, 1x128 groups: one warp per (row, group); lane owns 4 columns.
+template <typename InT>
+__global__ void quant_fp8_group128(QuantArgs a) {
+  const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = (int)ceil_div(a.cols, 128);
+  const long r = warp_id / G;
+  const int g = (int)(warp_id % G);
+  if (r >= a.rows) return;
+  const int st = row_state(a, r);
+  if (st < 0) return;
+  const InT *x = static_cast<const InT *>(a.x) + r * a.cols;
+  uint8_t *codes = static_cast<uint8_t *>(a.codes) + r * a.cols;
+  float *scales = static_cast<float *>(a.scales);
+  const int c0 = g * 128 + lane * 4;
+  float v[4];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[i] = (st > 0 && c0 + i < a.cols) ? load_elem<InT>(x, c0 + i) : 0.f;
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  amax = warp_max(amax);
+  const float scale = fp8_group_scale(amax);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) packed |= f32_to_e4m3(__fdiv_rn(v[i], scale)) << (8 * i);
+  if (st == 0) packed = 0;
+  if (c0 + 3 < a.cols && (a.cols & 3) == 0) {
+    *reinterpret_cast<uint32_t *>(codes + c0) = packed;
+  } else {
+    for (int i = 0; i < 4; ++i)
+      if (c0 + i < a.cols) codes[c0 + i] = (packed >> (8 * i)) & 0xff;
+  }
+  if (lane == 0) scales[r * G + g] = st > 0 ? scale : 0.f;
+}
+
+// ---- fp8 per row (token): one CTA of 256 threads per row.
+template <typename InT>
+__global__ void quant_fp8_row(QuantArgs a) {
+  const long r = blockIdx.x;
+  const int st = row_state(a, r);
+  if (st < 0) return;
+  const InT *x = static_cast<const InT *>(a.x) + r * a.cols;
+  uint8_t *codes = static_cast<uint8_t *>(a.codes) + r * a.cols;
+  __shared__ float red[8];
+  float amax = 0.f;
+  for (int c = threadIdx.x; c < a.cols; c += blockDim.x) amax = fmaxf(amax, fabsf(load_elem<InT>(x, c)));
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
+  const float scale = fp8_group_scale(amax);
+  for (int c = threadIdx.x; c < a.cols; c += blockDim.x)
+    codes[c] = st > 0 ? (uint8_t)f32_to_e4m3(__fdiv_rn(load_elem<InT>(x, c), scale)) : 0;
+  if (threadIdx.x == 0) static_cast<float *>(a.scales)[r] = st > 0 ? scale : 0.f;
+}
+
+// ---- fp8 per tensor (static or dynamic): one CTA (1024 threads) for the
+// whole tensor; used by no large workload (the per-tensor scheme is rare).
+template <typename InT>
+__global__ void quant_fp8_tensor(QuantArgs a, int dynamic) {
+  __shared__ float red[32];
+  float scale;
+  if (dynamic) {
+    float amax = 0.f;
+    for (long r = 0; r < a.rows; ++r) {
+      if (row_state(a, r) <= 0) continue;
+      const InT *x = static_cast<const InT *>(a.x) + r * a.cols;
+      for (int c = threadIdx.x; c < a.cols; c += blockDim.x) amax = fmaxf(amax, fabsf(load_elem<InT>(x, c)));
+    }
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
+    scale = fp8_group_scale(amax);
+  } else {
+    scale = a.param[0];
+  }
+  for (long r = 0; r < a.rows; ++r) {
+    const int st = row_state(a, r);
+    if (st < 0) continue;
+    const InT *x = static_cast<const InT *>(a.x) + r * a.cols;
+    uint8_t *codes = static_cast<uint8_t *>(a.codes) + r * a.cols;
+    for (int c = threadIdx.x; c < a.cols; c += blockDim.x)
+      codes[c] = st > 0 ? (uint8_t)f32_to_e4m3(__fdiv_rn(load_elem<InT>(x, c), scale)) : 0;
+  }
+  if (threadIdx.x == 0) static_cast<float *>(a.scales)[0] = scale;
+}
+
+// ---- NVFP4 x16: one thread per group of 16 (8 code bytes + 1 scale byte).
+template <typename InT>
+__global__ void quant_nvfp4(QuantArgs a) {
+  const long gid = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int G = a.cols / 16;
+  const long r = gid / G;
+  const int g = (int)(gid % G);
+  if (r >= a.rows) return;
+  const int st = row_state(a, r);
+  if (st < 0) return;
+  uint8_t *codes = static_cast<uint8_t *>(a.codes) + r * (a.cols / 2) + g * 8;
+  uint8_t *scales = static_cast<uint8_t *>(a.scales) + r * G + g;
+  if (st == 0) {
+    *reinterpret_cast<uint2 *>(codes) = make_uint2(0, 0);
+    *scales = 0;
+    return;
+  }
+  const float gs = a.sorted_ids ? a.param[a.expert_ids[r / a.BM]] : a.param[0];
+  const InT *x = static_cast<const InT *>(a.x) + r * a.cols + g * 16;
+  float v[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[i] = load_elem<InT>(x, i);
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  const uint32_t s = f32_to_e4m3(__fdiv_rn(__fdiv_rn(amax, kE2m1Max), gs));
+  const float sv = e4m3_to_f32(s);
+  uint32_t lo = 0, hi = 0;
+  if (sv != 0.f) {
+    const float denom = __fmul_rn(sv, gs);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2)
+      lo |= f32x2_to_e2m1x2(__fdiv_rn(v[i], denom), __fdiv_rn(v[i + 1], denom)) << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2)
+      hi |= f32x2_to_e2m1x2(__fdiv_rn(v[8 + i], denom), __fdiv_rn(v[9 + i], denom)) << (4 * i);
+  }
+  *reinterpret_cast<uint2 *>(codes) = make_uint2(lo, hi);
+  *scales = (uint8_t)s;
+}
+
+template <typename InT>
+cudaError_t launch_quant_t(const QuantArgs &a, cudaStream_t stream) {
+  if (a.rows <= 0 || a.cols <= 0) return cudaSuccess;
+  switch (a.afmt) {
+    case A_FP8_GROUP128_DYN: {
+      const long warps = a.rows * ceil_div(a.cols, 128);
+      quant_fp8_group128<InT><<<(unsigned)ceil_div(warps * 32, 256), 256, 0, stream>>>(a);
+      break;
+    }
+    case A_FP8_TOKEN_DYN:
+      quant_fp8_row<InT><<<(unsigned)a.rows, 256, 0, stream>>>(a);
+      break;
+    case A_FP8_TENSOR_STATIC:
+    case A_FP8_TENSOR_DYN:
+      quant_fp8_tensor<InT><<<1, 1024, 0, stream>>>(a, a.afmt == A_FP8_TENSOR_DYN);
+      break;
+    case A_NVFP4_DYN: {
+      const long groups = a.rows * (a.cols / 16);
+      quant_nvfp4<InT><<<(unsigned)ceil_div(groups, 128), 128, 0, stream>>>(a);
+      break;
+    }
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant(const QuantArgs &a, cudaStream_t stream) {
+  return a.x_is_f32 ? launch_quant_t<float>(a, stream) : launch_quant_t<uint16_t>(a, stream);
+}
+
+}  // namespace moe

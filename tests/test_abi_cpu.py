@@ -1,0 +1,98 @@
+"""CPU-side checks of the C-ABI library: it loads, it exports every symbol the
+header declares, and host-side validation rejects bad arguments before any
+launch (these paths never touch the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from quantized_moe_expert_topk_gb300 import build
+    build.build()
+    import quantized_moe_expert_topk_gb300 as m
+    return m
+
+
+def header_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_header_symbols_are_exported(moe):
+    declared = header_functions()
+    assert declared, "no declarations found"
+    assert declared == set(moe.EXPORTS)
+    L = moe.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+    assert moe.moe_abi_version() == 1
+
+
+def test_status_strings(moe):
+    assert moe.status_str(0) == "ok"
+    assert moe.status_str(2) == "unsupported combination"
+
+
+def test_align_capacity_formula(moe):
+    # S + min(El, S) * (BM - 1), rounded up to whole blocks
+    assert moe.moe_align_capacity(64, 4, 32, 64) == ((256 + 32 * 63 + 63) // 64) * 64
+    assert moe.moe_align_capacity(1, 4, 96, 64) == 4 * 64
+    assert moe.moe_align_capacity(0, 2, 8, 64) == 0
+
+
+def test_workspace_size_and_validation(moe):
+    p = moe.make_problem(64, 2880, 2880, 4, 32, 32, "mxfp4", "bf16", "swiglu_oai", "interleaved")
+    assert moe.moe_workspace_size(p) > 64 * 2880 * 4
+    bad = [
+        moe.make_problem(64, 2880, 2880, 4, 32, 32, "mxfp4", "fp8_token_dyn", "silu", "separated"),
+        moe.make_problem(64, 2000, 2880, 4, 32, 32, "mxfp4", "bf16", "silu", "separated"),
+        moe.make_problem(64, 2880, 2880, 0, 32, 32, "bf16", "bf16", "silu", "separated"),
+        moe.make_problem(64, 2880, 2880, 4, 32, 2000, "bf16", "bf16", "silu", "separated"),
+        # NVFP4 needs the stage-1 / stage-2 globals
+        moe.make_problem(64, 256, 256, 2, 8, 8, "nvfp4", "nvfp4_dyn", "silu", "separated"),
+    ]
+    for b in bad:
+        assert moe.moe_workspace_size(b) == 0
+
+
+def test_fused_experts_rejects_bad_arguments_without_launching(moe):
+    L = moe.lib()
+    p = moe.make_problem(16, 256, 512, 2, 8, 8, "bf16", "bf16", "silu", "separated")
+    w = moe.Weight(None, None, None, None, 0)
+    rc = L.moe_fused_experts(ctypes.byref(p), None, ctypes.byref(w), ctypes.byref(w), None, None,
+                             None, None, 0, None, None)
+    assert rc == 1  # MOE_ERR_INVALID_ARG: null weight codes
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    w = moe.Weight(fake, None, None, None, 0)
+    rc = L.moe_fused_experts(ctypes.byref(p), fake, ctypes.byref(w), ctypes.byref(w), fake, fake,
+                             None, fake, 16, fake, None)
+    assert rc == 3  # MOE_ERR_WORKSPACE: far too small
+    p = moe.make_problem(16, 256, 512, 2, 8, 8, "bf16", "fp8_token_dyn", "silu", "separated")
+    rc = L.moe_fused_experts(ctypes.byref(p), fake, ctypes.byref(w), ctypes.byref(w), fake, fake,
+                             None, fake, 1 << 30, fake, None)
+    assert rc == 2  # unsupported (weight, activation) pair
+    unaligned = ctypes.c_void_p(0x1004)
+    p = moe.make_problem(16, 256, 512, 2, 8, 8, "bf16", "bf16", "silu", "separated")
+    rc = L.moe_fused_experts(ctypes.byref(p), unaligned, ctypes.byref(w), ctypes.byref(w), fake,
+                             fake, None, fake, 1 << 30, fake, None)
+    assert rc == 1  # misaligned hidden states
+
+
+def test_quant_and_align_validation(moe):
+    L = moe.lib()
+    fake = ctypes.c_void_p(0x1000)
+    assert L.moe_quant_act(fake, 4, 24, 5, fake, fake, fake, None) == 2   # NVFP4 cols % 16
+    assert L.moe_quant_act(fake, 4, 32, 0, fake, fake, fake, None) == 1   # bf16: nothing to do
+    assert L.moe_quant_act(fake, 4, 32, 1, None, fake, fake, None) == 1   # static scale missing
+    assert L.moe_align_block_size(fake, 4, 2, None, 8, 2000, 64, fake, fake, fake, None, None) == 1
+    assert L.moe_align_block_size(fake, 4, 2, None, 8, 8, 0, fake, fake, fake, None, None) == 1
