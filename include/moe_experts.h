@@ -193,6 +193,23 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
                       const int32_t *expert_map, void *workspace, size_t ws_bytes, void *out_bf16,
                       void *stream);
 
+/* No-allocation variant of moe_fused_experts (the pages have no counterpart:
+ * it exists for callers that cannot allocate device memory -- hosts that own
+ * every allocation and give out no scratch buffer, runtimes that must not call
+ * cudaMalloc on the call path).  Same inputs and output as moe_fused_experts,
+ * no workspace: the scratch is a file-scope device array of
+ * moe_noalloc_scratch_bytes() bytes (32 MiB) that each GPU loading the library
+ * holds until exit.  Problems needing more (moe_workspace_size) return
+ * MOE_ERR_WORKSPACE.  The first call on a device looks up the array's address
+ * (cudaGetSymbolAddress) and should come before any stream capture.  All calls
+ * on a device share the array: calls that overlap on the GPU race, so order
+ * them on one stream.  Allocates nothing. */
+size_t moe_noalloc_scratch_bytes(void);
+int moe_fused_experts_noalloc(const moe_problem_t *p, const void *hidden_bf16,
+                              const moe_weight_t *w13, const moe_weight_t *w2,
+                              const int32_t *topk_ids, const float *topk_weights,
+                              const int32_t *expert_map, void *out_bf16, void *stream);
+
 /* Device error word: first error recorded by a bounded device wait or a
  * device-side check since the last reset (0 = none).  Reads synchronously
  * (call after synchronising the streams that ran the kernels). */

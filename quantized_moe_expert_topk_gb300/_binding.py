@@ -29,7 +29,8 @@ BLOCK_M = 64
 EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align_capacity",
            "moe_align_block_size", "moe_quant_act", "moe_w13_workspace_size",
            "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_reduce", "moe_fused_experts",
-           "moe_get_device_error", "moe_reset_device_error")
+           "moe_get_device_error", "moe_reset_device_error", "moe_noalloc_scratch_bytes",
+           "moe_fused_experts_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -80,6 +81,8 @@ def lib() -> ctypes.CDLL:
         "moe_fused_experts": (i, [P, p, W, W, p, p, p, p, sz, p, p]),
         "moe_get_device_error": (i, [ctypes.POINTER(ctypes.c_int)]),
         "moe_reset_device_error": (i, []),
+        "moe_noalloc_scratch_bytes": (sz, []),
+        "moe_fused_experts_noalloc": (i, [P, p, W, W, p, p, p, p, p]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -187,6 +190,20 @@ def moe_fused_experts(prob: Problem, hidden, w13: dict, w2: dict, topk_ids, topk
         ctypes.byref(prob), _ptr(hidden), ctypes.byref(W13), ctypes.byref(W2), _ptr(topk_ids),
         _ptr(topk_weights), _ptr(expert_map), _ptr(workspace), ws_bytes, _ptr(out),
         _stream(stream)))
+
+
+def moe_noalloc_scratch_bytes() -> int:
+    return int(lib().moe_noalloc_scratch_bytes())
+
+
+def moe_fused_experts_noalloc(prob: Problem, hidden, w13: dict, w2: dict, topk_ids, topk_weights,
+                              expert_map, out, stream=None):
+    """moe_fused_experts without a workspace: the library's static device
+    scratch is used instead (for callers that cannot allocate)."""
+    W13, W2 = make_weight(w13), make_weight(w2)
+    _check("moe_fused_experts_noalloc", lib().moe_fused_experts_noalloc(
+        ctypes.byref(prob), _ptr(hidden), ctypes.byref(W13), ctypes.byref(W2), _ptr(topk_ids),
+        _ptr(topk_weights), _ptr(expert_map), _ptr(out), _stream(stream)))
 
 
 def moe_get_device_error() -> int:

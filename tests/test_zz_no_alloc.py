@@ -1,0 +1,58 @@
+"""moe_fused_experts_noalloc: the fused-experts entry point for callers that
+cannot allocate device memory (it runs on the library's static device scratch
+instead of a caller workspace).  Its output must match moe_fused_experts on
+the same inputs, on two calls in a row (the second call reuses scratch that
+still holds the first call's contents).  This file is collected last."""
+import pytest
+import torch
+
+from helpers import to_device
+from moe_workloads import make_custom, make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import quantized_moe_expert_topk_gb300 as m
+    m.lib()
+    return m
+
+
+def compare_two_calls(moe, wl, tol_rel):
+    wl = to_device(wl)
+    layer = moe.FusedExperts.from_workload(wl)
+    ref = layer(wl.x, wl.topk_ids, wl.topk_weights, wl.expert_map)
+    outs = []
+    for _ in range(2):
+        out = torch.full_like(ref, float("nan"))
+        moe.moe_fused_experts_noalloc(layer.prob, wl.x, wl.w13, wl.w2, wl.topk_ids,
+                                      wl.topk_weights, wl.expert_map, out)
+        torch.cuda.synchronize()
+        outs.append(out.float())
+    r = ref.float()
+    rms = r.pow(2).mean().sqrt().item()
+    for o in outs:
+        assert torch.isfinite(o).all()
+        assert (o - r).abs().max().item() <= tol_rel * rms + 1e-3
+
+
+def test_noalloc_matches_workspace_entry_point(moe):
+    # decode-shaped MXFP4 layer (the scratch keeps the sort, the intermediate
+    # and the fp32 accumulator); then a bf16 layer with different sizes, so
+    # the second problem runs on scratch the first one left behind
+    compare_two_calls(moe, make_workload("gptoss20b_mxfp4_m64", device="cuda"), 3e-2)
+    compare_two_calls(moe, make_custom(M=37, K=256, N=160, E=6, T=2, seed=11), 1e-2)
+    compare_two_calls(moe, make_custom(M=50, K=288, N=128, E=5, T=2, wfmt="fp8_block128",
+                                       afmt="fp8_group128_dyn", seed=12), 3e-2)
+
+
+def test_noalloc_rejects_problems_larger_than_its_scratch(moe):
+    wl = make_workload("dsv3_fp8block_m4096", device="cuda", E=8)
+    layer = moe.FusedExperts.from_workload(wl)
+    assert moe.moe_workspace_size(layer.prob) > moe.moe_noalloc_scratch_bytes()
+    out = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoEError) as e:
+        moe.moe_fused_experts_noalloc(layer.prob, wl.x, wl.w13, wl.w2, wl.topk_ids,
+                                      wl.topk_weights, wl.expert_map, out)
+    assert e.value.status == 3  # MOE_ERR_WORKSPACE
