@@ -327,10 +327,10 @@ def run_ours(args):
     value = world * wl.M / (ms / 1e3)
 
     # dominant kernel (w13 GEMM + activation), timed alone on its own stream
-    k_ms = time_w13_kernel(moe, wl, layer, dev, stream, max(args.steps, 50))
+    k_ms, stage_ms = time_w13_kernel(moe, wl, layer, dev, stream, max(args.steps, 50))
     hbm, bf16_tf, peak_src = measured_peaks()
     achieved = alg["w13_kernel_bytes"] / (k_ms / 1e3) / 1e9
-    traffic = profile_traffic("moe_w13_gemm", wl.name)
+    traffic = profile_traffic("moe_w13", wl.name)
     layer_roof_ms = max(alg["layer_bytes"] / (hbm * 1e9), alg["flops"] / (bf16_tf * 1e12)) * 1e3
 
     # end to end through the C ABI with host buffers (pinned), copies inside
@@ -348,7 +348,8 @@ def run_ours(args):
                      "frac": achieved / hbm, "traffic": traffic,
                      "kernel": "w13 grouped GEMM + activation",
                      "alg_bytes_per_launch": alg["w13_kernel_bytes"],
-                     "kernel_ms": k_ms, "peak_source": peak_src},
+                     "kernel_ms": k_ms, "peak_source": peak_src,
+                     "stage_ms": stage_ms},
         "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms,
                            "alg_bytes": alg["layer_bytes"], "alg_flops": alg["flops"],
                            "active_experts": alg["active_experts"], "live_slots": alg["live_slots"]},
@@ -380,31 +381,22 @@ def expert_counts(moe, wl, dev):
 
 
 def time_w13_kernel(moe, wl, layer, dev, stream, iters):
-    """Average duration of the w13 grouped GEMM launch (CUDA events on the
-    stream it is launched on)."""
+    """Average duration of the w13 kernel launch inside moe_fused_experts:
+    the library's stage timing records CUDA events around that launch on the
+    stream it is launched on (eager calls; the graph replays are not timed)."""
     import torch
-    cap = moe.moe_align_capacity(wl.M, wl.T, wl.El)
-    sorted_ids = torch.empty(cap, dtype=torch.int32, device=dev)
-    expert_ids = torch.empty(max(cap // moe.BLOCK_M, 1), dtype=torch.int32, device=dev)
-    ntp = torch.empty(1, dtype=torch.int32, device=dev)
-    s2 = moe.stage2_format(wl.wfmt, wl.afmt)
+    out = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device=dev)
     with torch.cuda.stream(stream):
-        moe.moe_align_block_size(wl.topk_ids, wl.expert_map, wl.E, wl.El, moe.BLOCK_M, sorted_ids,
-                                 expert_ids, ntp, None, stream=stream)
-        if wl.afmt != "bf16" or s2 != "bf16":
-            raise NotImplementedError("dominant-kernel timing covers the bf16-activation formats")
-        inter = torch.empty((cap, wl.N), dtype=torch.bfloat16, device=dev)
-        for _ in range(5):
-            moe.moe_grouped_gemm_w13_act(layer.prob, wl.x, None, wl.w13, sorted_ids, expert_ids,
-                                         ntp, inter, stream=stream)
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(stream)
+        for _ in range(3):
+            layer(wl.x, wl.topk_ids, wl.topk_weights, wl.expert_map, out=out, stream=stream)
+        torch.cuda.synchronize()
+        moe.moe_stage_timing(True)
         for _ in range(iters):
-            moe.moe_grouped_gemm_w13_act(layer.prob, wl.x, None, wl.w13, sorted_ids, expert_ids,
-                                         ntp, inter, stream=stream)
-        end.record(stream)
+            layer(wl.x, wl.topk_ids, wl.topk_weights, wl.expert_map, out=out, stream=stream)
+        moe.moe_stage_timing(False)
     torch.cuda.synchronize()
-    return start.elapsed_time(end) / iters
+    ms, calls = moe.moe_stage_times()
+    return ms["w13"] / calls, {k: v / calls for k, v in ms.items()}
 
 
 def time_e2e(moe, wl, layer, dev, stream, steps, warmup):

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum {
   MOE_OK = 0,
@@ -95,6 +95,8 @@ typedef struct {
   const float *global_scale; /* MOE_W_NVFP4 only: f32 [E_l] (dequant multiplies) */
   const void *bias;          /* optional [E_l,R]: bf16, or f32 if bias_is_f32 */
   int bias_is_f32;
+  const void *packed;        /* optional: the same weights repacked by moe_prepare_weights
+                                (MXFP4 only); enables the weight-streaming decode kernels */
 } moe_weight_t;
 
 typedef struct {
@@ -124,6 +126,22 @@ size_t moe_workspace_size(const moe_problem_t *p);
  * block_m-1 padding entries per expert that has a slot, rounded up to whole
  * blocks.  expert_ids needs moe_align_capacity()/block_m entries. */
 long moe_align_capacity(int M, int topk, int num_local_experts, int block_m);
+
+/* Load-time repack of MXFP4 weights for the weight-streaming decode kernels
+ * (the role of convert_weight_to_mxfp4_moe_kernel_format on the mxfp4.py
+ * page).  which = 0: w13 ([E_l, 2N, K/2] codes, [E_l, 2N, K/32] scales,
+ * gate rows paired with up rows per p->gate); which = 1: w2.  The packed
+ * buffer (moe_packed_weight_bytes bytes, 16-B aligned, caller-owned) holds
+ * the same codes and scales reordered into per-tile records.  Requires
+ * p->wfmt == MOE_W_MXFP4 and K, N multiples of 64; returns 0 bytes /
+ * MOE_ERR_UNSUPPORTED otherwise.  moe_fused_experts uses the streaming
+ * kernels when both w13.packed and w2.packed are set, the activations are
+ * bf16, the activation is SwiGLU-OAI with 0 < limit <= 64 and |beta| <= 64,
+ * and the batch is decode-sized (M*topk <= 32*E_l); otherwise the packed
+ * buffers are ignored. */
+size_t moe_packed_weight_bytes(const moe_problem_t *p, int which);
+int moe_prepare_weights(const moe_problem_t *p, int which, const moe_weight_t *w, void *packed,
+                        void *stream);
 
 /* Expert sort / block padding (the dispatch step named by
  * moe_sorting_dispatch_policy in AiterExperts.apply; the rule is this
@@ -209,6 +227,19 @@ int moe_fused_experts_noalloc(const moe_problem_t *p, const void *hidden_bf16,
                               const moe_weight_t *w13, const moe_weight_t *w2,
                               const int32_t *topk_ids, const float *topk_weights,
                               const int32_t *expert_map, void *out_bf16, void *stream);
+
+/* Per-stage timing of moe_fused_experts (a profiling aid).  While enabled,
+ * every moe_fused_experts call records a CUDA event pair around each of its
+ * kernel launches on the call's stream, waits for the last event before
+ * returning (the call becomes synchronous), and adds each launch's elapsed
+ * time to the accumulator of its stage.  moe_stage_timing(1) enables and
+ * resets, moe_stage_timing(0) disables; moe_stage_times copies the
+ * accumulated milliseconds [MOE_NUM_STAGES] and the number of timed calls.
+ * Not for use inside stream capture. */
+enum { MOE_STAGE_ALIGN = 0, MOE_STAGE_QUANT = 1, MOE_STAGE_W13 = 2, MOE_STAGE_REQUANT = 3,
+       MOE_STAGE_W2 = 4, MOE_STAGE_FINALIZE = 5, MOE_NUM_STAGES = 6 };
+int moe_stage_timing(int enable);
+int moe_stage_times(double *ms_out, int *calls_out);
 
 /* Device error word: first error recorded by a bounded device wait or a
  * device-side check since the last reset (0 = none).  Reads synchronously

@@ -30,7 +30,9 @@ EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align
            "moe_align_block_size", "moe_quant_act", "moe_w13_workspace_size",
            "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_reduce", "moe_fused_experts",
            "moe_get_device_error", "moe_reset_device_error", "moe_noalloc_scratch_bytes",
-           "moe_fused_experts_noalloc")
+           "moe_fused_experts_noalloc", "moe_packed_weight_bytes", "moe_prepare_weights",
+           "moe_stage_timing", "moe_stage_times")
+STAGES = ("align", "quant", "w13", "requant", "w2", "finalize")
 
 
 class MoEError(RuntimeError):
@@ -52,7 +54,7 @@ class Problem(ctypes.Structure):
 class Weight(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("global_scale", ctypes.c_void_p), ("bias", ctypes.c_void_p),
-                ("bias_is_f32", ctypes.c_int)]
+                ("bias_is_f32", ctypes.c_int), ("packed", ctypes.c_void_p)]
 
 
 _lib = None
@@ -83,6 +85,10 @@ def lib() -> ctypes.CDLL:
         "moe_reset_device_error": (i, []),
         "moe_noalloc_scratch_bytes": (sz, []),
         "moe_fused_experts_noalloc": (i, [P, p, W, W, p, p, p, p, p]),
+        "moe_packed_weight_bytes": (sz, [P, i]),
+        "moe_prepare_weights": (i, [P, i, W, p, p]),
+        "moe_stage_timing": (i, [i]),
+        "moe_stage_times": (i, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -121,7 +127,8 @@ def make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha=1.702
 def make_weight(w: dict) -> Weight:
     bias = w.get("bias")
     return Weight(_ptr(w["codes"]), _ptr(w.get("scales")), _ptr(w.get("global_scale")),
-                  _ptr(bias), int(bias is not None and bias.dtype == torch.float32))
+                  _ptr(bias), int(bias is not None and bias.dtype == torch.float32),
+                  _ptr(w.get("packed")))
 
 
 def stage2_format(wfmt: str, afmt: str) -> str:
@@ -206,6 +213,29 @@ def moe_fused_experts_noalloc(prob: Problem, hidden, w13: dict, w2: dict, topk_i
         _ptr(topk_weights), _ptr(expert_map), _ptr(out), _stream(stream)))
 
 
+def moe_packed_weight_bytes(prob: Problem, which: int) -> int:
+    return int(lib().moe_packed_weight_bytes(ctypes.byref(prob), which))
+
+
+def moe_prepare_weights(prob: Problem, which: int, w: dict, packed, stream=None):
+    W = make_weight(w)
+    _check("moe_prepare_weights", lib().moe_prepare_weights(
+        ctypes.byref(prob), which, ctypes.byref(W), _ptr(packed), _stream(stream)))
+
+
+def moe_stage_timing(enable: bool):
+    """Enable (and reset) or disable per-stage CUDA-event timing of moe_fused_experts."""
+    _check("moe_stage_timing", lib().moe_stage_timing(int(enable)))
+
+
+def moe_stage_times() -> tuple:
+    """(dict stage -> accumulated ms, number of timed calls)."""
+    ms = (ctypes.c_double * len(STAGES))()
+    calls = ctypes.c_int(0)
+    _check("moe_stage_times", lib().moe_stage_times(ms, ctypes.byref(calls)))
+    return dict(zip(STAGES, list(ms))), calls.value
+
+
 def moe_get_device_error() -> int:
     v = ctypes.c_int(0)
     _check("moe_get_device_error", lib().moe_get_device_error(ctypes.byref(v)))
@@ -223,11 +253,19 @@ class FusedExperts:
 
     def __init__(self, M, K, N, topk, E, El, wfmt, afmt, act, gate, w13: dict, w2: dict,
                  a1_scale=None, a2_scale=None, swiglu_alpha=1.702, swiglu_beta=1.0,
-                 swiglu_limit=7.0, device="cuda"):
+                 swiglu_limit=7.0, device="cuda", pack=True):
         self.prob = make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha,
                                  swiglu_beta, swiglu_limit, a1_scale, a2_scale)
         self._keep = (a1_scale, a2_scale)
-        self.w13, self.w2 = w13, w2
+        self.w13, self.w2 = dict(w13), dict(w2)
+        # load-time repack for the weight-streaming kernels (MXFP4, K and N
+        # multiples of 64); the C library decides per call whether to use it
+        if pack and moe_packed_weight_bytes(self.prob, 0) > 0:
+            for which, w in ((0, self.w13), (1, self.w2)):
+                buf = torch.empty(moe_packed_weight_bytes(self.prob, which), dtype=torch.uint8,
+                                  device=device)
+                moe_prepare_weights(self.prob, which, w, buf)
+                w["packed"] = buf
         self.M, self.K = M, K
         nbytes = moe_workspace_size(self.prob)
         if nbytes == 0:

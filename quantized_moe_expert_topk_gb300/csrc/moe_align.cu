@@ -17,6 +17,8 @@
 //   D. padding entries, expert_ids, tails.
 // Extra CTAs (blockIdx.x > 0) zero an optional fp32 buffer (the stage-2
 // accumulator) so the fused path needs no separate memset launch.
+#include <cuda_fp16.h>
+
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -38,18 +40,41 @@ __device__ __forceinline__ int local_of(const int32_t *ids, const int32_t *emap,
 __global__ void __launch_bounds__(kAlignThreads)
 align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict__ emap, int E,
              int El, int BM, int32_t *__restrict__ sorted, int32_t *__restrict__ expert_ids,
-             int32_t *__restrict__ ntp, int32_t *__restrict__ counts, long cap,
-             float *__restrict__ zero_buf, long zero_n) {
-  if (blockIdx.x > 0) {
+             int32_t *__restrict__ ntp, int32_t *__restrict__ counts, long cap, AlignExtras x,
+             int zero_ctas, int conv_ctas) {
+  if (blockIdx.x > 0 && (int)blockIdx.x <= zero_ctas) {
     // zeroing CTAs: 16-byte stores over the aligned body, scalar tail
-    const long n4 = zero_n / 4;
-    float4 *p4 = reinterpret_cast<float4 *>(zero_buf);
-    const long stride = (long)(gridDim.x - 1) * blockDim.x;
+    const long n4 = x.zero_n / 4;
+    float4 *p4 = reinterpret_cast<float4 *>(x.zero_buf);
+    const long stride = (long)zero_ctas * blockDim.x;
     for (long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < n4; i += stride)
       p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (long i = n4 * 4 + (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < zero_n;
+    for (long i = n4 * 4 + (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < x.zero_n;
          i += stride)
-      zero_buf[i] = 0.f;
+      x.zero_buf[i] = 0.f;
+    return;
+  }
+  if ((int)blockIdx.x > zero_ctas) {
+    // conversion CTAs: one warp per row of x; bf16 -> f16 scaled by 2^a so
+    // that the row maximum lands in [2^14, 2^15) (exact for bf16 values)
+    const int wid = ((int)blockIdx.x - 1 - zero_ctas) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (int r = wid; r < x.xM; r += conv_ctas * (blockDim.x >> 5)) {
+      const uint16_t *xr = x.x + (long)r * x.xK;
+      float amax = 0.f;
+      for (int c = lane; c < x.xK; c += 32) amax = fmaxf(amax, fabsf(bf16_to_f32(xr[c])));
+      amax = warp_max(amax);
+      int a = 0;
+      if (amax > 0.f) {
+        int ex;
+        frexpf(amax, &ex);  // amax = f * 2^ex, 0.5 <= f < 1
+        a = 15 - ex;
+      }
+      const float mul = ldexpf(1.0f, a);
+      __half *dst = static_cast<__half *>(x.x16) + (long)r * x.xK;
+      for (int c = lane; c < x.xK; c += 32) dst[c] = __float2half_rn(bf16_to_f32(xr[c]) * mul);
+      if (lane == 0) x.x_inv[r] = ldexpf(1.0f, -a);
+    }
     return;
   }
   extern __shared__ int smem[];
@@ -108,8 +133,27 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
     }
     if (lane == 31) off[El] = incl;
   }
+  // compact list of experts with at least one slot (ascending), by warp 1
+  if (warp == 1 && x.active) {
+    const int chunk = (El + 31) / 32;
+    const int e0 = lane * chunk;
+    int local = 0;
+    for (int e = e0; e < e0 + chunk && e < El; ++e) local += off[e] > 0;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int pos = incl - local;
+    for (int e = e0; e < e0 + chunk && e < El; ++e)
+      if (off[e] > 0) x.active[pos++] = e;
+    if (lane == 31) *x.n_active = incl;
+  }
   __syncthreads();
   // pad[e] = offset of expert e, off[e] = live count of e, off[El] = total
+  if (x.offsets)
+    for (int e = threadIdx.x; e < El; e += blockDim.x) x.offsets[e] = pad[e];
   for (int i = threadIdx.x; i < kAlignWarps * El; i += blockDim.x) cnt[i] += pad[i % El];
   __syncthreads();
 
@@ -145,8 +189,8 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
 
 cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *expert_map, int E,
                          int El, int BM, int32_t *sorted_ids, int32_t *expert_ids,
-                         int32_t *num_post_pad, int32_t *counts, long cap, float *zero_buf,
-                         long zero_n, cudaStream_t stream) {
+                         int32_t *num_post_pad, int32_t *counts, long cap,
+                         const AlignExtras &extra, cudaStream_t stream) {
   const size_t smem = sizeof(int) * ((size_t)kAlignWarps * El + 2 * (size_t)El + 1);
   if (smem > 48 * 1024) {
     // opt in once to the largest size this kernel can ask for (El = 1024), so
@@ -156,15 +200,19 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *e
         (int)(sizeof(int) * ((size_t)kAlignWarps * 1024 + 2 * 1024 + 1)));
     if (opt_in != cudaSuccess) return opt_in;
   }
-  int zero_ctas = 0;
-  if (zero_buf && zero_n > 0) {
+  int zero_ctas = 0, conv_ctas = 0;
+  if (extra.zero_buf && extra.zero_n > 0) {
     const long per_cta = (long)kAlignThreads * 4 * 8;
-    zero_ctas = (int)ceil_div(zero_n, per_cta);
+    zero_ctas = (int)ceil_div(extra.zero_n, per_cta);
     if (zero_ctas > 4 * 152) zero_ctas = 4 * 152;
   }
-  align_kernel<<<1 + zero_ctas, kAlignThreads, smem, stream>>>(
+  if (extra.x && extra.xM > 0) {
+    conv_ctas = (int)ceil_div(extra.xM, kAlignWarps);
+    if (conv_ctas > 2 * 152) conv_ctas = 2 * 152;
+  }
+  align_kernel<<<1 + zero_ctas + conv_ctas, kAlignThreads, smem, stream>>>(
       topk_ids, (long)M * T, expert_map, E, El, BM, sorted_ids, expert_ids, num_post_pad, counts,
-      cap, zero_buf, zero_n);
+      cap, extra, zero_ctas, conv_ctas);
   return cudaGetLastError();
 }
 

@@ -13,6 +13,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <math.h>
+
 #include <mutex>
 
 #include "../../include/moe_experts.h"
@@ -101,8 +103,8 @@ int validate_weight(const moe_problem_t *p, const moe_weight_t *w) {
 // Workspace layout of moe_fused_experts.
 struct Layout {
   long cap, blocks;
-  size_t sorted, expert_ids, ntp, counts, a1_codes, a1_scales, inter, inter_scales, staging, acc,
-      total;
+  size_t sorted, expert_ids, ntp, counts, offsets, active, n_active, x16, x_inv, a1_codes,
+      a1_scales, inter, inter_scales, staging, acc, total;
 };
 
 Layout make_layout(const moe_problem_t *p) {
@@ -116,6 +118,15 @@ Layout make_layout(const moe_problem_t *p) {
   L.expert_ids = o; o = align_up(o + (size_t)L.blocks * 4);
   L.ntp = o; o = align_up(o + 4);
   L.counts = o; o = align_up(o + (size_t)p->num_local_experts * 4);
+  L.offsets = o; o = align_up(o + (size_t)p->num_local_experts * 4);
+  L.active = o; o = align_up(o + (size_t)p->num_local_experts * 4);
+  L.n_active = o; o = align_up(o + 4);
+  if (p->wfmt == W_MXFP4 && p->afmt == A_BF16) {  // f16 copy of x for the streaming kernels
+    L.x16 = o; o = align_up(o + (size_t)p->M * p->K * 2);
+    L.x_inv = o; o = align_up(o + (size_t)p->M * 4);
+  } else {
+    L.x16 = L.x_inv = o;
+  }
   L.a1_codes = o; o = align_up(o + codes_bytes(p->afmt, p->M, p->K));
   L.a1_scales = o; o = align_up(o + scales_bytes(p->afmt, p->M, p->K));
   if (s2 == A_BF16) {
@@ -133,6 +144,83 @@ Layout make_layout(const moe_problem_t *p) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Per-device constants looked up once: SM count and the device error word.
+struct DeviceInfo {
+  int sm_count = 0;
+  int *err = nullptr;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+int device_info(DeviceInfo *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (d.sm_count == 0) {
+    int sms = 0;
+    void *err = nullptr;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaGetSymbolAddress(&err, moe::g_device_error_word) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    d.sm_count = sms;
+    d.err = static_cast<int *>(err);
+  }
+  *out = d;
+  return MOE_OK;
+}
+
+// ---- per-stage timing (moe_stage_timing): events around each launch
+struct StageTiming {
+  bool on = false;
+  int device = -1;
+  cudaEvent_t ev[MOE_NUM_STAGES][2] = {};
+  double ms[MOE_NUM_STAGES] = {};
+  int calls = 0;
+  bool used[MOE_NUM_STAGES] = {};
+};
+std::mutex g_timing_mu;
+StageTiming g_timing;
+
+struct StageScope {  // records the start event now and the stop event on done()
+  cudaStream_t st;
+  int stage;
+  bool on;
+  StageScope(int stage_, cudaStream_t st_) : st(st_), stage(stage_), on(g_timing.on) {
+    if (on) {
+      cudaEventRecord(g_timing.ev[stage][0], st);
+      g_timing.used[stage] = true;
+    }
+  }
+  void done() {
+    if (on) cudaEventRecord(g_timing.ev[stage][1], st);
+  }
+};
+
+// Adds the elapsed time of every stage launched by the finished call.
+void timing_collect() {
+  if (!g_timing.on) return;
+  for (int s = 0; s < MOE_NUM_STAGES; ++s) {
+    if (!g_timing.used[s]) continue;
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_timing.ev[s][1]) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, g_timing.ev[s][0], g_timing.ev[s][1]) == cudaSuccess)
+      g_timing.ms[s] += ms;
+    g_timing.used[s] = false;
+  }
+  g_timing.calls += 1;
+}
+
+// The weight-streaming decode path applies (see moe_prepare_weights in the header).
+bool stream_path(const moe_problem_t *p, const moe_weight_t *w13, const moe_weight_t *w2) {
+  return p->wfmt == W_MXFP4 && p->afmt == A_BF16 && w13->packed && w2->packed &&
+         p->act == ACT_SWIGLU_OAI && p->swiglu_limit > 0.f && p->swiglu_limit <= 64.f &&
+         fabsf(p->swiglu_beta) <= 64.f && p->K % 64 == 0 && p->N % 64 == 0 &&
+         !(w13->bias && w13->bias_is_f32) && !(w2->bias && w2->bias_is_f32) &&
+         aligned16(w13->packed) && aligned16(w2->packed) &&
+         (long)p->M * p->topk <= 32L * p->num_local_experts;
+}
 
 GemmArgs gemm_args(const moe_problem_t *p, int BM) {
   GemmArgs g;
@@ -159,13 +247,18 @@ int run_w13(const moe_problem_t *p, const void *a_codes, const void *a_scales,
   g.sorted_ids = sorted; g.expert_ids = eids; g.num_post_pad = ntp;
   g.out = s2 == A_BF16 ? inter : staging;
   g.out_f32 = s2 != A_BF16;
+  StageScope sc13(MOE_STAGE_W13, st);
   int rc = cuda_status(launch_gemm_w13(g, cap, st));
+  sc13.done();
   if (rc != MOE_OK || s2 == A_BF16) return rc;
   QuantArgs q;
   q.x = staging; q.x_is_f32 = 1; q.rows = cap; q.cols = p->N; q.afmt = s2;
   q.param = p->a2_scale; q.sorted_ids = sorted; q.expert_ids = eids; q.num_post_pad = ntp;
   q.S = p->M * p->topk; q.BM = kGenericBlockM; q.codes = inter; q.scales = inter_scales;
-  return cuda_status(launch_quant(q, st));
+  StageScope scq(MOE_STAGE_REQUANT, st);
+  rc = cuda_status(launch_quant(q, st));
+  scq.done();
+  return rc;
 }
 
 int run_w2(const moe_problem_t *p, const void *inter, const void *inter_scales,
@@ -179,9 +272,14 @@ int run_w2(const moe_problem_t *p, const void *inter, const void *inter_scales,
   g.w_bias = w2->bias; g.bias_f32 = w2->bias_is_f32;
   g.sorted_ids = sorted; g.expert_ids = eids; g.num_post_pad = ntp;
   g.acc = acc; g.topk_weights = topk_weights;
+  StageScope sc2(MOE_STAGE_W2, st);
   int rc = cuda_status(launch_gemm_w2(g, cap, st));
+  sc2.done();
   if (rc != MOE_OK) return rc;
-  return cuda_status(launch_finalize(acc, (long)p->M * p->K, out, st));
+  StageScope scf(MOE_STAGE_FINALIZE, st);
+  rc = cuda_status(launch_finalize(acc, (long)p->M * p->K, out, st));
+  scf.done();
+  return rc;
 }
 
 }  // namespace
@@ -227,7 +325,7 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int topk, const int32_t
   const long cap = moe_align_capacity(M, topk, num_local_experts, block_m);
   return cuda_status(launch_align(topk_ids, M, topk, expert_map, num_experts, num_local_experts,
                                   block_m, sorted_ids, expert_ids, num_post_pad, expert_counts,
-                                  cap, nullptr, 0, static_cast<cudaStream_t>(stream)));
+                                  cap, AlignExtras(), static_cast<cudaStream_t>(stream)));
 }
 
 int moe_quant_act(const void *x_bf16, int rows, int cols, int afmt, const float *scale_in,
@@ -322,11 +420,83 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
   float *acc = reinterpret_cast<float *>(ws + L.acc);
   const long MK = (long)p->M * p->K;
 
-  // 1. sort / pad (+ zero the stage-2 accumulator in the same launch)
-  if ((rc = cuda_status(launch_align(topk_ids, p->M, p->topk, expert_map, p->num_experts,
-                                     p->num_local_experts, kGenericBlockM, sorted, eids, ntp,
-                                     counts, L.cap, acc, MK, st))) != MOE_OK)
+  const bool streaming = stream_path(p, w13, w2);
+  DeviceInfo dinfo;
+  if (streaming && (rc = device_info(&dinfo)) != MOE_OK) return rc;
+
+  // 1. sort / pad (+ zero the stage-2 accumulator; for the streaming path also
+  //    the expert offsets, the active-expert list and the f16 copy of x)
+  AlignExtras ex;
+  ex.zero_buf = acc;
+  ex.zero_n = MK;
+  if (streaming) {
+    ex.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    ex.active = reinterpret_cast<int32_t *>(ws + L.active);
+    ex.n_active = reinterpret_cast<int32_t *>(ws + L.n_active);
+    ex.x = static_cast<const uint16_t *>(hidden_bf16);
+    ex.x16 = ws + L.x16;
+    ex.x_inv = reinterpret_cast<float *>(ws + L.x_inv);
+    ex.xM = p->M;
+    ex.xK = p->K;
+  }
+  std::lock_guard<std::mutex> timing_lock(g_timing_mu);
+  {
+    StageScope sc(MOE_STAGE_ALIGN, st);
+    rc = cuda_status(launch_align(topk_ids, p->M, p->topk, expert_map, p->num_experts,
+                                  p->num_local_experts, kGenericBlockM, sorted, eids, ntp, counts,
+                                  L.cap, ex, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+  }
+  if (streaming) {
+    StreamArgs sa;
+    memset(&sa, 0, sizeof(sa));
+    sa.M = p->M; sa.K = p->K; sa.N = p->N; sa.T = p->topk;
+    sa.max_active = p->num_local_experts;
+    sa.act = p->act; sa.gate = p->gate;
+    sa.alpha = p->swiglu_alpha; sa.beta = p->swiglu_beta; sa.limit = p->swiglu_limit;
+    sa.sorted_ids = sorted; sa.offsets = ex.offsets; sa.counts = counts;
+    sa.active = ex.active; sa.n_active = ex.n_active;
+    sa.err = dinfo.err;
+    // 2. gate/up: x16 x packed w13 -> f16 intermediate (+ bias, x-scale, SwiGLU-OAI)
+    StreamArgs s13 = sa;
+    s13.C = p->K;
+    s13.units_per_expert = stream_units_per_expert(1, p->N, p->K);
+    s13.ksplit = 1;
+    s13.kblocks = p->K / 64;
+    s13.packed = w13->packed; s13.bias = w13->bias;
+    s13.x16 = ex.x16; s13.x_inv = ex.x_inv;
+    s13.out = ws + L.inter;
+    {
+      StageScope sc(MOE_STAGE_W13, st);
+      rc = cuda_status(launch_stream(s13, 1, dinfo.sm_count, st));
+      sc.done();
+      if (rc != MOE_OK) return rc;
+    }
+    // 3. down: intermediate x packed w2 -> fp32 accumulator (+ bias, router weight)
+    StreamArgs s2 = sa;
+    s2.C = p->N;
+    s2.units_per_expert = stream_units_per_expert(0, p->N, p->K);
+    s2.kblocks = p->N / 64;
+    s2.ksplit = s2.kblocks >= 16 ? 2 : 1;
+    s2.packed = w2->packed; s2.bias = w2->bias;
+    s2.x16 = ws + L.inter;
+    s2.acc = acc; s2.topk_weights = topk_weights;
+    {
+      StageScope sc(MOE_STAGE_W2, st);
+      rc = cuda_status(launch_stream(s2, 0, dinfo.sm_count, st));
+      sc.done();
+      if (rc != MOE_OK) return rc;
+    }
+    // 4. bf16 output
+    {
+      StageScope sc(MOE_STAGE_FINALIZE, st);
+      rc = cuda_status(launch_finalize(acc, MK, out_bf16, st));
+      sc.done();
+    }
+    timing_collect();
     return rc;
+  }
   // 2. stage-1 activation quantisation
   const void *a_codes = hidden_bf16;
   const void *a_scales = nullptr;
@@ -335,7 +505,10 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     memset(&q, 0, sizeof(q));
     q.x = hidden_bf16; q.rows = p->M; q.cols = p->K; q.afmt = p->afmt; q.param = p->a1_scale;
     q.codes = ws + L.a1_codes; q.scales = ws + L.a1_scales; q.BM = 1;
-    if ((rc = cuda_status(launch_quant(q, st))) != MOE_OK) return rc;
+    StageScope sc(MOE_STAGE_QUANT, st);
+    rc = cuda_status(launch_quant(q, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
     a_codes = ws + L.a1_codes;
     a_scales = ws + L.a1_scales;
   }
@@ -344,8 +517,70 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
                     ws + L.inter_scales, ws + L.staging, L.cap, st)) != MOE_OK)
     return rc;
   // 4. down GEMM + weighted reduce + bf16 output
-  return run_w2(p, ws + L.inter, ws + L.inter_scales, w2, topk_weights, sorted, eids, ntp, acc,
-                out_bf16, L.cap, st);
+  rc = run_w2(p, ws + L.inter, ws + L.inter_scales, w2, topk_weights, sorted, eids, ntp, acc,
+              out_bf16, L.cap, st);
+  timing_collect();
+  return rc;
+}
+
+size_t moe_packed_weight_bytes(const moe_problem_t *p, int which) {
+  if (validate_problem(p) != MOE_OK || p->wfmt != W_MXFP4 || (which != 0 && which != 1))
+    return 0;
+  if (p->K % 64 != 0 || p->N % 64 != 0) return 0;
+  return stream_packed_bytes(which == 0, p->N, p->K, p->num_local_experts);
+}
+
+int moe_prepare_weights(const moe_problem_t *p, int which, const moe_weight_t *w, void *packed,
+                        void *stream) {
+  int rc = validate_problem(p);
+  if (rc != MOE_OK) return rc;
+  if (which != 0 && which != 1) return MOE_ERR_INVALID_ARG;
+  if (p->wfmt != W_MXFP4 || p->K % 64 != 0 || p->N % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((rc = validate_weight(p, w)) != MOE_OK) return rc;
+  if (!packed || !aligned16(packed)) return MOE_ERR_INVALID_ARG;
+  const int w13 = which == 0;
+  PackArgs a;
+  a.codes = static_cast<const unsigned char *>(w->codes);
+  a.scales = static_cast<const unsigned char *>(w->scales);
+  a.out = static_cast<unsigned char *>(packed);
+  a.total = (long)stream_packed_bytes(w13, p->N, p->K, p->num_local_experts);
+  a.units = stream_units_per_expert(w13, p->N, p->K);
+  a.w13 = w13;
+  a.N = p->N;
+  a.R = w13 ? 2 * p->N : p->K;
+  a.C = w13 ? p->K : p->N;
+  a.kblocks = a.C / 64;
+  a.gate = p->gate;
+  return cuda_status(launch_pack_mxfp4(a, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_stage_timing(int enable) {
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  if (enable) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (g_timing.device != dev) {
+      for (int s = 0; s < MOE_NUM_STAGES; ++s)
+        for (int k = 0; k < 2; ++k)
+          if (cudaEventCreate(&g_timing.ev[s][k]) != cudaSuccess) return MOE_ERR_CUDA;
+      g_timing.device = dev;
+    }
+    for (int s = 0; s < MOE_NUM_STAGES; ++s) {
+      g_timing.ms[s] = 0.0;
+      g_timing.used[s] = false;
+    }
+    g_timing.calls = 0;
+  }
+  g_timing.on = enable != 0;
+  return MOE_OK;
+}
+
+int moe_stage_times(double *ms_out, int *calls_out) {
+  if (!ms_out) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  for (int s = 0; s < MOE_NUM_STAGES; ++s) ms_out[s] = g_timing.ms[s];
+  if (calls_out) *calls_out = g_timing.calls;
+  return MOE_OK;
 }
 
 int moe_get_device_error(int *err_out) {

@@ -12,10 +12,23 @@ namespace moe {
 // expert sort pads every expert to a multiple of it.
 constexpr int kGenericBlockM = 64;
 
+// Optional extra work folded into the sort launch (extra CTAs / outputs).
+struct AlignExtras {
+  float *zero_buf = nullptr;      // zeroed (the stage-2 accumulator)
+  long zero_n = 0;
+  int32_t *offsets = nullptr;     // [El] start of each expert's rows in sorted_ids
+  int32_t *active = nullptr;      // [El] local experts with >= 1 slot, ascending
+  int32_t *n_active = nullptr;    // [1]
+  const uint16_t *x = nullptr;    // bf16 [M, K] -> x16 f16 [M, K] scaled per row by 2^a,
+  void *x16 = nullptr;            //   max |x16| in [2^14, 2^15); x_inv[row] = 2^-a
+  float *x_inv = nullptr;
+  int xM = 0, xK = 0;
+};
+
 cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *expert_map, int E,
                          int El, int BM, int32_t *sorted_ids, int32_t *expert_ids,
-                         int32_t *num_post_pad, int32_t *counts, long cap, float *zero_buf,
-                         long zero_n, cudaStream_t stream);
+                         int32_t *num_post_pad, int32_t *counts, long cap,
+                         const AlignExtras &extra, cudaStream_t stream);
 
 // Quantise rows of x (bf16, or fp32 when x_is_f32) into the activation format
 // `afmt`.  With `sorted_ids` set, the rows are sorted intermediate rows: rows
@@ -67,6 +80,33 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm_w13(const GemmArgs &a, long cap_rows, cudaStream_t stream);
 cudaError_t launch_gemm_w2(const GemmArgs &a, long cap_rows, cudaStream_t stream);
+// Weight-streaming decode kernels (moe_stream.cu), MXFP4 w4a16.
+struct StreamArgs {
+  int M, K, N, T, C;              // C: reduction length (K for w13, N for w2)
+  int units_per_expert, ksplit, kblocks, max_active;
+  int act, gate;
+  float alpha, beta, limit;
+  const void *packed;             // packed weight records
+  const void *bias;               // bf16 [El, R] or null
+  const void *x16;                // f16 rows: x [M, K] (w13) or the intermediate [cap, N] (w2)
+  const float *x_inv;             // w13: per-token inverse scale of x16
+  const int32_t *sorted_ids, *offsets, *counts, *active, *n_active;
+  void *out;                      // w13: f16 intermediate [cap, N]
+  float *acc;                     // w2: fp32 [M, K]
+  const float *topk_weights;
+  int *err;                       // device error word
+};
+struct PackArgs {
+  const unsigned char *codes, *scales;
+  unsigned char *out;
+  long total;
+  int kblocks, units, w13, N, R, C, gate;
+};
+size_t stream_packed_bytes(int w13, int N, int K, int El);
+int stream_units_per_expert(int w13, int N, int K);
+cudaError_t launch_pack_mxfp4(const PackArgs &p, cudaStream_t stream);
+cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream_t stream);
+
 cudaError_t launch_finalize(const float *acc, long n, void *out_bf16, cudaStream_t stream);
 cudaError_t launch_zero(float *buf, long n, cudaStream_t stream);
 

@@ -1,0 +1,374 @@
+// moe_stream.cu -- weight-streaming grouped GEMMs for decode-sized batches of
+// the MXFP4 w4a16 layer (few tokens per expert; the layer is bound by HBM
+// reads of the weights).  Same contract as the generic kernels
+// ("rocm_aiter_fused_experts" on page "vllm.model_executor.layers.fused_moe.
+// experts.rocm_aiter_moe"; MXFP4 layouts and SwiGLU constants from
+// "vLLM/vllm/model_executor/layers/quantization/mxfp4.py").
+//
+// Work unit: (active local expert, tile of 128 weight rows, k-range).  Each
+// unit streams its weight records once through a 4-stage shared-memory ring
+// filled by TMA bulk copies (one producer warp, mbarrier full/empty pairs,
+// every wait bounded); four consumer warps each own two m16 tiles.
+//
+// Arithmetic (swap-AB mma.sync m16n8k16, f16 x f16 -> fp32):
+//   A = weights: e2m1 codes converted two at a time by the hardware
+//       (cvt.rn.f16x2.e2m1x2) -- exact, no scale applied;
+//   B = the expert's tokens (up to 16 per pass, more passes re-stream the
+//       unit), already in f16 in HBM: stage-1 rows scaled per token by a power
+//       of two (exact for bf16 inputs), stage-2 rows are the bounded SwiGLU-OAI
+//       intermediate;
+//   the e8m0 scale of each (row, 32-element group) multiplies the fp32 partial
+//   of that group (two MMAs) into the accumulator.
+// W13 epilogue: x-scale, bias, SwiGLU-OAI of the (gate, up) rows the packed
+// layout pairs inside every m16 tile (rows 0-7 gate, 8-15 up of the same 8
+// outputs), f16 intermediate.  W2 epilogue: bias, router weight, fp32
+// red.add into the token accumulator (the reduce of TopKWeightAndReduceNoOP).
+//
+// Packed weight layout (moe_prepare_weights, load time, like the pages'
+// convert_weight_to_mxfp4_moe_kernel_format): records of 64 reduction
+// elements per unit, [expert][unit][k64][tile(8)][512 B codes | 32 B scales];
+// inside a tile the 512 code bytes are ordered so that lane L reads 16 bytes
+// that hold exactly its A-fragment bytes for two 32-element groups.
+#include <cuda_fp16.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+#include "moe_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int CW = 4;                       // consumer warps
+constexpr int MT = 2;                       // m16 tiles per consumer warp
+constexpr int ROWS = CW * MT * 16;          // 128 weight rows per unit
+constexpr int TILES = CW * MT;              // 8 m16 tiles per unit
+constexpr int TILE_BYTES = 512 + 32;        // codes + scales of one tile, one k64 block
+constexpr int REC_BYTES = TILES * TILE_BYTES;  // 4352 B per (unit, k64 block)
+constexpr int S_KB = 4;                     // k64 blocks per stage (256 reduction elements)
+constexpr int NS = 4;                       // pipeline stages
+constexpr int TOKMAX = 16;                  // tokens per pass (two n8 tiles)
+constexpr int XS = S_KB * 64 * 2 + 16;      // smem row stride of the token tile (528 B)
+constexpr int W_STAGE = S_KB * REC_BYTES;   // 17408 B
+constexpr int X_STAGE = TOKMAX * XS;        // 8448 B
+constexpr int STAGE_BYTES = W_STAGE + X_STAGE;
+constexpr int THREADS = (CW + 1) * 32;
+constexpr size_t SMEM_BYTES = (size_t)NS * STAGE_BYTES + 2 * NS * sizeof(uint64_t) + 16;
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr int kErrTimeout = 5;
+
+enum { MODE_W13 = 0, MODE_W2 = 1 };
+
+struct Unit {
+  int e, u, kb0, nkb, off, cnt;
+};
+
+__device__ __forceinline__ Unit decode_unit(const StreamArgs &a, int id) {
+  Unit r;
+  const int ks = id % a.ksplit;
+  const int rest = id / a.ksplit;
+  r.u = rest % a.units_per_expert;
+  r.e = a.active[rest / a.units_per_expert];
+  const int per = (a.kblocks + a.ksplit - 1) / a.ksplit;
+  r.kb0 = ks * per;
+  r.nkb = min(per, a.kblocks - r.kb0);
+  r.off = a.offsets[r.e];
+  r.cnt = a.counts[r.e];
+  return r;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NS * STAGE_BYTES);
+  uint64_t *empty = full + NS;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NS);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], CW);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  const int n_units = *a.n_active * a.units_per_expert * a.ksplit;
+  const int C = a.C;  // reduction length (K for W13, N for W2)
+
+  if (warp == CW) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int id = blockIdx.x; id < n_units && ok; id += gridDim.x) {
+      const Unit U = decode_unit(a, id);
+      for (int tok0 = 0; tok0 < U.cnt && ok; tok0 += TOKMAX) {
+        const int nt = min(TOKMAX, U.cnt - tok0);
+        // source row of token n of this pass (lane n < nt owns token n)
+        const unsigned char *xrow = nullptr;
+        if (lane < nt) {
+          const int r = U.off + tok0 + lane;
+          const long src = MODE == MODE_W13 ? (long)(a.sorted_ids[r] / a.T) : (long)r;
+          xrow = static_cast<const unsigned char *>(a.x16) + src * (long)C * 2;
+        }
+        for (int kb = 0; kb < U.nkb && ok; kb += S_KB) {
+          const int nkb = min(S_KB, U.nkb - kb);
+          const int slot = it % NS;
+          const uint32_t par = ((it / NS) & 1) ^ 1;
+          if (!mbar_wait_bounded(&empty[slot], par, kWaitCycles)) {
+            record_device_error(a.err, kErrTimeout);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          if (*abort_flag) { ok = false; break; }
+          unsigned char *ws = smem + (size_t)slot * STAGE_BYTES;
+          unsigned char *xs = ws + W_STAGE;
+          const uint32_t wbytes = (uint32_t)nkb * REC_BYTES;
+          const uint32_t xbytes = (uint32_t)nkb * 128;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[slot], wbytes + (uint32_t)nt * xbytes);
+            const unsigned char *src = static_cast<const unsigned char *>(a.packed) +
+                ((((long)U.e * a.units_per_expert + U.u) * a.kblocks) + U.kb0 + kb) * REC_BYTES;
+            tma_bulk_g2s(ws, src, wbytes, &full[slot]);
+          }
+          __syncwarp();
+          if (lane < nt)
+            tma_bulk_g2s(xs + lane * XS, xrow + (long)(U.kb0 + kb) * 128, xbytes, &full[slot]);
+          ++it;
+        }
+      }
+    }
+    // drain: every copy issued into the ring has landed before the CTA exits
+    if (lane == 0) {
+      const uint32_t first = it > NS ? it - NS : 0;
+      for (uint32_t j = first; j < it; ++j)
+        if (!mbar_wait_bounded(&full[j % NS], (j / NS) & 1, kWaitCycles)) {
+          record_device_error(a.err, kErrTimeout);
+          break;
+        }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t it = 0;
+  for (int id = blockIdx.x; id < n_units; id += gridDim.x) {
+    const Unit U = decode_unit(a, id);
+    for (int tok0 = 0; tok0 < U.cnt; tok0 += TOKMAX) {
+      const int nt = min(TOKMAX, U.cnt - tok0);
+      const int ntiles = (nt + 7) >> 3;
+      float acc[MT][2][4];
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[m][n][c] = 0.f;
+
+      for (int kb = 0; kb < U.nkb; kb += S_KB) {
+        const int nkb = min(S_KB, U.nkb - kb);
+        const int slot = it % NS;
+        if (!mbar_wait_bounded(&full[slot], (it / NS) & 1, kWaitCycles)) {
+          record_device_error(a.err, kErrTimeout);
+          *abort_flag = 1;
+        }
+        if (*abort_flag) return;
+        const unsigned char *ws = smem + (size_t)slot * STAGE_BYTES;
+        const uint32_t xs = smem_addr(ws + W_STAGE);
+        for (int b = 0; b < nkb; ++b) {
+          uint4 cw[MT];
+          uint32_t sw[MT];
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const unsigned char *tp = ws + b * REC_BYTES + (warp * MT + m) * TILE_BYTES;
+            cw[m] = *reinterpret_cast<const uint4 *>(tp + lane * 16);
+            sw[m] = *reinterpret_cast<const uint32_t *>(tp + 512 + g * 4);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            float part[MT][2][4];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              // B fragments of both n8 token tiles for this k16 step
+              uint32_t bf[4];
+              const int kl = b * 64 + kk * 32 + q * 16;
+              ldmatrix_x4_b16(bf, xs + ((lane & 7) + ((lane >> 4) << 3)) * XS +
+                                      (kl + ((lane >> 3) & 1) * 8) * 2);
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+                const uint32_t word = kk == 0 ? (q == 0 ? cw[m].x : cw[m].y)
+                                              : (q == 0 ? cw[m].z : cw[m].w);
+                uint32_t af[4];
+                e2m1x8_to_f16x2x4(word, af);
+                if (q == 0) {
+                  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+                  mma_f16_16816(part[m][0], af, bf[0], bf[1], zero);
+                  if (ntiles > 1) mma_f16_16816(part[m][1], af, bf[2], bf[3], zero);
+                } else {
+                  mma_f16_16816(part[m][0], af, bf[0], bf[1], part[m][0]);
+                  if (ntiles > 1) mma_f16_16816(part[m][1], af, bf[2], bf[3], part[m][1]);
+                }
+              }
+            }
+            // e8m0 scales of rows g and g+8 for this 32-element group
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              const uint32_t s_lo = (sw[m] >> (16 * kk)) & 0xff;
+              const uint32_t s_hi = (sw[m] >> (16 * kk + 8)) & 0xff;
+              const float f_lo = s_lo ? __uint_as_float(s_lo << 23) : __uint_as_float(0x00400000u);
+              const float f_hi = s_hi ? __uint_as_float(s_hi << 23) : __uint_as_float(0x00400000u);
+#pragma unroll
+              for (int n = 0; n < 2; ++n) {
+                if (n >= ntiles) break;
+                acc[m][n][0] = fmaf(part[m][n][0], f_lo, acc[m][n][0]);
+                acc[m][n][1] = fmaf(part[m][n][1], f_lo, acc[m][n][1]);
+                acc[m][n][2] = fmaf(part[m][n][2], f_hi, acc[m][n][2]);
+                acc[m][n][3] = fmaf(part[m][n][3], f_hi, acc[m][n][3]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        ++it;
+      }
+
+      // ------------------------------------------------------------ epilogue
+      if (MODE == MODE_W13) {
+        const int N = a.N;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const int j = U.u * 64 + (warp * MT + m) * 8 + g;
+          const long grow = a.gate == GATE_SEPARATED ? j : 2L * j;
+          const long urow = a.gate == GATE_SEPARATED ? (long)N + j : 2L * j + 1;
+          float bg = 0.f, bu = 0.f;
+          if (a.bias) {
+            const uint16_t *bb = static_cast<const uint16_t *>(a.bias) + (long)U.e * 2 * N;
+            bg = bf16_to_f32(bb[grow]);
+            bu = bf16_to_f32(bb[urow]);
+          }
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int tn = n * 8 + 2 * t + c;
+              if (tn >= nt) continue;
+              const int r = U.off + tok0 + tn;
+              const float xi = a.x_inv[a.sorted_ids[r] / a.T];
+              const float gv = acc[m][n][c] * xi + bg;
+              const float uv = acc[m][n][2 + c] * xi + bu;
+              const float z = act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit);
+              static_cast<__half *>(a.out)[(long)r * N + j] = __float2half_rn(z);
+            }
+        }
+      } else {
+        const int K = a.K;
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int i = U.u * ROWS + (warp * MT + m) * 16 + g + 8 * h;
+            if (i >= K) continue;
+            float bias = 0.f;
+            if (a.bias && U.kb0 == 0)
+              bias = bf16_to_f32(static_cast<const uint16_t *>(a.bias)[(long)U.e * K + i]);
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const int tn = n * 8 + 2 * t + c;
+                if (tn >= nt) continue;
+                const int s = a.sorted_ids[U.off + tok0 + tn];
+                const float wt = a.topk_weights[s];
+                atomicAdd(a.acc + (long)(s / a.T) * K + i, wt * (acc[m][n][2 * h + c] + bias));
+              }
+          }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- packing
+// One thread per packed byte.
+__global__ void pack_mxfp4_kernel(PackArgs p) {
+  const long o = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (o >= p.total) return;
+  const long rec = o / REC_BYTES;
+  const int within = (int)(o % REC_BYTES);
+  const int m = within / TILE_BYTES;
+  const int wb = within % TILE_BYTES;
+  const int kb = (int)(rec % p.kblocks);
+  const long eu = rec / p.kblocks;
+  const int u = (int)(eu % p.units);
+  const long e = eu / p.units;
+  int r16, byte_k = 0, grp = 0;
+  bool is_code = wb < 512;
+  if (is_code) {
+    const int lane = wb / 16, bi = wb % 16;
+    const int kk = bi / 8, q = (bi / 4) & 1, reg = bi & 3;
+    const int gg = lane >> 2, tt = lane & 3;
+    r16 = gg + 8 * (reg & 1);
+    byte_k = kb * 64 + kk * 32 + q * 16 + 2 * tt + 8 * (reg >> 1);  // even element index
+  } else {
+    const int sb = wb - 512;
+    const int gg = sb >> 2, s4 = sb & 3;
+    r16 = gg + 8 * (s4 & 1);
+    grp = kb * 2 + (s4 >> 1);
+  }
+  long row = -1;
+  if (p.w13) {
+    const int j = u * 64 + m * 8 + (r16 & 7);
+    const int up = r16 >= 8;
+    if (j < p.N) row = p.gate == GATE_SEPARATED ? (up ? (long)p.N + j : j) : 2L * j + up;
+  } else {
+    const long i = (long)u * ROWS + m * 16 + r16;
+    if (i < p.R) row = i;
+  }
+  unsigned char v;
+  if (is_code) {
+    v = (row >= 0 && byte_k < p.C) ? p.codes[((long)e * p.R + row) * (p.C / 2) + byte_k / 2] : 0;
+  } else {
+    v = (row >= 0 && grp < p.C / 32) ? p.scales[((long)e * p.R + row) * (p.C / 32) + grp] : 127;
+  }
+  p.out[o] = v;
+}
+
+}  // namespace
+
+size_t stream_packed_bytes(int w13, int N, int K, int El) {
+  const int units = w13 ? N / 64 : (int)ceil_div(K, ROWS);
+  const int C = w13 ? K : N;
+  const int kblocks = (int)ceil_div(C, 64);
+  return (size_t)El * units * kblocks * REC_BYTES;
+}
+
+cudaError_t launch_pack_mxfp4(const PackArgs &p, cudaStream_t stream) {
+  if (p.total <= 0) return cudaSuccess;
+  pack_mxfp4_kernel<<<(unsigned)ceil_div(p.total, 256), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+int stream_units_per_expert(int w13, int N, int K) { return w13 ? N / 64 : (int)ceil_div(K, ROWS); }
+
+cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream_t stream) {
+  auto kern = w13 ? stream_kernel<MODE_W13> : stream_kernel<MODE_W2>;
+  static bool attr_done[2] = {false, false};
+  if (!attr_done[w13]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[w13] = true;
+  }
+  const long max_units = (long)a.max_active * a.units_per_expert * a.ksplit;
+  long grid = 2L * sm_count;
+  if (grid > max_units) grid = max_units;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -35,7 +35,7 @@ def test_header_symbols_are_exported(moe):
     L = moe.lib()
     for name in declared:
         assert hasattr(L, name), name
-    assert moe.moe_abi_version() == 1
+    assert moe.moe_abi_version() == 2
 
 
 def test_status_strings(moe):
@@ -96,3 +96,18 @@ def test_quant_and_align_validation(moe):
     assert L.moe_quant_act(fake, 4, 32, 1, None, fake, fake, None) == 1   # static scale missing
     assert L.moe_align_block_size(fake, 4, 2, None, 8, 2000, 64, fake, fake, fake, None, None) == 1
     assert L.moe_align_block_size(fake, 4, 2, None, 8, 8, 0, fake, fake, fake, None, None) == 1
+
+
+def test_packed_weight_sizes(moe):
+    # records of 64 reduction elements x 128 rows: 8 tiles x (512 B codes + 32 B scales)
+    p = moe.make_problem(64, 2880, 2880, 4, 32, 32, "mxfp4", "bf16", "swiglu_oai", "interleaved")
+    w13 = moe.moe_packed_weight_bytes(p, 0)
+    w2 = moe.moe_packed_weight_bytes(p, 1)
+    assert w13 == 32 * (2880 // 64) * (2880 // 64) * 4352
+    assert w2 == 32 * 23 * (2880 // 64) * 4352       # ceil(2880 / 128) row tiles
+    # same payload as the canonical codes + scales (up to the padded last row tile)
+    assert w13 == 32 * 5760 * (2880 // 2 + 2880 // 32)
+    q = moe.make_problem(64, 2880, 2880, 4, 32, 32, "bf16", "bf16", "silu", "separated")
+    assert moe.moe_packed_weight_bytes(q, 0) == 0
+    r = moe.make_problem(64, 2880, 2848, 4, 32, 32, "mxfp4", "bf16", "silu", "separated")
+    assert moe.moe_packed_weight_bytes(r, 0) == 0     # N % 64 != 0: no streaming layout
