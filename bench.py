@@ -137,8 +137,16 @@ def algorithmic(wl, counts):
     out = wl.M * wl.K * 2
     ids = wl.M * wl.T * 8
     return dict(w13_bytes=w13, w2_bytes=w2, layer_bytes=w13 + w2 + act + out + ids,
-                w13_kernel_bytes=w13 + act, flops=6.0 * wl.N * wl.K * live, live_slots=live,
-                active_experts=len(active))
+                w13_kernel_bytes=w13 + act, flops=6.0 * wl.N * wl.K * live,
+                w13_flops=4.0 * wl.N * wl.K * live, live_slots=live, active_experts=len(active))
+
+
+def mma_dtype(wl):
+    """Operand type of the tensor-core contraction the CUDA path runs for this
+    workload (every format is decoded exactly into 16-bit operands)."""
+    if wl.wfmt == "mxfp4" and wl.afmt == "bf16":
+        return "f16"
+    return "bf16"
 
 
 def measured_peaks():
@@ -329,7 +337,13 @@ def run_ours(args):
     # dominant kernel (w13 GEMM + activation), timed alone on its own stream
     k_ms, stage_ms = time_w13_kernel(moe, wl, layer, dev, stream, max(args.steps, 50))
     hbm, bf16_tf, peak_src = measured_peaks()
-    achieved = alg["w13_kernel_bytes"] / (k_ms / 1e3) / 1e9
+    t_hbm = alg["w13_kernel_bytes"] / (hbm * 1e9)
+    t_tensor = alg["w13_flops"] / (bf16_tf * 1e12)  # f16 and bf16 share the dense rate
+    if t_hbm >= t_tensor:
+        bound, achieved, peak, punit = "hbm", alg["w13_kernel_bytes"] / (k_ms / 1e3) / 1e9, hbm, "GB/s"
+    else:
+        bound, achieved, peak, punit = ("tensor", alg["w13_flops"] / (k_ms / 1e3) / 1e12, bf16_tf,
+                                        "TFLOP/s")
     traffic = profile_traffic("moe_w13", wl.name)
     layer_roof_ms = max(alg["layer_bytes"] / (hbm * 1e9), alg["flops"] / (bf16_tf * 1e12)) * 1e3
 
@@ -339,15 +353,16 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": mma_dtype(wl), "data": "synthetic",
         "config": dict(workload_config(wl), parallelism=f"replicas{world}",
                        l2="no flush: each step streams all active experts' weights "
                           f"({alg['w13_bytes'] + alg['w2_bytes']} B > 129 MB L2)",
                        launch="CUDA graph of one step"),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": punit,
+                     "frac": achieved / peak, "traffic": traffic, "mma_dtype": mma_dtype(wl),
                      "kernel": "w13 grouped GEMM + activation",
                      "alg_bytes_per_launch": alg["w13_kernel_bytes"],
+                     "alg_flops_per_launch": alg["w13_flops"],
                      "kernel_ms": k_ms, "peak_source": peak_src,
                      "stage_ms": stage_ms},
         "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms,
@@ -358,7 +373,8 @@ def run_ours(args):
         "clocks": summarize_clocks(rows, "warmup soak + timed region"),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds,
+                                            max_tokens=None if wl.M <= 128 else 32)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:

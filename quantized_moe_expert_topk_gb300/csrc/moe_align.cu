@@ -55,15 +55,50 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
     return;
   }
   if ((int)blockIdx.x > zero_ctas) {
-    // conversion CTAs: one warp per row of x; bf16 -> f16 scaled by 2^a so
-    // that the row maximum lands in [2^14, 2^15) (exact for bf16 values)
-    const int wid = ((int)blockIdx.x - 1 - zero_ctas) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    // conversion CTAs: 128 threads per row of x, 8 rows per CTA; bf16 -> f16
+    // scaled by 2^a so that the row maximum lands in [2^14, 2^15) (exact for
+    // bf16 values).  Rows are 16-byte aligned (K % 64 == 0, checked by the
+    // caller); up to 4 x 8 values per thread stay in registers between the
+    // max pass and the convert pass.
+    __shared__ float red[kAlignThreads / 128][4];
+    const int k8 = x.xK / 8;
+    const int tr = threadIdx.x & 127, rsub = threadIdx.x >> 7, wr = tr >> 5;
     const int lane = threadIdx.x & 31;
-    for (int r = wid; r < x.xM; r += conv_ctas * (blockDim.x >> 5)) {
-      const uint16_t *xr = x.x + (long)r * x.xK;
+    const int rows_per_cta = blockDim.x / 128;
+    for (int base = ((int)blockIdx.x - 1 - zero_ctas) * rows_per_cta; base < x.xM;
+         base += conv_ctas * rows_per_cta) {
+      const int r = base + rsub;
+      const bool valid = r < x.xM;
+      const uint4 *xr = reinterpret_cast<const uint4 *>(x.x + (long)(valid ? r : 0) * x.xK);
+      uint4 v[4];
       float amax = 0.f;
-      for (int c = lane; c < x.xK; c += 32) amax = fmaxf(amax, fabsf(bf16_to_f32(xr[c])));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = tr + i * 128;
+        v[i] = (valid && c < k8) ? xr[c] : make_uint4(0, 0, 0, 0);
+      }
+      for (int c = tr + 512; valid && c < k8; c += 128) {
+        const uint4 u = xr[c];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[q] << 16)),
+                                   fabsf(__uint_as_float(w[q] & 0xffff0000u))));
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[q] << 16)),
+                                   fabsf(__uint_as_float(w[q] & 0xffff0000u))));
+      }
       amax = warp_max(amax);
+      if (lane == 0) red[rsub][wr] = amax;
+      __syncthreads();
+      amax = fmaxf(fmaxf(red[rsub][0], red[rsub][1]), fmaxf(red[rsub][2], red[rsub][3]));
+      __syncthreads();
+      if (!valid) continue;
       int a = 0;
       if (amax > 0.f) {
         int ex;
@@ -71,9 +106,25 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
         a = 15 - ex;
       }
       const float mul = ldexpf(1.0f, a);
-      __half *dst = static_cast<__half *>(x.x16) + (long)r * x.xK;
-      for (int c = lane; c < x.xK; c += 32) dst[c] = __float2half_rn(bf16_to_f32(xr[c]) * mul);
-      if (lane == 0) x.x_inv[r] = ldexpf(1.0f, -a);
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(x.x16) + (long)r * x.xK);
+      auto convert = [&](const uint4 &u) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const __half2 h = __floats2half2_rn(__uint_as_float(w[q] << 16) * mul,
+                                              __uint_as_float(w[q] & 0xffff0000u) * mul);
+          o[q] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+      };
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = tr + i * 128;
+        if (c < k8) dst[c] = convert(v[i]);
+      }
+      for (int c = tr + 512; c < k8; c += 128) dst[c] = convert(xr[c]);
+      if (tr == 0) x.x_inv[r] = ldexpf(1.0f, -a);
     }
     return;
   }
@@ -182,7 +233,10 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
   }
   for (long i = total + threadIdx.x; i < cap; i += blockDim.x) sorted[i] = (int32_t)S;
   for (long b = total / BM + threadIdx.x; b < cap / BM; b += blockDim.x) expert_ids[b] = -1;
-  if (threadIdx.x == 0) *ntp = total;
+  if (threadIdx.x == 0) {
+    *ntp = total;
+    if (x.counters) x.counters[0] = x.counters[1] = 0;
+  }
 }
 
 }  // namespace
@@ -207,7 +261,7 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *e
     if (zero_ctas > 4 * 152) zero_ctas = 4 * 152;
   }
   if (extra.x && extra.xM > 0) {
-    conv_ctas = (int)ceil_div(extra.xM, kAlignWarps);
+    conv_ctas = (int)ceil_div(extra.xM, kAlignThreads / 128);
     if (conv_ctas > 2 * 152) conv_ctas = 2 * 152;
   }
   align_kernel<<<1 + zero_ctas + conv_ctas, kAlignThreads, smem, stream>>>(

@@ -103,7 +103,7 @@ int validate_weight(const moe_problem_t *p, const moe_weight_t *w) {
 // Workspace layout of moe_fused_experts.
 struct Layout {
   long cap, blocks;
-  size_t sorted, expert_ids, ntp, counts, offsets, active, n_active, x16, x_inv, a1_codes,
+  size_t sorted, expert_ids, ntp, counts, offsets, active, n_active, counters, x16, x_inv, a1_codes,
       a1_scales, inter, inter_scales, staging, acc, total;
 };
 
@@ -121,6 +121,7 @@ Layout make_layout(const moe_problem_t *p) {
   L.offsets = o; o = align_up(o + (size_t)p->num_local_experts * 4);
   L.active = o; o = align_up(o + (size_t)p->num_local_experts * 4);
   L.n_active = o; o = align_up(o + 4);
+  L.counters = o; o = align_up(o + 8);
   if (p->wfmt == W_MXFP4 && p->afmt == A_BF16) {  // f16 copy of x for the streaming kernels
     L.x16 = o; o = align_up(o + (size_t)p->M * p->K * 2);
     L.x_inv = o; o = align_up(o + (size_t)p->M * 4);
@@ -433,6 +434,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     ex.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
     ex.active = reinterpret_cast<int32_t *>(ws + L.active);
     ex.n_active = reinterpret_cast<int32_t *>(ws + L.n_active);
+    ex.counters = reinterpret_cast<int32_t *>(ws + L.counters);
     ex.x = static_cast<const uint16_t *>(hidden_bf16);
     ex.x16 = ws + L.x16;
     ex.x_inv = reinterpret_cast<float *>(ws + L.x_inv);
@@ -467,6 +469,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     s13.packed = w13->packed; s13.bias = w13->bias;
     s13.x16 = ex.x16; s13.x_inv = ex.x_inv;
     s13.out = ws + L.inter;
+    s13.work_counter = ex.counters;
     {
       StageScope sc(MOE_STAGE_W13, st);
       rc = cuda_status(launch_stream(s13, 1, dinfo.sm_count, st));
@@ -482,6 +485,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     s2.packed = w2->packed; s2.bias = w2->bias;
     s2.x16 = ws + L.inter;
     s2.acc = acc; s2.topk_weights = topk_weights;
+    s2.work_counter = ex.counters + 1;
     {
       StageScope sc(MOE_STAGE_W2, st);
       rc = cuda_status(launch_stream(s2, 0, dinfo.sm_count, st));

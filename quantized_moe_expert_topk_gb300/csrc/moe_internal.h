@@ -19,6 +19,7 @@ struct AlignExtras {
   int32_t *offsets = nullptr;     // [El] start of each expert's rows in sorted_ids
   int32_t *active = nullptr;      // [El] local experts with >= 1 slot, ascending
   int32_t *n_active = nullptr;    // [1]
+  int32_t *counters = nullptr;    // [2] work counters of the streaming kernels, zeroed
   const uint16_t *x = nullptr;    // bf16 [M, K] -> x16 f16 [M, K] scaled per row by 2^a,
   void *x16 = nullptr;            //   max |x16| in [2^14, 2^15); x_inv[row] = 2^-a
   float *x_inv = nullptr;
@@ -95,6 +96,7 @@ struct StreamArgs {
   float *acc;                     // w2: fp32 [M, K]
   const float *topk_weights;
   int *err;                       // device error word
+  int *work_counter;              // zero at launch; units are claimed from it
 };
 struct PackArgs {
   const unsigned char *codes, *scales;

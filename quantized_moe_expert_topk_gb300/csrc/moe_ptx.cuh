@@ -51,10 +51,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
                                                   long long limit_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > limit_cycles) return false;
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    // the clock is read every 64 polls only (try_wait itself suspends the
+    // thread for a short while when the phase is not complete)
+    if ((n & 63) == 0 && clock64() - t0 > limit_cycles) return false;
   }
-  return true;
 }
 
 // TMA bulk copy global -> shared (this CTA), completing `bytes` of

@@ -5,10 +5,13 @@
 // experts.rocm_aiter_moe"; MXFP4 layouts and SwiGLU constants from
 // "vLLM/vllm/model_executor/layers/quantization/mxfp4.py").
 //
-// Work unit: (active local expert, tile of 128 weight rows, k-range).  Each
-// unit streams its weight records once through a 4-stage shared-memory ring
-// filled by TMA bulk copies (one producer warp, mbarrier full/empty pairs,
-// every wait bounded); four consumer warps each own two m16 tiles.
+// Work unit: (active local expert, tile of 128 weight rows, k-range).  Units
+// are claimed dynamically from a global counter (persistent CTAs, four per
+// SM); each unit streams its weight records once through a 4-stage
+// shared-memory ring filled by TMA bulk copies (one producer warp, mbarrier
+// full/empty pairs, every wait bounded, a descriptor per stage telling the
+// consumers which unit/pass/k-block it holds); four consumer warps each own
+// two m16 tiles.
 //
 // Arithmetic (swap-AB mma.sync m16n8k16, f16 x f16 -> fp32):
 //   A = weights: e2m1 codes converted two at a time by the hardware
@@ -45,19 +48,37 @@ constexpr int ROWS = CW * MT * 16;          // 128 weight rows per unit
 constexpr int TILES = CW * MT;              // 8 m16 tiles per unit
 constexpr int TILE_BYTES = 512 + 32;        // codes + scales of one tile, one k64 block
 constexpr int REC_BYTES = TILES * TILE_BYTES;  // 4352 B per (unit, k64 block)
-constexpr int S_KB = 4;                     // k64 blocks per stage (256 reduction elements)
+constexpr int S_KB = 2;                     // k64 blocks per stage (128 reduction elements)
 constexpr int NS = 4;                       // pipeline stages
 constexpr int TOKMAX = 16;                  // tokens per pass (two n8 tiles)
-constexpr int XS = S_KB * 64 * 2 + 16;      // smem row stride of the token tile (528 B)
-constexpr int W_STAGE = S_KB * REC_BYTES;   // 17408 B
-constexpr int X_STAGE = TOKMAX * XS;        // 8448 B
+constexpr int XS = S_KB * 64 * 2 + 16;      // smem row stride of the token tile (272 B)
+constexpr int W_STAGE = S_KB * REC_BYTES;   // 8704 B
+constexpr int X_STAGE = TOKMAX * XS;        // 4352 B
 constexpr int STAGE_BYTES = W_STAGE + X_STAGE;
 constexpr int THREADS = (CW + 1) * 32;
-constexpr size_t SMEM_BYTES = (size_t)NS * STAGE_BYTES + 2 * NS * sizeof(uint64_t) + 16;
+constexpr int CTAS_PER_SM = 4;
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int kErrTimeout = 5;
 
 enum { MODE_W13 = 0, MODE_W2 = 1 };
+enum { F_FIRST = 1, F_LAST = 2 };
+
+// Stage descriptor written by the producer next to the data it loads.
+struct StageDesc {
+  int id;    // unit id, -1 = no more work
+  int tok0;  // first token of this pass
+  int kb;    // first k64 block of this stage within the unit's k-range
+  int flags; // F_FIRST / F_LAST: first / last stage of the pass
+};
+
+struct Smem {
+  unsigned char stage[NS][STAGE_BYTES];
+  uint64_t full[NS];
+  uint64_t empty[NS];
+  StageDesc desc[NS];
+  int abort_flag;
+};
+constexpr size_t SMEM_BYTES = sizeof(Smem);
 
 struct Unit {
   int e, u, kb0, nkb, off, cnt;
@@ -77,66 +98,149 @@ __device__ __forceinline__ Unit decode_unit(const StreamArgs &a, int id) {
   return r;
 }
 
+// Byte `idx` of `w` (an e8m0 code c) as the fp32 value 2^(c-127): the byte is
+// moved to the top byte and shifted right once into the exponent field.  Code
+// 0 (2^-127, below the fp32 normal range) reads as 0.
+__device__ __forceinline__ float e8m0_byte_f32(uint32_t w, uint32_t idx) {
+  return __uint_as_float(__byte_perm(w, 0u, 0x0444u | (idx << 12)) >> 1);
+}
+
+// One k64 block of one consumer warp: MT m16 tiles x NTILES n8 token tiles.
+template <int NTILES>
+__device__ __forceinline__ void consume_k64(const unsigned char *tp0, uint32_t xs_k64, int lane,
+                                            float (&acc)[MT][2][4]) {
+  const int g = lane >> 2;
+  uint4 cw[MT];
+  uint32_t sw[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    const unsigned char *tp = tp0 + m * TILE_BYTES;
+    cw[m] = *reinterpret_cast<const uint4 *>(tp + lane * 16);
+    sw[m] = *reinterpret_cast<const uint32_t *>(tp + 512 + g * 4);
+  }
+  // B fragments of the four k16 steps (both n8 token tiles)
+  uint32_t bf[4][4];
+#pragma unroll
+  for (int s4 = 0; s4 < 4; ++s4) {
+    const uint32_t addr = xs_k64 + ((lane & 7) + ((lane >> 4) << 3)) * XS +
+                          (s4 * 16 + ((lane >> 3) & 1) * 8) * 2;
+    if (NTILES == 2) {
+      ldmatrix_x4_b16(bf[s4], addr);
+    } else {
+      uint32_t r2[2];
+      ldmatrix_x2_b16(r2, addr);
+      bf[s4][0] = r2[0];
+      bf[s4][1] = r2[1];
+    }
+  }
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    float part[MT][NTILES][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      uint32_t a0[4], a1[4];
+      e2m1x8_to_f16x2x4(kk == 0 ? cw[m].x : cw[m].z, a0);
+      e2m1x8_to_f16x2x4(kk == 0 ? cw[m].y : cw[m].w, a1);
+      const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int n = 0; n < NTILES; ++n) {
+        mma_f16_16816(part[m][n], a0, bf[2 * kk][2 * n], bf[2 * kk][2 * n + 1], zero);
+        mma_f16_16816(part[m][n], a1, bf[2 * kk + 1][2 * n], bf[2 * kk + 1][2 * n + 1],
+                      part[m][n]);
+      }
+    }
+    // e8m0 scales of rows g and g+8 for this 32-element group
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const float f_lo = e8m0_byte_f32(sw[m], 2 * kk);
+      const float f_hi = e8m0_byte_f32(sw[m], 2 * kk + 1);
+#pragma unroll
+      for (int n = 0; n < NTILES; ++n) {
+        acc[m][n][0] = fmaf(part[m][n][0], f_lo, acc[m][n][0]);
+        acc[m][n][1] = fmaf(part[m][n][1], f_lo, acc[m][n][1]);
+        acc[m][n][2] = fmaf(part[m][n][2], f_hi, acc[m][n][2]);
+        acc[m][n][3] = fmaf(part[m][n][3], f_hi, acc[m][n][3]);
+      }
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NS * STAGE_BYTES);
-  uint64_t *empty = full + NS;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NS);
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CW);
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], CW);
     }
-    *abort_flag = 0;
+    sm.abort_flag = 0;
     mbar_fence_init();
   }
   __syncthreads();
+  volatile int *abort_flag = &sm.abort_flag;
 
   const int n_units = *a.n_active * a.units_per_expert * a.ksplit;
   const int C = a.C;  // reduction length (K for W13, N for W2)
 
   if (warp == CW) {
     // ------------------------------------------------------------ producer
+    // Claims units from a global counter (dynamic load balance), streams each
+    // unit's weight records and the matching token rows into the ring, and
+    // ends with a terminator stage.
     uint32_t it = 0;
     bool ok = true;
-    for (int id = blockIdx.x; id < n_units && ok; id += gridDim.x) {
+    auto acquire_slot = [&](int &slot) -> bool {
+      slot = it % NS;
+      if (!mbar_wait_bounded(&sm.empty[slot], ((it / NS) & 1) ^ 1, kWaitCycles)) {
+        record_device_error(a.err, kErrTimeout);
+        *abort_flag = 1;
+      }
+      return !*abort_flag;
+    };
+    while (ok) {
+      int id = 0;
+      if (lane == 0) id = atomicAdd(a.work_counter, 1);
+      id = __shfl_sync(0xffffffffu, id, 0);
+      if (id >= n_units) {
+        int slot;
+        if (acquire_slot(slot) && lane == 0) {
+          sm.desc[slot] = StageDesc{-1, 0, 0, 0};
+          mbar_arrive(&sm.full[slot]);
+        }
+        ++it;
+        break;
+      }
       const Unit U = decode_unit(a, id);
       for (int tok0 = 0; tok0 < U.cnt && ok; tok0 += TOKMAX) {
         const int nt = min(TOKMAX, U.cnt - tok0);
-        // source row of token n of this pass (lane n < nt owns token n)
-        const unsigned char *xrow = nullptr;
+        const unsigned char *xrow = nullptr;  // lane n < nt loads token n of this pass
         if (lane < nt) {
           const int r = U.off + tok0 + lane;
           const long src = MODE == MODE_W13 ? (long)(a.sorted_ids[r] / a.T) : (long)r;
           xrow = static_cast<const unsigned char *>(a.x16) + src * (long)C * 2;
         }
-        for (int kb = 0; kb < U.nkb && ok; kb += S_KB) {
+        for (int kb = 0; kb < U.nkb; kb += S_KB) {
           const int nkb = min(S_KB, U.nkb - kb);
-          const int slot = it % NS;
-          const uint32_t par = ((it / NS) & 1) ^ 1;
-          if (!mbar_wait_bounded(&empty[slot], par, kWaitCycles)) {
-            record_device_error(a.err, kErrTimeout);
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          if (*abort_flag) { ok = false; break; }
-          unsigned char *ws = smem + (size_t)slot * STAGE_BYTES;
-          unsigned char *xs = ws + W_STAGE;
+          int slot;
+          if (!acquire_slot(slot)) { ok = false; break; }
+          unsigned char *ws = sm.stage[slot];
           const uint32_t wbytes = (uint32_t)nkb * REC_BYTES;
           const uint32_t xbytes = (uint32_t)nkb * 128;
           if (lane == 0) {
-            mbar_arrive_expect_tx(&full[slot], wbytes + (uint32_t)nt * xbytes);
+            sm.desc[slot] = StageDesc{id, tok0, kb, (kb == 0 ? F_FIRST : 0) |
+                                                     (kb + S_KB >= U.nkb ? F_LAST : 0)};
+            mbar_arrive_expect_tx(&sm.full[slot], wbytes + (uint32_t)nt * xbytes);
             const unsigned char *src = static_cast<const unsigned char *>(a.packed) +
                 ((((long)U.e * a.units_per_expert + U.u) * a.kblocks) + U.kb0 + kb) * REC_BYTES;
-            tma_bulk_g2s(ws, src, wbytes, &full[slot]);
+            tma_bulk_g2s(ws, src, wbytes, &sm.full[slot]);
           }
           __syncwarp();
           if (lane < nt)
-            tma_bulk_g2s(xs + lane * XS, xrow + (long)(U.kb0 + kb) * 128, xbytes, &full[slot]);
+            tma_bulk_g2s(ws + W_STAGE + lane * XS, xrow + (long)(U.kb0 + kb) * 128, xbytes,
+                         &sm.full[slot]);
           ++it;
         }
       }
@@ -145,7 +249,7 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
     if (lane == 0) {
       const uint32_t first = it > NS ? it - NS : 0;
       for (uint32_t j = first; j < it; ++j)
-        if (!mbar_wait_bounded(&full[j % NS], (j / NS) & 1, kWaitCycles)) {
+        if (!mbar_wait_bounded(&sm.full[j % NS], (j / NS) & 1, kWaitCycles)) {
           record_device_error(a.err, kErrTimeout);
           break;
         }
@@ -156,138 +260,102 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, t = lane & 3;
   uint32_t it = 0;
-  for (int id = blockIdx.x; id < n_units; id += gridDim.x) {
-    const Unit U = decode_unit(a, id);
-    for (int tok0 = 0; tok0 < U.cnt; tok0 += TOKMAX) {
-      const int nt = min(TOKMAX, U.cnt - tok0);
-      const int ntiles = (nt + 7) >> 3;
-      float acc[MT][2][4];
+  Unit U = {0, 0, 0, 0, 0, 0};
+  int nt = 0, ntiles = 0;
+  float acc[MT][2][4];
+  while (true) {
+    const int slot = it % NS;
+    if (!mbar_wait_bounded(&sm.full[slot], (it / NS) & 1, kWaitCycles)) {
+      record_device_error(a.err, kErrTimeout);
+      *abort_flag = 1;
+    }
+    if (*abort_flag) return;
+    StageDesc d;
+    {
+      const volatile int *dv = reinterpret_cast<const volatile int *>(&sm.desc[slot]);
+      d.id = dv[0];
+      d.tok0 = dv[1];
+      d.kb = dv[2];
+      d.flags = dv[3];
+    }
+    if (d.id < 0) break;
+    if (d.flags & F_FIRST) {
+      U = decode_unit(a, d.id);
+      nt = min(TOKMAX, U.cnt - d.tok0);
+      ntiles = (nt + 7) >> 3;
 #pragma unroll
       for (int m = 0; m < MT; ++m)
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int c = 0; c < 4; ++c) acc[m][n][c] = 0.f;
+    }
+    const int nkb = min(S_KB, U.nkb - d.kb);
+    const unsigned char *ws = sm.stage[slot];
+    const uint32_t xs = smem_addr(ws + W_STAGE);
+#pragma unroll
+    for (int b = 0; b < S_KB; ++b) {
+      if (b >= nkb) break;
+      const unsigned char *tp0 = ws + b * REC_BYTES + (warp * MT) * TILE_BYTES;
+      if (ntiles == 2) consume_k64<2>(tp0, xs + b * 128, lane, acc);
+      else consume_k64<1>(tp0, xs + b * 128, lane, acc);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    ++it;
+    if (!(d.flags & F_LAST)) continue;
 
-      for (int kb = 0; kb < U.nkb; kb += S_KB) {
-        const int nkb = min(S_KB, U.nkb - kb);
-        const int slot = it % NS;
-        if (!mbar_wait_bounded(&full[slot], (it / NS) & 1, kWaitCycles)) {
-          record_device_error(a.err, kErrTimeout);
-          *abort_flag = 1;
+    // -------------------------------------------------------------- epilogue
+    const int tok0 = d.tok0;
+    if (MODE == MODE_W13) {
+      const int N = a.N;
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const int j = U.u * 64 + (warp * MT + m) * 8 + g;
+        const long grow = a.gate == GATE_SEPARATED ? j : 2L * j;
+        const long urow = a.gate == GATE_SEPARATED ? (long)N + j : 2L * j + 1;
+        float bg = 0.f, bu = 0.f;
+        if (a.bias) {
+          const uint16_t *bb = static_cast<const uint16_t *>(a.bias) + (long)U.e * 2 * N;
+          bg = bf16_to_f32(bb[grow]);
+          bu = bf16_to_f32(bb[urow]);
         }
-        if (*abort_flag) return;
-        const unsigned char *ws = smem + (size_t)slot * STAGE_BYTES;
-        const uint32_t xs = smem_addr(ws + W_STAGE);
-        for (int b = 0; b < nkb; ++b) {
-          uint4 cw[MT];
-          uint32_t sw[MT];
 #pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            const unsigned char *tp = ws + b * REC_BYTES + (warp * MT + m) * TILE_BYTES;
-            cw[m] = *reinterpret_cast<const uint4 *>(tp + lane * 16);
-            sw[m] = *reinterpret_cast<const uint32_t *>(tp + 512 + g * 4);
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int tn = n * 8 + 2 * t + c;
+            if (tn >= nt) continue;
+            const int r = U.off + tok0 + tn;
+            const float xi = a.x_inv[a.sorted_ids[r] / a.T];
+            const float gv = acc[m][n][c] * xi + bg;
+            const float uv = acc[m][n][2 + c] * xi + bu;
+            const float z = act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit);
+            static_cast<__half *>(a.out)[(long)r * N + j] = __float2half_rn(z);
           }
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            float part[MT][2][4];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              // B fragments of both n8 token tiles for this k16 step
-              uint32_t bf[4];
-              const int kl = b * 64 + kk * 32 + q * 16;
-              ldmatrix_x4_b16(bf, xs + ((lane & 7) + ((lane >> 4) << 3)) * XS +
-                                      (kl + ((lane >> 3) & 1) * 8) * 2);
-#pragma unroll
-              for (int m = 0; m < MT; ++m) {
-                const uint32_t word = kk == 0 ? (q == 0 ? cw[m].x : cw[m].y)
-                                              : (q == 0 ? cw[m].z : cw[m].w);
-                uint32_t af[4];
-                e2m1x8_to_f16x2x4(word, af);
-                if (q == 0) {
-                  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-                  mma_f16_16816(part[m][0], af, bf[0], bf[1], zero);
-                  if (ntiles > 1) mma_f16_16816(part[m][1], af, bf[2], bf[3], zero);
-                } else {
-                  mma_f16_16816(part[m][0], af, bf[0], bf[1], part[m][0]);
-                  if (ntiles > 1) mma_f16_16816(part[m][1], af, bf[2], bf[3], part[m][1]);
-                }
-              }
-            }
-            // e8m0 scales of rows g and g+8 for this 32-element group
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              const uint32_t s_lo = (sw[m] >> (16 * kk)) & 0xff;
-              const uint32_t s_hi = (sw[m] >> (16 * kk + 8)) & 0xff;
-              const float f_lo = s_lo ? __uint_as_float(s_lo << 23) : __uint_as_float(0x00400000u);
-              const float f_hi = s_hi ? __uint_as_float(s_hi << 23) : __uint_as_float(0x00400000u);
-#pragma unroll
-              for (int n = 0; n < 2; ++n) {
-                if (n >= ntiles) break;
-                acc[m][n][0] = fmaf(part[m][n][0], f_lo, acc[m][n][0]);
-                acc[m][n][1] = fmaf(part[m][n][1], f_lo, acc[m][n][1]);
-                acc[m][n][2] = fmaf(part[m][n][2], f_hi, acc[m][n][2]);
-                acc[m][n][3] = fmaf(part[m][n][3], f_hi, acc[m][n][3]);
-              }
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        ++it;
       }
-
-      // ------------------------------------------------------------ epilogue
-      if (MODE == MODE_W13) {
-        const int N = a.N;
+    } else {
+      const int K = a.K;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          const int j = U.u * 64 + (warp * MT + m) * 8 + g;
-          const long grow = a.gate == GATE_SEPARATED ? j : 2L * j;
-          const long urow = a.gate == GATE_SEPARATED ? (long)N + j : 2L * j + 1;
-          float bg = 0.f, bu = 0.f;
-          if (a.bias) {
-            const uint16_t *bb = static_cast<const uint16_t *>(a.bias) + (long)U.e * 2 * N;
-            bg = bf16_to_f32(bb[grow]);
-            bu = bf16_to_f32(bb[urow]);
-          }
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = U.u * ROWS + (warp * MT + m) * 16 + g + 8 * h;
+          if (i >= K) continue;
+          float bias = 0.f;
+          if (a.bias && U.kb0 == 0)
+            bias = bf16_to_f32(static_cast<const uint16_t *>(a.bias)[(long)U.e * K + i]);
 #pragma unroll
           for (int n = 0; n < 2; ++n)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
               const int tn = n * 8 + 2 * t + c;
               if (tn >= nt) continue;
-              const int r = U.off + tok0 + tn;
-              const float xi = a.x_inv[a.sorted_ids[r] / a.T];
-              const float gv = acc[m][n][c] * xi + bg;
-              const float uv = acc[m][n][2 + c] * xi + bu;
-              const float z = act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit);
-              static_cast<__half *>(a.out)[(long)r * N + j] = __float2half_rn(z);
+              const int sidx = a.sorted_ids[U.off + tok0 + tn];
+              const float wt = a.topk_weights[sidx];
+              atomicAdd(a.acc + (long)(sidx / a.T) * K + i, wt * (acc[m][n][2 * h + c] + bias));
             }
         }
-      } else {
-        const int K = a.K;
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int i = U.u * ROWS + (warp * MT + m) * 16 + g + 8 * h;
-            if (i >= K) continue;
-            float bias = 0.f;
-            if (a.bias && U.kb0 == 0)
-              bias = bf16_to_f32(static_cast<const uint16_t *>(a.bias)[(long)U.e * K + i]);
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                const int tn = n * 8 + 2 * t + c;
-                if (tn >= nt) continue;
-                const int s = a.sorted_ids[U.off + tok0 + tn];
-                const float wt = a.topk_weights[s];
-                atomicAdd(a.acc + (long)(s / a.T) * K + i, wt * (acc[m][n][2 * h + c] + bias));
-              }
-          }
-      }
     }
   }
 }
@@ -364,7 +432,7 @@ cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream
     attr_done[w13] = true;
   }
   const long max_units = (long)a.max_active * a.units_per_expert * a.ksplit;
-  long grid = 2L * sm_count;
+  long grid = (long)CTAS_PER_SM * sm_count;
   if (grid > max_units) grid = max_units;
   if (grid <= 0) return cudaSuccess;
   kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(a);
