@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef enum {
   MOE_OK = 0,
@@ -96,7 +96,10 @@ typedef struct {
   const void *bias;          /* optional [E_l,R]: bf16, or f32 if bias_is_f32 */
   int bias_is_f32;
   const void *packed;        /* optional: the same weights repacked by moe_prepare_weights
-                                (MXFP4 only); enables the weight-streaming decode kernels */
+                                (MOE_LAYOUT_STREAM, MXFP4); enables the weight-streaming
+                                decode kernels */
+  const void *packed_tc;     /* optional: repacked with MOE_LAYOUT_TC (MXFP4 / NVFP4);
+                                enables the tcgen05 kernels for those formats */
 } moe_weight_t;
 
 typedef struct {
@@ -127,21 +130,25 @@ size_t moe_workspace_size(const moe_problem_t *p);
  * blocks.  expert_ids needs moe_align_capacity()/block_m entries. */
 long moe_align_capacity(int M, int topk, int num_local_experts, int block_m);
 
-/* Load-time repack of MXFP4 weights for the weight-streaming decode kernels
- * (the role of convert_weight_to_mxfp4_moe_kernel_format on the mxfp4.py
- * page).  which = 0: w13 ([E_l, 2N, K/2] codes, [E_l, 2N, K/32] scales,
- * gate rows paired with up rows per p->gate); which = 1: w2.  The packed
- * buffer (moe_packed_weight_bytes bytes, 16-B aligned, caller-owned) holds
- * the same codes and scales reordered into per-tile records.  Requires
- * p->wfmt == MOE_W_MXFP4 and K, N multiples of 64; returns 0 bytes /
- * MOE_ERR_UNSUPPORTED otherwise.  moe_fused_experts uses the streaming
- * kernels when both w13.packed and w2.packed are set, the activations are
- * bf16, the activation is SwiGLU-OAI with 0 < limit <= 64 and |beta| <= 64,
- * and the batch is decode-sized (M*topk <= 32*E_l); otherwise the packed
- * buffers are ignored. */
-size_t moe_packed_weight_bytes(const moe_problem_t *p, int which);
-int moe_prepare_weights(const moe_problem_t *p, int which, const moe_weight_t *w, void *packed,
-                        void *stream);
+/* Load-time repack of FP4 weights (the role of
+ * convert_weight_to_mxfp4_moe_kernel_format on the mxfp4.py page).
+ * which = 0: w13 ([E_l, 2N, K/2] codes + scales, gate/up rows per p->gate);
+ * which = 1: w2.  The packed buffer (moe_packed_weight_bytes bytes, 16-B
+ * aligned, caller-owned) holds the same codes and scales reordered into
+ * per-tile records.  Layouts:
+ *   MOE_LAYOUT_STREAM  MXFP4 with K, N multiples of 64 -> moe_weight_t.packed:
+ *     the weight-streaming decode kernels, used by moe_fused_experts when both
+ *     w13 and w2 carry it, the activations are bf16, the activation is
+ *     SwiGLU-OAI with 0 < limit <= 64 and |beta| <= 64, and M*topk <= 32*E_l;
+ *   MOE_LAYOUT_TC      MXFP4 or NVFP4 -> moe_weight_t.packed_tc: the tcgen05
+ *     kernels of those formats (prefill-sized batches).  They decode into
+ *     f16, so for MXFP4 every e8m0 exponent must lie in [-21, 13] (checked
+ *     here; this check synchronises `stream`), else MOE_ERR_UNSUPPORTED.
+ * Unsupported combinations return 0 bytes / MOE_ERR_UNSUPPORTED. */
+enum { MOE_LAYOUT_STREAM = 0, MOE_LAYOUT_TC = 1 };
+size_t moe_packed_weight_bytes(const moe_problem_t *p, int which, int layout);
+int moe_prepare_weights(const moe_problem_t *p, int which, int layout, const moe_weight_t *w,
+                        void *packed, void *stream);
 
 /* Expert sort / block padding (the dispatch step named by
  * moe_sorting_dispatch_policy in AiterExperts.apply; the rule is this
@@ -227,6 +234,17 @@ int moe_fused_experts_noalloc(const moe_problem_t *p, const void *hidden_bf16,
                               const moe_weight_t *w13, const moe_weight_t *w2,
                               const int32_t *topk_ids, const float *topk_weights,
                               const int32_t *expert_map, void *out_bf16, void *stream);
+
+/* Execution-path control of moe_fused_experts (process-wide; a tuning and
+ * testing aid).  AUTO (default): the weight-streaming decode kernels when
+ * their conditions hold (see moe_prepare_weights), else the tcgen05 kernels
+ * when M*topk >= 2048 (FP4 formats need MOE_LAYOUT_TC packed weights), else
+ * the generic mma.sync kernels.  GENERIC, STREAM
+ * (falls back to GENERIC where it does not apply) and TC force a path.  Set
+ * it before sizing the workspace: moe_workspace_size depends on it. */
+enum { MOE_PATH_AUTO = 0, MOE_PATH_GENERIC = 1, MOE_PATH_STREAM = 2, MOE_PATH_TC = 3 };
+int moe_set_path(int path);
+int moe_get_path(void);
 
 /* Per-stage timing of moe_fused_experts (a profiling aid).  While enabled,
  * every moe_fused_experts call records a CUDA event pair around each of its

@@ -31,7 +31,8 @@ EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align
            "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_reduce", "moe_fused_experts",
            "moe_get_device_error", "moe_reset_device_error", "moe_noalloc_scratch_bytes",
            "moe_fused_experts_noalloc", "moe_packed_weight_bytes", "moe_prepare_weights",
-           "moe_stage_timing", "moe_stage_times")
+           "moe_stage_timing", "moe_stage_times", "moe_set_path", "moe_get_path")
+PATHS = {"auto": 0, "generic": 1, "stream": 2, "tc": 3}
 STAGES = ("align", "quant", "w13", "requant", "w2", "finalize")
 
 
@@ -54,7 +55,8 @@ class Problem(ctypes.Structure):
 class Weight(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("global_scale", ctypes.c_void_p), ("bias", ctypes.c_void_p),
-                ("bias_is_f32", ctypes.c_int), ("packed", ctypes.c_void_p)]
+                ("bias_is_f32", ctypes.c_int), ("packed", ctypes.c_void_p),
+                ("packed_tc", ctypes.c_void_p)]
 
 
 _lib = None
@@ -85,9 +87,11 @@ def lib() -> ctypes.CDLL:
         "moe_reset_device_error": (i, []),
         "moe_noalloc_scratch_bytes": (sz, []),
         "moe_fused_experts_noalloc": (i, [P, p, W, W, p, p, p, p, p]),
-        "moe_packed_weight_bytes": (sz, [P, i]),
-        "moe_prepare_weights": (i, [P, i, W, p, p]),
+        "moe_packed_weight_bytes": (sz, [P, i, i]),
+        "moe_prepare_weights": (i, [P, i, i, W, p, p]),
         "moe_stage_timing": (i, [i]),
+        "moe_set_path": (i, [i]),
+        "moe_get_path": (i, []),
         "moe_stage_times": (i, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -128,7 +132,7 @@ def make_weight(w: dict) -> Weight:
     bias = w.get("bias")
     return Weight(_ptr(w["codes"]), _ptr(w.get("scales")), _ptr(w.get("global_scale")),
                   _ptr(bias), int(bias is not None and bias.dtype == torch.float32),
-                  _ptr(w.get("packed")))
+                  _ptr(w.get("packed")), _ptr(w.get("packed_tc")))
 
 
 def stage2_format(wfmt: str, afmt: str) -> str:
@@ -213,14 +217,30 @@ def moe_fused_experts_noalloc(prob: Problem, hidden, w13: dict, w2: dict, topk_i
         _ptr(topk_weights), _ptr(expert_map), _ptr(out), _stream(stream)))
 
 
-def moe_packed_weight_bytes(prob: Problem, which: int) -> int:
-    return int(lib().moe_packed_weight_bytes(ctypes.byref(prob), which))
+LAYOUTS = {"stream": 0, "tc": 1}
 
 
-def moe_prepare_weights(prob: Problem, which: int, w: dict, packed, stream=None):
+def moe_packed_weight_bytes(prob: Problem, which: int, layout: str = "stream") -> int:
+    return int(lib().moe_packed_weight_bytes(ctypes.byref(prob), which, LAYOUTS[layout]))
+
+
+def moe_prepare_weights(prob: Problem, which: int, w: dict, packed, layout: str = "stream",
+                        stream=None):
     W = make_weight(w)
     _check("moe_prepare_weights", lib().moe_prepare_weights(
-        ctypes.byref(prob), which, ctypes.byref(W), _ptr(packed), _stream(stream)))
+        ctypes.byref(prob), which, LAYOUTS[layout], ctypes.byref(W), _ptr(packed),
+        _stream(stream)))
+
+
+def moe_set_path(path: str):
+    """Force an execution path of moe_fused_experts ("auto", "generic",
+    "stream", "tc"); set it before sizing workspaces."""
+    _check("moe_set_path", lib().moe_set_path(PATHS[path]))
+
+
+def moe_get_path() -> str:
+    v = lib().moe_get_path()
+    return {i: k for k, i in PATHS.items()}[v]
 
 
 def moe_stage_timing(enable: bool):
@@ -258,14 +278,24 @@ class FusedExperts:
                                  swiglu_beta, swiglu_limit, a1_scale, a2_scale)
         self._keep = (a1_scale, a2_scale)
         self.w13, self.w2 = dict(w13), dict(w2)
-        # load-time repack for the weight-streaming kernels (MXFP4, K and N
-        # multiples of 64); the C library decides per call whether to use it
-        if pack and moe_packed_weight_bytes(self.prob, 0) > 0:
-            for which, w in ((0, self.w13), (1, self.w2)):
-                buf = torch.empty(moe_packed_weight_bytes(self.prob, which), dtype=torch.uint8,
-                                  device=device)
-                moe_prepare_weights(self.prob, which, w, buf)
-                w["packed"] = buf
+        # load-time repacks (weight-streaming decode kernels: MXFP4 with K, N
+        # multiples of 64; tcgen05 kernels: MXFP4 / NVFP4); the C library
+        # decides per call which path runs
+        for layout, key in (("stream", "packed"), ("tc", "packed_tc")):
+            if pack and moe_packed_weight_bytes(self.prob, 0, layout) > 0:
+                bufs = []
+                try:
+                    for which, w in ((0, self.w13), (1, self.w2)):
+                        buf = torch.empty(moe_packed_weight_bytes(self.prob, which, layout),
+                                          dtype=torch.uint8, device=device)
+                        moe_prepare_weights(self.prob, which, w, buf, layout)
+                        bufs.append((w, buf))
+                except MoEError as err:
+                    if err.status != 2:  # unsupported for these weights: no packed copy
+                        raise
+                    continue
+                for w, buf in bufs:
+                    w[key] = buf
         self.M, self.K = M, K
         nbytes = moe_workspace_size(self.prob)
         if nbytes == 0:

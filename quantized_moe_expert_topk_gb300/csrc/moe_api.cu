@@ -23,6 +23,7 @@
 
 namespace moe {
 __device__ int g_device_error_word = 0;
+__device__ int g_scale_range[2];  // e8m0 code range found by moe_prepare_weights
 }
 
 namespace {
@@ -100,6 +101,23 @@ int validate_weight(const moe_problem_t *p, const moe_weight_t *w) {
   return MOE_OK;
 }
 
+// ---- execution path (moe_set_path)
+int g_path = MOE_PATH_AUTO;
+constexpr long kTcMinSlots = 2048;  // slots from which the tcgen05 path is used
+
+// The tcgen05 prefill path handles this problem (workspace sized for it).
+bool tc_applies(const moe_problem_t *p) {
+  if (g_path == MOE_PATH_TC) return true;
+  return g_path == MOE_PATH_AUTO && (long)p->M * p->topk >= kTcMinSlots;
+}
+
+// Workspace layout of the tcgen05 path (sort blocks of 128 rows).
+struct TcLayout {
+  long cap, blocks;
+  size_t sorted, expert_ids, ntp, counts, a1_codes, a1_scales, a_sorted, a_rowscale,
+      a_groupscale, inter, staging, i_scales, acc, total;
+};
+
 // Workspace layout of moe_fused_experts.
 struct Layout {
   long cap, blocks;
@@ -138,6 +156,39 @@ Layout make_layout(const moe_problem_t *p) {
     L.inter = o; o = align_up(o + codes_bytes(s2, L.cap, p->N));
     L.inter_scales = o; o = align_up(o + scales_bytes(s2, L.cap, p->N));
     L.staging = o; o = align_up(o + (size_t)L.cap * p->N * 4);
+  }
+  L.acc = o; o = align_up(o + (size_t)p->M * p->K * 4);
+  L.total = o;
+  return L;
+}
+
+TcLayout make_tc_layout(const moe_problem_t *p) {
+  TcLayout L;
+  const int BM = kTcBlockM;
+  L.cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, BM);
+  L.blocks = L.cap / BM;
+  const int s2 = stage2_afmt(p);
+  size_t o = 0;
+  L.sorted = o; o = align_up(o + (size_t)L.cap * 4);
+  L.expert_ids = o; o = align_up(o + (size_t)L.blocks * 4);
+  L.ntp = o; o = align_up(o + 4);
+  L.counts = o; o = align_up(o + (size_t)p->num_local_experts * 4);
+  L.a1_codes = o; o = align_up(o + codes_bytes(p->afmt, p->M, p->K));
+  L.a1_scales = o; o = align_up(o + scales_bytes(p->afmt, p->M, p->K));
+  const bool fp8 = p->wfmt == W_FP8_TENSOR || p->wfmt == W_FP8_CHANNEL ||
+                   p->wfmt == W_FP8_BLOCK128;
+  L.a_sorted = o; o = align_up(o + (size_t)L.cap * p->K * (fp8 ? 1 : 2));
+  L.a_rowscale = o; o = align_up(o + (size_t)L.cap * 4);
+  L.a_groupscale = o; o = align_up(o + (size_t)L.cap * ceil_div(p->K, 128) * 4);
+  L.inter = o; o = align_up(o + (size_t)L.cap * p->N * 2);
+  if (s2 != A_BF16) {
+    L.staging = o; o = align_up(o + (size_t)L.cap * p->N * 4);
+    L.i_scales = o; o = align_up(o + scales_bytes(s2, L.cap, p->N));
+  } else if (p->wfmt == W_MXFP4) {  // fp32 staging -> f16 rows + row scales
+    L.staging = o; o = align_up(o + (size_t)L.cap * p->N * 4);
+    L.i_scales = o; o = align_up(o + (size_t)L.cap * 4);
+  } else {
+    L.staging = L.i_scales = o;
   }
   L.acc = o; o = align_up(o + (size_t)p->M * p->K * 4);
   L.total = o;
@@ -283,6 +334,13 @@ int run_w2(const moe_problem_t *p, const void *inter, const void *inter_scales,
   return rc;
 }
 
+// The tcgen05 prefill path: sort with 128-row blocks, stage-1 quantisation,
+// gather into sorted bf16 rows, tcgen05 w13 (+ requantisation to exact bf16 +
+// scales), tcgen05 w2 + reduce, bf16 output.
+int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *w13,
+                const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
+                const int32_t *expert_map, char *ws, void *out, cudaStream_t st);
+
 }  // namespace
 
 extern "C" {
@@ -310,8 +368,21 @@ long moe_align_capacity(int M, int topk, int num_local_experts, int block_m) {
 
 size_t moe_workspace_size(const moe_problem_t *p) {
   if (validate_problem(p) != MOE_OK) return 0;
-  return make_layout(p).total;
+  size_t n = make_layout(p).total;
+  if (tc_applies(p)) {
+    const size_t t = make_tc_layout(p).total;
+    if (t > n) n = t;
+  }
+  return n;
 }
+
+int moe_set_path(int path) {
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_TC) return MOE_ERR_INVALID_ARG;
+  g_path = path;
+  return MOE_OK;
+}
+
+int moe_get_path(void) { return g_path; }
 
 int moe_align_block_size(const int32_t *topk_ids, int M, int topk, const int32_t *expert_map,
                          int num_experts, int num_local_experts, int block_m,
@@ -414,6 +485,18 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
+  const bool streaming = (g_path == MOE_PATH_AUTO || g_path == MOE_PATH_STREAM) &&
+                         stream_path(p, w13, w2);
+  const bool fp4 = p->wfmt == W_MXFP4 || p->wfmt == W_NVFP4;
+  if (!streaming && tc_applies(p) &&
+      (!fp4 || (w13->packed_tc && w2->packed_tc && aligned16(w13->packed_tc) &&
+                aligned16(w2->packed_tc)))) {
+    if (ws_bytes < make_tc_layout(p).total) return MOE_ERR_WORKSPACE;
+    std::lock_guard<std::mutex> timing_lock(g_timing_mu);
+    rc = run_tc_path(p, hidden_bf16, w13, w2, topk_ids, topk_weights, expert_map, ws, out_bf16, st);
+    timing_collect();
+    return rc;
+  }
   int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
   int32_t *eids = reinterpret_cast<int32_t *>(ws + L.expert_ids);
   int32_t *ntp = reinterpret_cast<int32_t *>(ws + L.ntp);
@@ -421,7 +504,6 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
   float *acc = reinterpret_cast<float *>(ws + L.acc);
   const long MK = (long)p->M * p->K;
 
-  const bool streaming = stream_path(p, w13, w2);
   DeviceInfo dinfo;
   if (streaming && (rc = device_info(&dinfo)) != MOE_OK) return rc;
 
@@ -527,35 +609,75 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
   return rc;
 }
 
-size_t moe_packed_weight_bytes(const moe_problem_t *p, int which) {
-  if (validate_problem(p) != MOE_OK || p->wfmt != W_MXFP4 || (which != 0 && which != 1))
-    return 0;
-  if (p->K % 64 != 0 || p->N % 64 != 0) return 0;
-  return stream_packed_bytes(which == 0, p->N, p->K, p->num_local_experts);
+size_t moe_packed_weight_bytes(const moe_problem_t *p, int which, int layout) {
+  if (validate_problem(p) != MOE_OK || (which != 0 && which != 1)) return 0;
+  if (layout == MOE_LAYOUT_STREAM) {
+    if (p->wfmt != W_MXFP4 || p->K % 64 != 0 || p->N % 64 != 0) return 0;
+    return stream_packed_bytes(which == 0, p->N, p->K, p->num_local_experts);
+  }
+  if (layout == MOE_LAYOUT_TC) {
+    if (p->wfmt != W_MXFP4 && p->wfmt != W_NVFP4) return 0;
+    return tc_packed_bytes(which == 0, p->wfmt == W_NVFP4, p->N, p->K, p->num_local_experts);
+  }
+  return 0;
 }
 
-int moe_prepare_weights(const moe_problem_t *p, int which, const moe_weight_t *w, void *packed,
-                        void *stream) {
+int moe_prepare_weights(const moe_problem_t *p, int which, int layout, const moe_weight_t *w,
+                        void *packed, void *stream) {
   int rc = validate_problem(p);
   if (rc != MOE_OK) return rc;
-  if (which != 0 && which != 1) return MOE_ERR_INVALID_ARG;
-  if (p->wfmt != W_MXFP4 || p->K % 64 != 0 || p->N % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((which != 0 && which != 1) || (layout != MOE_LAYOUT_STREAM && layout != MOE_LAYOUT_TC))
+    return MOE_ERR_INVALID_ARG;
+  if (moe_packed_weight_bytes(p, which, layout) == 0) return MOE_ERR_UNSUPPORTED;
   if ((rc = validate_weight(p, w)) != MOE_OK) return rc;
   if (!packed || !aligned16(packed)) return MOE_ERR_INVALID_ARG;
   const int w13 = which == 0;
-  PackArgs a;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (layout == MOE_LAYOUT_STREAM) {
+    PackArgs a;
+    a.codes = static_cast<const unsigned char *>(w->codes);
+    a.scales = static_cast<const unsigned char *>(w->scales);
+    a.out = static_cast<unsigned char *>(packed);
+    a.total = (long)stream_packed_bytes(w13, p->N, p->K, p->num_local_experts);
+    a.units = stream_units_per_expert(w13, p->N, p->K);
+    a.w13 = w13;
+    a.N = p->N;
+    a.R = w13 ? 2 * p->N : p->K;
+    a.C = w13 ? p->K : p->N;
+    a.kblocks = a.C / 64;
+    a.gate = p->gate;
+    return cuda_status(launch_pack_mxfp4(a, st));
+  }
+  if (p->wfmt == W_MXFP4) {
+    // The tcgen05 kernels decode MXFP4 into f16: every e2m1 * 2^(c-127) is an
+    // exact f16 value when the exponent c-127 lies in [-21, 13].  Check the
+    // codes once at load time (this synchronises `stream`).
+    void *rng = nullptr;
+    if (cudaGetSymbolAddress(&rng, moe::g_scale_range) != cudaSuccess) return MOE_ERR_CUDA;
+    const long n = (long)p->num_local_experts * (w13 ? 2L * p->N : p->K) * ((w13 ? p->K : p->N) / 32);
+    int host[2] = {0, 0};
+    if (launch_scale_range(static_cast<const uint8_t *>(w->scales), n, static_cast<int *>(rng), st) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(host, rng, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (host[0] < 127 - 21 || host[1] > 127 + 13) return MOE_ERR_UNSUPPORTED;
+  }
+  TcPackArgs a;
   a.codes = static_cast<const unsigned char *>(w->codes);
   a.scales = static_cast<const unsigned char *>(w->scales);
   a.out = static_cast<unsigned char *>(packed);
-  a.total = (long)stream_packed_bytes(w13, p->N, p->K, p->num_local_experts);
-  a.units = stream_units_per_expert(w13, p->N, p->K);
+  a.nvfp4 = p->wfmt == W_NVFP4;
+  a.total = (long)tc_packed_bytes(w13, a.nvfp4, p->N, p->K, p->num_local_experts);
+  a.rec_bytes = a.nvfp4 ? 4096 + 128 * 4 : 4096 + 128 * 2;
   a.w13 = w13;
   a.N = p->N;
   a.R = w13 ? 2 * p->N : p->K;
   a.C = w13 ? p->K : p->N;
-  a.kblocks = a.C / 64;
+  a.kstages = (int)ceil_div(a.C, 64);
+  a.ntiles = tc_ntiles(w13, p->N, p->K);
   a.gate = p->gate;
-  return cuda_status(launch_pack_mxfp4(a, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_pack_tc_fp4(a, st));
 }
 
 int moe_stage_timing(int enable) {
@@ -598,3 +720,157 @@ int moe_reset_device_error(void) {
 }
 
 }  // extern "C"
+
+namespace {
+
+int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *w13,
+                const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
+                const int32_t *expert_map, char *ws, void *out, cudaStream_t st) {
+  const TcLayout L = make_tc_layout(p);
+  DeviceInfo dinfo;
+  int rc = device_info(&dinfo);
+  if (rc != MOE_OK) return rc;
+  int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+  int32_t *eids = reinterpret_cast<int32_t *>(ws + L.expert_ids);
+  int32_t *ntp = reinterpret_cast<int32_t *>(ws + L.ntp);
+  int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+  float *acc = reinterpret_cast<float *>(ws + L.acc);
+  const long MK = (long)p->M * p->K;
+  const int S = p->M * p->topk;
+  const int s2 = stage2_afmt(p);
+
+  // 1. sort / pad with 128-row blocks (+ zero the accumulator)
+  {
+    AlignExtras ex;
+    ex.zero_buf = acc;
+    ex.zero_n = MK;
+    StageScope sc(MOE_STAGE_ALIGN, st);
+    rc = cuda_status(launch_align(topk_ids, p->M, p->topk, expert_map, p->num_experts,
+                                  p->num_local_experts, kTcBlockM, sorted, eids, ntp, counts,
+                                  L.cap, ex, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+  }
+  // 2. stage-1 quantisation of x (once per token)
+  const void *codes = hidden;
+  const void *scales = nullptr;
+  if (p->afmt != A_BF16) {
+    QuantArgs q;
+    memset(&q, 0, sizeof(q));
+    q.x = hidden; q.rows = p->M; q.cols = p->K; q.afmt = p->afmt; q.param = p->a1_scale;
+    q.codes = ws + L.a1_codes; q.scales = ws + L.a1_scales; q.BM = 1;
+    StageScope sc(MOE_STAGE_QUANT, st);
+    rc = cuda_status(launch_quant(q, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+    codes = ws + L.a1_codes;
+    scales = ws + L.a1_scales;
+  }
+  // 3. gather: sorted bf16 rows (exact decode) + per-row / per-group scales
+  {
+    GatherArgs g;
+    g.sorted_ids = sorted; g.num_post_pad = ntp; g.S = S; g.T = p->topk; g.K = p->K;
+    g.afmt = p->afmt; g.codes = codes; g.scales = scales;
+    g.to_f16 = p->wfmt == W_MXFP4 || p->wfmt == W_NVFP4;
+    g.out = ws + L.a_sorted;
+    g.rowscale = reinterpret_cast<float *>(ws + L.a_rowscale);
+    g.groupscale = reinterpret_cast<float *>(ws + L.a_groupscale);
+    StageScope sc(MOE_STAGE_QUANT, st);
+    rc = cuda_status(launch_gather_rows(g, L.cap, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+  }
+  TcArgs base;
+  memset(&base, 0, sizeof(base));
+  base.M = p->M; base.K = p->K; base.N = p->N; base.T = p->topk; base.El = p->num_local_experts;
+  base.wfmt = p->wfmt; base.act = p->act; base.gate = p->gate;
+  base.alpha = p->swiglu_alpha; base.beta = p->swiglu_beta; base.limit = p->swiglu_limit;
+  base.sorted_ids = sorted; base.expert_ids = eids; base.num_post_pad = ntp; base.S = S;
+  base.err = dinfo.err;
+  // 4. gate/up GEMM + activation
+  {
+    TcArgs a = base;
+    a.R = 2 * p->N; a.C = p->K;
+    switch (p->afmt) {
+      case A_FP8_TENSOR_STATIC:
+      case A_FP8_TENSOR_DYN: a.a_scalar = static_cast<const float *>(scales); break;
+      case A_FP8_TOKEN_DYN: a.a_rowscale = reinterpret_cast<const float *>(ws + L.a_rowscale); break;
+      case A_FP8_GROUP128_DYN:
+        a.a_groupscale = reinterpret_cast<const float *>(ws + L.a_groupscale);
+        a.a_groups = (int)ceil_div(p->K, 128);
+        break;
+      case A_NVFP4_DYN: a.a_scalar = p->a1_scale; break;
+      default:
+        if (p->wfmt == W_MXFP4) a.a_rowscale = reinterpret_cast<const float *>(ws + L.a_rowscale);
+        break;
+    }
+    a.w_codes = w13->codes; a.w_scales = w13->scales; a.w_global = w13->global_scale;
+    a.w_bias = w13->bias; a.bias_f32 = w13->bias_is_f32; a.w_packed = w13->packed_tc;
+    const bool to_staging = s2 != A_BF16 || p->wfmt == W_MXFP4;
+    a.out = to_staging ? (void *)(ws + L.staging) : (void *)(ws + L.inter);
+    a.out_f32 = to_staging;
+    StageScope sc(MOE_STAGE_W13, st);
+    rc = cuda_status(launch_tc_gemm(a, ws + L.a_sorted, L.cap, 1, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+  }
+  if (s2 == A_BF16 && p->wfmt == W_MXFP4) {  // f16 intermediate with row scales
+    StageScope sc(MOE_STAGE_REQUANT, st);
+    rc = cuda_status(launch_rescale_rows(reinterpret_cast<const float *>(ws + L.staging), L.cap,
+                                         p->N, sorted, ntp, S, ws + L.inter,
+                                         reinterpret_cast<float *>(ws + L.i_scales), st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+  }
+  // 5. stage-2 requantisation into exact bf16 values + scales (sorted rows)
+  if (s2 != A_BF16) {
+    QuantArgs q;
+    memset(&q, 0, sizeof(q));
+    q.x = ws + L.staging; q.x_is_f32 = 1; q.rows = L.cap; q.cols = p->N; q.afmt = s2;
+    q.param = p->a2_scale; q.sorted_ids = sorted; q.expert_ids = eids; q.num_post_pad = ntp;
+    q.S = S; q.BM = kTcBlockM; q.scales = ws + L.i_scales;
+    if (s2 == A_NVFP4_DYN) {  // consumed as exact f16 by the kind::f16 GEMM
+      q.codes = nullptr;
+      q.decoded = ws + L.inter;
+      q.decoded_f16 = 1;
+    } else {                  // e4m3 codes consumed by the kind::f8f6f4 GEMM
+      q.codes = ws + L.inter;
+    }
+    StageScope sc(MOE_STAGE_REQUANT, st);
+    rc = cuda_status(launch_quant(q, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+  }
+  // 6. down GEMM + router weight + reduce
+  {
+    TcArgs a = base;
+    a.R = p->K; a.C = p->N;
+    switch (s2) {
+      case A_FP8_TENSOR_STATIC:
+      case A_FP8_TENSOR_DYN: a.a_scalar = reinterpret_cast<const float *>(ws + L.i_scales); break;
+      case A_FP8_TOKEN_DYN: a.a_rowscale = reinterpret_cast<const float *>(ws + L.i_scales); break;
+      case A_FP8_GROUP128_DYN:
+        a.a_groupscale = reinterpret_cast<const float *>(ws + L.i_scales);
+        a.a_groups = (int)ceil_div(p->N, 128);
+        break;
+      case A_NVFP4_DYN: a.a_expertscale = p->a2_scale; break;
+      default:
+        if (p->wfmt == W_MXFP4) a.a_rowscale = reinterpret_cast<const float *>(ws + L.i_scales);
+        break;
+    }
+    a.w_codes = w2->codes; a.w_scales = w2->scales; a.w_global = w2->global_scale;
+    a.w_bias = w2->bias; a.bias_f32 = w2->bias_is_f32; a.w_packed = w2->packed_tc;
+    a.acc = acc; a.topk_weights = topk_weights;
+    StageScope sc(MOE_STAGE_W2, st);
+    rc = cuda_status(launch_tc_gemm(a, ws + L.inter, L.cap, 0, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+  }
+  // 7. bf16 output
+  StageScope sc(MOE_STAGE_FINALIZE, st);
+  rc = cuda_status(launch_finalize(acc, MK, out, st));
+  sc.done();
+  return rc;
+}
+
+}  // namespace

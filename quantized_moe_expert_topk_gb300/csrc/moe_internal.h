@@ -11,6 +11,10 @@ namespace moe {
 // Tile height (sorted rows per block) of the mma.sync grouped GEMMs; the
 // expert sort pads every expert to a multiple of it.
 constexpr int kGenericBlockM = 64;
+// Tile height of the tcgen05 GEMMs (and the sort block of that path).
+constexpr int kTcBlockM = 128;
+// Largest packed FP4 weight record of one tcgen05 pipeline stage.
+constexpr int kTcRecMaxBytes = 4096 + 128 * 4;
 
 // Optional extra work folded into the sort launch (extra CTAs / outputs).
 struct AlignExtras {
@@ -49,6 +53,9 @@ struct QuantArgs {
   int BM;
   void *codes;
   void *scales;
+  void *decoded = nullptr;   // if set: exact bf16 of the dequantised codes (without
+                             // the scales an epilogue applies) instead of codes
+  int decoded_f16 = 0;       // the decoded values as f16 instead of bf16 (NVFP4)
 };
 cudaError_t launch_quant(const QuantArgs &a, cudaStream_t stream);
 
@@ -108,6 +115,53 @@ size_t stream_packed_bytes(int w13, int N, int K, int El);
 int stream_units_per_expert(int w13, int N, int K);
 cudaError_t launch_pack_mxfp4(const PackArgs &p, cudaStream_t stream);
 cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream_t stream);
+
+// tcgen05 grouped GEMMs (moe_tc.cu)
+struct TcArgs {
+  int M, K, N, T, El, R, C;
+  int wfmt, act, gate;
+  float alpha, beta, limit;
+  const float *a_scalar, *a_rowscale, *a_groupscale, *a_expertscale;
+  int a_groups;
+  const void *w_codes, *w_scales;
+  const float *w_global;
+  const void *w_bias;
+  int bias_f32;
+  const int32_t *sorted_ids, *expert_ids, *num_post_pad;
+  int S;
+  void *out;
+  int out_f32;
+  float *acc;
+  const float *topk_weights;
+  int *err;
+  const void *w_packed;  // FP4 formats: load-time packed records
+  int ntiles;            // set by the launcher
+  int rec_bytes;         // set by the launcher
+};
+struct GatherArgs {
+  const int32_t *sorted_ids, *num_post_pad;
+  int S, T, K, afmt;
+  const void *codes, *scales;
+  void *out;             // bf16 / f16 rows, or e4m3 codes for fp8 activations
+  float *rowscale, *groupscale;
+  int to_f16;            // f16 rows (FP4 weights: the f16 tensor-core kind)
+};
+cudaError_t launch_rescale_rows(const float *src, long cap, int N, const int32_t *sorted_ids,
+                                const int32_t *ntp, int S, void *dst, float *rowscale,
+                                cudaStream_t st);
+cudaError_t launch_scale_range(const uint8_t *s, long n, int *mn_mx, cudaStream_t st);
+struct TcPackArgs {
+  const unsigned char *codes, *scales;
+  unsigned char *out;
+  long total;
+  int rec_bytes, kstages, ntiles, w13, nvfp4, gate, N, R, C;
+};
+int tc_ntiles(int w13, int N, int K);
+size_t tc_packed_bytes(int w13, int nvfp4, int N, int K, int El);
+cudaError_t launch_pack_tc_fp4(const TcPackArgs &p, cudaStream_t st);
+cudaError_t launch_gather_rows(const GatherArgs &g, long cap_rows, cudaStream_t st);
+cudaError_t launch_tc_gemm(const TcArgs &a, const void *a_sorted, long cap_rows, int w13,
+                           cudaStream_t st);
 
 cudaError_t launch_finalize(const float *acc, long n, void *out_bf16, cudaStream_t stream);
 cudaError_t launch_zero(float *buf, long n, cudaStream_t stream);

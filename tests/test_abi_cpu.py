@@ -35,7 +35,7 @@ def test_header_symbols_are_exported(moe):
     L = moe.lib()
     for name in declared:
         assert hasattr(L, name), name
-    assert moe.moe_abi_version() == 2
+    assert moe.moe_abi_version() == 3
 
 
 def test_status_strings(moe):
@@ -101,13 +101,20 @@ def test_quant_and_align_validation(moe):
 def test_packed_weight_sizes(moe):
     # records of 64 reduction elements x 128 rows: 8 tiles x (512 B codes + 32 B scales)
     p = moe.make_problem(64, 2880, 2880, 4, 32, 32, "mxfp4", "bf16", "swiglu_oai", "interleaved")
-    w13 = moe.moe_packed_weight_bytes(p, 0)
-    w2 = moe.moe_packed_weight_bytes(p, 1)
+    w13 = moe.moe_packed_weight_bytes(p, 0, "stream")
+    w2 = moe.moe_packed_weight_bytes(p, 1, "stream")
     assert w13 == 32 * (2880 // 64) * (2880 // 64) * 4352
     assert w2 == 32 * 23 * (2880 // 64) * 4352       # ceil(2880 / 128) row tiles
     # same payload as the canonical codes + scales (up to the padded last row tile)
     assert w13 == 32 * 5760 * (2880 // 2 + 2880 // 32)
     q = moe.make_problem(64, 2880, 2880, 4, 32, 32, "bf16", "bf16", "silu", "separated")
-    assert moe.moe_packed_weight_bytes(q, 0) == 0
+    assert moe.moe_packed_weight_bytes(q, 0, "stream") == 0
+    assert moe.moe_packed_weight_bytes(q, 0, "tc") == 0
     r = moe.make_problem(64, 2880, 2848, 4, 32, 32, "mxfp4", "bf16", "silu", "separated")
-    assert moe.moe_packed_weight_bytes(r, 0) == 0     # N % 64 != 0: no streaming layout
+    assert moe.moe_packed_weight_bytes(r, 0, "stream") == 0  # N % 64 != 0: no streaming layout
+    # tcgen05 records: per (expert, tile of 64 outputs / 128 rows, 64-wide stage)
+    # 128 rows x 32 code bytes + 128 rows x 2 (MXFP4) or 4 (NVFP4) scale bytes
+    assert moe.moe_packed_weight_bytes(r, 0, "tc") == 32 * (2848 // 64 + 1) * (2880 // 64) * 4352
+    n = moe.make_problem(64, 4096, 1024, 2, 8, 8, "nvfp4", "nvfp4_dyn", "silu", "separated")
+    n.a1_scale = n.a2_scale = 0x1000  # never dereferenced by a size query
+    assert moe.moe_packed_weight_bytes(n, 1, "tc") == 8 * (4096 // 128) * (1024 // 64) * 4608
