@@ -18,7 +18,6 @@ against), rank 0 only.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -43,6 +42,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--M", type=int, default=None)
+    ap.add_argument("--E", type=int, default=None, help="routed experts (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -159,7 +159,8 @@ def measured_peaks():
 
 def profile_traffic(kernel_tag, workload):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel (source hash recorded in the summary)."""
+    the current source of the kernel: the summary lists the source files of
+    the kernel it measured and their hash, which must still match."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}__{workload}.txt")
     if not os.path.exists(path):
         return None
@@ -167,9 +168,9 @@ def profile_traffic(kernel_tag, workload):
     for line in open(path):
         if ":" in line:
             k, v = line.split(":", 1)
-            vals[k.strip()] = v.strip()
-    src = vals.get("source_sha256")
-    if not src or src != kernel_source_hash():
+            vals.setdefault(k.strip(), v.strip())
+    files = vals.get("source_files", "").split()
+    if not files or vals.get("source_sha256") != kernel_source_hash(files):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -177,10 +178,14 @@ def profile_traffic(kernel_tag, workload):
         return None
 
 
-def kernel_source_hash():
+def kernel_source_hash(files):
+    """sha256 (16 hex digits) of the named files under the package's csrc/, in order."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "quantized_moe_expert_topk_gb300", "csrc", "*"))):
-        h.update(open(f, "rb").read())
+    for f in files:
+        p = os.path.join(ROOT, "quantized_moe_expert_topk_gb300", "csrc", f)
+        if not os.path.exists(p):
+            return None
+        h.update(open(p, "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -280,6 +285,8 @@ def run_ours(args):
     from moe_workloads import make_workload
     cuda_build.build()
     over = {"M": args.M} if args.M else {}
+    if args.E:
+        over["E"] = args.E
     wl = make_workload(args.workload, device=dev, **over)
     layer = moe.FusedExperts.from_workload(wl)
     out = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device=dev)

@@ -137,6 +137,8 @@ struct TcArgs {
   const void *w_packed;  // FP4 formats: load-time packed records
   int ntiles;            // set by the launcher
   int rec_bytes;         // set by the launcher
+  int mgroup;            // raster: m-blocks that walk the n-tiles together (launcher)
+  long nblocks;          // m-blocks in the grid (launcher)
 };
 struct GatherArgs {
   const int32_t *sorted_ids, *num_post_pad;

@@ -105,6 +105,8 @@ __device__ __forceinline__ void red_add_v4(float *p, float x, float y, float z, 
                : "memory");
 }
 
+constexpr int kTcRasterGroup = 1;
+
 template <int MODE, int KIND>
 __global__ void __launch_bounds__(THREADS, 2)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -113,7 +115,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int blk = blockIdx.x, nt = blockIdx.y;
+  // Grouped raster: groups of `mgroup` m-blocks walk the n-tiles together, m
+  // fastest inside a group.  With one m-block per group (the setting used) the
+  // CTAs resident at one time share one A block and stream the weight tiles of
+  // its expert; an m-fastest order re-read A from DRAM once per n-tile wave.
+  int nt, blk;
+  {
+    const long id = blockIdx.x, span = (long)a.mgroup * a.ntiles;
+    const long g0 = id / span * a.mgroup;
+    const long gs = min((long)a.mgroup, a.nblocks - g0);
+    const long local = id - g0 * a.ntiles;
+    blk = (int)(g0 + local % gs);
+    nt = (int)(local / gs);
+  }
   if ((long)blk * BM >= (long)*a.num_post_pad) return;  // uniform for the CTA
   const int e = a.expert_ids[blk];
   if (e < 0 || e >= a.El) return;
@@ -646,8 +660,7 @@ cudaError_t launch_tc_t(const CUtensorMap &ta, const CUtensorMap &tb, const TcAr
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  tc_gemm_kernel<MODE, KIND><<<dim3((unsigned)blocks, (unsigned)a.ntiles), THREADS, SMEM_BYTES, st>>>(
-      ta, tb, a);
+  tc_gemm_kernel<MODE, KIND><<<(unsigned)(blocks * a.ntiles), THREADS, SMEM_BYTES, st>>>(ta, tb, a);
   return cudaGetLastError();
 }
 
@@ -699,6 +712,9 @@ cudaError_t launch_tc_gemm(const TcArgs &a_in, const void *a_sorted, long cap_ro
   a.ntiles = tc_ntiles(w13, a.N, a.K);
   const long blocks = cap_rows / BM;
   if (blocks <= 0) return cudaSuccess;
+  if (blocks * a.ntiles > 0x7fffffffL) return cudaErrorInvalidConfiguration;
+  a.nblocks = blocks;
+  a.mgroup = (int)min(blocks, (long)kTcRasterGroup);
   const int kind = a.wfmt == W_BF16 ? K_BF16 : (a.wfmt == W_MXFP4 || a.wfmt == W_NVFP4) ? K_FP4 : K_FP8;
   CUtensorMap ta, tb;
   if (!make_map(&ta, a_sorted, cap_rows, a.C, kind == K_FP8, BM)) return cudaErrorInvalidValue;
