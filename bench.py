@@ -282,6 +282,7 @@ def run_ours(args):
 
     import quantized_moe_expert_topk_gb300 as moe
     from quantized_moe_expert_topk_gb300 import build as cuda_build
+    from quantized_moe_expert_topk_gb300.ep import replica_max
     from moe_workloads import make_workload
     cuda_build.build()
     over = {"M": args.M} if args.M else {}
@@ -335,10 +336,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     rows = sampler.stop()
     ms = start.elapsed_time(end) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
+    ms = replica_max(ms, device=dev)  # slowest rank (no-op on one rank)
     value = world * wl.M / (ms / 1e3)
 
     # dominant kernel (w13 GEMM + activation), timed alone on its own stream
