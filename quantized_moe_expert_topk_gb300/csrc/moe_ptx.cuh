@@ -271,4 +271,16 @@ __host__ __device__ constexpr uint32_t umma_idesc_e4m3(int m, int n) {
          | ((uint32_t)(m >> 4) << 24);
 }
 
+// d0 += a0 * s, d1 += a1 * s in one packed fp32x2 FMA (round to nearest).
+__device__ __forceinline__ void fma_f32x2(float &d0, float &d1, float a0, float a1, float s) {
+  asm("{\n\t.reg .b64 pa, pd, ps;\n\t"
+      "mov.b64 pa, {%2, %3};\n\t"
+      "mov.b64 pd, {%0, %1};\n\t"
+      "mov.b64 ps, {%4, %4};\n\t"
+      "fma.rn.f32x2 pd, pa, ps, pd;\n\t"
+      "mov.b64 {%0, %1}, pd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(s));
+}
+
 }  // namespace moe

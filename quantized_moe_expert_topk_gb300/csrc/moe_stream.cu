@@ -7,11 +7,11 @@
 //
 // Work unit: (active local expert, tile of 128 weight rows, k-range).  Units
 // are claimed dynamically from a global counter (persistent CTAs, four per
-// SM); each unit streams its weight records once through a 4-stage
-// shared-memory ring filled by TMA bulk copies (one producer warp, mbarrier
-// full/empty pairs, every wait bounded, a descriptor per stage telling the
-// consumers which unit/pass/k-block it holds); four consumer warps each own
-// two m16 tiles.
+// SM); each unit streams its weight records once through a double-buffered
+// shared-memory ring (stages of 256 reduction elements, 17 KB of weights)
+// filled by TMA bulk copies (one producer warp, mbarrier full/empty pairs,
+// every wait bounded, a descriptor per stage telling the consumers which
+// unit/pass/k-block it holds); four consumer warps each own two m16 tiles.
 //
 // Arithmetic (swap-AB mma.sync m16n8k16, f16 x f16 -> fp32):
 //   A = weights: e2m1 codes converted two at a time by the hardware
@@ -48,12 +48,12 @@ constexpr int ROWS = CW * MT * 16;          // 128 weight rows per unit
 constexpr int TILES = CW * MT;              // 8 m16 tiles per unit
 constexpr int TILE_BYTES = 512 + 32;        // codes + scales of one tile, one k64 block
 constexpr int REC_BYTES = TILES * TILE_BYTES;  // 4352 B per (unit, k64 block)
-constexpr int S_KB = 2;                     // k64 blocks per stage (128 reduction elements)
-constexpr int NS = 4;                       // pipeline stages
+constexpr int S_KB = 4;                     // k64 blocks per stage (256 reduction elements)
+constexpr int NS = 2;                       // pipeline stages (double buffer)
 constexpr int TOKMAX = 16;                  // tokens per pass (two n8 tiles)
-constexpr int XS = S_KB * 64 * 2 + 16;      // smem row stride of the token tile (272 B)
-constexpr int W_STAGE = S_KB * REC_BYTES;   // 8704 B
-constexpr int X_STAGE = TOKMAX * XS;        // 4352 B
+constexpr int XS = S_KB * 64 * 2 + 16;      // smem row stride of the token tile (528 B)
+constexpr int W_STAGE = S_KB * REC_BYTES;   // 17408 B
+constexpr int X_STAGE = TOKMAX * XS;        // 8448 B
 constexpr int STAGE_BYTES = W_STAGE + X_STAGE;
 constexpr int THREADS = (CW + 1) * 32;
 constexpr int CTAS_PER_SM = 4;
@@ -63,12 +63,18 @@ constexpr int kErrTimeout = 5;
 enum { MODE_W13 = 0, MODE_W2 = 1 };
 enum { F_FIRST = 1, F_LAST = 2 };
 
-// Stage descriptor written by the producer next to the data it loads.
+struct Unit {
+  int e, u, kb0, nkb, off, cnt;
+};
+
+// Stage descriptor written by the producer next to the data it loads (the
+// unit's decoded fields too, so consumers start a unit without global loads).
 struct StageDesc {
   int id;    // unit id, -1 = no more work
   int tok0;  // first token of this pass
   int kb;    // first k64 block of this stage within the unit's k-range
   int flags; // F_FIRST / F_LAST: first / last stage of the pass
+  Unit unit;
 };
 
 struct Smem {
@@ -79,10 +85,6 @@ struct Smem {
   int abort_flag;
 };
 constexpr size_t SMEM_BYTES = sizeof(Smem);
-
-struct Unit {
-  int e, u, kb0, nkb, off, cnt;
-};
 
 __device__ __forceinline__ Unit decode_unit(const StreamArgs &a, int id) {
   Unit r;
@@ -156,10 +158,8 @@ __device__ __forceinline__ void consume_k64(const unsigned char *tp0, uint32_t x
       const float f_hi = e8m0_byte_f32(sw[m], 2 * kk + 1);
 #pragma unroll
       for (int n = 0; n < NTILES; ++n) {
-        acc[m][n][0] = fmaf(part[m][n][0], f_lo, acc[m][n][0]);
-        acc[m][n][1] = fmaf(part[m][n][1], f_lo, acc[m][n][1]);
-        acc[m][n][2] = fmaf(part[m][n][2], f_hi, acc[m][n][2]);
-        acc[m][n][3] = fmaf(part[m][n][3], f_hi, acc[m][n][3]);
+        fma_f32x2(acc[m][n][0], acc[m][n][1], part[m][n][0], part[m][n][1], f_lo);
+        fma_f32x2(acc[m][n][2], acc[m][n][3], part[m][n][2], part[m][n][3], f_hi);
       }
     }
   }
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
       if (id >= n_units) {
         int slot;
         if (acquire_slot(slot) && lane == 0) {
-          sm.desc[slot] = StageDesc{-1, 0, 0, 0};
+          sm.desc[slot] = StageDesc{-1, 0, 0, 0, Unit{0, 0, 0, 0, 0, 0}};
           mbar_arrive(&sm.full[slot]);
         }
         ++it;
@@ -230,8 +230,9 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
           const uint32_t wbytes = (uint32_t)nkb * REC_BYTES;
           const uint32_t xbytes = (uint32_t)nkb * 128;
           if (lane == 0) {
-            sm.desc[slot] = StageDesc{id, tok0, kb, (kb == 0 ? F_FIRST : 0) |
-                                                     (kb + S_KB >= U.nkb ? F_LAST : 0)};
+            sm.desc[slot] = StageDesc{id, tok0, kb,
+                                      (kb == 0 ? F_FIRST : 0) | (kb + S_KB >= U.nkb ? F_LAST : 0),
+                                      U};
             mbar_arrive_expect_tx(&sm.full[slot], wbytes + (uint32_t)nt * xbytes);
             const unsigned char *src = static_cast<const unsigned char *>(a.packed) +
                 ((((long)U.e * a.units_per_expert + U.u) * a.kblocks) + U.kb0 + kb) * REC_BYTES;
@@ -263,6 +264,8 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
   Unit U = {0, 0, 0, 0, 0, 0};
   int nt = 0, ntiles = 0;
   float acc[MT][2][4];
+  int tok_sid[2][2] = {{0, 0}, {0, 0}};      // sorted slot ids of this thread's tokens
+  float tok_f[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // W13: x_inv of the token; W2: router weight
   while (true) {
     const int slot = it % NS;
     if (!mbar_wait_bounded(&sm.full[slot], (it / NS) & 1, kWaitCycles)) {
@@ -280,7 +283,10 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
     }
     if (d.id < 0) break;
     if (d.flags & F_FIRST) {
-      U = decode_unit(a, d.id);
+      {
+        const volatile int *uv = reinterpret_cast<const volatile int *>(&sm.desc[slot].unit);
+        U.e = uv[0]; U.u = uv[1]; U.kb0 = uv[2]; U.nkb = uv[3]; U.off = uv[4]; U.cnt = uv[5];
+      }
       nt = min(TOKMAX, U.cnt - d.tok0);
       ntiles = (nt + 7) >> 3;
 #pragma unroll
@@ -289,6 +295,24 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
         for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int c = 0; c < 4; ++c) acc[m][n][c] = 0.f;
+      // epilogue operands of this thread's tokens, loaded now so that their
+      // latency hides behind the pass
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int tn = n * 8 + 2 * t + c;
+          tok_sid[n][c] = tn < nt ? a.sorted_ids[U.off + d.tok0 + tn] : 0;
+        }
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int tn = n * 8 + 2 * t + c;
+          tok_f[n][c] = tn >= nt ? 0.f
+                        : MODE == MODE_W13 ? a.x_inv[tok_sid[n][c] / a.T]
+                                           : a.topk_weights[tok_sid[n][c]];
+        }
     }
     const int nkb = min(S_KB, U.nkb - d.kb);
     const unsigned char *ws = sm.stage[slot];
@@ -327,7 +351,7 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
             const int tn = n * 8 + 2 * t + c;
             if (tn >= nt) continue;
             const int r = U.off + tok0 + tn;
-            const float xi = a.x_inv[a.sorted_ids[r] / a.T];
+            const float xi = tok_f[n][c];
             const float gv = acc[m][n][c] * xi + bg;
             const float uv = acc[m][n][2 + c] * xi + bu;
             const float z = act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit);
@@ -351,8 +375,8 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
             for (int c = 0; c < 2; ++c) {
               const int tn = n * 8 + 2 * t + c;
               if (tn >= nt) continue;
-              const int sidx = a.sorted_ids[U.off + tok0 + tn];
-              const float wt = a.topk_weights[sidx];
+              const int sidx = tok_sid[n][c];
+              const float wt = tok_f[n][c];
               atomicAdd(a.acc + (long)(sidx / a.T) * K + i, wt * (acc[m][n][2 * h + c] + bias));
             }
         }

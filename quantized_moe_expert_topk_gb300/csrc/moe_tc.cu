@@ -283,31 +283,48 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (promote) {
       const long RB = (a.R + 127) / 128, CB = KT;
       const float *ws = static_cast<const float *>(a.w_scales);
-      long blockrow[2];
+      const float *sa_row = a.a_groupscale + r * a.a_groups;
+      const float *sw_ptr[2];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) blockrow[cc] = group_row<MODE>(a, nt, 2 * h + cc) / 128;
+      for (int cc = 0; cc < 2; ++cc) {
+        const long br = group_row<MODE>(a, nt, 2 * h + cc) / 128;
+        sw_ptr[cc] = br < RB ? ws + ((long)e * RB + br) * CB : nullptr;
+      }
+      // the block scales of stage kb+2 are loaded while stage kb is promoted
+      auto load_f = [&](int kb, float (&f)[2]) {
+        const float sa = (live && kb < KT) ? sa_row[kb] : 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) f[cc] = (sw_ptr[cc] && kb < KT) ? sa * sw_ptr[cc][kb] : 0.f;
+      };
+      float f_cur[2], f_nxt[2];
+      load_f(0, f_cur);
+      load_f(1, f_nxt);
       for (int kb = 0; kb < KT; ++kb) {
         const int buf = kb & 1;
+        float f_far[2];
+        load_f(kb + 2, f_far);
         if (!wait_or_abort(&sm.acc_full[buf], (kb / 2) & 1, a, abort_flag)) break;
         tc_fence_after();
-        const float sa = live ? a.a_groupscale[r * a.a_groups + kb] : 0.f;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          const long br = blockrow[cc];
-          const float sw = br < RB ? ws[((long)e * RB + br) * CB + kb] : 0.f;
-          const float f = sa * sw;
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             float v[16];
             tmem_ld_32x32b_x16(trow + buf * BN + 64 * h + 32 * cc + 16 * p, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              acc[32 * cc + 16 * p + i] = fmaf(v[i], f, acc[32 * cc + 16 * p + i]);
+            for (int i = 0; i < 16; i += 2)
+              fma_f32x2(acc[32 * cc + 16 * p + i], acc[32 * cc + 16 * p + i + 1], v[i], v[i + 1],
+                        f_cur[cc]);
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          f_cur[cc] = f_nxt[cc];
+          f_nxt[cc] = f_far[cc];
+        }
       }
     } else if (wait_or_abort(&sm.done, 0, a, abort_flag)) {
       tc_fence_after();
