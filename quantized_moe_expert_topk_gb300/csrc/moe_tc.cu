@@ -9,15 +9,16 @@
 // TMEM.  Operand kinds:
 //   K_BF16  bf16 weights:   A (sorted bf16 rows) and B by 2-D TMA, kind::f16
 //   K_FP8   e4m3 weights:   A (sorted e4m3 codes) and B by 2-D TMA, kind::f8f6f4
-//   K_FP4   MXFP4 / NVFP4:  A by 2-D TMA; B streamed as load-time packed
-//                           records (TMA bulk copy) and decoded by four warps
-//                           into exact bf16 in the swizzled layout, kind::f16
+//   K_FP4   MXFP4 / NVFP4:  A (sorted f16 rows) by 2-D TMA; B streamed as
+//                           load-time packed records (TMA bulk copy) and
+//                           decoded by the eight epilogue warps into exact f16
+//                           (code x group scale) in the swizzled layout,
+//                           kind::f16 with f16 operands
 // Every stage is 128 bytes of reduction per row (64 bf16 / 128 e4m3), i.e. one
 // 128-byte swizzle atom.  Warp roles: warp 0 TMA producer; warp 1 TMEM owner,
 // lane 0 issues tcgen05.mma + tcgen05.commit; warps 2-9 epilogue (tcgen05.ld,
-// scales, bias, activation or router weight +
-// red.add); for FP4 weights the same eight warps decode B during the main
-// loop.  FP8 128x128 block scales: every 128-wide reduction block lands in
+// scales, bias, activation or router weight + red.add); for FP4 weights the
+// same eight warps decode B during the main loop.  FP8 128x128 block scales: every 128-wide reduction block lands in
 // one of two TMEM buffers and the epilogue warps fold it into registers with
 // a_scale[row, kb] * w_scale[block, kb] (promotion).  Two CTAs share an SM
 // (3-stage rings, 256 TMEM columns each), so one CTA's epilogue overlaps the
