@@ -21,6 +21,7 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_ptx.cuh"
 
 namespace moe {
 
@@ -42,6 +43,9 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
              int El, int BM, int32_t *__restrict__ sorted, int32_t *__restrict__ expert_ids,
              int32_t *__restrict__ ntp, int32_t *__restrict__ counts, long cap, AlignExtras x,
              int zero_ctas, int conv_ctas) {
+  // a dependent grid (the streaming GEMM) may be scheduled now: it waits for
+  // this grid's completion before it reads anything written here
+  griddep_launch_dependents();
   if (blockIdx.x > 0 && (int)blockIdx.x <= zero_ctas) {
     // zeroing CTAs: 16-byte stores over the aligned body, scalar tail
     const long n4 = x.zero_n / 4;

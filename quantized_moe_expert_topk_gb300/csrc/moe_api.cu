@@ -577,7 +577,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     // 4. bf16 output
     {
       StageScope sc(MOE_STAGE_FINALIZE, st);
-      rc = cuda_status(launch_finalize(acc, MK, out_bf16, st));
+      rc = cuda_status(launch_finalize(acc, MK, out_bf16, st, true));
       sc.done();
     }
     timing_collect();

@@ -24,6 +24,7 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_ptx.cuh"
 
 namespace moe {
 
@@ -405,6 +406,7 @@ cudaError_t launch_mode(const GemmArgs &a, long cap_rows, cudaStream_t stream) {
 }
 
 __global__ void finalize_kernel(const float *__restrict__ acc, long n, uint16_t *__restrict__ out) {
+  griddep_wait();  // the accumulator is complete (dependent launch after the w2 kernel)
   const long i = ((long)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (i + 3 < n) {
     const float4 v = *reinterpret_cast<const float4 *>(acc + i);
@@ -435,11 +437,11 @@ cudaError_t launch_gemm_w2(const GemmArgs &a, long cap_rows, cudaStream_t stream
   return launch_mode<MODE_W2>(a, cap_rows, stream);
 }
 
-cudaError_t launch_finalize(const float *acc, long n, void *out_bf16, cudaStream_t stream) {
+cudaError_t launch_finalize(const float *acc, long n, void *out_bf16, cudaStream_t stream,
+                            bool dependent) {
   if (n <= 0) return cudaSuccess;
-  finalize_kernel<<<(unsigned)ceil_div(ceil_div(n, 4), 256), 256, 0, stream>>>(
-      acc, n, static_cast<uint16_t *>(out_bf16));
-  return cudaGetLastError();
+  return launch_kernel(finalize_kernel, dim3((unsigned)ceil_div(ceil_div(n, 4), 256)), dim3(256), 0,
+                       stream, dependent, acc, n, static_cast<uint16_t *>(out_bf16));
 }
 
 cudaError_t launch_zero(float *buf, long n, cudaStream_t stream) {

@@ -8,6 +8,26 @@
 
 namespace moe {
 
+// Launch `kern` on `stream`; with `dependent` set, as a programmatic dependent
+// of the previous kernel in the stream (it may start while that kernel drains
+// and must call griddepcontrol.wait before reading that kernel's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool dependent, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = dependent ? attr : nullptr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Tile height (sorted rows per block) of the mma.sync grouped GEMMs; the
 // expert sort pads every expert to a multiple of it.
 constexpr int kGenericBlockM = 64;
@@ -165,7 +185,8 @@ cudaError_t launch_gather_rows(const GatherArgs &g, long cap_rows, cudaStream_t 
 cudaError_t launch_tc_gemm(const TcArgs &a, const void *a_sorted, long cap_rows, int w13,
                            cudaStream_t st);
 
-cudaError_t launch_finalize(const float *acc, long n, void *out_bf16, cudaStream_t stream);
+cudaError_t launch_finalize(const float *acc, long n, void *out_bf16, cudaStream_t stream,
+                            bool dependent = false);
 cudaError_t launch_zero(float *buf, long n, cudaStream_t stream);
 
 }  // namespace moe

@@ -48,15 +48,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // `limit_cycles` SM clock cycles and returns false (the caller records an
 // error and winds down); never spins forever.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
-                                                  long long limit_cycles) {
+                                                  long long limit_cycles,
+                                                  const volatile int *global_err = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    // the clock is read every 64 polls only (try_wait itself suspends the
-    // thread for a short while when the phase is not complete)
-    if ((n & 63) == 0 && clock64() - t0 > limit_cycles) return false;
+    // the clock (and the grid-wide error word, set by any CTA that gave up)
+    // is read every 64 polls only (try_wait itself suspends the thread for a
+    // short while when the phase is not complete)
+    if ((n & 63) == 0) {
+      if (clock64() - t0 > limit_cycles) return false;
+      if (global_err && *global_err) return false;
+    }
   }
+}
+
+// Programmatic dependent launch.  griddep_wait: the calling thread waits until
+// the grid launched before this one in the stream has completed and its memory
+// is visible (a no-op when this grid was not launched as a dependent).
+// griddep_launch_dependents: this CTA allows the next grid in the stream, if
+// launched as a dependent, to start (it still waits for completion itself).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Orders this thread's earlier generic-proxy view of global memory before its
+// later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // TMA bulk copy global -> shared (this CTA), completing `bytes` of
@@ -99,7 +121,9 @@ __device__ __forceinline__ void ldmatrix_x2_b16(uint32_t (&r)[2], uint32_t addr)
 // D = A(16x16 f16, row) * B(16x8 f16, col) + C, fp32 accumulate.
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                               uint32_t b1, const float (&c)[4]) {
-  asm volatile(
+  // register-only: not volatile, so the compiler may interleave it with the
+  // surrounding conversions
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%10,%11,%12,%13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -189,6 +213,17 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float (&v)[32
 }
 
 // 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(

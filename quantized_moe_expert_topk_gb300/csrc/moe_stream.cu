@@ -101,10 +101,11 @@ __device__ __forceinline__ Unit decode_unit(const StreamArgs &a, int id) {
 }
 
 // Byte `idx` of `w` (an e8m0 code c) as the fp32 value 2^(c-127): the byte is
-// moved to the top byte and shifted right once into the exponent field.  Code
-// 0 (2^-127, below the fp32 normal range) reads as 0.
+// isolated (one byte permute) and multiplied by 2^23 (an integer multiply-add,
+// off the integer/logic pipe) into the exponent field.  Code 0 (2^-127, below
+// the fp32 normal range) reads as 0.
 __device__ __forceinline__ float e8m0_byte_f32(uint32_t w, uint32_t idx) {
-  return __uint_as_float(__byte_perm(w, 0u, 0x0444u | (idx << 12)) >> 1);
+  return __uint_as_float(__byte_perm(w, 0u, 0x4440u | idx) * 8388608u);
 }
 
 // One k64 block of one consumer warp: MT m16 tiles x NTILES n8 token tiles.
@@ -166,7 +167,7 @@ __device__ __forceinline__ void consume_k64(const unsigned char *tp0, uint32_t x
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
+__global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -182,7 +183,6 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
   __syncthreads();
   volatile int *abort_flag = &sm.abort_flag;
 
-  const int n_units = *a.n_active * a.units_per_expert * a.ksplit;
   const int C = a.C;  // reduction length (K for W13, N for W2)
 
   if (warp == CW) {
@@ -190,11 +190,29 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
     // Claims units from a global counter (dynamic load balance), streams each
     // unit's weight records and the matching token rows into the ring, and
     // ends with a terminator stage.
+    //
+    // Dependent launch: the W13 grid may start while the sort grid runs, so
+    // its producer waits for it before reading any of its outputs (counts,
+    // offsets, the zeroed counters, the f16 copy of x).  The W2 grid starts
+    // once every W13 CTA got here (so the sort is complete); its producer
+    // already streams weights and waits for the W13 grid only before the
+    // first copy of the intermediate rows.
+    bool waited = false;
+    auto wait_prior = [&]() {
+      if (!waited) {
+        griddep_wait();
+        fence_proxy_async_global();
+        if (lane == 0) griddep_launch_dependents();
+        waited = true;
+      }
+    };
+    if (MODE == MODE_W13) wait_prior();
+    const int n_units = *a.n_active * a.units_per_expert * a.ksplit;
     uint32_t it = 0;
     bool ok = true;
     auto acquire_slot = [&](int &slot) -> bool {
       slot = it % NS;
-      if (!mbar_wait_bounded(&sm.empty[slot], ((it / NS) & 1) ^ 1, kWaitCycles)) {
+      if (!mbar_wait_bounded(&sm.empty[slot], ((it / NS) & 1) ^ 1, kWaitCycles, a.err)) {
         record_device_error(a.err, kErrTimeout);
         *abort_flag = 1;
       }
@@ -205,6 +223,7 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
       if (lane == 0) id = atomicAdd(a.work_counter, 1);
       id = __shfl_sync(0xffffffffu, id, 0);
       if (id >= n_units) {
+        wait_prior();  // also lets the next grid start
         int slot;
         if (acquire_slot(slot) && lane == 0) {
           sm.desc[slot] = StageDesc{-1, 0, 0, 0, Unit{0, 0, 0, 0, 0, 0}};
@@ -222,6 +241,8 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
           const long src = MODE == MODE_W13 ? (long)(a.sorted_ids[r] / a.T) : (long)r;
           xrow = static_cast<const unsigned char *>(a.x16) + src * (long)C * 2;
         }
+        const unsigned char *ubase = static_cast<const unsigned char *>(a.packed) +
+            ((((long)U.e * a.units_per_expert + U.u) * a.kblocks) + U.kb0) * REC_BYTES;
         for (int kb = 0; kb < U.nkb; kb += S_KB) {
           const int nkb = min(S_KB, U.nkb - kb);
           int slot;
@@ -234,11 +255,10 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
                                       (kb == 0 ? F_FIRST : 0) | (kb + S_KB >= U.nkb ? F_LAST : 0),
                                       U};
             mbar_arrive_expect_tx(&sm.full[slot], wbytes + (uint32_t)nt * xbytes);
-            const unsigned char *src = static_cast<const unsigned char *>(a.packed) +
-                ((((long)U.e * a.units_per_expert + U.u) * a.kblocks) + U.kb0 + kb) * REC_BYTES;
-            tma_bulk_g2s(ws, src, wbytes, &sm.full[slot]);
+            tma_bulk_g2s(ws, ubase + (long)kb * REC_BYTES, wbytes, &sm.full[slot]);
           }
           __syncwarp();
+          wait_prior();  // the token rows of W2 are the W13 grid's output
           if (lane < nt)
             tma_bulk_g2s(ws + W_STAGE + lane * XS, xrow + (long)(U.kb0 + kb) * 128, xbytes,
                          &sm.full[slot]);
@@ -268,7 +288,7 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
   float tok_f[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // W13: x_inv of the token; W2: router weight
   while (true) {
     const int slot = it % NS;
-    if (!mbar_wait_bounded(&sm.full[slot], (it / NS) & 1, kWaitCycles)) {
+    if (!mbar_wait_bounded(&sm.full[slot], (it / NS) & 1, kWaitCycles, a.err)) {
       record_device_error(a.err, kErrTimeout);
       *abort_flag = 1;
     }
@@ -317,12 +337,22 @@ __global__ void __launch_bounds__(THREADS) stream_kernel(StreamArgs a) {
     const int nkb = min(S_KB, U.nkb - d.kb);
     const unsigned char *ws = sm.stage[slot];
     const uint32_t xs = smem_addr(ws + W_STAGE);
+    const unsigned char *tw = ws + (warp * MT) * TILE_BYTES;
+    if (nkb == S_KB) {
+      // full stage: straight-line code over the S_KB blocks, so the
+      // conversions, MMAs and scale FMAs of different blocks interleave
+      if (ntiles == 2) {
 #pragma unroll
-    for (int b = 0; b < S_KB; ++b) {
-      if (b >= nkb) break;
-      const unsigned char *tp0 = ws + b * REC_BYTES + (warp * MT) * TILE_BYTES;
-      if (ntiles == 2) consume_k64<2>(tp0, xs + b * 128, lane, acc);
-      else consume_k64<1>(tp0, xs + b * 128, lane, acc);
+        for (int b = 0; b < S_KB; ++b) consume_k64<2>(tw + b * REC_BYTES, xs + b * 128, lane, acc);
+      } else {
+#pragma unroll
+        for (int b = 0; b < S_KB; ++b) consume_k64<1>(tw + b * REC_BYTES, xs + b * 128, lane, acc);
+      }
+    } else {
+      for (int b = 0; b < nkb; ++b) {
+        if (ntiles == 2) consume_k64<2>(tw + b * REC_BYTES, xs + b * 128, lane, acc);
+        else consume_k64<1>(tw + b * REC_BYTES, xs + b * 128, lane, acc);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[slot]);
@@ -459,8 +489,8 @@ cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream
   long grid = (long)CTAS_PER_SM * sm_count;
   if (grid > max_units) grid = max_units;
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(a);
-  return cudaGetLastError();
+  // a programmatic dependent of the previous kernel (the sort, or the W13 grid)
+  return launch_kernel(kern, dim3((unsigned)grid), dim3(THREADS), SMEM_BYTES, stream, true, a);
 }
 
 }  // namespace moe

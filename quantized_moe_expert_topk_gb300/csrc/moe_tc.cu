@@ -92,7 +92,7 @@ __device__ __forceinline__ uint32_t sw128(int n, int c) {
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, const TcArgs &a,
                                               volatile int *abort_flag) {
   if (*abort_flag) return false;
-  if (!mbar_wait_bounded(bar, parity, kWaitCycles)) {
+  if (!mbar_wait_bounded(bar, parity, kWaitCycles, a.err)) {
     record_device_error(a.err, kErrTimeout);
     *abort_flag = 1;
     return false;
@@ -166,14 +166,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const long rec_stride = (long)a.rec_bytes;
+      int issued = 0, issued_raw = 0;  // stages whose copies were started
       for (int kt = 0; kt < KT; ++kt) {
         const int s = kt % NS;
         const uint32_t par = ((kt / NS) & 1) ^ 1;
         if (!wait_or_abort(&sm.empty[s], par, a, abort_flag)) break;
+        issued = kt + 1;
         if (KIND == K_FP4) {
           mbar_arrive_expect_tx(&sm.full_a[s], STAGE_A);
           tma_load_2d(sm.a[s], &tmA, kt * BKE, blk * BM, &sm.full_a[s]);
           if (!wait_or_abort(&sm.raw_empty[s], par, a, abort_flag)) break;
+          issued_raw = kt + 1;
           const unsigned char *src = static_cast<const unsigned char *>(a.w_packed) +
               (((long)e * a.ntiles + nt) * KT + kt) * rec_stride;
           mbar_arrive_expect_tx(&sm.full_raw[s], (uint32_t)a.rec_bytes);
@@ -186,6 +189,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tma_load_2d(sm.b[s] + b * 4096, &tmB, kt * BKE,
                         (int)((long)e * a.R + group_row<MODE>(a, nt, b)), &sm.full_a[s]);
         }
+      }
+      if (*abort_flag) {
+        // after an abort, let the copies already issued land before the CTA
+        // exits (bounded; no early exit on the error word here)
+        for (int kt = issued > NS ? issued - NS : 0; kt < issued; ++kt)
+          mbar_wait_bounded(&sm.full_a[kt % NS], (kt / NS) & 1, kWaitCycles);
+        for (int kt = issued_raw > NS ? issued_raw - NS : 0; kt < issued_raw; ++kt)
+          mbar_wait_bounded(&sm.full_raw[kt % NS], (kt / NS) & 1, kWaitCycles);
       }
     }
   } else if (warp == 1) {
