@@ -92,6 +92,12 @@ __device__ __forceinline__ void tma_bulk_g2s(void *dst, const void *src, uint32_
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (a hint; no completion to wait for).
+// src and bytes must be multiples of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Four bytes of packed e2m1 pairs -> four f16x2 registers (low nibble in the
 // low half), one hardware convert per byte.  Exact: every e2m1 value is an
 // f16 value.

@@ -107,6 +107,7 @@ __device__ __forceinline__ void red_add_v4(float *p, float x, float y, float z, 
 }
 
 constexpr int kTcRasterGroup = 1;
+constexpr int kPrefetchStages = 12;  // FP4 weight records prefetched into L2 ahead
 
 template <int MODE, int KIND>
 __global__ void __launch_bounds__(THREADS, 2)
@@ -175,10 +176,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (KIND == K_FP4) {
           mbar_arrive_expect_tx(&sm.full_a[s], STAGE_A);
           tma_load_2d(sm.a[s], &tmA, kt * BKE, blk * BM, &sm.full_a[s]);
+          // the weight records of one tile are contiguous: keep the next
+          // kPrefetchStages of them on their way into L2, far ahead of the
+          // small shared-memory ring (the weight stream is latency-bound)
+          const unsigned char *tile_rec = static_cast<const unsigned char *>(a.w_packed) +
+              ((long)e * a.ntiles + nt) * KT * rec_stride;
+          {
+            const int p0 = kt == 0 ? 1 : kt + kPrefetchStages;
+            const int p1 = min(KT, kt == 0 ? 1 + kPrefetchStages : p0 + 1);
+            if (p0 < p1)
+              prefetch_l2_bulk(tile_rec + p0 * rec_stride, (uint32_t)((p1 - p0) * rec_stride));
+          }
           if (!wait_or_abort(&sm.raw_empty[s], par, a, abort_flag)) break;
           issued_raw = kt + 1;
-          const unsigned char *src = static_cast<const unsigned char *>(a.w_packed) +
-              (((long)e * a.ntiles + nt) * KT + kt) * rec_stride;
+          const unsigned char *src = tile_rec + kt * rec_stride;
           mbar_arrive_expect_tx(&sm.full_raw[s], (uint32_t)a.rec_bytes);
           tma_bulk_g2s(sm.raw[s], src, (uint32_t)a.rec_bytes, &sm.full_raw[s]);
         } else {
