@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--M", type=int, default=None)
     ap.add_argument("--E", type=int, default=None, help="routed experts (smaller profiling cases)")
+    ap.add_argument("--routing", action="store_true",
+                    help="include the fused router (logits -> top-k) in the timed step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -260,12 +262,29 @@ def workload_config(wl):
             "gate": wl.gate, "recipe": wl.recipe}
 
 
-def launches_per_step(wl):
+def kernel_path(wl):
+    """The kernel family moe_fused_experts picks for this workload (its
+    default, automatic selection)."""
+    slots = wl.M * wl.T
+    if (wl.wfmt == "mxfp4" and wl.afmt == "bf16" and wl.act == "swiglu_oai"
+            and wl.K % 64 == 0 and wl.N % 64 == 0 and slots <= 32 * wl.El):
+        return "stream"
+    return "tc" if slots >= 2048 else "generic"
+
+
+def launches_per_step(wl, routing=False):
+    """Kernels of this library launched by one step."""
     import quantized_moe_expert_topk_gb300 as moe
-    n = 1                                  # sort / pad (+ zero the accumulator)
+    path = kernel_path(wl)
+    s2 = moe.stage2_format(wl.wfmt, wl.afmt)
+    n = int(routing)                       # fused router
+    n += 1                                 # sort / pad (+ zero, + f16 copy of x when streaming)
+    if path == "stream":
+        return n + 3                       # w13, w2, finalize
     n += wl.afmt != "bf16"                 # stage-1 activation quantiser
+    n += path == "tc"                      # gather of the sorted activation rows
     n += 1                                 # w13 GEMM + activation
-    n += moe.stage2_format(wl.wfmt, wl.afmt) != "bf16"  # stage-2 requantiser
+    n += s2 != "bf16" or (path == "tc" and wl.wfmt == "mxfp4")  # requantiser / f16 rescale
     n += 2                                 # w2 GEMM + reduce, bf16 finalize
     return n
 
@@ -293,8 +312,21 @@ def run_ours(args):
     out = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
+    routed_k = wl.T
+    if args.routing:
+        if wl.E != wl.router_logits.shape[1]:
+            raise SystemExit("--routing: workloads with shared experts are not supported")
+        logits = wl.router_logits.float().contiguous()
+        r_ids = torch.empty_like(wl.topk_ids)
+        r_w = torch.empty_like(wl.topk_weights)
+
     def step():
-        layer(wl.x, wl.topk_ids, wl.topk_weights, wl.expert_map, out=out, stream=stream)
+        if args.routing:
+            moe.moe_route_topk(logits, routed_k, r_ids, r_w, scoring="softmax", renorm=True,
+                               stream=stream)
+            layer(wl.x, r_ids, r_w, wl.expert_map, out=out, stream=stream)
+        else:
+            layer(wl.x, wl.topk_ids, wl.topk_weights, wl.expert_map, out=out, stream=stream)
 
     # eager warm-up, then capture one step as a CUDA graph
     with torch.cuda.stream(stream):
@@ -374,9 +406,15 @@ def run_ours(args):
                            "alg_bytes": alg["layer_bytes"], "alg_flops": alg["flops"],
                            "active_experts": alg["active_experts"], "live_slots": alg["live_slots"]},
         "e2e": e2e,
-        "gpu_launches": launches_per_step(wl) * args.steps,
+        "gpu_launches": launches_per_step(wl, args.routing) * args.steps,
         "clocks": summarize_clocks(rows, "warmup soak + timed region"),
     }
+    if args.routing:
+        line["config"]["routing"] = "fused router in the step: softmax, top-k, renormalised"
+        line["routing"] = {"kernel_ms": time_router(moe, logits, routed_k, r_ids, r_w, stream),
+                           "path": kernel_path(wl)}
+    else:
+        line["config"]["path"] = kernel_path(wl)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds,
                                             max_tokens=None if wl.M <= 128 else 32)
@@ -399,6 +437,21 @@ def expert_counts(moe, wl, dev):
                              expert_ids, ntp, counts)
     torch.cuda.synchronize()
     return counts.cpu().tolist()
+
+
+def time_router(moe, logits, k, ids, w, stream, iters=200):
+    """Average duration of one router launch (CUDA events on its stream)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            moe.moe_route_topk(logits, k, ids, w, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            moe.moe_route_topk(logits, k, ids, w, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
 
 
 def time_w13_kernel(moe, wl, layer, dev, stream, iters):

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 typedef enum {
   MOE_OK = 0,
@@ -166,6 +166,37 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int topk, const int32_t
                          int num_experts, int num_local_experts, int block_m,
                          int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
                          int32_t *expert_counts, void *stream);
+
+/* Router: logits -> top-k expert ids and weights, the routing that the
+ * apply_monolithic path hands to the expert kernel together with the logits
+ * (GptOssMxfp4MoEMethod.apply_monolithic and Mxfp4MoEMethod.apply_monolithic
+ * on "vLLM/vllm/model_executor/layers/quantization/mxfp4.py" and
+ * QuarkOCP_MX_MoEMethod.apply_monolithic on the quark_moe page pass
+ * router_logits, num_expert_group, topk_group, e_score_correction_bias and
+ * routed_scaling_factor; the renormalised softmax top-k is the routing of the
+ * GPT-OSS layers there).  The pages name the arguments but print no algorithm;
+ * the rule implemented is the plain reading, per token t:
+ *   s_e = softmax(logits[t])_e        (scoring MOE_SCORE_SOFTMAX)
+ *       = 1 / (1 + exp(-logits[t,e])) (scoring MOE_SCORE_SIGMOID)
+ *   keys: c_e = s_e + bias_e with a bias (e_score_correction_bias), else the
+ *         logits themselves (same order as s, no rounding in the choice)
+ *   groups (num_groups > 1; E % num_groups == 0, contiguous groups): a group
+ *         scores the sum of its two largest keys with a bias, its largest key
+ *         without; only the topk_group best groups (ties to the lower group)
+ *         stay eligible
+ *   ids:  the topk eligible experts with the largest keys, in descending key
+ *         order, ties to the lower id
+ *   w_j = s_{id_j} (never the bias), divided by sum_j s_{id_j} when renorm,
+ *         times routed_scaling_factor.
+ *   logits  f32 or bf16 (logits_bf16 != 0) [M, E];  bias f32 [E] or NULL
+ *   topk_ids int32 [M, topk];  topk_weights f32 [M, topk]
+ * Limits: E <= 1024, topk <= 32, num_groups <= 32 (0 or 1 = no groups),
+ * topk <= topk_group * E / num_groups.  Computation in fp32. */
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+int moe_route_topk(const void *logits, int logits_bf16, int M, int num_experts, int topk,
+                   int scoring, int renorm, int num_groups, int topk_group, const float *bias,
+                   float routed_scaling_factor, int32_t *topk_ids, float *topk_weights,
+                   void *stream);
 
 /* Stage-1 activation quantiser (AiterFp8TensorExperts, AiterFp8ChannelExperts,
  * AiterFp8BlockExperts, QuarkNvfp4MoEMethod).  x is bf16 [rows, cols].

@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.orc_num_threads.restype = i; L.orc_num_threads.argtypes = []
         L.orc_route_topk.restype = None
         L.orc_route_topk.argtypes = [p, i, i, i, i, p, p]
+        L.orc_route_grouped.restype = None
+        L.orc_route_grouped.argtypes = [p, i, i, i, i, i, i, i, p, ctypes.c_double, p, p]
         L.orc_align_capacity.restype = l; L.orc_align_capacity.argtypes = [i, i, i, i]
         L.orc_align_block_size.restype = i
         L.orc_align_block_size.argtypes = [p, i, i, p, i, i, i, p, p, p, p]
@@ -142,6 +144,21 @@ def route_topk(logits: np.ndarray, k: int, renorm: bool = True):
     ids = np.zeros((M, k), np.int32)
     w = np.zeros((M, k), np.float64)
     lib().orc_route_topk(_ptr(lg), M, E, k, int(renorm), _ptr(ids), _ptr(w))
+    return ids, w
+
+
+def route_grouped(logits: np.ndarray, k: int, scoring: str = "softmax", renorm: bool = True,
+                  num_groups: int = 0, topk_group: int = 0, bias=None, scale: float = 1.0):
+    """Router of the apply_monolithic path (orc_route_grouped): ids int32 [M, k],
+    weights fp64 [M, k]."""
+    lg = _c(logits, np.float64)
+    M, E = lg.shape
+    b = _c(bias, np.float64)
+    ids = np.zeros((M, k), np.int32)
+    w = np.zeros((M, k), np.float64)
+    lib().orc_route_grouped(_ptr(lg), M, E, k, {"softmax": 0, "sigmoid": 1}[scoring], int(renorm),
+                            num_groups if num_groups > 1 else 1, topk_group, _ptr(b), float(scale),
+                            _ptr(ids), _ptr(w))
     return ids, w
 
 

@@ -186,6 +186,80 @@ void orc_route_topk(const double *logits, int M, int E, int k, int renorm,
   free(taken);
 }
 
+/* Router of the apply_monolithic path (router logits, num_expert_group,
+ * topk_group, e_score_correction_bias, routed_scaling_factor), read as:
+ *   s_e   = softmax(l)_e (scoring 0) or 1 / (1 + exp(-l_e)) (scoring 1)
+ *   key_e = s_e + bias_e with a bias, else l_e (the same order as s_e)
+ *   G > 1: group g (experts g*E/G .. (g+1)*E/G - 1) scores the sum of its two
+ *          largest keys (bias) or its largest key (no bias); the TG best
+ *          groups, ties to the lower group, stay eligible
+ *   ids   = the k eligible experts with the largest keys, descending, ties to
+ *           the lower id
+ *   w_j   = s_{id_j}, divided by their sum when renorm, times scale. */
+void orc_route_grouped(const double *logits, int M, int E, int k, int scoring, int renorm, int G,
+                       int TG, const double *bias, double scale, int32_t *ids, double *weights) {
+  double *sc = (double *)malloc(sizeof(double) * E);
+  double *key = (double *)malloc(sizeof(double) * E);
+  char *ok = (char *)malloc(E);
+  double *gscore = (double *)malloc(sizeof(double) * (G > 1 ? G : 1));
+  char *gkeep = (char *)malloc(G > 1 ? G : 1);
+  for (int t = 0; t < M; ++t) {
+    const double *l = logits + (size_t)t * E;
+    if (scoring == 0) {
+      double mx = l[0];
+      for (int e = 1; e < E; ++e) if (l[e] > mx) mx = l[e];
+      double z = 0.0;
+      for (int e = 0; e < E; ++e) { sc[e] = exp(l[e] - mx); z += sc[e]; }
+      for (int e = 0; e < E; ++e) sc[e] /= z;
+    } else {
+      for (int e = 0; e < E; ++e) sc[e] = 1.0 / (1.0 + exp(-l[e]));
+    }
+    for (int e = 0; e < E; ++e) {
+      key[e] = bias ? sc[e] + bias[e] : l[e];
+      ok[e] = 1;
+    }
+    if (G > 1) {
+      const int gs = E / G;
+      for (int g = 0; g < G; ++g) {
+        double b1 = -INFINITY, b2 = -INFINITY;
+        for (int e = g * gs; e < (g + 1) * gs; ++e) {
+          if (key[e] > b1) { b2 = b1; b1 = key[e]; }
+          else if (key[e] > b2) b2 = key[e];
+        }
+        gscore[g] = bias ? b1 + b2 : b1;
+        gkeep[g] = 0;
+      }
+      for (int j = 0; j < TG; ++j) {
+        int best = -1;
+        for (int g = 0; g < G; ++g)
+          if (!gkeep[g] && (best < 0 || gscore[g] > gscore[best])) best = g;
+        gkeep[best] = 1;
+      }
+      for (int e = 0; e < E; ++e) ok[e] = gkeep[e / gs];
+    }
+    double sel = 0.0;
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e)
+        if (ok[e] && (best < 0 || key[e] > key[best])) best = e;
+      ok[best] = 0;
+      ids[(size_t)t * k + j] = best;
+      weights[(size_t)t * k + j] = sc[best];
+      sel += sc[best];
+    }
+    for (int j = 0; j < k; ++j) {
+      double w = weights[(size_t)t * k + j];
+      if (renorm) w /= sel;
+      weights[(size_t)t * k + j] = w * scale;
+    }
+  }
+  free(sc);
+  free(key);
+  free(ok);
+  free(gscore);
+  free(gkeep);
+}
+
 /* ========================= expert sort / padding ======================== */
 
 static int local_expert(int32_t g, const int32_t *emap, int E, int El) {

@@ -31,7 +31,8 @@ EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align
            "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_reduce", "moe_fused_experts",
            "moe_get_device_error", "moe_reset_device_error", "moe_noalloc_scratch_bytes",
            "moe_fused_experts_noalloc", "moe_packed_weight_bytes", "moe_prepare_weights",
-           "moe_stage_timing", "moe_stage_times", "moe_set_path", "moe_get_path")
+           "moe_stage_timing", "moe_stage_times", "moe_set_path", "moe_get_path",
+           "moe_route_topk")
 PATHS = {"auto": 0, "generic": 1, "stream": 2, "tc": 3}
 STAGES = ("align", "quant", "w13", "requant", "w2", "finalize")
 
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
         "moe_align_capacity": (l, [i, i, i, i]),
         "moe_align_block_size": (i, [p, i, i, p, i, i, i, p, p, p, p, p]),
         "moe_quant_act": (i, [p, i, i, i, p, p, p, p]),
+        "moe_route_topk": (i, [p, i, i, i, i, i, i, i, i, p, ctypes.c_float, p, p, p]),
         "moe_w13_workspace_size": (sz, [P, i]),
         "moe_grouped_gemm_w13_act": (i, [P, p, p, W, p, p, p, i, p, p, p, sz, p]),
         "moe_grouped_gemm_w2_reduce": (i, [P, p, p, W, p, p, p, p, i, p, p, p]),
@@ -164,6 +166,23 @@ def moe_align_block_size(topk_ids, expert_map, E, El, block_m, sorted_ids, exper
     _check("moe_align_block_size", lib().moe_align_block_size(
         _ptr(topk_ids), M, T, _ptr(expert_map), E, El, block_m, _ptr(sorted_ids),
         _ptr(expert_ids), _ptr(num_post_pad), _ptr(expert_counts), _stream(stream)))
+
+
+SCORING = {"softmax": 0, "sigmoid": 1}
+
+
+def moe_route_topk(logits, topk: int, topk_ids, topk_weights, scoring: str = "softmax",
+                   renorm: bool = True, num_groups: int = 0, topk_group: int = 0, bias=None,
+                   routed_scaling_factor: float = 1.0, stream=None):
+    """logits f32 or bf16 [M, E] -> topk_ids int32 [M, topk], topk_weights f32 [M, topk]."""
+    M, E = logits.shape
+    bf16 = logits.dtype == torch.bfloat16
+    if not bf16 and logits.dtype != torch.float32:
+        raise TypeError("logits must be float32 or bfloat16")
+    _check("moe_route_topk", lib().moe_route_topk(
+        _ptr(logits), int(bf16), M, E, topk, SCORING[scoring], int(renorm), num_groups, topk_group,
+        _ptr(bias), float(routed_scaling_factor), _ptr(topk_ids), _ptr(topk_weights),
+        _stream(stream)))
 
 
 def moe_quant_act(x, afmt: str, scale_in, codes, scales, stream=None):

@@ -43,9 +43,13 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
              int El, int BM, int32_t *__restrict__ sorted, int32_t *__restrict__ expert_ids,
              int32_t *__restrict__ ntp, int32_t *__restrict__ counts, long cap, AlignExtras x,
              int zero_ctas, int conv_ctas) {
-  // a dependent grid (the streaming GEMM) may be scheduled now: it waits for
-  // this grid's completion before it reads anything written here
+  // Launched as a programmatic dependent of the previous kernel (the router,
+  // or whatever produced topk_ids): every CTA waits for it before reading the
+  // ids or overwriting buffers it may still read.  A dependent grid (the
+  // streaming GEMM) may be scheduled now: it waits for this grid's completion
+  // before it reads anything written here.
   griddep_launch_dependents();
+  griddep_wait();
   if (blockIdx.x > 0 && (int)blockIdx.x <= zero_ctas) {
     // zeroing CTAs: 16-byte stores over the aligned body, scalar tail
     const long n4 = x.zero_n / 4;
@@ -268,10 +272,9 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *e
     conv_ctas = (int)ceil_div(extra.xM, kAlignThreads / 128);
     if (conv_ctas > 2 * 152) conv_ctas = 2 * 152;
   }
-  align_kernel<<<1 + zero_ctas + conv_ctas, kAlignThreads, smem, stream>>>(
-      topk_ids, (long)M * T, expert_map, E, El, BM, sorted_ids, expert_ids, num_post_pad, counts,
-      cap, extra, zero_ctas, conv_ctas);
-  return cudaGetLastError();
+  return launch_kernel(align_kernel, dim3(1 + zero_ctas + conv_ctas), dim3(kAlignThreads), smem,
+                       stream, true, topk_ids, (long)M * T, expert_map, E, El, BM, sorted_ids,
+                       expert_ids, num_post_pad, counts, cap, extra, zero_ctas, conv_ctas);
 }
 
 }  // namespace moe

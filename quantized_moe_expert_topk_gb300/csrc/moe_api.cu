@@ -400,6 +400,27 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int topk, const int32_t
                                   cap, AlignExtras(), static_cast<cudaStream_t>(stream)));
 }
 
+int moe_route_topk(const void *logits, int logits_bf16, int M, int num_experts, int topk,
+                   int scoring, int renorm, int num_groups, int topk_group, const float *bias,
+                   float routed_scaling_factor, int32_t *topk_ids, float *topk_weights,
+                   void *stream) {
+  const int E = num_experts;
+  if (M < 0 || E < 1 || E > 1024 || topk < 1 || topk > 32 || topk > E) return MOE_ERR_INVALID_ARG;
+  if (scoring != MOE_SCORE_SOFTMAX && scoring != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (num_groups < 0 || num_groups > 32) return MOE_ERR_INVALID_ARG;
+  if (num_groups > 1) {
+    if (E % num_groups != 0 || topk_group < 1 || topk_group > num_groups) return MOE_ERR_INVALID_ARG;
+    if ((long)topk_group * (E / num_groups) < topk) return MOE_ERR_INVALID_ARG;
+  }
+  if (!(routed_scaling_factor == routed_scaling_factor)) return MOE_ERR_INVALID_ARG;  // NaN
+  if (M == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_weights) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_route(logits, logits_bf16 ? 1 : 0, M, E, topk, scoring, renorm ? 1 : 0,
+                                  num_groups > 1 ? num_groups : 1, topk_group, bias,
+                                  routed_scaling_factor, topk_ids, topk_weights,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
 int moe_quant_act(const void *x_bf16, int rows, int cols, int afmt, const float *scale_in,
                   void *codes, void *scales, void *stream) {
   if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;

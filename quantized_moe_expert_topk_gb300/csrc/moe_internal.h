@@ -185,6 +185,9 @@ cudaError_t launch_gather_rows(const GatherArgs &g, long cap_rows, cudaStream_t 
 cudaError_t launch_tc_gemm(const TcArgs &a, const void *a_sorted, long cap_rows, int w13,
                            cudaStream_t st);
 
+cudaError_t launch_route(const void *logits, int bf16_in, int M, int E, int topk, int scoring,
+                         int renorm, int G, int TG, const float *bias, float scale, int32_t *ids,
+                         float *weights, cudaStream_t st);
 cudaError_t launch_finalize(const float *acc, long n, void *out_bf16, cudaStream_t stream,
                             bool dependent = false);
 cudaError_t launch_zero(float *buf, long n, cudaStream_t stream);

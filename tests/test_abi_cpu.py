@@ -35,7 +35,7 @@ def test_header_symbols_are_exported(moe):
     L = moe.lib()
     for name in declared:
         assert hasattr(L, name), name
-    assert moe.moe_abi_version() == 3
+    assert moe.moe_abi_version() == 4
 
 
 def test_status_strings(moe):
@@ -118,3 +118,18 @@ def test_packed_weight_sizes(moe):
     n = moe.make_problem(64, 4096, 1024, 2, 8, 8, "nvfp4", "nvfp4_dyn", "silu", "separated")
     n.a1_scale = n.a2_scale = 0x1000  # never dereferenced by a size query
     assert moe.moe_packed_weight_bytes(n, 1, "tc") == 8 * (4096 // 128) * (1024 // 64) * 4608
+
+
+def test_route_validation(moe):
+    L = moe.lib()
+    fake = ctypes.c_void_p(0x1000)
+    f1 = ctypes.c_float(1.0)
+    # topk > E, topk > 32, E > 1024, bad scoring, groups not dividing E, too few eligible
+    assert L.moe_route_topk(fake, 0, 4, 8, 9, 0, 1, 0, 0, None, f1, fake, fake, None) == 1
+    assert L.moe_route_topk(fake, 0, 4, 64, 33, 0, 1, 0, 0, None, f1, fake, fake, None) == 1
+    assert L.moe_route_topk(fake, 0, 4, 2048, 4, 0, 1, 0, 0, None, f1, fake, fake, None) == 1
+    assert L.moe_route_topk(fake, 0, 4, 64, 4, 2, 1, 0, 0, None, f1, fake, fake, None) == 1
+    assert L.moe_route_topk(fake, 0, 4, 60, 4, 0, 1, 8, 2, None, f1, fake, fake, None) == 1
+    assert L.moe_route_topk(fake, 0, 4, 64, 9, 0, 1, 8, 1, None, f1, fake, fake, None) == 1
+    assert L.moe_route_topk(None, 0, 4, 64, 4, 0, 1, 0, 0, None, f1, fake, fake, None) == 1
+    assert L.moe_route_topk(None, 0, 0, 64, 4, 0, 1, 0, 0, None, f1, None, None, None) == 0
