@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 4
+#define MOE_ABI_VERSION 5
 
 typedef enum {
   MOE_OK = 0,
@@ -115,6 +115,14 @@ typedef struct {
   float swiglu_limit;     /* g' = min(g, limit), u clamped to [-limit, limit]; 0 = no clamp */
   const float *a1_scale;  /* device: FP8_TENSOR_STATIC stage-1 scale [1]; NVFP4 stage-1 global [1] */
   const float *a2_scale;  /* device: FP8_TENSOR_STATIC stage-2 scale [1]; NVFP4 stage-2 global [E_l] */
+  /* apply_router_weight_on_input (doweight_stage1 of rocm_aiter_fused_experts;
+   * the tkw1 path of AiterFp8ChannelExperts "applies topk_weights to FC1's
+   * output instead of FC2's"): 1 = the router weight multiplies the stage-1
+   * output, z' = w * act(g, u), before the stage-2 quantiser, and the stage-2
+   * reduce is unweighted: out[t] = sum_k (W2 z'_k + b2).  Requires topk == 1
+   * (_assert_topk1_for_router_weight_on_input); honoured by moe_fused_experts
+   * (and _noalloc); the step entry points return MOE_ERR_UNSUPPORTED with it. */
+  int router_weight_on_input;
 } moe_problem_t;
 
 /* Library / ABI identification. */

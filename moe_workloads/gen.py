@@ -55,12 +55,14 @@ class Workload:
     swiglu_limit: float = 7.0
     recipe: str = ""
     router_logits: Optional[torch.Tensor] = None
+    router_weight_on_input: bool = False  # the router weight scales the stage-1 output
 
     def problem(self) -> dict:
         return dict(M=self.M, K=self.K, N=self.N, T=self.T, E=self.E, El=self.El,
                     wfmt=self.wfmt, afmt=self.afmt, act=self.act, gate=self.gate,
                     swiglu_alpha=self.swiglu_alpha, swiglu_beta=self.swiglu_beta,
-                    swiglu_limit=self.swiglu_limit)
+                    swiglu_limit=self.swiglu_limit,
+                    router_weight_on_input=self.router_weight_on_input)
 
     def weight_bytes(self, w: dict, experts=None) -> int:
         """Bytes of codes + scales + biases (+ globals) for the given experts."""

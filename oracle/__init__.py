@@ -223,7 +223,7 @@ class _Problem(ctypes.Structure):
                 ("afmt", ctypes.c_int), ("act", ctypes.c_int), ("gate", ctypes.c_int),
                 ("swiglu_alpha", ctypes.c_double), ("swiglu_beta", ctypes.c_double),
                 ("swiglu_limit", ctypes.c_double), ("a1_scale", ctypes.c_void_p),
-                ("a2_scale", ctypes.c_void_p)]
+                ("a2_scale", ctypes.c_void_p), ("weight_on_stage1", ctypes.c_int)]
 
 
 class _Weight(ctypes.Structure):
@@ -269,7 +269,8 @@ def fused_experts(prob: dict, x_bits, w13: dict, w2: dict, topk_ids, topk_weight
     P = _Problem(prob["M"], prob["K"], prob["N"], prob["T"], prob["E"], prob["El"],
                  WFMT[prob["wfmt"]], AFMT[prob["afmt"]], ACT[prob["act"]], GATE[prob["gate"]],
                  float(prob.get("swiglu_alpha", 1.702)), float(prob.get("swiglu_beta", 1.0)),
-                 float(prob.get("swiglu_limit", 7.0)), _ptr(a1), _ptr(a2))
+                 float(prob.get("swiglu_limit", 7.0)), _ptr(a1), _ptr(a2),
+                 int(bool(prob.get("router_weight_on_input", False))))
     W13 = _weight(w13, keep)
     W2 = _weight(w2, keep)
     out = np.zeros((len(tok), prob["K"]), np.float64)
@@ -277,6 +278,8 @@ def fused_experts(prob: dict, x_bits, w13: dict, w2: dict, topk_ids, topk_weight
                                  _ptr(ids), _ptr(tw), _ptr(em), _ptr(tok), len(tok), _ptr(out))
     if rc == -1:
         raise ValueError("oracle: per-tensor dynamic stage-2 needs every token")
+    if rc == -3:
+        raise ValueError("oracle: the router weight on the stage-1 output needs topk == 1")
     if rc != 0:
         raise ValueError("oracle: a scale the format needs is missing")
     return out

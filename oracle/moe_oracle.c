@@ -546,6 +546,7 @@ typedef struct {
   double swiglu_alpha, swiglu_beta, swiglu_limit;
   const float *a1_scale; /* fp8 tensor static: [1]; NVFP4: one global [1] */
   const float *a2_scale; /* fp8 tensor static: [1]; NVFP4: per expert [El] */
+  int weight_on_stage1;  /* apply_router_weight_on_input: w scales the stage-1 output */
 } orc_problem;
 
 /* Stage-2 (intermediate) quantiser implied by the weight / activation format. */
@@ -573,6 +574,8 @@ int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
   if ((p->afmt == ORC_A_FP8_TENSOR_STATIC || p->afmt == ORC_A_NVFP4_DYN) && !p->a1_scale) return -2;
   if ((s2 == ORC_A_FP8_TENSOR_STATIC || s2 == ORC_A_NVFP4_DYN) && !p->a2_scale) return -2;
   if (p->wfmt == ORC_W_NVFP4 && (!w13->global_scale || !w2->global_scale)) return -2;
+  /* apply_router_weight_on_input is defined for one slot per token */
+  if (p->weight_on_stage1 && T != 1) return -3;
 
   /* 1. stage-1 activations of the requested tokens (QDQ where quantised). */
   double *a = (double *)malloc(sizeof(double) * n_tokens * K);
@@ -645,6 +648,9 @@ int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
       if (p->gate == ORC_GATE_SEPARATED) { g = h[s * 2 * N + j]; u = h[s * 2 * N + N + j]; }
       else { g = h[s * 2 * N + 2 * j]; u = h[s * 2 * N + 2 * j + 1]; }
       z[s * N + j] = act_and_mul(p->act, g, u, p->swiglu_alpha, p->swiglu_beta, p->swiglu_limit);
+      /* doweight_stage1 / tkw1: the router weight scales the stage-1 output
+       * (before the stage-2 quantiser) instead of the stage-2 output */
+      if (p->weight_on_stage1) z[s * N + j] *= slot_w[s];
     }
   if (s2 != ORC_A_BF16 && ns > 0) {
     float *zf = (float *)malloc(sizeof(float) * ns * N);
@@ -678,7 +684,7 @@ int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
           const double *zv = z + s * N;
           double acc = 0.0;
           for (long j = 0; j < N; ++j) acc += zv[j] * row[j];
-          out[slot_tok[s] * K + i] += slot_w[s] * (acc + b);
+          out[slot_tok[s] * K + i] += (p->weight_on_stage1 ? 1.0 : slot_w[s]) * (acc + b);
         }
       }
       free(row);

@@ -50,7 +50,7 @@ class Problem(ctypes.Structure):
                 ("afmt", ctypes.c_int), ("act", ctypes.c_int), ("gate", ctypes.c_int),
                 ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
                 ("swiglu_limit", ctypes.c_float), ("a1_scale", ctypes.c_void_p),
-                ("a2_scale", ctypes.c_void_p)]
+                ("a2_scale", ctypes.c_void_p), ("router_weight_on_input", ctypes.c_int)]
 
 
 class Weight(ctypes.Structure):
@@ -125,9 +125,11 @@ def _check(fn, rc):
 
 
 def make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha=1.702,
-                 swiglu_beta=1.0, swiglu_limit=7.0, a1_scale=None, a2_scale=None) -> Problem:
+                 swiglu_beta=1.0, swiglu_limit=7.0, a1_scale=None, a2_scale=None,
+                 router_weight_on_input=False) -> Problem:
     return Problem(M, K, N, topk, E, El, WFMT[wfmt], AFMT[afmt], ACT[act], GATE[gate],
-                   swiglu_alpha, swiglu_beta, swiglu_limit, _ptr(a1_scale), _ptr(a2_scale))
+                   swiglu_alpha, swiglu_beta, swiglu_limit, _ptr(a1_scale), _ptr(a2_scale),
+                   int(bool(router_weight_on_input)))
 
 
 def make_weight(w: dict) -> Weight:
@@ -292,9 +294,10 @@ class FusedExperts:
 
     def __init__(self, M, K, N, topk, E, El, wfmt, afmt, act, gate, w13: dict, w2: dict,
                  a1_scale=None, a2_scale=None, swiglu_alpha=1.702, swiglu_beta=1.0,
-                 swiglu_limit=7.0, device="cuda", pack=True):
+                 swiglu_limit=7.0, device="cuda", pack=True, router_weight_on_input=False):
         self.prob = make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha,
-                                 swiglu_beta, swiglu_limit, a1_scale, a2_scale)
+                                 swiglu_beta, swiglu_limit, a1_scale, a2_scale,
+                                 router_weight_on_input)
         self._keep = (a1_scale, a2_scale)
         self.w13, self.w2 = dict(w13), dict(w2)
         # load-time repacks (weight-streaming decode kernels: MXFP4 with K, N
@@ -330,6 +333,7 @@ class FusedExperts:
 
     @classmethod
     def from_workload(cls, wl, **kw):
+        kw.setdefault("router_weight_on_input", wl.router_weight_on_input)
         return cls(wl.M, wl.K, wl.N, wl.T, wl.E, wl.El, wl.wfmt, wl.afmt, wl.act, wl.gate,
                    wl.w13, wl.w2, wl.a1_scale, wl.a2_scale, wl.swiglu_alpha, wl.swiglu_beta,
                    wl.swiglu_limit, device=wl.x.device, **kw)

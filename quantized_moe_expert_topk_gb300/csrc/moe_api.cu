@@ -84,6 +84,8 @@ int validate_problem(const moe_problem_t *p) {
     return MOE_ERR_INVALID_ARG;
   if (!pair_supported(p->wfmt, p->afmt)) return MOE_ERR_UNSUPPORTED;
   if (p->num_local_experts > 1024) return MOE_ERR_UNSUPPORTED;
+  // the router weight on the stage-1 output is defined for one slot per token
+  if (p->router_weight_on_input && p->topk != 1) return MOE_ERR_UNSUPPORTED;
   // 32-element reduction tiles (and the 32-element MXFP4 / 16-element NVFP4 groups)
   if (p->K % 32 != 0 || p->N % 32 != 0) return MOE_ERR_UNSUPPORTED;
   if ((long)p->M * p->topk > (1L << 30)) return MOE_ERR_UNSUPPORTED;
@@ -281,17 +283,19 @@ GemmArgs gemm_args(const moe_problem_t *p, int BM) {
   g.wfmt = p->wfmt; g.act = p->act; g.gate = p->gate;
   g.alpha = p->swiglu_alpha; g.beta = p->swiglu_beta; g.limit = p->swiglu_limit;
   g.S = p->M * p->topk;
+  g.w_stage1 = p->router_weight_on_input ? 1 : 0;
   return g;
 }
 
 // Stage-1 GEMM (+ requantisation).  `staging` is the fp32 scratch when the
 // intermediate is requantised.
 int run_w13(const moe_problem_t *p, const void *a_codes, const void *a_scales,
-            const moe_weight_t *w13, const int32_t *sorted, const int32_t *eids,
-            const int32_t *ntp, void *inter, void *inter_scales, void *staging, long cap,
-            cudaStream_t st) {
+            const moe_weight_t *w13, const float *topk_weights, const int32_t *sorted,
+            const int32_t *eids, const int32_t *ntp, void *inter, void *inter_scales,
+            void *staging, long cap, cudaStream_t st) {
   const int s2 = stage2_afmt(p);
   GemmArgs g = gemm_args(p, kGenericBlockM);
+  g.topk_weights = topk_weights;  // read only with the router weight on the stage-1 output
   g.afmt = p->afmt;
   g.a_codes = a_codes; g.a_scales = a_scales; g.a_global = p->a1_scale;
   g.w_codes = w13->codes; g.w_scales = w13->scales; g.w_global = w13->global_scale;
@@ -450,7 +454,7 @@ int moe_grouped_gemm_w13_act(const moe_problem_t *p, const void *a_codes, const 
                              void *stream) {
   int rc = validate_problem(p);
   if (rc != MOE_OK) return rc;
-  if (block_m != kGenericBlockM) return MOE_ERR_UNSUPPORTED;
+  if (block_m != kGenericBlockM || p->router_weight_on_input) return MOE_ERR_UNSUPPORTED;
   if ((rc = validate_weight(p, w13)) != MOE_OK) return rc;
   if (p->M == 0) return MOE_OK;
   if (!a_codes || !aligned16(a_codes) || !sorted_ids || !expert_ids || !num_post_pad || !inter ||
@@ -464,7 +468,7 @@ int moe_grouped_gemm_w13_act(const moe_problem_t *p, const void *a_codes, const 
       return MOE_ERR_WORKSPACE;
   }
   const long cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, block_m);
-  return run_w13(p, a_codes, a_scales, w13, sorted_ids, expert_ids, num_post_pad, inter,
+  return run_w13(p, a_codes, a_scales, w13, nullptr, sorted_ids, expert_ids, num_post_pad, inter,
                  inter_scales, workspace, cap, static_cast<cudaStream_t>(stream));
 }
 
@@ -475,7 +479,7 @@ int moe_grouped_gemm_w2_reduce(const moe_problem_t *p, const void *inter, const 
                                void *out_bf16, void *stream) {
   int rc = validate_problem(p);
   if (rc != MOE_OK) return rc;
-  if (block_m != kGenericBlockM) return MOE_ERR_UNSUPPORTED;
+  if (block_m != kGenericBlockM || p->router_weight_on_input) return MOE_ERR_UNSUPPORTED;
   if ((rc = validate_weight(p, w2)) != MOE_OK) return rc;
   if (p->M == 0) return MOE_OK;
   if (!inter || !aligned16(inter) || !topk_weights || !sorted_ids || !expert_ids ||
@@ -563,6 +567,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     sa.sorted_ids = sorted; sa.offsets = ex.offsets; sa.counts = counts;
     sa.active = ex.active; sa.n_active = ex.n_active;
     sa.err = dinfo.err;
+    sa.w_stage1 = p->router_weight_on_input ? 1 : 0;
     // 2. gate/up: x16 x packed w13 -> f16 intermediate (+ bias, x-scale, SwiGLU-OAI)
     StreamArgs s13 = sa;
     s13.C = p->K;
@@ -571,6 +576,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     s13.kblocks = p->K / 64;
     s13.packed = w13->packed; s13.bias = w13->bias;
     s13.x16 = ex.x16; s13.x_inv = ex.x_inv;
+    s13.topk_weights = topk_weights;  // read only with the router weight on the stage-1 output
     s13.out = ws + L.inter;
     s13.work_counter = ex.counters;
     {
@@ -620,7 +626,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     a_scales = ws + L.a1_scales;
   }
   // 3. gate/up GEMM + activation (+ requantisation)
-  if ((rc = run_w13(p, a_codes, a_scales, w13, sorted, eids, ntp, ws + L.inter,
+  if ((rc = run_w13(p, a_codes, a_scales, w13, topk_weights, sorted, eids, ntp, ws + L.inter,
                     ws + L.inter_scales, ws + L.staging, L.cap, st)) != MOE_OK)
     return rc;
   // 4. down GEMM + weighted reduce + bf16 output
@@ -808,6 +814,8 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
   base.alpha = p->swiglu_alpha; base.beta = p->swiglu_beta; base.limit = p->swiglu_limit;
   base.sorted_ids = sorted; base.expert_ids = eids; base.num_post_pad = ntp; base.S = S;
   base.err = dinfo.err;
+  base.w_stage1 = p->router_weight_on_input ? 1 : 0;
+  base.topk_weights = topk_weights;
   // 4. gate/up GEMM + activation
   {
     TcArgs a = base;

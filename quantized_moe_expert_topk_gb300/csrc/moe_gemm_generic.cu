@@ -341,6 +341,8 @@ __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs a) {
       for (int h = 0; h < 2; ++h) {
         const long r = (long)blk * BM + wm * 32 + mi * 16 + (lane >> 2) + h * 8;
         const float rf = row_factor(mi, h);
+        // router weight on the stage-1 output (apply_router_weight_on_input)
+        const float zw = (a.w_stage1 && row_live[mi][h]) ? a.topk_weights[a.sorted_ids[r]] : 1.f;
 #pragma unroll
         for (int ni = 0; ni < 2; ++ni) {
           float z[2];
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs a) {
             const long wg = col_wrow[ni][c], wu = col_wrow[ni + 2][c];
             const float g = acc[mi][ni][h * 2 + c] * rf * col_factor(wg) + col_bias(wg);
             const float u = acc[mi][ni + 2][h * 2 + c] * rf * col_factor(wu) + col_bias(wu);
-            z[c] = row_live[mi][h] ? act_and_mul(a.act, g, u, a.alpha, a.beta, a.limit) : 0.f;
+            z[c] = row_live[mi][h] ? zw * act_and_mul(a.act, g, u, a.alpha, a.beta, a.limit) : 0.f;
           }
           const int j = nt * 64 + wn * 16 + ni * 8 + (lane & 3) * 2;
           if (j < a.N) {  // N is a multiple of 32, so j + 1 < N as well
@@ -372,7 +374,7 @@ __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs a) {
         const long r = (long)blk * BM + wm * 32 + mi * 16 + (lane >> 2) + h * 8;
         const int s = a.sorted_ids[r];
         const long t = s / a.T;
-        const float wt = a.topk_weights[s];
+        const float wt = a.w_stage1 ? 1.f : a.topk_weights[s];
         const float rf = row_factor(mi, h);
 #pragma unroll
         for (int ni = 0; ni < 4; ++ni)

@@ -105,6 +105,7 @@ struct GemmArgs {
   int out_f32;
   float *acc;       // W2: fp32 [M, K] accumulator
   const float *topk_weights;
+  int w_stage1;     // router weight on the stage-1 output (W13 multiplies, W2 does not)
 };
 cudaError_t launch_gemm_w13(const GemmArgs &a, long cap_rows, cudaStream_t stream);
 cudaError_t launch_gemm_w2(const GemmArgs &a, long cap_rows, cudaStream_t stream);
@@ -122,6 +123,7 @@ struct StreamArgs {
   void *out;                      // w13: f16 intermediate [cap, N]
   float *acc;                     // w2: fp32 [M, K]
   const float *topk_weights;
+  int w_stage1;                   // router weight on the stage-1 output (W13 multiplies, W2 not)
   int *err;                       // device error word
   int *work_counter;              // zero at launch; units are claimed from it
 };
@@ -154,6 +156,7 @@ struct TcArgs {
   float *acc;
   const float *topk_weights;
   int *err;
+  int w_stage1;          // router weight on the stage-1 output (W13 multiplies, W2 not)
   const void *w_packed;  // FP4 formats: load-time packed records
   int ntiles;            // set by the launcher
   int rec_bytes;         // set by the launcher

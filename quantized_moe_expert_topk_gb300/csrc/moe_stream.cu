@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
   float acc[MT][2][4];
   int tok_sid[2][2] = {{0, 0}, {0, 0}};      // sorted slot ids of this thread's tokens
   float tok_f[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // W13: x_inv of the token; W2: router weight
+  float tok_zw[2][2] = {{1.f, 1.f}, {1.f, 1.f}};  // W13: factor of the stage-1 output
   while (true) {
     const int slot = it % NS;
     if (!mbar_wait_bounded(&sm.full[slot], (it / NS) & 1, kWaitCycles, a.err)) {
@@ -329,9 +330,13 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int tn = n * 8 + 2 * t + c;
+          // W13: x_inv of the token (times the router weight when it applies to
+          // the stage-1 output); W2: the router weight (1 in that case)
+          const float wr = a.w_stage1 ? (MODE == MODE_W13 ? a.topk_weights[tok_sid[n][c]] : 1.f)
+                                      : (MODE == MODE_W13 ? 1.f : a.topk_weights[tok_sid[n][c]]);
           tok_f[n][c] = tn >= nt ? 0.f
-                        : MODE == MODE_W13 ? a.x_inv[tok_sid[n][c] / a.T]
-                                           : a.topk_weights[tok_sid[n][c]];
+                        : MODE == MODE_W13 ? a.x_inv[tok_sid[n][c] / a.T] : wr;
+          tok_zw[n][c] = MODE == MODE_W13 && tn < nt ? wr : 1.f;
         }
     }
     const int nkb = min(S_KB, U.nkb - d.kb);
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
             const float xi = tok_f[n][c];
             const float gv = acc[m][n][c] * xi + bg;
             const float uv = acc[m][n][2 + c] * xi + bu;
-            const float z = act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit);
+            const float z = tok_zw[n][c] * act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit);
             static_cast<__half *>(a.out)[(long)r * N + j] = __float2half_rn(z);
           }
       }

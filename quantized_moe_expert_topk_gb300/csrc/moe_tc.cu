@@ -382,6 +382,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                           : bf16_to_f32(static_cast<const uint16_t *>(a.w_bias)[i]);
       };
       if (MODE == MODE_W13) {
+        // router weight on the stage-1 output (apply_router_weight_on_input)
+        const float zw = (a.w_stage1 && live) ? a.topk_weights[s_id] : 1.f;
         const int jbase = nt * 64 + 32 * h;
         if (jbase < a.N) {  // N % 32 == 0: the 32 outputs are all in range or none
           const bool sep = a.gate == GATE_SEPARATED;
@@ -398,7 +400,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               const long urow = sep ? a.N + j : 2 * j + 1;
               const float gv = gacc * rf * col_factor(grow) + bias_of(grow);
               const float uv = uacc * rf * col_factor(urow) + bias_of(urow);
-              z[i] = live ? act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit) : 0.f;
+              z[i] = live ? zw * act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit) : 0.f;
             }
             if (a.out_f32) {
               float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + r * a.N + jbase + 16 * p);
@@ -418,7 +420,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       } else if (live) {
         const long t = s_id / a.T;
-        const float wt = a.topk_weights[s_id];
+        const float wt = a.w_stage1 ? 1.f : a.topk_weights[s_id];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const long i0 = (long)nt * BN + 64 * h + 32 * cc;

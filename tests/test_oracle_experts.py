@@ -194,6 +194,38 @@ def test_expert_parallel_partition_sum():
     np.testing.assert_allclose(acc, full, rtol=1e-12, atol=1e-14)
 
 
+@pytest.mark.parametrize("wfmt", ["bf16", "mxfp4"])
+def test_router_weight_on_stage1_output_closed_form(wfmt):
+    # apply_router_weight_on_input (top-1): the weight scales the stage-1 output
+    # and the stage-2 reduce is unweighted; without a stage-2 quantiser the layer
+    # is linear in z, so out_stage1 - out_standard = (1 - w) * b2 per token
+    wl = make_custom(M=9, K=64, N=64, E=4, T=1, wfmt=wfmt, act="swiglu_oai",
+                     gate="interleaved", bias=True, seed=17, renorm=False)
+    h = to_host(wl)
+    std = oracle.fused_experts(h["problem"], h["x"], h["w13"], h["w2"], h["topk_ids"],
+                               h["topk_weights"])
+    st1 = oracle.fused_experts(dict(h["problem"], router_weight_on_input=True), h["x"], h["w13"],
+                               h["w2"], h["topk_ids"], h["topk_weights"])
+    w = h["topk_weights"][:, 0].astype(np.float64)
+    assert (w < 0.999).all()  # the difference is visible
+    b2 = oracle.bf16_values(h["w2"]["bias"])[h["topk_ids"][:, 0]]
+    np.testing.assert_allclose(st1 - std, (1.0 - w)[:, None] * b2, rtol=1e-9, atol=1e-12)
+    # without biases the two placements give the same layer
+    w2nb = {k: v for k, v in h["w2"].items() if k != "bias"}
+    a = oracle.fused_experts(h["problem"], h["x"], h["w13"], w2nb, h["topk_ids"], h["topk_weights"])
+    b = oracle.fused_experts(dict(h["problem"], router_weight_on_input=True), h["x"], h["w13"],
+                             w2nb, h["topk_ids"], h["topk_weights"])
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+def test_router_weight_on_stage1_needs_top1():
+    wl = make_custom(M=4, K=64, N=32, E=4, T=2, seed=5)
+    h = to_host(wl)
+    with pytest.raises(ValueError):
+        oracle.fused_experts(dict(h["problem"], router_weight_on_input=True), h["x"], h["w13"],
+                             h["w2"], h["topk_ids"], h["topk_weights"])
+
+
 # ---- per-format single-expert hand examples (K = N = 32, power-of-two scales)
 
 def decode_e4m3(codes):
