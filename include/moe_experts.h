@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 5
+#define MOE_ABI_VERSION 6
 
 typedef enum {
   MOE_OK = 0,
@@ -123,6 +123,14 @@ typedef struct {
    * (_assert_topk1_for_router_weight_on_input); honoured by moe_fused_experts
    * (and _noalloc); the step entry points return MOE_ERR_UNSUPPORTED with it. */
   int router_weight_on_input;
+  /* num_local_tokens of rocm_aiter_fused_experts (AiterExperts.apply passes
+   * expert_tokens_meta.expert_num_tokens there): device int32 [1] holding the
+   * number n of valid tokens; only rows t < n of hidden_states / topk_ids take
+   * part, rows t >= n of the output are written as zeros (a padded dispatch
+   * buffer whose fill level is known on the device only; CUDA-graph friendly).
+   * NULL = all M tokens.  Read by moe_fused_experts (and _noalloc); not with
+   * MOE_A_FP8_TENSOR_DYN (its batch scale would cover the padding rows). */
+  const int32_t *num_local_tokens;
 } moe_problem_t;
 
 /* Library / ABI identification. */

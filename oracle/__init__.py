@@ -223,7 +223,8 @@ class _Problem(ctypes.Structure):
                 ("afmt", ctypes.c_int), ("act", ctypes.c_int), ("gate", ctypes.c_int),
                 ("swiglu_alpha", ctypes.c_double), ("swiglu_beta", ctypes.c_double),
                 ("swiglu_limit", ctypes.c_double), ("a1_scale", ctypes.c_void_p),
-                ("a2_scale", ctypes.c_void_p), ("weight_on_stage1", ctypes.c_int)]
+                ("a2_scale", ctypes.c_void_p), ("weight_on_stage1", ctypes.c_int),
+                ("n_valid_tokens", ctypes.c_int)]
 
 
 class _Weight(ctypes.Structure):
@@ -270,7 +271,8 @@ def fused_experts(prob: dict, x_bits, w13: dict, w2: dict, topk_ids, topk_weight
                  WFMT[prob["wfmt"]], AFMT[prob["afmt"]], ACT[prob["act"]], GATE[prob["gate"]],
                  float(prob.get("swiglu_alpha", 1.702)), float(prob.get("swiglu_beta", 1.0)),
                  float(prob.get("swiglu_limit", 7.0)), _ptr(a1), _ptr(a2),
-                 int(bool(prob.get("router_weight_on_input", False))))
+                 int(bool(prob.get("router_weight_on_input", False))),
+                 -1 if prob.get("num_local_tokens") is None else int(prob["num_local_tokens"]))
     W13 = _weight(w13, keep)
     W2 = _weight(w2, keep)
     out = np.zeros((len(tok), prob["K"]), np.float64)

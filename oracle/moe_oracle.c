@@ -547,6 +547,7 @@ typedef struct {
   const float *a1_scale; /* fp8 tensor static: [1]; NVFP4: one global [1] */
   const float *a2_scale; /* fp8 tensor static: [1]; NVFP4: per expert [El] */
   int weight_on_stage1;  /* apply_router_weight_on_input: w scales the stage-1 output */
+  int n_valid_tokens;    /* num_local_tokens: tokens t >= it take no part; -1 = all */
 } orc_problem;
 
 /* Stage-2 (intermediate) quantiser implied by the weight / activation format. */
@@ -607,6 +608,7 @@ int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
   for (long i = 0; i < n_tokens; ++i)
     for (long k = 0; k < T; ++k) {
       long t = tokens[i];
+      if (p->n_valid_tokens >= 0 && t >= p->n_valid_tokens) continue;  /* padding row */
       int l = local_expert(topk_ids[t * T + k], expert_map, p->E, p->El);
       if (l < 0) continue;
       slot_tok[ns] = i;

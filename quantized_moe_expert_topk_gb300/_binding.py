@@ -50,7 +50,8 @@ class Problem(ctypes.Structure):
                 ("afmt", ctypes.c_int), ("act", ctypes.c_int), ("gate", ctypes.c_int),
                 ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
                 ("swiglu_limit", ctypes.c_float), ("a1_scale", ctypes.c_void_p),
-                ("a2_scale", ctypes.c_void_p), ("router_weight_on_input", ctypes.c_int)]
+                ("a2_scale", ctypes.c_void_p), ("router_weight_on_input", ctypes.c_int),
+                ("num_local_tokens", ctypes.c_void_p)]
 
 
 class Weight(ctypes.Structure):
@@ -126,10 +127,12 @@ def _check(fn, rc):
 
 def make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha=1.702,
                  swiglu_beta=1.0, swiglu_limit=7.0, a1_scale=None, a2_scale=None,
-                 router_weight_on_input=False) -> Problem:
+                 router_weight_on_input=False, num_local_tokens=None) -> Problem:
+    """num_local_tokens: optional device int32 [1] tensor, the number of valid
+    tokens (read on the device at every call)."""
     return Problem(M, K, N, topk, E, El, WFMT[wfmt], AFMT[afmt], ACT[act], GATE[gate],
                    swiglu_alpha, swiglu_beta, swiglu_limit, _ptr(a1_scale), _ptr(a2_scale),
-                   int(bool(router_weight_on_input)))
+                   int(bool(router_weight_on_input)), _ptr(num_local_tokens))
 
 
 def make_weight(w: dict) -> Weight:
@@ -294,11 +297,12 @@ class FusedExperts:
 
     def __init__(self, M, K, N, topk, E, El, wfmt, afmt, act, gate, w13: dict, w2: dict,
                  a1_scale=None, a2_scale=None, swiglu_alpha=1.702, swiglu_beta=1.0,
-                 swiglu_limit=7.0, device="cuda", pack=True, router_weight_on_input=False):
+                 swiglu_limit=7.0, device="cuda", pack=True, router_weight_on_input=False,
+                 num_local_tokens=None):
         self.prob = make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha,
                                  swiglu_beta, swiglu_limit, a1_scale, a2_scale,
-                                 router_weight_on_input)
-        self._keep = (a1_scale, a2_scale)
+                                 router_weight_on_input, num_local_tokens)
+        self._keep = (a1_scale, a2_scale, num_local_tokens)
         self.w13, self.w2 = dict(w13), dict(w2)
         # load-time repacks (weight-streaming decode kernels: MXFP4 with K, N
         # multiples of 64; tcgen05 kernels: MXFP4 / NVFP4); the C library

@@ -31,7 +31,8 @@ constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
 
 __device__ __forceinline__ int local_of(const int32_t *ids, const int32_t *emap, long s, int E,
-                                        int El) {
+                                        int El, long s_valid) {
+  if (s >= s_valid) return -1;  // a token beyond the valid count (padded dispatch buffer)
   int g = ids[s];
   if (g < 0 || g >= E) return -1;
   int l = emap ? emap[g] : g;
@@ -136,6 +137,13 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
     }
     return;
   }
+  // slots of tokens at or beyond the valid count (when given) are dropped
+  long s_valid = S;
+  if (x.num_valid_tokens) {
+    const long n = *x.num_valid_tokens;
+    const long T = x.slots_per_token;
+    s_valid = n <= 0 ? 0 : (n * T < S ? n * T : S);
+  }
   extern __shared__ int smem[];
   int *cnt = smem;                     // [kAlignWarps][El]  per-warp counts -> prefixes
   int *off = smem + kAlignWarps * El;  // [El + 1]           expert offsets
@@ -153,7 +161,7 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
   // A. per-warp histogram
   for (long base = beg; base < end; base += 32) {
     const long s = base + lane;
-    const int l = s < end ? local_of(ids, emap, s, E, El) : -1;
+    const int l = s < end ? local_of(ids, emap, s, E, El, s_valid) : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, l);
     if (l >= 0 && lane == __ffs(peers) - 1) cnt[warp * El + l] += __popc(peers);
   }
@@ -219,7 +227,7 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
   // C. stable scatter
   for (long base = beg; base < end; base += 32) {
     const long s = base + lane;
-    const int l = s < end ? local_of(ids, emap, s, E, El) : -1;
+    const int l = s < end ? local_of(ids, emap, s, E, El, s_valid) : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, l);
     int pos = 0;
     if (l >= 0) pos = cnt[warp * El + l] + __popc(peers & lt_mask);
@@ -252,7 +260,9 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
 cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *expert_map, int E,
                          int El, int BM, int32_t *sorted_ids, int32_t *expert_ids,
                          int32_t *num_post_pad, int32_t *counts, long cap,
-                         const AlignExtras &extra, cudaStream_t stream) {
+                         const AlignExtras &extra_in, cudaStream_t stream) {
+  AlignExtras extra = extra_in;
+  extra.slots_per_token = T;
   const size_t smem = sizeof(int) * ((size_t)kAlignWarps * El + 2 * (size_t)El + 1);
   if (smem > 48 * 1024) {
     // opt in once to the largest size this kernel can ask for (El = 1024), so

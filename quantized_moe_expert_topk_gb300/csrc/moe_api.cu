@@ -86,6 +86,8 @@ int validate_problem(const moe_problem_t *p) {
   if (p->num_local_experts > 1024) return MOE_ERR_UNSUPPORTED;
   // the router weight on the stage-1 output is defined for one slot per token
   if (p->router_weight_on_input && p->topk != 1) return MOE_ERR_UNSUPPORTED;
+  // a per-tensor dynamic scale would span the padding rows beyond the valid tokens
+  if (p->num_local_tokens && p->afmt == A_FP8_TENSOR_DYN) return MOE_ERR_UNSUPPORTED;
   // 32-element reduction tiles (and the 32-element MXFP4 / 16-element NVFP4 groups)
   if (p->K % 32 != 0 || p->N % 32 != 0) return MOE_ERR_UNSUPPORTED;
   if ((long)p->M * p->topk > (1L << 30)) return MOE_ERR_UNSUPPORTED;
@@ -548,6 +550,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     ex.xM = p->M;
     ex.xK = p->K;
   }
+  ex.num_valid_tokens = p->num_local_tokens;
   std::lock_guard<std::mutex> timing_lock(g_timing_mu);
   {
     StageScope sc(MOE_STAGE_ALIGN, st);
@@ -771,6 +774,7 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     AlignExtras ex;
     ex.zero_buf = acc;
     ex.zero_n = MK;
+    ex.num_valid_tokens = p->num_local_tokens;
     StageScope sc(MOE_STAGE_ALIGN, st);
     rc = cuda_status(launch_align(topk_ids, p->M, p->topk, expert_map, p->num_experts,
                                   p->num_local_experts, kTcBlockM, sorted, eids, ntp, counts,

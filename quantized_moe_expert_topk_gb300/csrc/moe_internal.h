@@ -48,6 +48,8 @@ struct AlignExtras {
   void *x16 = nullptr;            //   max |x16| in [2^14, 2^15); x_inv[row] = 2^-a
   float *x_inv = nullptr;
   int xM = 0, xK = 0;
+  const int32_t *num_valid_tokens = nullptr;  // [1]: slots of tokens >= it are dropped
+  int slots_per_token = 1;                     // topk (set by launch_align)
 };
 
 cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *expert_map, int E,

@@ -226,6 +226,22 @@ def test_router_weight_on_stage1_needs_top1():
                              h["w2"], h["topk_ids"], h["topk_weights"])
 
 
+@pytest.mark.parametrize("n", [0, 1, 7, 12])
+def test_num_local_tokens_equals_the_leading_sub_batch(n):
+    # only tokens t < n take part: their rows equal the layer evaluated on the
+    # first n tokens alone (inputs sliced), the other rows are zero
+    wl = make_custom(M=12, K=64, N=32, E=4, T=2, wfmt="fp8_block128", afmt="fp8_group128_dyn",
+                     act="silu", bias=True, seed=12)
+    h = to_host(wl)
+    out = oracle.fused_experts(dict(h["problem"], num_local_tokens=n), h["x"], h["w13"], h["w2"],
+                               h["topk_ids"], h["topk_weights"])
+    assert (out[n:] == 0).all()
+    if n:
+        sub = oracle.fused_experts(dict(h["problem"], M=n), h["x"][:n], h["w13"], h["w2"],
+                                   h["topk_ids"][:n], h["topk_weights"][:n])
+        np.testing.assert_array_equal(out[:n], sub)
+
+
 # ---- per-format single-expert hand examples (K = N = 32, power-of-two scales)
 
 def decode_e4m3(codes):
