@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
       const int N = a.N;
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        const int j = U.u * 64 + (warp * MT + m) * 8 + g;
+        const int j = U.u * (TILES * 8) + (warp * MT + m) * 8 + g;
         const long grow = a.gate == GATE_SEPARATED ? j : 2L * j;
         const long urow = a.gate == GATE_SEPARATED ? (long)N + j : 2L * j + 1;
         float bg = 0.f, bu = 0.f;
@@ -448,7 +448,7 @@ __global__ void pack_mxfp4_kernel(PackArgs p) {
   }
   long row = -1;
   if (p.w13) {
-    const int j = u * 64 + m * 8 + (r16 & 7);
+    const int j = u * (TILES * 8) + m * 8 + (r16 & 7);
     const int up = r16 >= 8;
     if (j < p.N) row = p.gate == GATE_SEPARATED ? (up ? (long)p.N + j : j) : 2L * j + up;
   } else {
@@ -467,7 +467,7 @@ __global__ void pack_mxfp4_kernel(PackArgs p) {
 }  // namespace
 
 size_t stream_packed_bytes(int w13, int N, int K, int El) {
-  const int units = w13 ? N / 64 : (int)ceil_div(K, ROWS);
+  const int units = w13 ? N / (TILES * 8) : (int)ceil_div(K, ROWS);
   const int C = w13 ? K : N;
   const int kblocks = (int)ceil_div(C, 64);
   return (size_t)El * units * kblocks * REC_BYTES;
@@ -479,7 +479,9 @@ cudaError_t launch_pack_mxfp4(const PackArgs &p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-int stream_units_per_expert(int w13, int N, int K) { return w13 ? N / 64 : (int)ceil_div(K, ROWS); }
+int stream_units_per_expert(int w13, int N, int K) {
+  return w13 ? N / (TILES * 8) : (int)ceil_div(K, ROWS);
+}
 
 cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream_t stream) {
   auto kern = w13 ? stream_kernel<MODE_W13> : stream_kernel<MODE_W2>;
