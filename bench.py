@@ -284,7 +284,16 @@ def launches_per_step(wl, routing=False):
     n += wl.afmt != "bf16"                 # stage-1 activation quantiser
     n += path == "tc"                      # gather of the sorted activation rows
     n += 1                                 # w13 GEMM + activation
-    n += s2 != "bf16" or (path == "tc" and wl.wfmt == "mxfp4")  # requantiser / f16 rescale
+    if path == "tc":
+        # the tcgen05 W13 epilogue quantises NVFP4 itself and writes a bounded
+        # SwiGLU-OAI intermediate as f16; fp8 needs a requantiser, other MXFP4
+        # intermediates a per-row f16 rescale
+        mx_direct = (wl.wfmt == "mxfp4" and s2 == "bf16" and wl.act == "swiglu_oai"
+                     and 0 < wl.swiglu_limit <= 64 and abs(wl.swiglu_beta) <= 64
+                     and not wl.router_weight_on_input)
+        n += s2 not in ("bf16", "nvfp4_dyn") or (wl.wfmt == "mxfp4" and not mx_direct)
+    else:
+        n += s2 != "bf16"                  # stage-2 requantiser
     n += 2                                 # w2 GEMM + reduce, bf16 finalize
     return n
 

@@ -819,6 +819,11 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
   base.sorted_ids = sorted; base.expert_ids = eids; base.num_post_pad = ntp; base.S = S;
   base.err = dinfo.err;
   base.w_stage1 = p->router_weight_on_input ? 1 : 0;
+  // MXFP4 w4a16 with SwiGLU-OAI: |z| <= limit * (limit + |beta|) <= 8192 fits f16
+  // as it is (no per-row rescale pass); the router weight could scale it further
+  const bool mx_direct = p->wfmt == W_MXFP4 && s2 == A_BF16 && p->act == ACT_SWIGLU_OAI &&
+                         p->swiglu_limit > 0.f && p->swiglu_limit <= 64.f &&
+                         fabsf(p->swiglu_beta) <= 64.f && !p->router_weight_on_input;
   base.topk_weights = topk_weights;
   // 4. gate/up GEMM + activation
   {
@@ -839,15 +844,26 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     }
     a.w_codes = w13->codes; a.w_scales = w13->scales; a.w_global = w13->global_scale;
     a.w_bias = w13->bias; a.bias_f32 = w13->bias_is_f32; a.w_packed = w13->packed_tc;
-    const bool to_staging = s2 != A_BF16 || p->wfmt == W_MXFP4;
-    a.out = to_staging ? (void *)(ws + L.staging) : (void *)(ws + L.inter);
-    a.out_f32 = to_staging;
+    if (s2 == A_NVFP4_DYN) {        // stage-2 quantisation inside the epilogue
+      a.out = ws + L.inter;
+      a.out_mode = TC_OUT_NVFP4_F16;
+      a.out_global = p->a2_scale;
+    } else if (mx_direct) {         // bounded SwiGLU-OAI intermediate straight to f16
+      a.out = ws + L.inter;
+      a.out_mode = TC_OUT_F16;
+    } else if (s2 != A_BF16 || p->wfmt == W_MXFP4) {
+      a.out = ws + L.staging;       // fp32 staging, then a requantiser / row rescale
+      a.out_mode = TC_OUT_F32;
+    } else {
+      a.out = ws + L.inter;
+      a.out_mode = TC_OUT_BF16;
+    }
     StageScope sc(MOE_STAGE_W13, st);
     rc = cuda_status(launch_tc_gemm(a, ws + L.a_sorted, L.cap, 1, st));
     sc.done();
     if (rc != MOE_OK) return rc;
   }
-  if (s2 == A_BF16 && p->wfmt == W_MXFP4) {  // f16 intermediate with row scales
+  if (s2 == A_BF16 && p->wfmt == W_MXFP4 && !mx_direct) {  // f16 intermediate with row scales
     StageScope sc(MOE_STAGE_REQUANT, st);
     rc = cuda_status(launch_rescale_rows(reinterpret_cast<const float *>(ws + L.staging), L.cap,
                                          p->N, sorted, ntp, S, ws + L.inter,
@@ -855,8 +871,9 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     sc.done();
     if (rc != MOE_OK) return rc;
   }
-  // 5. stage-2 requantisation into exact bf16 values + scales (sorted rows)
-  if (s2 != A_BF16) {
+  // 5. stage-2 requantisation into exact bf16 values + scales (sorted rows);
+  //    NVFP4 was quantised in the W13 epilogue
+  if (s2 != A_BF16 && s2 != A_NVFP4_DYN) {
     QuantArgs q;
     memset(&q, 0, sizeof(q));
     q.x = ws + L.staging; q.x_is_f32 = 1; q.rows = L.cap; q.cols = p->N; q.afmt = s2;
@@ -888,7 +905,8 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
         break;
       case A_NVFP4_DYN: a.a_expertscale = p->a2_scale; break;
       default:
-        if (p->wfmt == W_MXFP4) a.a_rowscale = reinterpret_cast<const float *>(ws + L.i_scales);
+        if (p->wfmt == W_MXFP4 && !mx_direct)
+          a.a_rowscale = reinterpret_cast<const float *>(ws + L.i_scales);
         break;
     }
     a.w_codes = w2->codes; a.w_scales = w2->scales; a.w_global = w2->global_scale;

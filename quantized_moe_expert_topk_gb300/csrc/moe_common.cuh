@@ -14,6 +14,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -86,6 +87,45 @@ __device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
 // fp8 dynamic scale of a group: fl32(max(amax, 1e-12) / 448), IEEE divide.
 __device__ __forceinline__ float fp8_group_scale(float amax) {
   return __fdiv_rn(fmaxf(amax, kScaleFloor), kFp8Max);
+}
+
+// NVFP4 x16 quantiser of one group of 16 fp32 values (the decision rule of
+// QuarkNvfp4MoEMethod's dynamic activations): s = e4m3(fl32(fl32(amax/6)/gs)),
+// code = e2m1(fl32(v / fl32(e4m3(s) * gs))), zero codes when s decodes to 0.
+// Returns s; lo / hi hold the 16 codes (element 2i in the low nibble).
+__device__ __forceinline__ uint32_t nvfp4_quant16(const float (&v)[16], float gs, uint32_t &lo,
+                                                  uint32_t &hi) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const uint32_t s = f32_to_e4m3(__fdiv_rn(__fdiv_rn(amax, kE2m1Max), gs));
+  const float sv = e4m3_to_f32(s);
+  lo = hi = 0;
+  if (sv != 0.f) {
+    const float denom = __fmul_rn(sv, gs);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2)
+      lo |= f32x2_to_e2m1x2(__fdiv_rn(v[i], denom), __fdiv_rn(v[i + 1], denom)) << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2)
+      hi |= f32x2_to_e2m1x2(__fdiv_rn(v[8 + i], denom), __fdiv_rn(v[9 + i], denom)) << (4 * i);
+  }
+  return s;
+}
+
+// Element pair (byte i of the 8 code bytes) of a quantised NVFP4 group as the
+// exact product e2m1(code) * e4m3(s) (f16 when to_f16, else bf16); the global
+// scale stays with the consumer.
+__device__ __forceinline__ uint32_t nvfp4_decode_pair(uint32_t lo, uint32_t hi, int i, float sv,
+                                                      bool to_f16) {
+  const uint32_t byte = i < 4 ? (lo >> (8 * i)) & 0xff : (hi >> (8 * (i - 4))) & 0xff;
+  const float x0 = e2m1_to_f32(byte & 15) * sv, x1 = e2m1_to_f32(byte >> 4) * sv;
+  if (to_f16) {
+    const __half2 h2 = __floats2half2_rn(x0, x1);
+    return *reinterpret_cast<const uint32_t *>(&h2);
+  }
+  const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+  return *reinterpret_cast<const uint32_t *>(&h2);
 }
 
 // ---------------------------------------------------------------- activations

@@ -141,6 +141,11 @@ cudaError_t launch_pack_mxfp4(const PackArgs &p, cudaStream_t stream);
 cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream_t stream);
 
 // tcgen05 grouped GEMMs (moe_tc.cu)
+// Output of the tcgen05 W13 epilogue: bf16 rows, fp32 staging rows (a
+// separate requantiser follows), f16 rows (bounded SwiGLU-OAI intermediate),
+// or the stage-2 NVFP4 quantisation done in the epilogue, written as the exact
+// f16 values e2m1(code) * e4m3(scale) the W2 kernel consumes.
+enum { TC_OUT_BF16 = 0, TC_OUT_F32 = 1, TC_OUT_F16 = 2, TC_OUT_NVFP4_F16 = 3 };
 struct TcArgs {
   int M, K, N, T, El, R, C;
   int wfmt, act, gate;
@@ -154,7 +159,8 @@ struct TcArgs {
   const int32_t *sorted_ids, *expert_ids, *num_post_pad;
   int S;
   void *out;
-  int out_f32;
+  int out_mode;          // W13 output: TC_OUT_BF16 / _F32 (staging) / _F16 / _NVFP4_F16
+  const float *out_global;  // TC_OUT_NVFP4_F16: the stage-2 global per expert [El]
   float *acc;
   const float *topk_weights;
   int *err;

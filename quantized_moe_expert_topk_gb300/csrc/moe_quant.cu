@@ -169,39 +169,16 @@ __global__ void quant_nvfp4(QuantArgs a) {
   const float gs = a.sorted_ids ? a.param[a.expert_ids[r / a.BM]] : a.param[0];
   const InT *x = static_cast<const InT *>(a.x) + r * a.cols + g * 16;
   float v[16];
-  float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    v[i] = load_elem<InT>(x, i);
-    amax = fmaxf(amax, fabsf(v[i]));
-  }
-  const uint32_t s = f32_to_e4m3(__fdiv_rn(__fdiv_rn(amax, kE2m1Max), gs));
-  const float sv = e4m3_to_f32(s);
-  uint32_t lo = 0, hi = 0;
-  if (sv != 0.f) {
-    const float denom = __fmul_rn(sv, gs);
-#pragma unroll
-    for (int i = 0; i < 8; i += 2)
-      lo |= f32x2_to_e2m1x2(__fdiv_rn(v[i], denom), __fdiv_rn(v[i + 1], denom)) << (4 * i);
-#pragma unroll
-    for (int i = 0; i < 8; i += 2)
-      hi |= f32x2_to_e2m1x2(__fdiv_rn(v[8 + i], denom), __fdiv_rn(v[9 + i], denom)) << (4 * i);
-  }
+  for (int i = 0; i < 16; ++i) v[i] = load_elem<InT>(x, i);
+  uint32_t lo, hi;
+  const uint32_t s = nvfp4_quant16(v, gs, lo, hi);
   if (dec) {
-    // exact bf16 of e2m1(code) * e4m3(s); the global g is applied by the consumer
+    // exact bf16 / f16 of e2m1(code) * e4m3(s); the global g is applied by the consumer
+    const float sv = e4m3_to_f32(s);
     uint32_t w[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t byte = i < 4 ? (lo >> (8 * i)) & 0xff : (hi >> (8 * (i - 4))) & 0xff;
-      const float x0 = e2m1_to_f32(byte & 15) * sv, x1 = e2m1_to_f32(byte >> 4) * sv;
-      if (a.decoded_f16) {
-        const __half2 h2 = __floats2half2_rn(x0, x1);
-        w[i] = *reinterpret_cast<const uint32_t *>(&h2);
-      } else {
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-        w[i] = *reinterpret_cast<const uint32_t *>(&h2);
-      }
-    }
+    for (int i = 0; i < 8; ++i) w[i] = nvfp4_decode_pair(lo, hi, i, sv, a.decoded_f16 != 0);
     dec[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dec[1] = make_uint4(w[4], w[5], w[6], w[7]);
   } else {

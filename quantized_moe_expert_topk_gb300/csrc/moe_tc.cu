@@ -402,11 +402,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               const float uv = uacc * rf * col_factor(urow) + bias_of(urow);
               z[i] = live ? zw * act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit) : 0.f;
             }
-            if (a.out_f32) {
+            if (a.out_mode == TC_OUT_F32) {
               float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + r * a.N + jbase + 16 * p);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 dst[i] = make_float4(z[4 * i], z[4 * i + 1], z[4 * i + 2], z[4 * i + 3]);
+            } else if (a.out_mode == TC_OUT_NVFP4_F16 || a.out_mode == TC_OUT_F16) {
+              // the 16 outputs are one NVFP4 group (jbase is a multiple of 16)
+              uint32_t w[8];
+              if (a.out_mode == TC_OUT_NVFP4_F16) {
+                uint32_t lo, hi;
+                const uint32_t sq = nvfp4_quant16(z, a.out_global[e], lo, hi);
+                const float sv = e4m3_to_f32(sq);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = nvfp4_decode_pair(lo, hi, i, sv, true);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const __half2 h2 = __floats2half2_rn(z[2 * i], z[2 * i + 1]);
+                  w[i] = *reinterpret_cast<const uint32_t *>(&h2);
+                }
+              }
+              uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + r * a.N + jbase + 16 * p);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
             } else {
               uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + r * a.N + jbase + 16 * p);
 #pragma unroll
