@@ -221,7 +221,8 @@ int moe_route_topk(const void *logits, int logits_bf16, int M, int num_experts, 
  *     code = e2m1_rne_sat(fl32(x / fl32(e4m3(s) * g))); s == 0 gives zero codes.
  *   scale_in: device f32 [1] -- the static fp8 scale, or the NVFP4 global g.
  *   codes: u8 [rows, cols] (fp8) or [rows, cols/2] (NVFP4); scales as under moe_afmt.
- * MOE_A_BF16 is rejected (nothing to quantise). */
+ * x, codes and scales must be 16-byte aligned.  MOE_A_BF16 is rejected
+ * (nothing to quantise). */
 int moe_quant_act(const void *x_bf16, int rows, int cols, int afmt, const float *scale_in,
                   void *codes, void *scales, void *stream);
 

@@ -434,7 +434,7 @@ int moe_quant_act(const void *x_bf16, int rows, int cols, int afmt, const float 
   if (afmt == A_NVFP4_DYN && cols % 16 != 0) return MOE_ERR_UNSUPPORTED;
   if ((afmt == A_FP8_TENSOR_STATIC || afmt == A_NVFP4_DYN) && !scale_in) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
-  if (!x_bf16 || !codes || !scales || !aligned16(codes) || !aligned16(scales))
+  if (!x_bf16 || !aligned16(x_bf16) || !codes || !scales || !aligned16(codes) || !aligned16(scales))
     return MOE_ERR_INVALID_ARG;
   QuantArgs q;
   memset(&q, 0, sizeof(q));

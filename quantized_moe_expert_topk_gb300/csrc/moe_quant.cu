@@ -36,6 +36,21 @@ __device__ __forceinline__ float load_elem<float>(const float *x, long i) {
   return x[i];
 }
 
+// Four consecutive elements (4-element aligned) in one vector load.
+template <typename InT>
+__device__ __forceinline__ void load4(const InT *x, float (&v)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float *x, float (&v)[4]) {
+  const float4 f = *reinterpret_cast<const float4 *>(x);
+  v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+}
+template <>
+__device__ __forceinline__ void load4<uint16_t>(const uint16_t *x, float (&v)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(x);
+  v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
+  v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+
 // Row state of a sorted intermediate row: -1 beyond num_post_pad (skip),
 // 0 padding row (zero codes), 1 live row.
 __device__ __forceinline__ int row_state(const QuantArgs &a, long r) {
@@ -61,11 +76,14 @@ __global__ void quant_fp8_group128(QuantArgs a) {
   const int c0 = g * 128 + lane * 4;
   float v[4];
   float amax = 0.f;
+  if (st > 0 && c0 + 3 < a.cols && (a.cols & 3) == 0) {
+    load4<InT>(x + c0, v);  // one 16-byte (fp32) or 8-byte (bf16) load
+  } else {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[i] = (st > 0 && c0 + i < a.cols) ? load_elem<InT>(x, c0 + i) : 0.f;
-    amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < 4; ++i) v[i] = (st > 0 && c0 + i < a.cols) ? load_elem<InT>(x, c0 + i) : 0.f;
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(v[i]));
   amax = warp_max(amax);
   const float scale = fp8_group_scale(amax);
   uint32_t packed = 0;
