@@ -62,6 +62,21 @@ def test_edge_cases():
     check(wl)
 
 
+@pytest.mark.parametrize("path", ["auto", "generic", "stream", "tc"])
+def test_empty_batch(path):
+    # M = 0: nothing is launched, the call succeeds, the (0, K) output stays empty
+    import quantized_moe_expert_topk_gb300 as moe
+    try:
+        moe.moe_set_path(path)
+        wl = to_device(make_custom(M=0, K=256, N=256, E=8, T=2, wfmt="mxfp4", afmt="bf16",
+                                   act="swiglu_oai", gate="interleaved", seed=3, name="empty"))
+        out = run_gpu(wl)
+        assert out.shape == (0, 256)
+        assert moe.moe_get_device_error() == 0
+    finally:
+        moe.moe_set_path("auto")
+
+
 def test_all_masked_gives_zero():
     wl = make_custom(M=33, K=128, N=64, E=4, T=2, bias=True, seed=5, name="all-masked")
     wl.expert_map = torch.full((4,), -1, dtype=torch.int32)
