@@ -53,14 +53,16 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
   griddep_wait();
   if (blockIdx.x > 0 && (int)blockIdx.x <= zero_ctas) {
     // zeroing CTAs: 16-byte stores over the aligned body, scalar tail
-    const long n4 = x.zero_n / 4;
+    const long n4 = x.zero_buf ? x.zero_n / 4 : 0;
     float4 *p4 = reinterpret_cast<float4 *>(x.zero_buf);
     const long stride = (long)zero_ctas * blockDim.x;
     for (long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < n4; i += stride)
       p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (long i = n4 * 4 + (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < x.zero_n;
-         i += stride)
+    for (long i = n4 * 4 + (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+         x.zero_buf && i < x.zero_n; i += stride)
       x.zero_buf[i] = 0.f;
+    for (long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < x.zero_ints_n; i += stride)
+      x.zero_ints[i] = 0;
     return;
   }
   if ((int)blockIdx.x > zero_ctas) {
@@ -273,9 +275,11 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *e
     if (opt_in != cudaSuccess) return opt_in;
   }
   int zero_ctas = 0, conv_ctas = 0;
-  if (extra.zero_buf && extra.zero_n > 0) {
+  if ((extra.zero_buf && extra.zero_n > 0) || (extra.zero_ints && extra.zero_ints_n > 0)) {
     const long per_cta = (long)kAlignThreads * 4 * 8;
-    zero_ctas = (int)ceil_div(extra.zero_n, per_cta);
+    const long n = extra.zero_buf ? extra.zero_n : 0;
+    zero_ctas = (int)ceil_div(n + extra.zero_ints_n, per_cta);
+    if (zero_ctas < 1) zero_ctas = 1;
     if (zero_ctas > 4 * 152) zero_ctas = 4 * 152;
   }
   if (extra.x && extra.xM > 0) {

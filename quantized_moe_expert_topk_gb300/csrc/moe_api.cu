@@ -126,8 +126,13 @@ struct TcLayout {
 struct Layout {
   long cap, blocks;
   size_t sorted, expert_ids, ntp, counts, offsets, active, n_active, counters, x16, x_inv, a1_codes,
-      a1_scales, inter, inter_scales, staging, acc, total;
+      a1_scales, inter, inter_scales, staging, acc, hpart, fixcnt, total;
+  int w13_ksplit;  // k-split of the streaming W13 units (1: none)
+  long fixcnt_n;   // counters of the split W13 units
 };
+
+// SM count the split decisions assume (GB300); the grids use the real count.
+constexpr int kNominalSms = 152;
 
 Layout make_layout(const moe_problem_t *p) {
   Layout L;
@@ -162,6 +167,18 @@ Layout make_layout(const moe_problem_t *p) {
     L.staging = o; o = align_up(o + (size_t)L.cap * p->N * 4);
   }
   L.acc = o; o = align_up(o + (size_t)p->M * p->K * 4);
+  // split-K W13 of the streaming path (very small batches): fp32 partials per
+  // k-range and slot, and one counter per (pass, unit, consumer warp)
+  L.w13_ksplit = (p->wfmt == W_MXFP4 && p->afmt == A_BF16)
+                     ? stream_w13_ksplit(p->M, p->topk, p->num_local_experts, p->N, p->K, kNominalSms)
+                     : 1;
+  L.fixcnt_n = 0;
+  L.hpart = L.fixcnt = o;
+  if (L.w13_ksplit > 1) {
+    L.hpart = o; o = align_up(o + (size_t)L.w13_ksplit * p->M * p->topk * p->N * 8);
+    L.fixcnt_n = stream_w13_fixups(L.cap, p->N);
+    L.fixcnt = o; o = align_up(o + (size_t)L.fixcnt_n * 4);
+  }
   L.total = o;
   return L;
 }
@@ -335,7 +352,7 @@ int run_w2(const moe_problem_t *p, const void *inter, const void *inter_scales,
   sc2.done();
   if (rc != MOE_OK) return rc;
   StageScope scf(MOE_STAGE_FINALIZE, st);
-  rc = cuda_status(launch_finalize(acc, (long)p->M * p->K, out, st));
+  rc = cuda_status(launch_finalize(acc, (long)p->M * p->K, out, st, true));
   scf.done();
   return rc;
 }
@@ -551,6 +568,10 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     ex.xK = p->K;
   }
   ex.num_valid_tokens = p->num_local_tokens;
+  if (streaming && L.w13_ksplit > 1) {
+    ex.zero_ints = reinterpret_cast<int32_t *>(ws + L.fixcnt);
+    ex.zero_ints_n = L.fixcnt_n;
+  }
   std::lock_guard<std::mutex> timing_lock(g_timing_mu);
   {
     StageScope sc(MOE_STAGE_ALIGN, st);
@@ -575,8 +596,11 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     StreamArgs s13 = sa;
     s13.C = p->K;
     s13.units_per_expert = stream_units_per_expert(1, p->N, p->K);
-    s13.ksplit = 1;
+    s13.ksplit = L.w13_ksplit;
     s13.kblocks = p->K / 64;
+    s13.hpart = reinterpret_cast<float *>(ws + L.hpart);
+    s13.fix_cnt = reinterpret_cast<int *>(ws + L.fixcnt);
+    s13.S = p->M * p->topk;
     s13.packed = w13->packed; s13.bias = w13->bias;
     s13.x16 = ex.x16; s13.x_inv = ex.x_inv;
     s13.topk_weights = topk_weights;  // read only with the router weight on the stage-1 output
@@ -593,7 +617,16 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     s2.C = p->N;
     s2.units_per_expert = stream_units_per_expert(0, p->N, p->K);
     s2.kblocks = p->N / 64;
-    s2.ksplit = s2.kblocks >= 16 ? 2 : 1;
+    // split the reduction so that the units keep every CTA busy when few
+    // experts are active (about two units per CTA), at least 8 k64 blocks each
+    {
+      const long act = (long)p->M * p->topk < p->num_local_experts ? (long)p->M * p->topk
+                                                                   : p->num_local_experts;
+      const long units = act * s2.units_per_expert;
+      const long want = ceil_div(2L * 4 * kNominalSms, units > 0 ? units : 1);
+      const long cap_split = s2.kblocks / 8 > 1 ? s2.kblocks / 8 : 1;
+      s2.ksplit = (int)(want < 2 ? (cap_split >= 2 ? 2 : 1) : (want < cap_split ? want : cap_split));
+    }
     s2.packed = w2->packed; s2.bias = w2->bias;
     s2.x16 = ws + L.inter;
     s2.acc = acc; s2.topk_weights = topk_weights;

@@ -83,6 +83,10 @@ __device__ __forceinline__ long weight_row(const GemmArgs &a, int nt, int q) {
 template <int MODE, int WK>
 __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs a) {
   __shared__ __align__(16) Smem sm;
+  // dependent launch: wait for the producer of the sorted rows / operands
+  // (it may still be draining); the next kernel may be scheduled now
+  griddep_wait();
+  griddep_launch_dependents();
   const int blk = blockIdx.x;
   const int nt = blockIdx.y;
   if ((long)blk * BM >= (long)*a.num_post_pad) return;
@@ -396,15 +400,15 @@ cudaError_t launch_mode(const GemmArgs &a, long cap_rows, cudaStream_t stream) {
   const long ntiles = MODE == MODE_W13 ? ceil_div(a.N, 64) : ceil_div(a.K, BN);
   dim3 grid((unsigned)blocks, (unsigned)ntiles);
   switch (a.wfmt) {
-    case W_BF16: gemm_kernel<MODE, WK_BF16><<<grid, THREADS, 0, stream>>>(a); break;
+    case W_BF16: return launch_kernel(gemm_kernel<MODE, WK_BF16>, grid, dim3(THREADS), 0, stream, true, a);
     case W_FP8_TENSOR:
     case W_FP8_CHANNEL:
-    case W_FP8_BLOCK128: gemm_kernel<MODE, WK_FP8><<<grid, THREADS, 0, stream>>>(a); break;
-    case W_MXFP4: gemm_kernel<MODE, WK_MXFP4><<<grid, THREADS, 0, stream>>>(a); break;
-    case W_NVFP4: gemm_kernel<MODE, WK_NVFP4><<<grid, THREADS, 0, stream>>>(a); break;
+    case W_FP8_BLOCK128:
+      return launch_kernel(gemm_kernel<MODE, WK_FP8>, grid, dim3(THREADS), 0, stream, true, a);
+    case W_MXFP4: return launch_kernel(gemm_kernel<MODE, WK_MXFP4>, grid, dim3(THREADS), 0, stream, true, a);
+    case W_NVFP4: return launch_kernel(gemm_kernel<MODE, WK_NVFP4>, grid, dim3(THREADS), 0, stream, true, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 __global__ void finalize_kernel(const float *__restrict__ acc, long n, uint16_t *__restrict__ out) {

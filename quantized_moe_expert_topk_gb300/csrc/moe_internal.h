@@ -48,6 +48,8 @@ struct AlignExtras {
   void *x16 = nullptr;            //   max |x16| in [2^14, 2^15); x_inv[row] = 2^-a
   float *x_inv = nullptr;
   int xM = 0, xK = 0;
+  int32_t *zero_ints = nullptr;   // also zeroed (counters of the split W13 units)
+  long zero_ints_n = 0;
   const int32_t *num_valid_tokens = nullptr;  // [1]: slots of tokens >= it are dropped
   int slots_per_token = 1;                     // topk (set by launch_align)
 };
@@ -128,7 +130,18 @@ struct StreamArgs {
   int w_stage1;                   // router weight on the stage-1 output (W13 multiplies, W2 not)
   int *err;                       // device error word
   int *work_counter;              // zero at launch; units are claimed from it
+  // W13 with ksplit > 1: each k-range writes its fp32 (gate, up) partials to
+  // hpart[ks][slot][N][2]; the last of the ksplit arrivals of a (unit, pass,
+  // warp) -- counted in fix_cnt, zeroed by the sort -- sums them and applies
+  // bias and activation
+  float *hpart;
+  int *fix_cnt;
+  int S;                          // slots (M * T)
 };
+// k-split of the W13 streaming units for this problem (1 = whole K per unit).
+int stream_w13_ksplit(int M, int topk, int El, int N, int K, int sm_count);
+// Number of fixup counters of the split W13 units for a sort capacity.
+long stream_w13_fixups(long cap_rows, int N);
 struct PackArgs {
   const unsigned char *codes, *scales;
   unsigned char *out;

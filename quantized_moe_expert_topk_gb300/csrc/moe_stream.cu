@@ -166,7 +166,8 @@ __device__ __forceinline__ void consume_k64(const unsigned char *tp0, uint32_t x
   }
 }
 
-template <int MODE>
+// SPLIT (W13 only): the units are split along K; partials + last-arriver fixup.
+template <int MODE, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
@@ -366,7 +367,39 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
 
     // -------------------------------------------------------------- epilogue
     const int tok0 = d.tok0;
-    if (MODE == MODE_W13) {
+    bool finish = true;  // this warp applies the activation (W13)
+    if (MODE == MODE_W13 && SPLIT) {
+      // k-split: write this k-range's (gate, up) partials, already scaled by
+      // the token's x_inv; the last of the ksplit arrivals for this (unit,
+      // pass, warp) sums them below (no waiting: the others just move on)
+      const int N = a.N;
+      const int ks = d.id % a.ksplit;
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const int j = U.u * (TILES * 8) + (warp * MT + m) * 8 + g;
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int tn = n * 8 + 2 * t + c;
+            if (tn >= nt) continue;
+            const float xi = tok_f[n][c];
+            float2 *dst = reinterpret_cast<float2 *>(a.hpart) +
+                          ((long)ks * a.S + tok_sid[n][c]) * N + j;
+            *dst = make_float2(acc[m][n][c] * xi, acc[m][n][2 + c] * xi);
+          }
+      }
+      __threadfence();  // the partials are visible before the count says so
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        const long cidx = (((long)(U.off + tok0) >> 4) * a.units_per_expert + U.u) * CW + warp;
+        last = atomicAdd(a.fix_cnt + cidx, 1) == a.ksplit - 1;
+      }
+      finish = __shfl_sync(0xffffffffu, last, 0) != 0;
+      if (finish) __threadfence();  // and the others' partials are visible to us
+    }
+    if (MODE == MODE_W13 && finish) {
       const int N = a.N;
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
@@ -387,13 +420,23 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
             if (tn >= nt) continue;
             const int r = U.off + tok0 + tn;
             const float xi = tok_f[n][c];
-            const float gv = acc[m][n][c] * xi + bg;
-            const float uv = acc[m][n][2 + c] * xi + bu;
+            float gsum = acc[m][n][c] * xi, usum = acc[m][n][2 + c] * xi;
+            if (SPLIT) {  // the sum of every k-range's partial, in k order
+              gsum = usum = 0.f;
+              for (int ks = 0; ks < a.ksplit; ++ks) {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(a.hpart) +
+                                        ((long)ks * a.S + tok_sid[n][c]) * N + j);
+                gsum += v.x;
+                usum += v.y;
+              }
+            }
+            const float gv = gsum + bg;
+            const float uv = usum + bu;
             const float z = tok_zw[n][c] * act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit);
             static_cast<__half *>(a.out)[(long)r * N + j] = __float2half_rn(z);
           }
       }
-    } else {
+    } else if (MODE == MODE_W2) {
       const int K = a.K;
 #pragma unroll
       for (int m = 0; m < MT; ++m)
@@ -479,18 +522,33 @@ cudaError_t launch_pack_mxfp4(const PackArgs &p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+int stream_w13_ksplit(int M, int topk, int El, int N, int K, int sm_count) {
+  // split K only when the W13 units cannot give every CTA two of them; each
+  // k-range keeps at least two stages
+  const long act = (long)M * topk < El ? (long)M * topk : El;
+  const long units = act * (N / (TILES * 8));
+  const long want = units > 0 ? ceil_div(2L * CTAS_PER_SM * sm_count, units) : 1;
+  const long cap = (K / 64) / (2 * S_KB) > 1 ? (K / 64) / (2 * S_KB) : 1;
+  return (int)(want <= 1 ? 1 : (want < cap ? want : cap));
+}
+
+long stream_w13_fixups(long cap_rows, int N) { return (cap_rows / 16) * (N / (TILES * 8)) * CW; }
+
 int stream_units_per_expert(int w13, int N, int K) {
   return w13 ? N / (TILES * 8) : (int)ceil_div(K, ROWS);
 }
 
 cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream_t stream) {
-  auto kern = w13 ? stream_kernel<MODE_W13> : stream_kernel<MODE_W2>;
-  static bool attr_done[2] = {false, false};
-  if (!attr_done[w13]) {
+  const int variant = w13 ? (a.ksplit > 1 ? 2 : 1) : 0;
+  auto kern = variant == 2 ? stream_kernel<MODE_W13, true>
+              : variant == 1 ? stream_kernel<MODE_W13, false>
+                             : stream_kernel<MODE_W2, false>;
+  static bool attr_done[3] = {false, false, false};
+  if (!attr_done[variant]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done[w13] = true;
+    attr_done[variant] = true;
   }
   const long max_units = (long)a.max_active * a.units_per_expert * a.ksplit;
   long grid = (long)CTAS_PER_SM * sm_count;

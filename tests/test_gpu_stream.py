@@ -29,6 +29,10 @@ CASES = [
     dict(M=12, K=256, N=1088, E=4, T=2, gate="interleaved", bias=False),   # w2 split in two k-ranges
     dict(M=40, K=512, N=256, E=16, T=4, gate="separated", bias=True, mask_frac=0.4),
     dict(M=1, K=2880, N=2880, E=8, T=4, gate="interleaved", bias=True),
+    # very small batches: the W13 units are split along K (partials + fixup)
+    dict(M=1, K=2880, N=2880, E=128, T=4, gate="interleaved", bias=True),   # 5-way split
+    dict(M=2, K=1024, N=512, E=32, T=2, gate="separated", bias=True),      # ragged k-ranges
+    dict(M=3, K=2048, N=1024, E=64, T=4, gate="interleaved", bias=True, mask_frac=0.25),
     # more than 16 tokens on some experts: several passes per unit
     dict(M=64, K=256, N=128, E=8, T=2, gate="interleaved", bias=True),      # ~16 tokens/expert
     dict(M=60, K=320, N=192, E=4, T=2, gate="separated", bias=True),        # ~30: 1-2 passes, ragged
