@@ -37,7 +37,7 @@ _LIB = os.path.join(_HERE, "_liboracle.so")
 
 WFMT = {"bf16": 0, "fp8_tensor": 1, "fp8_channel": 2, "fp8_block128": 3, "mxfp4": 4, "nvfp4": 5}
 AFMT = {"bf16": 0, "fp8_tensor_static": 1, "fp8_tensor_dyn": 2, "fp8_token_dyn": 3,
-        "fp8_group128_dyn": 4, "nvfp4_dyn": 5}
+        "fp8_group128_dyn": 4, "nvfp4_dyn": 5, "mxfp4_dyn": 6, "mxfp8_dyn": 7}
 ACT = {"silu": 0, "gelu": 1, "swiglu_oai": 2}
 GATE = {"separated": 0, "interleaved": 1}
 
@@ -186,7 +186,8 @@ def align_block_size(topk_ids, expert_map, E: int, El: int, BM: int):
 def act_scale_shape(afmt: str, rows: int, cols: int):
     return {"fp8_tensor_static": (1,), "fp8_tensor_dyn": (1,), "fp8_token_dyn": (rows,),
             "fp8_group128_dyn": (rows, (cols + 127) // 128),
-            "nvfp4_dyn": (rows, cols // 16)}[afmt]
+            "nvfp4_dyn": (rows, cols // 16), "mxfp4_dyn": (rows, cols // 32),
+            "mxfp8_dyn": (rows, cols // 32)}[afmt]
 
 
 def quant_act(x_bits: np.ndarray, afmt: str, scale_in=None):
@@ -194,8 +195,11 @@ def quant_act(x_bits: np.ndarray, afmt: str, scale_in=None):
     Returns (codes uint8, scales f32 or e4m3 uint8)."""
     x = _c(x_bits, np.uint16)
     rows, cols = x.shape
-    if afmt == "nvfp4_dyn":
+    if afmt in ("nvfp4_dyn", "mxfp4_dyn"):
         codes = np.zeros((rows, cols // 2), np.uint8)
+        scales = np.zeros(act_scale_shape(afmt, rows, cols), np.uint8)
+    elif afmt == "mxfp8_dyn":
+        codes = np.zeros((rows, cols), np.uint8)
         scales = np.zeros(act_scale_shape(afmt, rows, cols), np.uint8)
     else:
         codes = np.zeros((rows, cols), np.uint8)

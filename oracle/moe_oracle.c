@@ -51,7 +51,8 @@
 enum { ORC_W_BF16 = 0, ORC_W_FP8_TENSOR = 1, ORC_W_FP8_CHANNEL = 2,
        ORC_W_FP8_BLOCK128 = 3, ORC_W_MXFP4 = 4, ORC_W_NVFP4 = 5 };
 enum { ORC_A_BF16 = 0, ORC_A_FP8_TENSOR_STATIC = 1, ORC_A_FP8_TENSOR_DYN = 2,
-       ORC_A_FP8_TOKEN_DYN = 3, ORC_A_FP8_GROUP128_DYN = 4, ORC_A_NVFP4_DYN = 5 };
+       ORC_A_FP8_TOKEN_DYN = 3, ORC_A_FP8_GROUP128_DYN = 4, ORC_A_NVFP4_DYN = 5,
+       ORC_A_MXFP4_DYN = 6, ORC_A_MXFP8_DYN = 7 };
 enum { ORC_ACT_SILU = 0, ORC_ACT_GELU = 1, ORC_ACT_SWIGLU_OAI = 2 };
 enum { ORC_GATE_SEPARATED = 0, ORC_GATE_INTERLEAVED = 1 };
 
@@ -339,6 +340,28 @@ static int nvfp4_encode_group(const float *x, double g, uint8_t *codes16) {
   return s;
 }
 
+/* OCP MX block of 32 fp32 values (MXFP4: e2m1 elements, emax 2; MXFP8: e4m3
+ * elements, emax 8), the conversion of the OCP Microscaling Formats (MX) v1.0
+ * specification: shared exponent X = floor(log2(amax)) - emax, clamped to the
+ * e8m0 range [-127, 127]; scale code X + 127; element code = RNE with
+ * saturation of x / 2^X (an exact power-of-two division).  amax == 0 gives
+ * scale code 0 and zero codes.  Element codes one per byte. */
+static int mx_encode_group(const float *x, int elem_fp4, uint8_t *codes32) {
+  double amax = 0.0;
+  for (int i = 0; i < 32; ++i) { double a = fabs((double)x[i]); if (a > amax) amax = a; }
+  if (amax == 0.0) { for (int i = 0; i < 32; ++i) codes32[i] = 0; return 0; }
+  int ex;
+  frexp(amax, &ex);                 /* amax = f * 2^ex, 0.5 <= f < 1 */
+  int X = (ex - 1) - (elem_fp4 ? 2 : 8);
+  if (X < -127) X = -127;
+  if (X > 127) X = 127;
+  for (int i = 0; i < 32; ++i) {
+    double v = ldexp((double)x[i], -X);
+    codes32[i] = (uint8_t)(elem_fp4 ? orc_e2m1_encode(v) : orc_e4m3_encode(v));
+  }
+  return X + 127;
+}
+
 /* Quantise fp32 rows.  Layouts (row-major):
  *   fp8 codes  u8 [rows, cols];  NVFP4 codes u8 [rows, cols/2] (even column in
  *   the low nibble);
@@ -381,6 +404,24 @@ static int quant_rows(const float *x, long rows, long cols, int afmt,
         double scale = fp8_dyn_scale(amax);
         ((float *)scales)[r * G + g] = (float)scale;
         fp8_encode_group(x + r * cols + c0, n, scale, codes + r * cols + c0);
+      }
+    return 0;
+  }
+  if (afmt == ORC_A_MXFP4_DYN || afmt == ORC_A_MXFP8_DYN) {
+    if (cols % 32) return -1;
+    const int fp4 = afmt == ORC_A_MXFP4_DYN;
+    long G = cols / 32;
+    uint8_t q[32];
+    for (long r = 0; r < rows; ++r)
+      for (long gi = 0; gi < G; ++gi) {
+        int sc = mx_encode_group(x + r * cols + gi * 32, fp4, q);
+        ((uint8_t *)scales)[r * G + gi] = (uint8_t)sc;
+        if (fp4) {
+          for (int i = 0; i < 16; ++i)
+            codes[r * (cols / 2) + gi * 16 + i] = (uint8_t)(q[2 * i] | (q[2 * i + 1] << 4));
+        } else {
+          memcpy(codes + r * cols + gi * 32, q, 32);
+        }
       }
     return 0;
   }
@@ -429,6 +470,16 @@ static void dequant_rows(const uint8_t *codes, const void *scales, long rows,
           v = orc_e2m1_decode(q) * orc_e4m3_decode(((const uint8_t *)scales)[r * (cols / 16) + c / 16]) * g;
           break;
         }
+        case ORC_A_MXFP4_DYN: {
+          uint8_t b = codes[r * (cols / 2) + c / 2];
+          int q = (c & 1) ? (b >> 4) : (b & 15);
+          v = orc_e2m1_decode(q) * orc_e8m0_decode(((const uint8_t *)scales)[r * (cols / 32) + c / 32]);
+          break;
+        }
+        case ORC_A_MXFP8_DYN:
+          v = orc_e4m3_decode(codes[r * cols + c]) *
+              orc_e8m0_decode(((const uint8_t *)scales)[r * (cols / 32) + c / 32]);
+          break;
         default: v = NAN;
       }
       out[r * cols + c] = v;
@@ -449,7 +500,7 @@ int orc_quant_act(const uint16_t *x_bf16, long rows, long cols, int afmt,
  * per_row_param is set (used for the stage-2 intermediate). */
 int orc_qdq_rows(const float *x, long rows, long cols, int afmt,
                  const float *param, int per_row_param, double *out) {
-  long ncodes = (afmt == ORC_A_NVFP4_DYN) ? rows * cols / 2 : rows * cols;
+  long ncodes = (afmt == ORC_A_NVFP4_DYN || afmt == ORC_A_MXFP4_DYN) ? rows * cols / 2 : rows * cols;
   long nscales = rows * ((cols + 15) / 16) + rows * ((cols + 127) / 128) + rows + 1;
   uint8_t *codes = (uint8_t *)malloc(ncodes > 0 ? ncodes : 1);
   float *scales = (float *)malloc(sizeof(float) * nscales);
@@ -557,6 +608,8 @@ static int stage2_afmt(const orc_problem *p) {
     case ORC_W_FP8_CHANNEL: return ORC_A_FP8_TOKEN_DYN;
     case ORC_W_FP8_BLOCK128: return ORC_A_FP8_GROUP128_DYN;
     case ORC_W_NVFP4: return ORC_A_NVFP4_DYN;
+    case ORC_W_MXFP4: /* w4a4 / w4a8: the intermediate in the activation format */
+      return (p->afmt == ORC_A_MXFP4_DYN || p->afmt == ORC_A_MXFP8_DYN) ? p->afmt : ORC_A_BF16;
     default: return ORC_A_BF16; /* no requantisation */
   }
 }
