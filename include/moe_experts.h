@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 6
+#define MOE_ABI_VERSION 7
 
 typedef enum {
   MOE_OK = 0,
@@ -65,17 +65,27 @@ typedef enum {
  * as the leaves' _supports_quant_scheme lists them:
  *   BF16 + BF16; FP8_TENSOR + FP8_TENSOR_STATIC | FP8_TENSOR_DYN;
  *   FP8_CHANNEL + FP8_TOKEN_DYN; FP8_BLOCK128 + FP8_GROUP128_DYN;
- *   MXFP4 + BF16 (w4a16); NVFP4 + NVFP4_DYN.
+ *   MXFP4 + BF16 (w4a16), MXFP4 + MXFP4_DYN (w4a4), MXFP4 + MXFP8_DYN (w4a8)
+ *   (AiterMxfp4Experts: "MXFP4 weights with a bf16 or MXFP4-dynamic
+ *   activation"; MXFP4 x MXFP8 as named by the mxfp4.py backends);
+ *   NVFP4 + NVFP4_DYN.
  * The intermediate (stage-2 input) uses the same scheme: per-tensor static
  * (a2_scale) or dynamic, per-token dynamic, 1x128 dynamic, NVFP4 x16 dynamic
- * with a per-expert global; bf16 for BF16 and MXFP4 weights. */
+ * with a per-expert global, MX; bf16 for BF16 weights and MXFP4 w4a16. */
 typedef enum {
   MOE_A_BF16 = 0,
   MOE_A_FP8_TENSOR_STATIC = 1, /* scale f32 [1] given                          */
   MOE_A_FP8_TENSOR_DYN = 2,    /* scale f32 [1] = amax/448 over the tensor     */
   MOE_A_FP8_TOKEN_DYN = 3,     /* scales f32 [rows]                            */
   MOE_A_FP8_GROUP128_DYN = 4,  /* scales f32 [rows, ceil(cols/128)]            */
-  MOE_A_NVFP4_DYN = 5          /* codes u8 [rows, cols/2], scales e4m3 [rows, cols/16] */
+  MOE_A_NVFP4_DYN = 5,         /* codes u8 [rows, cols/2], scales e4m3 [rows, cols/16] */
+  /* OCP MX, 32-element blocks with an e8m0 scale (cols % 32 == 0): X =
+   * floor(log2(amax)) - emax (2 for e2m1, 8 for e4m3) clamped to [-127, 127],
+   * scale code X + 127, element = RNE-saturating e2m1 / e4m3 of x / 2^X;
+   * amax == 0 gives scale code 0 and zero codes.  The stage-2 intermediate of
+   * these pairs uses the same format. */
+  MOE_A_MXFP4_DYN = 6,         /* codes u8 [rows, cols/2], scales e8m0 [rows, cols/32] */
+  MOE_A_MXFP8_DYN = 7          /* codes e4m3 [rows, cols],  scales e8m0 [rows, cols/32] */
 } moe_afmt;
 
 /* Activations of the gated MLP (_resolve_aiter_activation; SITU is not

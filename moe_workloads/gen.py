@@ -263,6 +263,16 @@ WORKLOADS = {
         M=128, K=2880, N=2880, E=128, T=4, mask_frac=0.25, wfmt="mxfp4", afmt="bf16",
         act="swiglu_oai", gate="interleaved", bias=True,
         recipe="as gptoss20b, E=128 with an expert map masking a random 25% (96 local)"),
+    # MXFP4 weights with OCP MX dynamic activations (the w4a4 / w4a8 variants of
+    # AiterMxfp4Experts and the MXFP4 x MXFP8 backends), GPT-OSS-20B shapes
+    "gptoss20b_w4a4_m64": dict(
+        M=64, K=2880, N=2880, E=32, T=4, wfmt="mxfp4", afmt="mxfp4_dyn", act="swiglu_oai",
+        gate="interleaved", bias=True,
+        recipe="as gptoss20b; activations and intermediate MXFP4 dynamic (e2m1 + e8m0/32)"),
+    "gptoss20b_w4a8_m64": dict(
+        M=64, K=2880, N=2880, E=32, T=4, wfmt="mxfp4", afmt="mxfp8_dyn", act="swiglu_oai",
+        gate="interleaved", bias=True,
+        recipe="as gptoss20b; activations and intermediate MXFP8 dynamic (e4m3 + e8m0/32)"),
     "mixtral_nvfp4_m8192": dict(
         M=8192, K=4096, N=14336, E=8, T=2, wfmt="nvfp4", afmt="nvfp4_dyn", act="silu",
         gate="separated",

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 
 WFMT = {"bf16": 0, "fp8_tensor": 1, "fp8_channel": 2, "fp8_block128": 3, "mxfp4": 4, "nvfp4": 5}
 AFMT = {"bf16": 0, "fp8_tensor_static": 1, "fp8_tensor_dyn": 2, "fp8_token_dyn": 3,
-        "fp8_group128_dyn": 4, "nvfp4_dyn": 5}
+        "fp8_group128_dyn": 4, "nvfp4_dyn": 5, "mxfp4_dyn": 6, "mxfp8_dyn": 7}
 ACT = {"silu": 0, "gelu": 1, "swiglu_oai": 2}
 GATE = {"separated": 0, "interleaved": 1}
 STAGE2 = {"fp8_channel": "fp8_token_dyn", "fp8_block128": "fp8_group128_dyn", "nvfp4": "nvfp4_dyn"}
@@ -144,6 +144,8 @@ def make_weight(w: dict) -> Weight:
 
 def stage2_format(wfmt: str, afmt: str) -> str:
     if wfmt == "fp8_tensor":
+        return afmt
+    if wfmt == "mxfp4" and afmt in ("mxfp4_dyn", "mxfp8_dyn"):  # w4a4 / w4a8
         return afmt
     return STAGE2.get(wfmt, "bf16")
 

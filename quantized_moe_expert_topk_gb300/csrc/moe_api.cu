@@ -41,6 +41,8 @@ int stage2_afmt(const moe_problem_t *p) {
     case W_FP8_CHANNEL: return A_FP8_TOKEN_DYN;
     case W_FP8_BLOCK128: return A_FP8_GROUP128_DYN;
     case W_NVFP4: return A_NVFP4_DYN;
+    case W_MXFP4:  // w4a4 / w4a8: the intermediate in the activation's MX format
+      return (p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN) ? p->afmt : A_BF16;
     default: return A_BF16;
   }
 }
@@ -51,7 +53,7 @@ bool pair_supported(int wfmt, int afmt) {
     case W_FP8_TENSOR: return afmt == A_FP8_TENSOR_STATIC || afmt == A_FP8_TENSOR_DYN;
     case W_FP8_CHANNEL: return afmt == A_FP8_TOKEN_DYN;
     case W_FP8_BLOCK128: return afmt == A_FP8_GROUP128_DYN;
-    case W_MXFP4: return afmt == A_BF16;
+    case W_MXFP4: return afmt == A_BF16 || afmt == A_MXFP4_DYN || afmt == A_MXFP8_DYN;
     case W_NVFP4: return afmt == A_NVFP4_DYN;
     default: return false;
   }
@@ -59,7 +61,8 @@ bool pair_supported(int wfmt, int afmt) {
 
 size_t codes_bytes(int afmt, long rows, long cols) {
   if (afmt == A_BF16) return 0;
-  return afmt == A_NVFP4_DYN ? (size_t)rows * cols / 2 : (size_t)rows * cols;
+  return (afmt == A_NVFP4_DYN || afmt == A_MXFP4_DYN) ? (size_t)rows * cols / 2
+                                                     : (size_t)rows * cols;
 }
 
 size_t scales_bytes(int afmt, long rows, long cols) {
@@ -69,6 +72,8 @@ size_t scales_bytes(int afmt, long rows, long cols) {
     case A_FP8_TOKEN_DYN: return (size_t)rows * 4;
     case A_FP8_GROUP128_DYN: return (size_t)rows * ceil_div(cols, 128) * 4;
     case A_NVFP4_DYN: return (size_t)rows * (cols / 16);
+    case A_MXFP4_DYN:
+    case A_MXFP8_DYN: return (size_t)rows * (cols / 32);
     default: return 0;
   }
 }
@@ -78,7 +83,7 @@ int validate_problem(const moe_problem_t *p) {
   if (p->M < 0 || p->K <= 0 || p->N <= 0 || p->topk < 1 || p->num_experts < 1 ||
       p->num_local_experts < 1)
     return MOE_ERR_INVALID_ARG;
-  if (p->wfmt < W_BF16 || p->wfmt > W_NVFP4 || p->afmt < A_BF16 || p->afmt > A_NVFP4_DYN ||
+  if (p->wfmt < W_BF16 || p->wfmt > W_NVFP4 || p->afmt < A_BF16 || p->afmt > A_MXFP8_DYN ||
       p->act < ACT_SILU || p->act > ACT_SWIGLU_OAI || p->gate < GATE_SEPARATED ||
       p->gate > GATE_INTERLEAVED)
     return MOE_ERR_INVALID_ARG;
@@ -447,8 +452,9 @@ int moe_route_topk(const void *logits, int logits_bf16, int M, int num_experts, 
 int moe_quant_act(const void *x_bf16, int rows, int cols, int afmt, const float *scale_in,
                   void *codes, void *scales, void *stream) {
   if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
-  if (afmt <= A_BF16 || afmt > A_NVFP4_DYN) return MOE_ERR_INVALID_ARG;
+  if (afmt <= A_BF16 || afmt > A_MXFP8_DYN) return MOE_ERR_INVALID_ARG;
   if (afmt == A_NVFP4_DYN && cols % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((afmt == A_MXFP4_DYN || afmt == A_MXFP8_DYN) && cols % 32 != 0) return MOE_ERR_UNSUPPORTED;
   if ((afmt == A_FP8_TENSOR_STATIC || afmt == A_NVFP4_DYN) && !scale_in) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (!x_bf16 || !aligned16(x_bf16) || !codes || !scales || !aligned16(codes) || !aligned16(scales))
@@ -532,7 +538,8 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
   const bool streaming = (g_path == MOE_PATH_AUTO || g_path == MOE_PATH_STREAM) &&
                          stream_path(p, w13, w2);
   const bool fp4 = p->wfmt == W_MXFP4 || p->wfmt == W_NVFP4;
-  if (!streaming && tc_applies(p) &&
+  const bool mx_act = p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN;  // generic kernels only
+  if (!streaming && !mx_act && tc_applies(p) &&
       (!fp4 || (w13->packed_tc && w2->packed_tc && aligned16(w13->packed_tc) &&
                 aligned16(w2->packed_tc)))) {
     if (ws_bytes < make_tc_layout(p).total) return MOE_ERR_WORKSPACE;

@@ -24,7 +24,7 @@ namespace moe {
 enum WFmt { W_BF16 = 0, W_FP8_TENSOR = 1, W_FP8_CHANNEL = 2, W_FP8_BLOCK128 = 3, W_MXFP4 = 4,
             W_NVFP4 = 5 };
 enum AFmt { A_BF16 = 0, A_FP8_TENSOR_STATIC = 1, A_FP8_TENSOR_DYN = 2, A_FP8_TOKEN_DYN = 3,
-            A_FP8_GROUP128_DYN = 4, A_NVFP4_DYN = 5 };
+            A_FP8_GROUP128_DYN = 4, A_NVFP4_DYN = 5, A_MXFP4_DYN = 6, A_MXFP8_DYN = 7 };
 enum Act { ACT_SILU = 0, ACT_GELU = 1, ACT_SWIGLU_OAI = 2 };
 enum Gate { GATE_SEPARATED = 0, GATE_INTERLEAVED = 1 };
 

@@ -37,7 +37,11 @@ constexpr int LDS = BK + 8;         // smem row stride (bf16): 80 B, conflict-fr
 constexpr int THREADS = 256;
 
 enum { MODE_W13 = 0, MODE_W2 = 1 };
-enum { WK_BF16 = 0, WK_FP8 = 1, WK_MXFP4 = 2, WK_NVFP4 = 3 };
+// Weight kinds; WK_MX_A4 / WK_MX_A8 are MXFP4 weights with MXFP4 / MXFP8
+// (OCP MX, e8m0 per 32) activations, decoded exactly to bf16 like the weights.
+enum { WK_BF16 = 0, WK_FP8 = 1, WK_MXFP4 = 2, WK_NVFP4 = 3, WK_MX_A4 = 4, WK_MX_A8 = 5 };
+template <int WK>
+constexpr bool mx_weights() { return WK == WK_MXFP4 || WK == WK_MX_A4 || WK == WK_MX_A8; }
 
 struct Smem {
   __nv_bfloat16 A[2][BM][LDS];
@@ -126,10 +130,16 @@ __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs a) {
       if (WK == WK_BF16 || WK == WK_MXFP4) {
         ra = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.a_codes) +
                                                    a_src * Kred + k0 + a_kc));
-      } else if (WK == WK_FP8) {
+      } else if (WK == WK_FP8 || WK == WK_MX_A8) {
         const uint2 v = __ldg(reinterpret_cast<const uint2 *>(
             static_cast<const uint8_t *>(a.a_codes) + a_src * Kred + k0 + a_kc));
         ra.x = v.x; ra.y = v.y;
+        if (WK == WK_MX_A8)  // one 32-element block per stage (BK == 32)
+          ra_sc = static_cast<const uint8_t *>(a.a_scales)[a_src * (Kred / 32) + k0 / 32];
+      } else if (WK == WK_MX_A4) {
+        ra.x = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(a.a_codes) +
+                                                        a_src * (Kred / 2) + (k0 + a_kc) / 2));
+        ra_sc = static_cast<const uint8_t *>(a.a_scales)[a_src * (Kred / 32) + k0 / 32];
       } else {
         ra.x = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(a.a_codes) +
                                                         a_src * (Kred / 2) + (k0 + a_kc) / 2));
@@ -150,7 +160,7 @@ __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs a) {
         const uint2 v = __ldg(reinterpret_cast<const uint2 *>(
             static_cast<const uint8_t *>(a.w_codes) + b_row_g * (Kred / 2) + (k0 + b_kc) / 2));
         rb0.x = v.x; rb0.y = v.y;
-        if (WK == WK_MXFP4)
+        if (mx_weights<WK>())
           rb_sc = static_cast<const uint8_t *>(a.w_scales)[b_row_g * (Kred / 32) + k0 / 32];
         else
           rb_sc = static_cast<const uint8_t *>(a.w_scales)[b_row_g * (Kred / 16) + (k0 + b_kc) / 16];
@@ -165,14 +175,24 @@ __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs a) {
       va = make_uint4(0, 0, 0, 0);
     } else if (WK == WK_BF16 || WK == WK_MXFP4) {
       va = ra;
-    } else if (WK == WK_FP8) {
+    } else if (WK == WK_FP8 || WK == WK_MX_A8) {
+      const float sc = WK == WK_MX_A8 ? e8m0_to_f32(ra_sc) : 1.f;  // exact in bf16
       uint32_t w[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t src = i < 2 ? ra.x : ra.y;
         const int sh = (i & 1) * 16;
-        w[i] = pack_bf16x2(e4m3_to_f32((src >> sh) & 0xff), e4m3_to_f32((src >> (sh + 8)) & 0xff));
+        w[i] = pack_bf16x2(e4m3_to_f32((src >> sh) & 0xff) * sc,
+                           e4m3_to_f32((src >> (sh + 8)) & 0xff) * sc);
       }
+      va = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if (WK == WK_MX_A4) {
+      const float sc = e8m0_to_f32(ra_sc);
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = pack_bf16x2(e2m1_to_f32((ra.x >> (8 * i)) & 15) * sc,
+                           e2m1_to_f32((ra.x >> (8 * i + 4)) & 15) * sc);
       va = make_uint4(w[0], w[1], w[2], w[3]);
     } else {
       const float sc = e4m3_to_f32(ra_sc);
@@ -203,7 +223,7 @@ __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs a) {
       v0 = make_uint4(w[0], w[1], w[2], w[3]);
       v1 = make_uint4(w[4], w[5], w[6], w[7]);
     } else {
-      const float sc = WK == WK_MXFP4 ? e8m0_to_f32(rb_sc) : e4m3_to_f32(rb_sc);
+      const float sc = mx_weights<WK>() ? e8m0_to_f32(rb_sc) : e4m3_to_f32(rb_sc);
       uint32_t w[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -405,7 +425,12 @@ cudaError_t launch_mode(const GemmArgs &a, long cap_rows, cudaStream_t stream) {
     case W_FP8_CHANNEL:
     case W_FP8_BLOCK128:
       return launch_kernel(gemm_kernel<MODE, WK_FP8>, grid, dim3(THREADS), 0, stream, true, a);
-    case W_MXFP4: return launch_kernel(gemm_kernel<MODE, WK_MXFP4>, grid, dim3(THREADS), 0, stream, true, a);
+    case W_MXFP4:
+      if (a.afmt == A_MXFP4_DYN)
+        return launch_kernel(gemm_kernel<MODE, WK_MX_A4>, grid, dim3(THREADS), 0, stream, true, a);
+      if (a.afmt == A_MXFP8_DYN)
+        return launch_kernel(gemm_kernel<MODE, WK_MX_A8>, grid, dim3(THREADS), 0, stream, true, a);
+      return launch_kernel(gemm_kernel<MODE, WK_MXFP4>, grid, dim3(THREADS), 0, stream, true, a);
     case W_NVFP4: return launch_kernel(gemm_kernel<MODE, WK_NVFP4>, grid, dim3(THREADS), 0, stream, true, a);
     default: return cudaErrorInvalidValue;
   }

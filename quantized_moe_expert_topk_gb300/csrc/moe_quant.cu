@@ -205,6 +205,46 @@ __global__ void quant_nvfp4(QuantArgs a) {
   *scales = (uint8_t)s;
 }
 
+// ---- OCP MX (32-element blocks, e8m0 scale): one warp per block, lane = element.
+//   X = floor(log2(amax)) - emax (2 for e2m1, 8 for e4m3), clamped to [-127, 127];
+//   scale code X + 127; code = RNE-saturating convert of x * 2^-X (exact scaling);
+//   amax == 0: scale code 0, zero codes.
+template <typename InT, bool FP4>
+__global__ void quant_mx(QuantArgs a) {
+  const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = a.cols / 32;
+  const long r = warp_id / G;
+  const int g = (int)(warp_id % G);
+  if (r >= a.rows) return;
+  const int st = row_state(a, r);
+  if (st < 0) return;
+  const float v = st > 0 ? load_elem<InT>(static_cast<const InT *>(a.x) + r * a.cols, g * 32 + lane)
+                         : 0.f;
+  const float amax = warp_max(fabsf(v));
+  int code_x = 0;  // e8m0 scale code
+  float q = 0.f;   // x * 2^-X
+  if (amax > 0.f) {
+    int ex;
+    frexpf(amax, &ex);  // amax = f * 2^ex, 0.5 <= f < 1: floor(log2(amax)) = ex - 1
+    int X = ex - 1 - (FP4 ? 2 : 8);
+    X = X < -127 ? -127 : (X > 127 ? 127 : X);
+    code_x = X + 127;
+    q = ldexpf(v, -X);
+  }
+  uint8_t *scales = static_cast<uint8_t *>(a.scales);
+  if (lane == 0) scales[r * G + g] = (uint8_t)code_x;
+  if (FP4) {
+    // element 2i in the low nibble: even lanes pack their pair
+    const float q_hi = __shfl_down_sync(0xffffffffu, q, 1);
+    if ((lane & 1) == 0)
+      static_cast<uint8_t *>(a.codes)[r * (a.cols / 2) + g * 16 + (lane >> 1)] =
+          (uint8_t)f32x2_to_e2m1x2(q, q_hi);
+  } else {
+    static_cast<uint8_t *>(a.codes)[r * a.cols + g * 32 + lane] = (uint8_t)f32_to_e4m3(q);
+  }
+}
+
 template <typename InT>
 cudaError_t launch_quant_t(const QuantArgs &a, cudaStream_t stream) {
   if (a.rows <= 0 || a.cols <= 0) return cudaSuccess;
@@ -224,6 +264,15 @@ cudaError_t launch_quant_t(const QuantArgs &a, cudaStream_t stream) {
     case A_NVFP4_DYN: {
       const long groups = a.rows * (a.cols / 16);
       quant_nvfp4<InT><<<(unsigned)ceil_div(groups, 128), 128, 0, stream>>>(a);
+      break;
+    }
+    case A_MXFP4_DYN:
+    case A_MXFP8_DYN: {
+      const long groups = a.rows * (a.cols / 32);  // one warp each
+      if (a.afmt == A_MXFP4_DYN)
+        quant_mx<InT, true><<<(unsigned)ceil_div(groups * 32, 256), 256, 0, stream>>>(a);
+      else
+        quant_mx<InT, false><<<(unsigned)ceil_div(groups * 32, 256), 256, 0, stream>>>(a);
       break;
     }
     default:

@@ -35,7 +35,7 @@ def test_header_symbols_are_exported(moe):
     L = moe.lib()
     for name in declared:
         assert hasattr(L, name), name
-    assert moe.moe_abi_version() == 6
+    assert moe.moe_abi_version() == 7
 
 
 def test_status_strings(moe):
@@ -92,6 +92,8 @@ def test_quant_and_align_validation(moe):
     L = moe.lib()
     fake = ctypes.c_void_p(0x1000)
     assert L.moe_quant_act(fake, 4, 24, 5, fake, fake, fake, None) == 2   # NVFP4 cols % 16
+    assert L.moe_quant_act(fake, 4, 48, 6, None, fake, fake, None) == 2   # MXFP4 cols % 32
+    assert L.moe_quant_act(fake, 4, 48, 7, None, fake, fake, None) == 2   # MXFP8 cols % 32
     assert L.moe_quant_act(fake, 4, 32, 0, fake, fake, fake, None) == 1   # bf16: nothing to do
     assert L.moe_quant_act(fake, 4, 32, 1, None, fake, fake, None) == 1   # static scale missing
     assert L.moe_align_block_size(fake, 4, 2, None, 8, 2000, 64, fake, fake, fake, None, None) == 1

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 FORMATS = [
     ("bf16", "bf16"), ("fp8_tensor", "fp8_tensor_static"), ("fp8_tensor", "fp8_tensor_dyn"),
     ("fp8_channel", "fp8_token_dyn"), ("fp8_block128", "fp8_group128_dyn"),
-    ("mxfp4", "bf16"), ("nvfp4", "nvfp4_dyn"),
+    ("mxfp4", "bf16"), ("nvfp4", "nvfp4_dyn"), ("mxfp4", "mxfp4_dyn"), ("mxfp4", "mxfp8_dyn"),
 ]
 
 
@@ -75,6 +75,14 @@ def test_empty_batch(path):
         assert moe.moe_get_device_error() == 0
     finally:
         moe.moe_set_path("auto")
+
+
+@pytest.mark.parametrize("afmt", ["mxfp4_dyn", "mxfp8_dyn"])
+def test_mx_activations_prefill_size(afmt):
+    # w4a4 / w4a8 at a prefill-sized batch (the generic kernels run them)
+    wl = make_custom(M=700, K=512, N=256, E=8, T=4, wfmt="mxfp4", afmt=afmt, act="swiglu_oai",
+                     gate="interleaved", bias=True, seed=17, name=f"mx_{afmt}")
+    check(wl, sample_tokens(wl))
 
 
 def test_all_masked_gives_zero():

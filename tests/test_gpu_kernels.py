@@ -93,6 +93,7 @@ def bits(x):
     ("fp8_group128_dyn", 37, 7168), ("fp8_group128_dyn", 5, 2880), ("fp8_group128_dyn", 3, 200),
     ("fp8_token_dyn", 33, 2880), ("fp8_tensor_dyn", 17, 512), ("fp8_tensor_static", 9, 320),
     ("nvfp4_dyn", 41, 4096), ("nvfp4_dyn", 3, 48),
+    ("mxfp4_dyn", 29, 2880), ("mxfp4_dyn", 2, 64), ("mxfp8_dyn", 31, 2880), ("mxfp8_dyn", 1, 32),
 ])
 def test_quant_act_bit_exact(moe, afmt, rows, cols):
     rng = np.random.default_rng(rows * cols)
@@ -105,7 +106,8 @@ def test_quant_act_bit_exact(moe, afmt, rows, cols):
     want_codes, want_scales = oracle.quant_act(bits(x), afmt, scale_in)
     dev = "cuda"
     codes = torch.zeros(want_codes.shape, dtype=torch.uint8, device=dev)
-    scales = torch.zeros(want_scales.shape, dtype=torch.uint8 if afmt == "nvfp4_dyn" else torch.float32,
+    byte_scales = afmt in ("nvfp4_dyn", "mxfp4_dyn", "mxfp8_dyn")
+    scales = torch.zeros(want_scales.shape, dtype=torch.uint8 if byte_scales else torch.float32,
                          device=dev)
     sin = None if scale_in is None else torch.from_numpy(scale_in).to(dev)
     moe.moe_quant_act(x.to(dev), afmt, sin, codes, scales)
