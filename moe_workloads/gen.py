@@ -273,6 +273,12 @@ WORKLOADS = {
         M=64, K=2880, N=2880, E=32, T=4, wfmt="mxfp4", afmt="mxfp8_dyn", act="swiglu_oai",
         gate="interleaved", bias=True,
         recipe="as gptoss20b; activations and intermediate MXFP8 dynamic (e4m3 + e8m0/32)"),
+    # bf16 weights at prefill size: the tcgen05 kind::f16 path without any
+    # decode or promotion (a reference point for the quantised kinds)
+    "mixtral_bf16_m4096": dict(
+        M=4096, K=4096, N=14336, E=8, T=2, wfmt="bf16", afmt="bf16", act="silu",
+        gate="separated",
+        recipe="bf16 weights N(0,0.02), x~N(0,1); softmax-top2 renormalised; SiLU"),
     "mixtral_nvfp4_m8192": dict(
         M=8192, K=4096, N=14336, E=8, T=2, wfmt="nvfp4", afmt="nvfp4_dyn", act="silu",
         gate="separated",
