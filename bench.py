@@ -149,7 +149,7 @@ def mma_dtype(wl):
     decodes, the tcgen05 FP8 kinds e4m3, everything else (and the generic
     kernels) exact bf16 decodes."""
     path = kernel_path(wl)
-    if wl.wfmt in ("mxfp4", "nvfp4") and path in ("stream", "tc") and wl.afmt in ("bf16", "nvfp4_dyn"):
+    if wl.wfmt in ("mxfp4", "nvfp4") and path in ("stream", "tc"):
         return "f16"
     if path == "tc" and wl.wfmt.startswith("fp8"):
         return "e4m3"
@@ -271,10 +271,15 @@ def kernel_path(wl):
     """The kernel family moe_fused_experts picks for this workload (its
     default, automatic selection)."""
     slots = wl.M * wl.T
-    if (wl.wfmt == "mxfp4" and wl.afmt == "bf16" and wl.act == "swiglu_oai"
+    bounded = (wl.act == "swiglu_oai" and 0 < wl.swiglu_limit <= 64
+               and abs(wl.swiglu_beta) <= 64)
+    mx_act = wl.afmt in ("mxfp4_dyn", "mxfp8_dyn")
+    # OCP MX activations run on the f16 kernels when the intermediate is bounded
+    mx_f16 = mx_act and wl.wfmt == "mxfp4" and bounded and not wl.router_weight_on_input
+    if (wl.wfmt == "mxfp4" and (wl.afmt == "bf16" or mx_f16) and wl.act == "swiglu_oai"
             and wl.K % 64 == 0 and wl.N % 64 == 0 and slots <= 32 * wl.El):
         return "stream"
-    if wl.afmt in ("mxfp4_dyn", "mxfp8_dyn"):  # OCP MX activations: generic kernels
+    if mx_act and not mx_f16:
         return "generic"
     return "tc" if slots >= 2048 else "generic"
 
@@ -286,19 +291,21 @@ def launches_per_step(wl, routing=False):
     s2 = moe.stage2_format(wl.wfmt, wl.afmt)
     n = int(routing)                       # fused router
     n += 1                                 # sort / pad (+ zero, + f16 copy of x when streaming)
-    if path == "stream":
-        return n + 3                       # w13, w2, finalize
-    n += wl.afmt != "bf16"                 # stage-1 activation quantiser
+    mx_act = wl.afmt in ("mxfp4_dyn", "mxfp8_dyn")
+    if path == "stream":                   # w13, (MX: intermediate QDQ), w2, finalize
+        return n + 3 + mx_act
+    n += wl.afmt != "bf16" and not (path == "tc" and mx_act)  # stage-1 quantiser (MX on tc: in the gather)
     n += path == "tc"                      # gather of the sorted activation rows
     n += 1                                 # w13 GEMM + activation
     if path == "tc":
-        # the tcgen05 W13 epilogue quantises NVFP4 itself and writes a bounded
-        # SwiGLU-OAI intermediate as f16; fp8 needs a requantiser, other MXFP4
-        # intermediates a per-row f16 rescale
+        # the tcgen05 W13 epilogue quantises NVFP4 and OCP MX itself and writes
+        # a bounded SwiGLU-OAI intermediate as f16; fp8 needs a requantiser,
+        # other MXFP4 w4a16 intermediates a per-row f16 rescale
         mx_direct = (wl.wfmt == "mxfp4" and s2 == "bf16" and wl.act == "swiglu_oai"
                      and 0 < wl.swiglu_limit <= 64 and abs(wl.swiglu_beta) <= 64
                      and not wl.router_weight_on_input)
-        n += s2 not in ("bf16", "nvfp4_dyn") or (wl.wfmt == "mxfp4" and not mx_direct)
+        n += (s2 not in ("bf16", "nvfp4_dyn", "mxfp4_dyn", "mxfp8_dyn")
+              or (wl.wfmt == "mxfp4" and s2 == "bf16" and not mx_direct))
     else:
         n += s2 != "bf16"                  # stage-2 requantiser
     n += 2                                 # w2 GEMM + reduce, bf16 finalize

@@ -68,9 +68,11 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
   if ((int)blockIdx.x > zero_ctas) {
     // conversion CTAs: 128 threads per row of x, 8 rows per CTA; bf16 -> f16
     // scaled by 2^a so that the row maximum lands in [2^14, 2^15) (exact for
-    // bf16 values).  Rows are 16-byte aligned (K % 64 == 0, checked by the
-    // caller); up to 4 x 8 values per thread stay in registers between the
-    // max pass and the convert pass.
+    // bf16 values).  With x_mx the values are first quantised to OCP MXFP4 /
+    // MXFP8 and dequantised (|QDQ(x)| <= 1.75 * 2^floor(log2 max|x|), so the
+    // same 2^a keeps them below 2^15).  Rows are 16-byte aligned (K % 64 == 0,
+    // checked by the caller); up to 4 x 8 values per thread stay in registers
+    // between the max pass and the convert pass.
     __shared__ float red[kAlignThreads / 128][4];
     const int k8 = x.xK / 8;
     const int tr = threadIdx.x & 127, rsub = threadIdx.x >> 7, wr = tr >> 5;
@@ -118,8 +120,20 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
       }
       const float mul = ldexpf(1.0f, a);
       uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(x.x16) + (long)r * x.xK);
+      // the four lanes of a 32-element block (chunk c holds elements 8c..8c+7
+      // and c % 4 == lane % 4) take every convert together
+      const unsigned gmask = 0xFu << (lane & 28);
       auto convert = [&](const uint4 &u) {
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        if (x.x_mx) {  // OCP MX quantise-dequantise of the block, then 2^a
+          float f[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            f[2 * q] = __uint_as_float(w[q] << 16);
+            f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+          }
+          return mx_qdq_f16x8(f, x.x_mx == 1, a, gmask);
+        }
         uint32_t o[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {

@@ -47,6 +47,16 @@ int stage2_afmt(const moe_problem_t *p) {
   }
 }
 
+// MXFP4 weights with OCP MX activations (w4a4 / w4a8) on the f16 kernels: the
+// dequantised activations are exact in f16 after a per-token power of two, and
+// with the bounded SwiGLU-OAI (no router weight folded in) the dequantised
+// intermediate fits f16 as it is.
+bool mx_act_f16(const moe_problem_t *p) {
+  return p->wfmt == W_MXFP4 && (p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN) &&
+         p->act == ACT_SWIGLU_OAI && p->swiglu_limit > 0.f && p->swiglu_limit <= 64.f &&
+         fabsf(p->swiglu_beta) <= 64.f && !p->router_weight_on_input;
+}
+
 bool pair_supported(int wfmt, int afmt) {
   switch (wfmt) {
     case W_BF16: return afmt == A_BF16;
@@ -154,7 +164,8 @@ Layout make_layout(const moe_problem_t *p) {
   L.active = o; o = align_up(o + (size_t)p->num_local_experts * 4);
   L.n_active = o; o = align_up(o + 4);
   L.counters = o; o = align_up(o + 8);
-  if (p->wfmt == W_MXFP4 && p->afmt == A_BF16) {  // f16 copy of x for the streaming kernels
+  const bool f16_x = p->wfmt == W_MXFP4 && (p->afmt == A_BF16 || mx_act_f16(p));
+  if (f16_x) {  // f16 copy of x for the streaming kernels
     L.x16 = o; o = align_up(o + (size_t)p->M * p->K * 2);
     L.x_inv = o; o = align_up(o + (size_t)p->M * 4);
   } else {
@@ -167,14 +178,17 @@ Layout make_layout(const moe_problem_t *p) {
     L.inter_scales = o;
     L.staging = o;
   } else {
-    L.inter = o; o = align_up(o + codes_bytes(s2, L.cap, p->N));
+    // codes, or (MX on the streaming kernels) the f16 of the dequantised rows
+    size_t ib = codes_bytes(s2, L.cap, p->N);
+    if (f16_x && ib < (size_t)L.cap * p->N * 2) ib = (size_t)L.cap * p->N * 2;
+    L.inter = o; o = align_up(o + ib);
     L.inter_scales = o; o = align_up(o + scales_bytes(s2, L.cap, p->N));
     L.staging = o; o = align_up(o + (size_t)L.cap * p->N * 4);
   }
   L.acc = o; o = align_up(o + (size_t)p->M * p->K * 4);
   // split-K W13 of the streaming path (very small batches): fp32 partials per
   // k-range and slot, and one counter per (pass, unit, consumer warp)
-  L.w13_ksplit = (p->wfmt == W_MXFP4 && p->afmt == A_BF16)
+  L.w13_ksplit = f16_x
                      ? stream_w13_ksplit(p->M, p->topk, p->num_local_experts, p->N, p->K, kNominalSms)
                      : 1;
   L.fixcnt_n = 0;
@@ -292,7 +306,7 @@ void timing_collect() {
 
 // The weight-streaming decode path applies (see moe_prepare_weights in the header).
 bool stream_path(const moe_problem_t *p, const moe_weight_t *w13, const moe_weight_t *w2) {
-  return p->wfmt == W_MXFP4 && p->afmt == A_BF16 && w13->packed && w2->packed &&
+  return p->wfmt == W_MXFP4 && (p->afmt == A_BF16 || mx_act_f16(p)) && w13->packed && w2->packed &&
          p->act == ACT_SWIGLU_OAI && p->swiglu_limit > 0.f && p->swiglu_limit <= 64.f &&
          fabsf(p->swiglu_beta) <= 64.f && p->K % 64 == 0 && p->N % 64 == 0 &&
          !(w13->bias && w13->bias_is_f32) && !(w2->bias && w2->bias_is_f32) &&
@@ -538,8 +552,10 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
   const bool streaming = (g_path == MOE_PATH_AUTO || g_path == MOE_PATH_STREAM) &&
                          stream_path(p, w13, w2);
   const bool fp4 = p->wfmt == W_MXFP4 || p->wfmt == W_NVFP4;
-  const bool mx_act = p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN;  // generic kernels only
-  if (!streaming && !mx_act && tc_applies(p) &&
+  // MX activations run on the f16 kernels when bounded, else on the generic ones
+  const bool mx_generic =
+      (p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN) && !mx_act_f16(p);
+  if (!streaming && !mx_generic && tc_applies(p) &&
       (!fp4 || (w13->packed_tc && w2->packed_tc && aligned16(w13->packed_tc) &&
                 aligned16(w2->packed_tc)))) {
     if (ws_bytes < make_tc_layout(p).total) return MOE_ERR_WORKSPACE;
@@ -573,6 +589,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     ex.x_inv = reinterpret_cast<float *>(ws + L.x_inv);
     ex.xM = p->M;
     ex.xK = p->K;
+    ex.x_mx = p->afmt == A_MXFP4_DYN ? 1 : p->afmt == A_MXFP8_DYN ? 2 : 0;
   }
   ex.num_valid_tokens = p->num_local_tokens;
   if (streaming && L.w13_ksplit > 1) {
@@ -611,11 +628,21 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     s13.packed = w13->packed; s13.bias = w13->bias;
     s13.x16 = ex.x16; s13.x_inv = ex.x_inv;
     s13.topk_weights = topk_weights;  // read only with the router weight on the stage-1 output
-    s13.out = ws + L.inter;
+    const bool mx = ex.x_mx != 0;  // MX intermediate: fp32 rows, then quantise-dequantise
+    s13.out = mx ? ws + L.staging : ws + L.inter;
+    s13.out_f32 = mx ? 1 : 0;
     s13.work_counter = ex.counters;
     {
       StageScope sc(MOE_STAGE_W13, st);
       rc = cuda_status(launch_stream(s13, 1, dinfo.sm_count, st));
+      sc.done();
+      if (rc != MOE_OK) return rc;
+    }
+    if (mx) {
+      StageScope sc(MOE_STAGE_REQUANT, st);
+      rc = cuda_status(launch_mx_qdq_rows(reinterpret_cast<const float *>(ws + L.staging), L.cap,
+                                          p->N, sorted, ntp, p->M * p->topk, ws + L.inter,
+                                          ex.x_mx == 1, 0, st, true));
       sc.done();
       if (rc != MOE_OK) return rc;
     }
@@ -822,10 +849,12 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     sc.done();
     if (rc != MOE_OK) return rc;
   }
-  // 2. stage-1 quantisation of x (once per token)
+  // 2. stage-1 quantisation of x (once per token); OCP MX activations are
+  //    quantised and dequantised by the gather itself
+  const bool mx = p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN;
   const void *codes = hidden;
   const void *scales = nullptr;
-  if (p->afmt != A_BF16) {
+  if (p->afmt != A_BF16 && !mx) {
     QuantArgs q;
     memset(&q, 0, sizeof(q));
     q.x = hidden; q.rows = p->M; q.cols = p->K; q.afmt = p->afmt; q.param = p->a1_scale;
@@ -888,6 +917,9 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
       a.out = ws + L.inter;
       a.out_mode = TC_OUT_NVFP4_F16;
       a.out_global = p->a2_scale;
+    } else if (mx) {                // OCP MX quantise-dequantise inside the epilogue
+      a.out = ws + L.inter;
+      a.out_mode = s2 == A_MXFP4_DYN ? TC_OUT_MX4_F16 : TC_OUT_MX8_F16;
     } else if (mx_direct) {         // bounded SwiGLU-OAI intermediate straight to f16
       a.out = ws + L.inter;
       a.out_mode = TC_OUT_F16;
@@ -912,8 +944,8 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     if (rc != MOE_OK) return rc;
   }
   // 5. stage-2 requantisation into exact bf16 values + scales (sorted rows);
-  //    NVFP4 was quantised in the W13 epilogue
-  if (s2 != A_BF16 && s2 != A_NVFP4_DYN) {
+  //    NVFP4 and OCP MX were quantised in the W13 epilogue
+  if (s2 != A_BF16 && s2 != A_NVFP4_DYN && !mx) {
     QuantArgs q;
     memset(&q, 0, sizeof(q));
     q.x = ws + L.staging; q.x_is_f32 = 1; q.rows = L.cap; q.cols = p->N; q.afmt = s2;
@@ -945,7 +977,7 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
         break;
       case A_NVFP4_DYN: a.a_expertscale = p->a2_scale; break;
       default:
-        if (p->wfmt == W_MXFP4 && !mx_direct)
+        if (p->wfmt == W_MXFP4 && !mx_direct && !mx)
           a.a_rowscale = reinterpret_cast<const float *>(ws + L.i_scales);
         break;
     }

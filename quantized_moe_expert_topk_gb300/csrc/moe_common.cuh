@@ -128,6 +128,76 @@ __device__ __forceinline__ uint32_t nvfp4_decode_pair(uint32_t lo, uint32_t hi, 
   return *reinterpret_cast<const uint32_t *>(&h2);
 }
 
+// 2^e as fp32, exact for e in [-126, 127].
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
+// OCP MX shared exponent of a block whose largest magnitude is amax (> 0):
+// floor(log2(amax)) - emax (emax 2 for e2m1, 8 for e4m3), clamped to the e8m0
+// range [-127, 127].  The block's codes are the RNE-saturating conversions of
+// x * 2^-X, an exact scaling (X <= 125 for any finite fp32 amax, so 2^-X is a
+// normal fp32).
+__device__ __forceinline__ int mx_shared_exp(float amax, int emax) {
+  int ex;
+  frexpf(amax, &ex);  // amax = f * 2^ex, 0.5 <= f < 1: floor(log2(amax)) = ex - 1
+  const int X = ex - 1 - emax;
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+
+// Two values of a block with shared exponent X: quantised (x * 2^-X, RNE
+// saturating to e2m1 when fp4, else e4m3), dequantised and multiplied by
+// 2^(X + a), as an f16 pair.  Exact wherever code * 2^(X + a) lies in f16's
+// range (a code has at most 4 significant bits); below 2^-126 the product is
+// far under f16's smallest subnormal and becomes 0.
+__device__ __forceinline__ uint32_t mx_qdq_pair_f16(float v0, float v1, bool fp4, int X, int a) {
+  const float inv = pow2f(-X);
+  const float outs = X + a >= -126 ? pow2f(X + a) : 0.f;
+  float d0, d1;
+  if (fp4) {
+    const uint32_t b = f32x2_to_e2m1x2(v0 * inv, v1 * inv);
+    d0 = e2m1_to_f32(b & 15u);
+    d1 = e2m1_to_f32(b >> 4);
+  } else {
+    d0 = e4m3_to_f32(f32_to_e4m3(v0 * inv));
+    d1 = e4m3_to_f32(f32_to_e4m3(v1 * inv));
+  }
+  const __half2 h = __floats2half2_rn(d0 * outs, d1 * outs);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Eight consecutive values of one 32-element OCP MX block quantised (MXFP4
+// when fp4, else MXFP8) and dequantised, times 2^a, as four packed f16 pairs.
+// The four consecutive lanes named by gmask hold the block's 32 values and
+// call this together; the block maximum is taken across them.  Same decisions
+// as the MX quantiser.
+__device__ __forceinline__ uint4 mx_qdq_f16x8(const float (&v)[8], bool fp4, int a,
+                                              unsigned gmask) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+  uint32_t o[4] = {0u, 0u, 0u, 0u};
+  if (amax > 0.f) {
+    const int X = mx_shared_exp(amax, fp4 ? 2 : 8);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = mx_qdq_pair_f16(v[2 * i], v[2 * i + 1], fp4, X, a);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// A whole 32-element block held by one thread, quantised and dequantised to
+// f16 (no extra power of two); out[i] holds elements 2i, 2i + 1.
+__device__ __forceinline__ void mx_qdq_f16x32(const float (&v)[32], bool fp4,
+                                              uint32_t (&out)[16]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int X = amax > 0.f ? mx_shared_exp(amax, fp4 ? 2 : 8) : 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    out[i] = amax > 0.f ? mx_qdq_pair_f16(v[2 * i], v[2 * i + 1], fp4, X, 0) : 0u;
+}
+
 // ---------------------------------------------------------------- activations
 __device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + expf(-v)); }
 

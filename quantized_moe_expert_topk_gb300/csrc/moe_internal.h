@@ -45,9 +45,10 @@ struct AlignExtras {
   int32_t *n_active = nullptr;    // [1]
   int32_t *counters = nullptr;    // [2] work counters of the streaming kernels, zeroed
   const uint16_t *x = nullptr;    // bf16 [M, K] -> x16 f16 [M, K] scaled per row by 2^a,
-  void *x16 = nullptr;            //   max |x16| in [2^14, 2^15); x_inv[row] = 2^-a
+  void *x16 = nullptr;            //   max |x| in [2^14, 2^15) after scaling; x_inv[row] = 2^-a
   float *x_inv = nullptr;
   int xM = 0, xK = 0;
+  int x_mx = 0;                   // 1 / 2: x16 holds the OCP MXFP4 / MXFP8 dequantised x
   int32_t *zero_ints = nullptr;   // also zeroed (counters of the split W13 units)
   long zero_ints_n = 0;
   const int32_t *num_valid_tokens = nullptr;  // [1]: slots of tokens >= it are dropped
@@ -82,6 +83,16 @@ struct QuantArgs {
   int decoded_f16 = 0;       // the decoded values as f16 instead of bf16 (NVFP4)
 };
 cudaError_t launch_quant(const QuantArgs &a, cudaStream_t stream);
+
+// fp32 intermediate rows -> f16 rows of their OCP MX (MXFP4 when fp4, else
+// MXFP8) quantise-dequantise, no row scale (the caller guarantees the f16
+// range).  With sorted_ids set, rows at or beyond *num_post_pad are skipped
+// and padding rows (sorted id >= S) become zeros (zero_pad) or are skipped;
+// otherwise all `rows` rows are converted.  `dependent`: launched as a
+// programmatic dependent.
+cudaError_t launch_mx_qdq_rows(const float *src, long rows, int N, const int32_t *sorted_ids,
+                               const int32_t *num_post_pad, int S, void *dst, int fp4,
+                               int zero_pad, cudaStream_t stream, bool dependent);
 
 struct GemmArgs {
   int M, K, N, T, El, BM;
@@ -124,7 +135,8 @@ struct StreamArgs {
   const void *x16;                // f16 rows: x [M, K] (w13) or the intermediate [cap, N] (w2)
   const float *x_inv;             // w13: per-token inverse scale of x16
   const int32_t *sorted_ids, *offsets, *counts, *active, *n_active;
-  void *out;                      // w13: f16 intermediate [cap, N]
+  void *out;                      // w13: f16 intermediate [cap, N] (fp32 with out_f32)
+  int out_f32;                    // w13: fp32 rows for a later requantiser
   float *acc;                     // w2: fp32 [M, K]
   const float *topk_weights;
   int w_stage1;                   // router weight on the stage-1 output (W13 multiplies, W2 not)
@@ -158,7 +170,8 @@ cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream
 // separate requantiser follows), f16 rows (bounded SwiGLU-OAI intermediate),
 // or the stage-2 NVFP4 quantisation done in the epilogue, written as the exact
 // f16 values e2m1(code) * e4m3(scale) the W2 kernel consumes.
-enum { TC_OUT_BF16 = 0, TC_OUT_F32 = 1, TC_OUT_F16 = 2, TC_OUT_NVFP4_F16 = 3 };
+enum { TC_OUT_BF16 = 0, TC_OUT_F32 = 1, TC_OUT_F16 = 2, TC_OUT_NVFP4_F16 = 3, TC_OUT_MX4_F16 = 4,
+       TC_OUT_MX8_F16 = 5 };
 struct TcArgs {
   int M, K, N, T, El, R, C;
   int wfmt, act, gate;
@@ -172,7 +185,8 @@ struct TcArgs {
   const int32_t *sorted_ids, *expert_ids, *num_post_pad;
   int S;
   void *out;
-  int out_mode;          // W13 output: TC_OUT_BF16 / _F32 (staging) / _F16 / _NVFP4_F16
+  int out_mode;          // W13 output: TC_OUT_BF16 / _F32 (staging) / _F16 / _NVFP4_F16 /
+                         // _MX4_F16 / _MX8_F16 (OCP MX quantise-dequantise into f16)
   const float *out_global;  // TC_OUT_NVFP4_F16: the stage-2 global per expert [El]
   float *acc;
   const float *topk_weights;

@@ -13,6 +13,7 @@
 //   fp8   scale = fl32(max(amax, 1e-12) / 448);  code = e4m3(fl32(x / scale))
 //   NVFP4 s = e4m3(fl32(fl32(amax / 6) / g));   code = e2m1(fl32(x / fl32(s * g)))
 //         (s == 0 gives zero codes)
+//   OCP MX X = floor(log2 amax) - emax (clamped);  code = RNE-sat(x * 2^-X)
 // All kernels are HBM-bound streaming passes: 16-byte loads, one warp (or
 // thread) per group, codes written with 4- or 8-byte stores.
 #include <cuda_bf16.h>
@@ -20,6 +21,7 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_ptx.cuh"
 
 namespace moe {
 
@@ -225,12 +227,9 @@ __global__ void quant_mx(QuantArgs a) {
   int code_x = 0;  // e8m0 scale code
   float q = 0.f;   // x * 2^-X
   if (amax > 0.f) {
-    int ex;
-    frexpf(amax, &ex);  // amax = f * 2^ex, 0.5 <= f < 1: floor(log2(amax)) = ex - 1
-    int X = ex - 1 - (FP4 ? 2 : 8);
-    X = X < -127 ? -127 : (X > 127 ? 127 : X);
+    const int X = mx_shared_exp(amax, FP4 ? 2 : 8);
     code_x = X + 127;
-    q = ldexpf(v, -X);
+    q = v * pow2f(-X);
   }
   uint8_t *scales = static_cast<uint8_t *>(a.scales);
   if (lane == 0) scales[r * G + g] = (uint8_t)code_x;
@@ -243,6 +242,35 @@ __global__ void quant_mx(QuantArgs a) {
   } else {
     static_cast<uint8_t *>(a.codes)[r * a.cols + g * 32 + lane] = (uint8_t)f32_to_e4m3(q);
   }
+}
+
+// fp32 rows -> f16 of their MX quantise-dequantise.  One thread per chunk of
+// 8 values: chunk c of row r is thread r * N/8 + c, and N/8 % 4 == 0, so the
+// four threads of a 32-element block are four aligned consecutive lanes of
+// one warp and share the row's fate.  zero_pad: padding rows get zeros
+// (else they are skipped, like rows at or beyond *ntp).
+__global__ void mx_qdq_rows_kernel(const float *__restrict__ src, long rows, int N,
+                                   const int32_t *__restrict__ sorted_ids,
+                                   const int32_t *__restrict__ ntp, int S,
+                                   uint16_t *__restrict__ dst, int fp4, int zero_pad) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int n8 = N / 8;
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long r = i / n8;
+  const int c = (int)(i - r * n8);
+  if (r >= rows || (ntp && r >= *ntp)) return;
+  const bool live = !sorted_ids || sorted_ids[r] < S;
+  if (!live && !zero_pad) return;
+  const unsigned gmask = 0xFu << (threadIdx.x & 28);
+  uint4 o = make_uint4(0u, 0u, 0u, 0u);
+  if (live) {
+    const float4 *s4 = reinterpret_cast<const float4 *>(src + r * N) + 2 * c;
+    const float4 u = s4[0], w = s4[1];
+    const float f[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
+    o = mx_qdq_f16x8(f, fp4 != 0, 0, gmask);
+  }
+  reinterpret_cast<uint4 *>(dst + r * N)[c] = o;
 }
 
 template <typename InT>
@@ -285,6 +313,15 @@ cudaError_t launch_quant_t(const QuantArgs &a, cudaStream_t stream) {
 
 cudaError_t launch_quant(const QuantArgs &a, cudaStream_t stream) {
   return a.x_is_f32 ? launch_quant_t<float>(a, stream) : launch_quant_t<uint16_t>(a, stream);
+}
+
+cudaError_t launch_mx_qdq_rows(const float *src, long rows, int N, const int32_t *sorted_ids,
+                               const int32_t *num_post_pad, int S, void *dst, int fp4,
+                               int zero_pad, cudaStream_t stream, bool dependent) {
+  if (rows <= 0) return cudaSuccess;
+  return launch_kernel(mx_qdq_rows_kernel, dim3((unsigned)ceil_div(rows * (N / 8), 256)),
+                       dim3(256), 0, stream, dependent, src, rows, N, sorted_ids, num_post_pad,
+                       S, static_cast<uint16_t *>(dst), fp4, zero_pad);
 }
 
 }  // namespace moe

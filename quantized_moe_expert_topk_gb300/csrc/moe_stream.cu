@@ -433,7 +433,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
             const float gv = gsum + bg;
             const float uv = usum + bu;
             const float z = tok_zw[n][c] * act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit);
-            static_cast<__half *>(a.out)[(long)r * N + j] = __float2half_rn(z);
+            if (a.out_f32)
+              static_cast<float *>(a.out)[(long)r * N + j] = z;
+            else
+              static_cast<__half *>(a.out)[(long)r * N + j] = __float2half_rn(z);
           }
       }
     } else if (MODE == MODE_W2) {

@@ -387,6 +387,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int jbase = nt * 64 + 32 * h;
         if (jbase < a.N) {  // N % 32 == 0: the 32 outputs are all in range or none
           const bool sep = a.gate == GATE_SEPARATED;
+          const bool mx_out = a.out_mode == TC_OUT_MX4_F16 || a.out_mode == TC_OUT_MX8_F16;
+          float zb[32];  // MX: the 32 outputs are one OCP MX block (jbase % 32 == 0)
 #pragma unroll
           for (int p = 0; p < 2; ++p) {  // 16 outputs per pass
             float z[16];
@@ -402,7 +404,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               const float uv = uacc * rf * col_factor(urow) + bias_of(urow);
               z[i] = live ? zw * act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit) : 0.f;
             }
-            if (a.out_mode == TC_OUT_F32) {
+            if (mx_out) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) zb[16 * p + i] = z[i];
+            } else if (a.out_mode == TC_OUT_F32) {
               float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + r * a.N + jbase + 16 * p);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
@@ -435,6 +440,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                     pack_bf16x2(z[8 * i + 4], z[8 * i + 5]),
                                     pack_bf16x2(z[8 * i + 6], z[8 * i + 7]));
             }
+          }
+          if (mx_out) {  // quantise-dequantise the block into exact f16
+            uint32_t w[16];
+            mx_qdq_f16x32(zb, a.out_mode == TC_OUT_MX4_F16, w);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + r * a.N + jbase);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
           }
         }
       } else if (live) {
@@ -484,9 +496,11 @@ __global__ void gather_rows_kernel(GatherArgs g) {
     const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g.codes) + t * g.K);
     for (int c = lane; c < g.K / 8; c += 32)
       reinterpret_cast<uint4 *>(dst)[c] = live ? src[c] : make_uint4(0, 0, 0, 0);
-  } else if (g.afmt == A_BF16) {
+  } else if (g.afmt == A_BF16 || g.afmt == A_MXFP4_DYN || g.afmt == A_MXFP8_DYN) {
     // f16 rows scaled by 2^a so that the row maximum lands in [2^14, 2^15)
-    // (exact for bf16 values); rowscale = 2^-a
+    // (exact for bf16 values); rowscale = 2^-a.  MX formats: g.codes is the
+    // bf16 x and each 32-element block is quantised and dequantised first
+    // (|QDQ(x)| <= 1.75 * 2^floor(log2 max|x|) stays below 2^15 after 2^a).
     const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g.codes) + t * g.K);
     float amax = 0.f;
     for (int c = lane; live && c < g.K / 8; c += 32) {
@@ -505,19 +519,33 @@ __global__ void gather_rows_kernel(GatherArgs g) {
     }
     const float mul = ldexpf(1.0f, a);
     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(g.out) + r * g.K);
+    const int mx = g.afmt == A_MXFP4_DYN ? 1 : g.afmt == A_MXFP8_DYN ? 2 : 0;
+    // chunk c holds elements 8c..8c+7 and c % 4 == lane % 4: the four lanes
+    // of a 32-element block run every iteration together (K % 32 == 0)
+    const unsigned gmask = 0xFu << (lane & 28);
     for (int c = lane; c < g.K / 8; c += 32) {
       uint4 o = make_uint4(0, 0, 0, 0);
       if (live) {
         const uint4 v = src[c];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t q[4];
+        if (mx) {
+          float f[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * mul,
-                                              __uint_as_float(w[i] & 0xffff0000u) * mul);
-          q[i] = *reinterpret_cast<const uint32_t *>(&h);
+          for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+          }
+          o = mx_qdq_f16x8(f, mx == 1, a, gmask);
+        } else {
+          uint32_t q[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * mul,
+                                                __uint_as_float(w[i] & 0xffff0000u) * mul);
+            q[i] = *reinterpret_cast<const uint32_t *>(&h);
+          }
+          o = make_uint4(q[0], q[1], q[2], q[3]);
         }
-        o = make_uint4(q[0], q[1], q[2], q[3]);
       }
       dst[c] = o;
     }

@@ -77,9 +77,33 @@ def test_empty_batch(path):
         moe.moe_set_path("auto")
 
 
+@pytest.mark.parametrize("path", ["stream", "tc", "generic"])
+@pytest.mark.parametrize("afmt", ["mxfp4_dyn", "mxfp8_dyn"])
+def test_mx_activations_each_path(afmt, path):
+    # w4a4 / w4a8 on every kernel family: the f16 kernels (streaming, tcgen05)
+    # take the exact f16 of the quantised-dequantised activations and
+    # intermediate, the generic kernels the codes and e8m0 scales.  The input
+    # spans 2^-12 .. 2^4 across its 32-element blocks, with all-zero blocks
+    # and one all-zero token, so every block gets its own shared exponent.
+    import quantized_moe_expert_topk_gb300 as moe
+    wl = make_custom(M=96, K=512, N=320, E=8, T=2, wfmt="mxfp4", afmt=afmt, act="swiglu_oai",
+                     gate="interleaved", bias=True, seed=zlib.crc32(afmt.encode()) % 1000,
+                     name=f"mx_{afmt}_{path}")
+    g = torch.Generator().manual_seed(5)
+    blk = torch.randint(-12, 5, (wl.M, wl.K // 32), generator=g).float().exp2()
+    blk[torch.rand((wl.M, wl.K // 32), generator=g) < 0.1] = 0.0
+    blk[7] = 0.0
+    wl.x = (wl.x.float() * blk.repeat_interleave(32, dim=1)).to(torch.bfloat16)
+    try:
+        moe.moe_set_path(path)
+        check(wl)
+    finally:
+        moe.moe_set_path("auto")
+
+
 @pytest.mark.parametrize("afmt", ["mxfp4_dyn", "mxfp8_dyn"])
 def test_mx_activations_prefill_size(afmt):
-    # w4a4 / w4a8 at a prefill-sized batch (the generic kernels run them)
+    # w4a4 / w4a8 at a prefill-sized batch (the tcgen05 kernels run them)
     wl = make_custom(M=700, K=512, N=256, E=8, T=4, wfmt="mxfp4", afmt=afmt, act="swiglu_oai",
                      gate="interleaved", bias=True, seed=17, name=f"mx_{afmt}")
     check(wl, sample_tokens(wl))
