@@ -70,7 +70,7 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
     // scaled by 2^a so that the row maximum lands in [2^14, 2^15) (exact for
     // bf16 values).  With x_mx the values are first quantised to OCP MXFP4 /
     // MXFP8 and dequantised (|QDQ(x)| <= 1.75 * 2^floor(log2 max|x|), so the
-    // same 2^a keeps them below 2^15).  Rows are 16-byte aligned (K % 64 == 0,
+    // same 2^a keeps them below 2^15).  Rows are 16-byte aligned (K % 32 == 0,
     // checked by the caller); up to 4 x 8 values per thread stay in registers
     // between the max pass and the convert pass.
     __shared__ float red[kAlignThreads / 128][4];

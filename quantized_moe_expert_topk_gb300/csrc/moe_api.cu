@@ -133,8 +133,9 @@ bool tc_applies(const moe_problem_t *p) {
 // Workspace layout of the tcgen05 path (sort blocks of 128 rows).
 struct TcLayout {
   long cap, blocks;
-  size_t sorted, expert_ids, ntp, counts, a1_codes, a1_scales, a_sorted, a_rowscale,
+  size_t sorted, expert_ids, ntp, counts, x16, x_inv, a1_codes, a1_scales, a_sorted, a_rowscale,
       a_groupscale, inter, staging, i_scales, acc, total;
+  bool f16_x;  // x converted to f16 once per token by the sort (MXFP4 weights)
 };
 
 // Workspace layout of moe_fused_experts.
@@ -213,6 +214,12 @@ TcLayout make_tc_layout(const moe_problem_t *p) {
   L.expert_ids = o; o = align_up(o + (size_t)L.blocks * 4);
   L.ntp = o; o = align_up(o + 4);
   L.counts = o; o = align_up(o + (size_t)p->num_local_experts * 4);
+  L.f16_x = p->wfmt == W_MXFP4 && (p->afmt == A_BF16 || mx_act_f16(p));
+  L.x16 = L.x_inv = o;
+  if (L.f16_x) {
+    L.x16 = o; o = align_up(o + (size_t)p->M * p->K * 2);
+    L.x_inv = o; o = align_up(o + (size_t)p->M * 4);
+  }
   L.a1_codes = o; o = align_up(o + codes_bytes(p->afmt, p->M, p->K));
   L.a1_scales = o; o = align_up(o + scales_bytes(p->afmt, p->M, p->K));
   const bool fp8 = p->wfmt == W_FP8_TENSOR || p->wfmt == W_FP8_CHANNEL ||
@@ -836,12 +843,21 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
   const int S = p->M * p->topk;
   const int s2 = stage2_afmt(p);
 
-  // 1. sort / pad with 128-row blocks (+ zero the accumulator)
+  // 1. sort / pad with 128-row blocks (+ zero the accumulator; MXFP4 weights:
+  //    + the f16 copy of x, quantised and dequantised first for MX activations)
   {
     AlignExtras ex;
     ex.zero_buf = acc;
     ex.zero_n = MK;
     ex.num_valid_tokens = p->num_local_tokens;
+    if (L.f16_x) {
+      ex.x = static_cast<const uint16_t *>(hidden);
+      ex.x16 = ws + L.x16;
+      ex.x_inv = reinterpret_cast<float *>(ws + L.x_inv);
+      ex.xM = p->M;
+      ex.xK = p->K;
+      ex.x_mx = p->afmt == A_MXFP4_DYN ? 1 : p->afmt == A_MXFP8_DYN ? 2 : 0;
+    }
     StageScope sc(MOE_STAGE_ALIGN, st);
     rc = cuda_status(launch_align(topk_ids, p->M, p->topk, expert_map, p->num_experts,
                                   p->num_local_experts, kTcBlockM, sorted, eids, ntp, counts,
@@ -872,6 +888,10 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     g.sorted_ids = sorted; g.num_post_pad = ntp; g.S = S; g.T = p->topk; g.K = p->K;
     g.afmt = p->afmt; g.codes = codes; g.scales = scales;
     g.to_f16 = p->wfmt == W_MXFP4 || p->wfmt == W_NVFP4;
+    if (L.f16_x) {
+      g.x16 = ws + L.x16;
+      g.x_inv = reinterpret_cast<const float *>(ws + L.x_inv);
+    }
     g.out = ws + L.a_sorted;
     g.rowscale = reinterpret_cast<float *>(ws + L.a_rowscale);
     g.groupscale = reinterpret_cast<float *>(ws + L.a_groupscale);

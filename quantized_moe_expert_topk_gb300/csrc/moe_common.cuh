@@ -143,25 +143,45 @@ __device__ __forceinline__ int mx_shared_exp(float amax, int emax) {
   return X < -127 ? -127 : (X > 127 ? 127 : X);
 }
 
+// (lo, hi) fp32 -> two e4m3fn codes (lo in bits 7..0), RNE, saturating.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Exact f16 pairs of two e2m1 codes (one byte, element 0 in bits 3..0) or of
+// two e4m3fn codes (element 0 in bits 7..0), by the hardware converts; the
+// first element lands in the low half.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t b) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+      : "=r"(r) : "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t c) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)c));
+  return r;
+}
+
 // Two values of a block with shared exponent X: quantised (x * 2^-X, RNE
 // saturating to e2m1 when fp4, else e4m3), dequantised and multiplied by
-// 2^(X + a), as an f16 pair.  Exact wherever code * 2^(X + a) lies in f16's
-// range (a code has at most 4 significant bits); below 2^-126 the product is
-// far under f16's smallest subnormal and becomes 0.
+// 2^(X + a), as an f16 pair.  The codes' f16 values are exact and so is
+// their fp32 product with the power of two, so the one rounding is the final
+// convert: exact wherever code * 2^(X + a) lies in f16's range (a code has at
+// most 4 significant bits); below 2^-126 the product is far under f16's
+// smallest subnormal and becomes 0.
 __device__ __forceinline__ uint32_t mx_qdq_pair_f16(float v0, float v1, bool fp4, int X, int a) {
   const float inv = pow2f(-X);
   const float outs = X + a >= -126 ? pow2f(X + a) : 0.f;
-  float d0, d1;
-  if (fp4) {
-    const uint32_t b = f32x2_to_e2m1x2(v0 * inv, v1 * inv);
-    d0 = e2m1_to_f32(b & 15u);
-    d1 = e2m1_to_f32(b >> 4);
-  } else {
-    d0 = e4m3_to_f32(f32_to_e4m3(v0 * inv));
-    d1 = e4m3_to_f32(f32_to_e4m3(v1 * inv));
-  }
-  const __half2 h = __floats2half2_rn(d0 * outs, d1 * outs);
-  return *reinterpret_cast<const uint32_t *>(&h);
+  const uint32_t h = fp4 ? e2m1x2_to_f16x2(f32x2_to_e2m1x2(v0 * inv, v1 * inv))
+                         : e4m3x2_to_f16x2(f32x2_to_e4m3x2(v0 * inv, v1 * inv));
+  const float2 d = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+  const __half2 o = __floats2half2_rn(d.x * outs, d.y * outs);
+  return *reinterpret_cast<const uint32_t *>(&o);
 }
 
 // Eight consecutive values of one 32-element OCP MX block quantised (MXFP4

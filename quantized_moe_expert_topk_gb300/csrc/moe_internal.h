@@ -205,6 +205,10 @@ struct GatherArgs {
   void *out;             // bf16 / f16 rows, or e4m3 codes for fp8 activations
   float *rowscale, *groupscale;
   int to_f16;            // f16 rows (FP4 weights: the f16 tensor-core kind)
+  // when set: the per-token f16 copy of x made by the sort's conversion CTAs
+  // (scaled by 2^a per token, x_inv = 2^-a), copied row by row
+  const void *x16 = nullptr;
+  const float *x_inv = nullptr;
 };
 cudaError_t launch_rescale_rows(const float *src, long cap, int N, const int32_t *sorted_ids,
                                 const int32_t *ntp, int S, void *dst, float *rowscale,

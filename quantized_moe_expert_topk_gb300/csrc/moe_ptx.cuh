@@ -265,14 +265,6 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int m, int n) {
          | ((uint32_t)(m >> 4) << 24);
 }
 
-// Two e4m3 codes (low byte -> low half) -> f16x2, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-  uint32_t r;
-  const uint16_t h = (uint16_t)two_bytes;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
-  return r;
-}
-
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));

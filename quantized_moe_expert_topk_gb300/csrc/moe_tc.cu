@@ -491,7 +491,12 @@ __global__ void gather_rows_kernel(GatherArgs g) {
   const int s = g.sorted_ids[r];
   const bool live = s < g.S;
   const long t = live ? s / g.T : 0;
-  if (g.afmt == A_BF16 && !g.to_f16) {
+  if (g.x16) {  // f16 token rows converted once per token by the sort
+    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(g.out) + r * g.K);
+    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g.x16) + t * g.K);
+    for (int c = lane; c < g.K / 8; c += 32) dst[c] = live ? src[c] : make_uint4(0, 0, 0, 0);
+    if (lane == 0) g.rowscale[r] = live ? g.x_inv[t] : 0.f;
+  } else if (g.afmt == A_BF16 && !g.to_f16) {
     uint16_t *dst = static_cast<uint16_t *>(g.out) + r * g.K;
     const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(g.codes) + t * g.K);
     for (int c = lane; c < g.K / 8; c += 32)
