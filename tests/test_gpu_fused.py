@@ -172,3 +172,17 @@ def test_repeatable_and_no_device_error():
     rms = a.pow(2).mean().sqrt().item()
     assert (a - b).abs().max().item() <= 1e-2 * rms  # fp32 atomics may reorder
     assert moe.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["gptoss20b_w4a4_m64", "gptoss20b_w4a8_m64"])
+def test_gptoss20b_mx_activation_workloads(name):
+    # the w4a4 / w4a8 decode workloads as the bench times them (streaming
+    # kernels), then at a prefill size on the tcgen05 kernels (sampled tokens)
+    check(make_workload(name, device="cuda"))
+    wl = make_workload(name, device="cuda", M=4096)
+    check(wl, sample_tokens(wl, 24, 24))
+
+
+def test_mixtral_bf16_prefill_workload():
+    wl = make_workload("mixtral_bf16_m4096", device="cuda")
+    check(wl, sample_tokens(wl, 24, 24))
