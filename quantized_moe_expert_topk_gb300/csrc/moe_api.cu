@@ -142,7 +142,7 @@ struct TcLayout {
 struct Layout {
   long cap, blocks;
   size_t sorted, expert_ids, ntp, counts, offsets, active, n_active, counters, x16, x_inv, a1_codes,
-      a1_scales, inter, inter_scales, staging, acc, hpart, fixcnt, total;
+      a1_scales, inter, inter_scales, staging, acc, hpart, fixcnt, done13, total;
   int w13_ksplit;  // k-split of the streaming W13 units (1: none)
   long fixcnt_n;   // counters of the split W13 units
 };
@@ -193,6 +193,8 @@ Layout make_layout(const moe_problem_t *p) {
                      ? stream_w13_ksplit(p->M, p->topk, p->num_local_experts, p->N, p->K, kNominalSms)
                      : 1;
   L.fixcnt_n = 0;
+  // completion counts per local expert of the fused W13 + W2 streaming grid
+  L.done13 = o; o = align_up(o + (size_t)p->num_local_experts * 4);
   L.hpart = L.fixcnt = o;
   if (L.w13_ksplit > 1) {
     L.hpart = o; o = align_up(o + (size_t)L.w13_ksplit * p->M * p->topk * p->N * 8);
@@ -599,9 +601,15 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     ex.x_mx = p->afmt == A_MXFP4_DYN ? 1 : p->afmt == A_MXFP8_DYN ? 2 : 0;
   }
   ex.num_valid_tokens = p->num_local_tokens;
+  // W13 and W2 run as one streaming grid unless W13 is split along K or an MX
+  // pass sits between them
+  const bool fused_stream = streaming && L.w13_ksplit == 1 && ex.x_mx == 0;
   if (streaming && L.w13_ksplit > 1) {
     ex.zero_ints = reinterpret_cast<int32_t *>(ws + L.fixcnt);
     ex.zero_ints_n = L.fixcnt_n;
+  } else if (fused_stream) {
+    ex.zero_ints = reinterpret_cast<int32_t *>(ws + L.done13);
+    ex.zero_ints_n = p->num_local_experts;
   }
   std::lock_guard<std::mutex> timing_lock(g_timing_mu);
   {
@@ -639,20 +647,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     s13.out = mx ? ws + L.staging : ws + L.inter;
     s13.out_f32 = mx ? 1 : 0;
     s13.work_counter = ex.counters;
-    {
-      StageScope sc(MOE_STAGE_W13, st);
-      rc = cuda_status(launch_stream(s13, 1, dinfo.sm_count, st));
-      sc.done();
-      if (rc != MOE_OK) return rc;
-    }
-    if (mx) {
-      StageScope sc(MOE_STAGE_REQUANT, st);
-      rc = cuda_status(launch_mx_qdq_rows(reinterpret_cast<const float *>(ws + L.staging), L.cap,
-                                          p->N, sorted, ntp, p->M * p->topk, ws + L.inter,
-                                          ex.x_mx == 1, 0, st, true));
-      sc.done();
-      if (rc != MOE_OK) return rc;
-    }
+    s13.done13 = fused_stream ? reinterpret_cast<int *>(ws + L.done13) : nullptr;
     // 3. down: intermediate x packed w2 -> fp32 accumulator (+ bias, router weight)
     StreamArgs s2 = sa;
     s2.C = p->N;
@@ -672,7 +667,26 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     s2.x16 = ws + L.inter;
     s2.acc = acc; s2.topk_weights = topk_weights;
     s2.work_counter = ex.counters + 1;
-    {
+    if (fused_stream) {  // 2 + 3 in one grid, one work queue
+      StageScope sc(MOE_STAGE_W13, st);
+      rc = cuda_status(launch_stream_fused(s13, s2, dinfo.sm_count, st));
+      sc.done();
+      if (rc != MOE_OK) return rc;
+    } else {
+      StageScope sc(MOE_STAGE_W13, st);
+      rc = cuda_status(launch_stream(s13, 1, dinfo.sm_count, st));
+      sc.done();
+      if (rc != MOE_OK) return rc;
+    }
+    if (mx) {
+      StageScope sc(MOE_STAGE_REQUANT, st);
+      rc = cuda_status(launch_mx_qdq_rows(reinterpret_cast<const float *>(ws + L.staging), L.cap,
+                                          p->N, sorted, ntp, p->M * p->topk, ws + L.inter,
+                                          ex.x_mx == 1, 0, st, true));
+      sc.done();
+      if (rc != MOE_OK) return rc;
+    }
+    if (!fused_stream) {
       StageScope sc(MOE_STAGE_W2, st);
       rc = cuda_status(launch_stream(s2, 0, dinfo.sm_count, st));
       sc.done();

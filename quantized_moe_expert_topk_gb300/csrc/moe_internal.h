@@ -149,6 +149,9 @@ struct StreamArgs {
   float *hpart;
   int *fix_cnt;
   int S;                          // slots (M * T)
+  // fused W13 + W2 grid (launch_stream_fused): per local expert, the count of
+  // (W13 unit, pass, consumer warp) epilogues done; zeroed by the sort
+  int *done13;
 };
 // k-split of the W13 streaming units for this problem (1 = whole K per unit).
 int stream_w13_ksplit(int M, int topk, int El, int N, int K, int sm_count);
@@ -164,6 +167,10 @@ size_t stream_packed_bytes(int w13, int N, int K, int El);
 int stream_units_per_expert(int w13, int N, int K);
 cudaError_t launch_pack_mxfp4(const PackArgs &p, cudaStream_t stream);
 cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream_t stream);
+// W13 and W2 as one persistent grid (W13 units without a k-split): the W2
+// units of an expert wait, bounded, for its W13 units' completion count.
+cudaError_t launch_stream_fused(const StreamArgs &a13, const StreamArgs &a2, int sm_count,
+                                cudaStream_t stream);
 
 // tcgen05 grouped GEMMs (moe_tc.cu)
 // Output of the tcgen05 W13 epilogue: bf16 rows, fp32 staging rows (a

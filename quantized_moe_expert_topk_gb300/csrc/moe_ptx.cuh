@@ -64,6 +64,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   }
 }
 
+// Acquire load of a global counter (gpu scope).
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Waits until the global counter *p reaches `need` (written by other CTAs of
+// the same grid that are already running), for at most `limit_cycles`;
+// returns false on timeout or when the grid-wide error word is set.
+__device__ __forceinline__ bool wait_count_bounded(const int *p, int need, long long limit_cycles,
+                                                   const volatile int *global_err) {
+  if (ld_acquire_gpu(p) >= need) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(p) < need) {
+    if (clock64() - t0 > limit_cycles) return false;
+    if (global_err && *global_err) return false;
+    __nanosleep(256);
+  }
+  return true;
+}
+
 // Programmatic dependent launch.  griddep_wait: the calling thread waits until
 // the grid launched before this one in the stream has completed and its memory
 // is visible (a no-op when this grid was not launched as a dependent).

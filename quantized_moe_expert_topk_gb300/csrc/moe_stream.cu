@@ -60,8 +60,12 @@ constexpr int CTAS_PER_SM = 4;
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int kErrTimeout = 5;
 
-enum { MODE_W13 = 0, MODE_W2 = 1 };
-enum { F_FIRST = 1, F_LAST = 2 };
+// MODE_FUSED: one persistent grid runs the W13 units, then the W2 units, from
+// one work queue (a = W13 arguments, b = W2 arguments); the W2 units of an
+// expert start their intermediate-row copies once every W13 unit of that
+// expert has written its rows (a per-expert completion count).
+enum { MODE_W13 = 0, MODE_W2 = 1, MODE_FUSED = 2 };
+enum { F_FIRST = 1, F_LAST = 2, F_W2 = 4 };  // F_W2: a W2 unit's stage (fused grid)
 
 struct Unit {
   int e, u, kb0, nkb, off, cnt;
@@ -167,8 +171,10 @@ __device__ __forceinline__ void consume_k64(const unsigned char *tp0, uint32_t x
 }
 
 // SPLIT (W13 only): the units are split along K; partials + last-arriver fixup.
+// `b` holds the W2 arguments of the fused grid (unused otherwise).
 template <int MODE, bool SPLIT>
-__global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs a) {
+__global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
+stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ StreamArgs b) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,7 +190,6 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
   __syncthreads();
   volatile int *abort_flag = &sm.abort_flag;
 
-  const int C = a.C;  // reduction length (K for W13, N for W2)
 
   if (warp == CW) {
     // ------------------------------------------------------------ producer
@@ -207,8 +212,11 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
         waited = true;
       }
     };
-    if (MODE == MODE_W13) wait_prior();
-    const int n_units = *a.n_active * a.units_per_expert * a.ksplit;
+    if (MODE != MODE_W2) wait_prior();
+    const int n_active = *a.n_active;
+    const int n13 = MODE == MODE_FUSED ? n_active * a.units_per_expert : 0;  // W13 ids first
+    const int n_units = MODE == MODE_FUSED ? n13 + n_active * b.units_per_expert * b.ksplit
+                                           : n_active * a.units_per_expert * a.ksplit;
     uint32_t it = 0;
     bool ok = true;
     auto acquire_slot = [&](int &slot) -> bool {
@@ -233,17 +241,35 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
         ++it;
         break;
       }
-      const Unit U = decode_unit(a, id);
+      // the unit's phase and the arguments of that phase
+      const bool w2 = MODE == MODE_W2 || (MODE == MODE_FUSED && id >= n13);
+      const bool pb = MODE == MODE_FUSED && w2;  // fields from b
+      const Unit U = pb ? decode_unit(b, id - n13) : decode_unit(a, id);
+      const int C = pb ? b.C : a.C;  // reduction length (K for W13, N for W2)
+      if (pb) {
+        // the intermediate rows of this expert are complete once every W13
+        // unit of it has finished every pass (one count per consumer warp);
+        // those units were claimed earlier by running CTAs
+        const int need = a.units_per_expert * CW * (int)ceil_div(U.cnt, TOKMAX);
+        if (!wait_count_bounded(a.done13 + U.e, need, kWaitCycles, a.err)) {
+          record_device_error(a.err, kErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        fence_proxy_async_global();  // their generic stores before our TMA reads
+      }
       for (int tok0 = 0; tok0 < U.cnt && ok; tok0 += TOKMAX) {
         const int nt = min(TOKMAX, U.cnt - tok0);
         const unsigned char *xrow = nullptr;  // lane n < nt loads token n of this pass
         if (lane < nt) {
           const int r = U.off + tok0 + lane;
-          const long src = MODE == MODE_W13 ? (long)(a.sorted_ids[r] / a.T) : (long)r;
-          xrow = static_cast<const unsigned char *>(a.x16) + src * (long)C * 2;
+          const long src = w2 ? (long)r : (long)(a.sorted_ids[r] / a.T);
+          xrow = static_cast<const unsigned char *>(pb ? b.x16 : a.x16) + src * (long)C * 2;
         }
-        const unsigned char *ubase = static_cast<const unsigned char *>(a.packed) +
-            ((((long)U.e * a.units_per_expert + U.u) * a.kblocks) + U.kb0) * REC_BYTES;
+        const int upe = pb ? b.units_per_expert : a.units_per_expert;
+        const int kblocks = pb ? b.kblocks : a.kblocks;
+        const unsigned char *ubase = static_cast<const unsigned char *>(pb ? b.packed : a.packed) +
+            ((((long)U.e * upe + U.u) * kblocks) + U.kb0) * REC_BYTES;
         for (int kb = 0; kb < U.nkb; kb += S_KB) {
           const int nkb = min(S_KB, U.nkb - kb);
           int slot;
@@ -253,7 +279,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
           const uint32_t xbytes = (uint32_t)nkb * 128;
           if (lane == 0) {
             sm.desc[slot] = StageDesc{id, tok0, kb,
-                                      (kb == 0 ? F_FIRST : 0) | (kb + S_KB >= U.nkb ? F_LAST : 0),
+                                      (kb == 0 ? F_FIRST : 0) | (kb + S_KB >= U.nkb ? F_LAST : 0) |
+                                          (pb ? F_W2 : 0),
                                       U};
             mbar_arrive_expect_tx(&sm.full[slot], wbytes + (uint32_t)nt * xbytes);
             tma_bulk_g2s(ws, ubase + (long)kb * REC_BYTES, wbytes, &sm.full[slot]);
@@ -288,6 +315,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
   int tok_sid[2][2] = {{0, 0}, {0, 0}};      // sorted slot ids of this thread's tokens
   float tok_f[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // W13: x_inv of the token; W2: router weight
   float tok_zw[2][2] = {{1.f, 1.f}, {1.f, 1.f}};  // W13: factor of the stage-1 output
+  bool w2 = MODE == MODE_W2;  // phase of the current unit
   while (true) {
     const int slot = it % NS;
     if (!mbar_wait_bounded(&sm.full[slot], (it / NS) & 1, kWaitCycles, a.err)) {
@@ -311,6 +339,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
       }
       nt = min(TOKMAX, U.cnt - d.tok0);
       ntiles = (nt + 7) >> 3;
+      if (MODE == MODE_FUSED) w2 = (d.flags & F_W2) != 0;
 #pragma unroll
       for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -333,11 +362,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
           const int tn = n * 8 + 2 * t + c;
           // W13: x_inv of the token (times the router weight when it applies to
           // the stage-1 output); W2: the router weight (1 in that case)
-          const float wr = a.w_stage1 ? (MODE == MODE_W13 ? a.topk_weights[tok_sid[n][c]] : 1.f)
-                                      : (MODE == MODE_W13 ? 1.f : a.topk_weights[tok_sid[n][c]]);
-          tok_f[n][c] = tn >= nt ? 0.f
-                        : MODE == MODE_W13 ? a.x_inv[tok_sid[n][c] / a.T] : wr;
-          tok_zw[n][c] = MODE == MODE_W13 && tn < nt ? wr : 1.f;
+          const float wr = a.w_stage1 ? (!w2 ? a.topk_weights[tok_sid[n][c]] : 1.f)
+                                      : (!w2 ? 1.f : a.topk_weights[tok_sid[n][c]]);
+          tok_f[n][c] = tn >= nt ? 0.f : !w2 ? a.x_inv[tok_sid[n][c] / a.T] : wr;
+          tok_zw[n][c] = !w2 && tn < nt ? wr : 1.f;
         }
     }
     const int nkb = min(S_KB, U.nkb - d.kb);
@@ -399,7 +427,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
       finish = __shfl_sync(0xffffffffu, last, 0) != 0;
       if (finish) __threadfence();  // and the others' partials are visible to us
     }
-    if (MODE == MODE_W13 && finish) {
+    if ((MODE == MODE_W13 && finish) || (MODE == MODE_FUSED && !w2)) {
       const int N = a.N;
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
@@ -439,8 +467,16 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
               static_cast<__half *>(a.out)[(long)r * N + j] = __float2half_rn(z);
           }
       }
-    } else if (MODE == MODE_W2) {
-      const int K = a.K;
+      if (MODE == MODE_FUSED) {
+        // this warp's rows of this (unit, pass) are written: count it for the
+        // expert (release: every lane's stores before the count)
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(a.done13 + U.e, 1);
+      }
+    } else if (MODE == MODE_W2 || MODE == MODE_FUSED) {
+      const StreamArgs &w = MODE == MODE_FUSED ? b : a;  // the W2 arguments
+      const int K = w.K;
 #pragma unroll
       for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -448,8 +484,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
           const int i = U.u * ROWS + (warp * MT + m) * 16 + g + 8 * h;
           if (i >= K) continue;
           float bias = 0.f;
-          if (a.bias && U.kb0 == 0)
-            bias = bf16_to_f32(static_cast<const uint16_t *>(a.bias)[(long)U.e * K + i]);
+          if (w.bias && U.kb0 == 0)
+            bias = bf16_to_f32(static_cast<const uint16_t *>(w.bias)[(long)U.e * K + i]);
 #pragma unroll
           for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -458,7 +494,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) stream_kernel(StreamArgs
               if (tn >= nt) continue;
               const int sidx = tok_sid[n][c];
               const float wt = tok_f[n][c];
-              atomicAdd(a.acc + (long)(sidx / a.T) * K + i, wt * (acc[m][n][2 * h + c] + bias));
+              atomicAdd(w.acc + (long)(sidx / w.T) * K + i, wt * (acc[m][n][2 * h + c] + bias));
             }
         }
     }
@@ -558,7 +594,28 @@ cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream
   if (grid > max_units) grid = max_units;
   if (grid <= 0) return cudaSuccess;
   // a programmatic dependent of the previous kernel (the sort, or the W13 grid)
-  return launch_kernel(kern, dim3((unsigned)grid), dim3(THREADS), SMEM_BYTES, stream, true, a);
+  return launch_kernel(kern, dim3((unsigned)grid), dim3(THREADS), SMEM_BYTES, stream, true, a, a);
+}
+
+cudaError_t launch_stream_fused(const StreamArgs &a13, const StreamArgs &a2, int sm_count,
+                                cudaStream_t stream) {
+  if (a13.ksplit != 1 || !a13.done13) return cudaErrorInvalidValue;
+  auto kern = stream_kernel<MODE_FUSED, false>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const long max_units = (long)a13.max_active * a13.units_per_expert +
+                         (long)a2.max_active * a2.units_per_expert * a2.ksplit;
+  long grid = (long)CTAS_PER_SM * sm_count;
+  if (grid > max_units) grid = max_units;
+  if (grid <= 0) return cudaSuccess;
+  // a programmatic dependent of the sort
+  return launch_kernel(kern, dim3((unsigned)grid), dim3(THREADS), SMEM_BYTES, stream, true, a13,
+                       a2);
 }
 
 }  // namespace moe
