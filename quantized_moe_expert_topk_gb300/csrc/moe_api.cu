@@ -601,9 +601,8 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     ex.x_mx = p->afmt == A_MXFP4_DYN ? 1 : p->afmt == A_MXFP8_DYN ? 2 : 0;
   }
   ex.num_valid_tokens = p->num_local_tokens;
-  // W13 and W2 run as one streaming grid unless W13 is split along K or an MX
-  // pass sits between them
-  const bool fused_stream = streaming && L.w13_ksplit == 1 && ex.x_mx == 0;
+  // W13 and W2 run as one streaming grid unless W13 is split along K
+  const bool fused_stream = streaming && L.w13_ksplit == 1;
   if (streaming && L.w13_ksplit > 1) {
     ex.zero_ints = reinterpret_cast<int32_t *>(ws + L.fixcnt);
     ex.zero_ints_n = L.fixcnt_n;
@@ -643,9 +642,12 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     s13.packed = w13->packed; s13.bias = w13->bias;
     s13.x16 = ex.x16; s13.x_inv = ex.x_inv;
     s13.topk_weights = topk_weights;  // read only with the router weight on the stage-1 output
-    const bool mx = ex.x_mx != 0;  // MX intermediate: fp32 rows, then quantise-dequantise
+    // MX intermediate: quantised and dequantised in the fused grid's W13
+    // epilogue, else fp32 rows and a pass of its own
+    const bool mx = ex.x_mx != 0 && !fused_stream;
     s13.out = mx ? ws + L.staging : ws + L.inter;
     s13.out_f32 = mx ? 1 : 0;
+    s13.out_mx = fused_stream ? ex.x_mx : 0;
     s13.work_counter = ex.counters;
     s13.done13 = fused_stream ? reinterpret_cast<int *>(ws + L.done13) : nullptr;
     // 3. down: intermediate x packed w2 -> fp32 accumulator (+ bias, router weight)

@@ -137,6 +137,8 @@ struct StreamArgs {
   const int32_t *sorted_ids, *offsets, *counts, *active, *n_active;
   void *out;                      // w13: f16 intermediate [cap, N] (fp32 with out_f32)
   int out_f32;                    // w13: fp32 rows for a later requantiser
+  int out_mx;                     // w13 in the fused grid: 1 / 2 = OCP MXFP4 / MXFP8
+                                  //   quantise-dequantise of the f16 intermediate
   float *acc;                     // w2: fp32 [M, K]
   const float *topk_weights;
   int w_stage1;                   // router weight on the stage-1 output (W13 multiplies, W2 not)

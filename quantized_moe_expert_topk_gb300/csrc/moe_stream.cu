@@ -86,6 +86,11 @@ struct Smem {
   uint64_t full[NS];
   uint64_t empty[NS];
   StageDesc desc[NS];
+  // MX intermediate (MXQ): per consumer-warp pair, the two warps' per-token
+  // maxima over their 16 outputs of a 32-output block (double-buffered by
+  // epilogue parity) and a barrier of two arrivals
+  uint64_t mx_bar[CW / 2];
+  float mx_amax[2][CW][TOKMAX];
   int abort_flag;
 };
 constexpr size_t SMEM_BYTES = sizeof(Smem);
@@ -172,7 +177,11 @@ __device__ __forceinline__ void consume_k64(const unsigned char *tp0, uint32_t x
 
 // SPLIT (W13 only): the units are split along K; partials + last-arriver fixup.
 // `b` holds the W2 arguments of the fused grid (unused otherwise).
-template <int MODE, bool SPLIT>
+// MXQ (W13 / fused, no split): the W13 epilogue quantises and dequantises the
+// intermediate into OCP MX (a.out_mx: 1 MXFP4, 2 MXFP8) before its f16 store.
+// A 32-output block spans the 16 outputs of two consumer warps (2w, 2w+1),
+// which exchange their per-token maxima through shared memory.
+template <int MODE, bool SPLIT, bool MXQ = false>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
 stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ StreamArgs b) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -184,6 +193,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], CW);
     }
+    for (int q = 0; q < CW / 2; ++q) mbar_init(&sm.mx_bar[q], 2);
     sm.abort_flag = 0;
     mbar_fence_init();
   }
@@ -316,6 +326,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
   float tok_f[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // W13: x_inv of the token; W2: router weight
   float tok_zw[2][2] = {{1.f, 1.f}, {1.f, 1.f}};  // W13: factor of the stage-1 output
   bool w2 = MODE == MODE_W2;  // phase of the current unit
+  uint32_t mx_ep = 0;         // MXQ: epilogues of this warp so far (barrier parity)
   while (true) {
     const int slot = it % NS;
     if (!mbar_wait_bounded(&sm.full[slot], (it / NS) & 1, kWaitCycles, a.err)) {
@@ -430,7 +441,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
     if ((MODE == MODE_W13 && finish) || (MODE == MODE_FUSED && !w2)) {
       const int N = a.N;
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
+      for (int m = 0; m < MT && !MXQ; ++m) {
         const int j = U.u * (TILES * 8) + (warp * MT + m) * 8 + g;
         const long grow = a.gate == GATE_SEPARATED ? j : 2L * j;
         const long urow = a.gate == GATE_SEPARATED ? (long)N + j : 2L * j + 1;
@@ -465,6 +476,69 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
               static_cast<float *>(a.out)[(long)r * N + j] = z;
             else
               static_cast<__half *>(a.out)[(long)r * N + j] = __float2half_rn(z);
+          }
+      }
+      if (MXQ) {
+        // z of output j = (this warp's m-tile m, row g) for token (n, c)
+        auto zval = [&](int m, int n, int c) -> float {
+          const int j = U.u * (TILES * 8) + (warp * MT + m) * 8 + g;
+          const long grow = a.gate == GATE_SEPARATED ? j : 2L * j;
+          const long urow = a.gate == GATE_SEPARATED ? (long)N + j : 2L * j + 1;
+          float bg = 0.f, bu = 0.f;
+          if (a.bias) {
+            const uint16_t *bb = static_cast<const uint16_t *>(a.bias) + (long)U.e * 2 * N;
+            bg = bf16_to_f32(bb[grow]);
+            bu = bf16_to_f32(bb[urow]);
+          }
+          const float xi = tok_f[n][c];
+          return tok_zw[n][c] * act_and_mul(a.act, acc[m][n][c] * xi + bg,
+                                            acc[m][n][2 + c] * xi + bu, a.alpha, a.beta, a.limit);
+        };
+        // per token, the largest |z| of this warp's 16 outputs (the lanes of
+        // one t hold the 8 g rows of both m tiles), then the pair's maximum;
+        // z is computed again for the store rather than held across the wait
+        float pa[2][2];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const bool in = n * 8 + 2 * t + c < nt;
+            float v = in ? fmaxf(fabsf(zval(0, n, c)), fabsf(zval(1, n, c))) : 0.f;
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            pa[n][c] = v;
+          }
+        const int buf = mx_ep & 1;
+        if (g == 0)
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) sm.mx_amax[buf][warp][n * 8 + 2 * t + c] = pa[n][c];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.mx_bar[warp >> 1]);
+        if (!mbar_wait_bounded(&sm.mx_bar[warp >> 1], mx_ep & 1, kWaitCycles, a.err)) {
+          record_device_error(a.err, kErrTimeout);
+          *abort_flag = 1;
+        }
+        if (*abort_flag) return;
+        ++mx_ep;
+        const bool fp4 = a.out_mx == 1;
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int tn = n * 8 + 2 * t + c;
+            if (tn >= nt) continue;
+            const float amax = fmaxf(pa[n][c], sm.mx_amax[buf][warp ^ 1][tn]);
+            uint32_t h = 0u;  // outputs j (m = 0) and j + 8 (m = 1) of this token
+            if (amax > 0.f)
+              h = mx_qdq_pair_f16(zval(0, n, c), zval(1, n, c), fp4,
+                                  mx_shared_exp(amax, fp4 ? 2 : 8), 0);
+            const long r = U.off + tok0 + tn;
+            const int j0 = U.u * (TILES * 8) + warp * MT * 8 + g;
+            uint16_t *dst = static_cast<uint16_t *>(a.out) + r * N;
+            dst[j0] = (uint16_t)(h & 0xffffu);
+            dst[j0 + 8] = (uint16_t)(h >> 16);
           }
       }
       if (MODE == MODE_FUSED) {
@@ -599,14 +673,15 @@ cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream
 
 cudaError_t launch_stream_fused(const StreamArgs &a13, const StreamArgs &a2, int sm_count,
                                 cudaStream_t stream) {
-  if (a13.ksplit != 1 || !a13.done13) return cudaErrorInvalidValue;
-  auto kern = stream_kernel<MODE_FUSED, false>;
-  static bool attr_done = false;
-  if (!attr_done) {
+  if (a13.ksplit != 1 || !a13.done13 || a13.out_f32) return cudaErrorInvalidValue;
+  const int variant = a13.out_mx ? 1 : 0;
+  auto kern = variant ? stream_kernel<MODE_FUSED, false, true> : stream_kernel<MODE_FUSED, false>;
+  static bool attr_done[2] = {false, false};
+  if (!attr_done[variant]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done[variant] = true;
   }
   const long max_units = (long)a13.max_active * a13.units_per_expert +
                          (long)a2.max_active * a2.units_per_expert * a2.ksplit;

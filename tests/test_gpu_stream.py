@@ -81,8 +81,10 @@ MX_CASES = [CASES[0], CASES[3], CASES[5], CASES[9]]
 @pytest.mark.parametrize("case", MX_CASES, ids=[f"case{i}" for i in (0, 3, 5, 9)])
 def test_stream_mx_activations(case, afmt):
     # w4a4 / w4a8 on the streaming kernels: x quantised and dequantised by the
-    # sort's conversion CTAs, the intermediate by a pass between the GEMMs
-    # (no stage-1 quantiser runs), against the oracle and the generic kernels
+    # sort's conversion CTAs (no stage-1 quantiser runs), the intermediate in
+    # the W13 epilogue of the fused grid, or, when W13 is split along K, by a
+    # pass of its own between the two grids; against the oracle and the
+    # generic kernels
     import quantized_moe_expert_topk_gb300 as moe
     wl = make_custom(wfmt="mxfp4", afmt=afmt, act="swiglu_oai", seed=22, name="stream_mx", **case)
     ref = run_oracle(wl, None, to_host(wl))
@@ -93,7 +95,8 @@ def test_stream_mx_activations(case, afmt):
         times, calls = moe.moe_stage_times()
     finally:
         moe.moe_stage_timing(False)
-    assert calls == 1 and times["quant"] == 0.0 and times["requant"] > 0.0, times
+    assert calls == 1 and times["quant"] == 0.0, times
+    assert (times["requant"] > 0.0) == (times["w2"] > 0.0), times  # two grids + pass, or one grid
     out_g = run(wl, False)
     err, tol, _ = compare(wl, out_s, ref)
     assert err <= tol, f"stream: {err:.4e} > {tol:.4e}"
