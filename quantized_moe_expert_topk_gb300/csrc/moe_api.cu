@@ -656,7 +656,9 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     s2.units_per_expert = stream_units_per_expert(0, p->N, p->K);
     s2.kblocks = p->N / 64;
     // split the reduction so that the units keep every CTA busy when few
-    // experts are active (about two units per CTA), at least 8 k64 blocks each
+    // experts are active (about two units per CTA), at least 8 k64 blocks each;
+    // in the fused grid, W2 units that already give every CTA two of them
+    // stay whole (fewer partial sums to add; measured 1-2% faster there)
     {
       const long act = (long)p->M * p->topk < p->num_local_experts ? (long)p->M * p->topk
                                                                    : p->num_local_experts;
@@ -664,6 +666,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
       const long want = ceil_div(2L * 4 * kNominalSms, units > 0 ? units : 1);
       const long cap_split = s2.kblocks / 8 > 1 ? s2.kblocks / 8 : 1;
       s2.ksplit = (int)(want < 2 ? (cap_split >= 2 ? 2 : 1) : (want < cap_split ? want : cap_split));
+      if (fused_stream && units >= 2L * 4 * kNominalSms) s2.ksplit = 1;
     }
     s2.packed = w2->packed; s2.bias = w2->bias;
     s2.x16 = ws + L.inter;
