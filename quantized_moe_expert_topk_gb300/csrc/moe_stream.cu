@@ -1,9 +1,15 @@
 // moe_stream.cu -- weight-streaming grouped GEMMs for decode-sized batches of
-// the MXFP4 w4a16 layer (few tokens per expert; the layer is bound by HBM
-// reads of the weights).  Same contract as the generic kernels
-// ("rocm_aiter_fused_experts" on page "vllm.model_executor.layers.fused_moe.
-// experts.rocm_aiter_moe"; MXFP4 layouts and SwiGLU constants from
+// the MXFP4 layer with bf16 or OCP MX activations (few tokens per expert; the
+// layer is bound by HBM reads of the weights).  Same contract as the generic
+// kernels ("rocm_aiter_fused_experts" on page "vllm.model_executor.layers.
+// fused_moe.experts.rocm_aiter_moe"; MXFP4 layouts and SwiGLU constants from
 // "vLLM/vllm/model_executor/layers/quantization/mxfp4.py").
+//
+// Normally one persistent grid (MODE_FUSED) runs both GEMMs from one work
+// queue: all W13 units, then all W2 units; a W2 unit copies its expert's
+// intermediate rows once that expert's W13 units have counted their
+// epilogues done.  Very small batches split the W13 units along K and run
+// the W13 and W2 grids one after the other.
 //
 // Work unit: (active local expert, tile of 128 weight rows, k-range).  Units
 // are claimed dynamically from a global counter (persistent CTAs, four per
@@ -24,7 +30,8 @@
 //   of that group (two MMAs) into the accumulator.
 // W13 epilogue: x-scale, bias, SwiGLU-OAI of the (gate, up) rows the packed
 // layout pairs inside every m16 tile (rows 0-7 gate, 8-15 up of the same 8
-// outputs), f16 intermediate.  W2 epilogue: bias, router weight, fp32
+// outputs), f16 intermediate (with MX activations quantised and dequantised
+// per 32-output block first).  W2 epilogue: bias, router weight, fp32
 // red.add into the token accumulator (the reduce of TopKWeightAndReduceNoOP).
 //
 // Packed weight layout (moe_prepare_weights, load time, like the pages'
