@@ -1,0 +1,91 @@
+"""CPU checks of bench.py's bookkeeping: which kernel family a workload takes
+(the reported `config.path` and `dtype`), the launch count behind the
+`gpu_launches` claim, and the algorithmic bytes and FLOPs of the roofline."""
+from types import SimpleNamespace
+
+import bench
+from moe_workloads import make_custom
+from moe_workloads.gen import WORKLOADS
+
+
+def shape(name, **override):
+    """The workload's shape and formats without drawing its tensors (the
+    fields the path, dtype and launch bookkeeping read)."""
+    spec = dict(WORKLOADS[name])
+    spec.update(override)
+    E = spec["E"] + spec.get("shared", 0)
+    masked = int(round(spec.get("mask_frac", 0.0) * E)) if spec.get("mask_frac", 0.0) > 0 else 0
+    return SimpleNamespace(name=name, M=spec["M"], K=spec["K"], N=spec["N"], E=E, El=E - masked,
+                           T=spec["T"], wfmt=spec["wfmt"], afmt=spec["afmt"], act=spec["act"],
+                           gate=spec["gate"], swiglu_limit=7.0, swiglu_beta=1.0,
+                           swiglu_alpha=1.702, router_weight_on_input=False)
+
+
+def make_workload(name, **override):
+    return shape(name, **override)
+
+
+def test_kernel_path_of_each_workload():
+    assert bench.kernel_path(make_workload("gptoss20b_mxfp4_m64")) == "stream"
+    assert bench.kernel_path(make_workload("gptoss20b_w4a4_m64")) == "stream"
+    assert bench.kernel_path(make_workload("gptoss20b_w4a8_m64")) == "stream"
+    assert bench.kernel_path(make_workload("tiny_bf16_m16")) == "generic"
+    # prefill sizes take the tcgen05 kernels; the streaming bound is 32 slots per expert
+    assert bench.kernel_path(make_workload("gptoss20b_w4a4_m64", M=4096)) == "tc"
+    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=512)) == "stream"
+    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=2048)) == "tc"
+
+
+def test_mx_activations_without_bounded_swiglu_stay_generic():
+    wl = make_workload("gptoss20b_w4a4_m64")
+    wl.act = "silu"
+    assert bench.kernel_path(wl) == "generic"
+    wl = make_workload("gptoss20b_w4a4_m64")
+    wl.router_weight_on_input = True
+    assert bench.kernel_path(wl) == "generic"
+
+
+def test_mma_dtype():
+    assert bench.mma_dtype(make_workload("gptoss20b_mxfp4_m64")) == "f16"
+    assert bench.mma_dtype(make_workload("gptoss20b_w4a8_m64")) == "f16"
+    assert bench.mma_dtype(make_workload("tiny_bf16_m16")) == "bf16"
+
+
+def test_launches_per_step():
+    c2 = make_workload("gptoss20b_mxfp4_m64")
+    assert bench.launches_per_step(c2, fused=True) == 3          # sort, one grid, finalize
+    assert bench.launches_per_step(c2, fused=False) == 4         # sort, w13, w2, finalize
+    assert bench.launches_per_step(c2, routing=True, fused=True) == 4
+    w4a4 = make_workload("gptoss20b_w4a4_m64")
+    assert bench.launches_per_step(w4a4, fused=True) == 3
+    assert bench.launches_per_step(w4a4, fused=False) == 5       # + the MX pass
+    # tcgen05 MX prefill: sort, gather, w13 (MX epilogue), w2, finalize
+    assert bench.launches_per_step(make_workload("gptoss20b_w4a4_m64", M=4096)) == 5
+    # generic bf16: sort, w13, w2, finalize
+    assert bench.launches_per_step(make_workload("tiny_bf16_m16")) == 4
+
+
+def test_shape_stand_in_matches_a_drawn_workload():
+    wl = make_custom(name="tiny_bf16_m16", **{k: v for k, v in WORKLOADS["tiny_bf16_m16"].items()
+                                              if k != "recipe"})
+    s = shape("tiny_bf16_m16")
+    for f in ("M", "K", "N", "E", "El", "T", "wfmt", "afmt", "act", "gate", "swiglu_limit",
+              "swiglu_beta", "router_weight_on_input"):
+        assert getattr(wl, f) == getattr(s, f), f
+
+
+def test_algorithmic_bytes_and_flops():
+    from moe_workloads import make_workload as draw
+    wl = draw("tiny_bf16_m16")
+    counts = [1] * wl.El  # every expert active, one slot each
+    a = bench.algorithmic(wl, counts)
+    w13 = wl.El * 2 * wl.N * wl.K * 2
+    w2 = wl.El * wl.K * wl.N * 2
+    assert a["w13_bytes"] == w13 and a["w2_bytes"] == w2
+    assert a["layer_bytes"] == w13 + w2 + 4 * wl.M * wl.K + 8 * wl.M * wl.T
+    assert a["fused_kernel_bytes"] == w13 + w2 + 2 * wl.M * wl.K
+    assert a["flops"] == 6.0 * wl.N * wl.K * wl.El
+    # an expert with no slot moves no weight bytes
+    counts[0] = 0
+    b = bench.algorithmic(wl, counts)
+    assert b["w13_bytes"] == w13 * (wl.El - 1) // wl.El
