@@ -278,7 +278,7 @@ def kernel_path(wl):
     # OCP MX activations run on the f16 kernels when the intermediate is bounded
     mx_f16 = mx_act and wl.wfmt == "mxfp4" and bounded and not wl.router_weight_on_input
     if (wl.wfmt == "mxfp4" and (wl.afmt == "bf16" or mx_f16) and wl.act == "swiglu_oai"
-            and wl.K % 64 == 0 and wl.N % 64 == 0 and slots <= 32 * wl.El):
+            and wl.K % 64 == 0 and wl.N % 64 == 0 and slots <= 64 * wl.El):
         return "stream"
     if mx_act and not mx_f16:
         return "generic"

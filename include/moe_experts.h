@@ -164,8 +164,9 @@ long moe_align_capacity(int M, int topk, int num_local_experts, int block_m);
  * per-tile records.  Layouts:
  *   MOE_LAYOUT_STREAM  MXFP4 with K, N multiples of 64 -> moe_weight_t.packed:
  *     the weight-streaming decode kernels, used by moe_fused_experts when both
- *     w13 and w2 carry it, the activations are bf16, the activation is
- *     SwiGLU-OAI with 0 < limit <= 64 and |beta| <= 64, and M*topk <= 32*E_l;
+ *     w13 and w2 carry it, the activations are bf16 (or OCP MX without the
+ *     router weight on the stage-1 output), the activation is SwiGLU-OAI with
+ *     0 < limit <= 64 and |beta| <= 64, and M*topk <= 64*E_l;
  *   MOE_LAYOUT_TC      MXFP4 or NVFP4 -> moe_weight_t.packed_tc: the tcgen05
  *     kernels of those formats (prefill-sized batches).  They decode into
  *     f16, so for MXFP4 every e8m0 exponent must lie in [-21, 13] (checked

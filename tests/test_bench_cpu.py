@@ -30,9 +30,10 @@ def test_kernel_path_of_each_workload():
     assert bench.kernel_path(make_workload("gptoss20b_w4a4_m64")) == "stream"
     assert bench.kernel_path(make_workload("gptoss20b_w4a8_m64")) == "stream"
     assert bench.kernel_path(make_workload("tiny_bf16_m16")) == "generic"
-    # prefill sizes take the tcgen05 kernels; the streaming bound is 32 slots per expert
+    # prefill sizes take the tcgen05 kernels; the streaming bound is 64 slots per expert
     assert bench.kernel_path(make_workload("gptoss20b_w4a4_m64", M=4096)) == "tc"
     assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=512)) == "stream"
+    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=1024)) == "stream"
     assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=2048)) == "tc"
 
 

@@ -148,7 +148,7 @@ def test_gptoss20b_mxfp4_decode_workload():
     check(make_workload("gptoss20b_mxfp4_m64", device="cuda"))
 
 
-@pytest.mark.parametrize("M", [1, 8, 32, 128, 512, 2048, 8192])
+@pytest.mark.parametrize("M", [1, 8, 32, 128, 512, 1024, 2048, 8192])
 def test_gptoss120b_mxfp4_sweep(M):
     wl = make_workload("gptoss120b_mxfp4_ep75", device="cuda", M=M)
     check(wl, sample_tokens(wl) if M > 128 else None)

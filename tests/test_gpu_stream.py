@@ -15,13 +15,13 @@ pytestmark = pytest.mark.gpu
 
 def run(wl, pack):
     """Runs the layer.  With pack (the streaming layout), the batch must be
-    within the streaming kernels' slot bound (M * T <= 32 per local expert),
+    within the streaming kernels' slot bound (M * T <= 64 per local expert),
     so that they are the kernels that run."""
     import quantized_moe_expert_topk_gb300 as moe
     layer = moe.FusedExperts.from_workload(wl, pack=pack)
     if pack:
         assert "packed" in layer.w13
-        assert wl.M * wl.T <= 32 * wl.El, "more slots than the streaming kernels take"
+        assert wl.M * wl.T <= 64 * wl.El, "more slots than the streaming kernels take"
     out = layer(wl.x, wl.topk_ids, wl.topk_weights, wl.expert_map)
     torch.cuda.synchronize()
     return out
