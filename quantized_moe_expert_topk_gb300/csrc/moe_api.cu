@@ -193,13 +193,14 @@ Layout make_layout(const moe_problem_t *p) {
                      ? stream_w13_ksplit(p->M, p->topk, p->num_local_experts, p->N, p->K, kNominalSms)
                      : 1;
   L.fixcnt_n = 0;
-  // completion counts per local expert of the fused W13 + W2 streaming grid
+  // completion counts per local expert of the fused W13 + W2 streaming grid,
+  // then the split W13 units' counters: one range for the sort to zero
   L.done13 = o; o = align_up(o + (size_t)p->num_local_experts * 4);
   L.hpart = L.fixcnt = o;
   if (L.w13_ksplit > 1) {
-    L.hpart = o; o = align_up(o + (size_t)L.w13_ksplit * p->M * p->topk * p->N * 8);
     L.fixcnt_n = stream_w13_fixups(L.cap, p->N);
     L.fixcnt = o; o = align_up(o + (size_t)L.fixcnt_n * 4);
+    L.hpart = o; o = align_up(o + (size_t)L.w13_ksplit * p->M * p->topk * p->N * 8);
   }
   L.total = o;
   return L;
@@ -604,14 +605,12 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     ex.x_mx = p->afmt == A_MXFP4_DYN ? 1 : p->afmt == A_MXFP8_DYN ? 2 : 0;
   }
   ex.num_valid_tokens = p->num_local_tokens;
-  // W13 and W2 run as one streaming grid unless W13 is split along K
-  const bool fused_stream = streaming && L.w13_ksplit == 1;
-  if (streaming && L.w13_ksplit > 1) {
-    ex.zero_ints = reinterpret_cast<int32_t *>(ws + L.fixcnt);
-    ex.zero_ints_n = L.fixcnt_n;
-  } else if (fused_stream) {
+  // W13 and W2 run as one streaming grid, except for MX activations with W13
+  // split along K (the MX epilogue needs a whole block in one CTA)
+  const bool fused_stream = streaming && (L.w13_ksplit == 1 || ex.x_mx == 0);
+  if (streaming) {  // the completion counts and the split counters, one range
     ex.zero_ints = reinterpret_cast<int32_t *>(ws + L.done13);
-    ex.zero_ints_n = p->num_local_experts;
+    ex.zero_ints_n = (long)((L.fixcnt - L.done13) / 4) + L.fixcnt_n;
   }
   std::lock_guard<std::mutex> timing_lock(g_timing_mu);
   {

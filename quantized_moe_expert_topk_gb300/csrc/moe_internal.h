@@ -169,8 +169,9 @@ size_t stream_packed_bytes(int w13, int N, int K, int El);
 int stream_units_per_expert(int w13, int N, int K);
 cudaError_t launch_pack_mxfp4(const PackArgs &p, cudaStream_t stream);
 cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream_t stream);
-// W13 and W2 as one persistent grid (W13 units without a k-split): the W2
-// units of an expert wait, bounded, for its W13 units' completion count.
+// W13 and W2 as one persistent grid: the W2 units of an expert wait, bounded,
+// for its W13 units' completion count.  W13 may be split along K (not with
+// the MX epilogue).
 cudaError_t launch_stream_fused(const StreamArgs &a13, const StreamArgs &a2, int sm_count,
                                 cudaStream_t stream);
 

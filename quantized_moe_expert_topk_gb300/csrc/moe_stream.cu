@@ -5,11 +5,11 @@
 // fused_moe.experts.rocm_aiter_moe"; MXFP4 layouts and SwiGLU constants from
 // "vLLM/vllm/model_executor/layers/quantization/mxfp4.py").
 //
-// Normally one persistent grid (MODE_FUSED) runs both GEMMs from one work
-// queue: all W13 units, then all W2 units; a W2 unit copies its expert's
-// intermediate rows once that expert's W13 units have counted their
-// epilogues done.  Very small batches split the W13 units along K and run
-// the W13 and W2 grids one after the other.
+// One persistent grid (MODE_FUSED) runs both GEMMs from one work queue: all
+// W13 units, then all W2 units; a W2 unit copies its expert's intermediate
+// rows once that expert's W13 units have counted their epilogues done.  Very
+// small batches split the W13 units along K (partials + last-arriver fixup);
+// with MX activations those run the W13 and W2 grids one after the other.
 //
 // Work unit: (active local expert, tile of 128 weight rows, k-range).  Units
 // are claimed dynamically from a global counter (persistent CTAs, four per
@@ -182,7 +182,7 @@ __device__ __forceinline__ void consume_k64(const unsigned char *tp0, uint32_t x
   }
 }
 
-// SPLIT (W13 only): the units are split along K; partials + last-arriver fixup.
+// SPLIT (W13 / fused): the W13 units are split along K; partials + last-arriver fixup.
 // `b` holds the W2 arguments of the fused grid (unused otherwise).
 // MXQ (W13 / fused, no split): the W13 epilogue quantises and dequantises the
 // intermediate into OCP MX (a.out_mx: 1 MXFP4, 2 MXFP8) before its f16 store.
@@ -231,7 +231,8 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
     };
     if (MODE != MODE_W2) wait_prior();
     const int n_active = *a.n_active;
-    const int n13 = MODE == MODE_FUSED ? n_active * a.units_per_expert : 0;  // W13 ids first
+    const int n13 =  // W13 ids first
+        MODE == MODE_FUSED ? n_active * a.units_per_expert * (SPLIT ? a.ksplit : 1) : 0;
     const int n_units = MODE == MODE_FUSED ? n13 + n_active * b.units_per_expert * b.ksplit
                                            : n_active * a.units_per_expert * a.ksplit;
     uint32_t it = 0;
@@ -265,8 +266,9 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
       const int C = pb ? b.C : a.C;  // reduction length (K for W13, N for W2)
       if (pb) {
         // the intermediate rows of this expert are complete once every W13
-        // unit of it has finished every pass (one count per consumer warp);
-        // those units were claimed earlier by running CTAs
+        // unit of it has finished every pass (one count per consumer warp,
+        // from the warp that applies the epilogue: with a k-split, the last
+        // arrival); those units were claimed earlier by running CTAs
         const int need = a.units_per_expert * CW * (int)ceil_div(U.cnt, TOKMAX);
         if (!wait_count_bounded(a.done13 + U.e, need, kWaitCycles, a.err)) {
           record_device_error(a.err, kErrTimeout);
@@ -414,7 +416,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
     // -------------------------------------------------------------- epilogue
     const int tok0 = d.tok0;
     bool finish = true;  // this warp applies the activation (W13)
-    if (MODE == MODE_W13 && SPLIT) {
+    if ((MODE == MODE_W13 || (MODE == MODE_FUSED && !w2)) && SPLIT) {
       // k-split: write this k-range's (gate, up) partials, already scaled by
       // the token's x_inv; the last of the ksplit arrivals for this (unit,
       // pass, warp) sums them below (no waiting: the others just move on)
@@ -445,7 +447,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
       finish = __shfl_sync(0xffffffffu, last, 0) != 0;
       if (finish) __threadfence();  // and the others' partials are visible to us
     }
-    if ((MODE == MODE_W13 && finish) || (MODE == MODE_FUSED && !w2)) {
+    if ((MODE == MODE_W13 || (MODE == MODE_FUSED && !w2)) && finish) {
       const int N = a.N;
 #pragma unroll
       for (int m = 0; m < MT && !MXQ; ++m) {
@@ -555,7 +557,9 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
         __syncwarp();
         if (lane == 0) atomicAdd(a.done13 + U.e, 1);
       }
-    } else if (MODE == MODE_W2 || MODE == MODE_FUSED) {
+    } else if (MODE == MODE_W2 || (MODE == MODE_FUSED && (!SPLIT || w2))) {
+      // (a W13 warp of a split unit that left the fixup to another arrival
+      // has nothing to do here)
       const StreamArgs &w = MODE == MODE_FUSED ? b : a;  // the W2 arguments
       const int K = w.K;
 #pragma unroll
@@ -680,17 +684,20 @@ cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream
 
 cudaError_t launch_stream_fused(const StreamArgs &a13, const StreamArgs &a2, int sm_count,
                                 cudaStream_t stream) {
-  if (a13.ksplit != 1 || !a13.done13 || a13.out_f32) return cudaErrorInvalidValue;
-  const int variant = a13.out_mx ? 1 : 0;
-  auto kern = variant ? stream_kernel<MODE_FUSED, false, true> : stream_kernel<MODE_FUSED, false>;
-  static bool attr_done[2] = {false, false};
+  // the MX epilogue exchanges block maxima inside one CTA: no k-split with it
+  if (!a13.done13 || a13.out_f32 || (a13.out_mx && a13.ksplit != 1)) return cudaErrorInvalidValue;
+  const int variant = a13.out_mx ? 1 : a13.ksplit > 1 ? 2 : 0;
+  auto kern = variant == 1   ? stream_kernel<MODE_FUSED, false, true>
+              : variant == 2 ? stream_kernel<MODE_FUSED, true>
+                             : stream_kernel<MODE_FUSED, false>;
+  static bool attr_done[3] = {false, false, false};
   if (!attr_done[variant]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done[variant] = true;
   }
-  const long max_units = (long)a13.max_active * a13.units_per_expert +
+  const long max_units = (long)a13.max_active * a13.units_per_expert * a13.ksplit +
                          (long)a2.max_active * a2.units_per_expert * a2.ksplit;
   long grid = (long)CTAS_PER_SM * sm_count;
   if (grid > max_units) grid = max_units;
