@@ -358,7 +358,7 @@ int run_w13(const moe_problem_t *p, const void *a_codes, const void *a_scales,
   int rc = cuda_status(launch_gemm_w13(g, cap, st));
   sc13.done();
   if (rc != MOE_OK || s2 == A_BF16) return rc;
-  QuantArgs q;
+  QuantArgs q{};
   q.x = staging; q.x_is_f32 = 1; q.rows = cap; q.cols = p->N; q.afmt = s2;
   q.param = p->a2_scale; q.sorted_ids = sorted; q.expert_ids = eids; q.num_post_pad = ntp;
   q.S = p->M * p->topk; q.BM = kGenericBlockM; q.codes = inter; q.scales = inter_scales;
@@ -486,8 +486,7 @@ int moe_quant_act(const void *x_bf16, int rows, int cols, int afmt, const float 
   if (rows == 0) return MOE_OK;
   if (!x_bf16 || !aligned16(x_bf16) || !codes || !scales || !aligned16(codes) || !aligned16(scales))
     return MOE_ERR_INVALID_ARG;
-  QuantArgs q;
-  memset(&q, 0, sizeof(q));
+  QuantArgs q{};  // every field zero / its default
   q.x = x_bf16; q.x_is_f32 = 0; q.rows = rows; q.cols = cols; q.afmt = afmt; q.param = scale_in;
   q.codes = codes; q.scales = scales; q.BM = 1;
   return cuda_status(launch_quant(q, static_cast<cudaStream_t>(stream)));
@@ -712,8 +711,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
   const void *a_codes = hidden_bf16;
   const void *a_scales = nullptr;
   if (p->afmt != A_BF16) {
-    QuantArgs q;
-    memset(&q, 0, sizeof(q));
+    QuantArgs q{};  // every field zero / its default
     q.x = hidden_bf16; q.rows = p->M; q.cols = p->K; q.afmt = p->afmt; q.param = p->a1_scale;
     q.codes = ws + L.a1_codes; q.scales = ws + L.a1_scales; q.BM = 1;
     StageScope sc(MOE_STAGE_QUANT, st);
@@ -892,8 +890,7 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
   const void *codes = hidden;
   const void *scales = nullptr;
   if (p->afmt != A_BF16 && !mx) {
-    QuantArgs q;
-    memset(&q, 0, sizeof(q));
+    QuantArgs q{};  // every field zero / its default
     q.x = hidden; q.rows = p->M; q.cols = p->K; q.afmt = p->afmt; q.param = p->a1_scale;
     q.codes = ws + L.a1_codes; q.scales = ws + L.a1_scales; q.BM = 1;
     StageScope sc(MOE_STAGE_QUANT, st);
@@ -987,8 +984,7 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
   // 5. stage-2 requantisation into exact bf16 values + scales (sorted rows);
   //    NVFP4 and OCP MX were quantised in the W13 epilogue
   if (s2 != A_BF16 && s2 != A_NVFP4_DYN && !mx) {
-    QuantArgs q;
-    memset(&q, 0, sizeof(q));
+    QuantArgs q{};  // every field zero / its default
     q.x = ws + L.staging; q.x_is_f32 = 1; q.rows = L.cap; q.cols = p->N; q.afmt = s2;
     q.param = p->a2_scale; q.sorted_ids = sorted; q.expert_ids = eids; q.num_post_pad = ntp;
     q.S = S; q.BM = kTcBlockM; q.scales = ws + L.i_scales;
