@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 7
+#define MOE_ABI_VERSION 8
 
 typedef enum {
   MOE_OK = 0,
@@ -323,6 +323,15 @@ int moe_stage_times(double *ms_out, int *calls_out);
  * (call after synchronising the streams that ran the kernels). */
 int moe_get_device_error(int *err_out);
 int moe_reset_device_error(void);
+
+/* Self-test of the failure detection (no part of the computation): enqueues
+ * on `stream` one CTA that waits on a shared-memory barrier nothing completes,
+ * with the same bounded wait every pipeline of this library uses, for
+ * limit_cycles SM clock cycles (1 <= limit_cycles < 2^40).  When the limit runs
+ * out the kernel records MOE_ERR_TIMEOUT in the device error word and returns;
+ * the context stays usable.  Returns MOE_ERR_INVALID_ARG (nothing launched)
+ * for a limit out of range. */
+int moe_selftest_bounded_wait(long long limit_cycles, void *stream);
 
 #ifdef __cplusplus
 }

@@ -15,7 +15,7 @@ from ._binding import (ACT, AFMT, BLOCK_M, EXPORTS, GATE, LIB_PATH, WFMT, FusedE
                        moe_set_path, moe_get_path, PATHS, moe_route_topk, SCORING,
                        moe_get_device_error, moe_grouped_gemm_w2_reduce,
                        moe_grouped_gemm_w13_act, moe_quant_act, moe_reset_device_error,
-                       moe_w13_workspace_size, moe_workspace_size, stage2_format, status_str)
+                       moe_selftest_bounded_wait, moe_w13_workspace_size, moe_workspace_size, stage2_format, status_str)
 
 __all__ = [
     "ACT", "AFMT", "BLOCK_M", "EXPORTS", "GATE", "LIB_PATH", "WFMT", "FusedExperts", "MoEError",
@@ -26,6 +26,6 @@ __all__ = [
     "moe_get_path", "PATHS", "moe_route_topk", "SCORING",
     "moe_get_device_error",
     "moe_grouped_gemm_w2_reduce", "moe_grouped_gemm_w13_act", "moe_quant_act",
-    "moe_reset_device_error", "moe_w13_workspace_size", "moe_workspace_size", "stage2_format",
+    "moe_reset_device_error", "moe_selftest_bounded_wait", "moe_w13_workspace_size", "moe_workspace_size", "stage2_format",
     "status_str",
 ]

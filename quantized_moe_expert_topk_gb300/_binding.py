@@ -29,7 +29,8 @@ BLOCK_M = 64
 EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align_capacity",
            "moe_align_block_size", "moe_quant_act", "moe_w13_workspace_size",
            "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_reduce", "moe_fused_experts",
-           "moe_get_device_error", "moe_reset_device_error", "moe_noalloc_scratch_bytes",
+           "moe_get_device_error", "moe_reset_device_error", "moe_selftest_bounded_wait",
+           "moe_noalloc_scratch_bytes",
            "moe_fused_experts_noalloc", "moe_packed_weight_bytes", "moe_prepare_weights",
            "moe_stage_timing", "moe_stage_times", "moe_set_path", "moe_get_path",
            "moe_route_topk")
@@ -88,6 +89,7 @@ def lib() -> ctypes.CDLL:
         "moe_fused_experts": (i, [P, p, W, W, p, p, p, p, sz, p, p]),
         "moe_get_device_error": (i, [ctypes.POINTER(ctypes.c_int)]),
         "moe_reset_device_error": (i, []),
+        "moe_selftest_bounded_wait": (i, [ctypes.c_longlong, ctypes.c_void_p]),
         "moe_noalloc_scratch_bytes": (sz, []),
         "moe_fused_experts_noalloc": (i, [P, p, W, W, p, p, p, p, p]),
         "moe_packed_weight_bytes": (sz, [P, i, i]),
@@ -290,6 +292,13 @@ def moe_get_device_error() -> int:
 
 def moe_reset_device_error():
     _check("moe_reset_device_error", lib().moe_reset_device_error())
+
+
+def moe_selftest_bounded_wait(limit_cycles: int, stream=None):
+    """Enqueue the failure-detection self-test: a bounded wait that runs out
+    after `limit_cycles` SM cycles and records MOE_ERR_TIMEOUT (5)."""
+    _check("moe_selftest_bounded_wait",
+           lib().moe_selftest_bounded_wait(int(limit_cycles), _stream(stream)))
 
 
 # ------------------------------------------------------------------- convenience

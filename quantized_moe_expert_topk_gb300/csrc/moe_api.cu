@@ -842,6 +842,14 @@ int moe_reset_device_error(void) {
   return cuda_status(cudaMemcpyToSymbol(moe::g_device_error_word, &zero, sizeof(int)));
 }
 
+int moe_selftest_bounded_wait(long long limit_cycles, void *stream) {
+  if (limit_cycles < 1 || limit_cycles >= (1LL << 40)) return MOE_ERR_INVALID_ARG;
+  DeviceInfo dinfo;
+  int rc = device_info(&dinfo);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(launch_selftest_wait(dinfo.err, limit_cycles, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 namespace {

@@ -84,6 +84,10 @@ struct QuantArgs {
 };
 cudaError_t launch_quant(const QuantArgs &a, cudaStream_t stream);
 
+// Failure-detection self-test (moe_selftest.cu): one bounded wait that runs
+// out and records MOE_ERR_TIMEOUT in *err.
+cudaError_t launch_selftest_wait(int *err, long long limit_cycles, cudaStream_t stream);
+
 // fp32 intermediate rows -> f16 rows of their OCP MX (MXFP4 when fp4, else
 // MXFP8) quantise-dequantise, no row scale (the caller guarantees the f16
 // range).  With sorted_ids set, rows at or beyond *num_post_pad are skipped

@@ -35,7 +35,7 @@ def test_header_symbols_are_exported(moe):
     L = moe.lib()
     for name in declared:
         assert hasattr(L, name), name
-    assert moe.moe_abi_version() == 7
+    assert moe.moe_abi_version() == 8
 
 
 def test_status_strings(moe):
@@ -135,3 +135,10 @@ def test_route_validation(moe):
     assert L.moe_route_topk(fake, 0, 4, 64, 9, 0, 1, 8, 1, None, f1, fake, fake, None) == 1
     assert L.moe_route_topk(None, 0, 4, 64, 4, 0, 1, 0, 0, None, f1, fake, fake, None) == 1
     assert L.moe_route_topk(None, 0, 0, 64, 4, 0, 1, 0, 0, None, f1, None, None, None) == 0
+
+
+def test_selftest_validation(moe):
+    # out-of-range limits are rejected on the host, nothing is launched
+    L = moe.lib()
+    for bad in (0, -5, 1 << 40):
+        assert L.moe_selftest_bounded_wait(ctypes.c_longlong(bad), None) == 1
