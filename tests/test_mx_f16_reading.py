@@ -1,9 +1,12 @@
 """The reading that lets the f16 kernels take OCP MX activations: the
 quantise-dequantise (QDQ) of a bf16 row, times the power of two 2^a that puts
 the row's largest |x| in [2^14, 2^15), is exactly representable in f16 and
-stays below 2^15, except for blocks more than about 2^24 below the row's
-largest value; and the QDQ of a bounded SwiGLU-OAI intermediate fits f16 as it
-is.  Checked with the oracle's QDQ (fp64) and numpy's float16, no GPU."""
+stays below 2^15, for every block whose largest value is within 2^21 (MXFP8)
+or 2^35 (MXFP4) of the row's (the smallest code of such a block, times its
+scale and 2^a, is still a multiple of f16's subnormal step 2^-24); further
+below, a block's smallest values may round.  And the QDQ of a bounded
+SwiGLU-OAI intermediate fits f16 as it is.  Checked with the oracle's QDQ
+(fp64) and numpy's float16, no GPU."""
 import numpy as np
 import pytest
 
@@ -52,12 +55,28 @@ def test_qdq_of_bounded_swiglu_intermediate_fits_f16(fmt):
 
 
 def test_the_stated_tail_is_where_exactness_ends():
-    # a block 2^-30 below the row's largest value falls under f16's subnormal
-    # range after the row's power of two: the tail the reading excludes
+    # a block 2^-40 below the row's largest value falls under f16's subnormal
+    # step after the row's power of two: the tail the reading excludes
     x = np.zeros((1, 64), np.float32)
     x[0, :32] = 3.0
-    x[0, 32:] = np.float32(3.0 * 2.0 ** -30) * np.linspace(0.5, 1.0, 32, dtype=np.float32)
+    x[0, 32:] = np.float32(3.0 * 2.0 ** -40) * np.linspace(0.5, 1.0, 32, dtype=np.float32)
     q = oracle.qdq_rows(x, "mxfp8_dyn", None)
     _, ex = np.frexp(3.0)
     v = q[0] * np.exp2(15 - int(ex))
     assert _f16_exact(v[:32]) and not _f16_exact(v[32:])
+
+
+@pytest.mark.parametrize("fmt,rel", [("mxfp8_dyn", 21), ("mxfp4_dyn", 35)])
+def test_exact_up_to_the_stated_distance(fmt, rel):
+    # a block whose largest value is 2^-rel of the row's, holding values down
+    # to 2^-12 of its own maximum (so its smallest codes occur): still exact
+    rng = np.random.default_rng(rel)
+    for _ in range(50):
+        x = np.zeros((1, 64), np.float32)
+        x[0, :32] = np.float32(1.999)
+        b = rng.uniform(-1, 1, 32) * np.exp2(rng.uniform(-12, 0, 32))
+        b[0] = 1.0
+        x[0, 32:] = (b * 1.999 * 2.0 ** -rel).astype(np.float32)
+        q = oracle.qdq_rows(x, fmt, None)
+        _, ex = np.frexp(np.abs(x).max())
+        assert _f16_exact(q[0] * np.exp2(15 - int(ex)))
