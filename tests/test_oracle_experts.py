@@ -320,3 +320,36 @@ def test_single_expert_dequant_layouts(wfmt):
     z = F.silu(torch.from_numpy(h[:, :N])) * torch.from_numpy(h[:, N:])
     zq = oracle.qdq_rows(z.numpy().astype(np.float32), s2, param)
     np.testing.assert_allclose(out, 0.5 * (zq @ W2.T), rtol=1e-11, atol=1e-13)
+
+
+def test_static_per_tensor_fp8_uses_each_stage_own_scale():
+    # FP8 per-tensor weights with static activation scales: stage 1 quantises
+    # x with a1_scale, stage 2 quantises z with a2_scale (distinct values here,
+    # so swapping them, or quantising stage 2 dynamically, changes the result)
+    rng = np.random.default_rng(23)
+    K = N = 32
+    x = torch.from_numpy(rng.normal(0, 1, (1, K)).astype(np.float32)).to(torch.bfloat16)
+
+    def make(R, C):
+        codes = rng.integers(0, 256, (1, R, C)).astype(np.uint8)
+        codes[(codes & 0x7F) == 0x7F] = 0x38  # no NaN codes
+        return {"codes": codes, "scales": np.array([0.125], np.float32)}, decode_e4m3(codes[0]) * 0.125
+
+    w13, W13 = make(2 * N, K)
+    w2, W2 = make(K, N)
+    a1 = np.array([0.02], np.float32)
+    a2 = np.array([0.5], np.float32)
+    p = prob(1, K, N, 1, 1, wfmt="fp8_tensor", afmt="fp8_tensor_static", act="silu",
+             a1_scale=a1, a2_scale=a2)
+    ids, tw = np.zeros((1, 1), np.int32), np.array([[0.75]], np.float32)
+    out = oracle.fused_experts(p, bits_of(x), w13, w2, ids, tw)
+    a = oracle.qdq_rows(x.float().numpy(), "fp8_tensor_static", a1)
+    h = a @ W13.T
+    z = F.silu(torch.from_numpy(h[:, :N])) * torch.from_numpy(h[:, N:])
+    zq = oracle.qdq_rows(z.numpy().astype(np.float32), "fp8_tensor_static", a2)
+    np.testing.assert_allclose(out, 0.75 * (zq @ W2.T), rtol=1e-11, atol=1e-13)
+    # and the static rule itself: code = e4m3(x / s), value = code * s
+    s = float(a1[0])
+    xf = x.float().numpy()[0]
+    ref = torch.from_numpy((xf / np.float32(s)).astype(np.float32)).to(torch.float8_e4m3fn)
+    np.testing.assert_array_equal(a[0], ref.double().numpy() * s)
