@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 8
+#define MOE_ABI_VERSION 9
 
 typedef enum {
   MOE_OK = 0,
@@ -66,8 +66,9 @@ typedef enum {
  *   BF16 + BF16; FP8_TENSOR + FP8_TENSOR_STATIC | FP8_TENSOR_DYN;
  *   FP8_CHANNEL + FP8_TOKEN_DYN; FP8_BLOCK128 + FP8_GROUP128_DYN;
  *   MXFP4 + BF16 (w4a16), MXFP4 + MXFP4_DYN (w4a4), MXFP4 + MXFP8_DYN (w4a8)
- *   (AiterMxfp4Experts: "MXFP4 weights with a bf16 or MXFP4-dynamic
- *   activation"; MXFP4 x MXFP8 as named by the mxfp4.py backends);
+ *   (AiterMxfp4Experts takes MXFP4 weights with bf16 or dynamically
+ *   MXFP4-quantised activations; MXFP4 x MXFP8 as named by the mxfp4.py
+ *   backends);
  *   NVFP4 + NVFP4_DYN.
  * The intermediate (stage-2 input) uses the same scheme: per-tensor static
  * (a2_scale) or dynamic, per-token dynamic, 1x128 dynamic, NVFP4 x16 dynamic
@@ -126,8 +127,9 @@ typedef struct {
   const float *a1_scale;  /* device: FP8_TENSOR_STATIC stage-1 scale [1]; NVFP4 stage-1 global [1] */
   const float *a2_scale;  /* device: FP8_TENSOR_STATIC stage-2 scale [1]; NVFP4 stage-2 global [E_l] */
   /* apply_router_weight_on_input (doweight_stage1 of rocm_aiter_fused_experts;
-   * the tkw1 path of AiterFp8ChannelExperts "applies topk_weights to FC1's
-   * output instead of FC2's"): 1 = the router weight multiplies the stage-1
+   * the tkw1 path of AiterFp8ChannelExperts on the rocm_aiter_moe page moves
+   * the router-weight multiply from the second GEMM's output to the first's):
+   * 1 = the router weight multiplies the stage-1
    * output, z' = w * act(g, u), before the stage-2 quantiser, and the stage-2
    * reduce is unweighted: out[t] = sum_k (W2 z'_k + b2).  Requires topk == 1
    * (_assert_topk1_for_router_weight_on_input); honoured by moe_fused_experts
@@ -141,7 +143,18 @@ typedef struct {
    * NULL = all M tokens.  Read by moe_fused_experts (and _noalloc); not with
    * MOE_A_FP8_TENSOR_DYN (its batch scale would cover the padding rows). */
   const int32_t *num_local_tokens;
+  /* Kernel family of this problem (moe_path; a tuning and testing aid, read
+   * per call, no process-wide state).  MOE_PATH_AUTO (0, the value of a
+   * zero-initialised struct): the weight-streaming decode kernels when their
+   * conditions hold (see moe_prepare_weights), else the tcgen05 kernels when
+   * M*topk >= 2048 (FP4 formats need MOE_LAYOUT_TC packed weights), else the
+   * generic mma.sync kernels.  GENERIC, STREAM (falls back to GENERIC where
+   * it does not apply) and TC force a family.  moe_workspace_size depends on
+   * it. */
+  int path;
 } moe_problem_t;
+
+enum { MOE_PATH_AUTO = 0, MOE_PATH_GENERIC = 1, MOE_PATH_STREAM = 2, MOE_PATH_TC = 3 };
 
 /* Library / ABI identification. */
 int moe_abi_version(void);
@@ -285,31 +298,23 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
  * moe_noalloc_scratch_bytes() bytes (32 MiB) that each GPU loading the library
  * holds until exit.  Problems needing more (moe_workspace_size) return
  * MOE_ERR_WORKSPACE.  The first call on a device looks up the array's address
- * (cudaGetSymbolAddress) and should come before any stream capture.  All calls
- * on a device share the array: calls that overlap on the GPU race, so order
- * them on one stream.  Allocates nothing. */
+ * (cudaGetSymbolAddress) and should come before any stream capture; that
+ * address is kept for the life of the process, so a process using this entry
+ * point must not call cudaDeviceReset (the array would be loaded again
+ * elsewhere).  All calls on a device share the array: calls that overlap on
+ * the GPU race, so order them on one stream.  Allocates nothing. */
 size_t moe_noalloc_scratch_bytes(void);
 int moe_fused_experts_noalloc(const moe_problem_t *p, const void *hidden_bf16,
                               const moe_weight_t *w13, const moe_weight_t *w2,
                               const int32_t *topk_ids, const float *topk_weights,
                               const int32_t *expert_map, void *out_bf16, void *stream);
 
-/* Execution-path control of moe_fused_experts (process-wide; a tuning and
- * testing aid).  AUTO (default): the weight-streaming decode kernels when
- * their conditions hold (see moe_prepare_weights), else the tcgen05 kernels
- * when M*topk >= 2048 (FP4 formats need MOE_LAYOUT_TC packed weights), else
- * the generic mma.sync kernels.  GENERIC, STREAM
- * (falls back to GENERIC where it does not apply) and TC force a path.  Set
- * it before sizing the workspace: moe_workspace_size depends on it. */
-enum { MOE_PATH_AUTO = 0, MOE_PATH_GENERIC = 1, MOE_PATH_STREAM = 2, MOE_PATH_TC = 3 };
-int moe_set_path(int path);
-int moe_get_path(void);
-
 /* Per-stage timing of moe_fused_experts (a profiling aid).  While enabled,
  * every moe_fused_experts call records a CUDA event pair around each of its
  * kernel launches on the call's stream, waits for the last event before
  * returning (the call becomes synchronous), and adds each launch's elapsed
- * time to the accumulator of its stage.  moe_stage_timing(1) enables and
+ * time to the accumulator of its stage; timed calls are serialised by one
+ * process-wide lock.  While disabled (the default) calls take no lock.  moe_stage_timing(1) enables and
  * resets, moe_stage_timing(0) disables; moe_stage_times copies the
  * accumulated milliseconds [MOE_NUM_STAGES] and the number of timed calls.
  * Not for use inside stream capture. */

@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.orc_qdq_rows.restype = i; L.orc_qdq_rows.argtypes = [p, l, l, i, p, i, p]
         L.orc_fused_experts.restype = i
         L.orc_fused_experts.argtypes = [p, p, p, p, p, p, p, p, i, p]
+        L.orc_fused_experts_x.restype = i
+        L.orc_fused_experts_x.argtypes = [p, p, p, p, p, p, p, p, i, p, p, p]
         _lib = L
     return _lib
 
@@ -252,12 +254,18 @@ def _weight(w: dict, keep: list):
 
 
 def fused_experts(prob: dict, x_bits, w13: dict, w2: dict, topk_ids, topk_weights,
-                  expert_map=None, tokens=None) -> np.ndarray:
+                  expert_map=None, tokens=None, round_to_bf16: bool = False,
+                  intermediate: bool = False):
     """fp64 output rows [len(tokens), K] of the fused experts (before bf16 rounding).
 
     prob: M K N T E El wfmt afmt act gate [swiglu_alpha swiglu_beta swiglu_limit a1_scale a2_scale]
     w13/w2: dict(codes=, scales=, global_scale=, bias=) in the canonical layouts
-    (bf16 arrays as uint16 bit patterns)."""
+    (bf16 arrays as uint16 bit patterns).
+    round_to_bf16: return the layer's bf16 output instead (each value rounded
+    to nearest-even bf16, the last step of the computation), still as fp64.
+    intermediate: also return (z_pre, z_post), [len(tokens) * T, N] fp64: the
+    stage-1 output of slot k of tokens[i] in row i*T + k, before and after the
+    stage-2 quantise-dequantise (rows of dropped slots are zero)."""
     keep = []
     x = _c(x_bits, np.uint16); keep.append(x)
     ids = _c(topk_ids, np.int32); keep.append(ids)
@@ -280,12 +288,21 @@ def fused_experts(prob: dict, x_bits, w13: dict, w2: dict, topk_ids, topk_weight
     W13 = _weight(w13, keep)
     W2 = _weight(w2, keep)
     out = np.zeros((len(tok), prob["K"]), np.float64)
-    rc = lib().orc_fused_experts(ctypes.byref(P), _ptr(x), ctypes.byref(W13), ctypes.byref(W2),
-                                 _ptr(ids), _ptr(tw), _ptr(em), _ptr(tok), len(tok), _ptr(out))
+    z_pre = z_post = None
+    if intermediate:
+        z_pre = np.zeros((len(tok) * prob["T"], prob["N"]), np.float64)
+        z_post = np.zeros_like(z_pre)
+    rc = lib().orc_fused_experts_x(ctypes.byref(P), _ptr(x), ctypes.byref(W13), ctypes.byref(W2),
+                                   _ptr(ids), _ptr(tw), _ptr(em), _ptr(tok), len(tok), _ptr(out),
+                                   _ptr(z_pre), _ptr(z_post))
     if rc == -1:
         raise ValueError("oracle: per-tensor dynamic stage-2 needs every token")
     if rc == -3:
         raise ValueError("oracle: the router weight on the stage-1 output needs topk == 1")
     if rc != 0:
         raise ValueError("oracle: a scale the format needs is missing")
+    if round_to_bf16:
+        out = bf16_values(bf16_bits(out))
+    if intermediate:
+        return out, z_pre, z_post
     return out

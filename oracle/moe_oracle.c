@@ -617,11 +617,15 @@ static int stage2_afmt(const orc_problem *p) {
 /* Computes out[n_tokens, K] (fp64, before the final bf16 rounding) for the
  * listed tokens.  Returns 0, or -1 for an unsupported request (per-tensor
  * dynamic stage-2 needs every token, because its scale spans all slots). */
-int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
-                      const orc_weight *w13, const orc_weight *w2,
-                      const int32_t *topk_ids, const float *topk_weights,
-                      const int32_t *expert_map, const int32_t *tokens,
-                      int n_tokens, double *out) {
+/* The fused experts of the requested tokens.  When z_pre / z_post are given
+ * ([n_tokens * T, N] each, zeroed here), row i*T + k receives the stage-1
+ * output of slot k of tokens[i] before and after the stage-2 quantiser (the
+ * same values step 4 computes; dropped slots stay zero). */
+int orc_fused_experts_x(const orc_problem *p, const uint16_t *x_bf16,
+                        const orc_weight *w13, const orc_weight *w2,
+                        const int32_t *topk_ids, const float *topk_weights,
+                        const int32_t *expert_map, const int32_t *tokens,
+                        int n_tokens, double *out, double *z_pre, double *z_post) {
   const long M = p->M, K = p->K, N = p->N, T = p->T;
   const int s2 = stage2_afmt(p);
   if (s2 == ORC_A_FP8_TENSOR_DYN && n_tokens != M) return -1;
@@ -656,6 +660,7 @@ int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
   /* 2. live slots of the requested tokens. */
   long ns = 0;
   long *slot_tok = (long *)malloc(sizeof(long) * n_tokens * T + 1);
+  long *slot_row = (long *)malloc(sizeof(long) * n_tokens * T + 1);
   int *slot_exp = (int *)malloc(sizeof(int) * n_tokens * T + 1);
   double *slot_w = (double *)malloc(sizeof(double) * n_tokens * T + 1);
   for (long i = 0; i < n_tokens; ++i)
@@ -665,6 +670,7 @@ int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
       int l = local_expert(topk_ids[t * T + k], expert_map, p->E, p->El);
       if (l < 0) continue;
       slot_tok[ns] = i;
+      slot_row[ns] = i * T + k;
       slot_exp[ns] = l;
       slot_w[ns] = (double)topk_weights[t * T + k];
       ++ns;
@@ -707,6 +713,10 @@ int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
        * (before the stage-2 quantiser) instead of the stage-2 output */
       if (p->weight_on_stage1) z[s * N + j] *= slot_w[s];
     }
+  if (z_pre) {
+    memset(z_pre, 0, sizeof(double) * n_tokens * T * N);
+    for (long s = 0; s < ns; ++s) memcpy(z_pre + slot_row[s] * N, z + s * N, sizeof(double) * N);
+  }
   if (s2 != ORC_A_BF16 && ns > 0) {
     float *zf = (float *)malloc(sizeof(float) * ns * N);
     for (long i = 0; i < ns * N; ++i) zf[i] = (float)z[i];
@@ -719,6 +729,11 @@ int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
       orc_qdq_rows(zf, ns, N, s2, p->a2_scale, 0, z);
     }
     free(zf);
+  }
+
+  if (z_post) {
+    memset(z_post, 0, sizeof(double) * n_tokens * T * N);
+    for (long s = 0; s < ns; ++s) memcpy(z_post + slot_row[s] * N, z + s * N, sizeof(double) * N);
   }
 
   /* 5. down GEMM and the top-k weighted reduce. */
@@ -746,6 +761,15 @@ int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
     }
   }
 
-  free(a); free(slot_tok); free(slot_exp); free(slot_w); free(h); free(z);
+  free(a); free(slot_tok); free(slot_row); free(slot_exp); free(slot_w); free(h); free(z);
   return 0;
+}
+
+int orc_fused_experts(const orc_problem *p, const uint16_t *x_bf16,
+                      const orc_weight *w13, const orc_weight *w2,
+                      const int32_t *topk_ids, const float *topk_weights,
+                      const int32_t *expert_map, const int32_t *tokens,
+                      int n_tokens, double *out) {
+  return orc_fused_experts_x(p, x_bf16, w13, w2, topk_ids, topk_weights, expert_map, tokens,
+                             n_tokens, out, NULL, NULL);
 }

@@ -32,8 +32,7 @@ EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align
            "moe_get_device_error", "moe_reset_device_error", "moe_selftest_bounded_wait",
            "moe_noalloc_scratch_bytes",
            "moe_fused_experts_noalloc", "moe_packed_weight_bytes", "moe_prepare_weights",
-           "moe_stage_timing", "moe_stage_times", "moe_set_path", "moe_get_path",
-           "moe_route_topk")
+           "moe_stage_timing", "moe_stage_times", "moe_route_topk")
 PATHS = {"auto": 0, "generic": 1, "stream": 2, "tc": 3}
 STAGES = ("align", "quant", "w13", "requant", "w2", "finalize")
 
@@ -52,7 +51,7 @@ class Problem(ctypes.Structure):
                 ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
                 ("swiglu_limit", ctypes.c_float), ("a1_scale", ctypes.c_void_p),
                 ("a2_scale", ctypes.c_void_p), ("router_weight_on_input", ctypes.c_int),
-                ("num_local_tokens", ctypes.c_void_p)]
+                ("num_local_tokens", ctypes.c_void_p), ("path", ctypes.c_int)]
 
 
 class Weight(ctypes.Structure):
@@ -95,8 +94,6 @@ def lib() -> ctypes.CDLL:
         "moe_packed_weight_bytes": (sz, [P, i, i]),
         "moe_prepare_weights": (i, [P, i, i, W, p, p]),
         "moe_stage_timing": (i, [i]),
-        "moe_set_path": (i, [i]),
-        "moe_get_path": (i, []),
         "moe_stage_times": (i, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -129,12 +126,13 @@ def _check(fn, rc):
 
 def make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha=1.702,
                  swiglu_beta=1.0, swiglu_limit=7.0, a1_scale=None, a2_scale=None,
-                 router_weight_on_input=False, num_local_tokens=None) -> Problem:
+                 router_weight_on_input=False, num_local_tokens=None, path="auto") -> Problem:
     """num_local_tokens: optional device int32 [1] tensor, the number of valid
-    tokens (read on the device at every call)."""
+    tokens (read on the device at every call).  path: kernel family of this
+    problem ("auto", "generic", "stream", "tc")."""
     return Problem(M, K, N, topk, E, El, WFMT[wfmt], AFMT[afmt], ACT[act], GATE[gate],
                    swiglu_alpha, swiglu_beta, swiglu_limit, _ptr(a1_scale), _ptr(a2_scale),
-                   int(bool(router_weight_on_input)), _ptr(num_local_tokens))
+                   int(bool(router_weight_on_input)), _ptr(num_local_tokens), PATHS[path])
 
 
 def make_weight(w: dict) -> Weight:
@@ -260,17 +258,6 @@ def moe_prepare_weights(prob: Problem, which: int, w: dict, packed, layout: str 
         _stream(stream)))
 
 
-def moe_set_path(path: str):
-    """Force an execution path of moe_fused_experts ("auto", "generic",
-    "stream", "tc"); set it before sizing workspaces."""
-    _check("moe_set_path", lib().moe_set_path(PATHS[path]))
-
-
-def moe_get_path() -> str:
-    v = lib().moe_get_path()
-    return {i: k for k, i in PATHS.items()}[v]
-
-
 def moe_stage_timing(enable: bool):
     """Enable (and reset) or disable per-stage CUDA-event timing of moe_fused_experts."""
     _check("moe_stage_timing", lib().moe_stage_timing(int(enable)))
@@ -309,10 +296,10 @@ class FusedExperts:
     def __init__(self, M, K, N, topk, E, El, wfmt, afmt, act, gate, w13: dict, w2: dict,
                  a1_scale=None, a2_scale=None, swiglu_alpha=1.702, swiglu_beta=1.0,
                  swiglu_limit=7.0, device="cuda", pack=True, router_weight_on_input=False,
-                 num_local_tokens=None):
+                 num_local_tokens=None, path="auto"):
         self.prob = make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha,
                                  swiglu_beta, swiglu_limit, a1_scale, a2_scale,
-                                 router_weight_on_input, num_local_tokens)
+                                 router_weight_on_input, num_local_tokens, path)
         self._keep = (a1_scale, a2_scale, num_local_tokens)
         self.w13, self.w2 = dict(w13), dict(w2)
         # load-time repacks (weight-streaming decode kernels: MXFP4 with K, N

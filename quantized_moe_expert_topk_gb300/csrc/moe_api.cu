@@ -15,6 +15,7 @@
 
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/moe_experts.h"
@@ -95,7 +96,7 @@ int validate_problem(const moe_problem_t *p) {
     return MOE_ERR_INVALID_ARG;
   if (p->wfmt < W_BF16 || p->wfmt > W_NVFP4 || p->afmt < A_BF16 || p->afmt > A_MXFP8_DYN ||
       p->act < ACT_SILU || p->act > ACT_SWIGLU_OAI || p->gate < GATE_SEPARATED ||
-      p->gate > GATE_INTERLEAVED)
+      p->gate > GATE_INTERLEAVED || p->path < MOE_PATH_AUTO || p->path > MOE_PATH_TC)
     return MOE_ERR_INVALID_ARG;
   if (!pair_supported(p->wfmt, p->afmt)) return MOE_ERR_UNSUPPORTED;
   if (p->num_local_experts > 1024) return MOE_ERR_UNSUPPORTED;
@@ -120,14 +121,13 @@ int validate_weight(const moe_problem_t *p, const moe_weight_t *w) {
   return MOE_OK;
 }
 
-// ---- execution path (moe_set_path)
-int g_path = MOE_PATH_AUTO;
+// ---- execution path (moe_problem_t.path)
 constexpr long kTcMinSlots = 2048;  // slots from which the tcgen05 path is used
 
 // The tcgen05 prefill path handles this problem (workspace sized for it).
 bool tc_applies(const moe_problem_t *p) {
-  if (g_path == MOE_PATH_TC) return true;
-  return g_path == MOE_PATH_AUTO && (long)p->M * p->topk >= kTcMinSlots;
+  if (p->path == MOE_PATH_TC) return true;
+  return p->path == MOE_PATH_AUTO && (long)p->M * p->topk >= kTcMinSlots;
 }
 
 // Workspace layout of the tcgen05 path (sort blocks of 128 rows).
@@ -274,6 +274,10 @@ int device_info(DeviceInfo *out) {
 }
 
 // ---- per-stage timing (moe_stage_timing): events around each launch
+// Stage timing is a profiling aid: while it is on, calls take g_timing_mu for
+// their whole duration (their events and accumulators are shared).  While it
+// is off, no call touches the lock or the shared state, so host threads that
+// feed different streams run concurrently.
 struct StageTiming {
   bool on = false;
   int device = -1;
@@ -284,25 +288,11 @@ struct StageTiming {
 };
 std::mutex g_timing_mu;
 StageTiming g_timing;
-
-struct StageScope {  // records the start event now and the stop event on done()
-  cudaStream_t st;
-  int stage;
-  bool on;
-  StageScope(int stage_, cudaStream_t st_) : st(st_), stage(stage_), on(g_timing.on) {
-    if (on) {
-      cudaEventRecord(g_timing.ev[stage][0], st);
-      g_timing.used[stage] = true;
-    }
-  }
-  void done() {
-    if (on) cudaEventRecord(g_timing.ev[stage][1], st);
-  }
-};
+std::atomic<bool> g_timing_on{false};
+thread_local bool t_timing = false;  // this thread's call is being timed
 
 // Adds the elapsed time of every stage launched by the finished call.
 void timing_collect() {
-  if (!g_timing.on) return;
   for (int s = 0; s < MOE_NUM_STAGES; ++s) {
     if (!g_timing.used[s]) continue;
     float ms = 0.f;
@@ -313,6 +303,39 @@ void timing_collect() {
   }
   g_timing.calls += 1;
 }
+
+// One timed call: holds the timing lock (only while timing is on) from the
+// first launch to the collection of its events.
+struct TimedCall {
+  std::unique_lock<std::mutex> lk;
+  bool active = false;
+  TimedCall() {
+    if (g_timing_on.load(std::memory_order_acquire)) {
+      lk = std::unique_lock<std::mutex>(g_timing_mu);
+      active = g_timing.on;
+    }
+    t_timing = active;
+  }
+  ~TimedCall() {
+    if (active) timing_collect();
+    t_timing = false;
+  }
+};
+
+struct StageScope {  // records the start event now and the stop event on done()
+  cudaStream_t st;
+  int stage;
+  bool on;
+  StageScope(int stage_, cudaStream_t st_) : st(st_), stage(stage_), on(t_timing) {
+    if (on) {
+      cudaEventRecord(g_timing.ev[stage][0], st);
+      g_timing.used[stage] = true;
+    }
+  }
+  void done() {
+    if (on) cudaEventRecord(g_timing.ev[stage][1], st);
+  }
+};
 
 // The weight-streaming decode path applies (see moe_prepare_weights in the header).
 bool stream_path(const moe_problem_t *p, const moe_weight_t *w13, const moe_weight_t *w2) {
@@ -430,14 +453,6 @@ size_t moe_workspace_size(const moe_problem_t *p) {
   }
   return n;
 }
-
-int moe_set_path(int path) {
-  if (path < MOE_PATH_AUTO || path > MOE_PATH_TC) return MOE_ERR_INVALID_ARG;
-  g_path = path;
-  return MOE_OK;
-}
-
-int moe_get_path(void) { return g_path; }
 
 int moe_align_block_size(const int32_t *topk_ids, int M, int topk, const int32_t *expert_map,
                          int num_experts, int num_local_experts, int block_m,
@@ -561,7 +576,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
-  const bool streaming = (g_path == MOE_PATH_AUTO || g_path == MOE_PATH_STREAM) &&
+  const bool streaming = (p->path == MOE_PATH_AUTO || p->path == MOE_PATH_STREAM) &&
                          stream_path(p, w13, w2);
   const bool fp4 = p->wfmt == W_MXFP4 || p->wfmt == W_NVFP4;
   // MX activations run on the f16 kernels when bounded, else on the generic ones
@@ -571,10 +586,9 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
       (!fp4 || (w13->packed_tc && w2->packed_tc && aligned16(w13->packed_tc) &&
                 aligned16(w2->packed_tc)))) {
     if (ws_bytes < make_tc_layout(p).total) return MOE_ERR_WORKSPACE;
-    std::lock_guard<std::mutex> timing_lock(g_timing_mu);
-    rc = run_tc_path(p, hidden_bf16, w13, w2, topk_ids, topk_weights, expert_map, ws, out_bf16, st);
-    timing_collect();
-    return rc;
+    TimedCall timed;
+    return run_tc_path(p, hidden_bf16, w13, w2, topk_ids, topk_weights, expert_map, ws, out_bf16,
+                       st);
   }
   int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
   int32_t *eids = reinterpret_cast<int32_t *>(ws + L.expert_ids);
@@ -611,7 +625,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     ex.zero_ints = reinterpret_cast<int32_t *>(ws + L.done13);
     ex.zero_ints_n = (long)((L.fixcnt - L.done13) / 4) + L.fixcnt_n;
   }
-  std::lock_guard<std::mutex> timing_lock(g_timing_mu);
+  TimedCall timed;
   {
     StageScope sc(MOE_STAGE_ALIGN, st);
     rc = cuda_status(launch_align(topk_ids, p->M, p->topk, expert_map, p->num_experts,
@@ -704,7 +718,6 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
       rc = cuda_status(launch_finalize(acc, MK, out_bf16, st, true));
       sc.done();
     }
-    timing_collect();
     return rc;
   }
   // 2. stage-1 activation quantisation
@@ -726,10 +739,8 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
                     ws + L.inter_scales, ws + L.staging, L.cap, st)) != MOE_OK)
     return rc;
   // 4. down GEMM + weighted reduce + bf16 output
-  rc = run_w2(p, ws + L.inter, ws + L.inter_scales, w2, topk_weights, sorted, eids, ntp, acc,
-              out_bf16, L.cap, st);
-  timing_collect();
-  return rc;
+  return run_w2(p, ws + L.inter, ws + L.inter_scales, w2, topk_weights, sorted, eids, ntp, acc,
+                out_bf16, L.cap, st);
 }
 
 size_t moe_packed_weight_bytes(const moe_problem_t *p, int which, int layout) {
@@ -821,6 +832,7 @@ int moe_stage_timing(int enable) {
     g_timing.calls = 0;
   }
   g_timing.on = enable != 0;
+  g_timing_on.store(g_timing.on, std::memory_order_release);
   return MOE_OK;
 }
 

@@ -16,7 +16,10 @@
 //    rejected with MOE_ERR_WORKSPACE before anything is launched.
 //  - The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (with that device current) and caches it; make that
-//    first call before any stream capture on the device.
+//    first call before any stream capture on the device.  The cached address
+//    belongs to the device's primary context: do not call cudaDeviceReset (or
+//    otherwise tear that context down) in a process that uses this entry
+//    point, since the array would be loaded again at another address.
 //  - Every call on a device shares the one array and it keeps the last
 //    call's contents.  Calls that overlap on the GPU (different streams, no
 //    ordering between them) race on it; serialise them.  What must start at

@@ -24,9 +24,9 @@ def to_device(wl, dev="cuda"):
     return wl
 
 
-def run_gpu(wl):
+def run_gpu(wl, path="auto"):
     import quantized_moe_expert_topk_gb300 as moe
-    layer = moe.FusedExperts.from_workload(wl)
+    layer = moe.FusedExperts.from_workload(wl, path=path)
     out = layer(wl.x, wl.topk_ids, wl.topk_weights, wl.expert_map)
     torch.cuda.synchronize()
     return out
@@ -41,10 +41,10 @@ def sample_tokens(wl, n_first=32, n_rand=32, seed=1):
     return np.unique(np.concatenate([np.arange(n_first), rest])).astype(np.int32)
 
 
-def run_oracle(wl, tokens=None, host=None):
+def run_oracle(wl, tokens=None, host=None, **kw):
     h = host if host is not None else to_host(wl)
     return oracle.fused_experts(h["problem"], h["x"], h["w13"], h["w2"], h["topk_ids"],
-                                h["topk_weights"], h["expert_map"], tokens)
+                                h["topk_weights"], h["expert_map"], tokens, **kw)
 
 
 def bf16_half_ulp(ref: np.ndarray) -> np.ndarray:

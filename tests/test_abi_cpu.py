@@ -35,7 +35,7 @@ def test_header_symbols_are_exported(moe):
     L = moe.lib()
     for name in declared:
         assert hasattr(L, name), name
-    assert moe.moe_abi_version() == 8
+    assert moe.moe_abi_version() == 9
 
 
 def test_status_strings(moe):
@@ -142,3 +142,64 @@ def test_selftest_validation(moe):
     L = moe.lib()
     for bad in (0, -5, 1 << 40):
         assert L.moe_selftest_bounded_wait(ctypes.c_longlong(bad), None) == 1
+
+
+def test_noalloc_reports_the_same_status_for_invalid_problems(moe):
+    # an invalid problem has no workspace size; the no-allocation entry point
+    # then returns exactly what moe_fused_experts returns (nothing launched)
+    L = moe.lib()
+    fake = ctypes.c_void_p(0x1000)
+    w = moe.Weight(fake, fake, fake, None, 0)
+    bad = [
+        moe.make_problem(16, 256, 512, 2, 8, 8, "bf16", "fp8_token_dyn", "silu", "separated"),
+        moe.make_problem(16, 250, 512, 2, 8, 8, "bf16", "bf16", "silu", "separated"),
+        moe.make_problem(16, 256, 512, 0, 8, 8, "bf16", "bf16", "silu", "separated"),
+        moe.make_problem(16, 256, 512, 2, 8, 8, "nvfp4", "nvfp4_dyn", "silu", "separated"),
+    ]
+    p = moe.make_problem(16, 256, 512, 2, 8, 8, "bf16", "bf16", "silu", "separated")
+    p.path = 7  # no such kernel family
+    bad.append(p)
+    for b in bad:
+        assert moe.moe_workspace_size(b) == 0
+        rc_ws = L.moe_fused_experts(ctypes.byref(b), fake, ctypes.byref(w), ctypes.byref(w), fake,
+                                    fake, None, None, 0, fake, None)
+        rc_na = L.moe_fused_experts_noalloc(ctypes.byref(b), fake, ctypes.byref(w),
+                                            ctypes.byref(w), fake, fake, None, fake, None)
+        assert rc_ws == rc_na and rc_ws in (1, 2), (rc_ws, rc_na)
+
+
+def test_path_is_a_field_of_the_problem(moe):
+    # the kernel family is chosen per problem (no process-wide switch): the
+    # workspace query of the same shapes follows each problem's own field
+    a = moe.make_problem(4096, 1024, 512, 2, 8, 8, "bf16", "bf16", "silu", "separated")
+    g = moe.make_problem(4096, 1024, 512, 2, 8, 8, "bf16", "bf16", "silu", "separated",
+                         path="generic")
+    t = moe.make_problem(16, 1024, 512, 2, 8, 8, "bf16", "bf16", "silu", "separated", path="tc")
+    t_auto = moe.make_problem(16, 1024, 512, 2, 8, 8, "bf16", "bf16", "silu", "separated")
+    assert moe.moe_workspace_size(a) > moe.moe_workspace_size(g) > 0
+    assert moe.moe_workspace_size(t) > moe.moe_workspace_size(t_auto) > 0
+    assert not hasattr(moe.lib(), "moe_set_path") or "moe_set_path" not in moe.EXPORTS
+
+
+def test_step_entry_points_validate_before_launching(moe):
+    L = moe.lib()
+    fake = ctypes.c_void_p(0x1000)
+    w = moe.Weight(fake, fake, None, None, 0)
+    p = moe.make_problem(16, 256, 512, 2, 8, 8, "fp8_block128", "fp8_group128_dyn", "silu",
+                         "separated")
+    args13 = lambda bm, ws, nbytes, inter=fake: (ctypes.byref(p), fake, fake, ctypes.byref(w), fake,
+                                                 fake, fake, bm, inter, fake, ws, nbytes, None)
+    assert L.moe_grouped_gemm_w13_act(*args13(32, fake, 1 << 30)) == 2      # block_m 32
+    need = moe.moe_w13_workspace_size(p, 64)
+    assert need > 0
+    assert L.moe_grouped_gemm_w13_act(*args13(64, fake, need - 1)) == 3     # workspace short
+    assert L.moe_grouped_gemm_w13_act(*args13(64, None, 0)) == 3            # workspace missing
+    assert L.moe_grouped_gemm_w13_act(*args13(64, fake, need, None)) == 1   # no intermediate
+    args2 = lambda bm, acc: (ctypes.byref(p), fake, fake, ctypes.byref(w), fake, fake, fake, fake,
+                             bm, acc, fake, None)
+    assert L.moe_grouped_gemm_w2_reduce(*args2(32, fake)) == 2
+    assert L.moe_grouped_gemm_w2_reduce(*args2(64, None)) == 1              # no accumulator
+    r = moe.make_problem(16, 256, 512, 1, 8, 8, "bf16", "bf16", "silu", "separated",
+                         router_weight_on_input=True)
+    assert L.moe_grouped_gemm_w2_reduce(ctypes.byref(r), fake, None, ctypes.byref(w), fake, fake,
+                                        fake, fake, 64, fake, fake, None) == 2

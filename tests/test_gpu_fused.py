@@ -20,10 +20,10 @@ FORMATS = [
 ]
 
 
-def check(wl, tokens=None):
+def check(wl, tokens=None, path="auto"):
     host = to_host(wl)
     ref = run_oracle(wl, tokens, host)
-    out = run_gpu(to_device(wl))
+    out = run_gpu(to_device(wl), path)
     err, tol, rms = compare(wl, out, ref, tokens)
     assert rms > 0 or wl.expert_map is not None
     assert err <= tol, f"{wl.name}: max|err| {err:.4e} > tol {tol:.4e} (rms {rms:.4e})"
@@ -66,15 +66,11 @@ def test_edge_cases():
 def test_empty_batch(path):
     # M = 0: nothing is launched, the call succeeds, the (0, K) output stays empty
     import quantized_moe_expert_topk_gb300 as moe
-    try:
-        moe.moe_set_path(path)
-        wl = to_device(make_custom(M=0, K=256, N=256, E=8, T=2, wfmt="mxfp4", afmt="bf16",
-                                   act="swiglu_oai", gate="interleaved", seed=3, name="empty"))
-        out = run_gpu(wl)
-        assert out.shape == (0, 256)
-        assert moe.moe_get_device_error() == 0
-    finally:
-        moe.moe_set_path("auto")
+    wl = to_device(make_custom(M=0, K=256, N=256, E=8, T=2, wfmt="mxfp4", afmt="bf16",
+                               act="swiglu_oai", gate="interleaved", seed=3, name="empty"))
+    out = run_gpu(wl, path)
+    assert out.shape == (0, 256)
+    assert moe.moe_get_device_error() == 0
 
 
 @pytest.mark.parametrize("path", ["stream", "tc", "generic"])
@@ -85,7 +81,6 @@ def test_mx_activations_each_path(afmt, path):
     # intermediate, the generic kernels the codes and e8m0 scales.  The input
     # spans 2^-12 .. 2^4 across its 32-element blocks, with all-zero blocks
     # and one all-zero token, so every block gets its own shared exponent.
-    import quantized_moe_expert_topk_gb300 as moe
     wl = make_custom(M=96, K=512, N=320, E=8, T=2, wfmt="mxfp4", afmt=afmt, act="swiglu_oai",
                      gate="interleaved", bias=True, seed=zlib.crc32(afmt.encode()) % 1000,
                      name=f"mx_{afmt}_{path}")
@@ -94,11 +89,7 @@ def test_mx_activations_each_path(afmt, path):
     blk[torch.rand((wl.M, wl.K // 32), generator=g) < 0.1] = 0.0
     blk[7] = 0.0
     wl.x = (wl.x.float() * blk.repeat_interleave(32, dim=1)).to(torch.bfloat16)
-    try:
-        moe.moe_set_path(path)
-        check(wl)
-    finally:
-        moe.moe_set_path("auto")
+    check(wl, path=path)
 
 
 @pytest.mark.parametrize("afmt", ["mxfp4_dyn", "mxfp8_dyn"])

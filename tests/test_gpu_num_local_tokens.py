@@ -22,26 +22,19 @@ CASES = [
 ]
 
 
-@pytest.fixture
-def restore_path():
-    yield
-    moe.moe_set_path("auto")
-
-
-def _layer(wl, n_dev):
+def _layer(wl, n_dev, path="auto"):
     return moe.FusedExperts(wl.M, wl.K, wl.N, wl.T, wl.E, wl.El, wl.wfmt, wl.afmt, wl.act,
                             wl.gate, wl.w13, wl.w2, wl.a1_scale, wl.a2_scale,
-                            num_local_tokens=n_dev)
+                            num_local_tokens=n_dev, path=path)
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-{c[6]}" for c in CASES])
-def test_valid_token_count(case, restore_path):
+def test_valid_token_count(case):
     wfmt, afmt, act, gate, M, T, path = case
     wl = to_device(make_custom(M=M, K=256, N=256, E=8, T=T, wfmt=wfmt, afmt=afmt, act=act,
                                gate=gate, bias=True, seed=41, name=f"nlt_{wfmt}"))
-    moe.moe_set_path(path)
     n_dev = torch.zeros(1, dtype=torch.int32, device="cuda")
-    layer = _layer(wl, n_dev)
+    layer = _layer(wl, n_dev, path)
     h = to_host(wl)
     for n in (0, 1, M // 2 + 3, M):
         n_dev.fill_(n)
@@ -56,7 +49,7 @@ def test_valid_token_count(case, restore_path):
             assert err <= tolerance(wl.wfmt, rms), (n, err, rms)
 
 
-def test_one_graph_serves_every_fill_level(restore_path):
+def test_one_graph_serves_every_fill_level():
     wl = to_device(make_custom(M=64, K=256, N=256, E=8, T=4, wfmt="mxfp4", afmt="bf16",
                                act="swiglu_oai", gate="interleaved", bias=True, seed=43,
                                name="nlt_graph"))

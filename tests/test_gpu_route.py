@@ -74,6 +74,22 @@ def test_router_parity(case, dtype):
         assert set(ids[t].tolist()) != set() and len(set(ids[t].tolist())) == k
         gap = abs(np.sort(keys[t, ids[t]]).sum() - np.sort(keys[t, oids[t]]).sum())
         assert gap < 1e-5, (t, ids[t], oids[t], gap)
+        if G > 1:
+            # the kernel's ids lie in groups that are eligible up to a near tie:
+            # each group it used scores at least the topk_group-th best group
+            # score (fp64 keys) less 1e-5, and inside the groups it used no
+            # expert it skipped has a key above its chosen ones by 1e-5 or more
+            gs = E // G
+            kg = keys[t].reshape(G, gs)
+            score = (np.sort(kg, 1)[:, -2:].sum(1) if b64 is not None else kg.max(1))
+            cutoff = np.sort(score)[::-1][TG - 1]
+            used = sorted(set((ids[t] // gs).tolist()))
+            assert len(used) <= TG, (t, used)
+            assert all(score[gidx] >= cutoff - 1e-5 for gidx in used), (t, used, score)
+            pool = [e for gidx in used for e in range(gidx * gs, (gidx + 1) * gs)
+                    if e not in set(ids[t].tolist())]
+            if pool:
+                assert keys[t, pool].max() <= keys[t, ids[t]].min() + 1e-5, t
 
 
 def test_router_feeds_the_fused_layer():

@@ -20,31 +20,24 @@ CASES = [
 ]
 
 
-@pytest.fixture
-def restore_path():
-    yield
-    moe.moe_set_path("auto")
-
-
 def _case_id(c):
     return f"{c[0]}-{c[1]}"
 
 
 @pytest.mark.parametrize("case", CASES, ids=[_case_id(c) for c in CASES])
-def test_stage1_weight_parity(case, restore_path):
+def test_stage1_weight_parity(case):
     wfmt, afmt, act, gate, M, K, N, E, paths = case
     for path in paths:
         wl = make_custom(M=M, K=K, N=N, E=E, T=1, wfmt=wfmt, afmt=afmt, act=act, gate=gate,
                          bias=True, seed=23, renorm=False, name=f"w1_{wfmt}")
         wl.router_weight_on_input = True
         wl = to_device(wl)
-        moe.moe_set_path(path)
-        got = run_gpu(wl)
+        got = run_gpu(wl, path)
         err, tol, rms = compare(wl, got, run_oracle(wl))
         assert rms > 0 and err <= tol, (path, err, tol)
 
 
-def test_stage1_weight_prefill_size(restore_path):
+def test_stage1_weight_prefill_size():
     # M * topk >= 2048: the automatic choice is the tcgen05 path
     wl = make_custom(M=2048, K=512, N=256, E=8, T=1, wfmt="mxfp4", afmt="bf16", act="swiglu_oai",
                      gate="interleaved", bias=True, seed=29, renorm=False, name="w1_prefill")

@@ -1,4 +1,4 @@
-"""GPU parity of the tcgen05 prefill kernels (forced with moe_set_path("tc"))
+"""GPU parity of the tcgen05 prefill kernels (forced with the problem's path "tc")
 against the oracle: every weight format, activation and gate layout, on
 shapes with several 128-row blocks per expert and ragged reduction / output
 tiles."""
@@ -22,13 +22,11 @@ FORMATS = [
 @pytest.fixture()
 def tc_path():
     import quantized_moe_expert_topk_gb300 as moe
-    moe.moe_set_path("tc")
-    yield moe
-    moe.moe_set_path("auto")
+    return moe
 
 
 def run_tc(moe, wl):
-    layer = moe.FusedExperts.from_workload(wl)
+    layer = moe.FusedExperts.from_workload(wl, path="tc")
     out = layer(wl.x, wl.topk_ids, wl.topk_weights, wl.expert_map)
     torch.cuda.synchronize()
     return out

@@ -353,3 +353,57 @@ def test_static_per_tensor_fp8_uses_each_stage_own_scale():
     xf = x.float().numpy()[0]
     ref = torch.from_numpy((xf / np.float32(s)).astype(np.float32)).to(torch.float8_e4m3fn)
     np.testing.assert_array_equal(a[0], ref.double().numpy() * s)
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu"])
+def test_intermediate_rows_of_identity_experts(act):
+    # the stage-1 output of every live slot of an identity expert is act(x, x)
+    # (closed form); with bf16 weights there is no stage-2 quantiser, so the
+    # rows before and after it agree, and a dropped slot's row stays zero
+    M, K, T, E = 4, 32, 2, 3
+    x = torch.randn(M, K, generator=torch.Generator().manual_seed(2)) * 2
+    xb = x.to(torch.bfloat16)
+    xd = xb.double()
+    w13, w2 = identity_experts(E, K)
+    ids = np.array([[0, 1], [2, 0], [1, 2], [0, 2]], np.int32)
+    w = np.full((M, T), 0.5, np.float32)
+    emap = np.array([0, 1, -1], np.int32)  # expert 2 dropped
+    out, z_pre, z_post = oracle.fused_experts(prob(M, K, K, T, E, act=act), bits_of(xb), w13, w2,
+                                              ids, w, emap, intermediate=True)
+    f = F.silu if act == "silu" else (lambda v: F.gelu(v, approximate="none"))
+    want = (f(xd) * xd).numpy()
+    for t in range(M):
+        for k in range(T):
+            row = z_pre[t * T + k]
+            if ids[t, k] == 2:
+                assert not row.any()
+            else:
+                np.testing.assert_allclose(row, want[t], rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(z_pre, z_post)
+
+
+def test_intermediate_rows_requantised_per_stage2_format():
+    # FP8 per-channel weights requantise the intermediate per token (one
+    # dynamic scale per row): every post-quantiser row is its pre-quantiser row
+    # through torch's e4m3 cast at scale max|row| / 448 (the format's rule)
+    wl = make_custom(M=6, K=64, N=48, E=3, T=2, wfmt="fp8_channel", afmt="fp8_token_dyn", seed=9)
+    h = to_host(wl)
+    _, z_pre, z_post = oracle.fused_experts(h["problem"], h["x"], h["w13"], h["w2"],
+                                            h["topk_ids"], h["topk_weights"], h["expert_map"],
+                                            intermediate=True)
+    zf = torch.from_numpy(z_pre).float()
+    scale = (zf.abs().amax(1, keepdim=True).clamp_min(1e-12) / 448.0)
+    q = (zf / scale).to(torch.float8_e4m3fn).double() * scale.double()
+    np.testing.assert_array_equal(z_post, q.numpy())
+
+
+def test_bf16_rounded_output_matches_torch_cast():
+    # the layer's last step: the fp64 result rounded to nearest-even bf16
+    wl = make_custom(M=9, K=64, N=32, E=4, T=2, seed=13)
+    h = to_host(wl)
+    args = (h["problem"], h["x"], h["w13"], h["w2"], h["topk_ids"], h["topk_weights"],
+            h["expert_map"])
+    out = oracle.fused_experts(*args)
+    out_bf16 = oracle.fused_experts(*args, round_to_bf16=True)
+    want = torch.from_numpy(out).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(out_bf16, want)
