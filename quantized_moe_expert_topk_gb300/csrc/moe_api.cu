@@ -134,8 +134,9 @@ bool tc_applies(const moe_problem_t *p) {
 struct TcLayout {
   long cap, blocks;
   size_t sorted, expert_ids, ntp, counts, x16, x_inv, a1_codes, a1_scales, a_sorted, a_rowscale,
-      a_groupscale, inter, staging, i_scales, acc, total;
+      a_groupscale, a_sf, inter, inter_sf, staging, i_scales, acc, total;
   bool f16_x;  // x converted to f16 once per token by the sort (MXFP4 weights)
+  bool bs;     // NVFP4 on the block-scaled kind: codes + scale-factor records
 };
 
 // Workspace layout of moe_fused_experts.
@@ -225,6 +226,20 @@ TcLayout make_tc_layout(const moe_problem_t *p) {
   }
   L.a1_codes = o; o = align_up(o + codes_bytes(p->afmt, p->M, p->K));
   L.a1_scales = o; o = align_up(o + scales_bytes(p->afmt, p->M, p->K));
+  L.bs = p->wfmt == W_NVFP4;
+  if (L.bs) {
+    // sorted e2m1 codes + scale-factor records of x; codes + records of the
+    // intermediate; the fp32 accumulator
+    L.a_sorted = o; o = align_up(o + (size_t)L.cap * p->K / 2);
+    L.a_sf = o; o = align_up(o + (size_t)L.blocks * ceil_div(p->K, kTcBsStage) * kTcSfRecBytes);
+    L.inter = o; o = align_up(o + (size_t)L.cap * p->N / 2);
+    L.inter_sf = o; o = align_up(o + (size_t)L.blocks * ceil_div(p->N, kTcBsStage) * kTcSfRecBytes);
+    L.a_rowscale = L.a_groupscale = L.staging = L.i_scales = o;
+    L.acc = o; o = align_up(o + (size_t)p->M * p->K * 4);
+    L.total = o;
+    return L;
+  }
+  L.a_sf = L.inter_sf = 0;
   const bool fp8 = p->wfmt == W_FP8_TENSOR || p->wfmt == W_FP8_CHANNEL ||
                    p->wfmt == W_FP8_BLOCK128;
   L.a_sorted = o; o = align_up(o + (size_t)L.cap * p->K * (fp8 ? 1 : 2));
@@ -803,12 +818,12 @@ int moe_prepare_weights(const moe_problem_t *p, int which, int layout, const moe
   a.out = static_cast<unsigned char *>(packed);
   a.nvfp4 = p->wfmt == W_NVFP4;
   a.total = (long)tc_packed_bytes(w13, a.nvfp4, p->N, p->K, p->num_local_experts);
-  a.rec_bytes = a.nvfp4 ? 4096 + 128 * 4 : 4096 + 128 * 2;
+  a.rec_bytes = a.nvfp4 ? kTcBsRecBytes : 4096 + 128 * 2;
   a.w13 = w13;
   a.N = p->N;
   a.R = w13 ? 2 * p->N : p->K;
   a.C = w13 ? p->K : p->N;
-  a.kstages = (int)ceil_div(a.C, 64);
+  a.kstages = (int)ceil_div(a.C, a.nvfp4 ? kTcBsStage : 64);
   a.ntiles = tc_ntiles(w13, p->N, p->K);
   a.gate = p->gate;
   return cuda_status(launch_pack_tc_fp4(a, st));
@@ -933,6 +948,7 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     g.out = ws + L.a_sorted;
     g.rowscale = reinterpret_cast<float *>(ws + L.a_rowscale);
     g.groupscale = reinterpret_cast<float *>(ws + L.a_groupscale);
+    if (L.bs) g.sf_out = ws + L.a_sf;
     StageScope sc(MOE_STAGE_QUANT, st);
     rc = cuda_status(launch_gather_rows(g, L.cap, st));
     sc.done();
@@ -971,7 +987,13 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     }
     a.w_codes = w13->codes; a.w_scales = w13->scales; a.w_global = w13->global_scale;
     a.w_bias = w13->bias; a.bias_f32 = w13->bias_is_f32; a.w_packed = w13->packed_tc;
-    if (s2 == A_NVFP4_DYN) {        // stage-2 quantisation inside the epilogue
+    if (L.bs) {                     // block-scaled: codes + scale-factor records
+      a.a_sf = ws + L.a_sf;
+      a.out = ws + L.inter;
+      a.out_sf = ws + L.inter_sf;
+      a.out_mode = TC_OUT_NVFP4_BS;
+      a.out_global = p->a2_scale;
+    } else if (s2 == A_NVFP4_DYN) { // stage-2 quantisation inside the epilogue
       a.out = ws + L.inter;
       a.out_mode = TC_OUT_NVFP4_F16;
       a.out_global = p->a2_scale;
@@ -1041,6 +1063,7 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     a.w_codes = w2->codes; a.w_scales = w2->scales; a.w_global = w2->global_scale;
     a.w_bias = w2->bias; a.bias_f32 = w2->bias_is_f32; a.w_packed = w2->packed_tc;
     a.acc = acc; a.topk_weights = topk_weights;
+    if (L.bs) a.a_sf = ws + L.inter_sf;
     StageScope sc(MOE_STAGE_W2, st);
     rc = cuda_status(launch_tc_gemm(a, ws + L.inter, L.cap, 0, st));
     sc.done();

@@ -184,8 +184,27 @@ cudaError_t launch_stream_fused(const StreamArgs &a13, const StreamArgs &a2, int
 // separate requantiser follows), f16 rows (bounded SwiGLU-OAI intermediate),
 // or the stage-2 NVFP4 quantisation done in the epilogue, written as the exact
 // f16 values e2m1(code) * e4m3(scale) the W2 kernel consumes.
+// TC_OUT_NVFP4_BS: the stage-2 NVFP4 quantisation done in the epilogue and
+// written as codes [cap, N/2] plus scale-factor records (out_sf) for the
+// block-scaled W2 kernel.
 enum { TC_OUT_BF16 = 0, TC_OUT_F32 = 1, TC_OUT_F16 = 2, TC_OUT_NVFP4_F16 = 3, TC_OUT_MX4_F16 = 4,
-       TC_OUT_MX8_F16 = 5 };
+       TC_OUT_MX8_F16 = 5, TC_OUT_NVFP4_BS = 6 };
+
+// Block-scaled NVFP4 operands of the tcgen05 kernels: every 256-element
+// reduction stage of a 128-row block carries one scale-factor record of
+// kTcSfRecBytes: four 512-byte chunks, one per 64-element MMA step, in the
+// order tcgen05.cp .32x128b.warpx4 expects (byte 16*(r%32) + 4*(r/32) + b of
+// chunk j = the ue4m3 scale of elements [64 j + 16 b, 64 j + 16 b + 16) of row
+// r of the block).  Weight records add the 128 rows' codes of the stage
+// (128 B per row, already in the 128-byte swizzle) in front: kTcBsRecBytes.
+constexpr int kTcBsStage = 256;                   // reduction elements per stage
+constexpr int kTcSfRecBytes = 2048;               // 4 x 512
+constexpr int kTcBsRecBytes = 16384 + kTcSfRecBytes;
+__host__ __device__ constexpr long tc_sf_offset(long r, long j, long ks_count) {
+  // byte of the scale of element j (along the reduction) of block row r
+  return ((r / 128) * ks_count + j / kTcBsStage) * kTcSfRecBytes +
+         ((j % kTcBsStage) / 64) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (j % 64) / 16;
+}
 struct TcArgs {
   int M, K, N, T, El, R, C;
   int wfmt, act, gate;
@@ -207,6 +226,8 @@ struct TcArgs {
   int *err;
   int w_stage1;          // router weight on the stage-1 output (W13 multiplies, W2 not)
   const void *w_packed;  // FP4 formats: load-time packed records
+  const void *a_sf;      // block-scaled NVFP4: scale-factor records of the A rows
+  void *out_sf;          // TC_OUT_NVFP4_BS: scale-factor records of the intermediate
   int ntiles;            // set by the launcher
   int rec_bytes;         // set by the launcher
   int mgroup;            // raster: m-blocks that walk the n-tiles together (launcher)
@@ -223,6 +244,9 @@ struct GatherArgs {
   // (scaled by 2^a per token, x_inv = 2^-a), copied row by row
   const void *x16 = nullptr;
   const float *x_inv = nullptr;
+  // block-scaled NVFP4 (afmt A_NVFP4_DYN): out receives the codes [cap, K/2]
+  // and sf_out the scale-factor records of the sorted rows
+  void *sf_out = nullptr;
 };
 cudaError_t launch_rescale_rows(const float *src, long cap, int N, const int32_t *sorted_ids,
                                 const int32_t *ntp, int S, void *dst, float *rowscale,

@@ -310,3 +310,70 @@ __device__ __forceinline__ void fma_f32x2(float &d0, float &d1, float a0, float 
 }
 
 }  // namespace moe
+
+// ----------------------------------------------------------------------------
+// Block-scaled tcgen05 MMA (PTX ISA, "tcgen05.mma" with .block_scale, and
+// "tcgen05.cp"; the forms below are the ones the ISA lists for sm_100a /
+// sm_103a: kind::mxf4nvf4 with .scale_vec::4X, 32x128b.warpx4 copies).
+namespace moe {
+
+// D[tmem] (+)= (A .* SFA) * (B .* SFB)^T, kind::mxf4nvf4, scale_vec::4X: A and
+// B are packed e2m1 (two per byte, K-major, 64 elements = 32 bytes per
+// instruction), each 16-element block of a row carries one ue4m3 scale
+// factor; fp32 accumulate.  sfa / sfb: Tensor Memory addresses of the scale
+// factors of this instruction's 64-element K step (layout: tc_sf_layout).
+__device__ __forceinline__ void umma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf4nvf4 (the ISA's descriptor table for
+// .kind::mxf8f6f4 / .kind::mxf4 / .kind::mxf4nvf4), both operands K-major:
+//   bits  0-1  sparsity selector (0), bit 2 dense (0), bit 3 reserved
+//   bits  4-5  scale-factor id of B (0: the whole 32-bit word, 4X)
+//   bits  7-9  A type: E2M1 = 1 (the mxf4 kinds' encoding)
+//   bits 10-12 B type: E2M1 = 1
+//   bits 13-14 negate A / B (0); bits 15-16 transpose A / B (0: K-major)
+//   bits 17-22 N >> 3
+//   bit  23    scale-factor type: UE4M3 = 0, UE8M0 = 1
+//   bits 24-28 M >> 4
+//   bits 29-30 scale-factor id of A (0)
+//   bit  31    K of the instruction: 0 = 64 (dense)
+// The accumulator is fp32 for these kinds (no D-type field).
+__host__ __device__ constexpr uint32_t umma_idesc_nvf4(int m, int n) {
+  return (1u << 7)                       // A: E2M1
+         | (1u << 10)                    // B: E2M1
+         | ((uint32_t)(n >> 3) << 17)    // N
+         | (0u << 23)                    // scale factors UE4M3
+         | ((uint32_t)(m >> 4) << 24);   // M
+}
+
+// Shared-memory descriptor of one scale-factor chunk for tcgen05.cp
+// .32x128b: 32 rows of 16 bytes, no swizzle; core matrices (8 rows x 16 B)
+// 128 bytes apart along the rows (stride byte offset); one core matrix wide,
+// so the leading byte offset is not used.
+__device__ __forceinline__ uint64_t sf_smem_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);   // start address
+  d |= (uint64_t)(128 >> 4) << 32;           // stride byte offset
+  d |= (uint64_t)1 << 46;                     // descriptor version
+  return d;                                   // layout 0: no swizzle
+}
+
+// Copy 32 rows x 128 bits from shared memory (descriptor) to Tensor Memory
+// columns [taddr, taddr + 4), replicated into all four 32-lane quarters
+// (.warpx4): lane 32q + i, column c + w holds bytes [16 i + 4 w, 16 i + 4 w + 4)
+// of the chunk.  Issued by one thread; ordered before the MMAs it issues later.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+}  // namespace moe
