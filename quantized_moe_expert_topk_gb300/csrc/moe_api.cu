@@ -818,13 +818,13 @@ int moe_prepare_weights(const moe_problem_t *p, int which, int layout, const moe
   a.out = static_cast<unsigned char *>(packed);
   a.nvfp4 = p->wfmt == W_NVFP4;
   a.total = (long)tc_packed_bytes(w13, a.nvfp4, p->N, p->K, p->num_local_experts);
-  a.rec_bytes = a.nvfp4 ? kTcBsRecBytes : 4096 + 128 * 2;
+  a.rec_bytes = 4096 + 128 * 2;
   a.w13 = w13;
   a.N = p->N;
   a.R = w13 ? 2 * p->N : p->K;
   a.C = w13 ? p->K : p->N;
   a.kstages = (int)ceil_div(a.C, a.nvfp4 ? kTcBsStage : 64);
-  a.ntiles = tc_ntiles(w13, p->N, p->K);
+  a.ntiles = a.nvfp4 ? bs_ntiles(w13, p->N, p->K) : tc_ntiles(w13, p->N, p->K);
   a.gate = p->gate;
   return cuda_status(launch_pack_tc_fp4(a, st));
 }
@@ -991,7 +991,6 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
       a.a_sf = ws + L.a_sf;
       a.out = ws + L.inter;
       a.out_sf = ws + L.inter_sf;
-      a.out_mode = TC_OUT_NVFP4_BS;
       a.out_global = p->a2_scale;
     } else if (s2 == A_NVFP4_DYN) { // stage-2 quantisation inside the epilogue
       a.out = ws + L.inter;
@@ -1011,7 +1010,8 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
       a.out_mode = TC_OUT_BF16;
     }
     StageScope sc(MOE_STAGE_W13, st);
-    rc = cuda_status(launch_tc_gemm(a, ws + L.a_sorted, L.cap, 1, st));
+    rc = cuda_status(L.bs ? launch_bs_gemm(a, ws + L.a_sorted, L.cap, 1, dinfo.sm_count, st)
+                          : launch_tc_gemm(a, ws + L.a_sorted, L.cap, 1, st));
     sc.done();
     if (rc != MOE_OK) return rc;
   }
@@ -1065,7 +1065,8 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     a.acc = acc; a.topk_weights = topk_weights;
     if (L.bs) a.a_sf = ws + L.inter_sf;
     StageScope sc(MOE_STAGE_W2, st);
-    rc = cuda_status(launch_tc_gemm(a, ws + L.inter, L.cap, 0, st));
+    rc = cuda_status(L.bs ? launch_bs_gemm(a, ws + L.inter, L.cap, 0, dinfo.sm_count, st)
+                          : launch_tc_gemm(a, ws + L.inter, L.cap, 0, st));
     sc.done();
     if (rc != MOE_OK) return rc;
   }

@@ -184,22 +184,17 @@ cudaError_t launch_stream_fused(const StreamArgs &a13, const StreamArgs &a2, int
 // separate requantiser follows), f16 rows (bounded SwiGLU-OAI intermediate),
 // or the stage-2 NVFP4 quantisation done in the epilogue, written as the exact
 // f16 values e2m1(code) * e4m3(scale) the W2 kernel consumes.
-// TC_OUT_NVFP4_BS: the stage-2 NVFP4 quantisation done in the epilogue and
-// written as codes [cap, N/2] plus scale-factor records (out_sf) for the
-// block-scaled W2 kernel.
 enum { TC_OUT_BF16 = 0, TC_OUT_F32 = 1, TC_OUT_F16 = 2, TC_OUT_NVFP4_F16 = 3, TC_OUT_MX4_F16 = 4,
-       TC_OUT_MX8_F16 = 5, TC_OUT_NVFP4_BS = 6 };
+       TC_OUT_MX8_F16 = 5 };
 
-// Block-scaled NVFP4 operands of the tcgen05 kernels: every 256-element
+// Block-scaled NVFP4 operands (moe_bs.cu): every 256-element
 // reduction stage of a 128-row block carries one scale-factor record of
 // kTcSfRecBytes: four 512-byte chunks, one per 64-element MMA step, in the
 // order tcgen05.cp .32x128b.warpx4 expects (byte 16*(r%32) + 4*(r/32) + b of
 // chunk j = the ue4m3 scale of elements [64 j + 16 b, 64 j + 16 b + 16) of row
-// r of the block).  Weight records add the 128 rows' codes of the stage
-// (128 B per row, already in the 128-byte swizzle) in front: kTcBsRecBytes.
+// r of the block).
 constexpr int kTcBsStage = 256;                   // reduction elements per stage
 constexpr int kTcSfRecBytes = 2048;               // 4 x 512
-constexpr int kTcBsRecBytes = 16384 + kTcSfRecBytes;
 __host__ __device__ constexpr long tc_sf_offset(long r, long j, long ks_count) {
   // byte of the scale of element j (along the reduction) of block row r
   return ((r / 128) * ks_count + j / kTcBsStage) * kTcSfRecBytes +
@@ -227,7 +222,7 @@ struct TcArgs {
   int w_stage1;          // router weight on the stage-1 output (W13 multiplies, W2 not)
   const void *w_packed;  // FP4 formats: load-time packed records
   const void *a_sf;      // block-scaled NVFP4: scale-factor records of the A rows
-  void *out_sf;          // TC_OUT_NVFP4_BS: scale-factor records of the intermediate
+  void *out_sf;          // block-scaled NVFP4 W13: scale-factor records of the intermediate
   int ntiles;            // set by the launcher
   int rec_bytes;         // set by the launcher
   int mgroup;            // raster: m-blocks that walk the n-tiles together (launcher)
@@ -264,6 +259,16 @@ cudaError_t launch_pack_tc_fp4(const TcPackArgs &p, cudaStream_t st);
 cudaError_t launch_gather_rows(const GatherArgs &g, long cap_rows, cudaStream_t st);
 cudaError_t launch_tc_gemm(const TcArgs &a, const void *a_sorted, long cap_rows, int w13,
                            cudaStream_t st);
+// Persistent block-scaled NVFP4 grouped GEMMs (moe_bs.cu): A = packed e2m1
+// codes [cap, C/2] + scale-factor records (a.a_sf); B = the MOE_LAYOUT_TC
+// records of NVFP4 weights (a.w_packed).  W13 writes the NVFP4 intermediate
+// (codes into a.out [cap, N/2], scale factors into a.out_sf); W2 adds the
+// weighted outputs into a.acc.  grid = min(tiles, sm_count), one CTA per SM.
+int bs_ntiles(int w13, int N, int K);
+size_t bs_packed_bytes(int w13, int N, int K, int El);
+cudaError_t launch_pack_bs(const TcPackArgs &p, cudaStream_t st);
+cudaError_t launch_bs_gemm(const TcArgs &a, const void *a_codes, long cap_rows, int w13,
+                           int sm_count, cudaStream_t st);
 
 cudaError_t launch_route(const void *logits, int bf16_in, int M, int E, int topk, int scoring,
                          int renorm, int G, int TG, const float *bias, float scale, int32_t *ids,

@@ -14,20 +14,12 @@
 //                           decoded by the eight epilogue warps into exact f16
 //                           (code x group scale) in the swizzled layout,
 //                           kind::f16 with f16 operands
-//   K_NVF4  NVFP4 w4a4:     block-scaled MMA on the codes themselves
-//                           (kind::mxf4nvf4, scale_vec::4X): A (sorted e2m1
-//                           codes) by 2-D TMA plus its scale-factor record by
-//                           a bulk copy; B as load-time records (codes already
-//                           swizzled + scale factors), one bulk copy each; the
-//                           issuing thread moves each stage's ue4m3 scale
-//                           factors into Tensor Memory with tcgen05.cp before
-//                           the stage's four MMAs (256 reduction elements per
-//                           stage, 128 bytes of codes per row)
-// Every stage is 128 bytes of reduction per row (64 bf16 / 128 e4m3 / 256
-// e2m1), i.e. one 128-byte swizzle atom.  Warp roles: warp 0 TMA producer; warp 1 TMEM owner,
+// Every stage is 128 bytes of reduction per row (64 bf16 / 128 e4m3), i.e. one
+// 128-byte swizzle atom.  Warp roles: warp 0 TMA producer; warp 1 TMEM owner,
 // lane 0 issues tcgen05.mma + tcgen05.commit; warps 2-9 epilogue (tcgen05.ld,
 // scales, bias, activation or router weight + red.add); for FP4 weights the
-// same eight warps decode B during the main loop.  FP8 128x128 block scales: every 128-wide reduction block lands in
+// same eight warps decode B during the main loop.  (NVFP4 weights run on the
+// block-scaled kernels of moe_bs.cu; the gather below prepares their A rows.)  FP8 128x128 block scales: every 128-wide reduction block lands in
 // one of two TMEM buffers and the epilogue warps fold it into registers with
 // a_scale[row, kb] * w_scale[block, kb] (promotion).  Two CTAs share an SM
 // (3-stage rings, 256 TMEM columns each), so one CTA's epilogue overlaps the
@@ -62,16 +54,7 @@ constexpr long long kWaitCycles = 4000000000LL;
 constexpr int kErrTimeout = 5;
 
 enum { MODE_W13 = 0, MODE_W2 = 1 };
-enum { K_BF16 = 0, K_FP8 = 1, K_FP4 = 2, K_NVF4 = 3 };
-// Tensor Memory columns of the block-scaled kind: accumulator [0, 128), the
-// scale factors of the stage's four MMA steps for A at [128, 144) and for B at
-// [144, 160) (four columns per step; see tc_cp_32x128b_x4).  Scale-factor
-// layout in Tensor Memory (the ISA's block-scaling layout for M = 128 and
-// N = 128): row r of a 128-row operand takes its 32-bit scale word for one
-// MMA step from column base + r / 32 of lane r % 32, replicated in the four
-// 32-lane quarters; byte b of the word scales the b-th 16-element block of the
-// step's 64 elements.
-constexpr uint32_t kSfaCol = 128, kSfbCol = 144;
+enum { K_BF16 = 0, K_FP8 = 1, K_FP4 = 2 };
 
 struct Smem {
   unsigned char a[NS][STAGE_A];
@@ -125,9 +108,7 @@ __device__ __forceinline__ void red_add_v4(float *p, float x, float y, float z, 
 }
 
 constexpr int kTcRasterGroup = 1;
-constexpr int kTcRasterGroupBs = 8;
 constexpr int kPrefetchStages = 12;  // FP4 weight records prefetched into L2 ahead
-constexpr int kPrefetchStagesBs = 4;  // block-scaled records (4x the reduction per stage)
 
 template <int MODE, int KIND>
 __global__ void __launch_bounds__(THREADS, 2)
@@ -154,8 +135,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int e = a.expert_ids[blk];
   if (e < 0 || e >= a.El) return;
   const bool promote = KIND == K_FP8 && a.wfmt == W_FP8_BLOCK128;
-  // reduction elements per stage
-  const int BKE = KIND == K_FP8 ? 128 : KIND == K_NVF4 ? kTcBsStage : 64;
+  const int BKE = KIND == K_FP8 ? 128 : 64;  // reduction elements per stage
   const int KT = (a.C + BKE - 1) / BKE;
 
   if (threadIdx.x == 0) {
@@ -213,25 +193,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const unsigned char *src = tile_rec + kt * rec_stride;
           mbar_arrive_expect_tx(&sm.full_raw[s], (uint32_t)a.rec_bytes);
           tma_bulk_g2s(sm.raw[s], src, (uint32_t)a.rec_bytes, &sm.full_raw[s]);
-        } else if (KIND == K_NVF4) {
-          const unsigned char *tile_rec = static_cast<const unsigned char *>(a.w_packed) +
-              ((long)e * a.ntiles + nt) * KT * (long)kTcBsRecBytes;
-          {
-            const int p0 = kt == 0 ? 1 : kt + kPrefetchStagesBs;
-            const int p1 = min(KT, kt == 0 ? 1 + kPrefetchStagesBs : p0 + 1);
-            if (p0 < p1)
-              prefetch_l2_bulk(tile_rec + (long)p0 * kTcBsRecBytes,
-                               (uint32_t)((p1 - p0) * kTcBsRecBytes));
-          }
-          const unsigned char *rec = tile_rec + (long)kt * kTcBsRecBytes;
-          mbar_arrive_expect_tx(&sm.full_a[s], STAGE_A + kTcSfRecBytes + kTcBsRecBytes);
-          tma_load_2d(sm.a[s], &tmA, kt * 128, blk * BM, &sm.full_a[s]);  // bytes of codes
-          tma_bulk_g2s(sm.raw[s],
-                       static_cast<const unsigned char *>(a.a_sf) +
-                           ((long)blk * KT + kt) * kTcSfRecBytes,
-                       kTcSfRecBytes, &sm.full_a[s]);
-          tma_bulk_g2s(sm.b[s], rec, STAGE_B, &sm.full_a[s]);
-          tma_bulk_g2s(sm.raw[s] + kTcSfRecBytes, rec + STAGE_B, kTcSfRecBytes, &sm.full_a[s]);
         } else {
           mbar_arrive_expect_tx(&sm.full_a[s], STAGE_A + STAGE_B);
           tma_load_2d(sm.a[s], &tmA, kt * BKE, blk * BM, &sm.full_a[s]);
@@ -253,10 +214,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = KIND == K_FP8    ? umma_idesc_e4m3(BM, BN)
-                                 : KIND == K_FP4  ? umma_idesc_f16(BM, BN)
-                                 : KIND == K_NVF4 ? umma_idesc_nvf4(BM, BN)
-                                                  : umma_idesc_bf16(BM, BN);
+      constexpr uint32_t idesc = KIND == K_FP8   ? umma_idesc_e4m3(BM, BN)
+                                 : KIND == K_FP4 ? umma_idesc_f16(BM, BN)
+                                                 : umma_idesc_bf16(BM, BN);
       for (int kt = 0; kt < KT; ++kt) {
         const int s = kt % NS;
         const uint32_t par = (kt / NS) & 1;
@@ -274,22 +234,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         const uint64_t ad = umma_desc_sw128(smem_addr(sm.a[s]));
         const uint64_t bd = umma_desc_sw128(smem_addr(sm.b[s]));
-        if (KIND == K_NVF4) {
-          // this stage's scale factors into Tensor Memory (ordered before the
-          // MMAs below, which are issued by the same thread)
-          const uint32_t sfa = smem_addr(sm.raw[s]), sfb = sfa + kTcSfRecBytes;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            tc_cp_32x128b_x4(tmem + kSfaCol + 4 * j, sf_smem_desc(sfa + 512 * j));
-            tc_cp_32x128b_x4(tmem + kSfbCol + 4 * j, sf_smem_desc(sfb + 512 * j));
-          }
-        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // 4 MMAs of 32 bytes of reduction each
           if (KIND == K_FP8) umma_f8(d, ad + 2 * j, bd + 2 * j, idesc, (fresh && j == 0) ? 0u : 1u);
-          else if (KIND == K_NVF4)
-            umma_nvf4(d, ad + 2 * j, bd + 2 * j, idesc, tmem + kSfaCol + 4 * j,
-                      tmem + kSfbCol + 4 * j, (fresh && j == 0) ? 0u : 1u);
           else umma_f16(d, ad + 2 * j, bd + 2 * j, idesc, (fresh && j == 0) ? 0u : 1u);
         }
         umma_commit(&sm.empty[s]);
@@ -439,20 +386,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // router weight on the stage-1 output (apply_router_weight_on_input)
         const float zw = (a.w_stage1 && live) ? a.topk_weights[s_id] : 1.f;
         const int jbase = nt * 64 + 32 * h;
-        const long ks_out = ceil_div(a.N, kTcBsStage);
-        if (a.out_mode == TC_OUT_NVFP4_BS) {
-          // scale factors of the intermediate's reduction tail that no output
-          // covers must read as zero (not stale bytes) in the W2 stage
-          uint8_t *sf = static_cast<uint8_t *>(a.out_sf);
-          if (jbase >= a.N) {
-            for (long j0 = jbase; j0 < jbase + 32 && j0 < ks_out * kTcBsStage; j0 += 16)
-              sf[tc_sf_offset(r, j0, ks_out)] = 0;
-          }
-          if (nt == a.ntiles - 1 && h == 1) {
-            for (long j0 = (long)a.ntiles * 64; j0 < ks_out * kTcBsStage; j0 += 16)
-              sf[tc_sf_offset(r, j0, ks_out)] = 0;
-          }
-        }
         if (jbase < a.N) {  // N % 32 == 0: the 32 outputs are all in range or none
           const bool sep = a.gate == GATE_SEPARATED;
           const bool mx_out = a.out_mode == TC_OUT_MX4_F16 || a.out_mode == TC_OUT_MX8_F16;
@@ -475,15 +408,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (mx_out) {
 #pragma unroll
               for (int i = 0; i < 16; ++i) zb[16 * p + i] = z[i];
-            } else if (a.out_mode == TC_OUT_NVFP4_BS) {
-              // one NVFP4 group (jbase + 16 p is a multiple of 16): codes into
-              // the row, its scale into the intermediate's scale-factor records
-              uint32_t lo, hi;
-              const uint32_t sq = nvfp4_quant16(z, a.out_global[e], lo, hi);
-              const long j0 = jbase + 16 * p;
-              *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.out) + r * (a.N / 2) + j0 / 2) =
-                  make_uint2(lo, hi);
-              static_cast<uint8_t *>(a.out_sf)[tc_sf_offset(r, j0, ks_out)] = (uint8_t)sq;
             } else if (a.out_mode == TC_OUT_F32) {
               float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + r * a.N + jbase + 16 * p);
 #pragma unroll
@@ -801,59 +725,6 @@ __global__ void pack_tc_fp4_kernel(TcPackArgs p) {
   p.out[o] = v;
 }
 
-// Load-time records of NVFP4 weights for the block-scaled kernel: per
-// (expert, n-tile, 256-wide reduction stage) the 128 tile rows' codes (128
-// bytes each) in the 128-byte swizzle (16-byte chunk c of row n at
-// sw128(n, c)), then the stage's scale-factor record (tc_sf_offset order).
-// Rows follow the kernel's tile order; zeros past the tensor.  One thread per
-// record byte.
-__global__ void pack_tc_bs_kernel(TcPackArgs p) {
-  const long o = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (o >= p.total) return;
-  const long rec = o / kTcBsRecBytes;
-  const int wb = (int)(o % kTcBsRecBytes);
-  const int kt = (int)(rec % p.kstages);
-  const long ent = rec / p.kstages;
-  const int nt = (int)(ent % p.ntiles);
-  const long e = ent / p.ntiles;
-  int n;
-  long k;  // code byte (codes) or group index (scales) along the row
-  const bool code = wb < 16384;
-  if (code) {
-    n = (wb / 1024) * 8 + (wb % 1024) / 128;
-    const int c = ((wb % 128) / 16) ^ (n & 7);
-    k = (long)kt * 128 + c * 16 + (wb % 16);
-  } else {
-    const int w = wb - 16384;
-    const int j = w / 512, ww = w % 512;
-    n = 32 * ((ww % 16) / 4) + ww / 16;
-    k = (long)kt * 16 + j * 4 + (ww % 4);
-  }
-  const int b = n >> 5;
-  long row;
-  bool valid;
-  if (p.w13) {
-    if (p.gate == GATE_SEPARATED) {
-      const long jj = (long)nt * 64 + (b >> 1) * 32 + (n & 31);
-      valid = jj < p.N;
-      row = (b & 1) ? p.N + jj : jj;
-    } else {
-      row = (long)nt * 128 + n;
-      valid = row < 2L * p.N;
-    }
-  } else {
-    row = (long)nt * 128 + n;
-    valid = row < p.R;
-  }
-  unsigned char v = 0;
-  if (code) {
-    if (valid && k < p.C / 2) v = p.codes[((long)e * p.R + row) * (p.C / 2) + k];
-  } else {
-    if (valid && k < p.C / 16) v = p.scales[((long)e * p.R + row) * (p.C / 16) + k];
-  }
-  p.out[o] = v;
-}
-
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -904,21 +775,24 @@ cudaError_t launch_tc_t(const CUtensorMap &ta, const CUtensorMap &tb, const TcAr
 
 }  // namespace
 
+// 2-D K-major byte tensor map with the 128-byte swizzle (the block-scaled
+// kernels' A operand: rows of packed e2m1 codes).
+bool make_tc_map_u8(CUtensorMap *tm, const void *base, long rows, long cols, int box_rows) {
+  return make_map(tm, base, rows, cols, true, box_rows);
+}
+
 int tc_ntiles(int w13, int N, int K) { return w13 ? (int)ceil_div(N, 64) : (int)ceil_div(K, BN); }
 
 size_t tc_packed_bytes(int w13, int nvfp4, int N, int K, int El) {
+  if (nvfp4) return bs_packed_bytes(w13, N, K, El);  // block-scaled records
   const int C = w13 ? K : N;
-  if (nvfp4)  // block-scaled records
-    return (size_t)El * tc_ntiles(w13, N, K) * ceil_div(C, kTcBsStage) * kTcBsRecBytes;
   return (size_t)El * tc_ntiles(w13, N, K) * ceil_div(C, 64) * (4096 + 128 * 2);
 }
 
 cudaError_t launch_pack_tc_fp4(const TcPackArgs &p, cudaStream_t st) {
   if (p.total <= 0) return cudaSuccess;
-  if (p.nvfp4)
-    pack_tc_bs_kernel<<<(unsigned)ceil_div(p.total, 256), 256, 0, st>>>(p);
-  else
-    pack_tc_fp4_kernel<<<(unsigned)ceil_div(p.total, 256), 256, 0, st>>>(p);
+  if (p.nvfp4) return launch_pack_bs(p, st);
+  pack_tc_fp4_kernel<<<(unsigned)ceil_div(p.total, 256), 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -956,23 +830,11 @@ cudaError_t launch_tc_gemm(const TcArgs &a_in, const void *a_sorted, long cap_ro
   if (blocks <= 0) return cudaSuccess;
   if (blocks * a.ntiles > 0x7fffffffL) return cudaErrorInvalidConfiguration;
   a.nblocks = blocks;
-  const int kind = a.wfmt == W_BF16    ? K_BF16
-                   : a.wfmt == W_NVFP4 ? K_NVF4
-                   : a.wfmt == W_MXFP4 ? K_FP4
-                                       : K_FP8;
-  // block-scaled NVFP4: groups of m-blocks walk the n-tiles together, so the
-  // CTAs resident at once share each weight tile (its codes are 4x smaller
-  // than the f16 A rows the other kinds keep in L2)
-  a.mgroup = (int)min(blocks, (long)(kind == K_NVF4 ? kTcRasterGroupBs : kTcRasterGroup));
+  a.mgroup = (int)min(blocks, (long)kTcRasterGroup);
+  const int kind = a.wfmt == W_BF16 ? K_BF16 : (a.wfmt == W_MXFP4 || a.wfmt == W_NVFP4) ? K_FP4 : K_FP8;
   CUtensorMap ta, tb;
-  // A: bf16 / f16 rows, e4m3 codes, or (block-scaled) packed e2m1 bytes
-  if (!make_map(&ta, a_sorted, cap_rows, kind == K_NVF4 ? a.C / 2 : a.C,
-                kind == K_FP8 || kind == K_NVF4, BM))
-    return cudaErrorInvalidValue;
-  if (kind == K_NVF4) {
-    tb = ta;  // unused: the weights arrive as bulk-copied records
-    a.rec_bytes = kTcBsRecBytes;
-  } else if (kind == K_FP4) {
+  if (!make_map(&ta, a_sorted, cap_rows, a.C, kind == K_FP8, BM)) return cudaErrorInvalidValue;
+  if (kind == K_FP4) {
     tb = ta;  // unused
     a.rec_bytes = a.wfmt == W_NVFP4 ? 4096 + 128 * 4 : 4096 + 128 * 2;
   } else if (!make_map(&tb, a.w_codes, (long)a.El * a.R, a.C, kind == K_FP8, 32)) {
@@ -982,14 +844,12 @@ cudaError_t launch_tc_gemm(const TcArgs &a_in, const void *a_sorted, long cap_ro
     switch (kind) {
       case K_BF16: return launch_tc_t<MODE_W13, K_BF16>(ta, tb, a, blocks, st);
       case K_FP8: return launch_tc_t<MODE_W13, K_FP8>(ta, tb, a, blocks, st);
-      case K_NVF4: return launch_tc_t<MODE_W13, K_NVF4>(ta, tb, a, blocks, st);
       default: return launch_tc_t<MODE_W13, K_FP4>(ta, tb, a, blocks, st);
     }
   }
   switch (kind) {
     case K_BF16: return launch_tc_t<MODE_W2, K_BF16>(ta, tb, a, blocks, st);
     case K_FP8: return launch_tc_t<MODE_W2, K_FP8>(ta, tb, a, blocks, st);
-    case K_NVF4: return launch_tc_t<MODE_W2, K_NVF4>(ta, tb, a, blocks, st);
     default: return launch_tc_t<MODE_W2, K_FP4>(ta, tb, a, blocks, st);
   }
 }
