@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import glob
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -18,7 +19,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD = os.path.join(PKG, "_build")
+# objects per host architecture, so a copy of the tree moved to another
+# machine never links objects compiled for this one
+BUILD = os.path.join(PKG, "_build", platform.machine() or "host")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
@@ -54,8 +57,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
 
+    headers = [p for p in _deps() if not p.endswith(".cu")]
+    newest_header = max((os.path.getmtime(p) for p in headers), default=0.0)
+
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        # a translation unit is recompiled when it or any header is newer than its object
+        if (not force and not extra_flags and os.path.exists(obj)
+                and os.path.getmtime(obj) >= max(os.path.getmtime(src), newest_header)):
+            return obj
         cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)

@@ -18,13 +18,17 @@
 //   warp 0      TMA producer: per stage the A rows' codes (2-D TMA, 128-byte
 //               swizzle), the A scale-factor record, the B record (codes
 //               pre-swizzled + scale factors) -- 54 KB, one mbarrier
-//   warp 1      TMEM owner; lane 0 copies each stage's scale factors into
-//               Tensor Memory (tcgen05.cp) and issues the four MMAs
+//   warp 1      TMEM owner; lane 0 issues each stage's four MMAs
 //   warps 2-17  epilogue: each thread owns one row and 64 accumulator
 //               columns; it copies them to registers, releases the
 //               accumulator (the next tile's MMAs start) and then applies
 //               the scales, bias, activation and NVFP4 quantiser (W13) or the
 //               router weight and the fp32 reduce (W2)
+//   warp 18     lane 0 copies each stage's scale factors from shared memory
+//               into one of two Tensor Memory buffers (tcgen05.cp), one stage
+//               ahead of the MMAs that read them; a commit on sf_full hands
+//               the buffer to the MMA thread, whose commit on sf_empty hands
+//               it back
 // Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, stops
 // issuing, lets its copies and MMAs land, frees its Tensor Memory and exits.
 #include <cuda.h>
@@ -46,17 +50,23 @@ constexpr int STAGE_A = BM * 128;                  // 16 KB of A codes
 constexpr int STAGE_B = BN * 128;                  // 32 KB of B codes
 constexpr int SFB_BYTES = 2 * kTcSfRecBytes;       // B scale factors (256 rows)
 constexpr int NUM_EPI = 16;
-constexpr int THREADS = (2 + NUM_EPI) * 32;        // 576
+constexpr int CP_WARP = 2 + NUM_EPI;               // warp 18
+constexpr int THREADS = (3 + NUM_EPI) * 32;        // 608
 constexpr int TMEM_COLS = 512;
-// Tensor Memory columns: accumulator [0, 256); scale factors of the stage's
-// four MMA steps, A at [256, 272) (4 per step), B at [272, 304) (8 per step:
-// rows 0-127, then rows 128-255).  Layout of one 128-row block's scale words
-// as in moe_tc.cu (row r in column base + r / 32 of lane r % 32, in all four
-// lane quarters; byte b scales the b-th 16-element block of the step).
-constexpr uint32_t kAccCol = 0, kSfaCol = 256, kSfbCol = 272;
+// Tensor Memory columns: accumulator [0, 256); two buffers of one stage's
+// scale factors (four MMA steps) at 256 + 48 b: A at +0 (4 columns per step),
+// B at +16 (8 per step: rows 0-127, then rows 128-255).  Layout of one
+// 128-row block's scale words as in moe_tc.cu's kind (row r in column
+// base + r / 32 of lane r % 32, in all four lane quarters; byte b scales the
+// b-th 16-element block of the step).
+constexpr uint32_t kAccCol = 0, kSfCol = 256, kSfBufCols = 48, kSfbOff = 16;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int kErrTimeout = 5;
 constexpr int kRasterGroup = 8;  // m-blocks that walk the n-tiles together
+// Weight records are prefetched into L2 this many stages ahead of the ring
+// (by the CTA of the first m-block of each raster group only: the others of
+// the group read the same records), so the ring's copies hit L2.
+constexpr int kPrefetchAhead = 8;
 
 enum { MODE_W13 = 0, MODE_W2 = 1 };
 
@@ -66,7 +76,8 @@ struct Smem {
   unsigned char sfa[NS][kTcSfRecBytes];
   unsigned char sfb[NS][SFB_BYTES];
   uint64_t full[NS], empty[NS];
-  uint64_t acc_full, acc_empty, drain;
+  uint64_t sf_full[2], sf_empty[2];
+  uint64_t acc_full, acc_empty, drain, cp_drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -172,9 +183,14 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.sf_full[b], 1);
+      mbar_init(&sm.sf_empty[b], 1);
+    }
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_empty, NUM_EPI);
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.cp_drain, 1);
     sm.abort_flag = 0;
     mbar_fence_init();
   }
@@ -203,8 +219,14 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
                                     ((long)e * a.ntiles + nt) * KT * (long)(STAGE_B + SFB_BYTES);
         const unsigned char *asf = static_cast<const unsigned char *>(a.a_sf) +
                                    (long)blk * KT * kTcSfRecBytes;
+        const bool leader = (blk % kRasterGroup) == 0;
+        if (leader && kPrefetchAhead > 0)
+          prefetch_l2_bulk(brec, (uint32_t)(min(KT, kPrefetchAhead) * (STAGE_B + SFB_BYTES)));
         for (int kt = 0; kt < KT; ++kt, ++g) {
           const int s = (int)(g % NS);
+          if (leader && kPrefetchAhead > 0 && kt + kPrefetchAhead < KT)
+            prefetch_l2_bulk(brec + (long)(kt + kPrefetchAhead) * (STAGE_B + SFB_BYTES),
+                             (uint32_t)(STAGE_B + SFB_BYTES));
           if (!wait_or_abort(&sm.empty[s], (uint32_t)(((g / NS) & 1) ^ 1), a.err, abort_flag)) {
             break;
           }
@@ -238,23 +260,21 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
         tc_fence_after();
         for (int kt = 0; kt < KT; ++kt, ++g) {
           const int s = (int)(g % NS);
+          const int b = (int)(g & 1);
+          // the stage's operands have landed and its scale factors are in
+          // Tensor Memory buffer b
           if (!wait_or_abort(&sm.full[s], (uint32_t)((g / NS) & 1), a.err, abort_flag)) break;
+          if (!wait_or_abort(&sm.sf_full[b], (uint32_t)((g >> 1) & 1), a.err, abort_flag)) break;
           tc_fence_after();
-          const uint32_t sfa = smem_addr(sm.sfa[s]), sfb = smem_addr(sm.sfb[s]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            tc_cp_32x128b_x4(tmem + kSfaCol + 4 * j, sf_smem_desc(sfa + 512 * j));
-            tc_cp_32x128b_x4(tmem + kSfbCol + 8 * j, sf_smem_desc(sfb + 512 * j));
-            tc_cp_32x128b_x4(tmem + kSfbCol + 8 * j + 4,
-                             sf_smem_desc(sfb + kTcSfRecBytes + 512 * j));
-          }
+          const uint32_t sf = tmem + kSfCol + kSfBufCols * b;
           const uint64_t ad = umma_desc_sw128(smem_addr(sm.a[s]));
           const uint64_t bd = umma_desc_sw128(smem_addr(sm.b[s]));
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            umma_nvf4(tmem + kAccCol, ad + 2 * j, bd + 2 * j, idesc, tmem + kSfaCol + 4 * j,
-                      tmem + kSfbCol + 8 * j, (kt == 0 && j == 0) ? 0u : 1u);
+            umma_nvf4(tmem + kAccCol, ad + 2 * j, bd + 2 * j, idesc, sf + 4 * j,
+                      sf + kSfbOff + 8 * j, (kt == 0 && j == 0) ? 0u : 1u);
           umma_commit(&sm.empty[s]);
+          umma_commit(&sm.sf_empty[b]);
         }
         if (*abort_flag) break;
         umma_commit(&sm.acc_full);
@@ -264,6 +284,41 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
       // is freed
       umma_commit(&sm.drain);
       mbar_wait_bounded(&sm.drain, 0, kWaitCycles);
+    }
+  } else if (warp == CP_WARP) {
+    // ------------------------------------------------------------ scale factors
+    if (lane == 0) {
+      long g = 0;
+      for (long t = blockIdx.x; t < ntiles_total && !*abort_flag; t += gridDim.x) {
+        int blk, nt;
+        tile_coords(t, a.nblocks, a.ntiles, blk, nt);
+        if ((long)blk * BM >= ntp) continue;
+        const int e = a.expert_ids[blk];
+        if (e < 0 || e >= a.El) continue;
+        for (int kt = 0; kt < KT; ++kt, ++g) {
+          const int s = (int)(g % NS);
+          const int b = (int)(g & 1);
+          // buffer b is free (the MMAs of stage g - 2 are done) and the
+          // stage's scale factors are in shared memory
+          if (!wait_or_abort(&sm.sf_empty[b], (uint32_t)(((g >> 1) & 1) ^ 1), a.err, abort_flag))
+            break;
+          if (!wait_or_abort(&sm.full[s], (uint32_t)((g / NS) & 1), a.err, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t sf = tmem + kSfCol + kSfBufCols * b;
+          const uint32_t sfa = smem_addr(sm.sfa[s]), sfb = smem_addr(sm.sfb[s]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tc_cp_32x128b_x4(sf + 4 * j, sf_smem_desc(sfa + 512 * j));
+            tc_cp_32x128b_x4(sf + kSfbOff + 8 * j, sf_smem_desc(sfb + 512 * j));
+            tc_cp_32x128b_x4(sf + kSfbOff + 8 * j + 4, sf_smem_desc(sfb + kTcSfRecBytes + 512 * j));
+          }
+          umma_commit(&sm.sf_full[b]);
+        }
+        if (*abort_flag) break;
+      }
+      // every copy issued above has completed before Tensor Memory is freed
+      umma_commit(&sm.cp_drain);
+      mbar_wait_bounded(&sm.cp_drain, 0, kWaitCycles);
     }
   } else {
     // ------------------------------------------------------------ epilogue
