@@ -338,6 +338,20 @@ int moe_reset_device_error(void);
  * for a limit out of range. */
 int moe_selftest_bounded_wait(long long limit_cycles, void *stream);
 
+/* Tensor-core rate probe (a measurement aid with no counterpart on the pages:
+ * it gives the benchmark the dense rate of each tcgen05 operand kind on this
+ * GPU).  Enqueues on `stream` one CTA per SM; each issues `iters` MMAs of
+ * 128 x n x k into Tensor Memory with its operands already in shared memory
+ * (no loads, no epilogue) and waits, bounded, for them to finish.
+ *   kind 0: f16 x f16 (k = 16);  kind 1: e4m3 x e4m3 (k = 32);
+ *   kind 2: e2m1 x e2m1 with ue4m3 scales per 16 (kind::mxf4nvf4, k = 64)
+ *   n: 128 or 256;  1 <= iters <= 2^31
+ * The work is sm_count * iters * 2 * 128 * n * k floating-point operations;
+ * *sm_count_out (may be NULL) receives the SM count used.  The caller times
+ * the launch (CUDA events on `stream`).  MOE_ERR_INVALID_ARG for arguments
+ * out of range (nothing launched). */
+int moe_mma_probe(int kind, int n, long long iters, int *sm_count_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

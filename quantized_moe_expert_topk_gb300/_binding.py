@@ -32,7 +32,7 @@ EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align
            "moe_get_device_error", "moe_reset_device_error", "moe_selftest_bounded_wait",
            "moe_noalloc_scratch_bytes",
            "moe_fused_experts_noalloc", "moe_packed_weight_bytes", "moe_prepare_weights",
-           "moe_stage_timing", "moe_stage_times", "moe_route_topk")
+           "moe_stage_timing", "moe_stage_times", "moe_route_topk", "moe_mma_probe")
 PATHS = {"auto": 0, "generic": 1, "stream": 2, "tc": 3}
 STAGES = ("align", "quant", "w13", "requant", "w2", "finalize")
 
@@ -94,6 +94,7 @@ def lib() -> ctypes.CDLL:
         "moe_packed_weight_bytes": (sz, [P, i, i]),
         "moe_prepare_weights": (i, [P, i, i, W, p, p]),
         "moe_stage_timing": (i, [i]),
+        "moe_mma_probe": (i, [i, i, ctypes.c_longlong, ctypes.POINTER(ctypes.c_int), p]),
         "moe_stage_times": (i, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -269,6 +270,19 @@ def moe_stage_times() -> tuple:
     calls = ctypes.c_int(0)
     _check("moe_stage_times", lib().moe_stage_times(ms, ctypes.byref(calls)))
     return dict(zip(STAGES, list(ms))), calls.value
+
+
+MMA_KINDS = {"f16": (0, 16), "e4m3": (1, 32), "nvfp4": (2, 64)}
+
+
+def moe_mma_probe(kind: str, n: int, iters: int, stream=None) -> float:
+    """Enqueue the tensor-core rate probe; returns the floating-point
+    operations it performs (time the launch with CUDA events on `stream`)."""
+    code, k = MMA_KINDS[kind]
+    sms = ctypes.c_int(0)
+    _check("moe_mma_probe", lib().moe_mma_probe(code, n, int(iters), ctypes.byref(sms),
+                                                _stream(stream)))
+    return float(sms.value) * iters * 2.0 * 128 * n * k
 
 
 def moe_get_device_error() -> int:

@@ -231,9 +231,9 @@ TcLayout make_tc_layout(const moe_problem_t *p) {
     // sorted e2m1 codes + scale-factor records of x; codes + records of the
     // intermediate; the fp32 accumulator
     L.a_sorted = o; o = align_up(o + (size_t)L.cap * p->K / 2);
-    L.a_sf = o; o = align_up(o + (size_t)L.blocks * ceil_div(p->K, kTcBsStage) * kTcSfRecBytes);
+    L.a_sf = o; o = align_up(o + (size_t)L.blocks * ceil_div(p->K, kTcBsStage) * kBsSfaRecBytes);
     L.inter = o; o = align_up(o + (size_t)L.cap * p->N / 2);
-    L.inter_sf = o; o = align_up(o + (size_t)L.blocks * ceil_div(p->N, kTcBsStage) * kTcSfRecBytes);
+    L.inter_sf = o; o = align_up(o + (size_t)L.blocks * ceil_div(p->N, kTcBsStage) * kBsSfaRecBytes);
     L.a_rowscale = L.a_groupscale = L.staging = L.i_scales = o;
     L.acc = o; o = align_up(o + (size_t)p->M * p->K * 4);
     L.total = o;
@@ -867,6 +867,17 @@ int moe_get_device_error(int *err_out) {
 int moe_reset_device_error(void) {
   const int zero = 0;
   return cuda_status(cudaMemcpyToSymbol(moe::g_device_error_word, &zero, sizeof(int)));
+}
+
+int moe_mma_probe(int kind, int n, long long iters, int *sm_count_out, void *stream) {
+  if (kind < 0 || kind > 2 || (n != 128 && n != 256) || iters < 1 || iters > (1LL << 31))
+    return MOE_ERR_INVALID_ARG;
+  DeviceInfo dinfo;
+  int rc = device_info(&dinfo);
+  if (rc != MOE_OK) return rc;
+  if (sm_count_out) *sm_count_out = dinfo.sm_count;
+  return cuda_status(launch_mma_probe(kind, n, (long)iters, dinfo.sm_count, dinfo.err,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 int moe_selftest_bounded_wait(long long limit_cycles, void *stream) {

@@ -17,7 +17,7 @@
 // end of the current one.  Warp roles:
 //   warp 0      TMA producer: per stage the A rows' codes (2-D TMA, 128-byte
 //               swizzle), the A scale-factor record, the B record (codes
-//               pre-swizzled + scale factors) -- 54 KB, one mbarrier
+//               pre-swizzled + scale factors) -- 72 KB, one mbarrier
 //   warp 1      TMEM owner; lane 0 issues each stage's four MMAs
 //   warps 2-17  epilogue: each thread owns one row and 64 accumulator
 //               columns; it copies them to registers, releases the
@@ -25,7 +25,9 @@
 //               the scales, bias, activation and NVFP4 quantiser (W13) or the
 //               router weight and the fp32 reduce (W2)
 //   warp 18     lane 0 copies each stage's scale factors from shared memory
-//               into one of two Tensor Memory buffers (tcgen05.cp), one stage
+//               into one of two Tensor Memory buffers (six tcgen05.cp
+//               .128x256b: two for A, four for B; a copy instruction costs
+//               the tensor pipe about the same whatever its width), one stage
 //               ahead of the MMAs that read them; a commit on sf_full hands
 //               the buffer to the MMA thread, whose commit on sf_empty hands
 //               it back
@@ -45,20 +47,24 @@ namespace {
 
 constexpr int BM = kTcBlockM;  // 128 sorted rows
 constexpr int BN = 256;        // weight rows per tile
-constexpr int NS = 4;          // stages in the ring
+constexpr int NS = 3;          // stages in the ring
 constexpr int STAGE_A = BM * 128;                  // 16 KB of A codes
 constexpr int STAGE_B = BN * 128;                  // 32 KB of B codes
-constexpr int SFB_BYTES = 2 * kTcSfRecBytes;       // B scale factors (256 rows)
+// B scale factors of a stage: one 4 KB .128x256b source per MMA step, row L =
+// [step words of rows L % 32 + 32 w of rows 0-127 | the same for rows
+// 128-255] (the layout of bs_sfa_offset with the B halves in place of the
+// step pair)
+constexpr int SFB_BYTES = 4 * 4096;
 constexpr int NUM_EPI = 16;
 constexpr int CP_WARP = 2 + NUM_EPI;               // warp 18
 constexpr int THREADS = (3 + NUM_EPI) * 32;        // 608
 constexpr int TMEM_COLS = 512;
 // Tensor Memory columns: accumulator [0, 256); two buffers of one stage's
 // scale factors (four MMA steps) at 256 + 48 b: A at +0 (4 columns per step),
-// B at +16 (8 per step: rows 0-127, then rows 128-255).  Layout of one
-// 128-row block's scale words as in moe_tc.cu's kind (row r in column
-// base + r / 32 of lane r % 32, in all four lane quarters; byte b scales the
-// b-th 16-element block of the step).
+// B at +16 (8 per step: rows 0-127, then rows 128-255).  Within the 4 columns
+// of a 128-row block and step, lane L column w holds the scale word of row
+// L % 32 + 32 w, the same in all four lane quarters; byte b of a word scales
+// the b-th 16-element block of the step.
 constexpr uint32_t kAccCol = 0, kSfCol = 256, kSfBufCols = 48, kSfbOff = 16;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int kErrTimeout = 5;
@@ -73,11 +79,16 @@ enum { MODE_W13 = 0, MODE_W2 = 1 };
 struct Smem {
   unsigned char a[NS][STAGE_A];
   unsigned char b[NS][STAGE_B];
-  unsigned char sfa[NS][kTcSfRecBytes];
+  unsigned char sfa[NS][kBsSfaRecBytes];
   unsigned char sfb[NS][SFB_BYTES];
   uint64_t full[NS], empty[NS];
   uint64_t sf_full[2], sf_empty[2];
   uint64_t acc_full, acc_empty, drain, cp_drain;
+  // W13: the scale factors of a tile's 128 intermediate columns (one 4 KB
+  // .128x256b source of the W2 operand; its 32 distinct rows) are assembled
+  // here and written out with 16-byte stores; double-buffered by tile
+  unsigned char sf_stage[2][1024];
+  uint64_t staged[2], freed[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -191,6 +202,10 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
     mbar_init(&sm.acc_empty, NUM_EPI);
     mbar_init(&sm.drain, 1);
     mbar_init(&sm.cp_drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.staged[b], NUM_EPI);
+      mbar_init(&sm.freed[b], NUM_EPI);
+    }
     sm.abort_flag = 0;
     mbar_fence_init();
   }
@@ -218,7 +233,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
         const unsigned char *brec = static_cast<const unsigned char *>(a.w_packed) +
                                     ((long)e * a.ntiles + nt) * KT * (long)(STAGE_B + SFB_BYTES);
         const unsigned char *asf = static_cast<const unsigned char *>(a.a_sf) +
-                                   (long)blk * KT * kTcSfRecBytes;
+                                   (long)blk * KT * kBsSfaRecBytes;
         const bool leader = (blk % kRasterGroup) == 0;
         if (leader && kPrefetchAhead > 0)
           prefetch_l2_bulk(brec, (uint32_t)(min(KT, kPrefetchAhead) * (STAGE_B + SFB_BYTES)));
@@ -231,9 +246,9 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
             break;
           }
           const unsigned char *rec = brec + (long)kt * (STAGE_B + SFB_BYTES);
-          mbar_arrive_expect_tx(&sm.full[s], STAGE_A + kTcSfRecBytes + STAGE_B + SFB_BYTES);
+          mbar_arrive_expect_tx(&sm.full[s], STAGE_A + kBsSfaRecBytes + STAGE_B + SFB_BYTES);
           tma_load_2d(sm.a[s], &tmA, kt * 128, blk * BM, &sm.full[s]);
-          tma_bulk_g2s(sm.sfa[s], asf + (long)kt * kTcSfRecBytes, kTcSfRecBytes, &sm.full[s]);
+          tma_bulk_g2s(sm.sfa[s], asf + (long)kt * kBsSfaRecBytes, kBsSfaRecBytes, &sm.full[s]);
           tma_bulk_g2s(sm.b[s], rec, STAGE_B, &sm.full[s]);
           tma_bulk_g2s(sm.sfb[s], rec + STAGE_B, SFB_BYTES, &sm.full[s]);
         }
@@ -307,11 +322,11 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
           const uint32_t sf = tmem + kSfCol + kSfBufCols * b;
           const uint32_t sfa = smem_addr(sm.sfa[s]), sfb = smem_addr(sm.sfb[s]);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            tc_cp_32x128b_x4(sf + 4 * j, sf_smem_desc(sfa + 512 * j));
-            tc_cp_32x128b_x4(sf + kSfbOff + 8 * j, sf_smem_desc(sfb + 512 * j));
-            tc_cp_32x128b_x4(sf + kSfbOff + 8 * j + 4, sf_smem_desc(sfb + kTcSfRecBytes + 512 * j));
-          }
+          for (int p = 0; p < 2; ++p)  // A: steps 2p, 2p + 1 -> columns 8p .. 8p + 7
+            tc_cp_128x256b(sf + 8 * p, sf256_smem_desc(sfa + 4096 * p));
+#pragma unroll
+          for (int j = 0; j < 4; ++j)  // B: step j -> columns 8j .. 8j + 7
+            tc_cp_128x256b(sf + kSfbOff + 8 * j, sf256_smem_desc(sfb + 4096 * j));
           umma_commit(&sm.sf_full[b]);
         }
         if (*abort_flag) break;
@@ -325,7 +340,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
     const int q = warp & 3;             // TMEM lane quarter of this warp
     const int cq = (warp - 2) >> 2;     // column quarter: tile columns [64 cq, 64 cq + 64)
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16) + kAccCol + 64 * cq;
-    long tc = 0;
+    long tc = 0, etile = 0;
     const float a_sc = a.a_scalar ? a.a_scalar[0] : 1.f;
     const long ks_out = ceil_div(a.N, kTcBsStage);
     for (long t = blockIdx.x; t < ntiles_total; t += gridDim.x) {
@@ -362,10 +377,11 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
         const float zw = (a.w_stage1 && live) ? a.topk_weights[s_id] : 1.f;
         const int jbase = nt * 128 + 32 * cq;
         const bool sep = a.gate == GATE_SEPARATED;
-        uint8_t *sf = static_cast<uint8_t *>(a.out_sf);
+        uint8_t sfq[2] = {0, 0};  // this thread's two group scales (0 past N)
         if (jbase < a.N) {  // N % 32 == 0: all 32 outputs in range or none
           const uint16_t *bias = static_cast<const uint16_t *>(a.w_bias);
           const float *bias32 = static_cast<const float *>(a.w_bias);
+          uint32_t codes[4];
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             float z[16];
@@ -383,23 +399,47 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
               }
               z[i] = live ? zw * act_fast(a.act, gv, uv, a.alpha, a.beta, a.limit) : 0.f;
             }
-            uint32_t lo, hi;
-            const uint32_t sq = nvfp4_quant16_fast(z, a.out_global[e], lo, hi);
-            const long j0 = jbase + 16 * p;
-            *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.out) + r * (a.N / 2) + j0 / 2) =
-                make_uint2(lo, hi);
-            sf[tc_sf_offset(r, j0, ks_out)] = (uint8_t)sq;
+            sfq[p] = (uint8_t)nvfp4_quant16_fast(z, a.out_global[e], codes[2 * p], codes[2 * p + 1]);
           }
+          *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.out) + r * (a.N / 2) + jbase / 2) =
+              make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        }
+        // scale factors: this thread's two bytes into the staged source (row
+        // lane, half cq / 2, word q, bytes 2 (cq % 2) + {0, 1}), then every
+        // epilogue warp writes 16 of the source's 256 16-byte pieces
+        const int sb = (int)(etile & 1);
+        const uint32_t sph = (uint32_t)((etile >> 1) & 1);
+        bool ok = mbar_wait_bounded(&sm.freed[sb], sph ^ 1, kWaitCycles, a.err);
+        if (ok) {
+          *reinterpret_cast<uint16_t *>(&sm.sf_stage[sb][lane * 32 + (cq >> 1) * 16 + q * 4 +
+                                                        2 * (cq & 1)]) =
+              (uint16_t)(sfq[0] | (sfq[1] << 8));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.staged[sb]);
+          ok = mbar_wait_bounded(&sm.staged[sb], sph, kWaitCycles, a.err);
+        }
+        if (ok) {
+          const int ew = warp - 2;
+          uint8_t *sfo = static_cast<uint8_t *>(a.out_sf) +
+                         ((long)blk * ks_out + nt / 2) * kBsSfaRecBytes + (nt & 1) * 4096;
+          // the tile after the last one, if the last stage's second pair has
+          // no tile, gets zero scale factors
+          const bool tail = nt == a.ntiles - 1 && (nt & 1) == 0;
+          if (lane < 16) {
+            const int x = ew * 16 + lane;                  // 0..255
+            const int i = (x % 64) >> 1, half = x & 1, L = i + 32 * (x / 64);
+            const long off = (L / 8) * 256 + half * 128 + (L % 8) * 16;
+            *reinterpret_cast<uint4 *>(sfo + off) =
+                *reinterpret_cast<const uint4 *>(&sm.sf_stage[sb][i * 32 + half * 16]);
+            if (tail) *reinterpret_cast<uint4 *>(sfo + 4096 + off) = make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.freed[sb]);
         } else {
-          // no outputs here: the scale factors of this part of the
-          // intermediate's reduction must read as zero in the W2 stage
-          for (long j0 = jbase; j0 < jbase + 32 && j0 < ks_out * kTcBsStage; j0 += 16)
-            sf[tc_sf_offset(r, j0, ks_out)] = 0;
+          record_device_error(a.err, kErrTimeout);
+          *abort_flag = 1;
         }
-        if (nt == a.ntiles - 1 && cq == 3) {  // reduction tail beyond the last tile
-          for (long j0 = (long)a.ntiles * 128; j0 < ks_out * kTcBsStage; j0 += 16)
-            sf[tc_sf_offset(r, j0, ks_out)] = 0;
-        }
+        ++etile;
       } else if (live) {
         const long tok = s_id / a.T;
         const float wt = (a.w_stage1 ? 1.f : a.topk_weights[s_id]);
@@ -441,9 +481,8 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
 // Load-time records of NVFP4 weights for this kernel: per (expert, n-tile of
 // 256 weight rows, 256-wide reduction stage) the 256 tile rows' codes (128
 // bytes each, 128-byte swizzle: 16-byte chunk c of row n at
-// (n / 8) * 1024 + (n % 8) * 128 + ((c ^ (n % 8)) * 16)), then the scale
-// factors of rows 0-127 and of rows 128-255 (one record each, in the order
-// of tc_sf_offset).  W13 tile rows: SEPARATED -> eight groups of 32 rows,
+// (n / 8) * 1024 + (n % 8) * 128 + ((c ^ (n % 8)) * 16)), then the stage's
+// scale factors as four .128x256b sources (SFB_BYTES).  W13 tile rows: SEPARATED -> eight groups of 32 rows,
 // gate and up of outputs j0 + 32 i alternating; INTERLEAVED -> the rows
 // 2 j0 .. 2 j0 + 255 as stored.  Zeros past the tensor.  One thread per byte.
 __global__ void pack_bs_kernel(TcPackArgs p) {
@@ -464,11 +503,14 @@ __global__ void pack_bs_kernel(TcPackArgs p) {
     const int c = ((wb % 128) / 16) ^ (n & 7);
     k = (long)kt * 128 + c * 16 + (wb % 16);
   } else {
+    // source j (MMA step), row L, byte y of its 32: half y / 16 of the tile
+    // rows, scale word (y % 16) / 4 -> tile row 128 half + 32 w + L % 32
     const int w = wb - STAGE_B;
-    const int half = w / kTcSfRecBytes, ww = w % kTcSfRecBytes;
-    const int j = ww / 512, x = ww % 512;
-    n = 128 * half + 32 * ((x % 16) / 4) + x / 16;
-    k = (long)kt * 16 + j * 4 + (x % 4);
+    const int j = w / 4096, x = w % 4096;
+    const int L = (x / 256) * 8 + (x % 128) / 16;
+    const int y = ((x % 256) / 128) * 16 + (x % 16);
+    n = 128 * (y / 16) + 32 * ((y % 16) / 4) + (L % 32);
+    k = (long)kt * 16 + j * 4 + (y % 4);
   }
   const int b = n >> 5;  // 32-row group 0..7
   long row;

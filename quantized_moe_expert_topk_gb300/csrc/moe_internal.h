@@ -187,18 +187,26 @@ cudaError_t launch_stream_fused(const StreamArgs &a13, const StreamArgs &a2, int
 enum { TC_OUT_BF16 = 0, TC_OUT_F32 = 1, TC_OUT_F16 = 2, TC_OUT_NVFP4_F16 = 3, TC_OUT_MX4_F16 = 4,
        TC_OUT_MX8_F16 = 5 };
 
-// Block-scaled NVFP4 operands (moe_bs.cu): every 256-element
-// reduction stage of a 128-row block carries one scale-factor record of
-// kTcSfRecBytes: four 512-byte chunks, one per 64-element MMA step, in the
-// order tcgen05.cp .32x128b.warpx4 expects (byte 16*(r%32) + 4*(r/32) + b of
-// chunk j = the ue4m3 scale of elements [64 j + 16 b, 64 j + 16 b + 16) of row
-// r of the block).
-constexpr int kTcBsStage = 256;                   // reduction elements per stage
-constexpr int kTcSfRecBytes = 2048;               // 4 x 512
-__host__ __device__ constexpr long tc_sf_offset(long r, long j, long ks_count) {
-  // byte of the scale of element j (along the reduction) of block row r
-  return ((r / 128) * ks_count + j / kTcBsStage) * kTcSfRecBytes +
-         ((j % kTcBsStage) / 64) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (j % 64) / 16;
+// Block-scaled NVFP4 operands (moe_bs.cu).  Every 256-element reduction
+// stage of a 128-row block of the A operand carries an 8 KB scale-factor
+// record: two 4 KB sources of tcgen05.cp .128x256b, one per pair of 64-element
+// MMA steps (2p, 2p + 1).  A source is 128 rows of 32 bytes, no swizzle, in
+// 8-row x 16-byte core matrices (the row's two 16-byte halves 128 bytes apart,
+// 8-row groups 256 bytes apart).  Row L holds, in its first half, the scale
+// words of step 2p of block rows L % 32 + 32 w (w = 0..3; byte b of word w
+// scales elements [16 b, 16 b + 16) of the step) and, in its second half,
+// those of step 2p + 1: rows L, L + 32, L + 64 and L + 96 hold the same bytes,
+// which is the replication across the four 32-lane quarters of Tensor Memory
+// that the scale factors of an M = 128 MMA need (lane L, column 4 j + w = the
+// word of row L % 32 + 32 w for step j).
+constexpr int kTcBsStage = 256;      // reduction elements per stage
+constexpr int kBsSfaRecBytes = 8192; // 2 x 4 KB per (128-row block, stage)
+// Byte offset of the scale of element j (along the reduction) of block row r
+// in replica 0; the same byte is also stored at +1024, +2048 and +3072.
+__host__ __device__ constexpr long bs_sfa_offset(long r, long j, long ks_count) {
+  return ((r / 128) * ks_count + j / kTcBsStage) * kBsSfaRecBytes +
+         ((j % kTcBsStage) / 128) * 4096 + ((r % 32) / 8) * 256 + (((j % kTcBsStage) / 64) & 1) * 128 +
+         (r % 8) * 16 + ((r % 128) / 32) * 4 + (j % 64) / 16;
 }
 struct TcArgs {
   int M, K, N, T, El, R, C;
@@ -269,6 +277,11 @@ size_t bs_packed_bytes(int w13, int N, int K, int El);
 cudaError_t launch_pack_bs(const TcPackArgs &p, cudaStream_t st);
 cudaError_t launch_bs_gemm(const TcArgs &a, const void *a_codes, long cap_rows, int w13,
                            int sm_count, cudaStream_t st);
+
+// Tensor-core rate probe (moe_probe.cu): sm_count CTAs, each issuing `iters`
+// MMAs of 128 x n (kind 0: f16, 1: e4m3, 2: e2m1 + ue4m3 block scales).
+cudaError_t launch_mma_probe(int kind, int n, long iters, int sm_count, int *err,
+                             cudaStream_t st);
 
 cudaError_t launch_route(const void *logits, int bf16_in, int M, int E, int topk, int scoring,
                          int renorm, int G, int TG, const float *bias, float scale, int32_t *ids,

@@ -367,6 +367,27 @@ __device__ __forceinline__ uint64_t sf_smem_desc(uint32_t saddr) {
   return d;                                   // layout 0: no swizzle
 }
 
+// Shared-memory descriptor of a 128-row x 32-byte source for tcgen05.cp
+// .128x256b: no swizzle, 8-row x 16-byte core matrices; the two core
+// matrices of a row group 128 bytes apart (leading byte offset, along the
+// row), row groups 256 bytes apart (stride byte offset).
+__device__ __forceinline__ uint64_t sf256_smem_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);   // start address
+  d |= (uint64_t)(128 >> 4) << 16;           // leading byte offset
+  d |= (uint64_t)(256 >> 4) << 32;           // stride byte offset
+  d |= (uint64_t)1 << 46;                     // descriptor version
+  return d;                                   // layout 0: no swizzle
+}
+
+// Copy 128 rows x 256 bits from shared memory (descriptor) to Tensor Memory
+// columns [taddr, taddr + 8): lane L, column c + w receives bytes
+// [4 w, 4 w + 4) of row L.  Issued by one thread; ordered before the MMAs it
+// issues later.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Copy 32 rows x 128 bits from shared memory (descriptor) to Tensor Memory
 // columns [taddr, taddr + 4), replicated into all four 32-lane quarters
 // (.warpx4): lane 32q + i, column c + w holds bytes [16 i + 4 w, 16 i + 4 w + 4)

@@ -568,8 +568,12 @@ __global__ void gather_rows_kernel(GatherArgs g) {
     const int G = g.K / 16;
     const uint8_t *sc = static_cast<const uint8_t *>(g.scales) + t * G;
     uint8_t *sf = static_cast<uint8_t *>(g.sf_out);
-    for (int w = lane; w < KS * 16; w += 32)
-      sf[tc_sf_offset(r, (long)w * 16, KS)] = (live && w < G) ? sc[w] : 0;
+    for (int w = lane; w < KS * 16; w += 32) {
+      const uint8_t v = (live && w < G) ? sc[w] : 0;
+      const long o = bs_sfa_offset(r, (long)w * 16, KS);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sf[o + 1024 * q] = v;
+    }
   } else if (g.afmt == A_NVFP4_DYN) {
     // exact f16 (or bf16) of e2m1 * e4m3 scale; the global is applied later
     uint16_t *dst = static_cast<uint16_t *>(g.out) + r * g.K;

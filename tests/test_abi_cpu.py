@@ -119,7 +119,11 @@ def test_packed_weight_sizes(moe):
     assert moe.moe_packed_weight_bytes(r, 0, "tc") == 32 * (2848 // 64 + 1) * (2880 // 64) * 4352
     n = moe.make_problem(64, 4096, 1024, 2, 8, 8, "nvfp4", "nvfp4_dyn", "silu", "separated")
     n.a1_scale = n.a2_scale = 0x1000  # never dereferenced by a size query
-    assert moe.moe_packed_weight_bytes(n, 1, "tc") == 8 * (4096 // 128) * (1024 // 64) * 4608
+    # NVFP4 (block-scaled kind): per (expert, 256-row tile, 256-wide stage)
+    # 256 rows x 128 code bytes + four 4 KB scale-factor sources (each scale
+    # byte replicated for the four 32-lane quarters of Tensor Memory)
+    assert moe.moe_packed_weight_bytes(n, 1, "tc") == 8 * (4096 // 256) * (1024 // 256) * (32768 + 16384)
+    assert moe.moe_packed_weight_bytes(n, 0, "tc") == 8 * (1024 // 128) * (4096 // 256) * (32768 + 16384)
 
 
 def test_route_validation(moe):
