@@ -6,10 +6,13 @@
 A step is one pass of the whole hot path (sort/pad, activation quantisation
 where the format has one, w13 GEMM + activation, w2 GEMM + weighted reduce,
 bf16 output) over one batch, launched as one CUDA graph.  The default
-workload is the GPT-OSS-20B-shaped MXFP4 w4a16 decode layer (M=64, K=N=2880,
-E=32, top-4); every step streams all 32 experts' weights (424 MB > 129 MB L2),
-so no L2 flush is needed between steps.  Under torchrun each rank runs an
-independent replica (weak scaling: the path has no exchange step on one GPU).
+workload is the largest configuration, the Mixtral-8x7B-shaped NVFP4 w4a4
+prefill layer (M=8192, K=4096, N=14336, E=8, top-2); every step streams all
+8 experts' weights (0.9 GB of packed records > 129 MB L2), so no L2 flush is
+needed between steps.  --workload picks another (the GPT-OSS-20B MXFP4 decode
+layer, the DeepSeek-V3 FP8-block prefill, the GPT-OSS-120B sweep with --M).
+Under torchrun each rank runs an independent replica (weak scaling: the path
+has no exchange step on one GPU).
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
 token sample of the same workload (the slow program parity is checked
@@ -29,7 +32,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "gptoss20b_mxfp4_m64"
+DEFAULT_WORKLOAD = "mixtral_nvfp4_m8192"
 METRIC = "MoE layer tokens/s on 1 GB300"
 UNIT = "tokens/s"
 
@@ -146,10 +149,13 @@ def algorithmic(wl, counts):
 
 def mma_dtype(wl):
     """Operand type of the tensor-core contraction the CUDA path runs for this
-    workload: the streaming kernels and the tcgen05 FP4 kinds use exact f16
-    decodes, the tcgen05 FP8 kinds e4m3, everything else (and the generic
-    kernels) exact bf16 decodes."""
+    workload: NVFP4 on the tcgen05 path multiplies e2m1 codes with ue4m3 block
+    scales (kind::mxf4nvf4); the streaming kernels and the tcgen05 MXFP4
+    kinds use exact f16 decodes, the tcgen05 FP8 kinds e4m3, everything else
+    (and the generic kernels) exact bf16 decodes."""
     path = kernel_path(wl)
+    if wl.wfmt == "nvfp4" and path == "tc":
+        return "nvfp4"
     if wl.wfmt in ("mxfp4", "nvfp4") and path in ("stream", "tc"):
         return "f16"
     if path == "tc" and wl.wfmt.startswith("fp8"):
@@ -403,17 +409,20 @@ def run_ours(args):
     k_bytes = alg["fused_kernel_bytes"] if fused else alg["w13_kernel_bytes"]
     k_flops = alg["flops"] if fused else alg["w13_flops"]
     hbm, bf16_tf, peak_src = measured_peaks()
-    # the contraction's own dtype: f16 and bf16 share the dense rate; e4m3 is the
-    # measured bf16 rate times the nominal 2x ratio (4.5 / 2.25 PFLOP/s)
-    tens_tf = bf16_tf * (2.0 if mma_dtype(wl) == "e4m3" else 1.0)
-    if mma_dtype(wl) == "e4m3":
-        peak_src += " (bf16 x 2, nominal e4m3 ratio)"
+    # the contraction's own dtype: f16 and bf16 share the dense rate; e4m3 and
+    # NVFP4 take the measured bf16 rate times the nominal ratios of the dense
+    # peaks (4.5 / 2.25 and 13.5 / 2.25 PFLOP/s)
+    ratio = NOMINAL_RATIO[mma_dtype(wl)]
+    tens_tf = bf16_tf * ratio
+    if ratio != 1.0:
+        peak_src += f" (bf16 x {ratio:g}, nominal {mma_dtype(wl)} ratio)"
     t_hbm = k_bytes / (hbm * 1e9)
     t_tensor = k_flops / (tens_tf * 1e12)
     if t_hbm >= t_tensor:
         bound, achieved, peak, punit = "hbm", k_bytes / (k_ms / 1e3) / 1e9, hbm, "GB/s"
     else:
         bound, achieved, peak, punit = "tensor", k_flops / (k_ms / 1e3) / 1e12, tens_tf, "TFLOP/s"
+    probe = probe_tflops(moe, mma_dtype(wl), stream)
     traffic = profile_traffic("moe_stream_fused" if fused else "moe_w13", wl.name)
     layer_roof_ms = max(alg["layer_bytes"] / (hbm * 1e9), alg["flops"] / (tens_tf * 1e12)) * 1e3
 
@@ -435,7 +444,11 @@ def run_ours(args):
                      "alg_bytes_per_launch": k_bytes,
                      "alg_flops_per_launch": k_flops,
                      "kernel_ms": k_ms, "peak_source": peak_src,
-                     "stage_ms": stage_ms},
+                     "stage_ms": stage_ms,
+                     # the same kind's dense MMA rate measured on this GPU by the
+                     # library's probe (128 x 256 tiles, operands in shared memory)
+                     "probe_tflops": probe,
+                     "frac_of_probe": (k_flops / (k_ms / 1e3) / 1e12 / probe) if probe else None},
         "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms,
                            "alg_bytes": alg["layer_bytes"], "alg_flops": alg["flops"],
                            "active_experts": alg["active_experts"], "live_slots": alg["live_slots"]},
@@ -458,6 +471,25 @@ def run_ours(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+NOMINAL_RATIO = {"bf16": 1.0, "f16": 1.0, "e4m3": 2.0, "nvfp4": 6.0}
+
+
+def probe_tflops(moe, kind, stream, iters=1 << 16):
+    """Dense tcgen05 MMA rate of the kind (TFLOP/s), measured with the
+    library's probe (moe_mma_probe: one CTA per SM, 128 x 256 MMAs on operands
+    resident in shared memory), CUDA events on its stream."""
+    import torch
+    k = {"bf16": "f16", "f16": "f16", "e4m3": "e4m3", "nvfp4": "nvfp4"}[kind]
+    with torch.cuda.stream(stream):
+        moe.moe_mma_probe(k, 256, 4096, stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        flops = moe.moe_mma_probe(k, 256, iters, stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return flops / (a.elapsed_time(b) / 1e3) / 1e12
 
 
 def expert_counts(moe, wl, dev):

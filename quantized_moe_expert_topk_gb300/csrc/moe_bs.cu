@@ -25,15 +25,17 @@
 //               the scales, bias, activation and NVFP4 quantiser (W13) or the
 //               router weight and the fp32 reduce (W2)
 //   warp 18     lane 0 copies each stage's scale factors from shared memory
-//               into one of two Tensor Memory buffers (six tcgen05.cp
+//               into the stage's own Tensor Memory buffer (six tcgen05.cp
 //               .128x256b: two for A, four for B; a copy instruction costs
-//               the tensor pipe about the same whatever its width), one stage
-//               ahead of the MMAs that read them; a commit on sf_full hands
-//               the buffer to the MMA thread, whose commit on sf_empty hands
-//               it back
+//               the tensor pipe about the same whatever its width) as soon as
+//               the stage has landed, and hands it to the MMA thread with a
+//               commit on sf_full; the buffer is free again when the stage's
+//               MMAs are (the producer's next copies into the stage, which
+//               this warp waits for, come after that)
 // Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, stops
 // issuing, lets its copies and MMAs land, frees its Tensor Memory and exits.
 #include <cuda.h>
+#include <stddef.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -59,8 +61,8 @@ constexpr int NUM_EPI = 16;
 constexpr int CP_WARP = 2 + NUM_EPI;               // warp 18
 constexpr int THREADS = (3 + NUM_EPI) * 32;        // 608
 constexpr int TMEM_COLS = 512;
-// Tensor Memory columns: accumulator [0, 256); two buffers of one stage's
-// scale factors (four MMA steps) at 256 + 48 b: A at +0 (4 columns per step),
+// Tensor Memory columns: accumulator [0, 256); one buffer of scale factors
+// (four MMA steps) per ring stage at 256 + 48 s: A at +0 (4 columns per step),
 // B at +16 (8 per step: rows 0-127, then rows 128-255).  Within the 4 columns
 // of a 128-row block and step, lane L column w holds the scale word of row
 // L % 32 + 32 w, the same in all four lane quarters; byte b of a word scales
@@ -82,17 +84,23 @@ struct Smem {
   unsigned char sfa[NS][kBsSfaRecBytes];
   unsigned char sfb[NS][SFB_BYTES];
   uint64_t full[NS], empty[NS];
-  uint64_t sf_full[2], sf_empty[2];
+  uint64_t sf_full[NS];
   uint64_t acc_full, acc_empty, drain, cp_drain;
   // W13: the scale factors of a tile's 128 intermediate columns (one 4 KB
   // .128x256b source of the W2 operand; its 32 distinct rows) are assembled
   // here and written out with 16-byte stores; double-buffered by tile
-  unsigned char sf_stage[2][1024];
+  alignas(16) unsigned char sf_stage[2][1024];  // read and written in 16-byte pieces
   uint64_t staged[2], freed[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
+// operand stages start on 1024-byte boundaries (128-byte swizzle atoms), the
+// scale-factor sources and the staging buffer on 16-byte ones (bulk copies,
+// tcgen05.cp, 16-byte shared-memory accesses)
+static_assert(offsetof(Smem, b) % 1024 == 0 && offsetof(Smem, sfa) % 16 == 0 &&
+                  offsetof(Smem, sfb) % 16 == 0 && offsetof(Smem, sf_stage) % 16 == 0,
+              "shared-memory layout alignment");
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *err,
                                               volatile int *abort_flag) {
@@ -194,10 +202,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.sf_full[b], 1);
-      mbar_init(&sm.sf_empty[b], 1);
-    }
+    for (int s = 0; s < NS; ++s) mbar_init(&sm.sf_full[s], 1);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_empty, NUM_EPI);
     mbar_init(&sm.drain, 1);
@@ -275,13 +280,11 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
         tc_fence_after();
         for (int kt = 0; kt < KT; ++kt, ++g) {
           const int s = (int)(g % NS);
-          const int b = (int)(g & 1);
-          // the stage's operands have landed and its scale factors are in
-          // Tensor Memory buffer b
-          if (!wait_or_abort(&sm.full[s], (uint32_t)((g / NS) & 1), a.err, abort_flag)) break;
-          if (!wait_or_abort(&sm.sf_full[b], (uint32_t)((g >> 1) & 1), a.err, abort_flag)) break;
+          // the stage's operands have landed (the scale-factor warp waited
+          // for them) and its scale factors are in Tensor Memory buffer s
+          if (!wait_or_abort(&sm.sf_full[s], (uint32_t)((g / NS) & 1), a.err, abort_flag)) break;
           tc_fence_after();
-          const uint32_t sf = tmem + kSfCol + kSfBufCols * b;
+          const uint32_t sf = tmem + kSfCol + kSfBufCols * s;
           const uint64_t ad = umma_desc_sw128(smem_addr(sm.a[s]));
           const uint64_t bd = umma_desc_sw128(smem_addr(sm.b[s]));
 #pragma unroll
@@ -289,7 +292,6 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
             umma_nvf4(tmem + kAccCol, ad + 2 * j, bd + 2 * j, idesc, sf + 4 * j,
                       sf + kSfbOff + 8 * j, (kt == 0 && j == 0) ? 0u : 1u);
           umma_commit(&sm.empty[s]);
-          umma_commit(&sm.sf_empty[b]);
         }
         if (*abort_flag) break;
         umma_commit(&sm.acc_full);
@@ -312,14 +314,12 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
         if (e < 0 || e >= a.El) continue;
         for (int kt = 0; kt < KT; ++kt, ++g) {
           const int s = (int)(g % NS);
-          const int b = (int)(g & 1);
-          // buffer b is free (the MMAs of stage g - 2 are done) and the
-          // stage's scale factors are in shared memory
-          if (!wait_or_abort(&sm.sf_empty[b], (uint32_t)(((g >> 1) & 1) ^ 1), a.err, abort_flag))
-            break;
+          // the stage has landed: its scale factors are in shared memory and
+          // buffer s is free (the producer refilled the stage only after the
+          // MMAs of its previous round completed)
           if (!wait_or_abort(&sm.full[s], (uint32_t)((g / NS) & 1), a.err, abort_flag)) break;
           tc_fence_after();
-          const uint32_t sf = tmem + kSfCol + kSfBufCols * b;
+          const uint32_t sf = tmem + kSfCol + kSfBufCols * s;
           const uint32_t sfa = smem_addr(sm.sfa[s]), sfb = smem_addr(sm.sfb[s]);
 #pragma unroll
           for (int p = 0; p < 2; ++p)  // A: steps 2p, 2p + 1 -> columns 8p .. 8p + 7
@@ -327,7 +327,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
 #pragma unroll
           for (int j = 0; j < 4; ++j)  // B: step j -> columns 8j .. 8j + 7
             tc_cp_128x256b(sf + kSfbOff + 8 * j, sf256_smem_desc(sfb + 4096 * j));
-          umma_commit(&sm.sf_full[b]);
+          umma_commit(&sm.sf_full[s]);
         }
         if (*abort_flag) break;
       }

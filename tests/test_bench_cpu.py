@@ -50,6 +50,22 @@ def test_mma_dtype():
     assert bench.mma_dtype(make_workload("gptoss20b_mxfp4_m64")) == "f16"
     assert bench.mma_dtype(make_workload("gptoss20b_w4a8_m64")) == "f16"
     assert bench.mma_dtype(make_workload("tiny_bf16_m16")) == "bf16"
+    # NVFP4 prefill: the block-scaled FP4 kind, measured against the bf16 peak
+    # times the nominal FP4 / bf16 ratio of the dense peaks (13.5 / 2.25)
+    assert bench.mma_dtype(make_workload("mixtral_nvfp4_m8192")) == "nvfp4"
+    assert bench.NOMINAL_RATIO["nvfp4"] == 6.0 and bench.NOMINAL_RATIO["e4m3"] == 2.0
+    assert bench.mma_dtype(make_workload("dsv3_fp8block_m4096")) == "e4m3"
+
+
+def test_default_workload_is_the_largest_configuration():
+    # the NVFP4 Mixtral prefill has the most tokens and FLOPs of the five
+    assert bench.DEFAULT_WORKLOAD == "mixtral_nvfp4_m8192"
+    flops = {}
+    for name in ("tiny_bf16_m16", "gptoss20b_mxfp4_m64", "dsv3_fp8block_m4096",
+                 "gptoss120b_mxfp4_ep75", "mixtral_nvfp4_m8192"):
+        s = shape(name, M=8192) if name == "gptoss120b_mxfp4_ep75" else shape(name)
+        flops[name] = 6.0 * s.N * s.K * s.M * s.T
+    assert max(flops, key=flops.get) == bench.DEFAULT_WORKLOAD
 
 
 def test_launches_per_step():
