@@ -250,19 +250,44 @@ int moe_route_topk(const void *logits, int logits_bf16, int M, int num_experts, 
 int moe_quant_act(const void *x_bf16, int rows, int cols, int afmt, const float *scale_in,
                   void *codes, void *scales, void *stream);
 
-/* Stage-1 grouped GEMM + activation (+ stage-2 requantisation).
+/* Stage-1 grouped GEMM + activation (+ stage-2 requantisation), the first of
+ * the two stages rocm_aiter_fused_experts runs (the gate/up GEMM with the
+ * activation and the next stage's quantisation).
  * For every sorted row r < *num_post_pad with slot s = sorted_ids[r] < S,
  * token t = s / topk, local expert e = expert_ids[r / block_m]:
  *   h = dequant(A[t]) . dequant(W13[e])^T + b13[e];  z_j = act(gate_j, up_j)
- * and writes row r of the intermediate: bf16 [cap, N] for BF16 / MXFP4
- * weights; otherwise codes + scales in the stage-2 format
- * (u8 [cap, N] or [cap, N/2], scales f32 [cap] / [cap, ceil(N/128)] /
- * [1] or e4m3 [cap, N/16]).  Padding rows are written as zeros.
+ * and writes row r of the intermediate (padding rows as zeros).
  *   a_codes / a_scales: x bf16 [M, K] for bf16 activations, else the output of
- *   moe_quant_act.  block_m must be 64 (the tile height of this kernel).
- *   workspace: device scratch of moe_w13_workspace_size() bytes (fp32 staging
- *   of the pre-quantisation intermediate); may be NULL when that size is 0. */
+ *   moe_quant_act.  sorted_ids / expert_ids / num_post_pad: the output of
+ *   moe_align_block_size with the same block_m.
+ *   block_m = 64: the generic mma.sync kernels (every supported pair).
+ *   block_m = 128: the tcgen05 kernels (bf16, fp8 and NVFP4 activations; FP4
+ *     weights must carry their MOE_LAYOUT_TC records in packed_tc; OCP MX
+ *     activations return MOE_ERR_UNSUPPORTED).
+ * The intermediate (inter / inter_scales, sizes from moe_intermediate_size):
+ *   bf16 weights:  bf16 [cap, N];
+ *   FP8 weights:   e4m3 codes [cap, N] + the stage-2 scales (f32 [1] / [cap] /
+ *                  [cap, ceil(N/128)] for tensor / token / 1x128 groups);
+ *   MXFP4 w4a16:   block_m 64: bf16 [cap, N];  block_m 128: f16 [cap, N],
+ *                  multiplied per row by inter_scales f32 [cap] unless the
+ *                  activation is SwiGLU-OAI with 0 < limit <= 64 and
+ *                  |beta| <= 64 (then the f16 values themselves, no scales);
+ *   MXFP4 w4a4 / w4a8 (block_m 64): codes + e8m0 scales [cap, N/32];
+ *   NVFP4:         e2m1 codes [cap, N/2] (element 2i in the low nibble) +
+ *                  block_m 64: e4m3 scales [cap, N/16];  block_m 128: the
+ *                  block-scaled records: for each 128-row block and each
+ *                  256-column stage 8192 bytes, in which the scale of row r,
+ *                  column j sits at byte (((j % 256) / 128) * 4096
+ *                  + ((r % 32) / 8) * 256 + (((j % 256) / 64) % 2) * 128
+ *                  + (r % 8) * 16 + ((r % 128) / 32) * 4 + (j % 64) / 16) and
+ *                  again at +1024, +2048 and +3072 of its record (record
+ *                  index (r / 128) * ceil(N/256) + j / 256).
+ *   workspace: device scratch of moe_w13_workspace_size() bytes (block_m 64:
+ *   fp32 staging of a requantised intermediate; block_m 128: the gathered
+ *   rows); may be NULL when that size is 0. */
 size_t moe_w13_workspace_size(const moe_problem_t *p, int block_m);
+int moe_intermediate_size(const moe_problem_t *p, int block_m, size_t *inter_bytes,
+                          size_t *scales_bytes);
 int moe_grouped_gemm_w13_act(const moe_problem_t *p, const void *a_codes, const void *a_scales,
                              const moe_weight_t *w13, const int32_t *sorted_ids,
                              const int32_t *expert_ids, const int32_t *num_post_pad, int block_m,
@@ -272,8 +297,10 @@ int moe_grouped_gemm_w13_act(const moe_problem_t *p, const void *a_codes, const 
 /* Stage-2 grouped GEMM + top-k weighted reduce (TopKWeightAndReduceNoOP: the
  * reduce happens inside the experts computation).  For every live sorted row:
  *   y = dequant(inter[r]) . dequant(W2[e])^T + b2[e];  acc[t] += topk_weights[s] * y
- * then out_bf16 = bf16_rne(acc).  acc_f32 [M, K] is caller scratch; it is
- * zeroed by this call before the reduce.  Tokens with no live slot give 0. */
+ * then out_bf16 = bf16_rne(acc).  inter / inter_scales as the stage-1 call
+ * with the same block_m wrote them (block_m 64: generic kernels; 128: tcgen05
+ * kernels, same conditions).  acc_f32 [M, K] is caller scratch; it is zeroed
+ * by this call before the reduce.  Tokens with no live slot give 0. */
 int moe_grouped_gemm_w2_reduce(const moe_problem_t *p, const void *inter, const void *inter_scales,
                                const moe_weight_t *w2, const float *topk_weights,
                                const int32_t *sorted_ids, const int32_t *expert_ids,

@@ -32,7 +32,8 @@ EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align
            "moe_get_device_error", "moe_reset_device_error", "moe_selftest_bounded_wait",
            "moe_noalloc_scratch_bytes",
            "moe_fused_experts_noalloc", "moe_packed_weight_bytes", "moe_prepare_weights",
-           "moe_stage_timing", "moe_stage_times", "moe_route_topk", "moe_mma_probe")
+           "moe_stage_timing", "moe_stage_times", "moe_route_topk", "moe_mma_probe",
+           "moe_intermediate_size")
 PATHS = {"auto": 0, "generic": 1, "stream": 2, "tc": 3}
 STAGES = ("align", "quant", "w13", "requant", "w2", "finalize")
 
@@ -83,6 +84,7 @@ def lib() -> ctypes.CDLL:
         "moe_quant_act": (i, [p, i, i, i, p, p, p, p]),
         "moe_route_topk": (i, [p, i, i, i, i, i, i, i, i, p, ctypes.c_float, p, p, p]),
         "moe_w13_workspace_size": (sz, [P, i]),
+        "moe_intermediate_size": (i, [P, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
         "moe_grouped_gemm_w13_act": (i, [P, p, p, W, p, p, p, i, p, p, p, sz, p]),
         "moe_grouped_gemm_w2_reduce": (i, [P, p, p, W, p, p, p, p, i, p, p, p]),
         "moe_fused_experts": (i, [P, p, W, W, p, p, p, p, sz, p, p]),
@@ -166,6 +168,15 @@ def moe_workspace_size(prob: Problem) -> int:
 
 def moe_w13_workspace_size(prob: Problem, block_m=BLOCK_M) -> int:
     return int(lib().moe_w13_workspace_size(ctypes.byref(prob), block_m))
+
+
+def moe_intermediate_size(prob: Problem, block_m=BLOCK_M) -> tuple:
+    """(bytes of the intermediate, bytes of its scales) written by
+    moe_grouped_gemm_w13_act with this block_m."""
+    ib, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("moe_intermediate_size", lib().moe_intermediate_size(
+        ctypes.byref(prob), block_m, ctypes.byref(ib), ctypes.byref(sb)))
+    return int(ib.value), int(sb.value)
 
 
 def moe_align_block_size(topk_ids, expert_map, E, El, block_m, sorted_ids, expert_ids,

@@ -76,7 +76,7 @@ size_t codes_bytes(int afmt, long rows, long cols) {
                                                      : (size_t)rows * cols;
 }
 
-size_t scales_bytes(int afmt, long rows, long cols) {
+size_t scales_bytes_of(int afmt, long rows, long cols) {
   switch (afmt) {
     case A_FP8_TENSOR_STATIC:
     case A_FP8_TENSOR_DYN: return 4;
@@ -133,10 +133,9 @@ bool tc_applies(const moe_problem_t *p) {
 // Workspace layout of the tcgen05 path (sort blocks of 128 rows).
 struct TcLayout {
   long cap, blocks;
-  size_t sorted, expert_ids, ntp, counts, x16, x_inv, a1_codes, a1_scales, a_sorted, a_rowscale,
-      a_groupscale, a_sf, inter, inter_sf, staging, i_scales, acc, total;
+  size_t sorted, expert_ids, ntp, counts, x16, x_inv, a1_codes, a1_scales, scratch, inter,
+      i_scales, acc, total;
   bool f16_x;  // x converted to f16 once per token by the sort (MXFP4 weights)
-  bool bs;     // NVFP4 on the block-scaled kind: codes + scale-factor records
 };
 
 // Workspace layout of moe_fused_experts.
@@ -174,7 +173,7 @@ Layout make_layout(const moe_problem_t *p) {
     L.x16 = L.x_inv = o;
   }
   L.a1_codes = o; o = align_up(o + codes_bytes(p->afmt, p->M, p->K));
-  L.a1_scales = o; o = align_up(o + scales_bytes(p->afmt, p->M, p->K));
+  L.a1_scales = o; o = align_up(o + scales_bytes_of(p->afmt, p->M, p->K));
   if (s2 == A_BF16) {
     L.inter = o; o = align_up(o + (size_t)L.cap * p->N * 2);
     L.inter_scales = o;
@@ -184,7 +183,7 @@ Layout make_layout(const moe_problem_t *p) {
     size_t ib = codes_bytes(s2, L.cap, p->N);
     if (f16_x && ib < (size_t)L.cap * p->N * 2) ib = (size_t)L.cap * p->N * 2;
     L.inter = o; o = align_up(o + ib);
-    L.inter_scales = o; o = align_up(o + scales_bytes(s2, L.cap, p->N));
+    L.inter_scales = o; o = align_up(o + scales_bytes_of(s2, L.cap, p->N));
     L.staging = o; o = align_up(o + (size_t)L.cap * p->N * 4);
   }
   L.acc = o; o = align_up(o + (size_t)p->M * p->K * 4);
@@ -207,12 +206,62 @@ Layout make_layout(const moe_problem_t *p) {
   return L;
 }
 
+// MXFP4 w4a16 with SwiGLU-OAI: |z| <= limit * (limit + |beta|) <= 8192 fits f16
+// as it is (no per-row rescale pass); the router weight could scale it further.
+bool tc_mx_direct(const moe_problem_t *p) {
+  return p->wfmt == W_MXFP4 && stage2_afmt(p) == A_BF16 && p->act == ACT_SWIGLU_OAI &&
+         p->swiglu_limit > 0.f && p->swiglu_limit <= 64.f && fabsf(p->swiglu_beta) <= 64.f &&
+         !p->router_weight_on_input;
+}
+
+// Scratch of the tcgen05 stage 1 (the gathered A rows and their scales, fp32
+// staging of an intermediate that a separate pass requantises / rescales),
+// as offsets from its start; and the intermediate in the form stage 2 reads.
+struct TcScratch {
+  size_t a_sorted, a_rowscale, a_groupscale, a_sf, staging, total;
+};
+TcScratch tc_scratch_layout(const moe_problem_t *p, long cap) {
+  TcScratch L;
+  const int s2 = stage2_afmt(p);
+  const bool mx = p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN;
+  const bool fp8 = p->wfmt == W_FP8_TENSOR || p->wfmt == W_FP8_CHANNEL ||
+                   p->wfmt == W_FP8_BLOCK128;
+  const bool bs = p->wfmt == W_NVFP4;
+  const long blocks = cap / kTcBlockM;
+  size_t o = 0;
+  L.a_sorted = o;
+  o = align_up(o + (bs ? (size_t)cap * p->K / 2 : (size_t)cap * p->K * (fp8 ? 1 : 2)));
+  L.a_rowscale = o; o = align_up(o + (size_t)cap * 4);
+  L.a_groupscale = o; o = align_up(o + (fp8 ? (size_t)cap * ceil_div(p->K, 128) * 4 : 0));
+  L.a_sf = o; o = align_up(o + (bs ? (size_t)blocks * ceil_div(p->K, kTcBsStage) * kBsSfaRecBytes : 0));
+  const bool staged = !bs && !mx && (s2 != A_BF16 || (p->wfmt == W_MXFP4 && !tc_mx_direct(p)));
+  L.staging = o; o = align_up(o + (staged ? (size_t)cap * p->N * 4 : 0));
+  L.total = o;
+  return L;
+}
+void tc_inter_sizes(const moe_problem_t *p, long cap, size_t *inter, size_t *scales) {
+  const int s2 = stage2_afmt(p);
+  const bool mx = p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN;
+  if (p->wfmt == W_NVFP4) {  // e2m1 codes + scale-factor records
+    *inter = (size_t)cap * p->N / 2;
+    *scales = (size_t)(cap / kTcBlockM) * ceil_div(p->N, kTcBsStage) * kBsSfaRecBytes;
+  } else if (p->wfmt == W_MXFP4) {  // f16 values (MX: their QDQ), row scales unless direct
+    *inter = (size_t)cap * p->N * 2;
+    *scales = (mx || tc_mx_direct(p)) ? 0 : (size_t)cap * 4;
+  } else if (s2 == A_BF16) {
+    *inter = (size_t)cap * p->N * 2;
+    *scales = 0;
+  } else {  // e4m3 codes + the stage-2 scales, as the generic path writes them
+    *inter = codes_bytes(s2, cap, p->N);
+    *scales = scales_bytes_of(s2, cap, p->N);
+  }
+}
+
 TcLayout make_tc_layout(const moe_problem_t *p) {
   TcLayout L;
   const int BM = kTcBlockM;
   L.cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, BM);
   L.blocks = L.cap / BM;
-  const int s2 = stage2_afmt(p);
   size_t o = 0;
   L.sorted = o; o = align_up(o + (size_t)L.cap * 4);
   L.expert_ids = o; o = align_up(o + (size_t)L.blocks * 4);
@@ -225,36 +274,12 @@ TcLayout make_tc_layout(const moe_problem_t *p) {
     L.x_inv = o; o = align_up(o + (size_t)p->M * 4);
   }
   L.a1_codes = o; o = align_up(o + codes_bytes(p->afmt, p->M, p->K));
-  L.a1_scales = o; o = align_up(o + scales_bytes(p->afmt, p->M, p->K));
-  L.bs = p->wfmt == W_NVFP4;
-  if (L.bs) {
-    // sorted e2m1 codes + scale-factor records of x; codes + records of the
-    // intermediate; the fp32 accumulator
-    L.a_sorted = o; o = align_up(o + (size_t)L.cap * p->K / 2);
-    L.a_sf = o; o = align_up(o + (size_t)L.blocks * ceil_div(p->K, kTcBsStage) * kBsSfaRecBytes);
-    L.inter = o; o = align_up(o + (size_t)L.cap * p->N / 2);
-    L.inter_sf = o; o = align_up(o + (size_t)L.blocks * ceil_div(p->N, kTcBsStage) * kBsSfaRecBytes);
-    L.a_rowscale = L.a_groupscale = L.staging = L.i_scales = o;
-    L.acc = o; o = align_up(o + (size_t)p->M * p->K * 4);
-    L.total = o;
-    return L;
-  }
-  L.a_sf = L.inter_sf = 0;
-  const bool fp8 = p->wfmt == W_FP8_TENSOR || p->wfmt == W_FP8_CHANNEL ||
-                   p->wfmt == W_FP8_BLOCK128;
-  L.a_sorted = o; o = align_up(o + (size_t)L.cap * p->K * (fp8 ? 1 : 2));
-  L.a_rowscale = o; o = align_up(o + (size_t)L.cap * 4);
-  L.a_groupscale = o; o = align_up(o + (size_t)L.cap * ceil_div(p->K, 128) * 4);
-  L.inter = o; o = align_up(o + (size_t)L.cap * p->N * 2);
-  if (s2 != A_BF16) {
-    L.staging = o; o = align_up(o + (size_t)L.cap * p->N * 4);
-    L.i_scales = o; o = align_up(o + scales_bytes(s2, L.cap, p->N));
-  } else if (p->wfmt == W_MXFP4) {  // fp32 staging -> f16 rows + row scales
-    L.staging = o; o = align_up(o + (size_t)L.cap * p->N * 4);
-    L.i_scales = o; o = align_up(o + (size_t)L.cap * 4);
-  } else {
-    L.staging = L.i_scales = o;
-  }
+  L.a1_scales = o; o = align_up(o + scales_bytes_of(p->afmt, p->M, p->K));
+  L.scratch = o; o = align_up(o + tc_scratch_layout(p, L.cap).total);
+  size_t ib = 0, sb = 0;
+  tc_inter_sizes(p, L.cap, &ib, &sb);
+  L.inter = o; o = align_up(o + ib);
+  L.i_scales = o; o = align_up(o + sb);
   L.acc = o; o = align_up(o + (size_t)p->M * p->K * 4);
   L.total = o;
   return L;
@@ -433,6 +458,25 @@ int run_w2(const moe_problem_t *p, const void *inter, const void *inter_scales,
 int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *w13,
                 const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
                 const int32_t *expert_map, char *ws, void *out, cudaStream_t st);
+int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales, const void *x16,
+              const float *x_inv, const moe_weight_t *w13, const float *topk_weights,
+              const int32_t *sorted, const int32_t *eids, const int32_t *ntp, long cap,
+              char *scratch, void *inter, void *i_scales, const DeviceInfo &dinfo,
+              cudaStream_t st);
+int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
+              const moe_weight_t *w2, const float *topk_weights, const int32_t *sorted,
+              const int32_t *eids, const int32_t *ntp, long cap, float *acc,
+              const DeviceInfo &dinfo, cudaStream_t st);
+
+// The step entry points with block_m = 128 run the tcgen05 kernels: every
+// weight format, with bf16 / fp8 / NVFP4 activations (FP4 weights need their
+// MOE_LAYOUT_TC records).
+int tc_steps_supported(const moe_problem_t *p, const moe_weight_t *w) {
+  if (p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN) return MOE_ERR_UNSUPPORTED;
+  if ((p->wfmt == W_MXFP4 || p->wfmt == W_NVFP4) && (!w->packed_tc || !aligned16(w->packed_tc)))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
 
 }  // namespace
 
@@ -522,10 +566,29 @@ int moe_quant_act(const void *x_bf16, int rows, int cols, int afmt, const float 
   return cuda_status(launch_quant(q, static_cast<cudaStream_t>(stream)));
 }
 
+int moe_intermediate_size(const moe_problem_t *p, int block_m, size_t *inter_bytes,
+                          size_t *scales_bytes) {
+  if (!inter_bytes || !scales_bytes) return MOE_ERR_INVALID_ARG;
+  int rc = validate_problem(p);
+  if (rc != MOE_OK) return rc;
+  if (block_m != kGenericBlockM && block_m != kTcBlockM) return MOE_ERR_UNSUPPORTED;
+  const long cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, block_m);
+  if (block_m == kTcBlockM) {
+    tc_inter_sizes(p, cap, inter_bytes, scales_bytes);
+  } else {
+    const int s2 = stage2_afmt(p);
+    *inter_bytes = s2 == A_BF16 ? (size_t)cap * p->N * 2 : codes_bytes(s2, cap, p->N);
+    *scales_bytes = scales_bytes_of(s2, cap, p->N);
+  }
+  return MOE_OK;
+}
+
 size_t moe_w13_workspace_size(const moe_problem_t *p, int block_m) {
-  if (validate_problem(p) != MOE_OK || block_m != kGenericBlockM) return 0;
-  if (stage2_afmt(p) == A_BF16) return 0;
-  return (size_t)moe_align_capacity(p->M, p->topk, p->num_local_experts, block_m) * p->N * 4;
+  if (validate_problem(p) != MOE_OK) return 0;
+  const long cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, block_m);
+  if (block_m == kTcBlockM) return tc_scratch_layout(p, cap).total;
+  if (block_m != kGenericBlockM || stage2_afmt(p) == A_BF16) return 0;
+  return (size_t)cap * p->N * 4;
 }
 
 int moe_grouped_gemm_w13_act(const moe_problem_t *p, const void *a_codes, const void *a_scales,
@@ -535,22 +598,31 @@ int moe_grouped_gemm_w13_act(const moe_problem_t *p, const void *a_codes, const 
                              void *stream) {
   int rc = validate_problem(p);
   if (rc != MOE_OK) return rc;
-  if (block_m != kGenericBlockM || p->router_weight_on_input) return MOE_ERR_UNSUPPORTED;
+  if ((block_m != kGenericBlockM && block_m != kTcBlockM) || p->router_weight_on_input)
+    return MOE_ERR_UNSUPPORTED;
   if ((rc = validate_weight(p, w13)) != MOE_OK) return rc;
+  if (block_m == kTcBlockM && (rc = tc_steps_supported(p, w13)) != MOE_OK) return rc;
   if (p->M == 0) return MOE_OK;
   if (!a_codes || !aligned16(a_codes) || !sorted_ids || !expert_ids || !num_post_pad || !inter ||
       !aligned16(inter))
     return MOE_ERR_INVALID_ARG;
   if (p->afmt != A_BF16 && !a_scales) return MOE_ERR_INVALID_ARG;
-  const int s2 = stage2_afmt(p);
-  if (s2 != A_BF16) {
-    if (!inter_scales || !aligned16(inter_scales)) return MOE_ERR_INVALID_ARG;
-    if (!workspace || !aligned16(workspace) || ws_bytes < moe_w13_workspace_size(p, block_m))
-      return MOE_ERR_WORKSPACE;
-  }
+  size_t ib = 0, sb = 0;
+  moe_intermediate_size(p, block_m, &ib, &sb);
+  if (sb > 0 && (!inter_scales || !aligned16(inter_scales))) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_w13_workspace_size(p, block_m);
+  if (need > 0 && (!workspace || !aligned16(workspace) || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, block_m);
+  if (block_m == kTcBlockM) {
+    DeviceInfo dinfo;
+    if ((rc = device_info(&dinfo)) != MOE_OK) return rc;
+    return tc_stage1(p, a_codes, a_scales, nullptr, nullptr, w13, nullptr, sorted_ids, expert_ids,
+                     num_post_pad, cap, static_cast<char *>(workspace), inter, inter_scales, dinfo,
+                     st);
+  }
   return run_w13(p, a_codes, a_scales, w13, nullptr, sorted_ids, expert_ids, num_post_pad, inter,
-                 inter_scales, workspace, cap, static_cast<cudaStream_t>(stream));
+                 inter_scales, workspace, cap, st);
 }
 
 int moe_grouped_gemm_w2_reduce(const moe_problem_t *p, const void *inter, const void *inter_scales,
@@ -560,16 +632,28 @@ int moe_grouped_gemm_w2_reduce(const moe_problem_t *p, const void *inter, const 
                                void *out_bf16, void *stream) {
   int rc = validate_problem(p);
   if (rc != MOE_OK) return rc;
-  if (block_m != kGenericBlockM || p->router_weight_on_input) return MOE_ERR_UNSUPPORTED;
+  if ((block_m != kGenericBlockM && block_m != kTcBlockM) || p->router_weight_on_input)
+    return MOE_ERR_UNSUPPORTED;
   if ((rc = validate_weight(p, w2)) != MOE_OK) return rc;
+  if (block_m == kTcBlockM && (rc = tc_steps_supported(p, w2)) != MOE_OK) return rc;
   if (p->M == 0) return MOE_OK;
   if (!inter || !aligned16(inter) || !topk_weights || !sorted_ids || !expert_ids ||
       !num_post_pad || !acc_f32 || !aligned16(acc_f32) || !out_bf16 || !aligned16(out_bf16))
     return MOE_ERR_INVALID_ARG;
-  if (stage2_afmt(p) != A_BF16 && !inter_scales) return MOE_ERR_INVALID_ARG;
+  size_t ib = 0, sb = 0;
+  moe_intermediate_size(p, block_m, &ib, &sb);
+  if (sb > 0 && !inter_scales) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, block_m);
   if ((rc = cuda_status(launch_zero(acc_f32, (long)p->M * p->K, st))) != MOE_OK) return rc;
+  if (block_m == kTcBlockM) {
+    DeviceInfo dinfo;
+    if ((rc = device_info(&dinfo)) != MOE_OK) return rc;
+    if ((rc = tc_stage2(p, inter, inter_scales, w2, topk_weights, sorted_ids, expert_ids,
+                        num_post_pad, cap, acc_f32, dinfo, st)) != MOE_OK)
+      return rc;
+    return cuda_status(launch_finalize(acc_f32, (long)p->M * p->K, out_bf16, st));
+  }
   return run_w2(p, inter, inter_scales, w2, topk_weights, sorted_ids, expert_ids, num_post_pad,
                 acc_f32, out_bf16, cap, st);
 }
@@ -892,6 +976,156 @@ int moe_selftest_bounded_wait(long long limit_cycles, void *stream) {
 
 namespace {
 
+// Stage 1 of the tcgen05 path: the stage-1 rows gathered into sort order
+// (a_codes / a_scales: bf16 x or moe_quant_act's output; x16 / x_inv: the
+// sort's per-token f16 copy of x, when made), the W13 GEMM + activation, and
+// the intermediate in the form stage 2 reads (inter / i_scales, see
+// tc_inter_sizes).  `scratch` holds tc_scratch_layout(p, cap).total bytes.
+int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales, const void *x16,
+              const float *x_inv, const moe_weight_t *w13, const float *topk_weights,
+              const int32_t *sorted, const int32_t *eids, const int32_t *ntp, long cap,
+              char *scratch, void *inter, void *i_scales, const DeviceInfo &dinfo,
+              cudaStream_t st) {
+  const TcScratch L = tc_scratch_layout(p, cap);
+  const int S = p->M * p->topk;
+  const int s2 = stage2_afmt(p);
+  const bool mx = p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN;
+  const bool bs = p->wfmt == W_NVFP4;
+  const bool mx_direct = tc_mx_direct(p);
+  int rc;
+  // gather: sorted rows (codes as they are, or exact f16 / bf16 values) +
+  // per-row / per-group scales, or (NVFP4) codes + scale-factor records
+  {
+    GatherArgs g;
+    g.sorted_ids = sorted; g.num_post_pad = ntp; g.S = S; g.T = p->topk; g.K = p->K;
+    g.afmt = p->afmt; g.codes = a_codes; g.scales = a_scales;
+    g.to_f16 = p->wfmt == W_MXFP4;
+    g.x16 = x16;
+    g.x_inv = x_inv;
+    g.out = scratch + L.a_sorted;
+    g.rowscale = reinterpret_cast<float *>(scratch + L.a_rowscale);
+    g.groupscale = reinterpret_cast<float *>(scratch + L.a_groupscale);
+    if (bs) g.sf_out = scratch + L.a_sf;
+    StageScope sc(MOE_STAGE_QUANT, st);
+    rc = cuda_status(launch_gather_rows(g, cap, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+  }
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.M = p->M; a.K = p->K; a.N = p->N; a.T = p->topk; a.El = p->num_local_experts;
+  a.wfmt = p->wfmt; a.act = p->act; a.gate = p->gate;
+  a.alpha = p->swiglu_alpha; a.beta = p->swiglu_beta; a.limit = p->swiglu_limit;
+  a.sorted_ids = sorted; a.expert_ids = eids; a.num_post_pad = ntp; a.S = S;
+  a.err = dinfo.err;
+  a.w_stage1 = p->router_weight_on_input ? 1 : 0;
+  a.topk_weights = topk_weights;
+  a.R = 2 * p->N; a.C = p->K;
+  switch (p->afmt) {
+    case A_FP8_TENSOR_STATIC:
+    case A_FP8_TENSOR_DYN: a.a_scalar = static_cast<const float *>(a_scales); break;
+    case A_FP8_TOKEN_DYN: a.a_rowscale = reinterpret_cast<const float *>(scratch + L.a_rowscale); break;
+    case A_FP8_GROUP128_DYN:
+      a.a_groupscale = reinterpret_cast<const float *>(scratch + L.a_groupscale);
+      a.a_groups = (int)ceil_div(p->K, 128);
+      break;
+    case A_NVFP4_DYN: a.a_scalar = p->a1_scale; break;
+    default:
+      if (p->wfmt == W_MXFP4) a.a_rowscale = reinterpret_cast<const float *>(scratch + L.a_rowscale);
+      break;
+  }
+  a.w_codes = w13->codes; a.w_scales = w13->scales; a.w_global = w13->global_scale;
+  a.w_bias = w13->bias; a.bias_f32 = w13->bias_is_f32; a.w_packed = w13->packed_tc;
+  a.out = inter;
+  if (bs) {                       // block-scaled: codes + scale-factor records
+    a.a_sf = scratch + L.a_sf;
+    a.out_sf = i_scales;
+    a.out_global = p->a2_scale;
+  } else if (mx) {                // OCP MX quantise-dequantise inside the epilogue
+    a.out_mode = s2 == A_MXFP4_DYN ? TC_OUT_MX4_F16 : TC_OUT_MX8_F16;
+  } else if (mx_direct) {         // bounded SwiGLU-OAI intermediate straight to f16
+    a.out_mode = TC_OUT_F16;
+  } else if (s2 != A_BF16 || p->wfmt == W_MXFP4) {
+    a.out = scratch + L.staging;  // fp32 staging, then a requantiser / row rescale
+    a.out_mode = TC_OUT_F32;
+  } else {
+    a.out_mode = TC_OUT_BF16;
+  }
+  {
+    StageScope sc(MOE_STAGE_W13, st);
+    rc = cuda_status(bs ? launch_bs_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
+                        : launch_tc_gemm(a, scratch + L.a_sorted, cap, 1, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+  }
+  if (s2 == A_BF16 && p->wfmt == W_MXFP4 && !mx_direct) {  // f16 intermediate with row scales
+    StageScope sc(MOE_STAGE_REQUANT, st);
+    rc = cuda_status(launch_rescale_rows(reinterpret_cast<const float *>(scratch + L.staging), cap,
+                                         p->N, sorted, ntp, S, inter,
+                                         static_cast<float *>(i_scales), st));
+    sc.done();
+    return rc;
+  }
+  // stage-2 requantisation of the fp8 formats into e4m3 codes + scales
+  // (NVFP4 and OCP MX were quantised in the W13 epilogue)
+  if (s2 != A_BF16 && !bs && !mx) {
+    QuantArgs q{};  // every field zero / its default
+    q.x = scratch + L.staging; q.x_is_f32 = 1; q.rows = cap; q.cols = p->N; q.afmt = s2;
+    q.param = p->a2_scale; q.sorted_ids = sorted; q.expert_ids = eids; q.num_post_pad = ntp;
+    q.S = S; q.BM = kTcBlockM; q.scales = i_scales; q.codes = inter;
+    StageScope sc(MOE_STAGE_REQUANT, st);
+    rc = cuda_status(launch_quant(q, st));
+    sc.done();
+  }
+  return rc;
+}
+
+// Stage 2 of the tcgen05 path: the W2 GEMM + router weight + fp32 reduce into
+// acc (zeroed by the caller) from the intermediate stage 1 wrote.
+int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
+              const moe_weight_t *w2, const float *topk_weights, const int32_t *sorted,
+              const int32_t *eids, const int32_t *ntp, long cap, float *acc,
+              const DeviceInfo &dinfo, cudaStream_t st) {
+  const int s2 = stage2_afmt(p);
+  const bool mx = p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN;
+  const bool bs = p->wfmt == W_NVFP4;
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.M = p->M; a.K = p->K; a.N = p->N; a.T = p->topk; a.El = p->num_local_experts;
+  a.wfmt = p->wfmt; a.act = p->act; a.gate = p->gate;
+  a.alpha = p->swiglu_alpha; a.beta = p->swiglu_beta; a.limit = p->swiglu_limit;
+  a.sorted_ids = sorted; a.expert_ids = eids; a.num_post_pad = ntp; a.S = p->M * p->topk;
+  a.err = dinfo.err;
+  a.w_stage1 = p->router_weight_on_input ? 1 : 0;
+  a.R = p->K; a.C = p->N;
+  switch (s2) {
+    case A_FP8_TENSOR_STATIC:
+    case A_FP8_TENSOR_DYN: a.a_scalar = static_cast<const float *>(i_scales); break;
+    case A_FP8_TOKEN_DYN: a.a_rowscale = static_cast<const float *>(i_scales); break;
+    case A_FP8_GROUP128_DYN:
+      a.a_groupscale = static_cast<const float *>(i_scales);
+      a.a_groups = (int)ceil_div(p->N, 128);
+      break;
+    case A_NVFP4_DYN: a.a_expertscale = p->a2_scale; break;
+    default:
+      if (p->wfmt == W_MXFP4 && !tc_mx_direct(p) && !mx)
+        a.a_rowscale = static_cast<const float *>(i_scales);
+      break;
+  }
+  a.w_codes = w2->codes; a.w_scales = w2->scales; a.w_global = w2->global_scale;
+  a.w_bias = w2->bias; a.bias_f32 = w2->bias_is_f32; a.w_packed = w2->packed_tc;
+  a.acc = acc; a.topk_weights = topk_weights;
+  if (bs) a.a_sf = i_scales;
+  StageScope sc(MOE_STAGE_W2, st);
+  const int rc = cuda_status(bs ? launch_bs_gemm(a, inter, cap, 0, dinfo.sm_count, st)
+                                : launch_tc_gemm(a, inter, cap, 0, st));
+  sc.done();
+  return rc;
+}
+
+// The tcgen05 prefill path: sort with 128-row blocks (+ zero the accumulator;
+// MXFP4 weights: + the f16 copy of x), stage-1 quantisation, stage 1, stage 2,
+// bf16 output.
 int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *w13,
                 const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
                 const int32_t *expert_map, char *ws, void *out, cudaStream_t st) {
@@ -905,11 +1139,6 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
   int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
   float *acc = reinterpret_cast<float *>(ws + L.acc);
   const long MK = (long)p->M * p->K;
-  const int S = p->M * p->topk;
-  const int s2 = stage2_afmt(p);
-
-  // 1. sort / pad with 128-row blocks (+ zero the accumulator; MXFP4 weights:
-  //    + the f16 copy of x, quantised and dequantised first for MX activations)
   {
     AlignExtras ex;
     ex.zero_buf = acc;
@@ -930,8 +1159,8 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     sc.done();
     if (rc != MOE_OK) return rc;
   }
-  // 2. stage-1 quantisation of x (once per token); OCP MX activations are
-  //    quantised and dequantised by the gather itself
+  // stage-1 quantisation of x (once per token); OCP MX activations are
+  // quantised and dequantised by the sort's conversion CTAs
   const bool mx = p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN;
   const void *codes = hidden;
   const void *scales = nullptr;
@@ -946,142 +1175,14 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     codes = ws + L.a1_codes;
     scales = ws + L.a1_scales;
   }
-  // 3. gather: sorted bf16 rows (exact decode) + per-row / per-group scales
-  {
-    GatherArgs g;
-    g.sorted_ids = sorted; g.num_post_pad = ntp; g.S = S; g.T = p->topk; g.K = p->K;
-    g.afmt = p->afmt; g.codes = codes; g.scales = scales;
-    g.to_f16 = p->wfmt == W_MXFP4 || p->wfmt == W_NVFP4;
-    if (L.f16_x) {
-      g.x16 = ws + L.x16;
-      g.x_inv = reinterpret_cast<const float *>(ws + L.x_inv);
-    }
-    g.out = ws + L.a_sorted;
-    g.rowscale = reinterpret_cast<float *>(ws + L.a_rowscale);
-    g.groupscale = reinterpret_cast<float *>(ws + L.a_groupscale);
-    if (L.bs) g.sf_out = ws + L.a_sf;
-    StageScope sc(MOE_STAGE_QUANT, st);
-    rc = cuda_status(launch_gather_rows(g, L.cap, st));
-    sc.done();
-    if (rc != MOE_OK) return rc;
-  }
-  TcArgs base;
-  memset(&base, 0, sizeof(base));
-  base.M = p->M; base.K = p->K; base.N = p->N; base.T = p->topk; base.El = p->num_local_experts;
-  base.wfmt = p->wfmt; base.act = p->act; base.gate = p->gate;
-  base.alpha = p->swiglu_alpha; base.beta = p->swiglu_beta; base.limit = p->swiglu_limit;
-  base.sorted_ids = sorted; base.expert_ids = eids; base.num_post_pad = ntp; base.S = S;
-  base.err = dinfo.err;
-  base.w_stage1 = p->router_weight_on_input ? 1 : 0;
-  // MXFP4 w4a16 with SwiGLU-OAI: |z| <= limit * (limit + |beta|) <= 8192 fits f16
-  // as it is (no per-row rescale pass); the router weight could scale it further
-  const bool mx_direct = p->wfmt == W_MXFP4 && s2 == A_BF16 && p->act == ACT_SWIGLU_OAI &&
-                         p->swiglu_limit > 0.f && p->swiglu_limit <= 64.f &&
-                         fabsf(p->swiglu_beta) <= 64.f && !p->router_weight_on_input;
-  base.topk_weights = topk_weights;
-  // 4. gate/up GEMM + activation
-  {
-    TcArgs a = base;
-    a.R = 2 * p->N; a.C = p->K;
-    switch (p->afmt) {
-      case A_FP8_TENSOR_STATIC:
-      case A_FP8_TENSOR_DYN: a.a_scalar = static_cast<const float *>(scales); break;
-      case A_FP8_TOKEN_DYN: a.a_rowscale = reinterpret_cast<const float *>(ws + L.a_rowscale); break;
-      case A_FP8_GROUP128_DYN:
-        a.a_groupscale = reinterpret_cast<const float *>(ws + L.a_groupscale);
-        a.a_groups = (int)ceil_div(p->K, 128);
-        break;
-      case A_NVFP4_DYN: a.a_scalar = p->a1_scale; break;
-      default:
-        if (p->wfmt == W_MXFP4) a.a_rowscale = reinterpret_cast<const float *>(ws + L.a_rowscale);
-        break;
-    }
-    a.w_codes = w13->codes; a.w_scales = w13->scales; a.w_global = w13->global_scale;
-    a.w_bias = w13->bias; a.bias_f32 = w13->bias_is_f32; a.w_packed = w13->packed_tc;
-    if (L.bs) {                     // block-scaled: codes + scale-factor records
-      a.a_sf = ws + L.a_sf;
-      a.out = ws + L.inter;
-      a.out_sf = ws + L.inter_sf;
-      a.out_global = p->a2_scale;
-    } else if (s2 == A_NVFP4_DYN) { // stage-2 quantisation inside the epilogue
-      a.out = ws + L.inter;
-      a.out_mode = TC_OUT_NVFP4_F16;
-      a.out_global = p->a2_scale;
-    } else if (mx) {                // OCP MX quantise-dequantise inside the epilogue
-      a.out = ws + L.inter;
-      a.out_mode = s2 == A_MXFP4_DYN ? TC_OUT_MX4_F16 : TC_OUT_MX8_F16;
-    } else if (mx_direct) {         // bounded SwiGLU-OAI intermediate straight to f16
-      a.out = ws + L.inter;
-      a.out_mode = TC_OUT_F16;
-    } else if (s2 != A_BF16 || p->wfmt == W_MXFP4) {
-      a.out = ws + L.staging;       // fp32 staging, then a requantiser / row rescale
-      a.out_mode = TC_OUT_F32;
-    } else {
-      a.out = ws + L.inter;
-      a.out_mode = TC_OUT_BF16;
-    }
-    StageScope sc(MOE_STAGE_W13, st);
-    rc = cuda_status(L.bs ? launch_bs_gemm(a, ws + L.a_sorted, L.cap, 1, dinfo.sm_count, st)
-                          : launch_tc_gemm(a, ws + L.a_sorted, L.cap, 1, st));
-    sc.done();
-    if (rc != MOE_OK) return rc;
-  }
-  if (s2 == A_BF16 && p->wfmt == W_MXFP4 && !mx_direct) {  // f16 intermediate with row scales
-    StageScope sc(MOE_STAGE_REQUANT, st);
-    rc = cuda_status(launch_rescale_rows(reinterpret_cast<const float *>(ws + L.staging), L.cap,
-                                         p->N, sorted, ntp, S, ws + L.inter,
-                                         reinterpret_cast<float *>(ws + L.i_scales), st));
-    sc.done();
-    if (rc != MOE_OK) return rc;
-  }
-  // 5. stage-2 requantisation into exact bf16 values + scales (sorted rows);
-  //    NVFP4 and OCP MX were quantised in the W13 epilogue
-  if (s2 != A_BF16 && s2 != A_NVFP4_DYN && !mx) {
-    QuantArgs q{};  // every field zero / its default
-    q.x = ws + L.staging; q.x_is_f32 = 1; q.rows = L.cap; q.cols = p->N; q.afmt = s2;
-    q.param = p->a2_scale; q.sorted_ids = sorted; q.expert_ids = eids; q.num_post_pad = ntp;
-    q.S = S; q.BM = kTcBlockM; q.scales = ws + L.i_scales;
-    if (s2 == A_NVFP4_DYN) {  // consumed as exact f16 by the kind::f16 GEMM
-      q.codes = nullptr;
-      q.decoded = ws + L.inter;
-      q.decoded_f16 = 1;
-    } else {                  // e4m3 codes consumed by the kind::f8f6f4 GEMM
-      q.codes = ws + L.inter;
-    }
-    StageScope sc(MOE_STAGE_REQUANT, st);
-    rc = cuda_status(launch_quant(q, st));
-    sc.done();
-    if (rc != MOE_OK) return rc;
-  }
-  // 6. down GEMM + router weight + reduce
-  {
-    TcArgs a = base;
-    a.R = p->K; a.C = p->N;
-    switch (s2) {
-      case A_FP8_TENSOR_STATIC:
-      case A_FP8_TENSOR_DYN: a.a_scalar = reinterpret_cast<const float *>(ws + L.i_scales); break;
-      case A_FP8_TOKEN_DYN: a.a_rowscale = reinterpret_cast<const float *>(ws + L.i_scales); break;
-      case A_FP8_GROUP128_DYN:
-        a.a_groupscale = reinterpret_cast<const float *>(ws + L.i_scales);
-        a.a_groups = (int)ceil_div(p->N, 128);
-        break;
-      case A_NVFP4_DYN: a.a_expertscale = p->a2_scale; break;
-      default:
-        if (p->wfmt == W_MXFP4 && !mx_direct && !mx)
-          a.a_rowscale = reinterpret_cast<const float *>(ws + L.i_scales);
-        break;
-    }
-    a.w_codes = w2->codes; a.w_scales = w2->scales; a.w_global = w2->global_scale;
-    a.w_bias = w2->bias; a.bias_f32 = w2->bias_is_f32; a.w_packed = w2->packed_tc;
-    a.acc = acc; a.topk_weights = topk_weights;
-    if (L.bs) a.a_sf = ws + L.inter_sf;
-    StageScope sc(MOE_STAGE_W2, st);
-    rc = cuda_status(L.bs ? launch_bs_gemm(a, ws + L.inter, L.cap, 0, dinfo.sm_count, st)
-                          : launch_tc_gemm(a, ws + L.inter, L.cap, 0, st));
-    sc.done();
-    if (rc != MOE_OK) return rc;
-  }
-  // 7. bf16 output
+  if ((rc = tc_stage1(p, codes, scales, L.f16_x ? ws + L.x16 : nullptr,
+                      L.f16_x ? reinterpret_cast<const float *>(ws + L.x_inv) : nullptr, w13,
+                      topk_weights, sorted, eids, ntp, L.cap, ws + L.scratch, ws + L.inter,
+                      ws + L.i_scales, dinfo, st)) != MOE_OK)
+    return rc;
+  if ((rc = tc_stage2(p, ws + L.inter, ws + L.i_scales, w2, topk_weights, sorted, eids, ntp,
+                      L.cap, acc, dinfo, st)) != MOE_OK)
+    return rc;
   StageScope sc(MOE_STAGE_FINALIZE, st);
   rc = cuda_status(launch_finalize(acc, MK, out, st));
   sc.done();

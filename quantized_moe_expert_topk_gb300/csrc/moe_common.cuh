@@ -113,21 +113,6 @@ __device__ __forceinline__ uint32_t nvfp4_quant16(const float (&v)[16], float gs
   return s;
 }
 
-// Element pair (byte i of the 8 code bytes) of a quantised NVFP4 group as the
-// exact product e2m1(code) * e4m3(s) (f16 when to_f16, else bf16); the global
-// scale stays with the consumer.
-__device__ __forceinline__ uint32_t nvfp4_decode_pair(uint32_t lo, uint32_t hi, int i, float sv,
-                                                      bool to_f16) {
-  const uint32_t byte = i < 4 ? (lo >> (8 * i)) & 0xff : (hi >> (8 * (i - 4))) & 0xff;
-  const float x0 = e2m1_to_f32(byte & 15) * sv, x1 = e2m1_to_f32(byte >> 4) * sv;
-  if (to_f16) {
-    const __half2 h2 = __floats2half2_rn(x0, x1);
-    return *reinterpret_cast<const uint32_t *>(&h2);
-  }
-  const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-  return *reinterpret_cast<const uint32_t *>(&h2);
-}
-
 // 2^e as fp32, exact for e in [-126, 127].
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
 

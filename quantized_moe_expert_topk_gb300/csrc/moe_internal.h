@@ -78,9 +78,6 @@ struct QuantArgs {
   int BM;
   void *codes;
   void *scales;
-  void *decoded = nullptr;   // if set: exact bf16 of the dequantised codes (without
-                             // the scales an epilogue applies) instead of codes
-  int decoded_f16 = 0;       // the decoded values as f16 instead of bf16 (NVFP4)
 };
 cudaError_t launch_quant(const QuantArgs &a, cudaStream_t stream);
 
@@ -182,10 +179,8 @@ cudaError_t launch_stream_fused(const StreamArgs &a13, const StreamArgs &a2, int
 // tcgen05 grouped GEMMs (moe_tc.cu)
 // Output of the tcgen05 W13 epilogue: bf16 rows, fp32 staging rows (a
 // separate requantiser follows), f16 rows (bounded SwiGLU-OAI intermediate),
-// or the stage-2 NVFP4 quantisation done in the epilogue, written as the exact
-// f16 values e2m1(code) * e4m3(scale) the W2 kernel consumes.
-enum { TC_OUT_BF16 = 0, TC_OUT_F32 = 1, TC_OUT_F16 = 2, TC_OUT_NVFP4_F16 = 3, TC_OUT_MX4_F16 = 4,
-       TC_OUT_MX8_F16 = 5 };
+// or the OCP MX quantise-dequantise of the intermediate as exact f16 values.
+enum { TC_OUT_BF16 = 0, TC_OUT_F32 = 1, TC_OUT_F16 = 2, TC_OUT_MX4_F16 = 3, TC_OUT_MX8_F16 = 4 };
 
 // Block-scaled NVFP4 operands (moe_bs.cu).  Every 256-element reduction
 // stage of a 128-row block of the A operand carries an 8 KB scale-factor
@@ -221,9 +216,9 @@ struct TcArgs {
   const int32_t *sorted_ids, *expert_ids, *num_post_pad;
   int S;
   void *out;
-  int out_mode;          // W13 output: TC_OUT_BF16 / _F32 (staging) / _F16 / _NVFP4_F16 /
+  int out_mode;          // W13 output: TC_OUT_BF16 / _F32 (staging) / _F16 /
                          // _MX4_F16 / _MX8_F16 (OCP MX quantise-dequantise into f16)
-  const float *out_global;  // TC_OUT_NVFP4_F16: the stage-2 global per expert [El]
+  const float *out_global;  // block-scaled NVFP4 W13: the stage-2 global per expert [El]
   float *acc;
   const float *topk_weights;
   int *err;

@@ -92,11 +92,7 @@ __global__ void quant_fp8_group128(QuantArgs a) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) packed |= f32_to_e4m3(__fdiv_rn(v[i], scale)) << (8 * i);
   if (st == 0) packed = 0;
-  if (a.decoded) {
-    __nv_bfloat16 *d = static_cast<__nv_bfloat16 *>(a.decoded) + r * a.cols;
-    for (int i = 0; i < 4; ++i)
-      if (c0 + i < a.cols) d[c0 + i] = __float2bfloat16_rn(e4m3_to_f32((packed >> (8 * i)) & 0xff));
-  } else if (c0 + 3 < a.cols && (a.cols & 3) == 0) {
+  if (c0 + 3 < a.cols && (a.cols & 3) == 0) {
     *reinterpret_cast<uint32_t *>(codes + c0) = packed;
   } else {
     for (int i = 0; i < 4; ++i)
@@ -123,9 +119,7 @@ __global__ void quant_fp8_row(QuantArgs a) {
   for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
   const float scale = fp8_group_scale(amax);
   for (int c = threadIdx.x; c < a.cols; c += blockDim.x) {
-    const uint8_t q = st > 0 ? (uint8_t)f32_to_e4m3(__fdiv_rn(load_elem<InT>(x, c), scale)) : 0;
-    if (a.decoded) static_cast<__nv_bfloat16 *>(a.decoded)[r * a.cols + c] = __float2bfloat16_rn(e4m3_to_f32(q));
-    else codes[c] = q;
+    codes[c] = st > 0 ? (uint8_t)f32_to_e4m3(__fdiv_rn(load_elem<InT>(x, c), scale)) : 0;
   }
   if (threadIdx.x == 0) static_cast<float *>(a.scales)[r] = st > 0 ? scale : 0.f;
 }
@@ -158,9 +152,7 @@ __global__ void quant_fp8_tensor(QuantArgs a, int dynamic) {
     const InT *x = static_cast<const InT *>(a.x) + r * a.cols;
     uint8_t *codes = static_cast<uint8_t *>(a.codes) + r * a.cols;
     for (int c = threadIdx.x; c < a.cols; c += blockDim.x) {
-      const uint8_t q = st > 0 ? (uint8_t)f32_to_e4m3(__fdiv_rn(load_elem<InT>(x, c), scale)) : 0;
-      if (a.decoded) static_cast<__nv_bfloat16 *>(a.decoded)[r * a.cols + c] = __float2bfloat16_rn(e4m3_to_f32(q));
-      else codes[c] = q;
+      codes[c] = st > 0 ? (uint8_t)f32_to_e4m3(__fdiv_rn(load_elem<InT>(x, c), scale)) : 0;
     }
   }
   if (threadIdx.x == 0) static_cast<float *>(a.scales)[0] = scale;
@@ -176,13 +168,10 @@ __global__ void quant_nvfp4(QuantArgs a) {
   if (r >= a.rows) return;
   const int st = row_state(a, r);
   if (st < 0) return;
-  uint8_t *codes = a.codes ? static_cast<uint8_t *>(a.codes) + r * (a.cols / 2) + g * 8 : nullptr;
+  uint8_t *codes = static_cast<uint8_t *>(a.codes) + r * (a.cols / 2) + g * 8;
   uint8_t *scales = static_cast<uint8_t *>(a.scales) + r * G + g;
-  uint4 *dec = a.decoded ? reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.decoded) + r * a.cols + g * 16)
-                         : nullptr;
   if (st == 0) {
-    if (dec) dec[0] = dec[1] = make_uint4(0, 0, 0, 0);
-    else *reinterpret_cast<uint2 *>(codes) = make_uint2(0, 0);
+    *reinterpret_cast<uint2 *>(codes) = make_uint2(0, 0);
     *scales = 0;
     return;
   }
@@ -193,17 +182,7 @@ __global__ void quant_nvfp4(QuantArgs a) {
   for (int i = 0; i < 16; ++i) v[i] = load_elem<InT>(x, i);
   uint32_t lo, hi;
   const uint32_t s = nvfp4_quant16(v, gs, lo, hi);
-  if (dec) {
-    // exact bf16 / f16 of e2m1(code) * e4m3(s); the global g is applied by the consumer
-    const float sv = e4m3_to_f32(s);
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = nvfp4_decode_pair(lo, hi, i, sv, a.decoded_f16 != 0);
-    dec[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dec[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  } else {
-    *reinterpret_cast<uint2 *>(codes) = make_uint2(lo, hi);
-  }
+  *reinterpret_cast<uint2 *>(codes) = make_uint2(lo, hi);
   *scales = (uint8_t)s;
 }
 

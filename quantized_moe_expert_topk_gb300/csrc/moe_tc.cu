@@ -251,7 +251,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // thread t decodes row t/2, chunks 4*(t&1) .. 4*(t&1)+3.
       const int t = threadIdx.x - 64;
       const int n = t >> 1, c0 = (t & 1) * 4;
-      const bool mx = a.wfmt == W_MXFP4;
+
       for (int kt = 0; kt < KT; ++kt) {
         const int s = kt % NS;
         const uint32_t par = (kt / NS) & 1;
@@ -259,27 +259,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!wait_or_abort(&sm.empty[s], par ^ 1, a, abort_flag)) break;
         const unsigned char *rec = sm.raw[s];
         const uint4 cw = *reinterpret_cast<const uint4 *>(rec + n * 32 + c0 * 4);
-        uint32_t sc;
-        if (mx) sc = rec[4096 + n * 2 + (c0 >> 2)];
-        else sc = *reinterpret_cast<const uint16_t *>(rec + 4096 + n * 4 + (c0 >> 1));
+        const uint32_t sc = rec[4096 + n * 2 + (c0 >> 2)];  // e8m0 of these 32 elements
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.raw_empty[s]);
         const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-        // group scale as an f16x2 pair (exact: e8m0 codes are range-checked at
-        // load time, e4m3 values are f16 values)
-        uint32_t sf[2];
-        if (mx) {
-          const uint32_t h = sc >= 113 ? (sc - 112) << 10 : 1u << (sc - 103);
-          sf[0] = sf[1] = h | (h << 16);
-        } else {
-          sf[0] = e4m3x2_to_f16x2((sc & 0xff) * 0x0101u);
-          sf[1] = e4m3x2_to_f16x2((sc >> 8) * 0x0101u);
-        }
+        // the group scale 2^(sc - 127) as an f16x2 pair (exact: the e8m0 codes
+        // are range-checked at load time)
+        const uint32_t sh = sc >= 113 ? (sc - 112) << 10 : 1u << (sc - 103);
+        const uint32_t f = sh | (sh << 16);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint32_t hv[4];
           e2m1x8_to_f16x2x4(words[u], hv);
-          const uint32_t f = sf[u >> 1];
           uint4 o;
           o.x = hmul2_u32(hv[0], f);
           o.y = hmul2_u32(hv[1], f);
@@ -413,21 +404,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 dst[i] = make_float4(z[4 * i], z[4 * i + 1], z[4 * i + 2], z[4 * i + 3]);
-            } else if (a.out_mode == TC_OUT_NVFP4_F16 || a.out_mode == TC_OUT_F16) {
-              // the 16 outputs are one NVFP4 group (jbase is a multiple of 16)
+            } else if (a.out_mode == TC_OUT_F16) {
               uint32_t w[8];
-              if (a.out_mode == TC_OUT_NVFP4_F16) {
-                uint32_t lo, hi;
-                const uint32_t sq = nvfp4_quant16(z, a.out_global[e], lo, hi);
-                const float sv = e4m3_to_f32(sq);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = nvfp4_decode_pair(lo, hi, i, sv, true);
-              } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const __half2 h2 = __floats2half2_rn(z[2 * i], z[2 * i + 1]);
-                  w[i] = *reinterpret_cast<const uint32_t *>(&h2);
-                }
+              for (int i = 0; i < 8; ++i) {
+                const __half2 h2 = __floats2half2_rn(z[2 * i], z[2 * i + 1]);
+                w[i] = *reinterpret_cast<const uint32_t *>(&h2);
               }
               uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + r * a.N + jbase + 16 * p);
               dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -483,8 +465,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 // ------------------------------------------------------------------ gather
 // Sorted-order activation rows for the w13 GEMM: e4m3 codes copied as they
-// are (fp8 formats), or exact bf16 (bf16 input; NVFP4 e2m1 * e4m3 scale), plus
-// per-row / per-group scales.  One warp per sorted row.
+// are (fp8 formats), e2m1 codes + scale-factor records (NVFP4, the
+// block-scaled kernels), bf16 rows, or f16 rows scaled per row by a power of
+// two (MXFP4 weights), plus per-row / per-group scales.  One warp per sorted
+// row.
 __global__ void gather_rows_kernel(GatherArgs g) {
   const long r = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -574,34 +558,6 @@ __global__ void gather_rows_kernel(GatherArgs g) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) sf[o + 1024 * q] = v;
     }
-  } else if (g.afmt == A_NVFP4_DYN) {
-    // exact f16 (or bf16) of e2m1 * e4m3 scale; the global is applied later
-    uint16_t *dst = static_cast<uint16_t *>(g.out) + r * g.K;
-    const uint8_t *src = static_cast<const uint8_t *>(g.codes) + t * (g.K / 2);
-    const uint8_t *sc = static_cast<const uint8_t *>(g.scales) + t * (g.K / 16);
-    for (int c = lane; c < g.K / 8; c += 32) {
-      uint4 o = make_uint4(0, 0, 0, 0);
-      if (live) {
-        const uint32_t v = *reinterpret_cast<const uint32_t *>(src + c * 4);
-        const float f = e4m3_to_f32(sc[c / 2]);
-        float x[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = e2m1_to_f32((v >> (4 * i)) & 15) * f;
-        if (g.to_f16) {
-          uint32_t q[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
-            q[i] = *reinterpret_cast<const uint32_t *>(&h);
-          }
-          o = make_uint4(q[0], q[1], q[2], q[3]);
-        } else {
-          o = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                         pack_bf16x2(x[6], x[7]));
-        }
-      }
-      reinterpret_cast<uint4 *>(dst)[c] = o;
-    }
   } else {  // fp8 codes, copied
     uint8_t *dst = static_cast<uint8_t *>(g.out) + r * g.K;
     const uint8_t *src = static_cast<const uint8_t *>(g.codes) + t * g.K;
@@ -683,7 +639,7 @@ __global__ void pack_tc_fp4_kernel(TcPackArgs p) {
   const long ent = rec / p.kstages;
   const int nt = (int)(ent % p.ntiles);
   const long e = ent / p.ntiles;
-  const int sb = p.nvfp4 ? 4 : 2;  // scale bytes per row per stage
+  const int sb = 2;  // e8m0 scale bytes per row per stage
   int n;
   bool code;
   int byte_in_row;
@@ -721,10 +677,8 @@ __global__ void pack_tc_fp4_kernel(TcPackArgs p) {
     const long k2 = (long)kt * 32 + byte_in_row;  // byte index along the row (2 codes per byte)
     v = (valid && k2 < p.C / 2) ? p.codes[((long)e * p.R + row) * (p.C / 2) + k2] : 0;
   } else {
-    const int per = p.nvfp4 ? 16 : 32;
-    const long grp = (long)kt * (64 / per) + byte_in_row;
-    v = (valid && grp < p.C / per) ? p.scales[((long)e * p.R + row) * (p.C / per) + grp]
-                                   : (p.nvfp4 ? 0 : 127);
+    const long grp = (long)kt * 2 + byte_in_row;
+    v = (valid && grp < p.C / 32) ? p.scales[((long)e * p.R + row) * (p.C / 32) + grp] : 127;
   }
   p.out[o] = v;
 }
@@ -835,12 +789,12 @@ cudaError_t launch_tc_gemm(const TcArgs &a_in, const void *a_sorted, long cap_ro
   if (blocks * a.ntiles > 0x7fffffffL) return cudaErrorInvalidConfiguration;
   a.nblocks = blocks;
   a.mgroup = (int)min(blocks, (long)kTcRasterGroup);
-  const int kind = a.wfmt == W_BF16 ? K_BF16 : (a.wfmt == W_MXFP4 || a.wfmt == W_NVFP4) ? K_FP4 : K_FP8;
+  const int kind = a.wfmt == W_BF16 ? K_BF16 : a.wfmt == W_MXFP4 ? K_FP4 : K_FP8;
   CUtensorMap ta, tb;
   if (!make_map(&ta, a_sorted, cap_rows, a.C, kind == K_FP8, BM)) return cudaErrorInvalidValue;
   if (kind == K_FP4) {
     tb = ta;  // unused
-    a.rec_bytes = a.wfmt == W_NVFP4 ? 4096 + 128 * 4 : 4096 + 128 * 2;
+    a.rec_bytes = 4096 + 128 * 2;
   } else if (!make_map(&tb, a.w_codes, (long)a.El * a.R, a.C, kind == K_FP8, 32)) {
     return cudaErrorInvalidValue;
   }

@@ -4,8 +4,10 @@ moe_grouped_gemm_w2_reduce (the two-stage split of rocm_aiter_fused_experts:
 sort, stage-1 quantisation, the stage-1 and stage-2 GEMMs).  The final output
 is checked against the fp64 oracle at the stated tolerance and against
 moe_fused_experts on the same inputs; the intermediate each stage-1 call
-writes (bf16 rows, or codes + scales in the stage-2 format) is decoded here
-and checked row by row against the oracle's stage-1 output of the same slot.
+writes (bf16 / f16 rows, or codes + scales in the stage-2 format) is decoded
+here and checked row by row against the oracle's stage-1 output of the same
+slot.  block_m 64 runs the generic kernels, block_m 128 the tcgen05 ones
+(block-scaled for NVFP4).
 """
 import zlib
 
@@ -53,11 +55,33 @@ def act_buffers(afmt, rows, cols, dev):
     return codes, scales
 
 
-def decode_rows(fmt, codes, scales, expert_of_row, a2_scale):
+def bs_sf_offset(r, j, ks):
+    """Byte of the scale of (row r, column j) in the block-scaled records
+    (replica 0), as include/moe_experts.h states the layout."""
+    jj = j % 256
+    return (((r // 128) * ks + j // 256) * 8192 + (jj // 128) * 4096 + ((r % 32) // 8) * 256
+            + ((jj // 64) % 2) * 128 + (r % 8) * 16 + ((r % 128) // 32) * 4 + (jj % 64) // 16)
+
+
+def decode_rows(fmt, codes, scales, expert_of_row, a2_scale, rows=None, N=None, ks=None):
     """fp64 values of intermediate rows stored in format `fmt` (this test's
-    own decoder of the layouts the header documents)."""
+    own decoder of the layouts the header documents).  fmt "f16" / "f16rs":
+    f16 rows (times the per-row scales); "nvfp4_bs": e2m1 codes with the
+    block-scaled records (rows: their sorted row numbers)."""
     if fmt == "bf16":
         return codes.double()
+    if fmt == "f16":
+        return codes.view(torch.float16).double()
+    if fmt == "f16rs":
+        return codes.view(torch.float16).double() * scales.double()[:, None]
+    if fmt == "nvfp4_bs":
+        c = codes.long()
+        v = torch.stack([E2M1[c & 15], E2M1[c >> 4]], dim=2).reshape(codes.shape[0], N)
+        g = torch.arange(N // 16)
+        off = torch.stack([torch.tensor([bs_sf_offset(int(r), 16 * int(k), ks) for k in g])
+                           for r in rows])
+        sc = scales.view(torch.uint8)[off].view(torch.float8_e4m3fn).double()
+        return v * sc.repeat_interleave(16, dim=1) * a2_scale.double()[expert_of_row][:, None]
     cols = codes.shape[1] * (2 if fmt in ("nvfp4_dyn", "mxfp4_dyn") else 1)
     if fmt in ("nvfp4_dyn", "mxfp4_dyn"):
         c = codes.long()
@@ -77,12 +101,24 @@ def decode_rows(fmt, codes, scales, expert_of_row, a2_scale):
     return v * s
 
 
+def inter_format(m, wl, block_m, scales_bytes):
+    s2 = m.stage2_format(wl.wfmt, wl.afmt)
+    if block_m == 128 and wl.wfmt == "nvfp4":
+        return "nvfp4_bs"
+    if block_m == 128 and wl.wfmt == "mxfp4":
+        return "f16rs" if scales_bytes else "f16"
+    return s2
+
+
 def run_steps(moe, wl, block_m=64):
     import quantized_moe_expert_topk_gb300 as m
     dev = wl.x.device
     prob = m.make_problem(wl.M, wl.K, wl.N, wl.T, wl.E, wl.El, wl.wfmt, wl.afmt, wl.act, wl.gate,
                           wl.swiglu_alpha, wl.swiglu_beta, wl.swiglu_limit, wl.a1_scale,
                           wl.a2_scale)
+    # the load-time packed copies (the tcgen05 kernels of FP4 weights read them)
+    layer = m.FusedExperts.from_workload(wl)
+    w13, w2 = layer.w13, layer.w2
     cap = m.moe_align_capacity(wl.M, wl.T, wl.El, block_m)
     i32 = torch.int32
     sorted_ids = torch.empty(cap, dtype=i32, device=dev)
@@ -97,21 +133,30 @@ def run_steps(moe, wl, block_m=64):
         a_codes, a_scales = act_buffers(wl.afmt, wl.M, wl.K, dev)
         m.moe_quant_act(wl.x, wl.afmt, wl.a1_scale, a_codes, a_scales)
     s2 = m.stage2_format(wl.wfmt, wl.afmt)
-    if s2 == "bf16":
-        inter, inter_scales = torch.empty((cap, wl.N), dtype=torch.bfloat16, device=dev), None
+    ib, sb = m.moe_intermediate_size(prob, block_m)
+    fmt = inter_format(m, wl, block_m, sb)
+    if fmt in ("bf16", "f16", "f16rs"):
+        inter = torch.empty((cap, wl.N), dtype=torch.bfloat16 if fmt == "bf16" else torch.float16,
+                            device=dev)
+        inter_scales = torch.empty(cap, dtype=torch.float32, device=dev) if sb else None
+    elif fmt == "nvfp4_bs":
+        inter = torch.empty((cap, wl.N // 2), dtype=torch.uint8, device=dev)
+        inter_scales = torch.zeros(sb, dtype=torch.uint8, device=dev)
     else:
         inter, inter_scales = act_buffers(s2, cap, wl.N, dev)
+    assert inter.numel() * inter.element_size() == ib
+    assert sb == (0 if inter_scales is None else inter_scales.numel() * inter_scales.element_size())
     nws = m.moe_w13_workspace_size(prob, block_m)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
-    m.moe_grouped_gemm_w13_act(prob, a_codes, a_scales, wl.w13, sorted_ids, expert_ids, ntp,
+    m.moe_grouped_gemm_w13_act(prob, a_codes, a_scales, w13, sorted_ids, expert_ids, ntp,
                                inter, inter_scales, ws, block_m)
     acc = torch.empty((wl.M, wl.K), dtype=torch.float32, device=dev)
     out = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device=dev)
-    m.moe_grouped_gemm_w2_reduce(prob, inter, inter_scales, wl.w2, wl.topk_weights, sorted_ids,
+    m.moe_grouped_gemm_w2_reduce(prob, inter, inter_scales, w2, wl.topk_weights, sorted_ids,
                                  expert_ids, ntp, acc, out, block_m)
     torch.cuda.synchronize()
     return dict(out=out, inter=inter, inter_scales=inter_scales, sorted_ids=sorted_ids,
-                expert_ids=expert_ids, ntp=int(ntp.item()), s2=s2, block_m=block_m)
+                expert_ids=expert_ids, ntp=int(ntp.item()), s2=fmt, block_m=block_m)
 
 
 def check_intermediate(wl, r, z_pre, z_post):
@@ -127,25 +172,27 @@ def check_intermediate(wl, r, z_pre, z_post):
     rows = torch.nonzero(live).flatten()
     eid = r["expert_ids"].cpu().long()[rows // r["block_m"]]
     a2 = wl.a2_scale.cpu() if wl.a2_scale is not None else None
+    whole = r["s2"] in ("fp8_tensor_static", "fp8_tensor_dyn", "nvfp4_bs")
     got = decode_rows(r["s2"], r["inter"].cpu()[rows],
                       None if r["inter_scales"] is None else
-                      (r["inter_scales"].cpu() if r["s2"] in ("fp8_tensor_static", "fp8_tensor_dyn")
-                       else r["inter_scales"].cpu()[rows]), eid, a2).numpy()
+                      (r["inter_scales"].cpu() if whole else r["inter_scales"].cpu()[rows]), eid, a2,
+                      rows=rows.tolist(), N=wl.N, ks=(wl.N + 255) // 256).numpy()
     want = z_post[sid[live].numpy()]
     pre = z_pre[sid[live].numpy()]
     rms = float(np.sqrt((pre ** 2).mean()))
     assert rms > 0
     err = np.abs(got - want)
     rel = float(np.sqrt((err ** 2).mean())) / rms
-    assert rel <= (1e-2 if r["s2"] == "bf16" else 2e-2), rel
+    assert rel <= (1e-2 if r["s2"] in ("bf16", "f16", "f16rs") else 2e-2), rel
     # one code step: a quarter of the row's largest magnitude bounds the gap
     # between neighbouring e2m1 / e4m3 grid points of any group of that row
     bound = 0.25 * np.abs(pre).max(axis=1, keepdims=True) + 1e-3 * rms
     assert (err <= bound).all(), float((err - bound).max())
 
 
+@pytest.mark.parametrize("block_m", [64, 128])
 @pytest.mark.parametrize("wfmt,afmt", FORMATS)
-def test_steps_match_oracle_and_fused(moe, wfmt, afmt):
+def test_steps_match_oracle_and_fused(moe, wfmt, afmt, block_m):
     # several tiles in every dimension plus ragged tails (as test_formats_small)
     act = "swiglu_oai" if wfmt == "mxfp4" else "silu"
     gate = "interleaved" if wfmt == "mxfp4" else "separated"
@@ -155,11 +202,16 @@ def test_steps_match_oracle_and_fused(moe, wfmt, afmt):
     host = to_host(wl)
     ref, z_pre, z_post = run_oracle(wl, None, host, intermediate=True)
     wl = to_device(wl)
-    r = run_steps(moe, wl)
+    if block_m == 128 and afmt in ("mxfp4_dyn", "mxfp8_dyn"):
+        with pytest.raises(moe.MoEError) as e:  # MX activations: block_m 64 only
+            run_steps(moe, wl, block_m)
+        assert e.value.status == 2
+        return
+    r = run_steps(moe, wl, block_m)
     err, tol, rms = compare(wl, r["out"], ref)
     assert rms > 0 and err <= tol, f"{wl.name}: {err:.4e} > {tol:.4e}"
     check_intermediate(wl, r, z_pre, z_post)
-    fused = run_gpu(wl, "generic")
+    fused = run_gpu(wl, "generic" if block_m == 64 else "tc")
     d = (fused.float() - r["out"].float()).abs().max().item()
     assert d <= 2 * tolerance(wl.wfmt, rms), d
     assert moe.moe_get_device_error() == 0
