@@ -317,6 +317,32 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
                       const int32_t *expert_map, void *workspace, size_t ws_bytes, void *out_bf16,
                       void *stream);
 
+/* The batched expert-parallel input format: the experts' rows arrive already
+ * grouped per local expert, each with a device-side count of valid rows, as
+ * AiterExperts.apply hands rocm_aiter_fused_experts the per-expert token
+ * counts of expert_tokens_meta (expert_num_tokens) under num_local_tokens
+ * (page "vllm.model_executor.layers.fused_moe.experts.rocm_aiter_moe").
+ * There is no routing and no sort: the padded blocks follow from a prefix sum
+ * of the counts on the device.
+ *   hidden_bf16        bf16 [E_l, max_tokens, K]; rows [e, 0:count[e]) are
+ *                      expert e's tokens, the rest padding (never read)
+ *   expert_num_tokens  device int32 [E_l]: count[e], clamped to [0, max_tokens]
+ *   out_bf16           bf16 [E_l, max_tokens, K] (overwritten):
+ *                      out[e, i] = W2_e act(W13_e QDQ(x[e, i]) + b13_e) + b2_e
+ *                      for i < count[e], 0 for the padding rows
+ * No top-k weight is applied (the combine that follows the experts weighs and
+ * sums a token's rows).  p gives K, N, num_local_experts, the formats, the
+ * activation and the scales; p->M, topk and num_experts are not read.  Not
+ * supported: router_weight_on_input, num_local_tokens, MOE_A_FP8_TENSOR_DYN.
+ * The tcgen05 kernels run when E_l * max_tokens >= 2048 (p->path as for
+ * moe_fused_experts, FP4 weights with their MOE_LAYOUT_TC records), else the
+ * generic ones.  workspace: moe_batched_workspace_size bytes, 256-B aligned. */
+size_t moe_batched_workspace_size(const moe_problem_t *p, int max_tokens);
+int moe_batched_experts(const moe_problem_t *p, int max_tokens, const void *hidden_bf16,
+                        const int32_t *expert_num_tokens, const moe_weight_t *w13,
+                        const moe_weight_t *w2, void *workspace, size_t ws_bytes, void *out_bf16,
+                        void *stream);
+
 /* No-allocation variant of moe_fused_experts (the pages have no counterpart:
  * it exists for callers that cannot allocate device memory -- hosts that own
  * every allocation and give out no scratch buffer, runtimes that must not call

@@ -306,3 +306,23 @@ def fused_experts(prob: dict, x_bits, w13: dict, w2: dict, topk_ids, topk_weight
     if intermediate:
         return out, z_pre, z_post
     return out
+
+
+def batched_experts(prob: dict, x_bits, counts, w13: dict, w2: dict) -> np.ndarray:
+    """Batched expert-parallel input: x_bits bf16 bits [E_l, max_tokens, K],
+    counts [E_l].  Row i of expert e gives expert e's output for i < counts[e]
+    (no top-k weight), 0 for the padding rows; fp64 [E_l, max_tokens, K].
+
+    Defined as the fused experts of E_l * max_tokens tokens with one slot each:
+    the slot of row (e, i) is local expert e with weight 1, and the padding
+    rows' slots are dropped (id -1)."""
+    x = np.asarray(x_bits)
+    El, T, K = x.shape
+    cnt = np.clip(np.asarray(counts, np.int64), 0, T)
+    ids = np.repeat(np.arange(El, dtype=np.int32), T).reshape(El, T)
+    ids[np.arange(T)[None, :] >= cnt[:, None]] = -1
+    q = dict(prob, M=El * T, T=1, E=El, El=El)
+    q.pop("num_local_tokens", None)
+    out = fused_experts(q, x.reshape(El * T, K), w13, w2, ids.reshape(El * T, 1),
+                        np.ones((El * T, 1), np.float32), None)
+    return out.reshape(El, T, K)

@@ -13,7 +13,7 @@ from ._binding import (ACT, AFMT, BLOCK_M, EXPORTS, GATE, LIB_PATH, WFMT, FusedE
                        moe_packed_weight_bytes, moe_prepare_weights,
                        moe_stage_timing, moe_stage_times, STAGES,
                        PATHS, moe_route_topk, SCORING, moe_mma_probe, MMA_KINDS,
-                       moe_intermediate_size,
+                       moe_intermediate_size, moe_batched_workspace_size, moe_batched_experts,
                        moe_get_device_error, moe_grouped_gemm_w2_reduce,
                        moe_grouped_gemm_w13_act, moe_quant_act, moe_reset_device_error,
                        moe_selftest_bounded_wait, moe_w13_workspace_size, moe_workspace_size, stage2_format, status_str)
@@ -25,7 +25,7 @@ __all__ = [
     "moe_fused_experts_noalloc", "moe_noalloc_scratch_bytes", "moe_packed_weight_bytes",
     "moe_prepare_weights", "moe_stage_timing", "moe_stage_times", "STAGES",
     "PATHS", "moe_route_topk", "SCORING", "moe_mma_probe", "MMA_KINDS",
-    "moe_intermediate_size",
+    "moe_intermediate_size", "moe_batched_workspace_size", "moe_batched_experts",
     "moe_get_device_error",
     "moe_grouped_gemm_w2_reduce", "moe_grouped_gemm_w13_act", "moe_quant_act",
     "moe_reset_device_error", "moe_selftest_bounded_wait", "moe_w13_workspace_size", "moe_workspace_size", "stage2_format",

@@ -33,7 +33,7 @@ EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align
            "moe_noalloc_scratch_bytes",
            "moe_fused_experts_noalloc", "moe_packed_weight_bytes", "moe_prepare_weights",
            "moe_stage_timing", "moe_stage_times", "moe_route_topk", "moe_mma_probe",
-           "moe_intermediate_size")
+           "moe_intermediate_size", "moe_batched_workspace_size", "moe_batched_experts")
 PATHS = {"auto": 0, "generic": 1, "stream": 2, "tc": 3}
 STAGES = ("align", "quant", "w13", "requant", "w2", "finalize")
 
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
         "moe_route_topk": (i, [p, i, i, i, i, i, i, i, i, p, ctypes.c_float, p, p, p]),
         "moe_w13_workspace_size": (sz, [P, i]),
         "moe_intermediate_size": (i, [P, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
+        "moe_batched_workspace_size": (sz, [P, i]),
+        "moe_batched_experts": (i, [P, i, p, p, W, W, p, sz, p, p]),
         "moe_grouped_gemm_w13_act": (i, [P, p, p, W, p, p, p, i, p, p, p, sz, p]),
         "moe_grouped_gemm_w2_reduce": (i, [P, p, p, W, p, p, p, p, i, p, p, p]),
         "moe_fused_experts": (i, [P, p, W, W, p, p, p, p, sz, p, p]),
@@ -239,6 +241,23 @@ def moe_fused_experts(prob: Problem, hidden, w13: dict, w2: dict, topk_ids, topk
         ctypes.byref(prob), _ptr(hidden), ctypes.byref(W13), ctypes.byref(W2), _ptr(topk_ids),
         _ptr(topk_weights), _ptr(expert_map), _ptr(workspace), ws_bytes, _ptr(out),
         _stream(stream)))
+
+
+def moe_batched_workspace_size(prob: Problem, max_tokens: int) -> int:
+    return int(lib().moe_batched_workspace_size(ctypes.byref(prob), max_tokens))
+
+
+def moe_batched_experts(prob: Problem, hidden, expert_num_tokens, w13: dict, w2: dict, workspace,
+                        out, stream=None):
+    """Batched expert-parallel input: hidden bf16 [E_l, max_tokens, K], valid
+    rows per expert in expert_num_tokens (device int32 [E_l]); out bf16
+    [E_l, max_tokens, K] (padding rows zero)."""
+    El, max_tokens, _ = hidden.shape
+    W13, W2 = make_weight(w13), make_weight(w2)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("moe_batched_experts", lib().moe_batched_experts(
+        ctypes.byref(prob), max_tokens, _ptr(hidden), _ptr(expert_num_tokens), ctypes.byref(W13),
+        ctypes.byref(W2), _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
 
 
 def moe_noalloc_scratch_bytes() -> int:

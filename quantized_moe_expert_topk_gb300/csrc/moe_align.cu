@@ -306,3 +306,87 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *e
 }
 
 }  // namespace moe
+
+// ------------------------------------------------------------------ batched
+// Batched expert-parallel input (no routing, no sort): the rows of local
+// expert e are the first count[e] rows of its max_tokens-row slice, so the
+// padded blocks follow from an exclusive scan of ceil(count[e] / BM) * BM.
+// CTA 0 builds sorted_ids (slot e * max_tokens + i, sentinel S past count[e])
+// and expert_ids; the other CTAs zero the fp32 accumulator and fill the
+// per-slot weights with 1.
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(1024)
+batched_align_kernel(const int32_t *__restrict__ counts_in, int El, int max_tokens, int BM,
+                     int32_t *__restrict__ sorted, int32_t *__restrict__ expert_ids,
+                     int32_t *__restrict__ ntp, long cap, float *__restrict__ zero_buf, long zero_n,
+                     float *__restrict__ ones, int zero_ctas) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const long S = (long)El * max_tokens;
+  if (blockIdx.x > 0) {
+    const long stride = (long)zero_ctas * blockDim.x;
+    for (long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < zero_n; i += stride)
+      zero_buf[i] = 0.f;
+    for (long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < S; i += stride) ones[i] = 1.f;
+    return;
+  }
+  __shared__ int off[1025];
+  __shared__ int cnt[1024];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < El; e += blockDim.x) {
+    const int c = counts_in[e];
+    cnt[e] = c < 0 ? 0 : (c > max_tokens ? max_tokens : c);
+  }
+  __syncthreads();
+  // exclusive scan of the padded sizes by warp 0 (El <= 1024)
+  if (warp == 0) {
+    const int chunk = (El + 31) / 32;
+    const int e0 = lane * chunk;
+    int local = 0;
+    for (int e = e0; e < e0 + chunk && e < El; ++e) local += (int)(ceil_div(cnt[e], BM) * BM);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e0 + chunk && e < El; ++e) {
+      off[e] = run;
+      run += (int)(ceil_div(cnt[e], BM) * BM);
+    }
+    if (lane == 31) off[El] = incl;
+  }
+  __syncthreads();
+  const int total = off[El];
+  for (int e = warp; e < El; e += blockDim.x / 32) {
+    const int o = off[e], c = cnt[e];
+    const int padded = (int)(ceil_div(c, BM) * BM);
+    for (int i = lane; i < padded; i += 32)
+      sorted[o + i] = i < c ? (int32_t)((long)e * max_tokens + i) : (int32_t)S;
+    for (int b = lane; b < padded / BM; b += 32) expert_ids[o / BM + b] = e;
+  }
+  for (long i = total + threadIdx.x; i < cap; i += blockDim.x) sorted[i] = (int32_t)S;
+  for (long b = total / BM + threadIdx.x; b < cap / BM; b += blockDim.x) expert_ids[b] = -1;
+  if (threadIdx.x == 0) *ntp = total;
+}
+
+}  // namespace
+
+cudaError_t launch_batched_align(const int32_t *counts, int El, int max_tokens, int BM,
+                                 int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
+                                 long cap, float *zero_buf, long zero_n, float *ones,
+                                 cudaStream_t stream) {
+  const long S = (long)El * max_tokens;
+  long n = zero_n > S ? zero_n : S;
+  int zero_ctas = (int)ceil_div(n, 1024L * 8);
+  if (zero_ctas < 1) zero_ctas = 1;
+  if (zero_ctas > 4 * 152) zero_ctas = 4 * 152;
+  return launch_kernel(batched_align_kernel, dim3(1 + zero_ctas), dim3(1024), 0, stream, true,
+                       counts, El, max_tokens, BM, sorted_ids, expert_ids, num_post_pad, cap,
+                       zero_buf, zero_n, ones, zero_ctas);
+}
+
+}  // namespace moe

@@ -468,6 +468,41 @@ int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
               const int32_t *eids, const int32_t *ntp, long cap, float *acc,
               const DeviceInfo &dinfo, cudaStream_t st);
 
+// The batched expert-parallel input as a problem of E_l * max_tokens tokens
+// with one slot each (the slot of row i of expert e is its local expert e,
+// weight 1).  The router weight on the stage-1 output and a valid-token count
+// do not apply; a per-tensor dynamic fp8 scale would span the padding rows.
+int batched_problem(const moe_problem_t *p, int max_tokens, moe_problem_t *q) {
+  if (!p || max_tokens < 1 || p->num_local_experts < 1) return MOE_ERR_INVALID_ARG;
+  if ((long)p->num_local_experts * max_tokens > (1L << 30)) return MOE_ERR_UNSUPPORTED;
+  if (p->router_weight_on_input || p->num_local_tokens || p->afmt == A_FP8_TENSOR_DYN)
+    return MOE_ERR_UNSUPPORTED;
+  *q = *p;
+  q->M = p->num_local_experts * max_tokens;
+  q->topk = 1;
+  q->num_experts = p->num_local_experts;
+  return validate_problem(q);
+}
+
+// The batched call runs the tcgen05 kernels under the same conditions as
+// moe_fused_experts, else the generic ones.
+bool batched_tc(const moe_problem_t *q, const moe_weight_t *w13, const moe_weight_t *w2) {
+  const bool fp4 = q->wfmt == W_MXFP4 || q->wfmt == W_NVFP4;
+  const bool mx_generic = (q->afmt == A_MXFP4_DYN || q->afmt == A_MXFP8_DYN) && !mx_act_f16(q);
+  return !mx_generic && tc_applies(q) &&
+         (!fp4 || (w13 && w2 && w13->packed_tc && w2->packed_tc && aligned16(w13->packed_tc) &&
+                   aligned16(w2->packed_tc)));
+}
+
+size_t batched_body_bytes(const moe_problem_t *q) {
+  size_t n = make_layout(q).total;
+  if (tc_applies(q)) {
+    const size_t t = make_tc_layout(q).total;
+    if (t > n) n = t;
+  }
+  return align_up(n);
+}
+
 // The step entry points with block_m = 128 run the tcgen05 kernels: every
 // weight format, with bf16 / fp8 / NVFP4 activations (FP4 weights need their
 // MOE_LAYOUT_TC records).
@@ -840,6 +875,106 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
   // 4. down GEMM + weighted reduce + bf16 output
   return run_w2(p, ws + L.inter, ws + L.inter_scales, w2, topk_weights, sorted, eids, ntp, acc,
                 out_bf16, L.cap, st);
+}
+
+size_t moe_batched_workspace_size(const moe_problem_t *p, int max_tokens) {
+  moe_problem_t q;
+  if (batched_problem(p, max_tokens, &q) != MOE_OK) return 0;
+  return batched_body_bytes(&q) + align_up((size_t)q.M * 4);
+}
+
+int moe_batched_experts(const moe_problem_t *p, int max_tokens, const void *hidden_bf16,
+                        const int32_t *expert_num_tokens, const moe_weight_t *w13,
+                        const moe_weight_t *w2, void *workspace, size_t ws_bytes, void *out_bf16,
+                        void *stream) {
+  moe_problem_t q;
+  int rc = batched_problem(p, max_tokens, &q);
+  if (rc != MOE_OK) return rc;
+  if ((rc = validate_weight(&q, w13)) != MOE_OK) return rc;
+  if ((rc = validate_weight(&q, w2)) != MOE_OK) return rc;
+  if (!hidden_bf16 || !aligned16(hidden_bf16) || !expert_num_tokens || !out_bf16 ||
+      !aligned16(out_bf16))
+    return MOE_ERR_INVALID_ARG;
+  const size_t body = batched_body_bytes(&q);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      ws_bytes < body + align_up((size_t)q.M * 4))
+    return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  float *ones = reinterpret_cast<float *>(ws + body);
+  DeviceInfo dinfo;
+  if ((rc = device_info(&dinfo)) != MOE_OK) return rc;
+  const bool mx = q.afmt == A_MXFP4_DYN || q.afmt == A_MXFP8_DYN;
+  const long MK = (long)q.M * q.K;
+  TimedCall timed;
+  if (batched_tc(&q, w13, w2)) {
+    const TcLayout L = make_tc_layout(&q);
+    int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+    int32_t *eids = reinterpret_cast<int32_t *>(ws + L.expert_ids);
+    int32_t *ntp = reinterpret_cast<int32_t *>(ws + L.ntp);
+    float *acc = reinterpret_cast<float *>(ws + L.acc);
+    {
+      StageScope sc(MOE_STAGE_ALIGN, st);
+      rc = cuda_status(launch_batched_align(expert_num_tokens, q.num_local_experts, max_tokens,
+                                            kTcBlockM, sorted, eids, ntp, L.cap, acc, MK, ones, st));
+      sc.done();
+      if (rc != MOE_OK) return rc;
+    }
+    const void *codes = hidden_bf16;
+    const void *scales = nullptr;
+    if (q.afmt != A_BF16 && !mx) {  // MX activations: quantised by the gather
+      QuantArgs qa{};
+      qa.x = hidden_bf16; qa.rows = q.M; qa.cols = q.K; qa.afmt = q.afmt; qa.param = q.a1_scale;
+      qa.codes = ws + L.a1_codes; qa.scales = ws + L.a1_scales; qa.BM = 1;
+      StageScope sc(MOE_STAGE_QUANT, st);
+      rc = cuda_status(launch_quant(qa, st));
+      sc.done();
+      if (rc != MOE_OK) return rc;
+      codes = ws + L.a1_codes;
+      scales = ws + L.a1_scales;
+    }
+    if ((rc = tc_stage1(&q, codes, scales, nullptr, nullptr, w13, ones, sorted, eids, ntp, L.cap,
+                        ws + L.scratch, ws + L.inter, ws + L.i_scales, dinfo, st)) != MOE_OK)
+      return rc;
+    if ((rc = tc_stage2(&q, ws + L.inter, ws + L.i_scales, w2, ones, sorted, eids, ntp, L.cap, acc,
+                        dinfo, st)) != MOE_OK)
+      return rc;
+    StageScope sc(MOE_STAGE_FINALIZE, st);
+    rc = cuda_status(launch_finalize(acc, MK, out_bf16, st));
+    sc.done();
+    return rc;
+  }
+  const Layout L = make_layout(&q);
+  int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+  int32_t *eids = reinterpret_cast<int32_t *>(ws + L.expert_ids);
+  int32_t *ntp = reinterpret_cast<int32_t *>(ws + L.ntp);
+  float *acc = reinterpret_cast<float *>(ws + L.acc);
+  {
+    StageScope sc(MOE_STAGE_ALIGN, st);
+    rc = cuda_status(launch_batched_align(expert_num_tokens, q.num_local_experts, max_tokens,
+                                          kGenericBlockM, sorted, eids, ntp, L.cap, acc, MK, ones,
+                                          st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+  }
+  const void *codes = hidden_bf16;
+  const void *scales = nullptr;
+  if (q.afmt != A_BF16) {
+    QuantArgs qa{};
+    qa.x = hidden_bf16; qa.rows = q.M; qa.cols = q.K; qa.afmt = q.afmt; qa.param = q.a1_scale;
+    qa.codes = ws + L.a1_codes; qa.scales = ws + L.a1_scales; qa.BM = 1;
+    StageScope sc(MOE_STAGE_QUANT, st);
+    rc = cuda_status(launch_quant(qa, st));
+    sc.done();
+    if (rc != MOE_OK) return rc;
+    codes = ws + L.a1_codes;
+    scales = ws + L.a1_scales;
+  }
+  if ((rc = run_w13(&q, codes, scales, w13, ones, sorted, eids, ntp, ws + L.inter,
+                    ws + L.inter_scales, ws + L.staging, L.cap, st)) != MOE_OK)
+    return rc;
+  return run_w2(&q, ws + L.inter, ws + L.inter_scales, w2, ones, sorted, eids, ntp, acc, out_bf16,
+                L.cap, st);
 }
 
 size_t moe_packed_weight_bytes(const moe_problem_t *p, int which, int layout) {

@@ -60,6 +60,16 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *e
                          int32_t *num_post_pad, int32_t *counts, long cap,
                          const AlignExtras &extra, cudaStream_t stream);
 
+// Batched expert-parallel input: sorted_ids / expert_ids / num_post_pad of
+// blocks of BM rows from per-expert counts (rows e * max_tokens + i, i <
+// count[e]), no sort; zero_buf [zero_n] zeroed and ones [El * max_tokens] set
+// to 1 (the per-slot weights) by extra CTAs.  cap = El * max_tokens + El * (BM - 1)
+// rounded up to BM bounds num_post_pad.
+cudaError_t launch_batched_align(const int32_t *counts, int El, int max_tokens, int BM,
+                                 int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
+                                 long cap, float *zero_buf, long zero_n, float *ones,
+                                 cudaStream_t stream);
+
 // Quantise rows of x (bf16, or fp32 when x_is_f32) into the activation format
 // `afmt`.  With `sorted_ids` set, the rows are sorted intermediate rows: rows
 // at or beyond *num_post_pad are skipped, padding rows get zero codes, and the

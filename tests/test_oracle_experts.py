@@ -407,3 +407,42 @@ def test_bf16_rounded_output_matches_torch_cast():
     out_bf16 = oracle.fused_experts(*args, round_to_bf16=True)
     want = torch.from_numpy(out).to(torch.bfloat16).double().numpy()
     np.testing.assert_array_equal(out_bf16, want)
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu"])
+def test_batched_identity_experts_and_padding_rows(act):
+    # identity experts: every valid row gives act(x, x); padding rows give 0
+    El, T, K = 3, 5, 32
+    x = (torch.randn(El, T, K, generator=torch.Generator().manual_seed(4)) * 2).to(torch.bfloat16)
+    w13, w2 = identity_experts(El, K)
+    counts = np.array([5, 0, 2])
+    out = oracle.batched_experts(prob(El * T, K, K, 1, El, act=act), bits_of(x), counts, w13, w2)
+    f = F.silu if act == "silu" else (lambda v: F.gelu(v, approximate="none"))
+    xd = x.double()
+    want = (f(xd) * xd).numpy()
+    for e in range(El):
+        np.testing.assert_allclose(out[e, :counts[e]], want[e, :counts[e]], rtol=1e-12, atol=1e-14)
+        assert not out[e, counts[e]:].any()
+
+
+def test_batched_rows_equal_each_expert_dense_mlp():
+    # each valid row of expert e is expert e's dense gated MLP of that row
+    # (torch matmul on the decoded bf16 weights, biases included)
+    El, T, K, N = 3, 4, 64, 32
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(El, T, K, generator=g).to(torch.bfloat16)
+    W13 = (torch.randn(El, 2 * N, K, generator=g) * 0.1).to(torch.bfloat16)
+    W2 = (torch.randn(El, K, N, generator=g) * 0.1).to(torch.bfloat16)
+    b13 = (torch.randn(El, 2 * N, generator=g) * 0.1).to(torch.bfloat16)
+    b2 = (torch.randn(El, K, generator=g) * 0.1).to(torch.bfloat16)
+    counts = np.array([4, 3, 1])
+    out = oracle.batched_experts(prob(El * T, K, N, 1, El), bits_of(x), counts,
+                                 {"codes": bits_of(W13), "bias": bits_of(b13)},
+                                 {"codes": bits_of(W2), "bias": bits_of(b2)})
+    for e in range(El):
+        h = x[e].double() @ W13[e].double().T + b13[e].double()
+        z = F.silu(h[:, :N]) * h[:, N:]
+        y = z @ W2[e].double().T + b2[e].double()
+        np.testing.assert_allclose(out[e, :counts[e]], y[:counts[e]].numpy(), rtol=1e-10,
+                                   atol=1e-12)
+        assert not out[e, counts[e]:].any()
