@@ -234,7 +234,8 @@ TcScratch tc_scratch_layout(const moe_problem_t *p, long cap) {
   L.a_rowscale = o; o = align_up(o + (size_t)cap * 4);
   L.a_groupscale = o; o = align_up(o + (fp8 ? (size_t)cap * ceil_div(p->K, 128) * 4 : 0));
   L.a_sf = o; o = align_up(o + (bs ? (size_t)blocks * ceil_div(p->K, kTcBsStage) * kBsSfaRecBytes : 0));
-  const bool staged = !bs && !mx && (s2 != A_BF16 || (p->wfmt == W_MXFP4 && !tc_mx_direct(p)));
+  const bool staged = !bs && !mx && p->wfmt != W_FP8_BLOCK128 &&
+                      (s2 != A_BF16 || (p->wfmt == W_MXFP4 && !tc_mx_direct(p)));
   L.staging = o; o = align_up(o + (staged ? (size_t)cap * p->N * 4 : 0));
   L.total = o;
   return L;
@@ -1172,10 +1173,13 @@ int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales,
   a.w_codes = w13->codes; a.w_scales = w13->scales; a.w_global = w13->global_scale;
   a.w_bias = w13->bias; a.bias_f32 = w13->bias_is_f32; a.w_packed = w13->packed_tc;
   a.out = inter;
+  const bool fp8b = p->wfmt == W_FP8_BLOCK128;
   if (bs) {                       // block-scaled: codes + scale-factor records
     a.a_sf = scratch + L.a_sf;
     a.out_sf = i_scales;
     a.out_global = p->a2_scale;
+  } else if (fp8b) {              // e4m3 codes + 1 x 128 scales from the epilogue
+    a.out_scales = static_cast<float *>(i_scales);
   } else if (mx) {                // OCP MX quantise-dequantise inside the epilogue
     a.out_mode = s2 == A_MXFP4_DYN ? TC_OUT_MX4_F16 : TC_OUT_MX8_F16;
   } else if (mx_direct) {         // bounded SwiGLU-OAI intermediate straight to f16
@@ -1188,8 +1192,9 @@ int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales,
   }
   {
     StageScope sc(MOE_STAGE_W13, st);
-    rc = cuda_status(bs ? launch_bs_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
-                        : launch_tc_gemm(a, scratch + L.a_sorted, cap, 1, st));
+    rc = cuda_status(bs     ? launch_bs_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
+                     : fp8b ? launch_fp8b_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
+                            : launch_tc_gemm(a, scratch + L.a_sorted, cap, 1, st));
     sc.done();
     if (rc != MOE_OK) return rc;
   }
@@ -1201,9 +1206,10 @@ int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales,
     sc.done();
     return rc;
   }
-  // stage-2 requantisation of the fp8 formats into e4m3 codes + scales
-  // (NVFP4 and OCP MX were quantised in the W13 epilogue)
-  if (s2 != A_BF16 && !bs && !mx) {
+  // stage-2 requantisation of the per-tensor / per-token fp8 formats into
+  // e4m3 codes + scales (NVFP4, FP8 block and OCP MX were quantised in the W13
+  // epilogue)
+  if (s2 != A_BF16 && !bs && !mx && !fp8b) {
     QuantArgs q{};  // every field zero / its default
     q.x = scratch + L.staging; q.x_is_f32 = 1; q.rows = cap; q.cols = p->N; q.afmt = s2;
     q.param = p->a2_scale; q.sorted_ids = sorted; q.expert_ids = eids; q.num_post_pad = ntp;
@@ -1253,7 +1259,9 @@ int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
   if (bs) a.a_sf = i_scales;
   StageScope sc(MOE_STAGE_W2, st);
   const int rc = cuda_status(bs ? launch_bs_gemm(a, inter, cap, 0, dinfo.sm_count, st)
-                                : launch_tc_gemm(a, inter, cap, 0, st));
+                             : p->wfmt == W_FP8_BLOCK128
+                                 ? launch_fp8b_gemm(a, inter, cap, 0, dinfo.sm_count, st)
+                                 : launch_tc_gemm(a, inter, cap, 0, st));
   sc.done();
   return rc;
 }

@@ -229,6 +229,7 @@ struct TcArgs {
   int out_mode;          // W13 output: TC_OUT_BF16 / _F32 (staging) / _F16 /
                          // _MX4_F16 / _MX8_F16 (OCP MX quantise-dequantise into f16)
   const float *out_global;  // block-scaled NVFP4 W13: the stage-2 global per expert [El]
+  float *out_scales;        // FP8-block W13: the intermediate's 1 x 128 scales [cap, ceil(N/128)]
   float *acc;
   const float *topk_weights;
   int *err;
@@ -282,6 +283,13 @@ size_t bs_packed_bytes(int w13, int N, int K, int El);
 cudaError_t launch_pack_bs(const TcPackArgs &p, cudaStream_t st);
 cudaError_t launch_bs_gemm(const TcArgs &a, const void *a_codes, long cap_rows, int w13,
                            int sm_count, cudaStream_t st);
+// Persistent FP8-block grouped GEMMs (moe_fp8.cu): A = e4m3 codes [cap, C]
+// with 1 x 128 scales (a.a_groupscale, a.a_groups per row), B = the canonical
+// e4m3 weights with 128 x 128 block scales.  W13 writes the intermediate as
+// e4m3 codes (a.out [cap, N]) + 1 x 128 scales (a.out_scales); W2 adds the
+// weighted outputs into a.acc.  grid = min(tiles, sm_count).
+cudaError_t launch_fp8b_gemm(const TcArgs &a, const void *a_codes, long cap_rows, int w13,
+                             int sm_count, cudaStream_t st);
 
 // Tensor-core rate probe (moe_probe.cu): sm_count CTAs, each issuing `iters`
 // MMAs of 128 x n (kind 0: f16, 1: e4m3, 2: e2m1 + ue4m3 block scales).
