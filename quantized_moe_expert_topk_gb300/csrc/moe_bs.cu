@@ -70,7 +70,11 @@ constexpr int TMEM_COLS = 512;
 constexpr uint32_t kAccCol = 0, kSfCol = 256, kSfBufCols = 48, kSfbOff = 16;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int kErrTimeout = 5;
-constexpr int kRasterGroup = 8;  // m-blocks that walk the n-tiles together
+// m-blocks that walk the n-tiles together: W13 (16 reduction stages per tile)
+// 32, W2 (long tiles) 16 -- measured on the Mixtral NVFP4 prefill: DRAM reads
+// of W13 2.09 / 1.46 / 1.11 GB for groups of 8 / 16 / 32, of W2 1.34 / 1.30 /
+// 1.44 GB
+template <int MODE> constexpr int kRasterGroup = MODE == 0 ? 32 : 16;
 // Weight records are prefetched into L2 this many stages ahead of the ring
 // (by the CTA of the first m-block of each raster group only: the others of
 // the group read the same records), so the ring's copies hit L2.
@@ -139,10 +143,12 @@ __device__ __forceinline__ void tmem_wait_ld() {
 // Tile t of the grid's list -> (m-block, n-tile): groups of kRasterGroup
 // m-blocks walk the n-tiles together, m fastest, so the CTAs working at one
 // time share each weight tile and each A block through L2.
+template <int MODE>
 __device__ __forceinline__ void tile_coords(long t, long nblocks, int ntiles, int &blk, int &nt) {
-  const long span = (long)kRasterGroup * ntiles;
-  const long g0 = t / span * kRasterGroup;
-  const long gs = min((long)kRasterGroup, nblocks - g0);
+  constexpr int G = kRasterGroup<MODE>;
+  const long span = (long)G * ntiles;
+  const long g0 = t / span * G;
+  const long gs = min((long)G, nblocks - g0);
   const long local = t - g0 * ntiles;
   blk = (int)(g0 + local % gs);
   nt = (int)(local / gs);
@@ -231,7 +237,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
       long g = 0;  // stages issued
       for (long t = blockIdx.x; t < ntiles_total && !*abort_flag; t += gridDim.x) {
         int blk, nt;
-        tile_coords(t, a.nblocks, a.ntiles, blk, nt);
+        tile_coords<MODE>(t, a.nblocks, a.ntiles, blk, nt);
         if ((long)blk * BM >= ntp) continue;
         const int e = a.expert_ids[blk];
         if (e < 0 || e >= a.El) continue;
@@ -239,7 +245,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
                                     ((long)e * a.ntiles + nt) * KT * (long)(STAGE_B + SFB_BYTES);
         const unsigned char *asf = static_cast<const unsigned char *>(a.a_sf) +
                                    (long)blk * KT * kBsSfaRecBytes;
-        const bool leader = (blk % kRasterGroup) == 0;
+        const bool leader = (blk % kRasterGroup<MODE>) == 0;
         if (leader && kPrefetchAhead > 0)
           prefetch_l2_bulk(brec, (uint32_t)(min(KT, kPrefetchAhead) * (STAGE_B + SFB_BYTES)));
         for (int kt = 0; kt < KT; ++kt, ++g) {
@@ -271,7 +277,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
       long g = 0, tc = 0;
       for (long t = blockIdx.x; t < ntiles_total && !*abort_flag; t += gridDim.x) {
         int blk, nt;
-        tile_coords(t, a.nblocks, a.ntiles, blk, nt);
+        tile_coords<MODE>(t, a.nblocks, a.ntiles, blk, nt);
         if ((long)blk * BM >= ntp) continue;
         const int e = a.expert_ids[blk];
         if (e < 0 || e >= a.El) continue;
@@ -308,7 +314,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
       long g = 0;
       for (long t = blockIdx.x; t < ntiles_total && !*abort_flag; t += gridDim.x) {
         int blk, nt;
-        tile_coords(t, a.nblocks, a.ntiles, blk, nt);
+        tile_coords<MODE>(t, a.nblocks, a.ntiles, blk, nt);
         if ((long)blk * BM >= ntp) continue;
         const int e = a.expert_ids[blk];
         if (e < 0 || e >= a.El) continue;
@@ -345,7 +351,7 @@ bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
     const long ks_out = ceil_div(a.N, kTcBsStage);
     for (long t = blockIdx.x; t < ntiles_total; t += gridDim.x) {
       int blk, nt;
-      tile_coords(t, a.nblocks, a.ntiles, blk, nt);
+      tile_coords<MODE>(t, a.nblocks, a.ntiles, blk, nt);
       if ((long)blk * BM >= ntp) continue;
       const int e = a.expert_ids[blk];
       if (e < 0 || e >= a.El) continue;
