@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--E", type=int, default=None, help="routed experts (smaller profiling cases)")
     ap.add_argument("--routing", action="store_true",
                     help="include the fused router (logits -> top-k) in the timed step")
+    ap.add_argument("--path", default="auto",
+                    choices=["auto", "generic", "stream", "tc", "tc_stream"],
+                    help="kernel family (moe_problem_t.path); auto: the library's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -147,16 +150,16 @@ def algorithmic(wl, counts):
                 w13_flops=4.0 * wl.N * wl.K * live, live_slots=live, active_experts=len(active))
 
 
-def mma_dtype(wl):
+def mma_dtype(wl, path="auto"):
     """Operand type of the tensor-core contraction the CUDA path runs for this
     workload: NVFP4 on the tcgen05 path multiplies e2m1 codes with ue4m3 block
     scales (kind::mxf4nvf4); the streaming kernels and the tcgen05 MXFP4
     kinds use exact f16 decodes, the tcgen05 FP8 kinds e4m3, everything else
     (and the generic kernels) exact bf16 decodes."""
-    path = kernel_path(wl)
+    path = kernel_path(wl, path)
     if wl.wfmt == "nvfp4" and path == "tc":
         return "nvfp4"
-    if wl.wfmt in ("mxfp4", "nvfp4") and path in ("stream", "tc"):
+    if wl.wfmt in ("mxfp4", "nvfp4") and path in ("stream", "tc", "tc_stream"):
         return "f16"
     if path == "tc" and wl.wfmt.startswith("fp8"):
         return "e4m3"
@@ -274,34 +277,49 @@ def workload_config(wl):
             "gate": wl.gate, "recipe": wl.recipe}
 
 
-def kernel_path(wl):
-    """The kernel family moe_fused_experts picks for this workload (its
-    default, automatic selection)."""
+def kernel_path(wl, path="auto"):
+    """The kernel family moe_fused_experts runs for this workload with the
+    problem's path field set to `path` (a forced family that does not apply
+    falls back to the automatic choice)."""
     slots = wl.M * wl.T
     bounded = (wl.act == "swiglu_oai" and 0 < wl.swiglu_limit <= 64
                and abs(wl.swiglu_beta) <= 64)
     mx_act = wl.afmt in ("mxfp4_dyn", "mxfp8_dyn")
     # OCP MX activations run on the f16 kernels when the intermediate is bounded
     mx_f16 = mx_act and wl.wfmt == "mxfp4" and bounded and not wl.router_weight_on_input
-    if (wl.wfmt == "mxfp4" and (wl.afmt == "bf16" or mx_f16) and wl.act == "swiglu_oai"
-            and wl.K % 64 == 0 and wl.N % 64 == 0 and slots <= 64 * wl.El):
+    aligned = wl.K % 64 == 0 and wl.N % 64 == 0
+    # MXFP4 w4a16 with a bounded SwiGLU-OAI: the tcgen05 weight-streaming
+    # kernels from 64 (exclusive) to 128 slots per local expert
+    tcs = (wl.wfmt == "mxfp4" and wl.afmt == "bf16" and bounded and aligned
+           and not wl.router_weight_on_input)
+    if tcs and (path == "tc_stream" or (path == "auto" and 64 * wl.El < slots <= 128 * wl.El)):
+        return "tc_stream"
+    stream_ok = (wl.wfmt == "mxfp4" and (wl.afmt == "bf16" or mx_f16) and wl.act == "swiglu_oai"
+                 and aligned and slots <= 64 * wl.El)
+    if stream_ok and path in ("auto", "stream"):
         return "stream"
     if mx_act and not mx_f16:
+        return "generic"
+    if path == "tc":
+        return "tc"
+    if path == "generic":
         return "generic"
     return "tc" if slots >= 2048 else "generic"
 
 
-def launches_per_step(wl, routing=False, fused=False):
+def launches_per_step(wl, routing=False, fused=False, path="auto"):
     """Kernels of this library launched by one step (`fused`: the streaming
     W13 and W2 ran as one grid)."""
     import quantized_moe_expert_topk_gb300 as moe
-    path = kernel_path(wl)
+    path = kernel_path(wl, path)
     s2 = moe.stage2_format(wl.wfmt, wl.afmt)
     n = int(routing)                       # fused router
     n += 1                                 # sort / pad (+ zero, + f16 copy of x when streaming)
     mx_act = wl.afmt in ("mxfp4_dyn", "mxfp8_dyn")
     if path == "stream":                   # w13, (MX: intermediate QDQ), w2, finalize
         return n + (2 if fused else 3 + mx_act)
+    if path == "tc_stream":                # gather, w13 (f16 intermediate), w2, finalize
+        return n + 4
     n += wl.afmt != "bf16" and not (path == "tc" and mx_act)  # stage-1 quantiser (MX on tc: in the gather)
     n += path == "tc"                      # gather of the sorted activation rows
     n += 1                                 # w13 GEMM + activation
@@ -312,7 +330,10 @@ def launches_per_step(wl, routing=False, fused=False):
         mx_direct = (wl.wfmt == "mxfp4" and s2 == "bf16" and wl.act == "swiglu_oai"
                      and 0 < wl.swiglu_limit <= 64 and abs(wl.swiglu_beta) <= 64
                      and not wl.router_weight_on_input)
-        n += (s2 not in ("bf16", "nvfp4_dyn", "mxfp4_dyn", "mxfp8_dyn")
+        # (the FP8-block kernel quantises its 1 x 128 groups in the epilogue)
+        fused_q = ("nvfp4_dyn", "mxfp4_dyn", "mxfp8_dyn") + (
+            ("fp8_group128_dyn",) if wl.wfmt == "fp8_block128" else ())
+        n += ((s2 != "bf16" and s2 not in fused_q)
               or (wl.wfmt == "mxfp4" and s2 == "bf16" and not mx_direct))
     else:
         n += s2 != "bf16"                  # stage-2 requantiser
@@ -339,7 +360,7 @@ def run_ours(args):
     if args.E:
         over["E"] = args.E
     wl = make_workload(args.workload, device=dev, **over)
-    layer = moe.FusedExperts.from_workload(wl)
+    layer = moe.FusedExperts.from_workload(wl, path=args.path)
     out = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -405,24 +426,24 @@ def run_ours(args):
     # dominant kernel (w13 GEMM + activation; on decode batches the one
     # streaming grid that runs both GEMMs), timed alone on its own stream
     k_ms, stage_ms = time_w13_kernel(moe, wl, layer, dev, stream, max(args.steps, 50))
-    fused = kernel_path(wl) == "stream" and stage_ms.get("w2", 0.0) == 0.0
+    fused = kernel_path(wl, args.path) == "stream" and stage_ms.get("w2", 0.0) == 0.0
     k_bytes = alg["fused_kernel_bytes"] if fused else alg["w13_kernel_bytes"]
     k_flops = alg["flops"] if fused else alg["w13_flops"]
     hbm, bf16_tf, peak_src = measured_peaks()
     # the contraction's own dtype: f16 and bf16 share the dense rate; e4m3 and
     # NVFP4 take the measured bf16 rate times the nominal ratios of the dense
     # peaks (4.5 / 2.25 and 13.5 / 2.25 PFLOP/s)
-    ratio = NOMINAL_RATIO[mma_dtype(wl)]
+    ratio = NOMINAL_RATIO[mma_dtype(wl, args.path)]
     tens_tf = bf16_tf * ratio
     if ratio != 1.0:
-        peak_src += f" (bf16 x {ratio:g}, nominal {mma_dtype(wl)} ratio)"
+        peak_src += f" (bf16 x {ratio:g}, nominal {mma_dtype(wl, args.path)} ratio)"
     t_hbm = k_bytes / (hbm * 1e9)
     t_tensor = k_flops / (tens_tf * 1e12)
     if t_hbm >= t_tensor:
         bound, achieved, peak, punit = "hbm", k_bytes / (k_ms / 1e3) / 1e9, hbm, "GB/s"
     else:
         bound, achieved, peak, punit = "tensor", k_flops / (k_ms / 1e3) / 1e12, tens_tf, "TFLOP/s"
-    probe = probe_tflops(moe, mma_dtype(wl), stream)
+    probe = probe_tflops(moe, mma_dtype(wl, args.path), stream)
     traffic = profile_traffic("moe_stream_fused" if fused else "moe_w13", wl.name)
     layer_roof_ms = max(alg["layer_bytes"] / (hbm * 1e9), alg["flops"] / (tens_tf * 1e12)) * 1e3
 
@@ -432,13 +453,13 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": mma_dtype(wl), "data": "synthetic",
+        "vs_baseline": None, "dtype": mma_dtype(wl, args.path), "data": "synthetic",
         "config": dict(workload_config(wl), parallelism=f"replicas{world}",
                        l2="no flush: each step streams all active experts' weights "
                           f"({alg['w13_bytes'] + alg['w2_bytes']} B > 129 MB L2)",
                        launch="CUDA graph of one step"),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": punit,
-                     "frac": achieved / peak, "traffic": traffic, "mma_dtype": mma_dtype(wl),
+                     "frac": achieved / peak, "traffic": traffic, "mma_dtype": mma_dtype(wl, args.path),
                      "kernel": ("w13 + w2 grouped GEMMs (one streaming grid)" if fused
                                 else "w13 grouped GEMM + activation"),
                      "alg_bytes_per_launch": k_bytes,
@@ -453,15 +474,15 @@ def run_ours(args):
                            "alg_bytes": alg["layer_bytes"], "alg_flops": alg["flops"],
                            "active_experts": alg["active_experts"], "live_slots": alg["live_slots"]},
         "e2e": e2e,
-        "gpu_launches": launches_per_step(wl, args.routing, fused) * args.steps,
+        "gpu_launches": launches_per_step(wl, args.routing, fused, args.path) * args.steps,
         "clocks": summarize_clocks(rows, "warmup soak + timed region"),
     }
     if args.routing:
         line["config"]["routing"] = "fused router in the step: softmax, top-k, renormalised"
         line["routing"] = {"kernel_ms": time_router(moe, logits, routed_k, r_ids, r_w, stream),
-                           "path": kernel_path(wl)}
+                           "path": kernel_path(wl, args.path)}
     else:
-        line["config"]["path"] = kernel_path(wl)
+        line["config"]["path"] = kernel_path(wl, args.path)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds,
                                             max_tokens=None if wl.M <= 128 else 32)

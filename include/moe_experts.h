@@ -145,16 +145,21 @@ typedef struct {
   const int32_t *num_local_tokens;
   /* Kernel family of this problem (moe_path; a tuning and testing aid, read
    * per call, no process-wide state).  MOE_PATH_AUTO (0, the value of a
-   * zero-initialised struct): the weight-streaming decode kernels when their
-   * conditions hold (see moe_prepare_weights), else the tcgen05 kernels when
-   * M*topk >= 2048 (FP4 formats need MOE_LAYOUT_TC packed weights), else the
-   * generic mma.sync kernels.  GENERIC, STREAM (falls back to GENERIC where
-   * it does not apply) and TC force a family.  moe_workspace_size depends on
-   * it. */
+   * zero-initialised struct): for MXFP4 w4a16 with the bounded SwiGLU-OAI
+   * (K, N multiples of 64, MOE_LAYOUT_STREAM and MOE_LAYOUT_TC weights) the
+   * tcgen05 weight-streaming kernels from 64 (exclusive) to 128 slots per
+   * local expert on average; otherwise the
+   * mma.sync weight-streaming kernels when their conditions hold (see
+   * moe_prepare_weights), else the tcgen05 kernels when M*topk >= 2048 (FP4
+   * formats need MOE_LAYOUT_TC packed weights), else the generic mma.sync
+   * kernels.  GENERIC, STREAM, TC and TC_STREAM force a family where it
+   * applies (else the automatic choice runs).  moe_workspace_size depends
+   * on it. */
   int path;
 } moe_problem_t;
 
-enum { MOE_PATH_AUTO = 0, MOE_PATH_GENERIC = 1, MOE_PATH_STREAM = 2, MOE_PATH_TC = 3 };
+enum { MOE_PATH_AUTO = 0, MOE_PATH_GENERIC = 1, MOE_PATH_STREAM = 2, MOE_PATH_TC = 3,
+       MOE_PATH_TC_STREAM = 4 };
 
 /* Library / ABI identification. */
 int moe_abi_version(void);

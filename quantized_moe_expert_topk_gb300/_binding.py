@@ -34,7 +34,7 @@ EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align
            "moe_fused_experts_noalloc", "moe_packed_weight_bytes", "moe_prepare_weights",
            "moe_stage_timing", "moe_stage_times", "moe_route_topk", "moe_mma_probe",
            "moe_intermediate_size", "moe_batched_workspace_size", "moe_batched_experts")
-PATHS = {"auto": 0, "generic": 1, "stream": 2, "tc": 3}
+PATHS = {"auto": 0, "generic": 1, "stream": 2, "tc": 3, "tc_stream": 4}
 STAGES = ("align", "quant", "w13", "requant", "w2", "finalize")
 
 
@@ -134,7 +134,7 @@ def make_problem(M, K, N, topk, E, El, wfmt, afmt, act, gate, swiglu_alpha=1.702
                  router_weight_on_input=False, num_local_tokens=None, path="auto") -> Problem:
     """num_local_tokens: optional device int32 [1] tensor, the number of valid
     tokens (read on the device at every call).  path: kernel family of this
-    problem ("auto", "generic", "stream", "tc")."""
+    problem ("auto", "generic", "stream", "tc", "tc_stream")."""
     return Problem(M, K, N, topk, E, El, WFMT[wfmt], AFMT[afmt], ACT[act], GATE[gate],
                    swiglu_alpha, swiglu_beta, swiglu_limit, _ptr(a1_scale), _ptr(a2_scale),
                    int(bool(router_weight_on_input)), _ptr(num_local_tokens), PATHS[path])

@@ -96,7 +96,7 @@ int validate_problem(const moe_problem_t *p) {
     return MOE_ERR_INVALID_ARG;
   if (p->wfmt < W_BF16 || p->wfmt > W_NVFP4 || p->afmt < A_BF16 || p->afmt > A_MXFP8_DYN ||
       p->act < ACT_SILU || p->act > ACT_SWIGLU_OAI || p->gate < GATE_SEPARATED ||
-      p->gate > GATE_INTERLEAVED || p->path < MOE_PATH_AUTO || p->path > MOE_PATH_TC)
+      p->gate > GATE_INTERLEAVED || p->path < MOE_PATH_AUTO || p->path > MOE_PATH_TC_STREAM)
     return MOE_ERR_INVALID_ARG;
   if (!pair_supported(p->wfmt, p->afmt)) return MOE_ERR_UNSUPPORTED;
   if (p->num_local_experts > 1024) return MOE_ERR_UNSUPPORTED;
@@ -130,11 +130,38 @@ bool tc_applies(const moe_problem_t *p) {
   return p->path == MOE_PATH_AUTO && (long)p->M * p->topk >= kTcMinSlots;
 }
 
+bool tc_mx_direct(const moe_problem_t *p);
+
+// Band of slots per local expert (on average) in which MXFP4 w4a16 problems
+// take the tcgen05 weight-streaming kernels.  Measured on the GPT-OSS-120B
+// shape (96 local experts, ms per step): up to 64 per expert the mma.sync
+// streaming kernels are faster (M = 1024, 43 per expert: 0.65 against 0.71);
+// at 85 per expert these kernels win (M = 2048: 0.72 against 0.94 on the
+// 128-row tcgen05 kernels); at 171 per expert the 128-row kernels win again
+// (M = 4096: 1.36 against 1.49).
+constexpr long kTcStreamMinPerExpert = 64, kTcStreamMaxPerExpert = 128;
+
+// The tcgen05 weight-streaming kernels can run this problem: MXFP4 weights
+// with bf16 activations and the bounded SwiGLU-OAI (an f16 intermediate with
+// no rescale), K and N multiples of 64 (needs MOE_LAYOUT_TC weights too).
+bool tcs_supported(const moe_problem_t *p) {
+  return p->wfmt == W_MXFP4 && p->afmt == A_BF16 && tc_mx_direct(p) && p->K % 64 == 0 &&
+         p->N % 64 == 0 && p->num_local_experts <= 1024;
+}
+// ... and runs it (workspace sized for it).
+bool tcs_applies(const moe_problem_t *p) {
+  if (!tcs_supported(p)) return false;
+  if (p->path == MOE_PATH_TC_STREAM) return true;
+  const long slots = (long)p->M * p->topk;
+  return p->path == MOE_PATH_AUTO && slots > kTcStreamMinPerExpert * p->num_local_experts &&
+         slots <= kTcStreamMaxPerExpert * p->num_local_experts;
+}
+
 // Workspace layout of the tcgen05 path (sort blocks of 128 rows).
 struct TcLayout {
   long cap, blocks;
-  size_t sorted, expert_ids, ntp, counts, x16, x_inv, a1_codes, a1_scales, scratch, inter,
-      i_scales, acc, total;
+  size_t sorted, expert_ids, ntp, counts, offsets, active, n_active, x16, x_inv, a1_codes,
+      a1_scales, scratch, inter, i_scales, acc, total;
   bool f16_x;  // x converted to f16 once per token by the sort (MXFP4 weights)
 };
 
@@ -268,6 +295,9 @@ TcLayout make_tc_layout(const moe_problem_t *p) {
   L.expert_ids = o; o = align_up(o + (size_t)L.blocks * 4);
   L.ntp = o; o = align_up(o + 4);
   L.counts = o; o = align_up(o + (size_t)p->num_local_experts * 4);
+  L.offsets = o; o = align_up(o + (size_t)p->num_local_experts * 4);
+  L.active = o; o = align_up(o + (size_t)p->num_local_experts * 4);
+  L.n_active = o; o = align_up(o + 4);
   L.f16_x = p->wfmt == W_MXFP4 && (p->afmt == A_BF16 || mx_act_f16(p));
   L.x16 = L.x_inv = o;
   if (L.f16_x) {
@@ -458,16 +488,20 @@ int run_w2(const moe_problem_t *p, const void *inter, const void *inter_scales,
 // scales), tcgen05 w2 + reduce, bf16 output.
 int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *w13,
                 const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
-                const int32_t *expert_map, char *ws, void *out, cudaStream_t st);
+                const int32_t *expert_map, char *ws, void *out, cudaStream_t st, bool tcs);
+// The sort's per-expert tables that the tcgen05 weight-streaming kernels read.
+struct TcsRefs {
+  const int32_t *offsets, *counts, *active, *n_active;
+};
 int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales, const void *x16,
               const float *x_inv, const moe_weight_t *w13, const float *topk_weights,
               const int32_t *sorted, const int32_t *eids, const int32_t *ntp, long cap,
               char *scratch, void *inter, void *i_scales, const DeviceInfo &dinfo,
-              cudaStream_t st);
+              cudaStream_t st, const TcsRefs *tcs = nullptr);
 int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
               const moe_weight_t *w2, const float *topk_weights, const int32_t *sorted,
               const int32_t *eids, const int32_t *ntp, long cap, float *acc,
-              const DeviceInfo &dinfo, cudaStream_t st);
+              const DeviceInfo &dinfo, cudaStream_t st, const TcsRefs *tcs = nullptr);
 
 // The batched expert-parallel input as a problem of E_l * max_tokens tokens
 // with one slot each (the slot of row i of expert e is its local expert e,
@@ -542,7 +576,7 @@ long moe_align_capacity(int M, int topk, int num_local_experts, int block_m) {
 size_t moe_workspace_size(const moe_problem_t *p) {
   if (validate_problem(p) != MOE_OK) return 0;
   size_t n = make_layout(p).total;
-  if (tc_applies(p)) {
+  if (tc_applies(p) || tcs_applies(p)) {
     const size_t t = make_tc_layout(p).total;
     if (t > n) n = t;
   }
@@ -711,19 +745,20 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
     return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
-  const bool streaming = (p->path == MOE_PATH_AUTO || p->path == MOE_PATH_STREAM) &&
+  const bool tc_records = w13->packed_tc && w2->packed_tc && aligned16(w13->packed_tc) &&
+                          aligned16(w2->packed_tc);
+  const bool tcs = tc_records && tcs_applies(p);
+  const bool streaming = !tcs && (p->path == MOE_PATH_AUTO || p->path == MOE_PATH_STREAM) &&
                          stream_path(p, w13, w2);
   const bool fp4 = p->wfmt == W_MXFP4 || p->wfmt == W_NVFP4;
   // MX activations run on the f16 kernels when bounded, else on the generic ones
   const bool mx_generic =
       (p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN) && !mx_act_f16(p);
-  if (!streaming && !mx_generic && tc_applies(p) &&
-      (!fp4 || (w13->packed_tc && w2->packed_tc && aligned16(w13->packed_tc) &&
-                aligned16(w2->packed_tc)))) {
+  if (tcs || (!streaming && !mx_generic && tc_applies(p) && (!fp4 || tc_records))) {
     if (ws_bytes < make_tc_layout(p).total) return MOE_ERR_WORKSPACE;
     TimedCall timed;
     return run_tc_path(p, hidden_bf16, w13, w2, topk_ids, topk_weights, expert_map, ws, out_bf16,
-                       st);
+                       st, tcs);
   }
   int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
   int32_t *eids = reinterpret_cast<int32_t *>(ws + L.expert_ids);
@@ -1121,7 +1156,7 @@ int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales,
               const float *x_inv, const moe_weight_t *w13, const float *topk_weights,
               const int32_t *sorted, const int32_t *eids, const int32_t *ntp, long cap,
               char *scratch, void *inter, void *i_scales, const DeviceInfo &dinfo,
-              cudaStream_t st) {
+              cudaStream_t st, const TcsRefs *tcs) {
   const TcScratch L = tc_scratch_layout(p, cap);
   const int S = p->M * p->topk;
   const int s2 = stage2_afmt(p);
@@ -1192,7 +1227,12 @@ int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales,
   }
   {
     StageScope sc(MOE_STAGE_W13, st);
-    rc = cuda_status(bs     ? launch_bs_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
+    if (tcs) {  // weight-streaming kernels: f16 intermediate (bounded SwiGLU-OAI)
+      a.offsets = tcs->offsets; a.counts = tcs->counts;
+      a.active = tcs->active; a.n_active = tcs->n_active;
+    }
+    rc = cuda_status(tcs    ? launch_tcs_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
+                     : bs   ? launch_bs_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
                      : fp8b ? launch_fp8b_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
                             : launch_tc_gemm(a, scratch + L.a_sorted, cap, 1, st));
     sc.done();
@@ -1226,7 +1266,7 @@ int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales,
 int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
               const moe_weight_t *w2, const float *topk_weights, const int32_t *sorted,
               const int32_t *eids, const int32_t *ntp, long cap, float *acc,
-              const DeviceInfo &dinfo, cudaStream_t st) {
+              const DeviceInfo &dinfo, cudaStream_t st, const TcsRefs *tcs) {
   const int s2 = stage2_afmt(p);
   const bool mx = p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN;
   const bool bs = p->wfmt == W_NVFP4;
@@ -1257,8 +1297,13 @@ int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
   a.w_bias = w2->bias; a.bias_f32 = w2->bias_is_f32; a.w_packed = w2->packed_tc;
   a.acc = acc; a.topk_weights = topk_weights;
   if (bs) a.a_sf = i_scales;
+  if (tcs) {
+    a.offsets = tcs->offsets; a.counts = tcs->counts;
+    a.active = tcs->active; a.n_active = tcs->n_active;
+  }
   StageScope sc(MOE_STAGE_W2, st);
-  const int rc = cuda_status(bs ? launch_bs_gemm(a, inter, cap, 0, dinfo.sm_count, st)
+  const int rc = cuda_status(tcs  ? launch_tcs_gemm(a, inter, cap, 0, dinfo.sm_count, st)
+                             : bs ? launch_bs_gemm(a, inter, cap, 0, dinfo.sm_count, st)
                              : p->wfmt == W_FP8_BLOCK128
                                  ? launch_fp8b_gemm(a, inter, cap, 0, dinfo.sm_count, st)
                                  : launch_tc_gemm(a, inter, cap, 0, st));
@@ -1271,7 +1316,7 @@ int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
 // bf16 output.
 int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *w13,
                 const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
-                const int32_t *expert_map, char *ws, void *out, cudaStream_t st) {
+                const int32_t *expert_map, char *ws, void *out, cudaStream_t st, bool tcs) {
   const TcLayout L = make_tc_layout(p);
   DeviceInfo dinfo;
   int rc = device_info(&dinfo);
@@ -1287,6 +1332,11 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     ex.zero_buf = acc;
     ex.zero_n = MK;
     ex.num_valid_tokens = p->num_local_tokens;
+    if (tcs) {  // per-expert tables of the weight-streaming kernels
+      ex.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+      ex.active = reinterpret_cast<int32_t *>(ws + L.active);
+      ex.n_active = reinterpret_cast<int32_t *>(ws + L.n_active);
+    }
     if (L.f16_x) {
       ex.x = static_cast<const uint16_t *>(hidden);
       ex.x16 = ws + L.x16;
@@ -1318,13 +1368,20 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     codes = ws + L.a1_codes;
     scales = ws + L.a1_scales;
   }
+  TcsRefs tr{};
+  if (tcs) {
+    tr.counts = counts;
+    tr.offsets = reinterpret_cast<const int32_t *>(ws + L.offsets);
+    tr.active = reinterpret_cast<const int32_t *>(ws + L.active);
+    tr.n_active = reinterpret_cast<const int32_t *>(ws + L.n_active);
+  }
   if ((rc = tc_stage1(p, codes, scales, L.f16_x ? ws + L.x16 : nullptr,
                       L.f16_x ? reinterpret_cast<const float *>(ws + L.x_inv) : nullptr, w13,
                       topk_weights, sorted, eids, ntp, L.cap, ws + L.scratch, ws + L.inter,
-                      ws + L.i_scales, dinfo, st)) != MOE_OK)
+                      ws + L.i_scales, dinfo, st, tcs ? &tr : nullptr)) != MOE_OK)
     return rc;
   if ((rc = tc_stage2(p, ws + L.inter, ws + L.i_scales, w2, topk_weights, sorted, eids, ntp,
-                      L.cap, acc, dinfo, st)) != MOE_OK)
+                      L.cap, acc, dinfo, st, tcs ? &tr : nullptr)) != MOE_OK)
     return rc;
   StageScope sc(MOE_STAGE_FINALIZE, st);
   rc = cuda_status(launch_finalize(acc, MK, out, st));

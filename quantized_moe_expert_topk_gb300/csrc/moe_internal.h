@@ -241,6 +241,9 @@ struct TcArgs {
   int rec_bytes;         // set by the launcher
   int mgroup;            // raster: m-blocks that walk the n-tiles together (launcher)
   long nblocks;          // m-blocks in the grid (launcher)
+  // weight-streaming tcgen05 kernels (moe_tcs.cu): the sort's per-expert
+  // sorted-row offsets and slot counts [El], the active-expert list and its length
+  const int32_t *offsets, *counts, *active, *n_active;
 };
 struct GatherArgs {
   const int32_t *sorted_ids, *num_post_pad;
@@ -273,6 +276,15 @@ cudaError_t launch_pack_tc_fp4(const TcPackArgs &p, cudaStream_t st);
 cudaError_t launch_gather_rows(const GatherArgs &g, long cap_rows, cudaStream_t st);
 cudaError_t launch_tc_gemm(const TcArgs &a, const void *a_sorted, long cap_rows, int w13,
                            cudaStream_t st);
+// Weight-streaming tcgen05 grouped GEMMs (moe_tcs.cu), MXFP4 w4a16 with the
+// bounded SwiGLU-OAI: the weights (TC-packed records) are the MMA's M operand,
+// up to 256 of an expert's sorted f16 rows (rows_f16 [cap_rows, C]) its N
+// operand.  W13 writes the f16 intermediate [cap_rows, N] (a.out); W2 adds
+// the router-weighted rows into a.acc.  Needs a.offsets / counts / active /
+// n_active from the sort and C % 64 == 0.
+int tcs_ntiles(int w13, int N, int K);
+cudaError_t launch_tcs_gemm(const TcArgs &a, const void *rows_f16, long cap_rows, int w13,
+                            int sm_count, cudaStream_t st);
 // Persistent block-scaled NVFP4 grouped GEMMs (moe_bs.cu): A = packed e2m1
 // codes [cap, C/2] + scale-factor records (a.a_sf); B = the MOE_LAYOUT_TC
 // records of NVFP4 weights (a.w_packed).  W13 writes the NVFP4 intermediate

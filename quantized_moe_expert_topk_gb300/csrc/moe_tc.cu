@@ -739,6 +739,12 @@ bool make_tc_map_u8(CUtensorMap *tm, const void *base, long rows, long cols, int
   return make_map(tm, base, rows, cols, true, box_rows);
 }
 
+// 2-D K-major 16-bit tensor map with the 128-byte swizzle (the weight-streaming
+// kernels' slot rows).
+bool make_tc_map_b16(CUtensorMap *tm, const void *base, long rows, long cols, int box_rows) {
+  return make_map(tm, base, rows, cols, false, box_rows);
+}
+
 int tc_ntiles(int w13, int N, int K) { return w13 ? (int)ceil_div(N, 64) : (int)ceil_div(K, BN); }
 
 size_t tc_packed_bytes(int w13, int nvfp4, int N, int K, int El) {

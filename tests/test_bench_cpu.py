@@ -30,11 +30,20 @@ def test_kernel_path_of_each_workload():
     assert bench.kernel_path(make_workload("gptoss20b_w4a4_m64")) == "stream"
     assert bench.kernel_path(make_workload("gptoss20b_w4a8_m64")) == "stream"
     assert bench.kernel_path(make_workload("tiny_bf16_m16")) == "generic"
-    # prefill sizes take the tcgen05 kernels; the streaming bound is 64 slots per expert
+    # prefill sizes take the tcgen05 kernels; MXFP4 w4a16 with 64 to 128 slots
+    # per local expert the tcgen05 weight-streaming kernels
     assert bench.kernel_path(make_workload("gptoss20b_w4a4_m64", M=4096)) == "tc"
     assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=512)) == "stream"
-    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=1024)) == "stream"
-    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=2048)) == "tc"
+    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=1536)) == "stream"
+    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=2048)) == "tc_stream"
+    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=3072)) == "tc_stream"
+    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=4096)) == "tc"
+    assert bench.kernel_path(make_workload("gptoss20b_mxfp4_m64", M=4096)) == "tc"
+    # a forced family where it applies, else the automatic choice
+    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=512), "tc") == "tc"
+    assert bench.kernel_path(make_workload("gptoss120b_mxfp4_ep75", M=512), "stream") == "stream"
+    assert bench.kernel_path(make_workload("gptoss20b_mxfp4_m64"), "tc_stream") == "tc_stream"
+    assert bench.kernel_path(make_workload("tiny_bf16_m16"), "tc_stream") == "generic"
 
 
 def test_mx_activations_without_bounded_swiglu_stay_generic():
@@ -78,6 +87,10 @@ def test_launches_per_step():
     assert bench.launches_per_step(w4a4, fused=False) == 5       # + the MX pass
     # tcgen05 MX prefill: sort, gather, w13 (MX epilogue), w2, finalize
     assert bench.launches_per_step(make_workload("gptoss20b_w4a4_m64", M=4096)) == 5
+    # tcgen05 weight streaming: sort, gather, w13, w2, finalize
+    assert bench.launches_per_step(make_workload("gptoss120b_mxfp4_ep75", M=2048)) == 5
+    # FP8 block: sort, quant, gather, w13 (1 x 128 requantisation inside), w2, finalize
+    assert bench.launches_per_step(make_workload("dsv3_fp8block_m4096")) == 6
     # generic bf16: sort, w13, w2, finalize
     assert bench.launches_per_step(make_workload("tiny_bf16_m16")) == 4
 

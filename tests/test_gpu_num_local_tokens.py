@@ -16,6 +16,7 @@ CASES = [
     # wfmt, afmt, act, gate, M, T, path
     ("mxfp4", "bf16", "swiglu_oai", "interleaved", 64, 4, "stream"),
     ("mxfp4", "bf16", "swiglu_oai", "interleaved", 64, 4, "tc"),
+    ("mxfp4", "bf16", "swiglu_oai", "interleaved", 64, 4, "tc_stream"),
     ("bf16", "bf16", "silu", "separated", 40, 2, "generic"),
     ("fp8_block128", "fp8_group128_dyn", "silu", "separated", 48, 2, "tc"),
     ("nvfp4", "nvfp4_dyn", "silu", "separated", 48, 2, "generic"),
