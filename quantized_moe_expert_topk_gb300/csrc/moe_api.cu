@@ -15,6 +15,7 @@
 
 #include <math.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -148,6 +149,11 @@ bool tcs_supported(const moe_problem_t *p) {
   return p->wfmt == W_MXFP4 && p->afmt == A_BF16 && tc_mx_direct(p) && p->K % 64 == 0 &&
          p->N % 64 == 0 && p->num_local_experts <= 1024;
 }
+// Sort block of the tcgen05 weight-streaming kernels: their passes start
+// anywhere in an expert's rows, so 16-row blocks (fewer padding rows to
+// gather) instead of the 128 of the other tcgen05 kernels.
+constexpr int kTcsBlockM = 16;
+
 // ... and runs it (workspace sized for it).
 bool tcs_applies(const moe_problem_t *p) {
   if (!tcs_supported(p)) return false;
@@ -285,9 +291,9 @@ void tc_inter_sizes(const moe_problem_t *p, long cap, size_t *inter, size_t *sca
   }
 }
 
-TcLayout make_tc_layout(const moe_problem_t *p) {
+TcLayout make_tc_layout(const moe_problem_t *p, bool tcs = false) {
   TcLayout L;
-  const int BM = kTcBlockM;
+  const int BM = tcs ? kTcsBlockM : kTcBlockM;
   L.cap = moe_align_capacity(p->M, p->topk, p->num_local_experts, BM);
   L.blocks = L.cap / BM;
   size_t o = 0;
@@ -576,10 +582,8 @@ long moe_align_capacity(int M, int topk, int num_local_experts, int block_m) {
 size_t moe_workspace_size(const moe_problem_t *p) {
   if (validate_problem(p) != MOE_OK) return 0;
   size_t n = make_layout(p).total;
-  if (tc_applies(p) || tcs_applies(p)) {
-    const size_t t = make_tc_layout(p).total;
-    if (t > n) n = t;
-  }
+  if (tc_applies(p)) n = std::max(n, make_tc_layout(p).total);
+  if (tcs_applies(p)) n = std::max(n, make_tc_layout(p, true).total);
   return n;
 }
 
@@ -755,7 +759,7 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
   const bool mx_generic =
       (p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN) && !mx_act_f16(p);
   if (tcs || (!streaming && !mx_generic && tc_applies(p) && (!fp4 || tc_records))) {
-    if (ws_bytes < make_tc_layout(p).total) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < make_tc_layout(p, tcs).total) return MOE_ERR_WORKSPACE;
     TimedCall timed;
     return run_tc_path(p, hidden_bf16, w13, w2, topk_ids, topk_weights, expert_map, ws, out_bf16,
                        st, tcs);
@@ -1317,7 +1321,7 @@ int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
 int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *w13,
                 const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
                 const int32_t *expert_map, char *ws, void *out, cudaStream_t st, bool tcs) {
-  const TcLayout L = make_tc_layout(p);
+  const TcLayout L = make_tc_layout(p, tcs);
   DeviceInfo dinfo;
   int rc = device_info(&dinfo);
   if (rc != MOE_OK) return rc;
@@ -1347,8 +1351,8 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     }
     StageScope sc(MOE_STAGE_ALIGN, st);
     rc = cuda_status(launch_align(topk_ids, p->M, p->topk, expert_map, p->num_experts,
-                                  p->num_local_experts, kTcBlockM, sorted, eids, ntp, counts,
-                                  L.cap, ex, st));
+                                  p->num_local_experts, tcs ? kTcsBlockM : kTcBlockM, sorted, eids,
+                                  ntp, counts, L.cap, ex, st));
     sc.done();
     if (rc != MOE_OK) return rc;
   }

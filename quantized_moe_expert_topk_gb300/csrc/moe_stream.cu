@@ -98,6 +98,12 @@ struct Smem {
   // epilogue parity) and a barrier of two arrivals
   uint64_t mx_bar[CW / 2];
   float mx_amax[2][CW][TOKMAX];
+  // per consumer warp, the epilogue operands of the pass's tokens (slot id;
+  // W13: x_inv of the token, W2: router weight; W13: factor of the stage-1
+  // output), loaded at the pass's first stage and read by its epilogue (in
+  // shared memory rather than registers, which the main loop needs)
+  int tok_sid[CW][TOKMAX];
+  float tok_f[CW][TOKMAX], tok_zw[CW][TOKMAX];
   int abort_flag;
 };
 constexpr size_t SMEM_BYTES = sizeof(Smem);
@@ -331,9 +337,13 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
   Unit U = {0, 0, 0, 0, 0, 0};
   int nt = 0, ntiles = 0;
   float acc[MT][2][4];
-  int tok_sid[2][2] = {{0, 0}, {0, 0}};      // sorted slot ids of this thread's tokens
-  float tok_f[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // W13: x_inv of the token; W2: router weight
-  float tok_zw[2][2] = {{1.f, 1.f}, {1.f, 1.f}};  // W13: factor of the stage-1 output
+  // this thread's tokens n * 8 + 2 t + c (n, c in {0, 1}) of the pass
+  int *const tok_sid_w = sm.tok_sid[warp];
+  float *const tok_f_w = sm.tok_f[warp];
+  float *const tok_zw_w = sm.tok_zw[warp];
+#define TOK_SID(n, c) tok_sid_w[(n) * 8 + 2 * t + (c)]
+#define TOK_F(n, c) tok_f_w[(n) * 8 + 2 * t + (c)]
+#define TOK_ZW(n, c) tok_zw_w[(n) * 8 + 2 * t + (c)]
   bool w2 = MODE == MODE_W2;  // phase of the current unit
   uint32_t mx_ep = 0;         // MXQ: epilogues of this warp so far (barrier parity)
   while (true) {
@@ -366,27 +376,25 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
         for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int c = 0; c < 4; ++c) acc[m][n][c] = 0.f;
-      // epilogue operands of this thread's tokens, loaded now so that their
+      // epilogue operands of the pass's tokens (lanes 0-3 write them; the
+      // epilogue reads them after the pass), loaded now so that their
       // latency hides behind the pass
+      if (g == 0) {
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int tn = n * 8 + 2 * t + c;
-          tok_sid[n][c] = tn < nt ? a.sorted_ids[U.off + d.tok0 + tn] : 0;
-        }
-#pragma unroll
-      for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int tn = n * 8 + 2 * t + c;
-          // W13: x_inv of the token (times the router weight when it applies to
-          // the stage-1 output); W2: the router weight (1 in that case)
-          const float wr = a.w_stage1 ? (!w2 ? a.topk_weights[tok_sid[n][c]] : 1.f)
-                                      : (!w2 ? 1.f : a.topk_weights[tok_sid[n][c]]);
-          tok_f[n][c] = tn >= nt ? 0.f : !w2 ? a.x_inv[tok_sid[n][c] / a.T] : wr;
-          tok_zw[n][c] = !w2 && tn < nt ? wr : 1.f;
-        }
+          for (int c = 0; c < 2; ++c) {
+            const int tn = n * 8 + 2 * t + c;
+            const int sid = tn < nt ? a.sorted_ids[U.off + d.tok0 + tn] : 0;
+            // W13: x_inv of the token (times the router weight when it applies
+            // to the stage-1 output); W2: the router weight (1 in that case)
+            const float wr = a.w_stage1 ? (!w2 ? a.topk_weights[sid] : 1.f)
+                                        : (!w2 ? 1.f : a.topk_weights[sid]);
+            TOK_SID(n, c) = sid;
+            TOK_F(n, c) = tn >= nt ? 0.f : !w2 ? a.x_inv[sid / a.T] : wr;
+            TOK_ZW(n, c) = !w2 && tn < nt ? wr : 1.f;
+          }
+      }
     }
     const int nkb = min(S_KB, U.nkb - d.kb);
     const unsigned char *ws = sm.stage[slot];
@@ -431,9 +439,9 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
           for (int c = 0; c < 2; ++c) {
             const int tn = n * 8 + 2 * t + c;
             if (tn >= nt) continue;
-            const float xi = tok_f[n][c];
+            const float xi = TOK_F(n, c);
             float2 *dst = reinterpret_cast<float2 *>(a.hpart) +
-                          ((long)ks * a.S + tok_sid[n][c]) * N + j;
+                          ((long)ks * a.S + TOK_SID(n, c)) * N + j;
             *dst = make_float2(acc[m][n][c] * xi, acc[m][n][2 + c] * xi);
           }
       }
@@ -467,20 +475,20 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
             const int tn = n * 8 + 2 * t + c;
             if (tn >= nt) continue;
             const int r = U.off + tok0 + tn;
-            const float xi = tok_f[n][c];
+            const float xi = TOK_F(n, c);
             float gsum = acc[m][n][c] * xi, usum = acc[m][n][2 + c] * xi;
             if (SPLIT) {  // the sum of every k-range's partial, in k order
               gsum = usum = 0.f;
               for (int ks = 0; ks < a.ksplit; ++ks) {
                 const float2 v = __ldcg(reinterpret_cast<const float2 *>(a.hpart) +
-                                        ((long)ks * a.S + tok_sid[n][c]) * N + j);
+                                        ((long)ks * a.S + TOK_SID(n, c)) * N + j);
                 gsum += v.x;
                 usum += v.y;
               }
             }
             const float gv = gsum + bg;
             const float uv = usum + bu;
-            const float z = tok_zw[n][c] * act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit);
+            const float z = TOK_ZW(n, c) * act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit);
             if (a.out_f32)
               static_cast<float *>(a.out)[(long)r * N + j] = z;
             else
@@ -499,8 +507,8 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
             bg = bf16_to_f32(bb[grow]);
             bu = bf16_to_f32(bb[urow]);
           }
-          const float xi = tok_f[n][c];
-          return tok_zw[n][c] * act_and_mul(a.act, acc[m][n][c] * xi + bg,
+          const float xi = TOK_F(n, c);
+          return TOK_ZW(n, c) * act_and_mul(a.act, acc[m][n][c] * xi + bg,
                                             acc[m][n][2 + c] * xi + bu, a.alpha, a.beta, a.limit);
         };
         // per token, the largest |z| of this warp's 16 outputs (the lanes of
@@ -577,14 +585,18 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
             for (int c = 0; c < 2; ++c) {
               const int tn = n * 8 + 2 * t + c;
               if (tn >= nt) continue;
-              const int sidx = tok_sid[n][c];
-              const float wt = tok_f[n][c];
+              const int sidx = TOK_SID(n, c);
+              const float wt = TOK_F(n, c);
               atomicAdd(w.acc + (long)(sidx / w.T) * K + i, wt * (acc[m][n][2 * h + c] + bias));
             }
         }
     }
   }
 }
+
+#undef TOK_SID
+#undef TOK_F
+#undef TOK_ZW
 
 // ---------------------------------------------------------------- packing
 // One thread per packed byte.
