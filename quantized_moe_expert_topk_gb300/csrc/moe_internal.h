@@ -165,6 +165,9 @@ struct StreamArgs {
   // fused W13 + W2 grid (launch_stream_fused): per local expert, the count of
   // (W13 unit, pass, consumer warp) epilogues done; zeroed by the sort
   int *done13;
+  // tokens per pass of the fused grid: 16 (0 reads as 16), or 32 (no k-split,
+  // no MX epilogue; three CTAs per SM): both argument blocks the same
+  int tok_pass;
 };
 // k-split of the W13 streaming units for this problem (1 = whole K per unit).
 int stream_w13_ksplit(int M, int topk, int El, int N, int K, int sm_count);

@@ -22,8 +22,8 @@
 // Arithmetic (swap-AB mma.sync m16n8k16, f16 x f16 -> fp32):
 //   A = weights: e2m1 codes converted two at a time by the hardware
 //       (cvt.rn.f16x2.e2m1x2) -- exact, no scale applied;
-//   B = the expert's tokens (up to 16 per pass, more passes re-stream the
-//       unit), already in f16 in HBM: stage-1 rows scaled per token by a power
+//   B = the expert's tokens (up to 16 or 32 per pass, more passes re-stream
+//       the unit), already in f16 in HBM: stage-1 rows scaled per token by a power
 //       of two (exact for bf16 inputs), stage-2 rows are the bounded SwiGLU-OAI
 //       intermediate;
 //   the e8m0 scale of each (row, 32-element group) multiplies the fp32 partial
@@ -57,13 +57,16 @@ constexpr int TILE_BYTES = 512 + 32;        // codes + scales of one tile, one k
 constexpr int REC_BYTES = TILES * TILE_BYTES;  // 4352 B per (unit, k64 block)
 constexpr int S_KB = 4;                     // k64 blocks per stage (256 reduction elements)
 constexpr int NS = 2;                       // pipeline stages (double buffer)
-constexpr int TOKMAX = 16;                  // tokens per pass (two n8 tiles)
 constexpr int XS = S_KB * 64 * 2 + 16;      // smem row stride of the token tile (528 B)
 constexpr int W_STAGE = S_KB * REC_BYTES;   // 17408 B
-constexpr int X_STAGE = TOKMAX * XS;        // 8448 B
-constexpr int STAGE_BYTES = W_STAGE + X_STAGE;
 constexpr int THREADS = (CW + 1) * 32;
-constexpr int CTAS_PER_SM = 4;
+// Tokens per pass TOK (n8 tiles TOK / 8): 16 at four CTAs per SM, or -- when
+// the experts hold more than 32 slots each, for which 16-token passes would
+// decode each weight tile three times or more -- 32 at three CTAs per SM (the
+// token tiles take the shared memory and the accumulators the registers of
+// the fourth).
+template <int TOK> constexpr int ctas_per_sm() { return TOK == 16 ? 4 : 3; }
+template <int TOK> constexpr int stage_bytes() { return W_STAGE + TOK * XS; }
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int kErrTimeout = 5;
 
@@ -88,8 +91,9 @@ struct StageDesc {
   Unit unit;
 };
 
+template <int TOK>
 struct Smem {
-  unsigned char stage[NS][STAGE_BYTES];
+  unsigned char stage[NS][stage_bytes<TOK>()];
   uint64_t full[NS];
   uint64_t empty[NS];
   StageDesc desc[NS];
@@ -97,16 +101,19 @@ struct Smem {
   // maxima over their 16 outputs of a 32-output block (double-buffered by
   // epilogue parity) and a barrier of two arrivals
   uint64_t mx_bar[CW / 2];
-  float mx_amax[2][CW][TOKMAX];
+  float mx_amax[2][CW][TOK];
   // per consumer warp, the epilogue operands of the pass's tokens (slot id;
   // W13: x_inv of the token, W2: router weight; W13: factor of the stage-1
   // output), loaded at the pass's first stage and read by its epilogue (in
   // shared memory rather than registers, which the main loop needs)
-  int tok_sid[CW][TOKMAX];
-  float tok_f[CW][TOKMAX], tok_zw[CW][TOKMAX];
+  int tok_sid[CW][TOK];
+  float tok_f[CW][TOK], tok_zw[CW][TOK];
   int abort_flag;
 };
-constexpr size_t SMEM_BYTES = sizeof(Smem);
+template <int TOK> constexpr size_t smem_bytes() { return sizeof(Smem<TOK>); }
+static_assert(ctas_per_sm<16>() * (smem_bytes<16>() + 1024) <= 228 * 1024 &&
+                  ctas_per_sm<32>() * (smem_bytes<32>() + 1024) <= 228 * 1024,
+              "shared memory per SM");
 
 __device__ __forceinline__ Unit decode_unit(const StreamArgs &a, int id) {
   Unit r;
@@ -130,10 +137,11 @@ __device__ __forceinline__ float e8m0_byte_f32(uint32_t w, uint32_t idx) {
   return __uint_as_float(__byte_perm(w, 0u, 0x4440u | idx) * 8388608u);
 }
 
-// One k64 block of one consumer warp: MT m16 tiles x NTILES n8 token tiles.
-template <int NTILES>
+// One k64 block of one consumer warp: MT m16 tiles x NTILES n8 token tiles
+// (of the NT the accumulators hold).
+template <int NTILES, int NT>
 __device__ __forceinline__ void consume_k64(const unsigned char *tp0, uint32_t xs_k64, int lane,
-                                            float (&acc)[MT][2][4]) {
+                                            float (&acc)[MT][NT][4]) {
   const int g = lane >> 2;
   uint4 cw[MT];
   uint32_t sw[MT];
@@ -143,46 +151,46 @@ __device__ __forceinline__ void consume_k64(const unsigned char *tp0, uint32_t x
     cw[m] = *reinterpret_cast<const uint4 *>(tp + lane * 16);
     sw[m] = *reinterpret_cast<const uint32_t *>(tp + 512 + g * 4);
   }
-  // B fragments of the four k16 steps (both n8 token tiles)
-  uint32_t bf[4][4];
-#pragma unroll
-  for (int s4 = 0; s4 < 4; ++s4) {
-    const uint32_t addr = xs_k64 + ((lane & 7) + ((lane >> 4) << 3)) * XS +
-                          (s4 * 16 + ((lane >> 3) & 1) * 8) * 2;
-    if (NTILES == 2) {
-      ldmatrix_x4_b16(bf[s4], addr);
-    } else {
-      uint32_t r2[2];
-      ldmatrix_x2_b16(r2, addr);
-      bf[s4][0] = r2[0];
-      bf[s4][1] = r2[1];
-    }
-  }
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
-    float part[MT][NTILES][4];
+    // B fragments of k16 steps 2 kk and 2 kk + 1: n8 tiles in pairs (tokens
+    // 16 p .. 16 p + 15) by one ldmatrix x4, an odd last tile by an x2
+    uint32_t bf[2][NTILES][2];
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2) {
+      const int s4 = 2 * kk + s2;
+#pragma unroll
+      for (int p = 0; p < (NTILES + 1) / 2; ++p) {
+        const uint32_t addr = xs_k64 + (p * 16 + (lane & 7) + ((lane >> 4) << 3)) * XS +
+                              (s4 * 16 + ((lane >> 3) & 1) * 8) * 2;
+        if (2 * p + 1 < NTILES) {
+          uint32_t r[4];
+          ldmatrix_x4_b16(r, addr);
+          bf[s2][2 * p][0] = r[0]; bf[s2][2 * p][1] = r[1];
+          bf[s2][2 * p + 1][0] = r[2]; bf[s2][2 * p + 1][1] = r[3];
+        } else {
+          uint32_t r[2];
+          ldmatrix_x2_b16(r, addr);
+          bf[s2][2 * p][0] = r[0]; bf[s2][2 * p][1] = r[1];
+        }
+      }
+    }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       uint32_t a0[4], a1[4];
       e2m1x8_to_f16x2x4(kk == 0 ? cw[m].x : cw[m].z, a0);
       e2m1x8_to_f16x2x4(kk == 0 ? cw[m].y : cw[m].w, a1);
+      // e8m0 scales of rows g and g+8 for this 32-element group
+      const float f_lo = e8m0_byte_f32(sw[m], 2 * kk);
+      const float f_hi = e8m0_byte_f32(sw[m], 2 * kk + 1);
       const float zero[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int n = 0; n < NTILES; ++n) {
-        mma_f16_16816(part[m][n], a0, bf[2 * kk][2 * n], bf[2 * kk][2 * n + 1], zero);
-        mma_f16_16816(part[m][n], a1, bf[2 * kk + 1][2 * n], bf[2 * kk + 1][2 * n + 1],
-                      part[m][n]);
-      }
-    }
-    // e8m0 scales of rows g and g+8 for this 32-element group
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      const float f_lo = e8m0_byte_f32(sw[m], 2 * kk);
-      const float f_hi = e8m0_byte_f32(sw[m], 2 * kk + 1);
-#pragma unroll
-      for (int n = 0; n < NTILES; ++n) {
-        fma_f32x2(acc[m][n][0], acc[m][n][1], part[m][n][0], part[m][n][1], f_lo);
-        fma_f32x2(acc[m][n][2], acc[m][n][3], part[m][n][2], part[m][n][3], f_hi);
+        float part[4];
+        mma_f16_16816(part, a0, bf[0][n][0], bf[0][n][1], zero);
+        mma_f16_16816(part, a1, bf[1][n][0], bf[1][n][1], part);
+        fma_f32x2(acc[m][n][0], acc[m][n][1], part[0], part[1], f_lo);
+        fma_f32x2(acc[m][n][2], acc[m][n][3], part[2], part[3], f_hi);
       }
     }
   }
@@ -194,11 +202,13 @@ __device__ __forceinline__ void consume_k64(const unsigned char *tp0, uint32_t x
 // intermediate into OCP MX (a.out_mx: 1 MXFP4, 2 MXFP8) before its f16 store.
 // A 32-output block spans the 16 outputs of two consumer warps (2w, 2w+1),
 // which exchange their per-token maxima through shared memory.
-template <int MODE, bool SPLIT, bool MXQ = false>
-__global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
+template <int MODE, bool SPLIT, bool MXQ = false, int TOK = 16>
+__global__ void __launch_bounds__(THREADS, ctas_per_sm<TOK>())
 stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ StreamArgs b) {
+  static_assert(TOK == 16 || (TOK == 32 && !SPLIT && !MXQ), "pass width");
+  constexpr int NT = TOK / 8;  // n8 token tiles per pass
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  Smem<TOK> &sm = *reinterpret_cast<Smem<TOK> *>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -275,7 +285,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
         // unit of it has finished every pass (one count per consumer warp,
         // from the warp that applies the epilogue: with a k-split, the last
         // arrival); those units were claimed earlier by running CTAs
-        const int need = a.units_per_expert * CW * (int)ceil_div(U.cnt, TOKMAX);
+        const int need = a.units_per_expert * CW * (int)ceil_div(U.cnt, TOK);
         if (!wait_count_bounded(a.done13 + U.e, need, kWaitCycles, a.err)) {
           record_device_error(a.err, kErrTimeout);
           *abort_flag = 1;
@@ -283,8 +293,8 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
         }
         fence_proxy_async_global();  // their generic stores before our TMA reads
       }
-      for (int tok0 = 0; tok0 < U.cnt && ok; tok0 += TOKMAX) {
-        const int nt = min(TOKMAX, U.cnt - tok0);
+      for (int tok0 = 0; tok0 < U.cnt && ok; tok0 += TOK) {
+        const int nt = min(TOK, U.cnt - tok0);
         const unsigned char *xrow = nullptr;  // lane n < nt loads token n of this pass
         if (lane < nt) {
           const int r = U.off + tok0 + lane;
@@ -336,7 +346,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
   uint32_t it = 0;
   Unit U = {0, 0, 0, 0, 0, 0};
   int nt = 0, ntiles = 0;
-  float acc[MT][2][4];
+  float acc[MT][NT][4];
   // this thread's tokens n * 8 + 2 t + c (n, c in {0, 1}) of the pass
   int *const tok_sid_w = sm.tok_sid[warp];
   float *const tok_f_w = sm.tok_f[warp];
@@ -367,13 +377,13 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
         const volatile int *uv = reinterpret_cast<const volatile int *>(&sm.desc[slot].unit);
         U.e = uv[0]; U.u = uv[1]; U.kb0 = uv[2]; U.nkb = uv[3]; U.off = uv[4]; U.cnt = uv[5];
       }
-      nt = min(TOKMAX, U.cnt - d.tok0);
+      nt = min(TOK, U.cnt - d.tok0);
       ntiles = (nt + 7) >> 3;
       if (MODE == MODE_FUSED) w2 = (d.flags & F_W2) != 0;
 #pragma unroll
       for (int m = 0; m < MT; ++m)
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
           for (int c = 0; c < 4; ++c) acc[m][n][c] = 0.f;
       // epilogue operands of the pass's tokens (lanes 0-3 write them; the
@@ -381,7 +391,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
       // latency hides behind the pass
       if (g == 0) {
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const int tn = n * 8 + 2 * t + c;
@@ -400,20 +410,26 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
     const unsigned char *ws = sm.stage[slot];
     const uint32_t xs = smem_addr(ws + W_STAGE);
     const unsigned char *tw = ws + (warp * MT) * TILE_BYTES;
-    if (nkb == S_KB) {
-      // full stage: straight-line code over the S_KB blocks, so the
+    if (nkb == S_KB && ntiles == NT) {
+      // full stage and pass: straight-line code over the S_KB blocks, so the
       // conversions, MMAs and scale FMAs of different blocks interleave
-      if (ntiles == 2) {
 #pragma unroll
-        for (int b = 0; b < S_KB; ++b) consume_k64<2>(tw + b * REC_BYTES, xs + b * 128, lane, acc);
-      } else {
+      for (int b = 0; b < S_KB; ++b)
+        consume_k64<NT, NT>(tw + b * REC_BYTES, xs + b * 128, lane, acc);
+    } else if (nkb == S_KB && ntiles == 1) {
 #pragma unroll
-        for (int b = 0; b < S_KB; ++b) consume_k64<1>(tw + b * REC_BYTES, xs + b * 128, lane, acc);
-      }
+      for (int b = 0; b < S_KB; ++b)
+        consume_k64<1, NT>(tw + b * REC_BYTES, xs + b * 128, lane, acc);
     } else {
       for (int b = 0; b < nkb; ++b) {
-        if (ntiles == 2) consume_k64<2>(tw + b * REC_BYTES, xs + b * 128, lane, acc);
-        else consume_k64<1>(tw + b * REC_BYTES, xs + b * 128, lane, acc);
+        const unsigned char *tb = tw + b * REC_BYTES;
+        const uint32_t xb = xs + b * 128;
+        if (ntiles == 1) consume_k64<1, NT>(tb, xb, lane, acc);
+        else if (ntiles == 2) consume_k64<2, NT>(tb, xb, lane, acc);
+        else if constexpr (NT == 4) {
+          if (ntiles == 3) consume_k64<3, NT>(tb, xb, lane, acc);
+          else consume_k64<4, NT>(tb, xb, lane, acc);
+        }
       }
     }
     __syncwarp();
@@ -434,7 +450,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
       for (int m = 0; m < MT; ++m) {
         const int j = U.u * (TILES * 8) + (warp * MT + m) * 8 + g;
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const int tn = n * 8 + 2 * t + c;
@@ -469,7 +485,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
           bu = bf16_to_f32(bb[urow]);
         }
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const int tn = n * 8 + 2 * t + c;
@@ -516,7 +532,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
         // z is computed again for the store rather than held across the wait
         float pa[2][2];
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const bool in = n * 8 + 2 * t + c < nt;
@@ -528,7 +544,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
         const int buf = mx_ep & 1;
         if (g == 0)
 #pragma unroll
-          for (int n = 0; n < 2; ++n)
+          for (int n = 0; n < NT; ++n)
 #pragma unroll
             for (int c = 0; c < 2; ++c) sm.mx_amax[buf][warp][n * 8 + 2 * t + c] = pa[n][c];
         __syncwarp();
@@ -541,7 +557,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
         ++mx_ep;
         const bool fp4 = a.out_mx == 1;
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const int tn = n * 8 + 2 * t + c;
@@ -580,7 +596,7 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
           if (w.bias && U.kb0 == 0)
             bias = bf16_to_f32(static_cast<const uint16_t *>(w.bias)[(long)U.e * K + i]);
 #pragma unroll
-          for (int n = 0; n < 2; ++n)
+          for (int n = 0; n < NT; ++n)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
               const int tn = n * 8 + 2 * t + c;
@@ -663,7 +679,7 @@ int stream_w13_ksplit(int M, int topk, int El, int N, int K, int sm_count) {
   // k-range keeps at least two stages
   const long act = (long)M * topk < El ? (long)M * topk : El;
   const long units = act * (N / (TILES * 8));
-  const long want = units > 0 ? ceil_div(2L * CTAS_PER_SM * sm_count, units) : 1;
+  const long want = units > 0 ? ceil_div(2L * ctas_per_sm<16>() * sm_count, units) : 1;
   const long cap = (K / 64) / (2 * S_KB) > 1 ? (K / 64) / (2 * S_KB) : 1;
   return (int)(want <= 1 ? 1 : (want < cap ? want : cap));
 }
@@ -682,41 +698,46 @@ cudaError_t launch_stream(const StreamArgs &a, int w13, int sm_count, cudaStream
   static bool attr_done[3] = {false, false, false};
   if (!attr_done[variant]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+                                         (int)smem_bytes<16>());
     if (e != cudaSuccess) return e;
     attr_done[variant] = true;
   }
   const long max_units = (long)a.max_active * a.units_per_expert * a.ksplit;
-  long grid = (long)CTAS_PER_SM * sm_count;
+  long grid = (long)ctas_per_sm<16>() * sm_count;
   if (grid > max_units) grid = max_units;
   if (grid <= 0) return cudaSuccess;
   // a programmatic dependent of the previous kernel (the sort, or the W13 grid)
-  return launch_kernel(kern, dim3((unsigned)grid), dim3(THREADS), SMEM_BYTES, stream, true, a, a);
+  return launch_kernel(kern, dim3((unsigned)grid), dim3(THREADS), smem_bytes<16>(), stream, true,
+                       a, a);
 }
 
 cudaError_t launch_stream_fused(const StreamArgs &a13, const StreamArgs &a2, int sm_count,
                                 cudaStream_t stream) {
   // the MX epilogue exchanges block maxima inside one CTA: no k-split with it
   if (!a13.done13 || a13.out_f32 || (a13.out_mx && a13.ksplit != 1)) return cudaErrorInvalidValue;
-  const int variant = a13.out_mx ? 1 : a13.ksplit > 1 ? 2 : 0;
-  auto kern = variant == 1   ? stream_kernel<MODE_FUSED, false, true>
+  // 32-token passes: only without the k-split and the MX epilogue
+  const bool wide = a13.tok_pass == 32;
+  if (wide && (a13.out_mx || a13.ksplit != 1 || a2.tok_pass != 32)) return cudaErrorInvalidValue;
+  const int variant = wide ? 3 : a13.out_mx ? 1 : a13.ksplit > 1 ? 2 : 0;
+  auto kern = variant == 3   ? stream_kernel<MODE_FUSED, false, false, 32>
+              : variant == 1 ? stream_kernel<MODE_FUSED, false, true>
               : variant == 2 ? stream_kernel<MODE_FUSED, true>
                              : stream_kernel<MODE_FUSED, false>;
-  static bool attr_done[3] = {false, false, false};
+  const size_t smem = wide ? smem_bytes<32>() : smem_bytes<16>();
+  static bool attr_done[4] = {false, false, false, false};
   if (!attr_done[variant]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+                                         (int)smem);
     if (e != cudaSuccess) return e;
     attr_done[variant] = true;
   }
   const long max_units = (long)a13.max_active * a13.units_per_expert * a13.ksplit +
                          (long)a2.max_active * a2.units_per_expert * a2.ksplit;
-  long grid = (long)CTAS_PER_SM * sm_count;
+  long grid = (long)(wide ? ctas_per_sm<32>() : ctas_per_sm<16>()) * sm_count;
   if (grid > max_units) grid = max_units;
   if (grid <= 0) return cudaSuccess;
   // a programmatic dependent of the sort
-  return launch_kernel(kern, dim3((unsigned)grid), dim3(THREADS), SMEM_BYTES, stream, true, a13,
-                       a2);
+  return launch_kernel(kern, dim3((unsigned)grid), dim3(THREADS), smem, stream, true, a13, a2);
 }
 
 }  // namespace moe
