@@ -149,6 +149,15 @@ bool tcs_supported(const moe_problem_t *p) {
   return p->wfmt == W_MXFP4 && p->afmt == A_BF16 && tc_mx_direct(p) && p->K % 64 == 0 &&
          p->N % 64 == 0 && p->num_local_experts <= 1024;
 }
+// MXFP4 w4a16 prefill batches above kTcStreamMaxPerExpert slots per local
+// expert take the tcgen05 kernels that decode each weight stage once for two
+// 128-slot blocks (moe_tcd.cu) instead of once per block.
+bool tcd_applies(const moe_problem_t *p) {
+  return p->path == MOE_PATH_AUTO && tc_applies(p) && tcs_supported(p) && p->wfmt == W_MXFP4 &&
+         tcd_supported(p->num_local_experts) &&
+         (long)p->M * p->topk > kTcStreamMaxPerExpert * p->num_local_experts;
+}
+
 // Sort block of the tcgen05 weight-streaming kernels: their passes start
 // anywhere in an expert's rows, so 16-row blocks (fewer padding rows to
 // gather) instead of the 128 of the other tcgen05 kernels.
@@ -501,10 +510,12 @@ int run_w2(const moe_problem_t *p, const void *inter, const void *inter_scales,
 // scales), tcgen05 w2 + reduce, bf16 output.
 int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *w13,
                 const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
-                const int32_t *expert_map, char *ws, void *out, cudaStream_t st, bool tcs);
+                const int32_t *expert_map, char *ws, void *out, cudaStream_t st, bool tcs,
+                bool pair);
 // The sort's per-expert tables that the tcgen05 weight-streaming kernels read.
 struct TcsRefs {
   const int32_t *offsets, *counts, *active, *n_active;
+  bool pair;  // the block-pair kernels (moe_tcd.cu) instead of the weight-streaming ones
 };
 int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales, const void *x16,
               const float *x_inv, const moe_weight_t *w13, const float *topk_weights,
@@ -768,8 +779,9 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
   if (tcs || (!streaming && !mx_generic && tc_applies(p) && (!fp4 || tc_records))) {
     if (ws_bytes < make_tc_layout(p, tcs).total) return MOE_ERR_WORKSPACE;
     TimedCall timed;
+    const bool pair = !tcs && tc_records && tcd_applies(p);
     return run_tc_path(p, hidden_bf16, w13, w2, topk_ids, topk_weights, expert_map, ws, out_bf16,
-                       st, tcs);
+                       st, tcs, pair);
   }
   int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
   int32_t *eids = reinterpret_cast<int32_t *>(ws + L.expert_ids);
@@ -1248,7 +1260,9 @@ int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales,
       a.offsets = tcs->offsets; a.counts = tcs->counts;
       a.active = tcs->active; a.n_active = tcs->n_active;
     }
-    rc = cuda_status(tcs    ? launch_tcs_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
+    rc = cuda_status(tcs && tcs->pair
+                         ? launch_tcd_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
+                     : tcs  ? launch_tcs_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
                      : bs   ? launch_bs_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
                      : fp8b ? launch_fp8b_gemm(a, scratch + L.a_sorted, cap, 1, dinfo.sm_count, st)
                             : launch_tc_gemm(a, scratch + L.a_sorted, cap, 1, st));
@@ -1319,7 +1333,8 @@ int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
     a.active = tcs->active; a.n_active = tcs->n_active;
   }
   StageScope sc(MOE_STAGE_W2, st);
-  const int rc = cuda_status(tcs  ? launch_tcs_gemm(a, inter, cap, 0, dinfo.sm_count, st)
+  const int rc = cuda_status(tcs && tcs->pair ? launch_tcd_gemm(a, inter, cap, 0, dinfo.sm_count, st)
+                             : tcs  ? launch_tcs_gemm(a, inter, cap, 0, dinfo.sm_count, st)
                              : bs ? launch_bs_gemm(a, inter, cap, 0, dinfo.sm_count, st)
                              : p->wfmt == W_FP8_BLOCK128
                                  ? launch_fp8b_gemm(a, inter, cap, 0, dinfo.sm_count, st)
@@ -1331,9 +1346,12 @@ int tc_stage2(const moe_problem_t *p, const void *inter, const void *i_scales,
 // The tcgen05 prefill path: sort with 128-row blocks (+ zero the accumulator;
 // MXFP4 weights: + the f16 copy of x), stage-1 quantisation, stage 1, stage 2,
 // bf16 output.
+// tcs: the weight-streaming kernels (16-row sort blocks); pair: the
+// block-pair kernels (128-row blocks); both read the sort's per-expert tables.
 int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *w13,
                 const moe_weight_t *w2, const int32_t *topk_ids, const float *topk_weights,
-                const int32_t *expert_map, char *ws, void *out, cudaStream_t st, bool tcs) {
+                const int32_t *expert_map, char *ws, void *out, cudaStream_t st, bool tcs,
+                bool pair) {
   const TcLayout L = make_tc_layout(p, tcs);
   DeviceInfo dinfo;
   int rc = device_info(&dinfo);
@@ -1349,7 +1367,7 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     ex.zero_buf = acc;
     ex.zero_n = MK;
     ex.num_valid_tokens = p->num_local_tokens;
-    if (tcs) {  // per-expert tables of the weight-streaming kernels
+    if (tcs || pair) {  // per-expert tables of the weight-streaming / block-pair kernels
       ex.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
       ex.active = reinterpret_cast<int32_t *>(ws + L.active);
       ex.n_active = reinterpret_cast<int32_t *>(ws + L.n_active);
@@ -1386,7 +1404,8 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     scales = ws + L.a1_scales;
   }
   TcsRefs tr{};
-  if (tcs) {
+  tr.pair = pair;
+  if (tcs || pair) {
     tr.counts = counts;
     tr.offsets = reinterpret_cast<const int32_t *>(ws + L.offsets);
     tr.active = reinterpret_cast<const int32_t *>(ws + L.active);
@@ -1395,10 +1414,10 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
   if ((rc = tc_stage1(p, codes, scales, L.f16_x ? ws + L.x16 : nullptr,
                       L.f16_x ? reinterpret_cast<const float *>(ws + L.x_inv) : nullptr, w13,
                       topk_weights, sorted, eids, ntp, L.cap, ws + L.scratch, ws + L.inter,
-                      ws + L.i_scales, dinfo, st, tcs ? &tr : nullptr)) != MOE_OK)
+                      ws + L.i_scales, dinfo, st, (tcs || pair) ? &tr : nullptr)) != MOE_OK)
     return rc;
   if ((rc = tc_stage2(p, ws + L.inter, ws + L.i_scales, w2, topk_weights, sorted, eids, ntp,
-                      L.cap, acc, dinfo, st, tcs ? &tr : nullptr)) != MOE_OK)
+                      L.cap, acc, dinfo, st, (tcs || pair) ? &tr : nullptr)) != MOE_OK)
     return rc;
   StageScope sc(MOE_STAGE_FINALIZE, st);
   rc = cuda_status(launch_finalize(acc, MK, out, st));

@@ -247,6 +247,7 @@ struct TcArgs {
   // weight-streaming tcgen05 kernels (moe_tcs.cu): the sort's per-expert
   // sorted-row offsets and slot counts [El], the active-expert list and its length
   const int32_t *offsets, *counts, *active, *n_active;
+  int rec_tiles;         // moe_tcd.cu: 128-row record tiles per expert (launcher)
 };
 struct GatherArgs {
   const int32_t *sorted_ids, *num_post_pad;
@@ -285,6 +286,13 @@ cudaError_t launch_tc_gemm(const TcArgs &a, const void *a_sorted, long cap_rows,
 // operand.  W13 writes the f16 intermediate [cap_rows, N] (a.out); W2 adds
 // the router-weighted rows into a.acc.  Needs a.offsets / counts / active /
 // n_active from the sort and C % 64 == 0.
+// tcgen05 grouped GEMMs of MXFP4 w4a16 prefill batches whose experts hold
+// more than one 128-slot block (moe_tcd.cu): each 256-row weight stage is
+// decoded once for a pair of blocks.  rows_f16 [cap_rows, C]; needs the
+// sort's per-expert tables (128-row blocks) and the TC-packed records.
+bool tcd_supported(int El);
+cudaError_t launch_tcd_gemm(const TcArgs &a, const void *rows_f16, long cap_rows, int w13,
+                            int sm_count, cudaStream_t st);
 int tcs_ntiles(int w13, int N, int K);
 cudaError_t launch_tcs_gemm(const TcArgs &a, const void *rows_f16, long cap_rows, int w13,
                             int sm_count, cudaStream_t st);

@@ -1,0 +1,462 @@
+// moe_tcd.cu -- tcgen05 grouped GEMMs for MXFP4 weights with bf16 activations
+// (w4a16, GptOssMxfp4MoEMethod on the mxfp4.py page; the two GEMM stages of
+// rocm_aiter_fused_experts on page
+// "vllm.model_executor.layers.fused_moe.experts.rocm_aiter_moe") at prefill
+// batches whose experts hold more than one 128-slot block each.
+//
+// The tensor cores multiply f16 operands (kind::f16, fp32 accumulation in
+// Tensor Memory), so the e2m1 weights are decoded to exact f16 (code x 2^e)
+// on the SMs -- ALU work per weight element.  These kernels decode each
+// 256-row weight stage once and multiply it with two 128-slot blocks of the
+// expert (two accumulators of 128 x 256 in Tensor Memory), halving the decode
+// work per FLOP against one block per decoded tile.
+//   unit   (active local expert, pair of its 128-slot blocks, 256 weight rows)
+//   A      the pair's sorted f16 rows (per-token power-of-two scaled x, or the
+//          intermediate), 2-D TMA with the 128-byte swizzle, 16 KB per block
+//   B      two load-time 128-row records (e2m1 codes + e8m0 scales of 64
+//          reduction elements; MOE_LAYOUT_TC) decoded into the swizzled f16
+//          layout, 32 KB
+// One CTA per SM walks units u = blockIdx.x, + gridDim.x, ... (experts in
+// order, their block pairs, the weight tiles fastest: the CTAs working at one
+// time share the pair's rows and the weight records through L2).  Warp roles:
+//   warp 0      TMA producer (A tiles, records) into a 3-stage ring, and L2
+//               prefetches of the unit's next records
+//   warp 1      TMEM owner; lane 0 issues the stage's MMAs (4 per block) and
+//               commits
+//   warps 2-17  decode each stage's records (thread t: row t / 2, 32 elements)
+//               during the main loop; at a unit's end they drain the two
+//               accumulators (lane quarter warp % 4, 64 columns each) and
+//               apply the epilogue: W13 x-scale, bias, SwiGLU-OAI, f16
+//               intermediate; W2 bias, router weight, fp32 red.add
+// Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, stops
+// issuing, lets its copies and MMAs land, frees its Tensor Memory and exits.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <stddef.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+#include "moe_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;                // slot rows per block
+constexpr int BN = 256;                // weight rows per unit
+constexpr int NS = 3;                  // ring stages
+constexpr int STAGE_A = BM * 128;      // 16 KB of f16 rows (64 reduction elements)
+constexpr int STAGE_B = BN * 128;      // 32 KB of decoded f16 weights
+constexpr int REC = 4096 + 128 * 2;    // one 128-row MXFP4 record of a stage
+constexpr int NUM_EPI = 16;
+constexpr int THREADS = (2 + NUM_EPI) * 32;  // 576
+constexpr int TMEM_COLS = 512;         // two accumulators of 256 columns
+constexpr int kMaxActive = 1024;
+constexpr int kPrefetch = 8;           // record stages prefetched into L2 ahead
+constexpr long long kWaitCycles = 4000000000LL;
+constexpr int kErrTimeout = 5;
+
+enum { MODE_W13 = 0, MODE_W2 = 1 };
+
+struct Smem {
+  unsigned char a[NS][2][STAGE_A];
+  unsigned char b[NS][STAGE_B];
+  unsigned char raw[NS][2][REC];
+  // full: the stage's A tiles landed; raw_full: its weight records landed
+  // (the decoders start on those without waiting for A); b_full: decoded
+  uint64_t full[NS], raw_full[NS], empty[NS], b_full[NS];
+  uint64_t acc_full, acc_empty, drain;
+  int unit_pre[kMaxActive + 1];  // units of the active experts before each one
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
+static_assert(offsetof(Smem, b) % 1024 == 0 && offsetof(Smem, raw) % 16 == 0 && REC % 16 == 0,
+              "shared-memory layout alignment");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *err,
+                                              volatile int *abort_flag) {
+  if (*abort_flag) return false;
+  if (!mbar_wait_bounded(bar, parity, kWaitCycles, err)) {
+    record_device_error(err, kErrTimeout);
+    *abort_flag = 1;
+    return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void red_add_v4(float *p, float x, float y, float z, float w) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(x), "f"(y), "f"(z),
+               "f"(w)
+               : "memory");
+}
+
+// Swizzled byte offset of 16-byte chunk c of row n in a tile of 128-byte rows.
+__device__ __forceinline__ uint32_t sw128(int n, int c) {
+  return (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
+}
+
+// NV (8 or 16) consecutive bias values of expert e from row `row` (a
+// multiple of 8), with 16-byte loads (zeros without a bias).
+template <int NV>
+__device__ __forceinline__ void load_bias(const TcArgs &a, int e, long row, float (&o)[NV]) {
+  if (!a.w_bias) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) o[i] = 0.f;
+    return;
+  }
+  const long i0 = (long)e * a.R + row;
+  if (a.bias_f32) {
+    const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(a.w_bias) + i0);
+#pragma unroll
+    for (int v = 0; v < NV / 4; ++v) {
+      const float4 f = p[v];
+      o[4 * v] = f.x; o[4 * v + 1] = f.y; o[4 * v + 2] = f.z; o[4 * v + 3] = f.w;
+    }
+  } else {
+    const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.w_bias) + i0);
+#pragma unroll
+    for (int v = 0; v < NV / 8; ++v) {
+      const uint4 u = p[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        o[8 * v + 2 * k] = __uint_as_float(w[k] << 16);
+        o[8 * v + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+      }
+    }
+  }
+}
+
+struct Unit {
+  int e, blk0, nblk, nt, nrec;  // expert, first block, blocks (1 or 2), weight tile, records
+};
+
+// This CTA's units in the same order in every role.
+struct Walker {
+  const TcArgs *a;
+  const int *pre;
+  int n_act;
+  long u, total;
+  __device__ Walker(const TcArgs &args, const int *pre_, int n_act_)
+      : a(&args), pre(pre_), n_act(n_act_), u(blockIdx.x), total(pre_[n_act_]) {}
+  __device__ bool get(Unit &un) const {
+    if (u >= total) return false;
+    int lo = 0, hi = n_act - 1;  // the active expert whose range holds u
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    const int e = a->active[lo];
+    const int nb = (a->counts[e] + BM - 1) / BM;
+    const long local = u - pre[lo];
+    const int p = (int)(local / a->ntiles);
+    un.e = e;
+    un.nt = (int)(local % a->ntiles);
+    un.blk0 = a->offsets[e] / BM + 2 * p;
+    un.nblk = min(2, nb - 2 * p);
+    un.nrec = min(2, a->rec_tiles - 2 * un.nt);
+    return true;
+  }
+  __device__ void next() { u += gridDim.x; }
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KT = a.C / 64;  // the caller guarantees C % 64 == 0
+  const int n_act = *a.n_active;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.raw_full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.b_full[s], NUM_EPI);
+    }
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.acc_empty, NUM_EPI);
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    mbar_fence_init();
+  }
+  // units before each active expert (block pairs x weight tiles), by warp 0
+  if (warp == 0) {
+    const int chunk = (n_act + 31) / 32;
+    const int i0 = lane * chunk;
+    int local = 0;
+    for (int i = i0; i < i0 + chunk && i < n_act; ++i)
+      local += (((a.counts[a.active[i]] + BM - 1) / BM + 1) / 2) * a.ntiles;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int i = i0; i < i0 + chunk && i < n_act; ++i) {
+      sm.unit_pre[i] = run;
+      run += (((a.counts[a.active[i]] + BM - 1) / BM + 1) / 2) * a.ntiles;
+    }
+    if (lane == 31) sm.unit_pre[n_act] = incl;
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int *abort_flag = &sm.abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      long g = 0;
+      Walker wk(a, sm.unit_pre, n_act);
+      Unit un;
+      while (!*abort_flag && wk.get(un)) {
+        const unsigned char *rec0 = static_cast<const unsigned char *>(a.w_packed) +
+                                    ((long)un.e * a.rec_tiles + 2 * un.nt) * KT * (long)REC;
+        const long rec_stride = (long)KT * REC;  // the second record tile
+        for (int kt = 0; kt < KT; ++kt, ++g) {
+          if (kt + kPrefetch < KT)
+            for (int r = 0; r < un.nrec; ++r)
+              prefetch_l2_bulk(rec0 + r * rec_stride + (long)(kt + kPrefetch) * REC, (uint32_t)REC);
+          const int s = (int)(g % NS);
+          if (!wait_or_abort(&sm.empty[s], (uint32_t)(((g / NS) & 1) ^ 1), a.err, abort_flag))
+            break;
+          mbar_arrive_expect_tx(&sm.raw_full[s], (uint32_t)(un.nrec * REC));
+          for (int r = 0; r < un.nrec; ++r)
+            tma_bulk_g2s(sm.raw[s][r], rec0 + r * rec_stride + (long)kt * REC, (uint32_t)REC,
+                         &sm.raw_full[s]);
+          mbar_arrive_expect_tx(&sm.full[s], (uint32_t)(un.nblk * STAGE_A));
+          for (int b = 0; b < un.nblk; ++b)
+            tma_load_2d(sm.a[s][b], &tmA, kt * 64, (un.blk0 + b) * BM, &sm.full[s]);
+        }
+        wk.next();
+      }
+      if (*abort_flag)  // let the copies already issued land before the CTA exits
+        for (long k = g > NS ? g - NS : 0; k < g; ++k) {
+          mbar_wait_bounded(&sm.raw_full[k % NS], (uint32_t)((k / NS) & 1), kWaitCycles);
+          mbar_wait_bounded(&sm.full[k % NS], (uint32_t)((k / NS) & 1), kWaitCycles);
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      long g = 0, tc = 0;
+      Walker wk(a, sm.unit_pre, n_act);
+      Unit un;
+      while (!*abort_flag && wk.get(un)) {
+        // the epilogue has drained the previous unit's accumulators
+        if (!wait_or_abort(&sm.acc_empty, (uint32_t)((tc & 1) ^ 1), a.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t idesc = umma_idesc_f16(BM, un.nrec * 128);
+        for (int kt = 0; kt < KT; ++kt, ++g) {
+          const int s = (int)(g % NS);
+          const uint32_t par = (uint32_t)((g / NS) & 1);
+          if (!wait_or_abort(&sm.full[s], par, a.err, abort_flag)) break;
+          if (!wait_or_abort(&sm.b_full[s], par, a.err, abort_flag)) break;
+          tc_fence_after();
+          const uint64_t bd = umma_desc_sw128(smem_addr(sm.b[s]));
+          for (int b = 0; b < un.nblk; ++b) {
+            const uint64_t ad = umma_desc_sw128(smem_addr(sm.a[s][b]));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)  // 16 reduction elements (32 bytes) each
+              umma_f16(tmem + (uint32_t)(b * BN), ad + 2 * j, bd + 2 * j, idesc,
+                       (kt == 0 && j == 0) ? 0u : 1u);
+          }
+          umma_commit(&sm.empty[s]);
+        }
+        if (*abort_flag) break;
+        umma_commit(&sm.acc_full);
+        ++tc;
+        wk.next();
+      }
+      // every MMA issued above has completed before Tensor Memory is freed
+      umma_commit(&sm.drain);
+      mbar_wait_bounded(&sm.drain, 0, kWaitCycles);
+    }
+  } else {
+    // ------------------------------------------- decoders, then the epilogue
+    const int t = threadIdx.x - 64;      // 0..511
+    const int n = t >> 1, h = t & 1;     // decoded row, 32-element half
+    const int rec = n >> 7, rn = n & 127;
+    const int q = warp & 3;              // TMEM lane quarter
+    const int cq = (warp - 2) >> 2;      // 64-column quarter of the 256 columns
+    long g = 0, tc = 0;
+    Walker wk(a, sm.unit_pre, n_act);
+    Unit un;
+    while (!*abort_flag && wk.get(un)) {
+      for (int kt = 0; kt < KT; ++kt, ++g) {
+        const int s = (int)(g % NS);
+        if (!wait_or_abort(&sm.raw_full[s], (uint32_t)((g / NS) & 1), a.err, abort_flag)) break;
+        if (rec < un.nrec) {
+          const unsigned char *rp = sm.raw[s][rec];
+          const uint4 cw = *reinterpret_cast<const uint4 *>(rp + rn * 32 + h * 16);
+          const uint32_t sc = rp[4096 + rn * 2 + h];
+          // 2^(sc - 127) as an f16x2 pair; exact: TC-packed records exist only
+          // for scale codes in [106, 140] (range-checked at load time)
+          const uint32_t sh = sc >= 113 ? (sc - 112) << 10 : 1u << (sc - 103);
+          const uint32_t f = sh | (sh << 16);
+          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t hv[4];
+            e2m1x8_to_f16x2x4(words[u], hv);
+            uint4 o;
+            o.x = hmul2_u32(hv[0], f);
+            o.y = hmul2_u32(hv[1], f);
+            o.z = hmul2_u32(hv[2], f);
+            o.w = hmul2_u32(hv[3], f);
+            *reinterpret_cast<uint4 *>(sm.b[s] + sw128(n, 4 * h + u)) = o;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.b_full[s]);
+      }
+      if (*abort_flag) break;
+
+      // ---------------------------------------------------------- epilogue
+      if (!wait_or_abort(&sm.acc_full, (uint32_t)(tc & 1), a.err, abort_flag)) break;
+      tc_fence_after();
+      const int r_rec = 2 * un.nt + (cq >> 1);  // record tile of this thread's columns
+      const bool col_live = (cq >> 1) < un.nrec;
+      for (int b = 0; b < un.nblk; ++b) {
+        const long r = (long)(un.blk0 + b) * BM + q * 32 + lane;  // sorted row
+        float acc[64];
+        {
+          const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + cq * 64);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            float v[16];
+            tmem_ld_32x32b_x16(taddr + 16 * p, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[16 * p + i] = v[i];
+          }
+        }
+        const int s_id = a.sorted_ids[r];
+        const bool live = s_id < a.S && col_live;
+        if (MODE == MODE_W13) {
+          const int jbase = r_rec * 64 + 32 * (cq & 1);
+          if (live && jbase < a.N) {  // N % 32 == 0: the 32 outputs all in range or none
+            const bool sep = a.gate == GATE_SEPARATED;
+            const float rf = a.a_rowscale[r];
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + r * a.N + jbase);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {  // 8 outputs per pass
+              // the pass's gate and up biases: SEPARATED rows j and N + j,
+              // INTERLEAVED rows 2j, 2j + 1 (16 consecutive)
+              const long j0 = jbase + 8 * p;
+              float bg[8], bu[8];
+              if (sep) {
+                load_bias<8>(a, un.e, j0, bg);
+                load_bias<8>(a, un.e, (long)a.N + j0, bu);
+              } else {
+                float b[16];
+                load_bias<16>(a, un.e, 2 * j0, b);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  bg[i] = b[2 * i];
+                  bu[i] = b[2 * i + 1];
+                }
+              }
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 8; i += 2) {
+                float z2[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  const int ii = 8 * p + i + k;
+                  const float gacc = sep ? acc[ii] : acc[2 * ii];
+                  const float uacc = sep ? acc[32 + ii] : acc[2 * ii + 1];
+                  z2[k] = act_and_mul(a.act, gacc * rf + bg[i + k], uacc * rf + bu[i + k],
+                                      a.alpha, a.beta, a.limit);
+                }
+                const __half2 h2 = __floats2half2_rn(z2[0], z2[1]);
+                w[i >> 1] = *reinterpret_cast<const uint32_t *>(&h2);
+              }
+              dst[p] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        } else if (live) {
+          const long tok = s_id / a.T;
+          const float wt = a.w_stage1 ? 1.f : a.topk_weights[s_id];
+          const long k0 = (long)r_rec * 128 + 64 * (cq & 1);
+          float *dst = a.acc + tok * a.K + k0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // 16 outputs per chunk (K % 16 == 0)
+            if (k0 + 16 * c >= a.K) break;
+            float b[16];
+            load_bias<16>(a, un.e, k0 + 16 * c, b);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              red_add_v4(dst + 16 * c + 4 * i, wt * (acc[16 * c + 4 * i] + b[4 * i]),
+                         wt * (acc[16 * c + 4 * i + 1] + b[4 * i + 1]),
+                         wt * (acc[16 * c + 4 * i + 2] + b[4 * i + 2]),
+                         wt * (acc[16 * c + 4 * i + 3] + b[4 * i + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_empty);  // the next unit's MMAs may start
+      ++tc;
+      wk.next();
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_tcd_t(const CUtensorMap &ta, const TcArgs &a, int grid, cudaStream_t st) {
+  static int attr_dev[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_dev[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tcd_gemm_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_dev[dev] = 1;
+  }
+  tcd_gemm_kernel<MODE><<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(ta, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// 2-D K-major 16-bit tensor map with the 128-byte swizzle (moe_tc.cu).
+bool make_tc_map_b16(CUtensorMap *tm, const void *base, long rows, long cols, int box_rows);
+
+bool tcd_supported(int El) { return El <= kMaxActive; }
+
+cudaError_t launch_tcd_gemm(const TcArgs &a_in, const void *rows_f16, long cap_rows, int w13,
+                            int sm_count, cudaStream_t st) {
+  TcArgs a = a_in;
+  a.rec_tiles = tc_ntiles(w13, a.N, a.K);          // 128-row record tiles
+  a.ntiles = (a.rec_tiles + 1) / 2;                 // 256-row units
+  if (cap_rows <= 0) return cudaSuccess;
+  if (a.C % 64 != 0 || !a.active || !a.offsets || !a.counts || !a.n_active || !a.w_packed ||
+      a.El > kMaxActive)
+    return cudaErrorInvalidValue;
+  CUtensorMap ta;
+  if (!make_tc_map_b16(&ta, rows_f16, cap_rows, a.C, BM)) return cudaErrorInvalidValue;
+  return w13 ? launch_tcd_t<MODE_W13>(ta, a, sm_count, st)
+             : launch_tcd_t<MODE_W2>(ta, a, sm_count, st);
+}
+
+}  // namespace moe
