@@ -19,8 +19,9 @@
 // One CTA per SM walks units u = blockIdx.x, + gridDim.x, ... (experts in
 // order, their block pairs, the weight tiles fastest: the CTAs working at one
 // time share the pair's rows and the weight records through L2).  Warp roles:
-//   warp 0      TMA producer (A tiles, records) into a 3-stage ring, and L2
-//               prefetches of the unit's next records
+//   warp 0      lane 0: TMA producer (A tiles, records) into a 3-stage ring,
+//               and L2 prefetches of the unit's next records; lanes 1-31
+//               stage each unit's 256 biases in shared memory (two buffers)
 //   warp 1      TMEM owner; lane 0 issues the stage's MMAs (4 per block) and
 //               commits
 //   warps 2-17  decode each stage's records (thread t: row t / 2, 32 elements)
@@ -66,13 +67,19 @@ struct Smem {
   // (the decoders start on those without waiting for A); b_full: decoded
   uint64_t full[NS], raw_full[NS], empty[NS], b_full[NS];
   uint64_t acc_full, acc_empty, drain;
+  // the unit's biases, staged by the producer warp's lanes 1-31: W13 (gate,
+  // up) of its 128 outputs, W2 its 256 output rows; double-buffered by unit
+  alignas(16) float bias[2][256];
+  uint64_t bias_full[2], bias_empty[2];
   int unit_pre[kMaxActive + 1];  // units of the active experts before each one
   uint32_t tmem_base;
   int abort_flag;
 };
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
-static_assert(offsetof(Smem, b) % 1024 == 0 && offsetof(Smem, raw) % 16 == 0 && REC % 16 == 0,
+static_assert(offsetof(Smem, b) % 1024 == 0 && offsetof(Smem, raw) % 16 == 0 && REC % 16 == 0 &&
+                  offsetof(Smem, bias) % 16 == 0,
               "shared-memory layout alignment");
+constexpr int kBiasLanes = 31;  // producer-warp lanes 1-31
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *err,
@@ -97,36 +104,22 @@ __device__ __forceinline__ uint32_t sw128(int n, int c) {
   return (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
 }
 
-// NV (8 or 16) consecutive bias values of expert e from row `row` (a
-// multiple of 8), with 16-byte loads (zeros without a bias).
-template <int NV>
-__device__ __forceinline__ void load_bias(const TcArgs &a, int e, long row, float (&o)[NV]) {
-  if (!a.w_bias) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i) o[i] = 0.f;
-    return;
+// Activation of one (gate, up) pair with the fast exponential and divide
+// intrinsics (a few fp32 ulps, far below the f16 intermediate's step).
+__device__ __forceinline__ float act_fast(int act, float g, float u, float alpha, float beta,
+                                          float limit) {
+  if (act == ACT_SILU) return __fdividef(g, 1.0f + __expf(-g)) * u;
+  if (act == ACT_GELU) return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f)) * u;
+  if (limit > 0.0f) {
+    g = fminf(g, limit);
+    u = fminf(fmaxf(u, -limit), limit);
   }
-  const long i0 = (long)e * a.R + row;
-  if (a.bias_f32) {
-    const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(a.w_bias) + i0);
-#pragma unroll
-    for (int v = 0; v < NV / 4; ++v) {
-      const float4 f = p[v];
-      o[4 * v] = f.x; o[4 * v + 1] = f.y; o[4 * v + 2] = f.z; o[4 * v + 3] = f.w;
-    }
-  } else {
-    const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.w_bias) + i0);
-#pragma unroll
-    for (int v = 0; v < NV / 8; ++v) {
-      const uint4 u = p[v];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        o[8 * v + 2 * k] = __uint_as_float(w[k] << 16);
-        o[8 * v + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-      }
-    }
-  }
+  return (u + beta) * __fdividef(g, 1.0f + __expf(-alpha * g));
+}
+
+__device__ __forceinline__ float bias_value(const TcArgs &a, long i) {
+  return a.bias_f32 ? static_cast<const float *>(a.w_bias)[i]
+                    : bf16_to_f32(static_cast<const uint16_t *>(a.w_bias)[i]);
 }
 
 struct Unit {
@@ -182,6 +175,10 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_empty, NUM_EPI);
     mbar_init(&sm.drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.bias_full[b], kBiasLanes);
+      mbar_init(&sm.bias_empty[b], NUM_EPI);
+    }
     sm.abort_flag = 0;
     mbar_fence_init();
   }
@@ -247,6 +244,37 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
           mbar_wait_bounded(&sm.raw_full[k % NS], (uint32_t)((k / NS) & 1), kWaitCycles);
           mbar_wait_bounded(&sm.full[k % NS], (uint32_t)((k / NS) & 1), kWaitCycles);
         }
+    } else {
+      // lanes 1-31: the biases of each unit, into buffer (unit index % 2)
+      long tc = 0;
+      Walker wk(a, sm.unit_pre, n_act);
+      Unit un;
+      while (!*abort_flag && wk.get(un)) {
+        const int buf = (int)(tc & 1);
+        if (!wait_or_abort(&sm.bias_empty[buf], (uint32_t)(((tc >> 1) & 1) ^ 1), a.err,
+                           abort_flag))
+          break;
+        const long b0 = (long)un.e * a.R;
+        for (int i = lane - 1; i < 256; i += kBiasLanes) {
+          float v = 0.f;
+          const int rr = i >> 7;  // record (128 columns) of this value
+          if (a.w_bias && rr < un.nrec) {
+            if (MODE == MODE_W13) {  // (gate, up) of output (2 nt + rr) 64 + (i % 128) / 2
+              const long j = (long)(2 * un.nt + rr) * 64 + ((i & 127) >> 1);
+              const bool up = (i & 1) != 0;
+              const long row = a.gate == GATE_SEPARATED ? (up ? (long)a.N + j : j) : 2 * j + up;
+              if (j < a.N) v = bias_value(a, b0 + row);
+            } else {  // output row (2 nt + rr) 128 + i % 128
+              const long k = (long)(2 * un.nt + rr) * 128 + (i & 127);
+              if (k < a.R) v = bias_value(a, b0 + k);
+            }
+          }
+          sm.bias[buf][i] = v;
+        }
+        mbar_arrive(&sm.bias_full[buf]);
+        ++tc;
+        wk.next();
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -330,6 +358,9 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
       tc_fence_after();
       const int r_rec = 2 * un.nt + (cq >> 1);  // record tile of this thread's columns
       const bool col_live = (cq >> 1) < un.nrec;
+      const int bbuf = (int)(tc & 1);
+      if (!wait_or_abort(&sm.bias_full[bbuf], (uint32_t)((tc >> 1) & 1), a.err, abort_flag)) break;
+      const float *bias_s = sm.bias[bbuf];
       for (int b = 0; b < un.nblk; ++b) {
         const long r = (long)(un.blk0 + b) * BM + q * 32 + lane;  // sorted row
         float acc[64];
@@ -353,21 +384,14 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
             uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + r * a.N + jbase);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {  // 8 outputs per pass
-              // the pass's gate and up biases: SEPARATED rows j and N + j,
-              // INTERLEAVED rows 2j, 2j + 1 (16 consecutive)
-              const long j0 = jbase + 8 * p;
-              float bg[8], bu[8];
-              if (sep) {
-                load_bias<8>(a, un.e, j0, bg);
-                load_bias<8>(a, un.e, (long)a.N + j0, bu);
-              } else {
-                float b[16];
-                load_bias<16>(a, un.e, 2 * j0, b);
+              // the staged (gate, up) biases of these 8 outputs
+              const float4 *bp = reinterpret_cast<const float4 *>(
+                  bias_s + 2 * (64 * (cq >> 1) + 32 * (cq & 1) + 8 * p));
+              float bgu[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  bg[i] = b[2 * i];
-                  bu[i] = b[2 * i + 1];
-                }
+              for (int v = 0; v < 4; ++v) {
+                const float4 f = bp[v];
+                bgu[4 * v] = f.x; bgu[4 * v + 1] = f.y; bgu[4 * v + 2] = f.z; bgu[4 * v + 3] = f.w;
               }
               uint32_t w[4];
 #pragma unroll
@@ -378,8 +402,8 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
                   const int ii = 8 * p + i + k;
                   const float gacc = sep ? acc[ii] : acc[2 * ii];
                   const float uacc = sep ? acc[32 + ii] : acc[2 * ii + 1];
-                  z2[k] = act_and_mul(a.act, gacc * rf + bg[i + k], uacc * rf + bu[i + k],
-                                      a.alpha, a.beta, a.limit);
+                  z2[k] = act_fast(a.act, gacc * rf + bgu[2 * (i + k)],
+                                   uacc * rf + bgu[2 * (i + k) + 1], a.alpha, a.beta, a.limit);
                 }
                 const __half2 h2 = __floats2half2_rn(z2[0], z2[1]);
                 w[i >> 1] = *reinterpret_cast<const uint32_t *>(&h2);
@@ -396,7 +420,13 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
           for (int c = 0; c < 4; ++c) {  // 16 outputs per chunk (K % 16 == 0)
             if (k0 + 16 * c >= a.K) break;
             float b[16];
-            load_bias<16>(a, un.e, k0 + 16 * c, b);
+            const float4 *bp =
+                reinterpret_cast<const float4 *>(bias_s + 128 * (cq >> 1) + 64 * (cq & 1) + 16 * c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const float4 f = bp[v];
+              b[4 * v] = f.x; b[4 * v + 1] = f.y; b[4 * v + 2] = f.z; b[4 * v + 3] = f.w;
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               red_add_v4(dst + 16 * c + 4 * i, wt * (acc[16 * c + 4 * i] + b[4 * i]),
@@ -408,7 +438,10 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.acc_empty);  // the next unit's MMAs may start
+      if (lane == 0) {
+        mbar_arrive(&sm.acc_empty);  // the next unit's MMAs may start
+        mbar_arrive(&sm.bias_empty[bbuf]);
+      }
       ++tc;
       wk.next();
     }

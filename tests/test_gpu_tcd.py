@@ -46,9 +46,13 @@ def test_block_pairs_match_oracle(case):
     torch.cuda.synchronize()
     err, tol, rms = compare(wl, out, ref, tok)
     assert err <= tol, f"{wl.name}: max|err| {err:.4e} > tol {tol:.4e} (rms {rms:.4e})"
-    # the 128-row tcgen05 kernels agree up to the order of the fp32 sums
+    # the 128-row tcgen05 kernels agree up to the order of the fp32 sums and
+    # the last fp32 bits of the activation (fast exponential here), which can
+    # move an f16 intermediate and then a bf16 output by one rounding step
     tc = moe.FusedExperts.from_workload(wl, path="tc")(wl.x, wl.topk_ids, wl.topk_weights,
                                                         wl.expert_map)
     torch.cuda.synchronize()
-    assert (out.float() - tc.float()).abs().max().item() <= 1e-2 * rms
+    diff = (out.float() - tc.float()).abs()
+    bound = 1e-2 * rms + tc.float().abs() * 2.0**-7  # one bf16 step of the value
+    assert bool((diff <= bound).all()), f"max cross-path diff {diff.max().item():.4e}"
     assert moe.moe_get_device_error() == 0
