@@ -28,7 +28,14 @@
 //               quantises the row's 128 outputs (one 1 x 128 group, its
 //               maximum gathered from the four threads that hold it) into
 //               e4m3 codes + an fp32 scale (W13), or multiplies the router
-//               weight and adds into the fp32 token accumulator (W2)
+//               weight and adds into the fp32 token accumulator (W2): each
+//               warp transposes its 32 rows through shared memory 16 columns
+//               at a time, so that one red.add instruction covers 8 rows x 64
+//               contiguous bytes instead of 32 rows x 16 bytes
+//   warp 18     each stage's scales (the 128 rows' activation-group scales and
+//               the block scales of the eight 32-row weight groups) into a
+//               shared-memory ring, ahead of the MMAs, so that the epilogue
+//               reads no scale from global memory
 // Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, stops
 // issuing, lets its copies and MMAs land, frees its Tensor Memory and exits.
 #include <cuda.h>
@@ -46,33 +53,54 @@ namespace {
 constexpr int BM = kTcBlockM;  // 128 sorted rows
 constexpr int BN = 256;        // weight rows per tile
 constexpr int BK = 128;        // reduction elements (= bytes) per stage: one scale block
-constexpr int NS = 4;          // stages in the ring
+// stages in the ring: W2 keeps one fewer to make room for its transposition
+// buffers
+template <int MODE> constexpr int ring_stages() { return MODE == 0 ? 4 : 3; }
+constexpr int NSC = 8;         // stages in the scale ring
+constexpr int SC_FLOATS = 136; // per scale stage: 128 rows + 8 weight groups
 constexpr int STAGE_A = BM * BK;                   // 16 KB
 constexpr int STAGE_B = BN * BK;                   // 32 KB
 constexpr int NUM_EPI = 16;
-constexpr int THREADS = (2 + NUM_EPI) * 32;        // 576
+constexpr int SCALE_WARP = 2 + NUM_EPI;             // 18
+constexpr int THREADS = (3 + NUM_EPI) * 32;        // 608
 constexpr int TMEM_COLS = 512;                     // two promotion buffers of 256 columns
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr int kErrTimeout = 5;
 constexpr int kRasterGroup = 8;
 
+
 enum { MODE_W13 = 0, MODE_W2 = 1 };
 
+template <int MODE>
 struct Smem {
+  static constexpr int NS = ring_stages<MODE>();
   unsigned char a[NS][STAGE_A];
   unsigned char b[NS][STAGE_B];
   uint64_t full[NS], empty[NS];
   uint64_t acc_full[2], acc_empty[2], drain;
+  // scale ring: [0, 128) the rows' activation-group scales of the stage's
+  // block, [128, 136) the block scales of weight group c (32 rows) = 0..7
+  alignas(16) float sc[NSC][SC_FLOATS];
+  uint64_t sc_full[NSC], sc_empty[NSC];
   // W13: the per-thread maxima of a row's 1 x 128 group (four threads hold
   // it), double-buffered by tile
-  alignas(16) float amax_stage[2][BM][4];
+  alignas(16) float amax_stage[MODE == 0 ? 2 : 1][BM][4];
+  // W2: per epilogue warp, 32 rows x 16 columns of outputs, each row's four
+  // 16-byte units stored at unit (u ^ ((row >> 1) & 3)) (conflict-free both
+  // ways)
+  alignas(16) float xpose[MODE == 0 ? 1 : NUM_EPI][32 * 16];
   uint64_t staged[2], freed[2];
   uint32_t tmem_base;
   int abort_flag;
 };
-constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
-static_assert(offsetof(Smem, b) % 1024 == 0 && offsetof(Smem, amax_stage) % 16 == 0,
+template <int MODE> constexpr size_t smem_bytes() { return sizeof(Smem<MODE>) + 1024; }
+static_assert(offsetof(Smem<0>, b) % 1024 == 0 && offsetof(Smem<1>, b) % 1024 == 0 &&
+                  offsetof(Smem<0>, sc) % 16 == 0 && offsetof(Smem<1>, sc) % 16 == 0 &&
+                  offsetof(Smem<0>, amax_stage) % 16 == 0 && offsetof(Smem<1>, xpose) % 16 == 0 &&
+                  (SC_FLOATS * 4) % 16 == 0,
               "shared-memory layout alignment");
+static_assert(smem_bytes<0>() <= 227 * 1024 && smem_bytes<1>() <= 227 * 1024,
+              "shared memory per CTA");
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, int *err,
                                               volatile int *abort_flag) {
@@ -83,6 +111,28 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, in
     return false;
   }
   return true;
+}
+
+// Activation of one (gate, up) pair with the fast exponential and divide
+// intrinsics (a few fp32 ulps, far below the e4m3 intermediate's step).
+__device__ __forceinline__ float act_fast(int act, float g, float u, float alpha, float beta,
+                                          float limit) {
+  if (act == ACT_SILU) return __fdividef(g, 1.0f + __expf(-g)) * u;
+  if (act == ACT_GELU) return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f)) * u;
+  if (limit > 0.0f) {
+    g = fminf(g, limit);
+    u = fminf(fmaxf(u, -limit), limit);
+  }
+  return (u + beta) * __fdividef(g, 1.0f + __expf(-alpha * g));
+}
+
+// An epilogue wait whose outcome is the same on every lane of the warp (the
+// warp then leaves its loops together: its shuffles and warp barriers never
+// wait for a lane that has left).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *err,
+                                          volatile int *abort_flag) {
+  const bool ok = wait_or_abort(bar, parity, err, abort_flag);
+  return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ void red_add_v4(float *p, float x, float y, float z, float w) {
@@ -116,9 +166,10 @@ template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const TcArgs a) {
+  constexpr int NS = ring_stages<MODE>();
   extern __shared__ unsigned char smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                       ~uintptr_t(1023));
+  Smem<MODE> &sm = *reinterpret_cast<Smem<MODE> *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KT = (int)ceil_div(a.C, BK);
   const long ntiles_total = a.nblocks * a.ntiles;
@@ -127,6 +178,10 @@ fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     for (int s = 0; s < NS; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
+    }
+    for (int s = 0; s < NSC; ++s) {
+      mbar_init(&sm.sc_full[s], 32);
+      mbar_init(&sm.sc_empty[s], NUM_EPI);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.acc_full[b], 1);
@@ -206,13 +261,42 @@ fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       umma_commit(&sm.drain);
       mbar_wait_bounded(&sm.drain, 0, kWaitCycles);
     }
+  } else if (warp == SCALE_WARP) {
+    // ------------------------------------------------------------ scale ring
+    {  // one entry per stage, in the MMAs' order
+      const float *ws = static_cast<const float *>(a.w_scales);
+      const long RB = ceil_div(a.R, 128), CB = KT;
+      long g = 0;
+      for (long t = blockIdx.x; t < ntiles_total && !*abort_flag; t += gridDim.x) {
+        int blk, nt;
+        tile_coords(t, a.nblocks, a.ntiles, blk, nt);
+        if ((long)blk * BM >= ntp) continue;
+        const int e = a.expert_ids[blk];
+        if (e < 0 || e >= a.El) continue;
+        const float *sa = a.a_groupscale + (long)blk * BM * a.a_groups;
+        // the lanes 0-7 each own one weight group's block-scale row (none
+        // past the weight's R rows); a 32-row group never crosses a block
+        const float *swc = nullptr;
+        if (lane < 8) {
+          const long wr = group_row<MODE>(a, nt, lane);
+          if (wr < a.R) swc = ws + ((long)e * RB + wr / 128) * CB;
+        }
+        for (int kt = 0; kt < KT; ++kt, ++g) {
+          const int s = (int)(g % NSC);
+          if (!wait_or_abort(&sm.sc_empty[s], (uint32_t)(((g / NSC) & 1) ^ 1), a.err, abort_flag))
+            break;
+#pragma unroll
+          for (int i = lane; i < BM; i += 32) sm.sc[s][i] = sa[(long)i * a.a_groups + kt];
+          if (lane < 8) sm.sc[s][BM + lane] = swc ? swc[kt] : 0.f;
+          mbar_arrive(&sm.sc_full[s]);
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;           // TMEM lane quarter of this warp
     const int cq = (warp - 2) >> 2;   // tile columns [64 cq, 64 cq + 64)
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + 64 * cq;
-    const float *ws = static_cast<const float *>(a.w_scales);
-    const long RB = ceil_div(a.R, 128), CB = KT;
     const bool sep = MODE == MODE_W13 && a.gate == GATE_SEPARATED;
     long g = 0, etile = 0;
     bool ok = true;
@@ -225,24 +309,23 @@ fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       const long r = (long)blk * BM + q * 32 + lane;
       const int s_id = a.sorted_ids[r];
       const bool live = s_id < a.S;
-      // weight scale rows of this thread's two 32-column halves (block of
-      // 128 weight rows; a 32-row group never crosses a block boundary)
-      const long wr0 = group_row<MODE>(a, nt, 2 * cq), wr1 = group_row<MODE>(a, nt, 2 * cq + 1);
-      const float *sw0 = wr0 < a.R ? ws + ((long)e * RB + wr0 / 128) * CB : nullptr;
-      const float *sw1 = wr1 < a.R ? ws + ((long)e * RB + wr1 / 128) * CB : nullptr;
-      const float *sa = a.a_groupscale + r * a.a_groups;
       float acc[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-      float fa = live ? sa[0] : 0.f;
-      float f0 = sw0 ? fa * sw0[0] : 0.f, f1 = sw1 ? fa * sw1[0] : 0.f;
       for (int kt = 0; kt < KT; ++kt, ++g) {
         const int b = (int)(g & 1);
-        // the next block's scales are loaded while this one is folded
-        const float fa_n = (live && kt + 1 < KT) ? sa[kt + 1] : 0.f;
-        const float f0_n = (sw0 && kt + 1 < KT) ? fa_n * sw0[kt + 1] : 0.f;
-        const float f1_n = (sw1 && kt + 1 < KT) ? fa_n * sw1[kt + 1] : 0.f;
-        if (!wait_or_abort(&sm.acc_full[b], (uint32_t)((g >> 1) & 1), a.err, abort_flag)) {
+        // this block's scales from the ring: the row's activation-group
+        // scale times the block scales of this thread's two weight groups
+        const int s = (int)(g % NSC);
+        if (!warp_wait(&sm.sc_full[s], (uint32_t)((g / NSC) & 1), a.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const float fa = live ? sm.sc[s][q * 32 + lane] : 0.f;
+        const float f0 = fa * sm.sc[s][BM + 2 * cq], f1 = fa * sm.sc[s][BM + 2 * cq + 1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sc_empty[s]);
+        if (!warp_wait(&sm.acc_full[b], (uint32_t)((g >> 1) & 1), a.err, abort_flag)) {
           ok = false;
           break;
         }
@@ -259,8 +342,6 @@ fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.acc_empty[b]);  // the tensor cores may refill it
-        f0 = f0_n;
-        f1 = f1_n;
       }
       if (!ok) break;
       auto bias_of = [&](long wrow) -> float {
@@ -269,7 +350,7 @@ fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         return a.bias_f32 ? static_cast<const float *>(a.w_bias)[i]
                           : bf16_to_f32(static_cast<const uint16_t *>(a.w_bias)[i]);
       };
-      if (MODE == MODE_W13) {
+      if constexpr (MODE == MODE_W13) {
         // outputs jbase .. jbase + 31 of the row: SEPARATED -> gate acc[i],
         // up acc[32 + i]; INTERLEAVED -> gate acc[2 i], up acc[2 i + 1]
         const int jbase = nt * 128 + 32 * cq;
@@ -283,18 +364,18 @@ fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           const long grow = sep ? j : 2 * j, urow = sep ? a.N + j : 2 * j + 1;
           const float gv = (sep ? acc[i] : acc[2 * i]) + (in ? bias_of(grow) : 0.f);
           const float uv = (sep ? acc[32 + i] : acc[2 * i + 1]) + (in ? bias_of(urow) : 0.f);
-          z[i] = (live && in) ? zw * act_and_mul(a.act, gv, uv, a.alpha, a.beta, a.limit) : 0.f;
+          z[i] = (live && in) ? zw * act_fast(a.act, gv, uv, a.alpha, a.beta, a.limit) : 0.f;
           amax = fmaxf(amax, fabsf(z[i]));
         }
         // the row's 1 x 128 group maximum from its four threads
         const int sb = (int)(etile & 1);
         const uint32_t sph = (uint32_t)((etile >> 1) & 1);
-        ok = mbar_wait_bounded(&sm.freed[sb], sph ^ 1, kWaitCycles, a.err);
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sm.freed[sb], sph ^ 1, kWaitCycles, a.err));
         if (ok) {
           sm.amax_stage[sb][q * 32 + lane][cq] = amax;
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.staged[sb]);
-          ok = mbar_wait_bounded(&sm.staged[sb], sph, kWaitCycles, a.err);
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sm.staged[sb], sph, kWaitCycles, a.err));
         }
         if (ok) {
           const float4 m4 = *reinterpret_cast<const float4 *>(&sm.amax_stage[sb][q * 32 + lane][0]);
@@ -318,18 +399,41 @@ fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           *abort_flag = 1;
         }
         ++etile;
-      } else if (live) {
-        const long tok = s_id / a.T;
-        const float wt = a.w_stage1 ? 1.f : a.topk_weights[s_id];
+      } else {
+        // outputs i0 .. i0 + 63 of the row (token tok), 16 columns at a time
+        // through this warp's transposition buffer: lane l then adds row
+        // 8 j + l / 4, columns 4 (l % 4) .. + 3 of the chunk
+        const int tok = live ? s_id / a.T : -1;  // -1: padding row
+        const float wt = live ? (a.w_stage1 ? 1.f : a.topk_weights[s_id]) : 0.f;
         const long i0 = (long)nt * BN + 64 * cq;
-        float *dst = a.acc + tok * a.K + i0;
+        float4 *xp = reinterpret_cast<float4 *>(sm.xpose[warp - 2]);
+        const int sw_w = (lane >> 1) & 3;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (i0 + 4 * i >= a.K) break;
-          float y[4];
+        for (int ch = 0; ch < 4; ++ch) {
+          if (i0 + 16 * ch >= a.K) break;  // warp-uniform
 #pragma unroll
-          for (int u = 0; u < 4; ++u) y[u] = wt * (acc[4 * i + u] + bias_of(i0 + 4 * i + u));
-          red_add_v4(dst + 4 * i, y[0], y[1], y[2], y[3]);
+          for (int u = 0; u < 4; ++u) {
+            const int c = 16 * ch + 4 * u;
+            const long col = i0 + c;  // K % 4 == 0: the 4 columns all in range or none
+            const bool in = col < a.K;
+            xp[lane * 4 + (u ^ sw_w)] =
+                make_float4(wt * (acc[c] + (in ? bias_of(col) : 0.f)),
+                            wt * (acc[c + 1] + (in ? bias_of(col + 1) : 0.f)),
+                            wt * (acc[c + 2] + (in ? bias_of(col + 2) : 0.f)),
+                            wt * (acc[c + 3] + (in ? bias_of(col + 3) : 0.f)));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int rho = 8 * j + (lane >> 2), u = lane & 3;
+            const int tok_r = __shfl_sync(0xffffffffu, tok, rho);
+            const long col = i0 + 16 * ch + 4 * u;
+            if (tok_r >= 0 && col < a.K) {
+              const float4 v = xp[rho * 4 + (u ^ ((rho >> 1) & 3))];
+              red_add_v4(a.acc + (long)tok_r * a.K + col, v.x, v.y, v.z, v.w);
+            }
+          }
+          __syncwarp();
         }
       }
     }
@@ -357,11 +461,12 @@ cudaError_t launch_fp8b_t(const CUtensorMap &ta, const CUtensorMap &tb, const Tc
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_dev[dev]) {
     cudaError_t e = cudaFuncSetAttribute(fp8b_gemm_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_bytes<MODE>());
     if (e != cudaSuccess) return e;
     attr_dev[dev] = 1;
   }
-  fp8b_gemm_kernel<MODE><<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(ta, tb, a);
+  fp8b_gemm_kernel<MODE><<<(unsigned)grid, THREADS, smem_bytes<MODE>(), st>>>(ta, tb, a);
   return cudaGetLastError();
 }
 
