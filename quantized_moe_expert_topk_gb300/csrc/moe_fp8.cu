@@ -85,10 +85,9 @@ struct Smem {
   // W13: the per-thread maxima of a row's 1 x 128 group (four threads hold
   // it), double-buffered by tile
   alignas(16) float amax_stage[MODE == 0 ? 2 : 1][BM][4];
-  // W2: per epilogue warp, 32 rows x 16 columns of outputs, each row's four
-  // 16-byte units stored at unit (u ^ ((row >> 1) & 3)) (conflict-free both
-  // ways)
-  alignas(16) float xpose[MODE == 0 ? 1 : NUM_EPI][32 * 16];
+  // W2: per epilogue warp, 32 rows x 32 columns of outputs, each row's eight
+  // 16-byte units stored at unit (u ^ (row & 7)) (conflict-free both ways)
+  alignas(16) float xpose[MODE == 0 ? 1 : NUM_EPI][32 * 32];
   uint64_t staged[2], freed[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -133,6 +132,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *e
                                           volatile int *abort_flag) {
   const bool ok = wait_or_abort(bar, parity, err, abort_flag);
   return __all_sync(0xffffffffu, ok);
+}
+
+// x / d from the reciprocal rd = 1 / d (rounded): the product, then one
+// correction by its fma residual (Markstein's quotient step) -- the correctly
+// rounded quotient except in rare cases, whose one-ulp difference the e4m3
+// rounding that follows absorbs but at a tie.
+__device__ __forceinline__ float div_by(float x, float d, float rd) {
+  const float q = x * rd;
+  return fmaf(fmaf(-q, d, x), rd, q);
 }
 
 __device__ __forceinline__ void red_add_v4(float *p, float x, float y, float z, float w) {
@@ -383,12 +391,13 @@ fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           if (lane == 0) mbar_arrive(&sm.freed[sb]);
           const float scale = fp8_group_scale(fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w)));
           if (in) {
+            const float rs = __frcp_rn(scale);
             uint32_t w[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              w[i] = f32x2_to_e4m3x2(__fdiv_rn(z[4 * i], scale), __fdiv_rn(z[4 * i + 1], scale)) |
-                     (f32x2_to_e4m3x2(__fdiv_rn(z[4 * i + 2], scale),
-                                      __fdiv_rn(z[4 * i + 3], scale)) << 16);
+              w[i] = f32x2_to_e4m3x2(div_by(z[4 * i], scale, rs), div_by(z[4 * i + 1], scale, rs)) |
+                     (f32x2_to_e4m3x2(div_by(z[4 * i + 2], scale, rs),
+                                      div_by(z[4 * i + 3], scale, rs)) << 16);
             uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.out) + r * a.N + jbase);
             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -400,23 +409,23 @@ fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
         ++etile;
       } else {
-        // outputs i0 .. i0 + 63 of the row (token tok), 16 columns at a time
+        // outputs i0 .. i0 + 63 of the row (token tok), 32 columns at a time
         // through this warp's transposition buffer: lane l then adds row
-        // 8 j + l / 4, columns 4 (l % 4) .. + 3 of the chunk
+        // 4 j + l / 8, columns 4 (l % 8) .. + 3 of the chunk (one 128-byte
+        // line per 8 lanes)
         const int tok = live ? s_id / a.T : -1;  // -1: padding row
         const float wt = live ? (a.w_stage1 ? 1.f : a.topk_weights[s_id]) : 0.f;
         const long i0 = (long)nt * BN + 64 * cq;
         float4 *xp = reinterpret_cast<float4 *>(sm.xpose[warp - 2]);
-        const int sw_w = (lane >> 1) & 3;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          if (i0 + 16 * ch >= a.K) break;  // warp-uniform
+        for (int ch = 0; ch < 2; ++ch) {
+          if (i0 + 32 * ch >= a.K) break;  // warp-uniform
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = 16 * ch + 4 * u;
+          for (int u = 0; u < 8; ++u) {
+            const int c = 32 * ch + 4 * u;
             const long col = i0 + c;  // K % 4 == 0: the 4 columns all in range or none
             const bool in = col < a.K;
-            xp[lane * 4 + (u ^ sw_w)] =
+            xp[lane * 8 + (u ^ (lane & 7))] =
                 make_float4(wt * (acc[c] + (in ? bias_of(col) : 0.f)),
                             wt * (acc[c + 1] + (in ? bias_of(col + 1) : 0.f)),
                             wt * (acc[c + 2] + (in ? bias_of(col + 2) : 0.f)),
@@ -424,12 +433,12 @@ fp8b_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           }
           __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int rho = 8 * j + (lane >> 2), u = lane & 3;
+          for (int j = 0; j < 8; ++j) {
+            const int rho = 4 * j + (lane >> 3), u = lane & 7;
             const int tok_r = __shfl_sync(0xffffffffu, tok, rho);
-            const long col = i0 + 16 * ch + 4 * u;
+            const long col = i0 + 32 * ch + 4 * u;
             if (tok_r >= 0 && col < a.K) {
-              const float4 v = xp[rho * 4 + (u ^ ((rho >> 1) & 3))];
+              const float4 v = xp[rho * 8 + (u ^ (rho & 7))];
               red_add_v4(a.acc + (long)tok_r * a.K + col, v.x, v.y, v.z, v.w);
             }
           }
