@@ -562,36 +562,93 @@ def time_w13_kernel(moe, wl, layer, dev, stream, iters):
 
 
 def time_e2e(moe, wl, layer, dev, stream, steps, warmup):
+    """The metric end to end through the public call, with every step's
+    host->device copy of its inputs (pinned host memory) and device->host
+    read of its output inside the timed region.  Pipelined as a server runs
+    it: two device buffer sets, uploads on one stream, the layer on the
+    compute stream, read-backs on a third, ordered by events, so step i+1's
+    upload and step i-1's read-back overlap step i's compute.  The serial
+    loop (upload, layer, read-back on one stream) is reported beside it."""
     import torch
     x_h = wl.x.cpu().pin_memory()
     ids_h = wl.topk_ids.cpu().pin_memory()
     w_h = wl.topk_weights.cpu().pin_memory()
-    out_h = torch.empty((wl.M, wl.K), dtype=torch.bfloat16).pin_memory()
-    x_d, ids_d, w_d = torch.empty_like(wl.x), torch.empty_like(wl.topk_ids), torch.empty_like(
-        wl.topk_weights)
-    out_d = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device=dev)
+    out_h = [torch.empty((wl.M, wl.K), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_d = [torch.empty_like(wl.x) for _ in range(2)]
+    ids_d = [torch.empty_like(wl.topk_ids) for _ in range(2)]
+    w_d = [torch.empty_like(wl.topk_weights) for _ in range(2)]
+    out_d = [torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def one():
-        x_d.copy_(x_h, non_blocking=True)
-        ids_d.copy_(ids_h, non_blocking=True)
-        w_d.copy_(w_h, non_blocking=True)
-        layer(x_d, ids_d, w_d, wl.expert_map, out=out_d, stream=stream)
-        out_h.copy_(out_d, non_blocking=True)
+    def piped(i):
+        b = i % 2
+        s_in.wait_event(ev_comp[b])  # step i-2's layer has read these inputs
+        with torch.cuda.stream(s_in):
+            x_d[b].copy_(x_h, non_blocking=True)
+            ids_d[b].copy_(ids_h, non_blocking=True)
+            w_d[b].copy_(w_h, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])  # step i-2's read-back has read this output
+        with torch.cuda.stream(stream):
+            layer(x_d[b], ids_d[b], w_d[b], wl.expert_map, out=out_d[b], stream=stream)
+            ev_comp[b].record(stream)
+        s_out.wait_event(ev_comp[b])
+        with torch.cuda.stream(s_out):
+            out_h[b].copy_(out_d[b], non_blocking=True)
+            ev_out[b].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(warmup, 3)):
-            one()
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(steps):
-            one()
-        end.record(stream)
+    def serial():
+        with torch.cuda.stream(stream):
+            x_d[0].copy_(x_h, non_blocking=True)
+            ids_d[0].copy_(ids_h, non_blocking=True)
+            w_d[0].copy_(w_h, non_blocking=True)
+            layer(x_d[0], ids_d[0], w_d[0], wl.expert_map, out=out_d[0], stream=stream)
+            out_h[0].copy_(out_d[0], non_blocking=True)
+
+    for i in range(max(warmup, 3)):
+        piped(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    stream.wait_event(start)
+    s_out.wait_event(start)
+    for i in range(steps):
+        piped(i)
+    end.record(s_out)  # after the last read-back, which follows every step's work
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
+    # the pipelined read-back holds the layer's output (the fp32 reduction
+    # order may differ between runs: compared within a small tolerance)
+    with torch.cuda.stream(stream):
+        ref = layer(x_d[0], ids_d[0], w_d[0], wl.expert_map, stream=stream)
+    torch.cuda.synchronize()
+    got, ref = out_h[(steps - 1) % 2].float(), ref.float().cpu()
+    rms = ref.pow(2).mean().sqrt().item()
+    if not (got - ref).abs().max().item() <= 1e-2 * rms + 1e-3:
+        raise RuntimeError("pipelined end-to-end output differs from the layer's output")
+    for _ in range(3):
+        serial()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_serial = max(3, min(steps, 20))
+    s0.record(stream)
+    for _ in range(n_serial):
+        serial()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    ms_serial = s0.elapsed_time(s1) / n_serial
     h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
     return {"value": wl.M / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": out_h.numel() * 2, "ms_per_step": ms,
-            "path": "moe_fused_experts with pinned host buffers, eager launches"}
+            "d2h_bytes_per_step": out_h[0].numel() * 2, "ms_per_step": ms,
+            "serial_value": wl.M / (ms_serial / 1e3), "serial_ms_per_step": ms_serial,
+            "path": "moe_fused_experts with pinned host buffers, eager launches",
+            "mode": "pipelined: step i+1's upload and step i-1's read-back (own streams, two "
+                    "device buffer sets) overlap step i's layer; every copy inside the timed "
+                    "region; serial_* = upload, layer and read-back on one stream"}
 
 
 def main():
