@@ -149,11 +149,16 @@ bool tcs_supported(const moe_problem_t *p) {
   return p->wfmt == W_MXFP4 && p->afmt == A_BF16 && tc_mx_direct(p) && p->K % 64 == 0 &&
          p->N % 64 == 0 && p->num_local_experts <= 1024;
 }
-// MXFP4 w4a16 prefill batches above kTcStreamMaxPerExpert slots per local
-// expert take the tcgen05 kernels that decode each weight stage once for two
-// 128-slot blocks (moe_tcd.cu) instead of once per block.
+// MXFP4 prefill batches above kTcStreamMaxPerExpert slots per local expert
+// take the tcgen05 kernels that decode each weight stage once for two
+// 128-slot blocks (moe_tcd.cu) instead of once per block: bf16 activations
+// with the bounded SwiGLU-OAI straight to f16 (w4a16), or OCP MX activations
+// under the same bounds (w4a4 / w4a8: the intermediate quantised and
+// dequantised per 32-output block in the W13 epilogue).
 bool tcd_applies(const moe_problem_t *p) {
-  return p->path == MOE_PATH_AUTO && tc_applies(p) && tcs_supported(p) && p->wfmt == W_MXFP4 &&
+  const bool formats = p->wfmt == W_MXFP4 && p->K % 64 == 0 && p->N % 64 == 0 &&
+                       (tcs_supported(p) || mx_act_f16(p));
+  return p->path == MOE_PATH_AUTO && tc_applies(p) && formats &&
          tcd_supported(p->num_local_experts) &&
          (long)p->M * p->topk > kTcStreamMaxPerExpert * p->num_local_experts;
 }

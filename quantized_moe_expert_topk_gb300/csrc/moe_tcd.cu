@@ -155,7 +155,10 @@ struct Walker {
   __device__ void next() { u += gridDim.x; }
 };
 
-template <int MODE>
+// MXO: the W13 epilogue of OCP MX activations (the intermediate quantised and
+// dequantised per 32-output block), a separate instantiation so that the
+// w4a16 kernel keeps its registers
+template <int MODE, bool MXO = false>
 __global__ void __launch_bounds__(THREADS, 1)
 tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
   extern __shared__ unsigned char smem_raw[];
@@ -378,7 +381,27 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
         const bool live = s_id < a.S && col_live;
         if (MODE == MODE_W13) {
           const int jbase = r_rec * 64 + 32 * (cq & 1);
-          if (live && jbase < a.N) {  // N % 32 == 0: the 32 outputs all in range or none
+          if (MXO && live && jbase < a.N) {
+            // OCP MX activations: the 32 outputs are one MX block (jbase % 32
+            // == 0), quantised and dequantised into exact f16 (the exact
+            // activation, as the other f16 kernels compute it)
+            const bool sep = a.gate == GATE_SEPARATED;
+            const float rf = a.a_rowscale[r];
+            float zb[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float gacc = sep ? acc[i] : acc[2 * i];
+              const float uacc = sep ? acc[32 + i] : acc[2 * i + 1];
+              zb[i] = act_and_mul(a.act, gacc * rf + bias_s[2 * (64 * (cq >> 1) + 32 * (cq & 1) + i)],
+                                  uacc * rf + bias_s[2 * (64 * (cq >> 1) + 32 * (cq & 1) + i) + 1],
+                                  a.alpha, a.beta, a.limit);
+            }
+            uint32_t w[16];
+            mx_qdq_f16x32(zb, a.out_mode == TC_OUT_MX4_F16, w);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + r * a.N + jbase);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          } else if (!MXO && live && jbase < a.N) {  // N % 32 == 0: all 32 outputs in range or none
             const bool sep = a.gate == GATE_SEPARATED;
             const float rf = a.a_rowscale[r];
             uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + r * a.N + jbase);
@@ -455,18 +478,18 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
   }
 }
 
-template <int MODE>
+template <int MODE, bool MXO>
 cudaError_t launch_tcd_t(const CUtensorMap &ta, const TcArgs &a, int grid, cudaStream_t st) {
   static int attr_dev[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_dev[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tcd_gemm_kernel<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(tcd_gemm_kernel<MODE, MXO>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_dev[dev] = 1;
   }
-  tcd_gemm_kernel<MODE><<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(ta, a);
+  tcd_gemm_kernel<MODE, MXO><<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(ta, a);
   return cudaGetLastError();
 }
 
@@ -488,8 +511,10 @@ cudaError_t launch_tcd_gemm(const TcArgs &a_in, const void *rows_f16, long cap_r
     return cudaErrorInvalidValue;
   CUtensorMap ta;
   if (!make_tc_map_b16(&ta, rows_f16, cap_rows, a.C, BM)) return cudaErrorInvalidValue;
-  return w13 ? launch_tcd_t<MODE_W13>(ta, a, sm_count, st)
-             : launch_tcd_t<MODE_W2>(ta, a, sm_count, st);
+  const bool mx_out = a.out_mode == TC_OUT_MX4_F16 || a.out_mode == TC_OUT_MX8_F16;
+  return !w13    ? launch_tcd_t<MODE_W2, false>(ta, a, sm_count, st)
+         : mx_out ? launch_tcd_t<MODE_W13, true>(ta, a, sm_count, st)
+                  : launch_tcd_t<MODE_W13, false>(ta, a, sm_count, st);
 }
 
 }  // namespace moe

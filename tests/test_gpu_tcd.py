@@ -3,7 +3,9 @@ SwiGLU-OAI; each 256-row weight stage decoded once for two 128-slot blocks of
 an expert), the automatic choice above 128 slots per local expert at prefill
 sizes: odd block counts (a pair with one block), an empty expert and a one-slot
 expert, an odd number of 128-row weight records (a half-width last tile), a
-ragged last W2 record, both gate layouts, bf16 and fp32 biases."""
+ragged last W2 record, both gate layouts, bf16 and fp32 biases; and the same
+kernels with OCP MX activations (w4a4 / w4a8: the intermediate quantised and
+dequantised per 32-output block in the W13 epilogue)."""
 import zlib
 
 import pytest
@@ -15,18 +17,20 @@ from moe_workloads import make_custom, to_host
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # name, M, K, N, E, T, gate, bias
-    ("pair_interleaved", 1100, 256, 192, 4, 2, "interleaved", "bf16"),   # W13: 3 records
-    ("pair_separated", 1300, 320, 128, 5, 2, "separated", "bf16"),       # W2: 3 records, last 64 rows
-    ("pair_f32_bias", 1200, 256, 256, 4, 2, "interleaved", "f32"),
+    # name, M, K, N, E, T, gate, bias, activations
+    ("pair_interleaved", 1100, 256, 192, 4, 2, "interleaved", "bf16", "bf16"),  # W13: 3 records
+    ("pair_separated", 1300, 320, 128, 5, 2, "separated", "bf16", "bf16"),  # W2: 3 records, last 64 rows
+    ("pair_f32_bias", 1200, 256, 256, 4, 2, "interleaved", "f32", "bf16"),
+    ("pair_w4a4", 1100, 256, 192, 4, 2, "interleaved", "bf16", "mxfp4_dyn"),
+    ("pair_w4a8", 1300, 320, 128, 5, 2, "separated", "f32", "mxfp8_dyn"),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_block_pairs_match_oracle(case):
     import quantized_moe_expert_topk_gb300 as moe
-    name, M, K, N, E, T, gate, bias = case
-    wl = make_custom(M=M, K=K, N=N, E=E, T=T, wfmt="mxfp4", afmt="bf16", act="swiglu_oai",
+    name, M, K, N, E, T, gate, bias, afmt = case
+    wl = make_custom(M=M, K=K, N=N, E=E, T=T, wfmt="mxfp4", afmt=afmt, act="swiglu_oai",
                      gate=gate, bias=True, seed=zlib.crc32(name.encode()) % 997, name=f"tcd/{name}")
     if bias == "f32":
         wl.w13["bias"] = wl.w13["bias"].float()
