@@ -212,6 +212,22 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int topk, const int32_t
                          int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
                          int32_t *expert_counts, void *stream);
 
+/* The same sort with caller scratch: batches of 8192 slots or more then run
+ * on several CTAs (the outputs are identical, bit for bit).
+ *   scratch        device memory, 16-byte aligned, caller-owned, of at least
+ *                  moe_align_scratch_bytes(M, topk, E_l) bytes (contents need
+ *                  no initialisation and are overwritten); NULL or smaller:
+ *                  the one-CTA sort of moe_align_block_size
+ * moe_align_scratch_bytes returns 0 for batches that always take one CTA (and
+ * for invalid arguments).  Errors as moe_align_block_size, plus
+ * MOE_ERR_INVALID_ARG for a misaligned scratch pointer. */
+size_t moe_align_scratch_bytes(int M, int topk, int num_local_experts);
+int moe_align_block_size_scratch(const int32_t *topk_ids, int M, int topk,
+                                 const int32_t *expert_map, int num_experts, int num_local_experts,
+                                 int block_m, int32_t *sorted_ids, int32_t *expert_ids,
+                                 int32_t *num_post_pad, int32_t *expert_counts, void *scratch,
+                                 size_t scratch_bytes, void *stream);
+
 /* Router: logits -> top-k expert ids and weights, the routing that the
  * apply_monolithic path hands to the expert kernel together with the logits
  * (GptOssMxfp4MoEMethod.apply_monolithic and Mxfp4MoEMethod.apply_monolithic

@@ -8,7 +8,8 @@ points; torch provides device memory and streams only.
 """
 from ._binding import (ACT, AFMT, BLOCK_M, EXPORTS, GATE, LIB_PATH, WFMT, FusedExperts, MoEError,
                        Problem, Weight, lib, make_problem, make_weight, moe_abi_version,
-                       moe_align_block_size, moe_align_capacity, moe_fused_experts,
+                       moe_align_block_size, moe_align_block_size_scratch,
+                       moe_align_capacity, moe_align_scratch_bytes, moe_fused_experts,
                        moe_fused_experts_noalloc, moe_noalloc_scratch_bytes,
                        moe_packed_weight_bytes, moe_prepare_weights,
                        moe_stage_timing, moe_stage_times, STAGES,
@@ -21,7 +22,8 @@ from ._binding import (ACT, AFMT, BLOCK_M, EXPORTS, GATE, LIB_PATH, WFMT, FusedE
 __all__ = [
     "ACT", "AFMT", "BLOCK_M", "EXPORTS", "GATE", "LIB_PATH", "WFMT", "FusedExperts", "MoEError",
     "Problem", "Weight", "lib", "make_problem", "make_weight", "moe_abi_version",
-    "moe_align_block_size", "moe_align_capacity", "moe_fused_experts",
+    "moe_align_block_size", "moe_align_block_size_scratch", "moe_align_capacity",
+    "moe_align_scratch_bytes", "moe_fused_experts",
     "moe_fused_experts_noalloc", "moe_noalloc_scratch_bytes", "moe_packed_weight_bytes",
     "moe_prepare_weights", "moe_stage_timing", "moe_stage_times", "STAGES",
     "PATHS", "moe_route_topk", "SCORING", "moe_mma_probe", "MMA_KINDS",

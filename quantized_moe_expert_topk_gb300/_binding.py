@@ -27,7 +27,8 @@ BLOCK_M = 64
 
 # Every symbol include/moe_experts.h declares.
 EXPORTS = ("moe_abi_version", "moe_status_str", "moe_workspace_size", "moe_align_capacity",
-           "moe_align_block_size", "moe_quant_act", "moe_w13_workspace_size",
+           "moe_align_block_size", "moe_align_scratch_bytes", "moe_align_block_size_scratch",
+           "moe_quant_act", "moe_w13_workspace_size",
            "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_reduce", "moe_fused_experts",
            "moe_get_device_error", "moe_reset_device_error", "moe_selftest_bounded_wait",
            "moe_noalloc_scratch_bytes",
@@ -81,6 +82,8 @@ def lib() -> ctypes.CDLL:
         "moe_workspace_size": (sz, [P]),
         "moe_align_capacity": (l, [i, i, i, i]),
         "moe_align_block_size": (i, [p, i, i, p, i, i, i, p, p, p, p, p]),
+        "moe_align_scratch_bytes": (sz, [i, i, i]),
+        "moe_align_block_size_scratch": (i, [p, i, i, p, i, i, i, p, p, p, p, p, sz, p]),
         "moe_quant_act": (i, [p, i, i, i, p, p, p, p]),
         "moe_route_topk": (i, [p, i, i, i, i, i, i, i, i, p, ctypes.c_float, p, p, p]),
         "moe_w13_workspace_size": (sz, [P, i]),
@@ -187,6 +190,20 @@ def moe_align_block_size(topk_ids, expert_map, E, El, block_m, sorted_ids, exper
     _check("moe_align_block_size", lib().moe_align_block_size(
         _ptr(topk_ids), M, T, _ptr(expert_map), E, El, block_m, _ptr(sorted_ids),
         _ptr(expert_ids), _ptr(num_post_pad), _ptr(expert_counts), _stream(stream)))
+
+
+def moe_align_scratch_bytes(M, topk, El):
+    return int(lib().moe_align_scratch_bytes(M, topk, El))
+
+
+def moe_align_block_size_scratch(topk_ids, expert_map, E, El, block_m, sorted_ids, expert_ids,
+                                 num_post_pad, expert_counts, scratch, stream=None):
+    M, T = topk_ids.shape
+    nbytes = scratch.numel() * scratch.element_size() if scratch is not None else 0
+    _check("moe_align_block_size_scratch", lib().moe_align_block_size_scratch(
+        _ptr(topk_ids), M, T, _ptr(expert_map), E, El, block_m, _ptr(sorted_ids),
+        _ptr(expert_ids), _ptr(num_post_pad), _ptr(expert_counts), _ptr(scratch), nbytes,
+        _stream(stream)))
 
 
 SCORING = {"softmax": 0, "sigmoid": 1}

@@ -17,6 +17,17 @@
 //   D. padding entries, expert_ids, tails.
 // Extra CTAs (blockIdx.x > 0) zero an optional fp32 buffer (the stage-2
 // accumulator) so the fused path needs no separate memset launch.
+//
+// Large batches with caller scratch (>= kMultiMinSlots slots) run the same
+// steps on NC CTAs in two grids, since every 32-slot round of a warp costs
+// about the same (measured ~2000 cycles, whatever the round holds):
+//   count grid:   NC CTAs, warp w of CTA c owns the (32 c + w)-th contiguous
+//                 range of the slots; step A; each CTA writes its per-expert
+//                 totals to scratch [NC][El];
+//   scatter grid: each CTA repeats step A for its own warps, adds the totals
+//                 of the CTAs before it (stable order across CTAs), then B,
+//                 C and its share of D; the zeroing / conversion CTAs ride in
+//                 this grid.
 #include <cuda_fp16.h>
 
 #include "moe_common.cuh"
@@ -29,6 +40,10 @@ namespace {
 
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
+// multi-CTA sort: 4 rounds of 32 slots per warp, from 2 CTAs' worth of slots
+constexpr long kMultiSlotsPerCta = 4L * 32 * kAlignWarps;
+constexpr long kMultiMinSlots = 2 * kMultiSlotsPerCta;
+constexpr int kMultiMaxCtas = 64;
 
 __device__ __forceinline__ int local_of(const int32_t *ids, const int32_t *emap, long s, int E,
                                         int El, long s_valid) {
@@ -39,33 +54,26 @@ __device__ __forceinline__ int local_of(const int32_t *ids, const int32_t *emap,
   return (l >= 0 && l < El) ? l : -1;
 }
 
-__global__ void __launch_bounds__(kAlignThreads)
-align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict__ emap, int E,
-             int El, int BM, int32_t *__restrict__ sorted, int32_t *__restrict__ expert_ids,
-             int32_t *__restrict__ ntp, int32_t *__restrict__ counts, long cap, AlignExtras x,
-             int zero_ctas, int conv_ctas) {
-  // Launched as a programmatic dependent of the previous kernel (the router,
-  // or whatever produced topk_ids): every CTA waits for it before reading the
-  // ids or overwriting buffers it may still read.  A dependent grid (the
-  // streaming GEMM) may be scheduled now: it waits for this grid's completion
-  // before it reads anything written here.
-  griddep_launch_dependents();
-  griddep_wait();
-  if (blockIdx.x > 0 && (int)blockIdx.x <= zero_ctas) {
+// The extra CTAs of a sort grid (index b from 0): the first zero_ctas zero
+// x.zero_buf / x.zero_ints, the next conv_ctas write the per-token f16 copy
+// of x.
+__device__ __forceinline__ void align_extra_cta(const AlignExtras &x, int zero_ctas, int conv_ctas,
+                                                int b) {
+  if (b < zero_ctas) {
     // zeroing CTAs: 16-byte stores over the aligned body, scalar tail
     const long n4 = x.zero_buf ? x.zero_n / 4 : 0;
     float4 *p4 = reinterpret_cast<float4 *>(x.zero_buf);
     const long stride = (long)zero_ctas * blockDim.x;
-    for (long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < n4; i += stride)
+    for (long i = (long)b * blockDim.x + threadIdx.x; i < n4; i += stride)
       p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (long i = n4 * 4 + (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+    for (long i = n4 * 4 + (long)b * blockDim.x + threadIdx.x;
          x.zero_buf && i < x.zero_n; i += stride)
       x.zero_buf[i] = 0.f;
-    for (long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < x.zero_ints_n; i += stride)
+    for (long i = (long)b * blockDim.x + threadIdx.x; i < x.zero_ints_n; i += stride)
       x.zero_ints[i] = 0;
     return;
   }
-  if ((int)blockIdx.x > zero_ctas) {
+  {
     // conversion CTAs: 128 threads per row of x, 8 rows per CTA; bf16 -> f16
     // scaled by 2^a so that the row maximum lands in [2^14, 2^15) (exact for
     // bf16 values).  With x_mx the values are first quantised to OCP MXFP4 /
@@ -78,7 +86,7 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
     const int tr = threadIdx.x & 127, rsub = threadIdx.x >> 7, wr = tr >> 5;
     const int lane = threadIdx.x & 31;
     const int rows_per_cta = blockDim.x / 128;
-    for (int base = ((int)blockIdx.x - 1 - zero_ctas) * rows_per_cta; base < x.xM;
+    for (int base = (b - zero_ctas) * rows_per_cta; base < x.xM;
          base += conv_ctas * rows_per_cta) {
       const int r = base + rsub;
       const bool valid = r < x.xM;
@@ -151,6 +159,24 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
       for (int c = tr + 512; c < k8; c += 128) dst[c] = convert(xr[c]);
       if (tr == 0) x.x_inv[r] = ldexpf(1.0f, -a);
     }
+    return;
+  }
+}
+
+__global__ void __launch_bounds__(kAlignThreads)
+align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict__ emap, int E,
+             int El, int BM, int32_t *__restrict__ sorted, int32_t *__restrict__ expert_ids,
+             int32_t *__restrict__ ntp, int32_t *__restrict__ counts, long cap, AlignExtras x,
+             int zero_ctas, int conv_ctas) {
+  // Launched as a programmatic dependent of the previous kernel (the router,
+  // or whatever produced topk_ids): every CTA waits for it before reading the
+  // ids or overwriting buffers it may still read.  A dependent grid (the
+  // streaming GEMM) may be scheduled now: it waits for this grid's completion
+  // before it reads anything written here.
+  griddep_launch_dependents();
+  griddep_wait();
+  if (blockIdx.x > 0) {
+    align_extra_cta(x, zero_ctas, conv_ctas, (int)blockIdx.x - 1);
     return;
   }
   // slots of tokens at or beyond the valid count (when given) are dropped
@@ -271,7 +297,185 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
   }
 }
 
+// The per-warp histogram of step A over the slots [beg, end) into
+// cnt[warp * El + local expert].
+__device__ __forceinline__ void warp_histogram(const int32_t *ids, const int32_t *emap, int E,
+                                               int El, long s_valid, long beg, long end, int *cnt,
+                                               int warp, int lane) {
+  for (long base = beg; base < end; base += 32) {
+    const long s = base + lane;
+    const int l = s < end ? local_of(ids, emap, s, E, El, s_valid) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, l);
+    if (l >= 0 && lane == __ffs(peers) - 1) cnt[warp * El + l] += __popc(peers);
+  }
+}
+
+__device__ __forceinline__ long valid_slots(long S, const AlignExtras &x) {
+  if (!x.num_valid_tokens) return S;
+  const long n = *x.num_valid_tokens;
+  const long T = x.slots_per_token;
+  return n <= 0 ? 0 : (n * T < S ? n * T : S);
+}
+
+// Count grid of the multi-CTA sort: per-CTA expert totals into ctot[c][El].
+__global__ void __launch_bounds__(kAlignThreads)
+align_count_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict__ emap,
+                   int E, int El, int32_t *__restrict__ ctot, AlignExtras x) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const long s_valid = valid_slots(S, x);
+  extern __shared__ int smem[];
+  int *cnt = smem;  // [kAlignWarps][El]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kAlignWarps * El; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const long per = ceil_div(S, (long)gridDim.x * kAlignWarps);
+  const long beg = ((long)blockIdx.x * kAlignWarps + warp) * per;
+  const long end = beg + per < S ? beg + per : S;
+  warp_histogram(ids, emap, E, El, s_valid, beg, end, cnt, warp, lane);
+  __syncthreads();
+  for (int e = threadIdx.x; e < El; e += blockDim.x) {
+    int t = 0;
+    for (int w = 0; w < kAlignWarps; ++w) t += cnt[w * El + e];
+    ctot[(long)blockIdx.x * El + e] = t;
+  }
+}
+
+// Scatter grid of the multi-CTA sort (CTAs nc.. are the extra CTAs).
+__global__ void __launch_bounds__(kAlignThreads)
+align_scatter_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict__ emap,
+                     int E, int El, int BM, int32_t *__restrict__ sorted,
+                     int32_t *__restrict__ expert_ids, int32_t *__restrict__ ntp,
+                     int32_t *__restrict__ counts, long cap, AlignExtras x,
+                     const int32_t *__restrict__ ctot, int nc, int zero_ctas, int conv_ctas) {
+  // waits for the count grid (and so for everything before it)
+  griddep_launch_dependents();
+  griddep_wait();
+  if ((int)blockIdx.x >= nc) {
+    align_extra_cta(x, zero_ctas, conv_ctas, (int)blockIdx.x - nc);
+    return;
+  }
+  const int c = blockIdx.x;
+  const long s_valid = valid_slots(S, x);
+  extern __shared__ int smem[];
+  int *cnt = smem;                     // [kAlignWarps][El]  per-warp counts -> positions
+  int *off = smem + kAlignWarps * El;  // [El + 1]           live counts, total
+  int *pad = off + El + 1;             // [El]               padded sizes -> offsets
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int i = threadIdx.x; i < kAlignWarps * El; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const long per = ceil_div(S, (long)nc * kAlignWarps);
+  const long beg = ((long)c * kAlignWarps + warp) * per;
+  const long end = beg + per < S ? beg + per : S;
+  // A. this CTA's per-warp histograms (the count grid's, again)
+  warp_histogram(ids, emap, E, El, s_valid, beg, end, cnt, warp, lane);
+  __syncthreads();
+  // B. per expert: the slots of the CTAs before this one, then a stable
+  // prefix over this CTA's warps; totals and padded sizes
+  for (int e = threadIdx.x; e < El; e += blockDim.x) {
+    int tot = 0, before = 0;
+    for (int k = 0; k < nc; ++k) {
+      const int v = ctot[(long)k * El + e];
+      tot += v;
+      before += k < c ? v : 0;
+    }
+    int run = before;
+    for (int w = 0; w < kAlignWarps; ++w) {
+      const int v = cnt[w * El + e];
+      cnt[w * El + e] = run;
+      run += v;
+    }
+    if (c == 0 && counts) counts[e] = tot;
+    pad[e] = (int)(ceil_div(tot, BM) * BM);
+    off[e] = tot;
+  }
+  __syncthreads();
+  // exclusive scan of pad[] by warp 0 (El <= 1024: 32 consecutive experts per lane)
+  if (warp == 0) {
+    const int chunk = (El + 31) / 32;
+    const int e0 = lane * chunk;
+    int local = 0;
+    for (int e = e0; e < e0 + chunk && e < El; ++e) local += pad[e];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e0 + chunk && e < El; ++e) {
+      const int p = pad[e];
+      pad[e] = run;
+      run += p;
+    }
+    if (lane == 31) off[El] = incl;
+  }
+  // compact list of experts with at least one slot (ascending), by CTA 0's warp 1
+  if (c == 0 && warp == 1 && x.active) {
+    const int chunk = (El + 31) / 32;
+    const int e0 = lane * chunk;
+    int local = 0;
+    for (int e = e0; e < e0 + chunk && e < El; ++e) local += off[e] > 0;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int pos = incl - local;
+    for (int e = e0; e < e0 + chunk && e < El; ++e)
+      if (off[e] > 0) x.active[pos++] = e;
+    if (lane == 31) *x.n_active = incl;
+  }
+  __syncthreads();
+  if (c == 0 && x.offsets)
+    for (int e = threadIdx.x; e < El; e += blockDim.x) x.offsets[e] = pad[e];
+  for (int i = threadIdx.x; i < kAlignWarps * El; i += blockDim.x) cnt[i] += pad[i % El];
+  __syncthreads();
+  // C. stable scatter of this CTA's slots
+  for (long base = beg; base < end; base += 32) {
+    const long s = base + lane;
+    const int l = s < end ? local_of(ids, emap, s, E, El, s_valid) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, l);
+    int pos = 0;
+    if (l >= 0) pos = cnt[warp * El + l] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (l >= 0) {
+      sorted[pos] = (int32_t)s;
+      if (lane == __ffs(peers) - 1) cnt[warp * El + l] += __popc(peers);
+    }
+    __syncwarp();
+  }
+  // D. this CTA's share of the padding, the block -> expert table and tails
+  const int total = off[El];
+  const int gw = c * kAlignWarps + warp, nw = nc * kAlignWarps;
+  for (int e = gw; e < El; e += nw) {
+    const int o = pad[e], live = off[e];
+    const int padded = (int)(ceil_div(live, BM) * BM);
+    for (int i = live + lane; i < padded; i += 32) sorted[o + i] = (int32_t)S;
+    for (int b = lane; b < padded / BM; b += 32) expert_ids[o / BM + b] = e;
+  }
+  const long gt = (long)c * blockDim.x + threadIdx.x, nt = (long)nc * blockDim.x;
+  for (long i = total + gt; i < cap; i += nt) sorted[i] = (int32_t)S;
+  for (long b = total / BM + gt; b < cap / BM; b += nt) expert_ids[b] = -1;
+  if (c == 0 && threadIdx.x == 0) {
+    *ntp = total;
+    if (x.counters) x.counters[0] = x.counters[1] = 0;
+  }
+}
+
 }  // namespace
+
+// CTAs of the multi-CTA sort for S slots (0: one CTA), and its scratch.
+int align_multi_ctas(long S) {
+  if (S < kMultiMinSlots) return 0;
+  const long n = ceil_div(S, (long)kMultiSlotsPerCta);
+  return (int)(n < kMultiMaxCtas ? n : kMultiMaxCtas);
+}
+size_t align_scratch_bytes(long S, int El) {
+  return (size_t)align_multi_ctas(S) * El * sizeof(int32_t);
+}
 
 cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *expert_map, int E,
                          int El, int BM, int32_t *sorted_ids, int32_t *expert_ids,
@@ -281,11 +485,21 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *e
   extra.slots_per_token = T;
   const size_t smem = sizeof(int) * ((size_t)kAlignWarps * El + 2 * (size_t)El + 1);
   if (smem > 48 * 1024) {
-    // opt in once to the largest size this kernel can ask for (El = 1024), so
-    // later calls (for instance inside a stream capture) make no attribute call
-    static const cudaError_t opt_in = cudaFuncSetAttribute(
-        align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)(sizeof(int) * ((size_t)kAlignWarps * 1024 + 2 * 1024 + 1)));
+    // opt in once to the largest size these kernels can ask for (El = 1024),
+    // so later calls (for instance inside a stream capture) make no attribute
+    // call
+    static const cudaError_t opt_in = [] {
+      const int most = (int)(sizeof(int) * ((size_t)kAlignWarps * 1024 + 2 * 1024 + 1));
+      cudaError_t e = cudaFuncSetAttribute(align_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(align_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 most);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(align_scatter_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+      return e;
+    }();
     if (opt_in != cudaSuccess) return opt_in;
   }
   int zero_ctas = 0, conv_ctas = 0;
@@ -300,8 +514,20 @@ cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *e
     conv_ctas = (int)ceil_div(extra.xM, kAlignThreads / 128);
     if (conv_ctas > 2 * 152) conv_ctas = 2 * 152;
   }
+  const long S = (long)M * T;
+  const int nc = align_multi_ctas(S);
+  if (nc > 0 && extra.scratch && extra.scratch_bytes >= align_scratch_bytes(S, El)) {
+    cudaError_t e = launch_kernel(align_count_kernel, dim3(nc), dim3(kAlignThreads),
+                                  sizeof(int) * (size_t)kAlignWarps * El, stream, true, topk_ids,
+                                  S, expert_map, E, El, extra.scratch, extra);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(align_scatter_kernel, dim3(nc + zero_ctas + conv_ctas),
+                         dim3(kAlignThreads), smem, stream, true, topk_ids, S, expert_map, E, El,
+                         BM, sorted_ids, expert_ids, num_post_pad, counts, cap, extra,
+                         static_cast<const int32_t *>(extra.scratch), nc, zero_ctas, conv_ctas);
+  }
   return launch_kernel(align_kernel, dim3(1 + zero_ctas + conv_ctas), dim3(kAlignThreads), smem,
-                       stream, true, topk_ids, (long)M * T, expert_map, E, El, BM, sorted_ids,
+                       stream, true, topk_ids, S, expert_map, E, El, BM, sorted_ids,
                        expert_ids, num_post_pad, counts, cap, extra, zero_ctas, conv_ctas);
 }
 

@@ -180,16 +180,16 @@ bool tcs_applies(const moe_problem_t *p) {
 // Workspace layout of the tcgen05 path (sort blocks of 128 rows).
 struct TcLayout {
   long cap, blocks;
-  size_t sorted, expert_ids, ntp, counts, offsets, active, n_active, x16, x_inv, a1_codes,
-      a1_scales, scratch, inter, i_scales, acc, total;
+  size_t sorted, expert_ids, ntp, counts, offsets, active, n_active, align_scr, x16, x_inv,
+      a1_codes, a1_scales, scratch, inter, i_scales, acc, total;
   bool f16_x;  // x converted to f16 once per token by the sort (MXFP4 weights)
 };
 
 // Workspace layout of moe_fused_experts.
 struct Layout {
   long cap, blocks;
-  size_t sorted, expert_ids, ntp, counts, offsets, active, n_active, counters, x16, x_inv, a1_codes,
-      a1_scales, inter, inter_scales, staging, acc, hpart, fixcnt, done13, total;
+  size_t sorted, expert_ids, ntp, counts, offsets, active, n_active, counters, align_scr, x16,
+      x_inv, a1_codes, a1_scales, inter, inter_scales, staging, acc, hpart, fixcnt, done13, total;
   int w13_ksplit;  // k-split of the streaming W13 units (1: none)
   long fixcnt_n;   // counters of the split W13 units
 };
@@ -219,6 +219,7 @@ Layout make_layout(const moe_problem_t *p) {
   L.active = o; o = align_up(o + (size_t)p->num_local_experts * 4);
   L.n_active = o; o = align_up(o + 4);
   L.counters = o; o = align_up(o + 8);
+  L.align_scr = o; o = align_up(o + align_scratch_bytes((long)p->M * p->topk, p->num_local_experts));
   const bool f16_x = p->wfmt == W_MXFP4 && (p->afmt == A_BF16 || mx_act_f16(p));
   if (f16_x) {  // f16 copy of x for the streaming kernels
     L.x16 = o; o = align_up(o + (size_t)p->M * p->K * 2);
@@ -325,6 +326,7 @@ TcLayout make_tc_layout(const moe_problem_t *p, bool tcs = false) {
   L.offsets = o; o = align_up(o + (size_t)p->num_local_experts * 4);
   L.active = o; o = align_up(o + (size_t)p->num_local_experts * 4);
   L.n_active = o; o = align_up(o + 4);
+  L.align_scr = o; o = align_up(o + align_scratch_bytes((long)p->M * p->topk, p->num_local_experts));
   L.f16_x = p->wfmt == W_MXFP4 && (p->afmt == A_BF16 || mx_act_f16(p));
   L.x16 = L.x_inv = o;
   if (L.f16_x) {
@@ -610,20 +612,39 @@ size_t moe_workspace_size(const moe_problem_t *p) {
   return n;
 }
 
-int moe_align_block_size(const int32_t *topk_ids, int M, int topk, const int32_t *expert_map,
-                         int num_experts, int num_local_experts, int block_m,
-                         int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
-                         int32_t *expert_counts, void *stream) {
+size_t moe_align_scratch_bytes(int M, int topk, int num_local_experts) {
+  if (M < 0 || topk < 1 || num_local_experts < 1 || num_local_experts > 1024) return 0;
+  return align_scratch_bytes((long)M * topk, num_local_experts);
+}
+
+int moe_align_block_size_scratch(const int32_t *topk_ids, int M, int topk,
+                                 const int32_t *expert_map, int num_experts, int num_local_experts,
+                                 int block_m, int32_t *sorted_ids, int32_t *expert_ids,
+                                 int32_t *num_post_pad, int32_t *expert_counts, void *scratch,
+                                 size_t scratch_bytes, void *stream) {
   if (M < 0 || topk < 1 || num_experts < 1 || num_local_experts < 1 ||
       num_local_experts > 1024 || block_m < 1 || block_m > 1024)
     return MOE_ERR_INVALID_ARG;
   if ((M > 0 && !topk_ids) || !sorted_ids || !expert_ids || !num_post_pad)
     return MOE_ERR_INVALID_ARG;
+  if (scratch && (reinterpret_cast<uintptr_t>(scratch) % 16) != 0) return MOE_ERR_INVALID_ARG;
   if ((long)M * topk > (1L << 30)) return MOE_ERR_UNSUPPORTED;
   const long cap = moe_align_capacity(M, topk, num_local_experts, block_m);
+  AlignExtras ex;
+  ex.scratch = static_cast<int32_t *>(scratch);
+  ex.scratch_bytes = scratch ? scratch_bytes : 0;
   return cuda_status(launch_align(topk_ids, M, topk, expert_map, num_experts, num_local_experts,
                                   block_m, sorted_ids, expert_ids, num_post_pad, expert_counts,
-                                  cap, AlignExtras(), static_cast<cudaStream_t>(stream)));
+                                  cap, ex, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_align_block_size(const int32_t *topk_ids, int M, int topk, const int32_t *expert_map,
+                         int num_experts, int num_local_experts, int block_m,
+                         int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
+                         int32_t *expert_counts, void *stream) {
+  return moe_align_block_size_scratch(topk_ids, M, topk, expert_map, num_experts,
+                                      num_local_experts, block_m, sorted_ids, expert_ids,
+                                      num_post_pad, expert_counts, nullptr, 0, stream);
 }
 
 int moe_route_topk(const void *logits, int logits_bf16, int M, int num_experts, int topk,
@@ -803,6 +824,8 @@ int moe_fused_experts(const moe_problem_t *p, const void *hidden_bf16, const moe
   AlignExtras ex;
   ex.zero_buf = acc;
   ex.zero_n = MK;
+  ex.scratch = reinterpret_cast<int32_t *>(ws + L.align_scr);
+  ex.scratch_bytes = align_scratch_bytes((long)p->M * p->topk, p->num_local_experts);
   if (streaming) {
     ex.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
     ex.active = reinterpret_cast<int32_t *>(ws + L.active);
@@ -1372,6 +1395,8 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
     ex.zero_buf = acc;
     ex.zero_n = MK;
     ex.num_valid_tokens = p->num_local_tokens;
+    ex.scratch = reinterpret_cast<int32_t *>(ws + L.align_scr);
+    ex.scratch_bytes = align_scratch_bytes((long)p->M * p->topk, p->num_local_experts);
     if (tcs || pair) {  // per-expert tables of the weight-streaming / block-pair kernels
       ex.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
       ex.active = reinterpret_cast<int32_t *>(ws + L.active);

@@ -53,7 +53,16 @@ struct AlignExtras {
   long zero_ints_n = 0;
   const int32_t *num_valid_tokens = nullptr;  // [1]: slots of tokens >= it are dropped
   int slots_per_token = 1;                     // topk (set by launch_align)
+  // scratch of the multi-CTA sort (align_scratch_bytes); null or too small:
+  // the one-CTA sort
+  int32_t *scratch = nullptr;
+  size_t scratch_bytes = 0;
 };
+
+// The multi-CTA sort of S slots: its CTAs (0 below its size threshold: the
+// one-CTA kernel) and its scratch bytes (per-CTA expert totals).
+int align_multi_ctas(long S);
+size_t align_scratch_bytes(long S, int El);
 
 cudaError_t launch_align(const int32_t *topk_ids, int M, int T, const int32_t *expert_map, int E,
                          int El, int BM, int32_t *sorted_ids, int32_t *expert_ids,

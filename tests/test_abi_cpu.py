@@ -207,3 +207,16 @@ def test_step_entry_points_validate_before_launching(moe):
                          router_weight_on_input=True)
     assert L.moe_grouped_gemm_w2_reduce(ctypes.byref(r), fake, None, ctypes.byref(w), fake, fake,
                                         fake, fake, 64, fake, fake, None) == 2
+
+
+def test_align_scratch_bytes():
+    # the multi-CTA sort needs per-CTA expert totals from 8192 slots on (4096
+    # slots per CTA, at most 64 CTAs); below that, and for invalid
+    # arguments, no scratch
+    import quantized_moe_expert_topk_gb300 as moe
+    assert moe.moe_align_scratch_bytes(1024, 4, 32) == 0
+    assert moe.moe_align_scratch_bytes(2048, 4, 96) == 2 * 96 * 4
+    assert moe.moe_align_scratch_bytes(4096, 9, 257) == 9 * 257 * 4
+    assert moe.moe_align_scratch_bytes(1 << 20, 8, 1024) == 64 * 1024 * 4
+    assert moe.moe_align_scratch_bytes(4096, 9, 2000) == 0
+    assert moe.moe_align_scratch_bytes(-1, 9, 8) == 0

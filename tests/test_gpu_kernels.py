@@ -16,7 +16,7 @@ def moe():
     return m
 
 
-def gpu_align(moe, ids, emap, E, El, BM):
+def gpu_align(moe, ids, emap, E, El, BM, scratch=False):
     M, T = ids.shape
     cap = moe.moe_align_capacity(M, T, El, BM)
     dev = "cuda"
@@ -26,7 +26,13 @@ def gpu_align(moe, ids, emap, E, El, BM):
     expert_ids = torch.full((max(cap // BM, 1),), -7, dtype=torch.int32, device=dev)
     ntp = torch.zeros(1, dtype=torch.int32, device=dev)
     counts = torch.full((El,), -7, dtype=torch.int32, device=dev)
-    moe.moe_align_block_size(t_ids, t_map, E, El, BM, sorted_ids, expert_ids, ntp, counts)
+    if scratch:  # the multi-CTA sort (from 8192 slots), garbage in its scratch
+        nb = moe.moe_align_scratch_bytes(M, T, El)
+        scr = torch.full((max(nb // 4, 1),), -5, dtype=torch.int32, device=dev)
+        moe.moe_align_block_size_scratch(t_ids, t_map, E, El, BM, sorted_ids, expert_ids, ntp,
+                                         counts, scr)
+    else:
+        moe.moe_align_block_size(t_ids, t_map, E, El, BM, sorted_ids, expert_ids, ntp, counts)
     torch.cuda.synchronize()
     return (sorted_ids.cpu().numpy()[:cap], expert_ids.cpu().numpy()[:cap // BM],
             int(ntp.item()), counts.cpu().numpy())
@@ -49,8 +55,9 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("M,T,E,El,BM,kind", CASES)
-def test_align_bit_exact(moe, M, T, E, El, BM, kind):
+@pytest.mark.parametrize("scratch", [False, True], ids=["one_cta", "scratch"])
+@pytest.mark.parametrize("M,T,E,El,BM,kind", CASES + [(70000, 4, 32, 32, 128, None)])
+def test_align_bit_exact(moe, M, T, E, El, BM, kind, scratch):
     rng = np.random.default_rng(M * 31 + T)
     ids = rng.integers(0, E, size=(M, T)).astype(np.int32)
     if M > 10:
@@ -67,7 +74,7 @@ def test_align_bit_exact(moe, M, T, E, El, BM, kind):
         emap[5] = 0
     elif kind == "all_masked":
         emap = np.full(E, -1, np.int32)
-    got = gpu_align(moe, ids, emap, E, El, BM)
+    got = gpu_align(moe, ids, emap, E, El, BM, scratch)
     want = oracle.align_block_size(ids, emap, E, El, BM)
     np.testing.assert_array_equal(got[0], want[0])
     np.testing.assert_array_equal(got[1], want[1])
