@@ -314,7 +314,9 @@ def launches_per_step(wl, routing=False, fused=False, path="auto"):
     path = kernel_path(wl, path)
     s2 = moe.stage2_format(wl.wfmt, wl.afmt)
     n = int(routing)                       # fused router
-    n += 1                                 # sort / pad (+ zero, + f16 copy of x when streaming)
+    # sort / pad (+ zero, + f16 copy of x when streaming): from 8192 slots the
+    # multi-CTA sort, a count grid and a scatter grid
+    n += 1 + (wl.M * wl.T >= 8192)
     mx_act = wl.afmt in ("mxfp4_dyn", "mxfp8_dyn")
     if path == "stream":                   # w13, (MX: intermediate QDQ), w2, finalize
         return n + (2 if fused else 3 + mx_act)

@@ -85,12 +85,13 @@ def test_launches_per_step():
     w4a4 = make_workload("gptoss20b_w4a4_m64")
     assert bench.launches_per_step(w4a4, fused=True) == 3
     assert bench.launches_per_step(w4a4, fused=False) == 5       # + the MX pass
-    # tcgen05 MX prefill: sort, gather, w13 (MX epilogue), w2, finalize
-    assert bench.launches_per_step(make_workload("gptoss20b_w4a4_m64", M=4096)) == 5
-    # tcgen05 weight streaming: sort, gather, w13, w2, finalize
-    assert bench.launches_per_step(make_workload("gptoss120b_mxfp4_ep75", M=2048)) == 5
-    # FP8 block: sort, quant, gather, w13 (1 x 128 requantisation inside), w2, finalize
-    assert bench.launches_per_step(make_workload("dsv3_fp8block_m4096")) == 6
+    # from 8192 slots the sort is two grids (count, scatter)
+    # tcgen05 MX prefill: sort (2), gather, w13 (MX epilogue), w2, finalize
+    assert bench.launches_per_step(make_workload("gptoss20b_w4a4_m64", M=4096)) == 6
+    # tcgen05 weight streaming: sort (2), gather, w13, w2, finalize
+    assert bench.launches_per_step(make_workload("gptoss120b_mxfp4_ep75", M=2048)) == 6
+    # FP8 block: sort (2), quant, gather, w13 (1 x 128 requantisation inside), w2, finalize
+    assert bench.launches_per_step(make_workload("dsv3_fp8block_m4096")) == 7
     # generic bf16: sort, w13, w2, finalize
     assert bench.launches_per_step(make_workload("tiny_bf16_m16")) == 4
 
