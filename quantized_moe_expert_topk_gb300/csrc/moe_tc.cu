@@ -548,15 +548,23 @@ __global__ void gather_rows_kernel(GatherArgs g) {
     const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(g.codes) +
                                                        t * (g.K / 2));
     for (int c = lane; c < g.K / 32; c += 32) dst[c] = live ? src[c] : make_uint4(0, 0, 0, 0);
+    // the four scales of a 64-element step are one aligned word of the
+    // record (and of each replica): one 4-byte load, four 4-byte stores
     const long KS = ceil_div(g.K, kTcBsStage);
     const int G = g.K / 16;
     const uint8_t *sc = static_cast<const uint8_t *>(g.scales) + t * G;
     uint8_t *sf = static_cast<uint8_t *>(g.sf_out);
-    for (int w = lane; w < KS * 16; w += 32) {
-      const uint8_t v = (live && w < G) ? sc[w] : 0;
-      const long o = bs_sfa_offset(r, (long)w * 16, KS);
+    for (int st = lane; st < KS * 4; st += 32) {
+      uint32_t v = 0;
+      if (live && 4 * st + 3 < G && (G & 3) == 0) {
+        v = reinterpret_cast<const uint32_t *>(sc)[st];
+      } else if (live) {
+        for (int b = 0; b < 4; ++b)
+          if (4 * st + b < G) v |= (uint32_t)sc[4 * st + b] << (8 * b);
+      }
+      const long o = bs_sfa_offset(r, (long)st * 64, KS);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sf[o + 1024 * q] = v;
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint32_t *>(sf + o + 1024 * q) = v;
     }
   } else {  // fp8 codes, copied
     uint8_t *dst = static_cast<uint8_t *>(g.out) + r * g.K;
