@@ -322,7 +322,10 @@ def launches_per_step(wl, routing=False, fused=False, path="auto"):
         return n + (2 if fused else 3 + mx_act)
     if path == "tc_stream":                # gather, w13 (f16 intermediate), w2, finalize
         return n + 4
-    n += wl.afmt != "bf16" and not (path == "tc" and mx_act)  # stage-1 quantiser (MX on tc: in the gather)
+    # stage-1 quantiser (on tc, MX activations and NVFP4 ones are quantised by
+    # the gather)
+    nv_in_gather = path == "tc" and wl.wfmt == "nvfp4" and wl.afmt == "nvfp4_dyn"
+    n += wl.afmt != "bf16" and not (path == "tc" and mx_act) and not nv_in_gather
     n += path == "tc"                      # gather of the sorted activation rows
     n += 1                                 # w13 GEMM + activation
     if path == "tc":

@@ -1234,6 +1234,10 @@ int tc_stage1(const moe_problem_t *p, const void *a_codes, const void *a_scales,
     g.rowscale = reinterpret_cast<float *>(scratch + L.a_rowscale);
     g.groupscale = reinterpret_cast<float *>(scratch + L.a_groupscale);
     if (bs) g.sf_out = scratch + L.a_sf;
+    if (bs && !a_scales) {  // NVFP4 rows quantised by the gather itself (bf16 x in a_codes)
+      g.x_nvfp4 = static_cast<const uint16_t *>(a_codes);
+      g.nv_global = p->a1_scale;
+    }
     StageScope sc(MOE_STAGE_QUANT, st);
     rc = cuda_status(launch_gather_rows(g, cap, st));
     sc.done();
@@ -1422,7 +1426,10 @@ int run_tc_path(const moe_problem_t *p, const void *hidden, const moe_weight_t *
   const bool mx = p->afmt == A_MXFP4_DYN || p->afmt == A_MXFP8_DYN;
   const void *codes = hidden;
   const void *scales = nullptr;
-  if (p->afmt != A_BF16 && !mx) {
+  // NVFP4 weights and activations: the gather quantises the rows it writes
+  // (tc_stage1 sees bf16 x and no scales)
+  const bool nvfp4_in_gather = p->wfmt == W_NVFP4 && p->afmt == A_NVFP4_DYN;
+  if (p->afmt != A_BF16 && !mx && !nvfp4_in_gather) {
     QuantArgs q{};  // every field zero / its default
     q.x = hidden; q.rows = p->M; q.cols = p->K; q.afmt = p->afmt; q.param = p->a1_scale;
     q.codes = ws + L.a1_codes; q.scales = ws + L.a1_scales; q.BM = 1;

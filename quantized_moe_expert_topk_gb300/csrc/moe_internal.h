@@ -272,6 +272,10 @@ struct GatherArgs {
   // block-scaled NVFP4 (afmt A_NVFP4_DYN): out receives the codes [cap, K/2]
   // and sf_out the scale-factor records of the sorted rows
   void *sf_out = nullptr;
+  // when set (NVFP4): codes and scales are quantised here from the bf16 token
+  // rows x_nvfp4 [M, K] with the global scale *nv_global (no quantiser pass)
+  const uint16_t *x_nvfp4 = nullptr;
+  const float *nv_global = nullptr;
 };
 cudaError_t launch_rescale_rows(const float *src, long cap, int N, const int32_t *sorted_ids,
                                 const int32_t *ntp, int S, void *dst, float *rowscale,

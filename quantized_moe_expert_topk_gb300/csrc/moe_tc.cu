@@ -540,6 +540,47 @@ __global__ void gather_rows_kernel(GatherArgs g) {
       dst[c] = o;
     }
     if (lane == 0) g.rowscale[r] = live ? ldexpf(1.0f, -a) : 0.f;
+  } else if (g.afmt == A_NVFP4_DYN && g.sf_out && g.x_nvfp4) {
+    // block-scaled operand quantised here from the token's bf16 row (the
+    // stage-1 quantiser's rule, nvfp4_quant16): lane l takes the 16-element
+    // group 32 i + l; the first lane of every four packs the step's four
+    // scales into its record word (and replicas); zeros for padding rows and
+    // past K
+    const long KS = ceil_div(g.K, kTcBsStage);
+    const int G = g.K / 16;
+    const float gs = g.nv_global[0];
+    const uint4 *xr = reinterpret_cast<const uint4 *>(g.x_nvfp4 + t * g.K);
+    uint8_t *dst = static_cast<uint8_t *>(g.out) + r * (g.K / 2);
+    uint8_t *sf = static_cast<uint8_t *>(g.sf_out);
+    for (int i = 0; i < (G + 31) / 32; ++i) {  // warp-uniform
+      const int grp = 32 * i + lane;
+      uint32_t lo = 0, hi = 0, sb = 0;
+      if (live && grp < G) {
+        const uint4 u0 = xr[2 * grp], u1 = xr[2 * grp + 1];
+        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        float v[16];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          v[2 * k] = __uint_as_float(w[k] << 16);
+          v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+        sb = nvfp4_quant16(v, gs, lo, hi);
+      }
+      if (grp < G) *reinterpret_cast<uint2 *>(dst + 8 * grp) = make_uint2(lo, hi);
+      const uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 1) << 8) |
+                            (__shfl_down_sync(0xffffffffu, sb, 2) << 16) |
+                            (__shfl_down_sync(0xffffffffu, sb, 3) << 24);
+      if ((lane & 3) == 0 && grp < G) {
+        const long o = bs_sfa_offset(r, (long)(grp / 4) * 64, KS);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint32_t *>(sf + o + 1024 * q) = word;
+      }
+    }
+    for (int st = (G + 3) / 4 + lane; st < KS * 4; st += 32) {  // steps past K
+      const long o = bs_sfa_offset(r, (long)st * 64, KS);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint32_t *>(sf + o + 1024 * q) = 0u;
+    }
   } else if (g.afmt == A_NVFP4_DYN && g.sf_out) {
     // block-scaled operand: the codes row as it is, and its ue4m3 scales into
     // the scale-factor records of the sorted rows (zeros past K and for
