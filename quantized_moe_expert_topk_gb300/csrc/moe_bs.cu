@@ -77,8 +77,10 @@ constexpr int kErrTimeout = 5;
 template <int MODE> constexpr int kRasterGroup = MODE == 0 ? 32 : 16;
 // Weight records are prefetched into L2 this many stages ahead of the ring
 // (by the CTA of the first m-block of each raster group only: the others of
-// the group read the same records), so the ring's copies hit L2.
-constexpr int kPrefetchAhead = 8;
+// the group read the same records), so the ring's copies hit L2.  Measured on
+// the Mixtral NVFP4 prefill (ms per step): 1.690 / 1.650 / 1.639 / 1.647 /
+// 1.659 for 0 / 2 / 4 / 8 / 16 stages.
+constexpr int kPrefetchAhead = 4;
 
 enum { MODE_W13 = 0, MODE_W2 = 1 };
 
