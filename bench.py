@@ -629,13 +629,14 @@ def time_e2e(moe, wl, layer, dev, stream, steps, warmup):
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
     # the pipelined read-back holds the layer's output (the fp32 reduction
-    # order may differ between runs: compared within a small tolerance)
+    # order may differ between runs, which can move a bf16 output by one
+    # rounding step: compared within 1e-2 rms + one bf16 step of the value)
     with torch.cuda.stream(stream):
         ref = layer(x_d[0], ids_d[0], w_d[0], wl.expert_map, stream=stream)
     torch.cuda.synchronize()
     got, ref = out_h[(steps - 1) % 2].float(), ref.float().cpu()
     rms = ref.pow(2).mean().sqrt().item()
-    if not (got - ref).abs().max().item() <= 1e-2 * rms + 1e-3:
+    if not bool(((got - ref).abs() <= 1e-2 * rms + 1e-3 + ref.abs() * 2.0**-7).all()):
         raise RuntimeError("pipelined end-to-end output differs from the layer's output")
     for _ in range(3):
         serial()

@@ -95,6 +95,15 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, in
   return true;
 }
 
+// A wait of the decoder / epilogue warps whose outcome is the same on every
+// lane (the warp leaves its loops together: its shuffles and warp barriers
+// never wait for a lane that has left).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *err,
+                                          volatile int *abort_flag) {
+  const bool ok = wait_or_abort(bar, parity, err, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void red_add_v4(float *p, float x, float y, float z, float w) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(x), "f"(y), "f"(z),
                "f"(w)
@@ -328,10 +337,10 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
     long g = 0, tc = 0;
     Walker wk(a, sm.unit_pre, n_act);
     Unit un;
-    while (!*abort_flag && wk.get(un)) {
+    while (!__any_sync(0xffffffffu, *abort_flag != 0) && wk.get(un)) {  // warp-uniform
       for (int kt = 0; kt < KT; ++kt, ++g) {
         const int s = (int)(g % NS);
-        if (!wait_or_abort(&sm.raw_full[s], (uint32_t)((g / NS) & 1), a.err, abort_flag)) break;
+        if (!warp_wait(&sm.raw_full[s], (uint32_t)((g / NS) & 1), a.err, abort_flag)) break;
         if (rec < un.nrec) {
           const unsigned char *rp = sm.raw[s][rec];
           const uint4 cw = *reinterpret_cast<const uint4 *>(rp + rn * 32 + h * 16);
@@ -357,15 +366,15 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.b_full[s]);
       }
-      if (*abort_flag) break;
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // the warp leaves together
 
       // ---------------------------------------------------------- epilogue
-      if (!wait_or_abort(&sm.acc_full, (uint32_t)(tc & 1), a.err, abort_flag)) break;
+      if (!warp_wait(&sm.acc_full, (uint32_t)(tc & 1), a.err, abort_flag)) break;
       tc_fence_after();
       const int r_rec = 2 * un.nt + (cq >> 1);  // record tile of this thread's columns
       const bool col_live = (cq >> 1) < un.nrec;
       const int bbuf = (int)(tc & 1);
-      if (!wait_or_abort(&sm.bias_full[bbuf], (uint32_t)((tc >> 1) & 1), a.err, abort_flag)) break;
+      if (!warp_wait(&sm.bias_full[bbuf], (uint32_t)((tc >> 1) & 1), a.err, abort_flag)) break;
       const float *bias_s = sm.bias[bbuf];
       for (int b = 0; b < un.nblk; ++b) {
         const long r = (long)(un.blk0 + b) * BM + q * 32 + lane;  // sorted row
@@ -381,7 +390,8 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
           }
         }
         const int s_id = a.sorted_ids[r];
-        const bool live = s_id < a.S && col_live;
+        const bool row_live = s_id < a.S;
+        const bool live = row_live && col_live;
         if (MODE == MODE_W13) {
           const int jbase = r_rec * 64 + 32 * (cq & 1);
           if (MXO && live && jbase < a.N) {
@@ -437,28 +447,41 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
               dst[p] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           }
-        } else if (live) {
-          const long tok = s_id / a.T;
-          const float wt = a.w_stage1 ? 1.f : a.topk_weights[s_id];
+        } else if (col_live) {  // warp-uniform
+          // outputs k0 .. k0 + 63 of the row, 16 columns at a time through
+          // this warp's own 16 rows of decoded-weight slot 0 (2 KB: free now,
+          // the unit's MMAs have completed and the next unit's wait for this
+          // epilogue; the warp decodes into them again only after it): lane l
+          // then adds row 8 j + l / 4, columns 4 (l % 4) .. + 3, so one red.add
+          // covers 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes
+          const int tok = row_live ? s_id / a.T : -1;  // -1: padding row
+          const float wt = row_live ? (a.w_stage1 ? 1.f : a.topk_weights[s_id]) : 0.f;
           const long k0 = (long)r_rec * 128 + 64 * (cq & 1);
-          float *dst = a.acc + tok * a.K + k0;
+          float4 *xp = reinterpret_cast<float4 *>(sm.b[0] + 2048 * (warp - 2));
+          const int sw_w = (lane >> 1) & 3;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {  // 16 outputs per chunk (K % 16 == 0)
-            if (k0 + 16 * c >= a.K) break;
-            float b[16];
+            if (k0 + 16 * c >= a.K) break;  // warp-uniform
             const float4 *bp =
                 reinterpret_cast<const float4 *>(bias_s + 128 * (cq >> 1) + 64 * (cq & 1) + 16 * c);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const float4 f = bp[v];
-              b[4 * v] = f.x; b[4 * v + 1] = f.y; b[4 * v + 2] = f.z; b[4 * v + 3] = f.w;
+            for (int u = 0; u < 4; ++u) {
+              const float4 f = bp[u];
+              xp[lane * 4 + (u ^ sw_w)] = make_float4(
+                  wt * (acc[16 * c + 4 * u] + f.x), wt * (acc[16 * c + 4 * u + 1] + f.y),
+                  wt * (acc[16 * c + 4 * u + 2] + f.z), wt * (acc[16 * c + 4 * u + 3] + f.w));
             }
+            __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              red_add_v4(dst + 16 * c + 4 * i, wt * (acc[16 * c + 4 * i] + b[4 * i]),
-                         wt * (acc[16 * c + 4 * i + 1] + b[4 * i + 1]),
-                         wt * (acc[16 * c + 4 * i + 2] + b[4 * i + 2]),
-                         wt * (acc[16 * c + 4 * i + 3] + b[4 * i + 3]));
+            for (int j = 0; j < 4; ++j) {
+              const int rho = 8 * j + (lane >> 2), u = lane & 3;
+              const int tok_r = __shfl_sync(0xffffffffu, tok, rho);
+              if (tok_r >= 0) {
+                const float4 v = xp[rho * 4 + (u ^ ((rho >> 1) & 3))];
+                red_add_v4(a.acc + (long)tok_r * a.K + k0 + 16 * c + 4 * u, v.x, v.y, v.z, v.w);
+              }
+            }
+            __syncwarp();
           }
         }
       }
