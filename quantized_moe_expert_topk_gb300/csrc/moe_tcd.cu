@@ -391,10 +391,14 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
         }
         const int s_id = a.sorted_ids[r];
         const bool row_live = s_id < a.S;
-        const bool live = row_live && col_live;
         if (MODE == MODE_W13) {
           const int jbase = r_rec * 64 + 32 * (cq & 1);
-          if (MXO && live && jbase < a.N) {
+          // the row's 32 f16 outputs (four 16-byte units) go through this
+          // warp's own 16 rows of decoded-weight slot 0 (free now, as for W2)
+          // and out 8 rows x 64 contiguous bytes per store instruction
+          uint4 *xp = reinterpret_cast<uint4 *>(sm.b[0] + 2048 * (warp - 2));
+          const int sw_w = (lane >> 1) & 3;
+          if (MXO && col_live && jbase < a.N) {  // warp-uniform
             // OCP MX activations: the 32 outputs are one MX block (jbase % 32
             // == 0), quantised and dequantised into exact f16 (the exact
             // activation, as the other f16 kernels compute it)
@@ -411,13 +415,12 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
             }
             uint32_t w[16];
             mx_qdq_f16x32(zb, a.out_mode == TC_OUT_MX4_F16, w);
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + r * a.N + jbase);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          } else if (!MXO && live && jbase < a.N) {  // N % 32 == 0: all 32 outputs in range or none
+            for (int i = 0; i < 4; ++i)
+              xp[lane * 4 + (i ^ sw_w)] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          } else if (!MXO && col_live && jbase < a.N) {  // warp-uniform; N % 32 == 0
             const bool sep = a.gate == GATE_SEPARATED;
             const float rf = a.a_rowscale[r];
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + r * a.N + jbase);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {  // 8 outputs per pass
               // the staged (gate, up) biases of these 8 outputs
@@ -444,8 +447,22 @@ tcd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const TcArgs a) {
                 const __half2 h2 = __floats2half2_rn(z2[0], z2[1]);
                 w[i >> 1] = *reinterpret_cast<const uint32_t *>(&h2);
               }
-              dst[p] = make_uint4(w[0], w[1], w[2], w[3]);
+              xp[lane * 4 + (p ^ sw_w)] = make_uint4(w[0], w[1], w[2], w[3]);
             }
+          }
+          if (col_live && jbase < a.N) {  // warp-uniform: the transposed stores
+            __syncwarp();
+            const int live_mask = __ballot_sync(0xffffffffu, row_live);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int rho = 8 * j + (lane >> 2), u = lane & 3;
+              if ((live_mask >> rho) & 1) {
+                const long rr = (long)(un.blk0 + b) * BM + q * 32 + rho;
+                reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + rr * a.N + jbase)[u] =
+                    xp[rho * 4 + (u ^ ((rho >> 1) & 3))];
+              }
+            }
+            __syncwarp();
           }
         } else if (col_live) {  // warp-uniform
           // outputs k0 .. k0 + 63 of the row, 16 columns at a time through
