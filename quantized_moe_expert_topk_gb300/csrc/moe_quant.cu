@@ -61,44 +61,64 @@ __device__ __forceinline__ int row_state(const QuantArgs &a, long r) {
   return a.sorted_ids[r] < a.S ? 1 : 0;
 }
 
-// ---- fp8, 1x128 groups: one warp per (row, group); lane owns 4 columns.
+// ---- fp8, 1x128 groups: one warp per 4 groups of a row; 8 lanes per group,
+// lane owns 16 consecutive columns (two 16-byte loads of bf16 in flight per
+// lane, the maximum reduced over the group's 8 lanes).  The same arithmetic per
+// element as a group per warp; a ragged last group (cols % 128) takes the
+// per-element path.
 template <typename InT>
 __global__ void quant_fp8_group128(QuantArgs a) {
   const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int G = (int)ceil_div(a.cols, 128);
-  const long r = warp_id / G;
-  const int g = (int)(warp_id % G);
-  if (r >= a.rows) return;
+  const int WG = (G + 3) / 4;  // warps per row
+  const long r = warp_id / WG;
+  const int g = (int)(warp_id % WG) * 4 + (lane >> 3);  // this lane's group
+  if (r >= a.rows) return;  // warp-uniform
   const int st = row_state(a, r);
-  if (st < 0) return;
+  if (st < 0) return;  // warp-uniform
+  const bool in = g < G;
   const InT *x = static_cast<const InT *>(a.x) + r * a.cols;
   uint8_t *codes = static_cast<uint8_t *>(a.codes) + r * a.cols;
   float *scales = static_cast<float *>(a.scales);
-  const int c0 = g * 128 + lane * 4;
-  float v[4];
+  const int c0 = g * 128 + (lane & 7) * 16;
+  float v[16];
+  const bool full = in && st > 0 && c0 + 15 < a.cols && (a.cols & 3) == 0;
+  if (full) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float f[4];
+      load4<InT>(x + c0 + 4 * q, f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[4 * q + i] = f[i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      v[i] = (in && st > 0 && c0 + i < a.cols) ? load_elem<InT>(x, c0 + i) : 0.f;
+  }
   float amax = 0.f;
-  if (st > 0 && c0 + 3 < a.cols && (a.cols & 3) == 0) {
-    load4<InT>(x + c0, v);  // one 16-byte (fp32) or 8-byte (bf16) load
-  } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = (st > 0 && c0 + i < a.cols) ? load_elem<InT>(x, c0 + i) : 0.f;
-  }
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
 #pragma unroll
-  for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  amax = warp_max(amax);
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float scale = fp8_group_scale(amax);
-  uint32_t packed = 0;
+  uint32_t packed[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) packed |= f32_to_e4m3(__fdiv_rn(v[i], scale)) << (8 * i);
-  if (st == 0) packed = 0;
-  if (c0 + 3 < a.cols && (a.cols & 3) == 0) {
-    *reinterpret_cast<uint32_t *>(codes + c0) = packed;
-  } else {
-    for (int i = 0; i < 4; ++i)
-      if (c0 + i < a.cols) codes[c0 + i] = (packed >> (8 * i)) & 0xff;
+  for (int q = 0; q < 4; ++q) {
+    packed[q] = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) packed[q] |= f32_to_e4m3(__fdiv_rn(v[4 * q + i], scale)) << (8 * i);
+    if (st == 0) packed[q] = 0;
   }
-  if (lane == 0) scales[r * G + g] = st > 0 ? scale : 0.f;
+  if (!in) return;
+  if (c0 + 15 < a.cols && (a.cols & 15) == 0) {
+    *reinterpret_cast<uint4 *>(codes + c0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  } else {
+    for (int i = 0; i < 16; ++i)
+      if (c0 + i < a.cols) codes[c0 + i] = (packed[i >> 2] >> (8 * (i & 3))) & 0xff;
+  }
+  if ((lane & 7) == 0) scales[r * G + g] = st > 0 ? scale : 0.f;
 }
 
 // ---- fp8 per row (token): one CTA of 256 threads per row.
@@ -257,7 +277,7 @@ cudaError_t launch_quant_t(const QuantArgs &a, cudaStream_t stream) {
   if (a.rows <= 0 || a.cols <= 0) return cudaSuccess;
   switch (a.afmt) {
     case A_FP8_GROUP128_DYN: {
-      const long warps = a.rows * ceil_div(a.cols, 128);
+      const long warps = a.rows * ((ceil_div(a.cols, 128) + 3) / 4);
       quant_fp8_group128<InT><<<(unsigned)ceil_div(warps * 32, 256), 256, 0, stream>>>(a);
       break;
     }
