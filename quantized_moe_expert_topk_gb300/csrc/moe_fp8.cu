@@ -15,7 +15,8 @@
 //
 // Tiles are 128 sorted rows (one expert) x 256 weight rows; one reduction
 // stage is one 128-wide block (128 bytes of codes per row).  One CTA per SM
-// walks a static list of tiles; its stage ring runs across tile boundaries.
+// walks a static list of tiles (block-major: each block's n-tiles in turn);
+// its stage ring runs across tile boundaries.
 // Warp roles:
 //   warp 0      TMA producer: the A rows (2-D TMA, 128-byte swizzle) and the
 //               256 weight rows as eight 32-row boxes -- 48 KB per stage
@@ -29,8 +30,8 @@
 //               maximum gathered from the four threads that hold it) into
 //               e4m3 codes + an fp32 scale (W13), or multiplies the router
 //               weight and adds into the fp32 token accumulator (W2): each
-//               warp transposes its 32 rows through shared memory 16 columns
-//               at a time, so that one red.add instruction covers 8 rows x 64
+//               warp transposes its 32 rows through shared memory 32 columns
+//               at a time, so that one red.add instruction covers 4 rows x 128
 //               contiguous bytes instead of 32 rows x 16 bytes
 //   warp 18     each stage's scales (the 128 rows' activation-group scales and
 //               the block scales of the eight 32-row weight groups) into a

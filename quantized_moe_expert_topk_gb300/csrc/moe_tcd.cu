@@ -1,5 +1,6 @@
 // moe_tcd.cu -- tcgen05 grouped GEMMs for MXFP4 weights with bf16 activations
-// (w4a16, GptOssMxfp4MoEMethod on the mxfp4.py page; the two GEMM stages of
+// (w4a16, GptOssMxfp4MoEMethod on the mxfp4.py page) or OCP MX activations
+// dequantised to exact f16 (w4a4 / w4a8; the two GEMM stages of
 // rocm_aiter_fused_experts on page
 // "vllm.model_executor.layers.fused_moe.experts.rocm_aiter_moe") at prefill
 // batches whose experts hold more than one 128-slot block each.
@@ -27,8 +28,13 @@
 //   warps 2-17  decode each stage's records (thread t: row t / 2, 32 elements)
 //               during the main loop; at a unit's end they drain the two
 //               accumulators (lane quarter warp % 4, 64 columns each) and
-//               apply the epilogue: W13 x-scale, bias, SwiGLU-OAI, f16
-//               intermediate; W2 bias, router weight, fp32 red.add
+//               apply the epilogue: W13 x-scale, bias, SwiGLU-OAI (MX
+//               activations: each thread's 32 outputs quantised and
+//               dequantised as one MX block), f16 intermediate; W2 bias,
+//               router weight, fp32 red.add.  Both write through the warp's
+//               own 16 rows of decoded-weight slot 0 (free during the
+//               epilogue), transposed so that one store / red.add
+//               instruction covers 8 rows x 64 contiguous bytes
 // Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, stops
 // issuing, lets its copies and MMAs land, frees its Tensor Memory and exits.
 #include <cuda.h>
