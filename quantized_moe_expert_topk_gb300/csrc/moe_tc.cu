@@ -466,7 +466,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // ------------------------------------------------------------------ gather
 // Sorted-order activation rows for the w13 GEMM: e4m3 codes copied as they
 // are (fp8 formats), e2m1 codes + scale-factor records (NVFP4, the
-// block-scaled kernels), bf16 rows, or f16 rows scaled per row by a power of
+// block-scaled kernels: quantised here from the bf16 rows, or copied from
+// moe_quant_act's output), bf16 rows, or f16 rows scaled per row by a power of
 // two (MXFP4 weights), plus per-row / per-group scales.  One warp per sorted
 // row.
 __global__ void gather_rows_kernel(GatherArgs g) {
