@@ -50,6 +50,29 @@ def test_valid_token_count(case):
             assert err <= tolerance(wl.wfmt, rms), (n, err, rms)
 
 
+def test_valid_token_count_multi_cta_sort():
+    # 8400 slots: the sort runs on several CTAs (count grid, scatter grid),
+    # which drop the slots of tokens >= n as the one-CTA sort does
+    M = 4200
+    wl = to_device(make_custom(M=M, K=128, N=128, E=8, T=2, wfmt="bf16", afmt="bf16", act="silu",
+                               gate="separated", bias=True, seed=47, name="nlt_multi_cta"))
+    assert moe.moe_align_scratch_bytes(M, 2, 8) > 0
+    n_dev = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layer = _layer(wl, n_dev)
+    h = to_host(wl)
+    for n in (0, 1, 2500, M):
+        n_dev.fill_(n)
+        out = layer(wl.x, wl.topk_ids, wl.topk_weights, wl.expert_map)
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy()
+        assert (got[n:] == 0).all(), n
+        if n:
+            ref = run_oracle(wl, host=dict(h, problem=dict(h["problem"], num_local_tokens=n)))
+            err = float(np.abs(got[:n] - ref[:n]).max())
+            rms = float(np.sqrt((ref[:n] ** 2).mean()))
+            assert err <= tolerance(wl.wfmt, rms), (n, err, rms)
+
+
 def test_one_graph_serves_every_fill_level():
     wl = to_device(make_custom(M=64, K=256, N=256, E=8, T=4, wfmt="mxfp4", afmt="bf16",
                                act="swiglu_oai", gate="interleaved", bias=True, seed=43,
