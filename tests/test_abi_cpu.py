@@ -98,6 +98,14 @@ def test_quant_and_align_validation(moe):
     assert L.moe_quant_act(fake, 4, 32, 1, None, fake, fake, None) == 1   # static scale missing
     assert L.moe_align_block_size(fake, 4, 2, None, 8, 2000, 64, fake, fake, fake, None, None) == 1
     assert L.moe_align_block_size(fake, 4, 2, None, 8, 8, 0, fake, fake, fake, None, None) == 1
+    # the scratch variant: same checks, plus a 16-byte-aligned scratch pointer
+    for El, bm in ((2000, 64), (8, 0)):
+        assert L.moe_align_block_size_scratch(fake, 4, 2, None, 8, El, bm, fake, fake, fake, None,
+                                              fake, 4096, None) == 1
+    assert L.moe_align_block_size_scratch(fake, 4096, 2, None, 8, 8, 64, fake, fake, fake, None,
+                                          ctypes.c_void_p(0x1008), 4096, None) == 1
+    assert L.moe_align_block_size_scratch(fake, 4, 2, None, 8, 8, 64, None, fake, fake, None,
+                                          fake, 4096, None) == 1  # sorted_ids missing
 
 
 def test_packed_weight_sizes(moe):
