@@ -13,8 +13,11 @@
 //   B. per expert, an exclusive prefix over warps (stable order) and the
 //      padded size; an exclusive scan over experts gives the block offsets;
 //   C. each warp walks its range in order and scatters every slot to
-//      base[warp][e] + (rank among earlier lanes of its group);
+//      offset[e] + (slots of e in earlier warps) + (rank among earlier
+//      lanes of its group); the first round reuses step A's expert ids;
 //   D. padding entries, expert_ids, tails.
+// Only the warps that hold slots take part in B (a batch of 4 slots: 4 of
+// the 32), and the block-size arithmetic is shifts for powers of two.
 // Extra CTAs (blockIdx.x > 0) zero an optional fp32 buffer (the stage-2
 // accumulator) so the fused path needs no separate memset launch.
 //
@@ -45,14 +48,32 @@ constexpr long kMultiSlotsPerCta = 4L * 32 * kAlignWarps;
 constexpr long kMultiMinSlots = 2 * kMultiSlotsPerCta;
 constexpr int kMultiMaxCtas = 64;
 
-__device__ __forceinline__ int local_of(const int32_t *ids, const int32_t *emap, long s, int E,
-                                        int El, long s_valid) {
-  if (s >= s_valid) return -1;  // a token beyond the valid count (padded dispatch buffer)
-  int g = ids[s];
+// Local expert of global expert id g (-1: masked, out of range or no slot).
+__device__ __forceinline__ int local_of_id(int g, const int32_t *emap, int E, int El) {
   if (g < 0 || g >= E) return -1;
   int l = emap ? emap[g] : g;
   return (l >= 0 && l < El) ? l : -1;
 }
+
+__device__ __forceinline__ int local_of(const int32_t *ids, const int32_t *emap, long s, int E,
+                                        int El, long s_valid) {
+  if (s >= s_valid) return -1;  // a token beyond the valid count (padded dispatch buffer)
+  return local_of_id(ids[s], emap, E, El);
+}
+
+// Division by the sort's block size for the non-negative counts, offsets and
+// capacities of a sort: a shift when it is a power of two (the block sizes
+// the library's kernels use), else the integer divide.
+struct BlockSize {
+  int bm, shift;
+  __device__ explicit BlockSize(int b) : bm(b), shift(-1) {
+    int k = 0;
+    while (k < 11 && (1 << k) < b) ++k;  // b <= 1024
+    if ((1 << k) == b) shift = k;
+  }
+  __device__ long div(long v) const { return shift >= 0 ? v >> shift : v / bm; }
+  __device__ int round_up(int v) const { return (int)(div((long)v + bm - 1) * bm); }
+};
 
 // The extra CTAs of a sort grid (index b from 0): the first zero_ctas zero
 // x.zero_buf / x.zero_ints, the next conv_ctas write the per-token f16 copy
@@ -192,18 +213,28 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
   int *pad = off + El + 1;             // [El]               padded sizes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned lt_mask = (1u << lane) - 1u;
-
-  for (int i = threadIdx.x; i < kAlignWarps * El; i += blockDim.x) cnt[i] = 0;
-  __syncthreads();
+  const BlockSize bs(BM);
 
   const long per = ceil_div(S, kAlignWarps);
   const long beg = (long)warp * per;
   const long end = beg + per < S ? beg + per : S;
+  // warps that hold slots (S <= 2^30: 32-bit arithmetic); the others have
+  // nothing to count or scatter, so their rows of cnt are never used
+  const int nwu = per > 0 ? (int)((uint32_t)(S + per - 1) / (uint32_t)per) : 0;
+  // the ids of each warp's first 32 slots, requested before the zeroing
+  int g0 = -1;
+  if (beg + lane < end && beg + lane < s_valid) g0 = ids[beg + lane];
 
-  // A. per-warp histogram
+  for (int i = threadIdx.x; i < nwu * El; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+
+  // A. per-warp histogram (the first round's local experts are kept for C)
+  int l0 = -1;
   for (long base = beg; base < end; base += 32) {
     const long s = base + lane;
-    const int l = s < end ? local_of(ids, emap, s, E, El, s_valid) : -1;
+    int l;
+    if (base == beg) l = l0 = local_of_id(g0, emap, E, El);
+    else l = s < end ? local_of(ids, emap, s, E, El, s_valid) : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, l);
     if (l >= 0 && lane == __ffs(peers) - 1) cnt[warp * El + l] += __popc(peers);
   }
@@ -212,13 +243,13 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
   // B. stable prefix over warps, totals and padded sizes
   for (int e = threadIdx.x; e < El; e += blockDim.x) {
     int run = 0;
-    for (int w = 0; w < kAlignWarps; ++w) {
+    for (int w = 0; w < nwu; ++w) {
       const int c = cnt[w * El + e];
       cnt[w * El + e] = run;
       run += c;
     }
     if (counts) counts[e] = run;
-    pad[e] = (int)(ceil_div(run, BM) * BM);
+    pad[e] = bs.round_up(run);
     off[e] = run;  // live count, kept for step D
   }
   __syncthreads();
@@ -263,16 +294,14 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
   // pad[e] = offset of expert e, off[e] = live count of e, off[El] = total
   if (x.offsets)
     for (int e = threadIdx.x; e < El; e += blockDim.x) x.offsets[e] = pad[e];
-  for (int i = threadIdx.x; i < kAlignWarps * El; i += blockDim.x) cnt[i] += pad[i % El];
-  __syncthreads();
 
-  // C. stable scatter
+  // C. stable scatter: expert offset + slots of the earlier warps + rank
   for (long base = beg; base < end; base += 32) {
     const long s = base + lane;
-    const int l = s < end ? local_of(ids, emap, s, E, El, s_valid) : -1;
+    const int l = base == beg ? l0 : (s < end ? local_of(ids, emap, s, E, El, s_valid) : -1);
     const unsigned peers = __match_any_sync(0xffffffffu, l);
     int pos = 0;
-    if (l >= 0) pos = cnt[warp * El + l] + __popc(peers & lt_mask);
+    if (l >= 0) pos = pad[l] + cnt[warp * El + l] + __popc(peers & lt_mask);
     __syncwarp();
     if (l >= 0) {
       sorted[pos] = (int32_t)s;
@@ -285,12 +314,14 @@ align_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__restrict_
   const int total = off[El];
   for (int e = warp; e < El; e += kAlignWarps) {
     const int o = pad[e], live = off[e];
-    const int padded = (int)(ceil_div(live, BM) * BM);
+    const int padded = bs.round_up(live);
+    const int ob = (int)bs.div(o), nb = (int)bs.div(padded);
     for (int i = live + lane; i < padded; i += 32) sorted[o + i] = (int32_t)S;
-    for (int b = lane; b < padded / BM; b += 32) expert_ids[o / BM + b] = e;
+    for (int b = lane; b < nb; b += 32) expert_ids[ob + b] = e;
   }
+  const long cap_blocks = bs.div(cap);
   for (long i = total + threadIdx.x; i < cap; i += blockDim.x) sorted[i] = (int32_t)S;
-  for (long b = total / BM + threadIdx.x; b < cap / BM; b += blockDim.x) expert_ids[b] = -1;
+  for (long b = bs.div(total) + threadIdx.x; b < cap_blocks; b += blockDim.x) expert_ids[b] = -1;
   if (threadIdx.x == 0) {
     *ntp = total;
     if (x.counters) x.counters[0] = x.counters[1] = 0;
@@ -357,6 +388,7 @@ align_scatter_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__r
   }
   const int c = blockIdx.x;
   const long s_valid = valid_slots(S, x);
+  const BlockSize bs(BM);
   extern __shared__ int smem[];
   int *cnt = smem;                     // [kAlignWarps][El]  per-warp counts -> positions
   int *off = smem + kAlignWarps * El;  // [El + 1]           live counts, total
@@ -387,7 +419,7 @@ align_scatter_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__r
       run += v;
     }
     if (c == 0 && counts) counts[e] = tot;
-    pad[e] = (int)(ceil_div(tot, BM) * BM);
+    pad[e] = bs.round_up(tot);
     off[e] = tot;
   }
   __syncthreads();
@@ -431,15 +463,13 @@ align_scatter_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__r
   __syncthreads();
   if (c == 0 && x.offsets)
     for (int e = threadIdx.x; e < El; e += blockDim.x) x.offsets[e] = pad[e];
-  for (int i = threadIdx.x; i < kAlignWarps * El; i += blockDim.x) cnt[i] += pad[i % El];
-  __syncthreads();
-  // C. stable scatter of this CTA's slots
+  // C. stable scatter of this CTA's slots: expert offset + slots before + rank
   for (long base = beg; base < end; base += 32) {
     const long s = base + lane;
     const int l = s < end ? local_of(ids, emap, s, E, El, s_valid) : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, l);
     int pos = 0;
-    if (l >= 0) pos = cnt[warp * El + l] + __popc(peers & lt_mask);
+    if (l >= 0) pos = pad[l] + cnt[warp * El + l] + __popc(peers & lt_mask);
     __syncwarp();
     if (l >= 0) {
       sorted[pos] = (int32_t)s;
@@ -452,13 +482,15 @@ align_scatter_kernel(const int32_t *__restrict__ ids, long S, const int32_t *__r
   const int gw = c * kAlignWarps + warp, nw = nc * kAlignWarps;
   for (int e = gw; e < El; e += nw) {
     const int o = pad[e], live = off[e];
-    const int padded = (int)(ceil_div(live, BM) * BM);
+    const int padded = bs.round_up(live);
+    const int ob = (int)bs.div(o), nb = (int)bs.div(padded);
     for (int i = live + lane; i < padded; i += 32) sorted[o + i] = (int32_t)S;
-    for (int b = lane; b < padded / BM; b += 32) expert_ids[o / BM + b] = e;
+    for (int b = lane; b < nb; b += 32) expert_ids[ob + b] = e;
   }
   const long gt = (long)c * blockDim.x + threadIdx.x, nt = (long)nc * blockDim.x;
+  const long cap_blocks = bs.div(cap);
   for (long i = total + gt; i < cap; i += nt) sorted[i] = (int32_t)S;
-  for (long b = total / BM + gt; b < cap / BM; b += nt) expert_ids[b] = -1;
+  for (long b = bs.div(total) + gt; b < cap_blocks; b += nt) expert_ids[b] = -1;
   if (c == 0 && threadIdx.x == 0) {
     *ntp = total;
     if (x.counters) x.counters[0] = x.counters[1] = 0;
@@ -561,6 +593,7 @@ batched_align_kernel(const int32_t *__restrict__ counts_in, int El, int max_toke
   __shared__ int off[1025];
   __shared__ int cnt[1024];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const BlockSize bs(BM);
   for (int e = threadIdx.x; e < El; e += blockDim.x) {
     const int c = counts_in[e];
     cnt[e] = c < 0 ? 0 : (c > max_tokens ? max_tokens : c);
@@ -571,7 +604,7 @@ batched_align_kernel(const int32_t *__restrict__ counts_in, int El, int max_toke
     const int chunk = (El + 31) / 32;
     const int e0 = lane * chunk;
     int local = 0;
-    for (int e = e0; e < e0 + chunk && e < El; ++e) local += (int)(ceil_div(cnt[e], BM) * BM);
+    for (int e = e0; e < e0 + chunk && e < El; ++e) local += bs.round_up(cnt[e]);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -581,7 +614,7 @@ batched_align_kernel(const int32_t *__restrict__ counts_in, int El, int max_toke
     int run = incl - local;
     for (int e = e0; e < e0 + chunk && e < El; ++e) {
       off[e] = run;
-      run += (int)(ceil_div(cnt[e], BM) * BM);
+      run += bs.round_up(cnt[e]);
     }
     if (lane == 31) off[El] = incl;
   }
@@ -589,13 +622,15 @@ batched_align_kernel(const int32_t *__restrict__ counts_in, int El, int max_toke
   const int total = off[El];
   for (int e = warp; e < El; e += blockDim.x / 32) {
     const int o = off[e], c = cnt[e];
-    const int padded = (int)(ceil_div(c, BM) * BM);
+    const int padded = bs.round_up(c);
+    const int ob = (int)bs.div(o), nb = (int)bs.div(padded);
     for (int i = lane; i < padded; i += 32)
       sorted[o + i] = i < c ? (int32_t)((long)e * max_tokens + i) : (int32_t)S;
-    for (int b = lane; b < padded / BM; b += 32) expert_ids[o / BM + b] = e;
+    for (int b = lane; b < nb; b += 32) expert_ids[ob + b] = e;
   }
+  const long cap_blocks = bs.div(cap);
   for (long i = total + threadIdx.x; i < cap; i += blockDim.x) sorted[i] = (int32_t)S;
-  for (long b = total / BM + threadIdx.x; b < cap / BM; b += blockDim.x) expert_ids[b] = -1;
+  for (long b = bs.div(total) + threadIdx.x; b < cap_blocks; b += blockDim.x) expert_ids[b] = -1;
   if (threadIdx.x == 0) *ntp = total;
 }
 
