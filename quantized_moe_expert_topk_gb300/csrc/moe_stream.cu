@@ -286,19 +286,14 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
       const bool pb = MODE == MODE_FUSED && w2;  // fields from b
       const Unit U = pb ? decode_unit(b, id - n13) : decode_unit(a, id);
       const int C = pb ? b.C : a.C;  // reduction length (K for W13, N for W2)
-      if (pb) {
-        // the intermediate rows of this expert are complete once every W13
-        // unit of it has finished every pass (one count per consumer warp,
-        // from the warp that applies the epilogue: with a k-split, the last
-        // arrival); those units were claimed earlier by running CTAs
-        const int need = a.units_per_expert * CW * (int)ceil_div(U.cnt, TOK);
-        if (!wait_count_bounded(a.done13 + U.e, need, kWaitCycles, a.err)) {
-          record_device_error(a.err, kErrTimeout);
-          *abort_flag = 1;
-          break;
-        }
-        fence_proxy_async_global();  // their generic stores before our TMA reads
-      }
+      // W2 in the fused grid: the intermediate rows of this expert are
+      // complete once every W13 unit of it has finished every pass (one count
+      // per consumer warp, from the warp that applies the epilogue: with a
+      // k-split, the last arrival); those units were claimed earlier by
+      // running CTAs.  The wait comes before the first copy of those rows:
+      // the unit's first weight stage (and its L2 prefetch) are already in
+      // flight while the W13 units finish.
+      bool rows_ready = !pb;
       for (int tok0 = 0; tok0 < U.cnt && ok; tok0 += TOK) {
         const int nt = min(TOK, U.cnt - tok0);
         const unsigned char *xrow = nullptr;  // lane n < nt loads token n of this pass
@@ -337,10 +332,23 @@ stream_kernel(const __grid_constant__ StreamArgs a, const __grid_constant__ Stre
           }
           __syncwarp();
           wait_prior();  // the token rows of W2 are the W13 grid's output
+          if (!rows_ready) {
+            const int need = a.units_per_expert * CW * (int)ceil_div(U.cnt, TOK);
+            if (!wait_count_bounded(a.done13 + U.e, need, kWaitCycles, a.err)) {
+              // the rows below are copied all the same (in bounds), so the
+              // stage's barrier completes; the consumers see the abort flag
+              record_device_error(a.err, kErrTimeout);
+              *abort_flag = 1;
+              ok = false;
+            }
+            fence_proxy_async_global();  // their generic stores before our TMA reads
+            rows_ready = true;
+          }
           if (lane < nt)
             tma_bulk_g2s(ws + W_STAGE + lane * XS, xrow + (long)(U.kb0 + kb) * 128, xbytes,
                          &sm.full[slot]);
           ++it;
+          if (!ok) break;
         }
       }
     }
