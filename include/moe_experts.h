@@ -38,7 +38,9 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 9
+/* Raised whenever an entry point is added or a struct or signature changes
+ * (10: moe_align_scratch_bytes and moe_align_block_size_scratch). */
+#define MOE_ABI_VERSION 10
 
 typedef enum {
   MOE_OK = 0,

@@ -35,7 +35,7 @@ def test_header_symbols_are_exported(moe):
     L = moe.lib()
     for name in declared:
         assert hasattr(L, name), name
-    assert moe.moe_abi_version() == 9
+    assert moe.moe_abi_version() == 10
 
 
 def test_status_strings(moe):
